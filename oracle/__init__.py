@@ -1,0 +1,219 @@
+"""Plain fp64 CPU oracle for RMSNorm / LayerNorm forward and backward.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module; the library and its
+binding never do.  The arithmetic lives in ``oracle.c`` (its header gives the
+definitions and the page passages they follow: the LayerNorm/RMSNorm and
+backward-pass paragraphs of "PyTorch atinge desempenho SOTA em normalizacao
+com torch.compile").  This file only compiles that C file with gcc and
+marshals numpy arrays to it.
+
+bf16 tensors are passed as their raw uint16 bit patterns.  Outputs are fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+RMS = 0
+LAYER = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def compile_c(src: str, out: str) -> str:
+    """gcc -O2 without fast-math or FMA contraction, so every operation is an
+    IEEE double operation in source order."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c (skipped when the shared object is newer)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(SRC)):
+        return _LIB
+    return compile_c(SRC, _LIB)
+
+
+def _ptr(a, typ):
+    if a is None:
+        return ctypes.cast(None, typ)
+    return a.ctypes.data_as(typ)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 inputs are passed as uint16 bit patterns")
+    return a
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"{what} failed with code {rc}")
+
+
+def _rows(rows, M):
+    if rows is None:
+        return None, M
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r, int(r.size)
+
+
+class Oracle:
+    """ctypes view of one compiled oracle shared object."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        lib.oracle_fwd_f64.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_double, ctypes.c_int, _dp, _dp, _dp]
+        lib.oracle_bwd_f64.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_double, ctypes.c_int, _dp, _dp, _dp]
+        lib.oracle_fwd_bf16.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                        _i64p, ctypes.c_int64, _dp, _dp, _dp]
+        lib.oracle_bwd_dx_bf16.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                           _i64p, ctypes.c_int64, _dp]
+        lib.oracle_param_grads_bf16.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64,
+                                                ctypes.c_int64, ctypes.c_double,
+                                                ctypes.c_int, _dp, _dp, _dp, _dp]
+        for f in (lib.oracle_fwd_f64, lib.oracle_bwd_f64, lib.oracle_fwd_bf16,
+                  lib.oracle_bwd_dx_bf16, lib.oracle_param_grads_bf16):
+            f.restype = ctypes.c_int
+        self.lib = lib
+        self.path = path
+
+    # -------------------------------------------------------------- fp64 API
+    def fwd_f64(self, x, gamma, beta, eps, mode):
+        """Forward on double inputs.  x: [M, N]. Returns (y, rstd, mean)."""
+        x = _f64(x)
+        M, N = x.shape
+        gamma = _f64(gamma)
+        beta = None if beta is None else _f64(beta)
+        y = np.empty((M, N), np.float64)
+        rstd = np.empty(M, np.float64)
+        mean = np.empty(M, np.float64)
+        _check(self.lib.oracle_fwd_f64(_ptr(x, _dp), _ptr(gamma, _dp), _ptr(beta, _dp),
+                                       M, N, float(eps), int(mode), _ptr(y, _dp),
+                                       _ptr(rstd, _dp), _ptr(mean, _dp)), "oracle_fwd_f64")
+        return y, rstd, mean
+
+    def bwd_f64(self, dy, x, gamma, eps, mode):
+        """Backward on double inputs. Returns (dx, dgamma, dbeta); dbeta is the
+        column sum of dy in LayerNorm mode and zeros in RMSNorm mode."""
+        x = _f64(x)
+        dy = _f64(dy)
+        M, N = x.shape
+        gamma = _f64(gamma)
+        dx = np.empty((M, N), np.float64)
+        dg = np.empty(N, np.float64)
+        db = np.empty(N, np.float64)
+        _check(self.lib.oracle_bwd_f64(_ptr(dy, _dp), _ptr(x, _dp), _ptr(gamma, _dp),
+                                       M, N, float(eps), int(mode), _ptr(dx, _dp),
+                                       _ptr(dg, _dp), _ptr(db, _dp)), "oracle_bwd_f64")
+        return dx, dg, db
+
+    # -------------------------------------------------------------- bf16 API
+    def fwd_bf16(self, x_bits, gamma_bits, beta_bits, eps, mode, rows=None):
+        """Forward on bf16 bit patterns, for all rows or the listed ones.
+        Returns (y [R, N], rstd [R], mean [R]) in fp64."""
+        x_bits = _u16(x_bits)
+        M, N = x_bits.shape
+        gamma_bits = _u16(gamma_bits)
+        beta_bits = None if beta_bits is None else _u16(beta_bits)
+        r, R = _rows(rows, M)
+        y = np.empty((R, N), np.float64)
+        rstd = np.empty(R, np.float64)
+        mean = np.empty(R, np.float64)
+        _check(self.lib.oracle_fwd_bf16(_ptr(x_bits, _u16p), _ptr(gamma_bits, _u16p),
+                                        _ptr(beta_bits, _u16p), M, N, float(eps),
+                                        int(mode), _ptr(r, _i64p), R, _ptr(y, _dp),
+                                        _ptr(rstd, _dp), _ptr(mean, _dp)),
+               "oracle_fwd_bf16")
+        return y, rstd, mean
+
+    def bwd_dx_bf16(self, dy_bits, x_bits, gamma_bits, eps, mode, rows=None):
+        """dx on bf16 bit patterns for all rows or the listed ones (fp64)."""
+        x_bits = _u16(x_bits)
+        dy_bits = _u16(dy_bits)
+        M, N = x_bits.shape
+        gamma_bits = _u16(gamma_bits)
+        r, R = _rows(rows, M)
+        dx = np.empty((R, N), np.float64)
+        _check(self.lib.oracle_bwd_dx_bf16(_ptr(dy_bits, _u16p), _ptr(x_bits, _u16p),
+                                           _ptr(gamma_bits, _u16p), M, N, float(eps),
+                                           int(mode), _ptr(r, _i64p), R, _ptr(dx, _dp)),
+               "oracle_bwd_dx_bf16")
+        return dx
+
+    def param_grads_bf16(self, dy_bits, x_bits, gamma_bits, eps, mode):
+        """Column reductions over all rows: (dgamma, dbeta, dgamma_abs,
+        dbeta_abs), the last two being sums of |summand| (tolerance scales)."""
+        x_bits = _u16(x_bits)
+        dy_bits = _u16(dy_bits)
+        M, N = x_bits.shape
+        gamma_bits = _u16(gamma_bits)
+        out = [np.empty(N, np.float64) for _ in range(4)]
+        _check(self.lib.oracle_param_grads_bf16(_ptr(dy_bits, _u16p), _ptr(x_bits, _u16p),
+                                                _ptr(gamma_bits, _u16p), M, N, float(eps),
+                                                int(mode), *[_ptr(o, _dp) for o in out]),
+               "oracle_param_grads_bf16")
+        return tuple(out)
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def fwd_f64(*a, **k):
+    return default().fwd_f64(*a, **k)
+
+
+def bwd_f64(*a, **k):
+    return default().bwd_f64(*a, **k)
+
+
+def fwd_bf16(*a, **k):
+    return default().fwd_bf16(*a, **k)
+
+
+def bwd_dx_bf16(*a, **k):
+    return default().bwd_dx_bf16(*a, **k)
+
+
+def param_grads_bf16(*a, **k):
+    return default().param_grads_bf16(*a, **k)
+
+
+def bf16_bits_to_f64(bits):
+    """Exact widening of bf16 bit patterns to float64 (numpy only)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)

@@ -1,0 +1,303 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for RMSNorm and LayerNorm,
+ * forward and backward, over the contiguous last dimension of a row-major
+ * [M, N] tensor.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file; only the tests, the package's smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * What it computes follows the page "PyTorch atinge desempenho SOTA em
+ * normalizacao com torch.compile" (matsubara.tec.br):
+ *   - its paragraph on LayerNorm (2016) and RMSNorm (2019): LayerNorm
+ *     normalises with the mean and the variance along one dimension and then
+ *     applies the trainable gamma (weight) and beta (bias); RMSNorm replaces
+ *     the mean/variance by the root mean square and has no beta;
+ *   - its paragraph on the forward pass: a reduction along a contiguous
+ *     dimension followed by pointwise operations;
+ *   - its paragraph on the backward pass: the gradients dX (input), dW
+ *     (gamma) and, for LayerNorm, dB (beta).
+ * The page prints no formula.  The plainest textbook reading is used and is
+ * written out once here (all arithmetic in double):
+ *
+ *   LayerNorm   mu = (1/N) sum_j x_j
+ *               v  = (1/N) sum_j (x_j - mu)^2          (population variance)
+ *               r  = 1 / sqrt(v + eps)                  (eps inside the root)
+ *               xhat_j = (x_j - mu) * r
+ *               y_j = xhat_j * gamma_j + beta_j
+ *   RMSNorm     ms = (1/N) sum_j x_j^2
+ *               r  = 1 / sqrt(ms + eps)
+ *               xhat_j = x_j * r
+ *               y_j = xhat_j * gamma_j
+ *   Backward    g_j = dy_j * gamma_j
+ *               c = (1/N) sum_j g_j * xhat_j
+ *               a = (1/N) sum_j g_j                     (LayerNorm only)
+ *               LayerNorm dx_j = r * (g_j - a - xhat_j * c)
+ *               RMSNorm   dx_j = r * (g_j - xhat_j * c)
+ *               dgamma_j = sum over rows of dy_ij * xhat_ij
+ *               dbeta_j  = sum over rows of dy_ij        (LayerNorm only)
+ *
+ * The backward formulas are the derivative of y with respect to x, gamma and
+ * beta under the forward definition above (chain rule through mu and r);
+ * the tests pin them to central finite differences of the forward.
+ *
+ * Every statistic is recomputed here in double from the inputs; nothing
+ * saved by another implementation is reused.  bf16 inputs are widened
+ * exactly (bf16 is the top half of an IEEE binary32).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_RMS 0
+#define ORACLE_LAYER 1
+
+/* bf16 bit pattern -> exact double value. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static void widen_row(const uint16_t *src, int64_t n, double *dst)
+{
+    for (int64_t j = 0; j < n; ++j)
+        dst[j] = bf16_bits_to_double(src[j]);
+}
+
+/* Row statistics: *mu receives the mean (0 for RMSNorm), *r the reciprocal
+ * of sqrt(variance-or-mean-square + eps). */
+static void row_stats(const double *x, int64_t n, double eps, int mode,
+                      double *mu, double *r)
+{
+    if (mode == ORACLE_LAYER) {
+        double s = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+            s += x[j];
+        double m = s / (double)n;
+        double q = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+            q += (x[j] - m) * (x[j] - m);
+        double v = q / (double)n;
+        *mu = m;
+        *r = 1.0 / sqrt(v + eps);
+    } else {
+        double q = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+            q += x[j] * x[j];
+        double ms = q / (double)n;
+        *mu = 0.0;
+        *r = 1.0 / sqrt(ms + eps);
+    }
+}
+
+/* Forward of one row.  beta may be NULL (treated as zero). */
+static void fwd_row(const double *x, const double *gamma, const double *beta,
+                    int64_t n, double eps, int mode,
+                    double *y, double *mu_out, double *r_out)
+{
+    double mu, r;
+    row_stats(x, n, eps, mode, &mu, &r);
+    for (int64_t j = 0; j < n; ++j) {
+        double xhat = (x[j] - mu) * r;
+        double b = (mode == ORACLE_LAYER && beta) ? beta[j] : 0.0;
+        y[j] = xhat * gamma[j] + b;
+    }
+    if (mu_out)
+        *mu_out = mu;
+    if (r_out)
+        *r_out = r;
+}
+
+/* Backward of one row: writes dx (if non-NULL) and adds this row's
+ * contribution to dgamma / dbeta (if non-NULL). The *_abs arrays, if given,
+ * accumulate the sums of absolute summands (used as tolerance scales). */
+static void bwd_row(const double *dy, const double *x, const double *gamma,
+                    int64_t n, double eps, int mode, double *dx,
+                    double *dgamma, double *dbeta,
+                    double *dgamma_abs, double *dbeta_abs)
+{
+    double mu, r;
+    row_stats(x, n, eps, mode, &mu, &r);
+    double sum_g = 0.0, sum_gxhat = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double xhat = (x[j] - mu) * r;
+        double g = dy[j] * gamma[j];
+        sum_g += g;
+        sum_gxhat += g * xhat;
+    }
+    double a = (mode == ORACLE_LAYER) ? sum_g / (double)n : 0.0;
+    double c = sum_gxhat / (double)n;
+    for (int64_t j = 0; j < n; ++j) {
+        double xhat = (x[j] - mu) * r;
+        double g = dy[j] * gamma[j];
+        if (dx)
+            dx[j] = r * (g - a - xhat * c);
+        if (dgamma)
+            dgamma[j] += dy[j] * xhat;
+        if (dgamma_abs)
+            dgamma_abs[j] += fabs(dy[j] * xhat);
+        if (mode == ORACLE_LAYER) {
+            if (dbeta)
+                dbeta[j] += dy[j];
+            if (dbeta_abs)
+                dbeta_abs[j] += fabs(dy[j]);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- f64 API */
+
+/* Forward over all M rows of double inputs.  y: [M, N]; rstd, mean: [M]
+ * (mean may be NULL).  Returns 0, or -1 on bad arguments. */
+int oracle_fwd_f64(const double *x, const double *gamma, const double *beta,
+                   int64_t M, int64_t N, double eps, int mode,
+                   double *y, double *rstd, double *mean)
+{
+    if (!x || !gamma || !y || M < 0 || N < 1)
+        return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        double mu, r;
+        fwd_row(x + i * N, gamma, beta, N, eps, mode, y + i * N, &mu, &r);
+        if (rstd)
+            rstd[i] = r;
+        if (mean)
+            mean[i] = mu;
+    }
+    return 0;
+}
+
+/* Backward over all M rows of double inputs.  dx: [M, N]; dgamma, dbeta:
+ * [N], overwritten (dbeta may be NULL).  Returns 0, or -1. */
+int oracle_bwd_f64(const double *dy, const double *x, const double *gamma,
+                   int64_t M, int64_t N, double eps, int mode,
+                   double *dx, double *dgamma, double *dbeta)
+{
+    if (!dy || !x || !gamma || M < 0 || N < 1)
+        return -1;
+    if (dgamma)
+        memset(dgamma, 0, sizeof(double) * (size_t)N);
+    if (dbeta)
+        memset(dbeta, 0, sizeof(double) * (size_t)N);
+    for (int64_t i = 0; i < M; ++i)
+        bwd_row(dy + i * N, x + i * N, gamma, N, eps, mode,
+                dx ? dx + i * N : NULL, dgamma, dbeta, NULL, NULL);
+    return 0;
+}
+
+/* --------------------------------------------------------------- bf16 API */
+
+/* Forward on bf16 inputs (bit patterns), for the rows listed in `rows`
+ * (all rows 0..M-1 in order when rows == NULL, nrows == M).  Output row k
+ * of y / rstd / mean belongs to input row rows[k].  Streams one row at a
+ * time, so [M, N] double tensors are never formed. */
+int oracle_fwd_bf16(const uint16_t *x, const uint16_t *gamma,
+                    const uint16_t *beta, int64_t M, int64_t N, double eps,
+                    int mode, const int64_t *rows, int64_t nrows,
+                    double *y, double *rstd, double *mean)
+{
+    if (!x || !gamma || M < 0 || N < 1 || nrows < 0)
+        return -1;
+    if (!rows && nrows != M)
+        return -1;
+    double *xr = malloc(sizeof(double) * (size_t)N);
+    double *g = malloc(sizeof(double) * (size_t)N);
+    double *b = beta ? malloc(sizeof(double) * (size_t)N) : NULL;
+    double *yr = y ? NULL : malloc(sizeof(double) * (size_t)N);
+    if (!xr || !g || (beta && !b) || (!y && !yr)) {
+        free(xr); free(g); free(b); free(yr);
+        return -2;
+    }
+    widen_row(gamma, N, g);
+    if (beta)
+        widen_row(beta, N, b);
+    int rc = 0;
+    for (int64_t k = 0; k < nrows; ++k) {
+        int64_t i = rows ? rows[k] : k;
+        if (i < 0 || i >= M) {
+            rc = -1;
+            break;
+        }
+        widen_row(x + i * N, N, xr);
+        double mu, r;
+        fwd_row(xr, g, b, N, eps, mode, y ? y + k * N : yr, &mu, &r);
+        if (rstd)
+            rstd[k] = r;
+        if (mean)
+            mean[k] = mu;
+    }
+    free(xr); free(g); free(b); free(yr);
+    return rc;
+}
+
+/* dx on bf16 inputs for the listed rows (same row convention as above). */
+int oracle_bwd_dx_bf16(const uint16_t *dy, const uint16_t *x,
+                       const uint16_t *gamma, int64_t M, int64_t N,
+                       double eps, int mode, const int64_t *rows,
+                       int64_t nrows, double *dx)
+{
+    if (!dy || !x || !gamma || !dx || M < 0 || N < 1 || nrows < 0)
+        return -1;
+    if (!rows && nrows != M)
+        return -1;
+    double *xr = malloc(sizeof(double) * (size_t)N);
+    double *dyr = malloc(sizeof(double) * (size_t)N);
+    double *g = malloc(sizeof(double) * (size_t)N);
+    if (!xr || !dyr || !g) {
+        free(xr); free(dyr); free(g);
+        return -2;
+    }
+    widen_row(gamma, N, g);
+    int rc = 0;
+    for (int64_t k = 0; k < nrows; ++k) {
+        int64_t i = rows ? rows[k] : k;
+        if (i < 0 || i >= M) {
+            rc = -1;
+            break;
+        }
+        widen_row(x + i * N, N, xr);
+        widen_row(dy + i * N, N, dyr);
+        bwd_row(dyr, xr, g, N, eps, mode, dx + k * N, NULL, NULL, NULL, NULL);
+    }
+    free(xr); free(dyr); free(g);
+    return rc;
+}
+
+/* Column reductions over ALL rows (in increasing row order) on bf16 inputs:
+ * dgamma_j = sum_i dy_ij * xhat_ij, dbeta_j = sum_i dy_ij (LayerNorm), plus
+ * the matching sums of absolute summands.  Any output pointer may be NULL.
+ * gamma is needed because the per-row statistics do not depend on it but
+ * the shared row routine takes it; it does not enter dgamma or dbeta. */
+int oracle_param_grads_bf16(const uint16_t *dy, const uint16_t *x,
+                            const uint16_t *gamma, int64_t M, int64_t N,
+                            double eps, int mode, double *dgamma,
+                            double *dbeta, double *dgamma_abs,
+                            double *dbeta_abs)
+{
+    if (!dy || !x || !gamma || M < 0 || N < 1)
+        return -1;
+    double *xr = malloc(sizeof(double) * (size_t)N);
+    double *dyr = malloc(sizeof(double) * (size_t)N);
+    double *g = malloc(sizeof(double) * (size_t)N);
+    if (!xr || !dyr || !g) {
+        free(xr); free(dyr); free(g);
+        return -2;
+    }
+    widen_row(gamma, N, g);
+    if (dgamma) memset(dgamma, 0, sizeof(double) * (size_t)N);
+    if (dbeta) memset(dbeta, 0, sizeof(double) * (size_t)N);
+    if (dgamma_abs) memset(dgamma_abs, 0, sizeof(double) * (size_t)N);
+    if (dbeta_abs) memset(dbeta_abs, 0, sizeof(double) * (size_t)N);
+    for (int64_t i = 0; i < M; ++i) {
+        widen_row(x + i * N, N, xr);
+        widen_row(dy + i * N, N, dyr);
+        bwd_row(dyr, xr, g, N, eps, mode, NULL, dgamma, dbeta, dgamma_abs,
+                dbeta_abs);
+    }
+    free(xr); free(dyr); free(g);
+    return 0;
+}
