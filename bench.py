@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""RMSNorm / LayerNorm forward+backward throughput on GB300.
+
+One step = norm_fwd + norm_bwd (three kernel launches: the fused forward,
+the fused backward row pass, the fixed-order dgamma/dbeta partial reduce)
+over one batch of seeded synthetic bf16 input resident in HBM.  The metric
+is achieved HBM bandwidth: the minimal (algorithmic) bytes of the step
+divided by its device time.  Minimal bytes per pass, with k = 1 (RMSNorm)
+or 2 (LayerNorm) and P the number of partial rows the backward writes:
+    forward  4MN + 2kN + 4kM    (read x, gamma[, beta]; write y, rstd[, mean])
+    backward 6MN + 2N + 4kM + 4kPN
+             (read x, dy, gamma, rstd[, mean]; write dx and the partials)
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (the fp64 CPU oracle, timed)
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU (rows are independent; no data-path collective) and rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm/LayerNorm fwd+bwd achieved HBM GB/s and % of GB300 peak per (M,N)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algo_bytes(M, N, mode, P):
+    k = 2 if mode == 1 else 1
+    fwd = 4 * M * N + 2 * k * N + 4 * k * M
+    bwd = 6 * M * N + 2 * N + 4 * k * M + 4 * k * P * N
+    return fwd, bwd
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    csrc = os.path.join(ROOT, "memory_bound_normalization_rmsnorm_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        rec = data[workload][kernel]
+        if rec.get("source_hash") != source_hash():
+            return None
+        return rec["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        # "under load": samples above the median power of the run
+        loaded = [s for s, p in zip(sm, pw) if p >= statistics.median(pw)] if pw else sm
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def gpu_index(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",")]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(w, rows, seed=0):
+    """Oracle fwd + dx + column sums on the first `rows` rows of the workload
+    distribution; returns (seconds, bytes by the same minimal-byte formula)."""
+    import oracle
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    case = wl.like(w, rows, w.N)
+    x, g, b, dy = wl.make_inputs(case, "cpu", seed=seed)
+    xb, gb_, dyb = wl.bf16_bits(x), wl.bf16_bits(g), wl.bf16_bits(dy)
+    bb = None if b is None else wl.bf16_bits(b)
+    eps = float(w.eps)
+    t0 = time.perf_counter()
+    oracle.fwd_bf16(xb, gb_, bb, eps, w.mode)
+    oracle.bwd_dx_bf16(dyb, xb, gb_, eps, w.mode)
+    oracle.param_grads_bf16(dyb, xb, gb_, eps, w.mode)
+    dt = time.perf_counter() - t0
+    f, bw = algo_bytes(rows, w.N, w.mode, 1)
+    return dt, f + bw
+
+
+def cpu_baseline(w, seconds=12.0):
+    import oracle
+
+    oracle.default()
+    rows = max(1, min(w.M, (1 << 20) // w.N))
+    dt, _ = oracle_sample(w, rows)
+    reps_rows = max(1, int(rows * seconds / max(dt, 1e-3)))
+    reps_rows = min(reps_rows, w.M)
+    total_t, total_b, done = 0.0, 0, 0
+    while done < reps_rows:
+        r = min(rows, reps_rows - done)
+        dt, nb = oracle_sample(w, r, seed=done + 1)
+        total_t += dt
+        total_b += nb
+        done += r
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.M} rows x N={w.N} ({w.mode_name}), fwd + dx + column "
+                      f"sums, fp64, single thread, {total_t:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, local = dist_setup()
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+    if rank != 0:
+        barrier(world)
+        return
+    import oracle
+
+    oracle.default()
+    # size one step so that warmup + steps take about two minutes in all
+    dt, _ = oracle_sample(w, 8)
+    per_row = dt / 8
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.M, budget / max(per_row, 1e-9))))
+    for i in range(args.warmup):
+        oracle_sample(w, rows, seed=1000 + i)
+    tt, tb = 0.0, 0
+    for i in range(args.steps):
+        dt, nb = oracle_sample(w, rows, seed=i)
+        tt += dt
+        tb += nb
+    value = tb / tt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N, "eps": w.eps},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} of {w.M} rows per step, fwd + dx + column sums, "
+                                   f"fp64, single thread"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+# ------------------------------------------------------------------ GPU arm
+class DirectStep:
+    """One fwd+bwd step through the C ABI with pre-marshalled arguments (no
+    per-call Python tensor checks inside the timed loop)."""
+
+    def __init__(self, gb, w, x, g, b, dy, stream):
+        import torch
+
+        M, N = w.M, w.N
+        dev = x.device
+        self.y = torch.empty_like(x)
+        self.dx = torch.empty_like(x)
+        self.rstd = torch.empty(M, dtype=torch.float32, device=dev)
+        self.mean = torch.empty(M, dtype=torch.float32, device=dev) if w.mode == 1 else None
+        self.dg = torch.empty(N, dtype=torch.float32, device=dev)
+        self.db = torch.empty(N, dtype=torch.float32, device=dev) if w.mode == 1 else None
+        nbytes = gb.norm_bwd_workspace_bytes(M, N, w.mode)
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        L = gb.lib()
+        vp = ctypes.c_void_p
+
+        def p(t):
+            return None if t is None else vp(t.data_ptr())
+
+        s = vp(stream.cuda_stream)
+        self.fwd_args = (L.norm_fwd, [p(x), p(g), p(b), M, N, ctypes.c_float(w.eps), w.mode,
+                                      p(self.y), p(self.rstd), p(self.mean), s])
+        self.bwd_args = (L.norm_bwd, [p(dy), p(x), p(g), p(self.rstd), p(self.mean), M, N,
+                                      w.mode, p(self.dx), p(self.dg), p(self.db), p(self.ws),
+                                      ctypes.c_size_t(self.ws.numel()), s])
+
+    def fwd(self):
+        f, a = self.fwd_args
+        st = f(*a)
+        if st:
+            raise RuntimeError(f"norm_fwd status {st}")
+
+    def bwd(self):
+        f, a = self.bwd_args
+        st = f(*a)
+        if st:
+            raise RuntimeError(f"norm_bwd status {st}")
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import memory_bound_normalization_rmsnorm_gb300 as gb
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+    x, g, b, dy = wl.make_inputs(w, dev, seed=w.seed + rank)
+    stream = torch.cuda.current_stream(dev)
+    step = DirectStep(gb, w, x, g, b, dy, stream)
+    plan_f = gb.norm_plan(w.M, w.N, w.mode, False)
+    plan_b = gb.norm_plan(w.M, w.N, w.mode, True)
+    P = plan_b["partials"]
+    fwd_b, bwd_b = algo_bytes(w.M, w.N, w.mode, P)
+
+    sampler = ClockSampler(gpu_index(local))
+    sampler.start()
+    for _ in range(args.warmup):
+        step.fwd()
+        step.bwd()
+    torch.cuda.synchronize()
+    if gb.norm_get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step.fwd()
+        ev[i][1].record(stream)
+        step.bwd()
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    if gb.norm_get_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    total_ms = t0.elapsed_time(t1)
+    total_ms_max = max_over_ranks(total_ms, world, dev)
+    fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    step_bytes = fwd_b + bwd_b
+    value = world * step_bytes * args.steps / (total_ms_max * 1e-3) / 1e9
+
+    # end to end through the public Python API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(gb, w, x, g, b, dy, dev, args.e2e_steps, fwd_b + bwd_b, world)
+
+    peak, peak_kind = peak_hbm()
+    bwd_gbs = bwd_b / (bwd_ms * 1e-3) / 1e9
+    fwd_gbs = fwd_b / (fwd_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(w.name, "norm_bwd_kernel")
+    roofline = {"bound": "hbm", "achieved": bwd_gbs, "peak": peak, "unit": "GB/s",
+                "frac": bwd_gbs / peak, "traffic": traffic,
+                "kernel": "norm_bwd (fused row kernel + fixed-order partial reduce)",
+                "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "bytes_per_launch": bwd_b, "launch_ms": bwd_ms}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
+                       "eps": w.eps, "io_dtype": "bf16", "accumulate": "fp32",
+                       "parallelism": f"replicas x{world} (rows independent)",
+                       "l2": "inputs larger than L2 (each of x, dy, y, dx is "
+                             f"{w.M * w.N * 2 / 1e6:.0f} MB > 129 MB); no flush",
+                       "plan_fwd": plan_f, "plan_bwd": plan_b},
+            "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
+            "pct_of_measured_peak": 100.0 * value / world / peak,
+            "fwd": {"ms": fwd_ms, "GB/s": fwd_gbs, "frac": fwd_gbs / peak, "bytes": fwd_b},
+            "bwd": {"ms": bwd_ms, "GB/s": bwd_gbs, "frac": bwd_gbs / peak, "bytes": bwd_b,
+                    "partials": P},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_e2e(gb, w, x, g, b, dy, dev, steps, step_bytes, world):
+    """Per step: pinned host -> device copies of x, dy, gamma(, beta), the
+    forward and backward passes, device -> pinned host copies of every
+    output; timed with CUDA events around the whole step."""
+    import torch
+
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hg = g.cpu().pin_memory()
+    hb = None if b is None else b.cpu().pin_memory()
+    dx_ = torch.empty_like(x)
+    ddy = torch.empty_like(dy)
+    dg_ = torch.empty_like(g)
+    db_ = None if b is None else torch.empty_like(b)
+    outs_h = None
+    h2d = hx.numel() * 2 + hdy.numel() * 2 + hg.numel() * 2 + (0 if hb is None else hb.numel() * 2)
+
+    def one():
+        nonlocal outs_h
+        dx_.copy_(hx, non_blocking=True)
+        ddy.copy_(hdy, non_blocking=True)
+        dg_.copy_(hg, non_blocking=True)
+        if hb is not None:
+            db_.copy_(hb, non_blocking=True)
+        y, rstd, mean = gb.norm_fwd(dx_, dg_, db_, w.eps, w.mode)
+        dxo, dgam, dbet = gb.norm_bwd(ddy, dx_, dg_, rstd, mean, w.mode)
+        outs = [t for t in (y, rstd, mean, dxo, dgam, dbet) if t is not None]
+        if outs_h is None:
+            outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        for h, d in zip(outs_h, outs):
+            h.copy_(d, non_blocking=True)
+        return outs
+
+    one()
+    torch.cuda.synchronize()
+    d2h = sum(h.numel() * h.element_size() for h in outs_h)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(steps):
+        one()
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1)
+    ms = max_over_ranks(ms, world, dev)
+    return {"value": world * step_bytes * steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
+            "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_32768x4096")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

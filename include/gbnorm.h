@@ -1,0 +1,176 @@
+/*
+ * gbnorm.h -- C ABI of the GB300 (sm_103a) RMSNorm / LayerNorm library.
+ *
+ * The operation (page "PyTorch atinge desempenho SOTA em normalizacao com
+ * torch.compile", matsubara.tec.br; paragraphs on LayerNorm/RMSNorm, on the
+ * forward pass and on the backward pass):
+ *   forward   a reduction along the contiguous last dimension of each row
+ *             (mean and variance for LayerNorm, mean square for RMSNorm),
+ *             then pointwise normalisation and the trainable scale gamma
+ *             (plus the shift beta for LayerNorm);
+ *   backward  dX from per-row dot products, dW (dgamma) and, for LayerNorm,
+ *             dB (dbeta) from a column reduction over all rows.
+ * Definitions used (the page prints none; the textbook reading):
+ *   LayerNorm  mean = sum(x)/N, var = sum((x-mean)^2)/N (population),
+ *              rstd = 1/sqrt(var + eps), y = (x-mean)*rstd*gamma + beta
+ *   RMSNorm    rstd = 1/sqrt(sum(x^2)/N + eps), y = x*rstd*gamma
+ *   backward   g = dy*gamma, xhat = (x-mean)*rstd (mean = 0 for RMSNorm),
+ *              c = sum(g*xhat)/N, a = sum(g)/N (LayerNorm; 0 for RMSNorm),
+ *              dx = rstd*(g - a - xhat*c),
+ *              dgamma = column sums of dy*xhat, dbeta = column sums of dy.
+ *
+ * Data layout.  x, y, dy, dx: bf16 [M, N], row-major, rows contiguous (row
+ * stride N elements).  gamma, beta: bf16 [N].  rstd, mean: fp32 [M].
+ * dgamma, dbeta: fp32 [N].  All arithmetic is fp32; bf16 results are
+ * rounded to nearest even.
+ *
+ * Ownership.  Every pointer is a DEVICE pointer owned by the caller.  The
+ * library allocates no device memory; the backward pass takes a caller
+ * workspace (see norm_bwd_workspace_bytes).  Outputs must not alias inputs.
+ *
+ * Requirements.  M >= 1, 8 <= N <= NORM_MAX_N, N % 8 == 0, and every
+ * pointer 16-byte aligned (so each row starts on a 16-byte boundary and is
+ * moved by 16-byte bulk copies and 128-bit loads/stores).  There is no
+ * slow path for other shapes: they are rejected with a status code.
+ *
+ * Execution.  Calls are asynchronous on `stream` (NULL = the legacy default
+ * stream) and thread-safe.  The return value reports argument validation
+ * and launch errors.  Execution errors surface at the caller's next
+ * synchronisation, or, for the library's own bounded waits, through
+ * norm_get_device_error.  Results are bitwise reproducible run to run for a
+ * given shape and device: every reduction, including the dgamma/dbeta
+ * column sums, is done in a fixed order without atomics.
+ */
+#ifndef GBNORM_H
+#define GBNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that callers need no CUDA
+ * header. */
+struct CUstream_st;
+typedef struct CUstream_st *norm_stream_t;
+
+/* Largest supported row length (columns). */
+#define NORM_MAX_N 262144
+
+typedef enum {
+    NORM_RMS = 0,   /* RMSNorm: no mean, no beta */
+    NORM_LAYER = 1  /* LayerNorm */
+} norm_mode_t;
+
+typedef enum {
+    NORM_OK = 0,
+    NORM_ERR_NULL = 1,           /* a required pointer is NULL */
+    NORM_ERR_SHAPE = 2,          /* M < 1, N < 8, N > NORM_MAX_N or N % 8 != 0 */
+    NORM_ERR_ALIGN = 3,          /* a pointer is not 16-byte aligned */
+    NORM_ERR_MODE = 4,           /* unknown mode, or a pointer given that the
+                                    mode forbids (beta/mean/dbeta for RMS) or
+                                    missing that it needs (mean for LAYER) */
+    NORM_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than required */
+    NORM_ERR_UNSUPPORTED = 6,    /* shape cannot be scheduled on this device */
+    NORM_ERR_CUDA = 7,           /* a CUDA runtime call failed */
+    NORM_ERR_DEVICE_TIMEOUT = 8, /* a kernel gave up a bounded wait */
+    NORM_ERR_ARG = 9             /* eps is negative or not finite */
+} norm_status_t;
+
+/*
+ * norm_fwd -- forward pass.
+ *   x      bf16 [M, N] input
+ *   gamma  bf16 [N] scale
+ *   beta   bf16 [N] shift; LAYER only (NULL means zero); must be NULL for RMS
+ *   eps    added to the variance (LAYER) or mean square (RMS) inside the
+ *          square root; finite and >= 0
+ *   y      bf16 [M, N] output
+ *   rstd   fp32 [M] output, 1/sqrt(var + eps) or 1/sqrt(meansq + eps)
+ *   mean   fp32 [M] output; required for LAYER, must be NULL for RMS
+ */
+norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta,
+                       int64_t M, int64_t N, float eps, norm_mode_t mode,
+                       void *y, float *rstd, float *mean,
+                       norm_stream_t stream);
+
+/*
+ * norm_bwd_workspace_bytes -- size of the workspace norm_bwd needs for this
+ * shape on the CURRENT device (it holds one fp32 row of dgamma partial sums,
+ * and for LAYER one of dbeta partial sums, per column-reduction split).
+ */
+norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode,
+                                       size_t *bytes);
+
+/*
+ * norm_bwd -- backward pass, reusing the statistics saved by norm_fwd.
+ *   dy      bf16 [M, N] gradient of y
+ *   x       bf16 [M, N] forward input
+ *   gamma   bf16 [N]
+ *   rstd    fp32 [M] from norm_fwd
+ *   mean    fp32 [M] from norm_fwd; required for LAYER, NULL for RMS
+ *   dx      bf16 [M, N] output
+ *   dgamma  fp32 [N] output
+ *   dbeta   fp32 [N] output for LAYER (NULL skips it); must be NULL for RMS
+ *   workspace, workspace_bytes  device scratch of at least
+ *           norm_bwd_workspace_bytes(M, N, mode) bytes, 16-byte aligned; its
+ *           contents on entry are ignored.  Two calls that overlap in time
+ *           must not share a workspace.
+ * Two kernels run on `stream`: the fused row pass (dx plus per-CTA partial
+ * column sums written to the workspace) and a fixed-order reduction of the
+ * partials into dgamma/dbeta.
+ */
+norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma,
+                       const float *rstd, const float *mean, int64_t M,
+                       int64_t N, norm_mode_t mode, void *dx, float *dgamma,
+                       float *dbeta, void *workspace, size_t workspace_bytes,
+                       norm_stream_t stream);
+
+/*
+ * norm_plan -- the launch plan the library uses for one pass (backward = 0
+ * for norm_fwd, 1 for norm_bwd) of an [M, N] problem: how rows are split
+ * across threads, CTAs and clusters, and how many tiles are kept in flight.
+ * With sm_count <= 0 it describes the CURRENT device (occupancy queried
+ * through the CUDA runtime) and equals what norm_fwd / norm_bwd launch.
+ * With sm_count > 0 and smem_optin_bytes > 0 it computes the plan for that
+ * hypothetical device without any CUDA call, assuming one resident CTA per
+ * SM (for host-side checks and planning).
+ */
+typedef struct {
+    int32_t cluster;           /* CTAs per thread-block cluster; each owns
+                                  N / cluster consecutive columns */
+    int32_t cols_per_cta;      /* N / cluster */
+    int32_t threads_per_row;   /* threads cooperating on one row (slice) */
+    int32_t chunks_per_thread; /* 16-byte chunks of a row per thread */
+    int32_t groups;            /* rows processed concurrently per CTA */
+    int32_t rows_per_group;    /* rows each group takes from a tile */
+    int32_t rows_per_tile;     /* groups * rows_per_group */
+    int32_t stages;            /* tiles in flight per CTA */
+    int32_t threads;           /* CTA size */
+    int32_t smem_bytes;        /* dynamic shared memory per CTA */
+    int64_t tiles;             /* ceil(M / rows_per_tile) */
+    int32_t grid;              /* CTAs launched */
+    int32_t partials;          /* clusters launched = partial rows written
+                                  by the backward pass */
+} norm_plan_t;
+
+norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
+                        int sm_count, int smem_optin_bytes, norm_plan_t *out);
+
+/* Static, human-readable description of a status code. */
+const char *norm_strerror(norm_status_t status);
+
+/*
+ * norm_get_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word, which kernels set when one of their bounded
+ * waits on an asynchronous copy gives up.  Returns NORM_OK or
+ * NORM_ERR_DEVICE_TIMEOUT (or NORM_ERR_CUDA).
+ */
+norm_status_t norm_get_device_error(norm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNORM_H */

@@ -1,0 +1,15 @@
+"""GB300 (sm_103a) RMSNorm / LayerNorm forward and backward.
+
+The computation runs in hand-written CUDA kernels behind the C ABI of
+include/gbnorm.h (libgbnorm.so); this package is its thin Python binding plus
+the seeded synthetic workloads used by the tests and the benchmark.
+"""
+from ._binding import (LAYER, RMS, NormError, declared_functions, lib, library_path,
+                       norm_bwd, norm_bwd_workspace_bytes, norm_fwd, norm_get_device_error, norm_plan,
+                       strerror)
+from .builder import build
+
+__all__ = [
+    "RMS", "LAYER", "NormError", "norm_fwd", "norm_bwd", "norm_bwd_workspace_bytes",
+    "norm_get_device_error", "norm_plan", "strerror", "lib", "library_path", "declared_functions", "build",
+]

@@ -1,0 +1,232 @@
+"""ctypes binding of libgbnorm.so (the C ABI of include/gbnorm.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the library.  PyTorch supplies device memory (outputs and the
+backward workspace are allocated with torch when the caller passes none) and
+the stream (torch's current stream unless one is given).  There is no
+fallback: if the shared library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import builder as _build
+
+RMS = 0
+LAYER = 1
+
+STATUS = {
+    0: "NORM_OK",
+    1: "NORM_ERR_NULL",
+    2: "NORM_ERR_SHAPE",
+    3: "NORM_ERR_ALIGN",
+    4: "NORM_ERR_MODE",
+    5: "NORM_ERR_WORKSPACE",
+    6: "NORM_ERR_UNSUPPORTED",
+    7: "NORM_ERR_CUDA",
+    8: "NORM_ERR_DEVICE_TIMEOUT",
+    9: "NORM_ERR_ARG",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class Plan(ctypes.Structure):
+    """Mirror of norm_plan_t."""
+    _fields_ = [("cluster", ctypes.c_int32), ("cols_per_cta", ctypes.c_int32),
+                ("threads_per_row", ctypes.c_int32), ("chunks_per_thread", ctypes.c_int32),
+                ("groups", ctypes.c_int32), ("rows_per_group", ctypes.c_int32),
+                ("rows_per_tile", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
+                ("partials", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class NormError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({strerror(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded ctypes library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it first "
+                    "(python -m memory_bound_normalization_rmsnorm_gb300.builder)")
+            L = ctypes.CDLL(path)
+            L.norm_fwd.argtypes = [_vp, _vp, _vp, _i64, _i64, ctypes.c_float, ctypes.c_int,
+                                   _vp, _vp, _vp, _vp]
+            L.norm_fwd.restype = ctypes.c_int
+            L.norm_bwd_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+            L.norm_bwd_workspace_bytes.restype = ctypes.c_int
+            L.norm_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp,
+                                   _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            L.norm_bwd.restype = ctypes.c_int
+            L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.POINTER(Plan)]
+            L.norm_plan.restype = ctypes.c_int
+            L.norm_strerror.argtypes = [ctypes.c_int]
+            L.norm_strerror.restype = ctypes.c_char_p
+            L.norm_get_device_error.argtypes = [_vp]
+            L.norm_get_device_error.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def declared_functions():
+    """Names of the functions include/gbnorm.h declares."""
+    hdr = os.path.join(_build.INCLUDE, "gbnorm.h")
+    text = open(hdr).read()
+    return sorted(set(re.findall(r"^(?:norm_status_t|const char \*)\s*(norm_\w+)\(",
+                                 text, flags=re.M)))
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().norm_strerror(int(status)).decode()
+    except RuntimeError:
+        return STATUS.get(status, "unknown")
+
+
+def _ptr(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        return _vp(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return _vp(stream.cuda_stream)
+    return _vp(int(stream))
+
+
+def _check_tensor(t, name, dtype, shape, device):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _rows(x):
+    if x.dim() < 1:
+        raise ValueError("x must have at least one dimension")
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    return M, N
+
+
+def norm_fwd(x, gamma, beta=None, eps=1e-5, mode=RMS, *, y=None, rstd=None, mean=None,
+             stream=None):
+    """Forward pass over the last dimension of x (bf16, contiguous).
+
+    Returns (y, rstd, mean); mean is None for RMSNorm.  rstd/mean have the
+    shape of x without its last dimension."""
+    mode = int(mode)
+    M, N = _rows(x)
+    dev = x.device
+    bf, f32 = torch.bfloat16, torch.float32
+    _check_tensor(x, "x", bf, x.shape, dev)
+    _check_tensor(gamma, "gamma", bf, (N,), dev)
+    _check_tensor(beta, "beta", bf, (N,), dev)
+    if y is None:
+        y = torch.empty_like(x)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=f32, device=dev)
+    if mode == LAYER and mean is None:
+        mean = torch.empty(x.shape[:-1], dtype=f32, device=dev)
+    _check_tensor(y, "y", bf, x.shape, dev)
+    _check_tensor(rstd, "rstd", f32, x.shape[:-1], dev)
+    _check_tensor(mean, "mean", f32, x.shape[:-1], dev)
+    st = lib().norm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), M, N, float(eps), mode, _ptr(y),
+                        _ptr(rstd), _ptr(mean), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_fwd")
+    return y, rstd, mean
+
+
+def norm_bwd_workspace_bytes(M, N, mode=RMS) -> int:
+    out = ctypes.c_size_t(0)
+    st = lib().norm_bwd_workspace_bytes(int(M), int(N), int(mode), ctypes.byref(out))
+    if st != 0:
+        raise NormError(st, "norm_bwd_workspace_bytes")
+    return int(out.value)
+
+
+def norm_bwd(dy, x, gamma, rstd, mean=None, mode=RMS, *, dx=None, dgamma=None, dbeta=None,
+             want_dbeta=True, workspace=None, stream=None):
+    """Backward pass.  Returns (dx, dgamma, dbeta); dbeta is None for RMSNorm
+    (or when want_dbeta is False)."""
+    mode = int(mode)
+    M, N = _rows(x)
+    dev = x.device
+    bf, f32 = torch.bfloat16, torch.float32
+    _check_tensor(x, "x", bf, x.shape, dev)
+    _check_tensor(dy, "dy", bf, x.shape, dev)
+    _check_tensor(gamma, "gamma", bf, (N,), dev)
+    _check_tensor(rstd, "rstd", f32, x.shape[:-1], dev)
+    _check_tensor(mean, "mean", f32, x.shape[:-1], dev)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dgamma is None:
+        dgamma = torch.empty(N, dtype=f32, device=dev)
+    if mode == LAYER and want_dbeta and dbeta is None:
+        dbeta = torch.empty(N, dtype=f32, device=dev)
+    _check_tensor(dx, "dx", bf, x.shape, dev)
+    _check_tensor(dgamma, "dgamma", f32, (N,), dev)
+    _check_tensor(dbeta, "dbeta", f32, (N,), dev)
+    if workspace is None:
+        with torch.cuda.device(dev):
+            nbytes = norm_bwd_workspace_bytes(M, N, mode)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    st = lib().norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(mean), M, N, mode,
+                        _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_bwd")
+    return dx, dgamma, dbeta
+
+
+def norm_plan(M, N, mode=RMS, backward=False, sm_count=0, smem_optin=0) -> dict:
+    """Launch plan of one pass (see norm_plan in gbnorm.h).  sm_count > 0
+    plans for a hypothetical device without touching CUDA."""
+    out = Plan()
+    st = lib().norm_plan(int(M), int(N), int(mode), 1 if backward else 0, int(sm_count),
+                         int(smem_optin), ctypes.byref(out))
+    if st != 0:
+        raise NormError(st, "norm_plan")
+    return out.as_dict()
+
+
+def norm_get_device_error(stream=None, device=None):
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    return lib().norm_get_device_error(_stream(stream, dev))

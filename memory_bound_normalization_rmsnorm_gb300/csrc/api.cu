@@ -1,0 +1,514 @@
+// api.cu -- the C ABI declared in include/gbnorm.h: argument validation,
+// the per-shape launch plan, and the kernel launches.
+//
+// Launch plan (variant choice by row length N).  Rows are cut into 16-byte
+// chunks; a group of `tpr` threads owns one row and each thread K chunks of
+// it, in registers.  Short rows (N <= 256) use a group of up to one warp,
+// so a warp holds one or several rows and reduces with shuffles only; longer
+// rows use several warps per row (shuffles plus a named-barrier fold); rows
+// too long for one CTA are split across a thread-block cluster whose CTAs
+// exchange partial statistics through distributed shared memory.  The
+// persistent-reduction threshold of about 1024 elements named in "PyTorch
+// atinge desempenho SOTA em normalizacao com torch.compile" (paragraph on
+// Inductor) is where the warp-per-row regime ends here as well
+// (N <= 2048 for the forward pass, whose rows sit in registers).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
+#include <tuple>
+
+#include "../../include/gbnorm.h"
+#include "common.cuh"
+
+namespace gbn {
+namespace {
+
+__device__ unsigned g_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+  unsigned *err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+std::set<std::pair<int, const void *>> g_attr_done;
+std::map<std::tuple<int, int, int64_t, int, int>, Plan> g_plans;
+
+norm_status_t device_info(DeviceInfo *out, int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return NORM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (d.sms == 0) {
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return NORM_ERR_CUDA;
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+      cudaGetLastError();
+      return NORM_ERR_CUDA;
+    }
+    d.err = static_cast<unsigned *>(p);
+    d.smem_optin = optin;
+    d.sms = sms;
+  }
+  *out = d;
+  *dev_out = dev;
+  return NORM_OK;
+}
+
+// Sets the per-function attributes a launch needs (once per device).
+norm_status_t prepare_function(int dev, const void *fn, int smem_optin) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_attr_done.count({dev, fn})) return NORM_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  g_attr_done.insert({dev, fn});
+  return NORM_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pow2ceil(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Optional plan override for tuning sweeps: GBNORM_PLAN="C=2,tpr=256,rpg=1,S=4"
+// (any subset).  Fields left out keep the heuristic's choice.
+struct Override {
+  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0;
+  bool any = false;
+};
+
+Override read_override() {
+  Override o;
+  const char *s = std::getenv("GBNORM_PLAN");
+  if (!s || !*s) return o;
+  char buf[256];
+  std::snprintf(buf, sizeof buf, "%s", s);
+  for (char *tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
+    char key[32];
+    int val = 0;
+    if (std::sscanf(tok, "%31[^=]=%d", key, &val) != 2) continue;
+    if (!std::strcmp(key, "C")) o.C = val;
+    else if (!std::strcmp(key, "tpr")) o.tpr = val;
+    else if (!std::strcmp(key, "rpg")) o.rpg = val;
+    else if (!std::strcmp(key, "S")) o.S = val;
+    else if (!std::strcmp(key, "G")) o.G = val;
+    else if (!std::strcmp(key, "ctas")) o.ctas = val;
+    o.any = true;
+  }
+  return o;
+}
+
+int round_k(int K, bool bwd) {
+  if (bwd) return K;  // 1..4 all compiled
+  return K == 7 ? 8 : K;
+}
+
+// Shape part of the plan for one pass: everything except the grid size.
+// Pure host arithmetic (no CUDA call).  `bwd` selects the backward kernel
+// (two tensors per stage, at most kMaxKBwd chunks per thread).
+norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
+                         const Override &ov, Plan *out) {
+  const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
+  const int ntensors = bwd ? 2 : 1;
+  const int nc = N / 8;
+  Plan p;
+
+  // Preferred chunks per thread (register budget without spills); up to
+  // kmax is allowed when a row slice needs it.
+  const int kpref = bwd ? 2 : 4;
+
+  // Column split: the smallest power-of-two cluster (up to 8) whose per-CTA
+  // slice fits kMaxThreads threads x kpref chunks, else the smallest (up to
+  // 16) that fits kmax chunks.  Slices are ceil(nc / C) chunks; the last CTA
+  // of a cluster takes the remainder.
+  int C = 1;
+  while (C < 8 && ceil_div(nc, C) > kMaxThreads * kpref) C <<= 1;
+  while (C <= 16 && ceil_div(nc, C) > kMaxThreads * kmax) C <<= 1;
+  if (ov.C) C = ov.C;
+  if (C < 1 || C > 16) return NORM_ERR_UNSUPPORTED;
+  p.C = C;
+  p.nsc = ceil_div(nc, C);
+  p.NS = p.nsc * 8;
+  if ((C - 1) * p.nsc >= nc) return NORM_ERR_UNSUPPORTED;  // a CTA would own nothing
+
+  // Threads per row: whole chunks per lane, about kpref chunks per thread.
+  int tpr;
+  if (p.nsc <= 32) tpr = pow2ceil(p.nsc);
+  else tpr = std::min(kMaxThreads, std::max(32, pow2ceil(ceil_div(p.nsc, kpref))));
+  if (ov.tpr) tpr = ov.tpr;
+  if (tpr < 1 || tpr > kMaxThreads || (tpr > 32 && tpr % 32) || (tpr < 32 && 32 % tpr))
+    return NORM_ERR_UNSUPPORTED;
+  p.tpr = tpr;
+  p.K = round_k(ceil_div(p.nsc, tpr), bwd);
+  if (p.K > kmax) return NORM_ERR_UNSUPPORTED;
+
+  int G = kMaxThreads / tpr;
+  if (tpr > 32) G = std::min(G, 8);
+  if (ov.G) G = ov.G;
+  if (G < 1 || G * tpr > kMaxThreads || (tpr > 32 && G > 15))
+    return NORM_ERR_UNSUPPORTED;
+
+  // Rows per tile: about 32 KB of stage per tensor, one row per group in a
+  // cluster (every row there costs a cluster barrier).
+  const int row_bytes = p.NS * 2;
+  int rpg = 1;
+  if (C == 1) rpg = std::max(1, (32 * 1024) / (row_bytes * G));
+  if (ov.rpg) rpg = ov.rpg;
+  if (rpg < 1 || (C > 1 && rpg != 1)) return NORM_ERR_UNSUPPORTED;
+
+  // Shrink the tile until at least two stages fit in shared memory.
+  const int budget = smem_optin - 1024;
+  const bool cl = C > 1;
+  int S = 0;
+  for (;;) {
+    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, tpr, ntensors, bwd, cl);
+    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, tpr, ntensors, bwd, cl);
+    const int per_stage = static_cast<int>(L2.total - L1.total);
+    const int fixed = static_cast<int>(L1.total) - per_stage;
+    S = (budget - fixed) / per_stage;
+    if (S >= 2 || ov.rpg || ov.G || (rpg == 1 && G == 1)) break;
+    if (rpg > 1) rpg = (rpg + 1) / 2;
+    else G = (G + 1) / 2;
+  }
+  S = std::min(S, 8);
+  if (ov.S) S = ov.S;
+  if (S < 2) return NORM_ERR_UNSUPPORTED;
+  p.G = G;
+  p.rpg = rpg;
+  p.RT = G * rpg;
+  p.S = S;
+  p.threads = G * tpr;
+  if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
+  const SmemLayout L = make_layout(p.RT, p.NS, S, G, tpr, ntensors, bwd, cl);
+  if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
+  // One stage's bytes are counted by a single mbarrier transaction count.
+  if (L.stage_bytes >= (1u << 20)) return NORM_ERR_UNSUPPORTED;
+  // The backward column-partial fold reuses the ring.
+  if (bwd && static_cast<int64_t>(2) * G * p.NS * 4 > static_cast<int64_t>(S) * L.stage_bytes)
+    return NORM_ERR_UNSUPPORTED;
+  p.smem = L.total;
+  p.ntiles = (M + p.RT - 1) / p.RT;
+  *out = p;
+  return NORM_OK;
+}
+
+void set_grid(Plan &p, int64_t resident_clusters) {
+  const int64_t clusters = std::min<int64_t>(resident_clusters, p.ntiles);
+  p.P = static_cast<int>(clusters);
+  p.grid = static_cast<int>(clusters * p.C);
+}
+
+// Full plan on the current device: shape part plus the occupancy-derived
+// grid (persistent: as many CTAs or clusters as can be resident at once).
+norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_t M, int N,
+                        Plan *out) {
+  const Override ov = read_override();
+  const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, 0);
+  if (!ov.any) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      *out = it->second;
+      return NORM_OK;
+    }
+  }
+  Plan p;
+  norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p);
+  if (st != NORM_OK) return st;
+
+  const void *fn = bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1) : fwd_kernel_ptr(mode, p.K, p.C > 1);
+  if (!fn) return NORM_ERR_UNSUPPORTED;
+  st = prepare_function(dev, fn, d.smem_optin);
+  if (st != NORM_OK) return st;
+
+  int64_t resident = 0;
+  if (p.C == 1) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, p.threads, p.smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return NORM_ERR_CUDA;
+    }
+    if (ov.ctas) per_sm = std::min(per_sm, ov.ctas);
+    resident = static_cast<int64_t>(per_sm) * d.sms;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = p.C;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(p.C * 64);
+    cfg.blockDim = dim3(p.threads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return NORM_ERR_CUDA;
+    }
+    resident = nclusters;
+  }
+  if (resident < 1) return NORM_ERR_UNSUPPORTED;
+  set_grid(p, resident);
+
+  if (!ov.any) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_plans[key] = p;
+  }
+  *out = p;
+  return NORM_OK;
+}
+
+norm_status_t launch(const void *fn, const Plan &p, const NormArgs &args, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (p.C > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = p.C;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  NormArgs a = args;
+  void *kargs[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, fn, kargs) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return NORM_OK;
+}
+
+norm_status_t check_common(int64_t M, int64_t N, norm_mode_t mode) {
+  if (mode != NORM_RMS && mode != NORM_LAYER) return NORM_ERR_MODE;
+  if (M < 1 || N < 8 || N > NORM_MAX_N || (N % 8) != 0) return NORM_ERR_SHAPE;
+  if (M > (int64_t(1) << 40)) return NORM_ERR_SHAPE;
+  return NORM_OK;
+}
+
+NormArgs base_args(const Plan &p, int64_t M, int N) {
+  NormArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.M = M;
+  a.N = N;
+  a.NS = p.NS;
+  a.nsc = p.nsc;
+  a.tpr = p.tpr;
+  a.G = p.G;
+  a.rpg = p.rpg;
+  a.RT = p.RT;
+  a.S = p.S;
+  a.P = p.P;
+  a.ntiles = p.ntiles;
+  a.invN = 1.0f / static_cast<float>(N);
+  return a;
+}
+
+}  // namespace
+}  // namespace gbn
+
+using namespace gbn;
+
+extern "C" {
+
+norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64_t M,
+                       int64_t N, float eps, norm_mode_t mode, void *y, float *rstd,
+                       float *mean, norm_stream_t stream) {
+  if (!x || !gamma || !y || !rstd) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  if (mode == NORM_RMS && (beta || mean)) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return NORM_ERR_ARG;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(y) || !aligned16(rstd) ||
+      (beta && !aligned16(beta)) || (mean && !aligned16(mean)))
+    return NORM_ERR_ALIGN;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  NormArgs a = base_args(p, M, static_cast<int>(N));
+  a.x = static_cast<const uint16_t *>(x);
+  a.gamma = static_cast<const uint16_t *>(gamma);
+  a.beta = static_cast<const uint16_t *>(beta);
+  a.out = static_cast<uint16_t *>(y);
+  a.rstd = rstd;
+  a.mean = mean;
+  a.err = d.err;
+  a.eps = eps;
+  return launch(fwd_kernel_ptr(mode, p.K, p.C > 1), p, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, size_t *bytes) {
+  if (!bytes) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  *bytes = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
+           (mode == NORM_LAYER ? 2u : 1u);
+  return NORM_OK;
+}
+
+norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
+                       const float *mean, int64_t M, int64_t N, norm_mode_t mode, void *dx,
+                       float *dgamma, float *dbeta, void *workspace, size_t workspace_bytes,
+                       norm_stream_t stream) {
+  if (!dy || !x || !gamma || !rstd || !dx || !dgamma) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  if (mode == NORM_RMS && (mean || dbeta)) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(rstd) ||
+      !aligned16(dx) || !aligned16(dgamma) || (mean && !aligned16(mean)) ||
+      (dbeta && !aligned16(dbeta)) || (workspace && !aligned16(workspace)))
+    return NORM_ERR_ALIGN;
+  if (!workspace) return NORM_ERR_WORKSPACE;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  const size_t need = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
+                      (mode == NORM_LAYER ? 2u : 1u);
+  if (workspace_bytes < need) return NORM_ERR_WORKSPACE;
+  NormArgs a = base_args(p, M, static_cast<int>(N));
+  a.x = static_cast<const uint16_t *>(x);
+  a.dy = static_cast<const uint16_t *>(dy);
+  a.gamma = static_cast<const uint16_t *>(gamma);
+  a.out = static_cast<uint16_t *>(dx);
+  a.rstd = const_cast<float *>(rstd);
+  a.mean = const_cast<float *>(mean);
+  a.ws = static_cast<float *>(workspace);
+  a.err = d.err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch(bwd_kernel_ptr(mode, p.K, p.C > 1), p, a, s)) != NORM_OK) return st;
+
+  const int nparts = (mode == NORM_LAYER && dbeta) ? 2 : 1;
+  const void *rfn = reduce_kernel_ptr();
+  const float *ws = static_cast<const float *>(workspace);
+  int P = p.P, n = static_cast<int>(N);
+  void *rargs[] = {&ws, &P, &n, &dgamma, &dbeta};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 127) / 128, nparts);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  if (cudaLaunchKernelExC(&cfg, rfn, rargs) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return NORM_OK;
+}
+
+norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, int sm_count,
+                        int smem_optin_bytes, norm_plan_t *out) {
+  if (!out) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  const bool bwd = backward != 0;
+  Plan p;
+  if (sm_count > 0) {
+    if (smem_optin_bytes <= 0) return NORM_ERR_ARG;
+    if ((st = shape_plan(mode, bwd, M, static_cast<int>(N), smem_optin_bytes, read_override(),
+                         &p)) != NORM_OK)
+      return st;
+    set_grid(p, sm_count / p.C);
+    if (p.grid < 1) return NORM_ERR_UNSUPPORTED;
+  } else {
+    DeviceInfo d;
+    int dev = 0;
+    if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+    if ((st = make_plan(d, dev, mode, bwd, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  }
+  out->cluster = p.C;
+  out->cols_per_cta = p.NS;
+  out->threads_per_row = p.tpr;
+  out->chunks_per_thread = p.K;
+  out->groups = p.G;
+  out->rows_per_group = p.rpg;
+  out->rows_per_tile = p.RT;
+  out->stages = p.S;
+  out->threads = p.threads;
+  out->smem_bytes = static_cast<int32_t>(p.smem);
+  out->tiles = p.ntiles;
+  out->grid = p.grid;
+  out->partials = p.P;
+  return NORM_OK;
+}
+
+const char *norm_strerror(norm_status_t s) {
+  switch (s) {
+    case NORM_OK: return "success";
+    case NORM_ERR_NULL: return "a required pointer is NULL";
+    case NORM_ERR_SHAPE: return "unsupported shape (need M >= 1, 8 <= N <= NORM_MAX_N, N % 8 == 0)";
+    case NORM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case NORM_ERR_MODE: return "mode/argument mismatch (beta, mean, dbeta only for LayerNorm; mean required there)";
+    case NORM_ERR_WORKSPACE: return "workspace missing or too small";
+    case NORM_ERR_UNSUPPORTED: return "shape cannot be scheduled on this device";
+    case NORM_ERR_CUDA: return "CUDA runtime error";
+    case NORM_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on an asynchronous copy";
+    case NORM_ERR_ARG: return "eps must be finite and >= 0";
+  }
+  return "unknown status";
+}
+
+norm_status_t norm_get_device_error(norm_stream_t stream) {
+  DeviceInfo d;
+  int dev = 0;
+  norm_status_t st = device_info(&d, &dev);
+  if (st != NORM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned h = 0;
+  if (cudaMemcpyAsync(&h, d.err, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(d.err, 0, sizeof h, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return h ? NORM_ERR_DEVICE_TIMEOUT : NORM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,303 @@
+// bwd.cu -- backward RMSNorm / LayerNorm: one fused row pass (dx, plus
+// per-CTA partial column sums for dgamma and dbeta) and a fixed-order
+// reduction of those partials.
+//
+// Follows the backward-pass paragraphs of "PyTorch atinge desempenho SOTA
+// em normalizacao com torch.compile" (matsubara.tec.br):
+//   - dX, dW and dB computed in ONE kernel so that dy and x are read once
+//     (the fused-reduction paragraph);
+//   - the column reduction split across CTAs, each CTA summing many rows
+//     into a partial row of a workspace that a second kernel reduces,
+//     without atomics (the split-reduction paragraph);
+//   - rows per partial set by how many CTAs run (the SPLIT_SIZE paragraph)
+//     and several loads kept in flight (the num_stages paragraph).
+// The saved rstd (and mean) of the forward pass are reused, not recomputed.
+#include "common.cuh"
+#include "ptx.cuh"
+#include "rowops.cuh"
+
+namespace gbn {
+
+namespace {
+
+// Issues tile `tile` into stage `s`: the rows' statistics with 4-byte
+// cp.async copies (one completion arrival per lane of warp 0), then x and
+// dy with bulk copies.  Must be called by all 32 lanes of warp 0.
+template <int MODE, bool CLUSTER>
+__device__ __forceinline__ void issue_bwd_tile(const NormArgs &a,
+                                               const SmemLayout &L,
+                                               unsigned char *smem, int64_t tile,
+                                               int s, int col0, int nsc_me,
+                                               uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
+  unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
+  float *stats = reinterpret_cast<float *>(smem + L.stats_off) +
+                 static_cast<size_t>(s) * a.RT * 2;
+  const int64_t row0 = tile * a.RT;
+  const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
+  for (int r = lane; r < nrows; r += 32) {
+    cp_async_4(stats + 2 * r, a.rstd + row0 + r);
+    if (MODE == kLayer) cp_async_4(stats + 2 * r + 1, a.mean + row0 + r);
+  }
+  cp_async_mbar_arrive(full);
+  __syncwarp();
+  if (lane == 0) {
+    if (!CLUSTER) {
+      const uint32_t bytes = static_cast<uint32_t>(nrows) * a.N * 2u;
+      mbar_arrive_expect_tx(full, 2u * bytes);
+      bulk_g2s(dst, a.x + row0 * a.N, bytes, full, pol);
+      bulk_g2s(dst + L.tensor_bytes, a.dy + row0 * a.N, bytes, full, pol);
+    } else {
+      const uint32_t bytes = static_cast<uint32_t>(nsc_me) * 16u;
+      const uint32_t stride = static_cast<uint32_t>(a.NS) * 2u;
+      mbar_arrive_expect_tx(full, 2u * bytes * nrows);
+      for (int r = 0; r < nrows; ++r) {
+        const int64_t off = (row0 + r) * a.N + col0;
+        bulk_g2s(dst + r * stride, a.x + off, bytes, full, pol);
+        bulk_g2s(dst + L.tensor_bytes + r * stride, a.dy + off, bytes, full, pol);
+      }
+    }
+  }
+}
+
+template <int MODE, int K, bool CLUSTER>
+__global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, CLUSTER);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+  float *red = reinterpret_cast<float *>(smem + L.red_off);
+  float *xch = reinterpret_cast<float *>(smem + L.xch_off);
+  const float *stats_all = reinterpret_cast<const float *>(smem + L.stats_off);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+
+  const int tid = threadIdx.x;
+  const int g = tid / a.tpr;
+  const int t = tid - g * a.tpr;
+  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
+  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
+  const int col0 = crank * a.NS;
+  // Chunks this CTA owns (the last CTA of a cluster may own fewer).
+  const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
+
+  if (tid == 0) {
+    for (int s = 0; s < a.S; ++s) mbar_init(full + s, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+
+  uint4 gv[K];
+  float accg[K][8], accb[K][8];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int c = t + k * a.tpr;
+    gv[k] = (c < nsc_me) ? ld_global_nc_v4(a.gamma + col0 + c * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      accg[k][e] = 0.f;
+      accb[k][e] = 0.f;
+    }
+  }
+
+  if (CLUSTER) cluster_sync(); else __syncthreads();
+
+  const uint64_t pol = l2_evict_first_policy();
+  if (tid < 32) {
+    for (int j = 0; j < a.S; ++j) {
+      const int64_t tile = cid + j * ncl;
+      if (tile < a.ntiles) issue_bwd_tile<MODE, CLUSTER>(a, L, smem, tile, j, col0, nsc_me, pol);
+    }
+  }
+
+  int rpar = 0, xpar = 0;
+  for (int64_t it = 0;; ++it) {
+    const int64_t tile = cid + it * ncl;
+    if (tile >= a.ntiles) break;
+    const int s = static_cast<int>(it % a.S);
+    const uint32_t par = static_cast<uint32_t>((it / a.S) & 1);
+    mbar_wait(full + s, par, a.err, abort_flag);
+    const int64_t row0 = tile * a.RT;
+    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
+    const unsigned char *stx = smem + static_cast<size_t>(s) * L.stage_bytes;
+    const unsigned char *std_ = stx + L.tensor_bytes;
+    const float *stats = stats_all + static_cast<size_t>(s) * a.RT * 2;
+
+    for (int q = 0; q < a.rpg; ++q) {
+      const int r = g + q * a.G;
+      const bool active = r < nrows;
+      const size_t roff = static_cast<size_t>(r) * a.NS * 2;
+      float rs = 0.f, mu = 0.f;
+      if (active) {
+        rs = stats[2 * r];
+        if (MODE == kLayer) mu = stats[2 * r + 1];
+      }
+      uint4 xv[K], dv[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int c = t + k * a.tpr;
+        const bool ok = active && c < nsc_me;
+        xv[k] = ok ? *reinterpret_cast<const uint4 *>(stx + roff + c * 16) : make_uint4(0, 0, 0, 0);
+        dv[k] = ok ? *reinterpret_cast<const uint4 *>(std_ + roff + c * 16) : make_uint4(0, 0, 0, 0);
+      }
+      // Row dot products sum(g) and sum(g * xhat); column partials.
+      float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = (bf_elem(xv[k], e) - mu) * rs;
+          const float d = bf_elem(dv[k], e);
+          const float gg = d * bf_elem(gv[k], e);
+          s2 = fmaf(gg, xh, s2);
+          if (MODE == kLayer) s1 += gg;
+          accg[k][e] = fmaf(d, xh, accg[k][e]);
+          if (MODE == kLayer) accb[k][e] += d;
+        }
+      }
+      Part p = group_allreduce<false>(Part{s1, s2, 0.f}, a.tpr, g, a.G, t, red, rpar);
+      if (CLUSTER) p = cluster_allreduce<false>(p, r, a.RT, t, xch, xpar);
+      const float av = (MODE == kLayer) ? p.a * a.invN : 0.f;
+      const float cv = p.b * a.invN;
+
+      if (active) {
+        uint16_t *dxrow = a.out + (row0 + r) * a.N + col0;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const int c = t + k * a.tpr;
+          if (c < nsc_me) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float xh = (bf_elem(xv[k], e) - mu) * rs;
+              const float gg = bf_elem(dv[k], e) * bf_elem(gv[k], e);
+              o[e] = rs * (gg - fmaf(xh, cv, av));
+            }
+            const uint4 packed = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                            pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+            st_global_cs_v4(dxrow + c * 8, packed);
+          }
+        }
+      }
+    }
+
+    __syncthreads();
+    if (tid < 32) {
+      const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
+      if (next < a.ntiles) {
+        if (tid == 0) fence_proxy_async_smem();
+        __syncwarp();
+        issue_bwd_tile<MODE, CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
+      }
+    }
+  }
+
+  // Column partials: fold the G groups of this CTA in group order through
+  // shared memory (the ring is idle now: every issued tile was consumed),
+  // then write one partial row slice per CTA.
+  __syncthreads();
+  float *accs = reinterpret_cast<float *>(smem);  // [G][NS] dgamma, [G][NS] dbeta
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int c = t + k * a.tpr;
+    if (c < nsc_me) {
+      float4 *dg = reinterpret_cast<float4 *>(accs + static_cast<size_t>(g) * a.NS + c * 8);
+      dg[0] = make_float4(accg[k][0], accg[k][1], accg[k][2], accg[k][3]);
+      dg[1] = make_float4(accg[k][4], accg[k][5], accg[k][6], accg[k][7]);
+      if (MODE == kLayer) {
+        float4 *db = reinterpret_cast<float4 *>(accs + static_cast<size_t>(a.G + g) * a.NS + c * 8);
+        db[0] = make_float4(accb[k][0], accb[k][1], accb[k][2], accb[k][3]);
+        db[1] = make_float4(accb[k][4], accb[k][5], accb[k][6], accb[k][7]);
+      }
+    }
+  }
+  __syncthreads();
+  const int nq = nsc_me * 2;      // float4s of this CTA's columns
+  const int nq_stride = a.NS / 4; // float4s per group row in shared memory
+  const int nparts = (MODE == kLayer) ? 2 : 1;
+  for (int w = 0; w < nparts; ++w) {
+    const float4 *src = reinterpret_cast<const float4 *>(accs + static_cast<size_t>(w) * a.G * a.NS);
+    float4 *dst = reinterpret_cast<float4 *>(a.ws + (static_cast<size_t>(w) * a.P + cid) * a.N + col0);
+    for (int j = tid; j < nq; j += blockDim.x) {
+      float4 acc = src[j];
+      for (int gg = 1; gg < a.G; ++gg) {
+        const float4 v = src[static_cast<size_t>(gg) * nq_stride + j];
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      dst[j] = acc;
+    }
+  }
+  if (CLUSTER) cluster_sync();
+}
+
+// dgamma[j] = sum over p of ws[p][j] (blockIdx.y = 0) and dbeta[j] = sum
+// over p of ws[P + p][j] (blockIdx.y = 1), p in increasing order within
+// each of the block's 8 warps' contiguous p ranges, the 8 warp sums then
+// added in warp order: a fixed order for a given P, so the result is
+// bitwise reproducible.  Each lane owns 4 consecutive columns.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(const float *__restrict__ ws,
+                                                              int P, int N,
+                                                              float *__restrict__ dgamma,
+                                                              float *__restrict__ dbeta) {
+  __shared__ float4 part[8][32];
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const float *src = ws + static_cast<size_t>(blockIdx.y) * P * N;
+  float *dst = blockIdx.y ? dbeta : dgamma;
+  const int col = (blockIdx.x * 32 + lane) * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < N) {
+    const int p0 = static_cast<int>((static_cast<int64_t>(P) * w) / 8);
+    const int p1 = static_cast<int>((static_cast<int64_t>(P) * (w + 1)) / 8);
+    int p = p0;
+    for (; p + 4 <= p1; p += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = __ldcg(reinterpret_cast<const float4 *>(src + static_cast<size_t>(p + u) * N + col));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+      }
+    }
+    for (; p < p1; ++p) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + static_cast<size_t>(p) * N + col));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+  }
+  part[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && col < N) {
+    float4 s = part[0][lane];
+#pragma unroll
+    for (int u = 1; u < 8; ++u) {
+      s.x += part[u][lane].x; s.y += part[u][lane].y;
+      s.z += part[u][lane].z; s.w += part[u][lane].w;
+    }
+    *reinterpret_cast<float4 *>(dst + col) = s;
+  }
+}
+
+template <int MODE, bool CLUSTER>
+const void *pick_bwd(int K) {
+  switch (K) {
+    case 1: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER>);
+    case 2: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER>);
+    case 3: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER>);
+    case 4: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER>);
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+const void *bwd_kernel_ptr(int mode, int K, bool cluster) {
+  if (mode == kRMS) return cluster ? pick_bwd<kRMS, true>(K) : pick_bwd<kRMS, false>(K);
+  return cluster ? pick_bwd<kLayer, true>(K) : pick_bwd<kLayer, false>(K);
+}
+
+const void *reduce_kernel_ptr() {
+  return reinterpret_cast<const void *>(&reduce_partials_kernel);
+}
+
+}  // namespace gbn

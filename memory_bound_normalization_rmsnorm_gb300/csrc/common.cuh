@@ -1,0 +1,114 @@
+// common.cuh -- types shared by the kernels and the host launcher.
+#pragma once
+#include <cstdint>
+
+namespace gbn {
+
+constexpr int kRMS = 0;
+constexpr int kLayer = 1;
+
+// Largest chunk counts per thread that are compiled (a chunk is 8 bf16 =
+// 16 bytes of one row).
+constexpr int kMaxKFwd = 8;
+constexpr int kMaxKBwd = 4;
+// Largest CTA (the kernels are compiled for at most this many threads, which
+// lets the compiler give each thread up to 128 registers).
+constexpr int kMaxThreads = 512;
+
+// Kernel arguments.  A "tile" is RT consecutive rows restricted to the
+// column slice [col0, col0 + NS) that one CTA of a cluster owns (the whole
+// row when the cluster has one CTA).  Each row of a tile is processed by a
+// group of `tpr` threads; a CTA has G groups; each group takes rpg rows of
+// every tile (RT = G * rpg).
+struct NormArgs {
+  const uint16_t *x;      // bf16 [M, N]
+  const uint16_t *dy;     // bf16 [M, N] (backward)
+  const uint16_t *gamma;  // bf16 [N]
+  const uint16_t *beta;   // bf16 [N] or null (forward, LayerNorm)
+  uint16_t *out;          // y (forward) or dx (backward), bf16 [M, N]
+  float *rstd;            // [M]: written by forward, read by backward
+  float *mean;            // [M]: same, LayerNorm only
+  float *ws;              // backward partial sums [P, N] (+ [P, N] for dbeta)
+  unsigned *err;          // device error word
+  int64_t M;
+  int64_t ntiles;
+  int N;    // row length
+  int NS;   // columns per CTA slice (N / cluster size)
+  int nsc;  // 16-byte chunks per slice (NS / 8)
+  int tpr;  // threads per row
+  int G;    // row groups per CTA
+  int rpg;  // rows per group per tile
+  int RT;   // rows per tile
+  int S;    // pipeline stages
+  int P;    // partial rows (backward) = number of clusters in the grid
+  float eps;
+  float invN;
+};
+
+// Byte offsets of the dynamic shared memory regions (all 16-byte aligned).
+struct SmemLayout {
+  uint32_t tensor_bytes;  // one tensor's share of a stage: RT * NS * 2
+  uint32_t stage_bytes;   // ntensors * tensor_bytes
+  uint32_t stats_off;     // backward: [S][RT][2] floats (rstd, mean)
+  uint32_t red_off;       // [2][G][W][4] floats, cross-warp group partials
+                          // (W = tpr / 32; only when tpr > 32)
+  uint32_t xch_off;       // [2][RT][4] floats, cross-CTA partials (clusters only)
+  uint32_t bar_off;       // [S] mbarriers
+  uint32_t flag_off;      // abort flag
+  uint32_t total;
+};
+
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) {
+  return a < b ? a : b;
+}
+
+__host__ __device__ inline uint32_t align16(uint32_t v) {
+  return (v + 15u) & ~15u;
+}
+
+__host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
+                                                  int tpr, int ntensors,
+                                                  bool stats, bool cluster) {
+  SmemLayout L;
+  L.tensor_bytes = static_cast<uint32_t>(RT) * static_cast<uint32_t>(NS) * 2u;
+  L.stage_bytes = L.tensor_bytes * static_cast<uint32_t>(ntensors);
+  uint32_t off = L.stage_bytes * static_cast<uint32_t>(S);
+  L.stats_off = off;
+  if (stats) off = align16(off + static_cast<uint32_t>(S * RT * 2) * 4u);
+  L.red_off = off;
+  if (tpr > 32) off = align16(off + static_cast<uint32_t>(2 * G * (tpr / 32) * 4) * 4u);
+  L.xch_off = off;
+  if (cluster) off = align16(off + static_cast<uint32_t>(2 * RT * 4) * 4u);
+  L.bar_off = off;
+  off = align16(off + static_cast<uint32_t>(S) * 8u);
+  L.flag_off = off;
+  off = align16(off + 4u);
+  L.total = off;
+  return L;
+}
+
+// Host-side launch plan.
+struct Plan {
+  int C = 1;       // CTAs per cluster (column split)
+  int NS = 0;      // columns per CTA
+  int nsc = 0;     // chunks per CTA slice
+  int tpr = 0;     // threads per row
+  int K = 0;       // chunks per thread
+  int G = 0;       // groups per CTA
+  int rpg = 1;     // rows per group per tile
+  int RT = 0;      // rows per tile
+  int S = 0;       // stages
+  int threads = 0; // G * tpr
+  uint32_t smem = 0;
+  int64_t ntiles = 0;
+  int grid = 0;    // CTAs
+  int P = 0;       // clusters in the grid (partial rows in backward)
+};
+
+// Kernel entry points, by (mode, K, cluster).  Return nullptr when that
+// combination is not compiled.
+const void *fwd_kernel_ptr(int mode, int K, bool cluster);
+const void *bwd_kernel_ptr(int mode, int K, bool cluster);
+const void *reduce_kernel_ptr();
+
+}  // namespace gbn

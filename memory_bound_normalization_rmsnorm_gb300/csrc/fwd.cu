@@ -1,0 +1,230 @@
+// fwd.cu -- forward RMSNorm / LayerNorm kernel (one fused pass per row:
+// row statistics, normalisation, scale and shift).
+//
+// Follows the forward-pass paragraph of "PyTorch atinge desempenho SOTA em
+// normalizacao com torch.compile" (a reduction along the contiguous
+// dimension followed by pointwise operations), fused into one kernel so
+// that HBM sees only the input and the output ("Kernel fusion elimina
+// gargalos de memoria" on the page "Otimizacao de Performance de GPU",
+// introl.com).
+//
+// Structure: a persistent grid; each CTA (or cluster of CTAs splitting the
+// columns) walks tiles of RT consecutive rows.  Thread 0 keeps S tiles in
+// flight with bulk asynchronous copies into a shared-memory ring, each
+// stage guarded by an mbarrier.  Row groups of `tpr` threads read their row
+// from shared memory into registers (16-byte chunks, conflict free), reduce
+// (warp butterfly, then warps of the group, then the CTAs of the cluster
+// through distributed shared memory), and write y with 16-byte streaming
+// stores.
+#include "common.cuh"
+#include "ptx.cuh"
+#include "rowops.cuh"
+
+namespace gbn {
+
+namespace {
+
+template <bool CLUSTER>
+__device__ __forceinline__ void issue_fwd_tile(const NormArgs &a,
+                                               const SmemLayout &L,
+                                               unsigned char *smem, int64_t tile,
+                                               int s, int col0, int nsc_me,
+                                               uint64_t pol) {
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
+  unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
+  const int64_t row0 = tile * a.RT;
+  const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
+  if (!CLUSTER) {
+    const uint32_t bytes = static_cast<uint32_t>(nrows) * a.N * 2u;
+    mbar_arrive_expect_tx(full, bytes);
+    bulk_g2s(dst, a.x + row0 * a.N, bytes, full, pol);
+  } else {
+    // Row r of the tile lands at r * NS * 2 (slice stride), nsc_me chunks.
+    const uint32_t bytes = static_cast<uint32_t>(nsc_me) * 16u;
+    const uint32_t stride = static_cast<uint32_t>(a.NS) * 2u;
+    mbar_arrive_expect_tx(full, bytes * nrows);
+    for (int r = 0; r < nrows; ++r)
+      bulk_g2s(dst + r * stride, a.x + (row0 + r) * a.N + col0, bytes, full, pol);
+  }
+}
+
+template <int MODE, int K, bool CLUSTER>
+__global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, CLUSTER);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+  float *red = reinterpret_cast<float *>(smem + L.red_off);
+  float *xch = reinterpret_cast<float *>(smem + L.xch_off);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+
+  const int tid = threadIdx.x;
+  const int g = tid / a.tpr;
+  const int t = tid - g * a.tpr;
+  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
+  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
+  const int col0 = crank * a.NS;
+  // Chunks this CTA owns (the last CTA of a cluster may own fewer).
+  const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
+
+  if (tid == 0) {
+    for (int s = 0; s < a.S; ++s) mbar_init(full + s, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+
+  // gamma (and beta) for this thread's chunks stay in registers for the
+  // whole kernel: the thread owns the same columns in every row.
+  uint4 gv[K], bv[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int c = t + k * a.tpr;
+    gv[k] = make_uint4(0, 0, 0, 0);
+    bv[k] = make_uint4(0, 0, 0, 0);
+    if (c < nsc_me) {
+      gv[k] = ld_global_nc_v4(a.gamma + col0 + c * 8);
+      if (MODE == kLayer && a.beta != nullptr)
+        bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
+    }
+  }
+
+  if (CLUSTER) cluster_sync(); else __syncthreads();
+
+  const uint64_t pol = l2_evict_first_policy();
+  if (tid == 0) {
+    for (int j = 0; j < a.S; ++j) {
+      const int64_t tile = cid + j * ncl;
+      if (tile < a.ntiles) issue_fwd_tile<CLUSTER>(a, L, smem, tile, j, col0, nsc_me, pol);
+    }
+  }
+
+  int rpar = 0, xpar = 0;
+  for (int64_t it = 0;; ++it) {
+    const int64_t tile = cid + it * ncl;
+    if (tile >= a.ntiles) break;
+    const int s = static_cast<int>(it % a.S);
+    const uint32_t par = static_cast<uint32_t>((it / a.S) & 1);
+    mbar_wait(full + s, par, a.err, abort_flag);
+    const int64_t row0 = tile * a.RT;
+    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
+    const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes;
+
+    for (int q = 0; q < a.rpg; ++q) {
+      const int r = g + q * a.G;
+      const bool active = r < nrows;
+      const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2;
+      uint4 xv[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int c = t + k * a.tpr;
+        xv[k] = (active && c < nsc_me)
+                    ? *reinterpret_cast<const uint4 *>(rowp + c * 16)
+                    : make_uint4(0, 0, 0, 0);
+      }
+      float mu = 0.f, rs;
+      if (MODE == kLayer) {
+        // This thread's (count, mean, M2), then Chan merges.
+        float sum = 0.f;
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          if (active && t + k * a.tpr < nsc_me) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum += bf_elem(xv[k], e);
+            cnt += 8;
+          }
+        }
+        const float n = static_cast<float>(cnt);
+        const float m = cnt ? sum / n : 0.f;
+        float q2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          if (active && t + k * a.tpr < nsc_me) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float d = bf_elem(xv[k], e) - m;
+              q2 = fmaf(d, d, q2);
+            }
+          }
+        }
+        Part p = group_allreduce<true>(Part{n, m, q2}, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) p = cluster_allreduce<true>(p, r, a.RT, t, xch, xpar);
+        mu = p.b;
+        rs = 1.0f / sqrtf(p.c * a.invN + a.eps);
+      } else {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float v = bf_elem(xv[k], e);
+            ss = fmaf(v, v, ss);
+          }
+        }
+        Part p = group_allreduce<false>(Part{ss, 0.f, 0.f}, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) p = cluster_allreduce<false>(p, r, a.RT, t, xch, xpar);
+        rs = 1.0f / sqrtf(p.a * a.invN + a.eps);
+      }
+
+      if (active) {
+        const int64_t row = row0 + r;
+        uint16_t *yrow = a.out + row * a.N + col0;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const int c = t + k * a.tpr;
+          if (c < nsc_me) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float xh = (bf_elem(xv[k], e) - mu) * rs;
+              o[e] = (MODE == kLayer) ? fmaf(xh, bf_elem(gv[k], e), bf_elem(bv[k], e))
+                                      : xh * bf_elem(gv[k], e);
+            }
+            const uint4 packed = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                            pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+            st_global_cs_v4(yrow + c * 8, packed);
+          }
+        }
+        if (t == 0 && crank == 0) {
+          a.rstd[row] = rs;
+          if (MODE == kLayer) a.mean[row] = mu;
+        }
+      }
+    }
+
+    // The stage is fully consumed: refill it with the tile S steps ahead.
+    __syncthreads();
+    if (tid == 0) {
+      const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
+      if (next < a.ntiles) {
+        fence_proxy_async_smem();
+        issue_fwd_tile<CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
+      }
+    }
+  }
+  // No CTA may leave while a peer could still read its shared memory.
+  if (CLUSTER) cluster_sync();
+}
+
+template <int MODE, bool CLUSTER>
+const void *pick_fwd(int K) {
+  switch (K) {
+    case 1: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER>);
+    case 2: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER>);
+    case 3: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER>);
+    case 4: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER>);
+    case 5: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER>);
+    case 6: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER>);
+    case 8: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER>);
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+const void *fwd_kernel_ptr(int mode, int K, bool cluster) {
+  if (mode == kRMS) return cluster ? pick_fwd<kRMS, true>(K) : pick_fwd<kRMS, false>(K);
+  return cluster ? pick_fwd<kLayer, true>(K) : pick_fwd<kLayer, false>(K);
+}
+
+}  // namespace gbn

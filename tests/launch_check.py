@@ -1,0 +1,132 @@
+"""Host-side check of the kernels' index arithmetic for a launch plan.
+
+Restates, for every CTA of a launch, the addresses the forward / backward /
+reduce kernels form (tiles, rows, 16-byte chunks, bulk-copy sizes, shared
+memory slots, partial rows) and asserts that each stays inside its buffer
+and meets the alignment rules of the copies.  Run on the CPU before a plan
+reaches the GPU; uses only the plan the library reports (norm_plan).
+"""
+from __future__ import annotations
+
+MAX_THREADS = 512
+TX_LIMIT = 1 << 20
+
+
+def _align16(v):
+    return (v + 15) & ~15
+
+
+def smem_layout(RT, NS, S, G, tpr, ntensors, stats, cluster):
+    """Same region order as the kernels' shared-memory layout."""
+    tensor = RT * NS * 2
+    stage = tensor * ntensors
+    off = stage * S
+    L = {"tensor": tensor, "stage": stage, "stats": off}
+    if stats:
+        off = _align16(off + S * RT * 2 * 4)
+    L["red"] = off
+    if tpr > 32:
+        off = _align16(off + 2 * G * (tpr // 32) * 4 * 4)
+    L["xch"] = off
+    if cluster:
+        off = _align16(off + 2 * RT * 4 * 4)
+    L["bar"] = off
+    off = _align16(off + S * 8)
+    L["flag"] = off
+    off = _align16(off + 4)
+    L["total"] = off
+    return L
+
+
+def check_plan(p, M, N, mode, backward, smem_optin=232448):
+    """Raise AssertionError if any access of the launch described by `p`
+    (a norm_plan dict) would leave its buffer or break an alignment rule."""
+    C, NS, tpr, K = p["cluster"], p["cols_per_cta"], p["threads_per_row"], p["chunks_per_thread"]
+    G, rpg, RT, S = p["groups"], p["rows_per_group"], p["rows_per_tile"], p["stages"]
+    threads, smem, ntiles, grid, P = p["threads"], p["smem_bytes"], p["tiles"], p["grid"], p["partials"]
+    nc = N // 8
+    nsc = NS // 8
+    assert N % 8 == 0 and NS % 8 == 0
+    assert threads == G * tpr <= MAX_THREADS and threads % 32 == 0
+    assert tpr >= 32 and tpr % 32 == 0 or (tpr < 32 and 32 % tpr == 0)
+    if tpr > 32:
+        assert 1 + (G - 1) <= 15, "named barrier id out of range"
+    assert RT == G * rpg and S >= 2
+    assert C >= 1 and grid % C == 0 and grid // C == P and P >= 1
+    assert C == 1 or rpg == 1
+    assert ntiles == -(-M // RT) and P <= ntiles
+    assert K * tpr >= nsc, "a chunk has no owner"
+    L = smem_layout(RT, NS, S, G, tpr, 2 if backward else 1, backward, C > 1)
+    assert smem == L["total"] <= smem_optin, "shared memory over the opt-in limit"
+    assert L["stage"] < TX_LIMIT
+    assert L["bar"] % 8 == 0 and L["stats"] % 16 == 0 and L["red"] % 16 == 0
+    if backward:
+        nparts = 2 if mode == 1 else 1
+        # column partial fold reuses the ring: nparts * G * NS floats
+        assert nparts * G * NS * 4 <= S * L["stage"]
+    # per CTA slice
+    for crank in range(C):
+        col0 = crank * NS
+        nsc_me = min(nsc, nc - crank * nsc)
+        assert nsc_me >= 1, "a CTA of the cluster owns no column"
+        assert col0 + nsc_me * 8 <= N
+        assert (col0 * 2) % 16 == 0
+        # chunk ownership: thread t, k < K -> c = t + k*tpr; valid iff c < nsc_me
+        owned = sorted(t + k * tpr for t in range(tpr) for k in range(K) if t + k * tpr < nsc_me)
+        assert owned == list(range(nsc_me)), "chunks not owned exactly once"
+        # smem reads of a row slot: r * NS*2 + c*16 + 16 <= tensor bytes
+        assert (RT - 1) * NS * 2 + (nsc_me - 1) * 16 + 16 <= L["tensor"]
+        # bulk copy sizes / alignment
+        if C == 1:
+            max_bytes = RT * N * 2
+            assert max_bytes <= L["tensor"] and max_bytes % 16 == 0
+        else:
+            assert nsc_me * 16 <= NS * 2 and (NS * 2) % 16 == 0
+        if backward:
+            nparts = 2 if mode == 1 else 1
+            last = ((nparts - 1) * P + (P - 1)) * N + col0 + nsc_me * 8
+            assert last <= nparts * P * N, "partial row write out of the workspace"
+    # tiles: every tile visited exactly once across clusters; rows in range
+    seen = 0
+    for cid in range(P):
+        it = 0
+        while True:
+            tile = cid + it * P
+            if tile >= ntiles:
+                break
+            row0 = tile * RT
+            nrows = min(RT, M - row0)
+            assert 1 <= nrows <= RT
+            assert (row0 + nrows) * N <= M * N
+            assert ((row0 * N) * 2) % 16 == 0
+            if backward:
+                assert (S - 1) * RT * 2 + 2 * (nrows - 1) + 1 < S * RT * 2
+            seen += 1
+            it += 1
+    assert seen == ntiles
+    # group scratch: slot (rpar*G + g)*W + w, 4 floats, rpar in {0, 1}
+    if tpr > 32:
+        W = tpr // 32
+        hi = ((1 * G + (G - 1)) * W + (W - 1)) * 4 + 4
+        assert L["red"] + hi * 4 <= L["xch"]
+    if C > 1:
+        hi = (1 * RT + (RT - 1)) * 4 + 4
+        assert L["xch"] + hi * 4 <= L["bar"]
+    return True
+
+
+def check_reduce(P, N, nparts):
+    """Reduce kernel: grid (ceil(N/128), nparts), 256 threads, lane owns 4
+    columns, warp w sums p in [P*w/8, P*(w+1)/8)."""
+    assert N % 4 == 0
+    gx = -(-N // 128)
+    for bx in (0, gx - 1):
+        for lane in range(32):
+            col = (bx * 32 + lane) * 4
+            if col < N:
+                assert col + 4 <= N
+                assert ((nparts - 1) * P + (P - 1)) * N + col + 4 <= nparts * P * N
+    ranges = [(P * w // 8, P * (w + 1) // 8) for w in range(8)]
+    covered = [p for a, b in ranges for p in range(a, b)]
+    assert covered == list(range(P))
+    return True

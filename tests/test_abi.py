@@ -1,0 +1,101 @@
+"""The C ABI library without a GPU: it loads, exports every function that
+include/gbnorm.h declares, and rejects bad arguments with the documented
+status codes before touching CUDA."""
+import ctypes
+import os
+
+import pytest
+import torch
+
+import memory_bound_normalization_rmsnorm_gb300 as gb
+
+
+def test_exports_every_declared_symbol():
+    names = gb.declared_functions()
+    assert set(names) >= {"norm_fwd", "norm_bwd", "norm_bwd_workspace_bytes",
+                          "norm_strerror", "norm_get_device_error", "norm_plan"}
+    L = ctypes.CDLL(gb.library_path())
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in gbnorm.h but not exported"
+
+
+def test_library_is_in_tree():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    assert os.path.commonpath([gb.library_path(), root]) == root
+
+
+def test_strerror_covers_all_codes():
+    seen = set()
+    for code in range(10):
+        s = gb.strerror(code)
+        assert s and s != "unknown status"
+        seen.add(s)
+    assert len(seen) == 10
+    assert gb.strerror(1234) == "unknown status"
+
+
+F = 16  # a fake, 16-byte aligned address: validation fails before any use
+
+
+def test_fwd_validation_codes():
+    f = gb.lib().norm_fwd
+    ok = dict(x=F, g=F, b=None, M=4, N=16, eps=1e-5, mode=0, y=F, r=F, m=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["g"], a["b"], a["M"], a["N"], a["eps"], a["mode"], a["y"],
+                 a["r"], a["m"], None)
+
+    assert call(x=None) == 1
+    assert call(y=None) == 1
+    assert call(r=None) == 1
+    assert call(M=0) == 2
+    assert call(N=12) == 2
+    assert call(N=0) == 2
+    assert call(N=262152) == 2
+    assert call(mode=2) == 4
+    assert call(b=F) == 4              # beta with RMSNorm
+    assert call(m=F) == 4              # mean with RMSNorm
+    assert call(mode=1) == 4           # LayerNorm without mean
+    assert call(eps=-1e-5) == 9
+    assert call(eps=float("inf")) == 9
+    assert call(x=F + 8) == 3
+    assert call(g=F + 2) == 3
+    assert call(mode=1, m=F + 4) == 3
+
+
+def test_bwd_validation_codes():
+    f = gb.lib().norm_bwd
+    ok = dict(dy=F, x=F, g=F, r=F, m=None, M=4, N=16, mode=0, dx=F, dg=F, db=None, ws=F,
+              wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["dy"], a["x"], a["g"], a["r"], a["m"], a["M"], a["N"], a["mode"], a["dx"],
+                 a["dg"], a["db"], a["ws"], a["wsb"], None)
+
+    assert call(dy=None) == 1
+    assert call(dg=None) == 1
+    assert call(M=-1) == 2
+    assert call(N=20) == 2
+    assert call(db=F) == 4
+    assert call(m=F) == 4
+    assert call(mode=1) == 4
+    assert call(ws=None) == 5
+    assert call(ws=F + 4) == 3
+    assert call(dx=F + 2) == 3
+
+
+def test_plan_is_pure_host_arithmetic():
+    """norm_plan for a described device works without any GPU and is
+    deterministic."""
+    a = gb.norm_plan(32768, 4096, 1, True, 152, 232448)
+    b = gb.norm_plan(32768, 4096, 1, True, 152, 232448)
+    assert a == b and a["grid"] >= 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device status")
+def test_no_device_reports_cuda_error():
+    with pytest.raises(gb.NormError) as e:
+        gb.norm_bwd_workspace_bytes(128, 1024, 0)
+    assert e.value.status == 7
