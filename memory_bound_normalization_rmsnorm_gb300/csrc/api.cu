@@ -434,7 +434,7 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   void *rargs[] = {&ws, &P, &n, &dgamma, &dbeta};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((n + 127) / 128, nparts);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(reduce_threads());
   cfg.stream = s;
   if (cudaLaunchKernelExC(&cfg, rfn, rargs) != cudaSuccess) {
     cudaGetLastError();

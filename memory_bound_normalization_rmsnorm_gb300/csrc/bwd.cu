@@ -21,19 +21,16 @@ namespace gbn {
 namespace {
 
 // Issues tile `tile` into stage `s`: the rows' statistics with 4-byte
-// cp.async copies (one completion arrival per lane of warp 0), then x and
-// dy with bulk copies.  Must be called by all 32 lanes of warp 0.
+// cp.async copies (one completion arrival per lane), then x and dy with
+// bulk copies.  Must be called by all 32 lanes of one warp.
 template <int MODE, bool CLUSTER>
-__device__ __forceinline__ void issue_bwd_tile(const NormArgs &a,
-                                               const SmemLayout &L,
-                                               unsigned char *smem, int64_t tile,
-                                               int s, int col0, int nsc_me,
-                                               uint64_t pol) {
+__device__ __forceinline__ void issue_bwd_tile(const NormArgs &a, const SmemLayout &L,
+                                               unsigned char *smem, int64_t tile, int s,
+                                               int col0, int nsc_me, uint64_t pol) {
   const int lane = threadIdx.x & 31;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
   unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
-  float *stats = reinterpret_cast<float *>(smem + L.stats_off) +
-                 static_cast<size_t>(s) * a.RT * 2;
+  float *stats = reinterpret_cast<float *>(smem + L.stats_off) + static_cast<size_t>(s) * a.RT * 2;
   const int64_t row0 = tile * a.RT;
   const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
   for (int r = lane; r < nrows; r += 32) {
@@ -70,10 +67,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   float *xch = reinterpret_cast<float *>(smem + L.xch_off);
   const float *stats_all = reinterpret_cast<const float *>(smem + L.stats_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
 
   const int tid = threadIdx.x;
   const int g = tid / a.tpr;
   const int t = tid - g * a.tpr;
+  const int nwarps = blockDim.x >> 5;
   const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
   const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
   const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
@@ -82,21 +81,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
 
   if (tid == 0) {
-    for (int s = 0; s < a.S; ++s) mbar_init(full + s, 1);
+    for (int s = 0; s < a.S; ++s) {
+      mbar_init(full + s, 1);
+      done_cnt[s] = 0;
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
 
-  uint4 gv[K];
-  float accg[K][8], accb[K][8];
+  // gamma (fp32 pairs) and the column accumulators of this thread's chunks
+  // live in registers for the whole kernel.
+  float2 gf[K][4], accg[K][4], accb[K][4];
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int c = t + k * a.tpr;
-    gv[k] = (c < nsc_me) ? ld_global_nc_v4(a.gamma + col0 + c * 8) : make_uint4(0, 0, 0, 0);
+    const uint4 gv = (c < nsc_me) ? ld_global_nc_v4(a.gamma + col0 + c * 8) : make_uint4(0, 0, 0, 0);
+    chunk_to_f2(gv, gf[k]);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      accg[k][e] = 0.f;
-      accb[k][e] = 0.f;
+    for (int p = 0; p < 4; ++p) {
+      accg[k][p] = splat2(0.f);
+      accb[k][p] = splat2(0.f);
     }
   }
 
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
     }
   }
 
+  const float invN = a.invN;
   int rpar = 0, xpar = 0;
   for (int64_t it = 0;; ++it) {
     const int64_t tile = cid + it * ncl;
@@ -120,72 +125,79 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
     const int64_t row0 = tile * a.RT;
     const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
     const unsigned char *stx = smem + static_cast<size_t>(s) * L.stage_bytes;
-    const unsigned char *std_ = stx + L.tensor_bytes;
     const float *stats = stats_all + static_cast<size_t>(s) * a.RT * 2;
 
     for (int q = 0; q < a.rpg; ++q) {
       const int r = g + q * a.G;
       const bool active = r < nrows;
-      const size_t roff = static_cast<size_t>(r) * a.NS * 2;
       float rs = 0.f, mu = 0.f;
       if (active) {
         rs = stats[2 * r];
         if (MODE == kLayer) mu = stats[2 * r + 1];
       }
-      uint4 xv[K], dv[K];
+      const float2 rs2 = splat2(rs);
+      const float2 nmu = splat2(-mu);
+      const unsigned char *xrow = stx + static_cast<size_t>(r) * a.NS * 2 + t * 16;
+      // xhat and g = dy * gamma stay in registers between the two passes.
+      float2 xh[K][4], gg[K][4];
+      float2 s1 = splat2(0.f), s2 = splat2(0.f);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        const int c = t + k * a.tpr;
-        const bool ok = active && c < nsc_me;
-        xv[k] = ok ? *reinterpret_cast<const uint4 *>(stx + roff + c * 16) : make_uint4(0, 0, 0, 0);
-        dv[k] = ok ? *reinterpret_cast<const uint4 *>(std_ + roff + c * 16) : make_uint4(0, 0, 0, 0);
-      }
-      // Row dot products sum(g) and sum(g * xhat); column partials.
-      float s1 = 0.f, s2 = 0.f;
+        const bool ok = active && (t + k * a.tpr < nsc_me);
+        uint4 xv = make_uint4(0, 0, 0, 0), dv = make_uint4(0, 0, 0, 0);
+        if (ok) {
+          xv = *reinterpret_cast<const uint4 *>(xrow + k * a.tpr * 16);
+          dv = *reinterpret_cast<const uint4 *>(xrow + L.tensor_bytes + k * a.tpr * 16);
+        }
+        float2 xf[4], df[4];
+        chunk_to_f2(xv, xf);
+        chunk_to_f2(dv, df);
 #pragma unroll
-      for (int k = 0; k < K; ++k) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xh = (bf_elem(xv[k], e) - mu) * rs;
-          const float d = bf_elem(dv[k], e);
-          const float gg = d * bf_elem(gv[k], e);
-          s2 = fmaf(gg, xh, s2);
-          if (MODE == kLayer) s1 += gg;
-          accg[k][e] = fmaf(d, xh, accg[k][e]);
-          if (MODE == kLayer) accb[k][e] += d;
+        for (int p = 0; p < 4; ++p) {
+          xh[k][p] = mul2(add2(xf[p], nmu), rs2);
+          gg[k][p] = mul2(df[p], gf[k][p]);
+          s2 = fma2(gg[k][p], xh[k][p], s2);
+          if (MODE == kLayer) s1 = add2(s1, gg[k][p]);
+          accg[k][p] = fma2(df[p], xh[k][p], accg[k][p]);
+          if (MODE == kLayer) accb[k][p] = add2(accb[k][p], df[p]);
         }
       }
-      Part p = group_allreduce<false>(Part{s1, s2, 0.f}, a.tpr, g, a.G, t, red, rpar);
-      if (CLUSTER) p = cluster_allreduce<false>(p, r, a.RT, t, xch, xpar);
-      const float av = (MODE == kLayer) ? p.a * a.invN : 0.f;
-      const float cv = p.b * a.invN;
+      float v[2] = {s1.x + s1.y, s2.x + s2.y};
+      if (MODE == kLayer) {
+        group_sum<2>(v, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) cluster_sum<2>(v, r, a.RT, t, xch, xpar);
+      } else {
+        float w1[1] = {v[1]};
+        group_sum<1>(w1, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) cluster_sum<1>(w1, r, a.RT, t, xch, xpar);
+        v[1] = w1[0];
+      }
+      const float2 av = splat2((MODE == kLayer) ? v[0] * invN : 0.f);
+      const float2 cv = splat2(v[1] * invN);
+      const float2 neg1 = splat2(-1.f);
 
       if (active) {
-        uint16_t *dxrow = a.out + (row0 + r) * a.N + col0;
+        uint16_t *dxrow = a.out + (row0 + r) * a.N + col0 + t * 8;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          const int c = t + k * a.tpr;
-          if (c < nsc_me) {
-            float o[8];
+          if (t + k * a.tpr < nsc_me) {
+            float2 o[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float xh = (bf_elem(xv[k], e) - mu) * rs;
-              const float gg = bf_elem(dv[k], e) * bf_elem(gv[k], e);
-              o[e] = rs * (gg - fmaf(xh, cv, av));
+            for (int p = 0; p < 4; ++p) {
+              // dx = rstd * (g - (xhat * c + a))
+              const float2 u = fma2(xh[k][p], cv, av);
+              o[p] = mul2(fma2(u, neg1, gg[k][p]), rs2);
             }
-            const uint4 packed = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                                            pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-            st_global_cs_v4(dxrow + c * 8, packed);
+            st_global_cs_v4(dxrow + k * a.tpr * 8, f2_to_chunk(o));
           }
         }
       }
     }
 
-    __syncthreads();
-    if (tid < 32) {
+    if (last_warp_done(done_cnt, s, nwarps)) {
       const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
       if (next < a.ntiles) {
-        if (tid == 0) fence_proxy_async_smem();
+        if ((tid & 31) == 0) fence_proxy_async_smem();
         __syncwarp();
         issue_bwd_tile<MODE, CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
       }
@@ -202,26 +214,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
     const int c = t + k * a.tpr;
     if (c < nsc_me) {
       float4 *dg = reinterpret_cast<float4 *>(accs + static_cast<size_t>(g) * a.NS + c * 8);
-      dg[0] = make_float4(accg[k][0], accg[k][1], accg[k][2], accg[k][3]);
-      dg[1] = make_float4(accg[k][4], accg[k][5], accg[k][6], accg[k][7]);
+      dg[0] = make_float4(accg[k][0].x, accg[k][0].y, accg[k][1].x, accg[k][1].y);
+      dg[1] = make_float4(accg[k][2].x, accg[k][2].y, accg[k][3].x, accg[k][3].y);
       if (MODE == kLayer) {
         float4 *db = reinterpret_cast<float4 *>(accs + static_cast<size_t>(a.G + g) * a.NS + c * 8);
-        db[0] = make_float4(accb[k][0], accb[k][1], accb[k][2], accb[k][3]);
-        db[1] = make_float4(accb[k][4], accb[k][5], accb[k][6], accb[k][7]);
+        db[0] = make_float4(accb[k][0].x, accb[k][0].y, accb[k][1].x, accb[k][1].y);
+        db[1] = make_float4(accb[k][2].x, accb[k][2].y, accb[k][3].x, accb[k][3].y);
       }
     }
   }
   __syncthreads();
-  const int nq = nsc_me * 2;      // float4s of this CTA's columns
-  const int nq_stride = a.NS / 4; // float4s per group row in shared memory
+  const int nq = nsc_me * 2;       // float4s of this CTA's columns
+  const int nq_stride = a.NS / 4;  // float4s per group row in shared memory
   const int nparts = (MODE == kLayer) ? 2 : 1;
   for (int w = 0; w < nparts; ++w) {
     const float4 *src = reinterpret_cast<const float4 *>(accs + static_cast<size_t>(w) * a.G * a.NS);
     float4 *dst = reinterpret_cast<float4 *>(a.ws + (static_cast<size_t>(w) * a.P + cid) * a.N + col0);
     for (int j = tid; j < nq; j += blockDim.x) {
       float4 acc = src[j];
-      for (int gg = 1; gg < a.G; ++gg) {
-        const float4 v = src[static_cast<size_t>(gg) * nq_stride + j];
+      for (int q = 1; q < a.G; ++q) {
+        const float4 v = src[static_cast<size_t>(q) * nq_stride + j];
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
       dst[j] = acc;
@@ -230,16 +242,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   if (CLUSTER) cluster_sync();
 }
 
+constexpr int kReduceWarps = 16;
+
 // dgamma[j] = sum over p of ws[p][j] (blockIdx.y = 0) and dbeta[j] = sum
-// over p of ws[P + p][j] (blockIdx.y = 1), p in increasing order within
-// each of the block's 8 warps' contiguous p ranges, the 8 warp sums then
-// added in warp order: a fixed order for a given P, so the result is
-// bitwise reproducible.  Each lane owns 4 consecutive columns.
-__global__ void __launch_bounds__(256) reduce_partials_kernel(const float *__restrict__ ws,
-                                                              int P, int N,
-                                                              float *__restrict__ dgamma,
-                                                              float *__restrict__ dbeta) {
-  __shared__ float4 part[8][32];
+// over p of ws[P + p][j] (blockIdx.y = 1).  Warp w of the block sums the
+// contiguous range p in [P*w/16, P*(w+1)/16) in increasing p; the 16 warp
+// sums are then added in warp order: a fixed order for a given P, so the
+// result is bitwise reproducible.  Each lane owns 4 consecutive columns.
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
+    const float *__restrict__ ws, int P, int N, float *__restrict__ dgamma,
+    float *__restrict__ dbeta) {
+  __shared__ float4 part[kReduceWarps][32];
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   const float *src = ws + static_cast<size_t>(blockIdx.y) * P * N;
@@ -247,8 +260,8 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const float *__res
   const int col = (blockIdx.x * 32 + lane) * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col < N) {
-    const int p0 = static_cast<int>((static_cast<int64_t>(P) * w) / 8);
-    const int p1 = static_cast<int>((static_cast<int64_t>(P) * (w + 1)) / 8);
+    const int p0 = static_cast<int>((static_cast<int64_t>(P) * w) / kReduceWarps);
+    const int p1 = static_cast<int>((static_cast<int64_t>(P) * (w + 1)) / kReduceWarps);
     int p = p0;
     for (; p + 4 <= p1; p += 4) {
       float4 v[4];
@@ -270,7 +283,7 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const float *__res
   if (w == 0 && col < N) {
     float4 s = part[0][lane];
 #pragma unroll
-    for (int u = 1; u < 8; ++u) {
+    for (int u = 1; u < kReduceWarps; ++u) {
       s.x += part[u][lane].x; s.y += part[u][lane].y;
       s.z += part[u][lane].z; s.w += part[u][lane].w;
     }
@@ -299,5 +312,7 @@ const void *bwd_kernel_ptr(int mode, int K, bool cluster) {
 const void *reduce_kernel_ptr() {
   return reinterpret_cast<const void *>(&reduce_partials_kernel);
 }
+
+int reduce_threads() { return kReduceWarps * 32; }
 
 }  // namespace gbn

@@ -54,7 +54,7 @@ struct SmemLayout {
                           // (W = tpr / 32; only when tpr > 32)
   uint32_t xch_off;       // [2][RT][4] floats, cross-CTA partials (clusters only)
   uint32_t bar_off;       // [S] mbarriers
-  uint32_t flag_off;      // abort flag
+  uint32_t flag_off;      // abort flag (int), then [S] ints: warps done per stage
   uint32_t total;
 };
 
@@ -82,7 +82,7 @@ __host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
   L.bar_off = off;
   off = align16(off + static_cast<uint32_t>(S) * 8u);
   L.flag_off = off;
-  off = align16(off + 4u);
+  off = align16(off + 4u + 4u * static_cast<uint32_t>(S));
   L.total = off;
   return L;
 }
@@ -110,5 +110,6 @@ struct Plan {
 const void *fwd_kernel_ptr(int mode, int K, bool cluster);
 const void *bwd_kernel_ptr(int mode, int K, bool cluster);
 const void *reduce_kernel_ptr();
+int reduce_threads();
 
 }  // namespace gbn

@@ -9,13 +9,18 @@
 // introl.com).
 //
 // Structure: a persistent grid; each CTA (or cluster of CTAs splitting the
-// columns) walks tiles of RT consecutive rows.  Thread 0 keeps S tiles in
-// flight with bulk asynchronous copies into a shared-memory ring, each
-// stage guarded by an mbarrier.  Row groups of `tpr` threads read their row
-// from shared memory into registers (16-byte chunks, conflict free), reduce
-// (warp butterfly, then warps of the group, then the CTAs of the cluster
-// through distributed shared memory), and write y with 16-byte streaming
-// stores.
+// columns) walks tiles of RT consecutive rows.  S tiles are kept in flight
+// with bulk asynchronous copies into a shared-memory ring, each stage
+// guarded by an mbarrier; the last warp to finish with a stage refills it,
+// so no warp ever waits for another outside its own row group.  Row groups
+// of `tpr` threads copy their row from shared memory into registers
+// (16-byte chunks, conflict free), compute the statistics with packed FP32
+// arithmetic, reduce (warp butterfly, then the warps of the group, then
+// the CTAs of the cluster through distributed shared memory), and write y
+// with 16-byte streaming stores.
+//
+// LayerNorm statistics are two-pass on the register-resident row: the mean
+// first, then the sum of squared deviations from it.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
@@ -25,11 +30,9 @@ namespace gbn {
 namespace {
 
 template <bool CLUSTER>
-__device__ __forceinline__ void issue_fwd_tile(const NormArgs &a,
-                                               const SmemLayout &L,
-                                               unsigned char *smem, int64_t tile,
-                                               int s, int col0, int nsc_me,
-                                               uint64_t pol) {
+__device__ __forceinline__ void issue_fwd_tile(const NormArgs &a, const SmemLayout &L,
+                                               unsigned char *smem, int64_t tile, int s,
+                                               int col0, int nsc_me, uint64_t pol) {
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
   unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
   const int64_t row0 = tile * a.RT;
@@ -56,10 +59,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   float *xch = reinterpret_cast<float *>(smem + L.xch_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
 
   const int tid = threadIdx.x;
   const int g = tid / a.tpr;
   const int t = tid - g * a.tpr;
+  const int nwarps = blockDim.x >> 5;
   const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
   const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
   const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
@@ -68,24 +73,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
 
   if (tid == 0) {
-    for (int s = 0; s < a.S; ++s) mbar_init(full + s, 1);
+    for (int s = 0; s < a.S; ++s) {
+      mbar_init(full + s, 1);
+      done_cnt[s] = 0;
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
 
-  // gamma (and beta) for this thread's chunks stay in registers for the
-  // whole kernel: the thread owns the same columns in every row.
-  uint4 gv[K], bv[K];
+  // gamma as fp32 pairs (and beta packed) for this thread's chunks stay in
+  // registers for the whole kernel: the thread owns the same columns in
+  // every row.
+  float2 gf[K][4];
+  uint4 bv[K];
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int c = t + k * a.tpr;
-    gv[k] = make_uint4(0, 0, 0, 0);
+    uint4 gv = make_uint4(0, 0, 0, 0);
     bv[k] = make_uint4(0, 0, 0, 0);
     if (c < nsc_me) {
-      gv[k] = ld_global_nc_v4(a.gamma + col0 + c * 8);
-      if (MODE == kLayer && a.beta != nullptr)
-        bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
+      gv = ld_global_nc_v4(a.gamma + col0 + c * 8);
+      if (MODE == kLayer && a.beta != nullptr) bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
     }
+    chunk_to_f2(gv, gf[k]);
   }
 
   if (CLUSTER) cluster_sync(); else __syncthreads();
@@ -98,6 +108,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
     }
   }
 
+  const float invN = a.invN;
   int rpar = 0, xpar = 0;
   for (int64_t it = 0;; ++it) {
     const int64_t tile = cid + it * ncl;
@@ -112,89 +123,82 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
     for (int q = 0; q < a.rpg; ++q) {
       const int r = g + q * a.G;
       const bool active = r < nrows;
-      const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2;
-      uint4 xv[K];
+      const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2 + t * 16;
+      float2 xf[K][4];
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        const int c = t + k * a.tpr;
-        xv[k] = (active && c < nsc_me)
-                    ? *reinterpret_cast<const uint4 *>(rowp + c * 16)
-                    : make_uint4(0, 0, 0, 0);
+        const bool ok = active && (t + k * a.tpr < nsc_me);
+        const uint4 v = ok ? *reinterpret_cast<const uint4 *>(rowp + k * a.tpr * 16)
+                           : make_uint4(0, 0, 0, 0);
+        chunk_to_f2(v, xf[k]);
       }
-      float mu = 0.f, rs;
+      float rs;
+      float2 nmu = splat2(0.f);
       if (MODE == kLayer) {
-        // This thread's (count, mean, M2), then Chan merges.
-        float sum = 0.f;
-        int cnt = 0;
+        // Pass 1: mean.
+        float2 acc = splat2(0.f);
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+          for (int p = 0; p < 4; ++p) acc = add2(acc, xf[k][p]);
+        float v1[1] = {acc.x + acc.y};
+        group_sum<1>(v1, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) cluster_sum<1>(v1, r, a.RT, t, xch, xpar);
+        const float mu = v1[0] * invN;
+        nmu = splat2(-mu);
+        // Pass 2: sum of squared deviations, over owned chunks only.
+        float2 q2 = splat2(0.f);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          if (active && t + k * a.tpr < nsc_me) {
+          if (t + k * a.tpr < nsc_me) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sum += bf_elem(xv[k], e);
-            cnt += 8;
-          }
-        }
-        const float n = static_cast<float>(cnt);
-        const float m = cnt ? sum / n : 0.f;
-        float q2 = 0.f;
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          if (active && t + k * a.tpr < nsc_me) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float d = bf_elem(xv[k], e) - m;
-              q2 = fmaf(d, d, q2);
+            for (int p = 0; p < 4; ++p) {
+              const float2 d = add2(xf[k][p], nmu);
+              q2 = fma2(d, d, q2);
             }
           }
         }
-        Part p = group_allreduce<true>(Part{n, m, q2}, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) p = cluster_allreduce<true>(p, r, a.RT, t, xch, xpar);
-        mu = p.b;
-        rs = 1.0f / sqrtf(p.c * a.invN + a.eps);
+        float v2[1] = {q2.x + q2.y};
+        group_sum<1>(v2, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) cluster_sum<1>(v2, r, a.RT, t, xch, xpar);
+        rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
+        if (active && t == 0 && crank == 0) a.mean[row0 + r] = mu;
       } else {
-        float ss = 0.f;
+        float2 q2 = splat2(0.f);
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
+        for (int k = 0; k < K; ++k)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float v = bf_elem(xv[k], e);
-            ss = fmaf(v, v, ss);
-          }
-        }
-        Part p = group_allreduce<false>(Part{ss, 0.f, 0.f}, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) p = cluster_allreduce<false>(p, r, a.RT, t, xch, xpar);
-        rs = 1.0f / sqrtf(p.a * a.invN + a.eps);
+          for (int p = 0; p < 4; ++p) q2 = fma2(xf[k][p], xf[k][p], q2);
+        float v2[1] = {q2.x + q2.y};
+        group_sum<1>(v2, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) cluster_sum<1>(v2, r, a.RT, t, xch, xpar);
+        rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
       }
 
       if (active) {
-        const int64_t row = row0 + r;
-        uint16_t *yrow = a.out + row * a.N + col0;
+        const float2 rs2 = splat2(rs);
+        uint16_t *yrow = a.out + (row0 + r) * a.N + col0 + t * 8;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          const int c = t + k * a.tpr;
-          if (c < nsc_me) {
-            float o[8];
+          if (t + k * a.tpr < nsc_me) {
+            float2 o[4];
+            float2 bf[4];
+            if (MODE == kLayer) chunk_to_f2(bv[k], bf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float xh = (bf_elem(xv[k], e) - mu) * rs;
-              o[e] = (MODE == kLayer) ? fmaf(xh, bf_elem(gv[k], e), bf_elem(bv[k], e))
-                                      : xh * bf_elem(gv[k], e);
+            for (int p = 0; p < 4; ++p) {
+              const float2 xh = mul2(MODE == kLayer ? add2(xf[k][p], nmu) : xf[k][p], rs2);
+              o[p] = (MODE == kLayer) ? fma2(xh, gf[k][p], bf[p]) : mul2(xh, gf[k][p]);
             }
-            const uint4 packed = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                                            pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-            st_global_cs_v4(yrow + c * 8, packed);
+            st_global_cs_v4(yrow + k * a.tpr * 8, f2_to_chunk(o));
           }
         }
-        if (t == 0 && crank == 0) {
-          a.rstd[row] = rs;
-          if (MODE == kLayer) a.mean[row] = mu;
-        }
+        if (t == 0 && crank == 0) a.rstd[row0 + r] = rs;
       }
     }
 
-    // The stage is fully consumed: refill it with the tile S steps ahead.
-    __syncthreads();
-    if (tid == 0) {
+    // This warp is done with the stage; the last warp to finish refills it
+    // with the tile S steps ahead.
+    if (last_warp_done(done_cnt, s, nwarps) && (tid & 31) == 0) {
       const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
       if (next < a.ntiles) {
         fence_proxy_async_smem();

@@ -1,7 +1,8 @@
 // rowops.cuh -- per-row building blocks shared by the forward and backward
-// kernels: bf16 packing, and fixed-order (hence bitwise reproducible)
-// reductions within a row group, across the warps of a group and across
-// the CTAs of a cluster.
+// kernels: bf16 <-> packed fp32 pairs, packed-FP32 arithmetic, fixed-order
+// (hence bitwise reproducible) sums within a row group, across the warps of
+// a group and across the CTAs of a cluster, and the shared-memory ring
+// refill hand-off.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -10,124 +11,118 @@
 
 namespace gbn {
 
-// --------------------------------------------------------------- bf16
-__device__ __forceinline__ float bf_lo(uint32_t w) {
-  return __uint_as_float(w << 16);
+// ------------------------------------------------------- bf16 <-> fp32
+// Two bf16 packed in a 32-bit word -> the two exact fp32 values (the
+// element at the lower address is .x).
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-__device__ __forceinline__ float bf_hi(uint32_t w) {
-  return __uint_as_float(w & 0xffff0000u);
-}
-// Element e (0..7) of a 16-byte chunk of 8 bf16.
-__device__ __forceinline__ float bf_elem(const uint4 &v, int e) {
-  const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
-  return (e & 1) ? bf_hi(w) : bf_lo(w);
-}
-// Round two floats to bf16 (nearest even) and pack: `lo` is the element at
-// the lower address.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+// Round two fp32 to bf16 (nearest even) and pack, .x at the lower address.
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-
-// --------------------------------------------------------- partials
-// A reduction payload of up to 3 floats, combined either by summation or
-// by Chan's pairwise merge of (count, mean, sum of squared deviations).
-struct Part {
-  float a, b, c;
-};
-
-__device__ __forceinline__ Part part_sum(const Part &lo, const Part &hi) {
-  return Part{lo.a + hi.a, lo.b + hi.b, lo.c + hi.c};
+__device__ __forceinline__ void chunk_to_f2(const uint4 &c, float2 (&v)[4]) {
+  v[0] = bf2_to_f2(c.x);
+  v[1] = bf2_to_f2(c.y);
+  v[2] = bf2_to_f2(c.z);
+  v[3] = bf2_to_f2(c.w);
+}
+__device__ __forceinline__ uint4 f2_to_chunk(const float2 (&v)[4]) {
+  return make_uint4(f2_to_bf2(v[0]), f2_to_bf2(v[1]), f2_to_bf2(v[2]), f2_to_bf2(v[3]));
 }
 
-// (n, mean, M2) merge.  `lo` is always the partial of the lower-indexed
-// participant, so every participant computes bit-identical results.
-__device__ __forceinline__ Part part_chan(const Part &lo, const Part &hi) {
-  if (hi.a == 0.f) return lo;
-  if (lo.a == 0.f) return hi;
-  const float n = lo.a + hi.a;
-  const float d = hi.b - lo.b;
-  const float wh = hi.a / n;
-  Part r;
-  r.a = n;
-  r.b = fmaf(d, wh, lo.b);
-  r.c = lo.c + hi.c + d * d * lo.a * wh;
-  return r;
+// ------------------------------------------ packed FP32 (two lanes per op)
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  return __ffma2_rn(a, b, c);
 }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 
-template <bool CHAN>
-__device__ __forceinline__ Part part_op(const Part &lo, const Part &hi) {
-  return CHAN ? part_chan(lo, hi) : part_sum(lo, hi);
-}
-
-__device__ __forceinline__ Part shfl_xor_part(const Part &p, int o) {
-  return Part{__shfl_xor_sync(0xffffffffu, p.a, o),
-              __shfl_xor_sync(0xffffffffu, p.b, o),
-              __shfl_xor_sync(0xffffffffu, p.c, o)};
-}
-__device__ __forceinline__ Part shfl_part(const Part &p, int src) {
-  return Part{__shfl_sync(0xffffffffu, p.a, src),
-              __shfl_sync(0xffffffffu, p.b, src),
-              __shfl_sync(0xffffffffu, p.c, src)};
-}
-
-// All-reduce over the `tpr` threads of a row group.  Butterfly within the
-// warp (lanes of one group when tpr <= 32), then, for tpr > 32, a fold of
-// the per-warp results in warp order through shared memory behind a named
-// barrier.  `red` is this CTA's [2][G][W][4] scratch, `rpar` the parity of
-// the buffer to use (flipped on return).  Every thread of the CTA must call
-// this the same number of times.
-template <bool CHAN>
-__device__ __forceinline__ Part group_allreduce(Part v, int tpr, int g, int G,
-                                                int t, float *red, int &rpar) {
-  const int lane = threadIdx.x & 31;
+// ------------------------------------------------------- group sums
+// Sum of NV values over the `tpr` threads of a row group, returned to every
+// thread of the group.  Butterfly within the warp (IEEE addition commutes,
+// so both partners of an exchange get the same bits), then for tpr > 32 the
+// per-warp totals are added in warp order from shared memory behind a named
+// barrier of the group's warps.  `red` is the CTA's [2][G][W][4] scratch and
+// `rpar` the buffer parity (flipped on return).  All threads of a group must
+// make the same calls.
+template <int NV>
+__device__ __forceinline__ void group_sum(float (&v)[NV], int tpr, int g, int G, int t,
+                                          float *red, int &rpar) {
   const int width = tpr < 32 ? tpr : 32;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     if (o < width) {
-      const Part other = shfl_xor_part(v, o);
-      v = ((lane & o) == 0) ? part_op<CHAN>(v, other) : part_op<CHAN>(other, v);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
     }
   }
   if (tpr > 32) {
     const int W = tpr >> 5;
     float *slot = red + (static_cast<size_t>(rpar * G + g) * W) * 4;
-    if (lane == 0) {
-      const int w = t >> 5;
-      *reinterpret_cast<float4 *>(slot + w * 4) = make_float4(v.a, v.b, v.c, 0.f);
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) slot[(t >> 5) * 4 + i] = v[i];
     }
     named_bar_sync(1 + g, tpr);
-    float4 f = *reinterpret_cast<const float4 *>(slot);
-    v = Part{f.x, f.y, f.z};
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = slot[i];
     for (int w = 1; w < W; ++w) {
-      f = *reinterpret_cast<const float4 *>(slot + w * 4);
-      v = part_op<CHAN>(v, Part{f.x, f.y, f.z});
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] += slot[w * 4 + i];
     }
     rpar ^= 1;
   }
-  return v;
 }
 
-// Combines the group partials of the C CTAs of a cluster for row slot `r`
-// of the tile, in CTA-rank order, so every CTA gets the same bits.  Also a
-// cluster-wide barrier: on return every thread of every CTA in the cluster
-// has passed the point of its call.  `xch` is this CTA's [2][RT][4] scratch.
-template <bool CHAN>
-__device__ __forceinline__ Part cluster_allreduce(Part v, int r, int RT, int t,
-                                                  float *xch, int &xpar) {
+// Sum of NV values over the C CTAs of the cluster for row slot `r`, in
+// CTA-rank order, so every CTA gets the same bits.  Also a cluster-wide
+// barrier: on return every thread of the cluster has passed the point of
+// its call.  `xch` is the CTA's [2][RT][4] scratch.
+template <int NV>
+__device__ __forceinline__ void cluster_sum(float (&v)[NV], int r, int RT, int t, float *xch,
+                                            int &xpar) {
   float *slot = xch + (static_cast<size_t>(xpar) * RT + r) * 4;
-  if (t == 0) *reinterpret_cast<float4 *>(slot) = make_float4(v.a, v.b, v.c, 0.f);
+  if (t == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) slot[i] = v[i];
+  }
   cluster_arrive_release();
   cluster_wait_acquire();
   const int C = static_cast<int>(cluster_nctarank());
   const int lane = threadIdx.x & 31;
   float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane < C) f = ld_dsmem_f32x4(slot, static_cast<uint32_t>(lane));
-  const Part mine{f.x, f.y, f.z};
-  Part acc = shfl_part(mine, 0);
-  for (int q = 1; q < C; ++q) acc = part_op<CHAN>(acc, shfl_part(mine, q));
+  const float mine[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float acc = __shfl_sync(0xffffffffu, mine[i], 0);
+    for (int q = 1; q < C; ++q) acc += __shfl_sync(0xffffffffu, mine[i], q);
+    v[i] = acc;
+  }
   xpar ^= 1;
-  return acc;
+}
+
+// ---------------------------------------------------- ring hand-off
+// Called by every warp of the CTA once it has finished reading stage `s`
+// (all of its loads from the stage have completed: their values were used).
+// Returns true in exactly one warp per use of the stage -- the last to
+// finish -- which then refills the stage.  No warp waits for another.
+__device__ __forceinline__ bool last_warp_done(int *cnt, int s, int nwarps) {
+  __syncwarp();
+  int last = 0;
+  if ((threadIdx.x & 31) == 0) {
+    __threadfence_block();
+    const int old = atomicAdd(cnt + s, 1);
+    last = (old == nwarps - 1);
+    if (last) {
+      cnt[s] = 0;
+      __threadfence_block();
+    }
+  }
+  return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
 }  // namespace gbn

@@ -33,7 +33,7 @@ def smem_layout(RT, NS, S, G, tpr, ntensors, stats, cluster):
     L["bar"] = off
     off = _align16(off + S * 8)
     L["flag"] = off
-    off = _align16(off + 4)
+    off = _align16(off + 4 + 4 * S)
     L["total"] = off
     return L
 
@@ -116,8 +116,8 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
 
 
 def check_reduce(P, N, nparts):
-    """Reduce kernel: grid (ceil(N/128), nparts), 256 threads, lane owns 4
-    columns, warp w sums p in [P*w/8, P*(w+1)/8)."""
+    """Reduce kernel: grid (ceil(N/128), nparts), 16 warps, lane owns 4
+    columns, warp w sums p in [P*w/16, P*(w+1)/16)."""
     assert N % 4 == 0
     gx = -(-N // 128)
     for bx in (0, gx - 1):
@@ -126,7 +126,7 @@ def check_reduce(P, N, nparts):
             if col < N:
                 assert col + 4 <= N
                 assert ((nparts - 1) * P + (P - 1)) * N + col + 4 <= nparts * P * N
-    ranges = [(P * w // 8, P * (w + 1) // 8) for w in range(8)]
+    ranges = [(P * w // 16, P * (w + 1) // 16) for w in range(16)]
     covered = [p for a, b in ranges for p in range(a, b)]
     assert covered == list(range(P))
     return True
