@@ -153,6 +153,9 @@ typedef struct {
     int32_t grid;              /* CTAs launched */
     int32_t partials;          /* clusters launched = partial rows written
                                   by the backward pass */
+    int32_t exact;             /* 1: every CTA slice is exactly
+                                  threads_per_row * chunks_per_thread chunks
+                                  (kernels without ownership tests) */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

@@ -144,16 +144,19 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   const int nc = N / 8;
   Plan p;
 
-  // Preferred chunks per thread (register budget without spills); up to
-  // kmax is allowed when a row slice needs it.
+  // Preferred chunks per thread, and the most that still fit in registers
+  // without spilling (ptxas -v: forward LayerNorm 4, RMSNorm 6; backward
+  // LayerNorm 2, RMSNorm 3); up to kmax only when a row needs it.
   const int kpref = bwd ? 2 : 4;
+  const int klim = bwd ? (mode == kLayer ? 2 : 3) : (mode == kLayer ? 4 : 6);
 
   // Column split: the smallest power-of-two cluster (up to 8) whose per-CTA
   // slice fits kMaxThreads threads x kpref chunks, else the smallest (up to
-  // 16) that fits kmax chunks.  Slices are ceil(nc / C) chunks; the last CTA
-  // of a cluster takes the remainder.
+  // 16) that fits klim, else kmax chunks.  Slices are ceil(nc / C) chunks;
+  // the last CTA of a cluster takes the remainder.
   int C = 1;
   while (C < 8 && ceil_div(nc, C) > kMaxThreads * kpref) C <<= 1;
+  while (C < 16 && ceil_div(nc, C) > kMaxThreads * klim) C <<= 1;
   while (C <= 16 && ceil_div(nc, C) > kMaxThreads * kmax) C <<= 1;
   if (ov.C) C = ov.C;
   if (C < 1 || C > 16) return NORM_ERR_UNSUPPORTED;
@@ -162,16 +165,43 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   p.NS = p.nsc * 8;
   if ((C - 1) * p.nsc >= nc) return NORM_ERR_UNSUPPORTED;  // a CTA would own nothing
 
-  // Threads per row: whole chunks per lane, about kpref chunks per thread.
-  int tpr;
-  if (p.nsc <= 32) tpr = pow2ceil(p.nsc);
-  else tpr = std::min(kMaxThreads, std::max(32, pow2ceil(ceil_div(p.nsc, kpref))));
-  if (ov.tpr) tpr = ov.tpr;
+  // Threads per row.  Preferred: an exact split of the slice into K chunks
+  // per thread over tpr = nsc / K threads, tpr a multiple of 32 (the EXACT
+  // kernels, which test no chunk ownership), with the largest K <= kpref,
+  // else the smallest K <= kmax.  Otherwise power-of-two groups with a
+  // ragged last chunk column.
+  const bool even = (nc % C) == 0;
+  int tpr = 0, K = 0;
+  bool exact = false;
+  auto try_exact = [&](int k) {
+    if (!even || p.nsc % k || (p.nsc / k) % 32 || p.nsc / k > kMaxThreads) return false;
+    if (!(bwd ? bwd_kernel_ptr(mode, k, C > 1, true) : fwd_kernel_ptr(mode, k, C > 1, true)))
+      return false;
+    tpr = p.nsc / k;
+    K = k;
+    exact = true;
+    return true;
+  };
+  if (ov.tpr) {
+    tpr = ov.tpr;
+    K = round_k(ceil_div(p.nsc, tpr), bwd);
+    exact = even && tpr % 32 == 0 && K * tpr == p.nsc;
+  } else {
+    bool found = false;
+    for (int k = kpref; k >= 1 && !found; --k) found = try_exact(k);
+    for (int k = kpref + 1; k <= klim && !found; ++k) found = try_exact(k);
+    if (!found) {
+      if (p.nsc <= 32) tpr = pow2ceil(p.nsc);
+      else tpr = std::min(kMaxThreads, std::max(32, pow2ceil(ceil_div(p.nsc, kpref))));
+      K = round_k(ceil_div(p.nsc, tpr), bwd);
+    }
+  }
   if (tpr < 1 || tpr > kMaxThreads || (tpr > 32 && tpr % 32) || (tpr < 32 && 32 % tpr))
     return NORM_ERR_UNSUPPORTED;
+  if (K > kmax) return NORM_ERR_UNSUPPORTED;
   p.tpr = tpr;
-  p.K = round_k(ceil_div(p.nsc, tpr), bwd);
-  if (p.K > kmax) return NORM_ERR_UNSUPPORTED;
+  p.K = K;
+  p.exact = exact;
 
   int G = kMaxThreads / tpr;
   if (tpr > 32) G = std::min(G, 8);
@@ -247,7 +277,8 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
   norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p);
   if (st != NORM_OK) return st;
 
-  const void *fn = bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1) : fwd_kernel_ptr(mode, p.K, p.C > 1);
+  const void *fn = bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact)
+                        : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact);
   if (!fn) return NORM_ERR_UNSUPPORTED;
   st = prepare_function(dev, fn, d.smem_optin);
   if (st != NORM_OK) return st;
@@ -376,7 +407,7 @@ norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64
   a.mean = mean;
   a.err = d.err;
   a.eps = eps;
-  return launch(fwd_kernel_ptr(mode, p.K, p.C > 1), p, a, reinterpret_cast<cudaStream_t>(stream));
+  return launch(fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact), p, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, size_t *bytes) {
@@ -425,7 +456,7 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   a.ws = static_cast<float *>(workspace);
   a.err = d.err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch(bwd_kernel_ptr(mode, p.K, p.C > 1), p, a, s)) != NORM_OK) return st;
+  if ((st = launch(bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact), p, a, s)) != NORM_OK) return st;
 
   const int nparts = (mode == NORM_LAYER && dbeta) ? 2 : 1;
   const void *rfn = reduce_kernel_ptr();
@@ -476,6 +507,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   out->tiles = p.ntiles;
   out->grid = p.grid;
   out->partials = p.P;
+  out->exact = p.exact ? 1 : 0;
   return NORM_OK;
 }
 

@@ -58,7 +58,9 @@ __device__ __forceinline__ void issue_bwd_tile(const NormArgs &a, const SmemLayo
   }
 }
 
-template <int MODE, int K, bool CLUSTER>
+// EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
+// chunk needs an ownership test and the warp butterfly is full width.
+template <int MODE, int K, bool CLUSTER, bool EXACT>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, CLUSTER);
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
       float2 s1 = splat2(0.f), s2 = splat2(0.f);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        const bool ok = active && (t + k * a.tpr < nsc_me);
+        const bool ok = active && (EXACT || t + k * a.tpr < nsc_me);
         uint4 xv = make_uint4(0, 0, 0, 0), dv = make_uint4(0, 0, 0, 0);
         if (ok) {
           xv = *reinterpret_cast<const uint4 *>(xrow + k * a.tpr * 16);
@@ -164,11 +166,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
       }
       float v[2] = {s1.x + s1.y, s2.x + s2.y};
       if (MODE == kLayer) {
-        group_sum<2>(v, a.tpr, g, a.G, t, red, rpar);
+        group_sum<2, EXACT>(v, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<2>(v, r, a.RT, t, xch, xpar);
       } else {
         float w1[1] = {v[1]};
-        group_sum<1>(w1, a.tpr, g, a.G, t, red, rpar);
+        group_sum<1, EXACT>(w1, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<1>(w1, r, a.RT, t, xch, xpar);
         v[1] = w1[0];
       }
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
         uint16_t *dxrow = a.out + (row0 + r) * a.N + col0 + t * 8;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          if (t + k * a.tpr < nsc_me) {
+          if (EXACT || t + k * a.tpr < nsc_me) {
             float2 o[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
@@ -292,21 +294,26 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
 }
 
 template <int MODE, bool CLUSTER>
-const void *pick_bwd(int K) {
+const void *pick_bwd(int K, bool e) {
   switch (K) {
-    case 1: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER>);
-    case 2: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER>);
-    case 3: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER>);
-    case 4: return reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER>);
+    case 1: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, false>);
+    case 2: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, false>);
+    case 3: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, false>);
+    case 4: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, false>);
     default: return nullptr;
   }
 }
 
 }  // namespace
 
-const void *bwd_kernel_ptr(int mode, int K, bool cluster) {
-  if (mode == kRMS) return cluster ? pick_bwd<kRMS, true>(K) : pick_bwd<kRMS, false>(K);
-  return cluster ? pick_bwd<kLayer, true>(K) : pick_bwd<kLayer, false>(K);
+const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact) {
+  if (mode == kRMS)
+    return cluster ? pick_bwd<kRMS, true>(K, exact) : pick_bwd<kRMS, false>(K, exact);
+  return cluster ? pick_bwd<kLayer, true>(K, exact) : pick_bwd<kLayer, false>(K, exact);
 }
 
 const void *reduce_kernel_ptr() {

@@ -94,6 +94,7 @@ struct Plan {
   int nsc = 0;     // chunks per CTA slice
   int tpr = 0;     // threads per row
   int K = 0;       // chunks per thread
+  bool exact = false; // slices divide evenly into K chunks x tpr threads, tpr >= 32
   int G = 0;       // groups per CTA
   int rpg = 1;     // rows per group per tile
   int RT = 0;      // rows per tile
@@ -105,10 +106,10 @@ struct Plan {
   int P = 0;       // clusters in the grid (partial rows in backward)
 };
 
-// Kernel entry points, by (mode, K, cluster).  Return nullptr when that
-// combination is not compiled.
-const void *fwd_kernel_ptr(int mode, int K, bool cluster);
-const void *bwd_kernel_ptr(int mode, int K, bool cluster);
+// Kernel entry points, by (mode, K, cluster, exact).  Return nullptr when
+// that combination is not compiled.
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
+const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
 const void *reduce_kernel_ptr();
 int reduce_threads();
 

@@ -51,7 +51,9 @@ __device__ __forceinline__ void issue_fwd_tile(const NormArgs &a, const SmemLayo
   }
 }
 
-template <int MODE, int K, bool CLUSTER>
+// EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
+// chunk needs an ownership test and the warp butterfly is full width.
+template <int MODE, int K, bool CLUSTER, bool EXACT>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, CLUSTER);
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
       float2 xf[K][4];
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        const bool ok = active && (t + k * a.tpr < nsc_me);
+        const bool ok = active && (EXACT || t + k * a.tpr < nsc_me);
         const uint4 v = ok ? *reinterpret_cast<const uint4 *>(rowp + k * a.tpr * 16)
                            : make_uint4(0, 0, 0, 0);
         chunk_to_f2(v, xf[k]);
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
 #pragma unroll
           for (int p = 0; p < 4; ++p) acc = add2(acc, xf[k][p]);
         float v1[1] = {acc.x + acc.y};
-        group_sum<1>(v1, a.tpr, g, a.G, t, red, rpar);
+        group_sum<1, EXACT>(v1, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<1>(v1, r, a.RT, t, xch, xpar);
         const float mu = v1[0] * invN;
         nmu = splat2(-mu);
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         float2 q2 = splat2(0.f);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          if (t + k * a.tpr < nsc_me) {
+          if (EXACT || t + k * a.tpr < nsc_me) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
               const float2 d = add2(xf[k][p], nmu);
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
           }
         }
         float v2[1] = {q2.x + q2.y};
-        group_sum<1>(v2, a.tpr, g, a.G, t, red, rpar);
+        group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<1>(v2, r, a.RT, t, xch, xpar);
         rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
         if (active && t == 0 && crank == 0) a.mean[row0 + r] = mu;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
 #pragma unroll
           for (int p = 0; p < 4; ++p) q2 = fma2(xf[k][p], xf[k][p], q2);
         float v2[1] = {q2.x + q2.y};
-        group_sum<1>(v2, a.tpr, g, a.G, t, red, rpar);
+        group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<1>(v2, r, a.RT, t, xch, xpar);
         rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
       }
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         uint16_t *yrow = a.out + (row0 + r) * a.N + col0 + t * 8;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          if (t + k * a.tpr < nsc_me) {
+          if (EXACT || t + k * a.tpr < nsc_me) {
             float2 o[4];
             float2 bf[4];
             if (MODE == kLayer) chunk_to_f2(bv[k], bf);
@@ -211,24 +213,32 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
 }
 
 template <int MODE, bool CLUSTER>
-const void *pick_fwd(int K) {
+const void *pick_fwd(int K, bool e) {
   switch (K) {
-    case 1: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER>);
-    case 2: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER>);
-    case 3: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER>);
-    case 4: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER>);
-    case 5: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER>);
-    case 6: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER>);
-    case 8: return reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER>);
+    case 1: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, false>);
+    case 2: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, false>);
+    case 3: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, false>);
+    case 4: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, false>);
+    case 5: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, false>);
+    case 6: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, false>);
+    case 8: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, true>)
+                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, false>);
     default: return nullptr;
   }
 }
 
 }  // namespace
 
-const void *fwd_kernel_ptr(int mode, int K, bool cluster) {
-  if (mode == kRMS) return cluster ? pick_fwd<kRMS, true>(K) : pick_fwd<kRMS, false>(K);
-  return cluster ? pick_fwd<kLayer, true>(K) : pick_fwd<kLayer, false>(K);
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact) {
+  if (mode == kRMS)
+    return cluster ? pick_fwd<kRMS, true>(K, exact) : pick_fwd<kRMS, false>(K, exact);
+  return cluster ? pick_fwd<kLayer, true>(K, exact) : pick_fwd<kLayer, false>(K, exact);
 }
 
 }  // namespace gbn

@@ -48,13 +48,14 @@ __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 // barrier of the group's warps.  `red` is the CTA's [2][G][W][4] scratch and
 // `rpar` the buffer parity (flipped on return).  All threads of a group must
 // make the same calls.
-template <int NV>
+// WIDE: the caller guarantees tpr >= 32 (all five butterfly levels).
+template <int NV, bool WIDE>
 __device__ __forceinline__ void group_sum(float (&v)[NV], int tpr, int g, int G, int t,
                                           float *red, int &rpar) {
-  const int width = tpr < 32 ? tpr : 32;
+  const int width = WIDE ? 32 : (tpr < 32 ? tpr : 32);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    if (o < width) {
+    if (WIDE || o < width) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
     }
@@ -69,6 +70,7 @@ __device__ __forceinline__ void group_sum(float (&v)[NV], int tpr, int g, int G,
     named_bar_sync(1 + g, tpr);
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = slot[i];
+#pragma unroll 4
     for (int w = 1; w < W; ++w) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) v[i] += slot[w * 4 + i];

@@ -56,6 +56,8 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
     assert C == 1 or rpg == 1
     assert ntiles == -(-M // RT) and P <= ntiles
     assert K * tpr >= nsc, "a chunk has no owner"
+    if p["exact"]:
+        assert tpr % 32 == 0 and K * tpr == nsc and nc % C == 0, "EXACT plan is not exact"
     L = smem_layout(RT, NS, S, G, tpr, 2 if backward else 1, backward, C > 1)
     assert smem == L["total"] <= smem_optin, "shared memory over the opt-in limit"
     assert L["stage"] < TX_LIMIT
