@@ -314,6 +314,8 @@ def run_ours(args):
     from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
 
     w = wl.WORKLOADS[args.workload]
+    if args.rows:
+        w = wl.like(w, args.rows, w.N)
     x, g, b, dy = wl.make_inputs(w, dev, seed=w.seed + rank)
     stream = torch.cuda.current_stream(dev)
     step = DirectStep(gb, w, x, g, b, dy, stream)
@@ -462,6 +464,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="layer_32768x4096")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override M (smaller cases for profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -219,11 +219,10 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 
   // Shrink the tile until at least two stages fit in shared memory.
   const int budget = smem_optin - 1024;
-  const bool cl = C > 1;
   int S = 0;
   for (;;) {
-    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, tpr, ntensors, bwd, cl);
-    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, tpr, ntensors, bwd, cl);
+    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, tpr, ntensors, bwd, C);
+    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, tpr, ntensors, bwd, C);
     const int per_stage = static_cast<int>(L2.total - L1.total);
     const int fixed = static_cast<int>(L1.total) - per_stage;
     S = (budget - fixed) / per_stage;
@@ -240,7 +239,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   p.S = S;
   p.threads = G * tpr;
   if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
-  const SmemLayout L = make_layout(p.RT, p.NS, S, G, tpr, ntensors, bwd, cl);
+  const SmemLayout L = make_layout(p.RT, p.NS, S, G, tpr, ntensors, bwd, C);
   if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
   // One stage's bytes are counted by a single mbarrier transaction count.
   if (L.stage_bytes >= (1u << 20)) return NORM_ERR_UNSUPPORTED;
@@ -369,6 +368,7 @@ NormArgs base_args(const Plan &p, int64_t M, int N) {
   a.RT = p.RT;
   a.S = p.S;
   a.P = p.P;
+  a.C = p.C;
   a.ntiles = p.ntiles;
   a.invN = 1.0f / static_cast<float>(N);
   return a;

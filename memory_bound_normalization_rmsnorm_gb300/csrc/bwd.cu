@@ -63,10 +63,9 @@ __device__ __forceinline__ void issue_bwd_tile(const NormArgs &a, const SmemLayo
 template <int MODE, int K, bool CLUSTER, bool EXACT>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, CLUSTER);
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
-  float *xch = reinterpret_cast<float *>(smem + L.xch_off);
   const float *stats_all = reinterpret_cast<const float *>(smem + L.stats_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
   int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
@@ -86,6 +85,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
     for (int s = 0; s < a.S; ++s) {
       mbar_init(full + s, 1);
       done_cnt[s] = 0;
+    }
+    if (CLUSTER) {
+      uint64_t *xb = reinterpret_cast<uint64_t *>(smem + L.xch_off +
+                                                  static_cast<uint32_t>(2 * a.RT * a.C * 4) * 4u);
+      mbar_init(xb, 1);
+      mbar_init(xb + 1, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -117,12 +122,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   }
 
   const float invN = a.invN;
-  int rpar = 0, xpar = 0;
-  for (int64_t it = 0;; ++it) {
-    const int64_t tile = cid + it * ncl;
-    if (tile >= a.ntiles) break;
-    const int s = static_cast<int>(it % a.S);
-    const uint32_t par = static_cast<uint32_t>((it / a.S) & 1);
+  int rpar = 0;
+  ClusterXch xch = make_xch(smem, L, a.RT, CLUSTER ? a.C : 1, crank);
+  // Stage s and its phase parity advance with the tile count (no division).
+  int s = 0;
+  uint32_t par = 0;
+  for (int64_t tile = cid; tile < a.ntiles; tile += ncl) {
     mbar_wait(full + s, par, a.err, abort_flag);
     const int64_t row0 = tile * a.RT;
     const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
@@ -167,11 +172,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
       float v[2] = {s1.x + s1.y, s2.x + s2.y};
       if (MODE == kLayer) {
         group_sum<2, EXACT>(v, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<2>(v, r, a.RT, t, xch, xpar);
+        if (CLUSTER) cluster_sum<2>(v, r, t, xch, a.err, abort_flag);
       } else {
         float w1[1] = {v[1]};
         group_sum<1, EXACT>(w1, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(w1, r, a.RT, t, xch, xpar);
+        if (CLUSTER) cluster_sum<1>(w1, r, t, xch, a.err, abort_flag);
         v[1] = w1[0];
       }
       const float2 av = splat2((MODE == kLayer) ? v[0] * invN : 0.f);
@@ -203,6 +208,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
         __syncwarp();
         issue_bwd_tile<MODE, CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
       }
+    }
+    if (++s == a.S) {
+      s = 0;
+      par ^= 1u;
     }
   }
 

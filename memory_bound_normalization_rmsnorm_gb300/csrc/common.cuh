@@ -41,6 +41,7 @@ struct NormArgs {
   int RT;   // rows per tile
   int S;    // pipeline stages
   int P;    // partial rows (backward) = number of clusters in the grid
+  int C;    // CTAs per cluster
   float eps;
   float invN;
 };
@@ -52,7 +53,8 @@ struct SmemLayout {
   uint32_t stats_off;     // backward: [S][RT][2] floats (rstd, mean)
   uint32_t red_off;       // [2][G][W][4] floats, cross-warp group partials
                           // (W = tpr / 32; only when tpr > 32)
-  uint32_t xch_off;       // [2][RT][4] floats, cross-CTA partials (clusters only)
+  uint32_t xch_off;       // clusters only: [2][RT][C][4] floats of cross-CTA
+                          // partials, then 2 mbarriers (one per buffer)
   uint32_t bar_off;       // [S] mbarriers
   uint32_t flag_off;      // abort flag (int), then [S] ints: warps done per stage
   uint32_t total;
@@ -66,9 +68,10 @@ __host__ __device__ inline uint32_t align16(uint32_t v) {
   return (v + 15u) & ~15u;
 }
 
+// C: CTAs per cluster (1: no cluster exchange region).
 __host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
                                                   int tpr, int ntensors,
-                                                  bool stats, bool cluster) {
+                                                  bool stats, int C) {
   SmemLayout L;
   L.tensor_bytes = static_cast<uint32_t>(RT) * static_cast<uint32_t>(NS) * 2u;
   L.stage_bytes = L.tensor_bytes * static_cast<uint32_t>(ntensors);
@@ -78,7 +81,7 @@ __host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
   L.red_off = off;
   if (tpr > 32) off = align16(off + static_cast<uint32_t>(2 * G * (tpr / 32) * 4) * 4u);
   L.xch_off = off;
-  if (cluster) off = align16(off + static_cast<uint32_t>(2 * RT * 4) * 4u);
+  if (C > 1) off = align16(off + static_cast<uint32_t>(2 * RT * C * 4) * 4u + 16u);
   L.bar_off = off;
   off = align16(off + static_cast<uint32_t>(S) * 8u);
   L.flag_off = off;

@@ -56,10 +56,9 @@ __device__ __forceinline__ void issue_fwd_tile(const NormArgs &a, const SmemLayo
 template <int MODE, int K, bool CLUSTER, bool EXACT>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, CLUSTER);
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
-  float *xch = reinterpret_cast<float *>(smem + L.xch_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
   int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
 
@@ -78,6 +77,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
     for (int s = 0; s < a.S; ++s) {
       mbar_init(full + s, 1);
       done_cnt[s] = 0;
+    }
+    if (CLUSTER) {
+      uint64_t *xb = reinterpret_cast<uint64_t *>(smem + L.xch_off +
+                                                  static_cast<uint32_t>(2 * a.RT * a.C * 4) * 4u);
+      mbar_init(xb, 1);
+      mbar_init(xb + 1, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -111,12 +116,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   }
 
   const float invN = a.invN;
-  int rpar = 0, xpar = 0;
-  for (int64_t it = 0;; ++it) {
-    const int64_t tile = cid + it * ncl;
-    if (tile >= a.ntiles) break;
-    const int s = static_cast<int>(it % a.S);
-    const uint32_t par = static_cast<uint32_t>((it / a.S) & 1);
+  int rpar = 0;
+  ClusterXch xch = make_xch(smem, L, a.RT, CLUSTER ? a.C : 1, crank);
+  // Stage s and its phase parity advance with the tile count (no division).
+  int s = 0;
+  uint32_t par = 0;
+  for (int64_t tile = cid; tile < a.ntiles; tile += ncl) {
     mbar_wait(full + s, par, a.err, abort_flag);
     const int64_t row0 = tile * a.RT;
     const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
           for (int p = 0; p < 4; ++p) acc = add2(acc, xf[k][p]);
         float v1[1] = {acc.x + acc.y};
         group_sum<1, EXACT>(v1, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(v1, r, a.RT, t, xch, xpar);
+        if (CLUSTER) cluster_sum<1>(v1, r, t, xch, a.err, abort_flag);
         const float mu = v1[0] * invN;
         nmu = splat2(-mu);
         // Pass 2: sum of squared deviations, over owned chunks only.
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         }
         float v2[1] = {q2.x + q2.y};
         group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(v2, r, a.RT, t, xch, xpar);
+        if (CLUSTER) cluster_sum<1>(v2, r, t, xch, a.err, abort_flag);
         rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
         if (active && t == 0 && crank == 0) a.mean[row0 + r] = mu;
       } else {
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
           for (int p = 0; p < 4; ++p) q2 = fma2(xf[k][p], xf[k][p], q2);
         float v2[1] = {q2.x + q2.y};
         group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(v2, r, a.RT, t, xch, xpar);
+        if (CLUSTER) cluster_sum<1>(v2, r, t, xch, a.err, abort_flag);
         rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
       }
 
@@ -206,6 +211,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         fence_proxy_async_smem();
         issue_fwd_tile<CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
       }
+    }
+    if (++s == a.S) {
+      s = 0;
+      par ^= 1u;
     }
   }
   // No CTA may leave while a peer could still read its shared memory.

@@ -157,6 +157,28 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(const void *local,
   return v;
 }
 
+// Shared::cluster address of `local` (this CTA's shared memory) in CTA
+// `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(const void *local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_addr(local)), "r"(rank));
+  return remote;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory whose
+// completion is counted (in bytes) on that CTA's mbarrier `remote_bar`.
+// Orders nothing else: no fence over this thread's other memory traffic.
+__device__ __forceinline__ void st_async_f32x4(uint32_t remote_addr, float4 v,
+                                               uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(remote_addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------ barriers
 // Named barrier for `nthreads` threads (multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

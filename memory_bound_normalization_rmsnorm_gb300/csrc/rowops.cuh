@@ -79,32 +79,68 @@ __device__ __forceinline__ void group_sum(float (&v)[NV], int tpr, int g, int G,
   }
 }
 
-// Sum of NV values over the C CTAs of the cluster for row slot `r`, in
-// CTA-rank order, so every CTA gets the same bits.  Also a cluster-wide
-// barrier: on return every thread of the cluster has passed the point of
-// its call.  `xch` is the CTA's [2][RT][4] scratch.
+// Cross-CTA exchange state of a cluster kernel.  Buffer b (two of them,
+// used alternately by successive rounds) holds [RT][C] float4 slots and has
+// one mbarrier; `phase` bit b is the parity of buffer b's current round.
+struct ClusterXch {
+  float *slots;    // [2][RT][C][4]
+  uint64_t *bars;  // [2]
+  int RT;
+  int C;
+  int crank;
+  int buf;
+  uint32_t phase;
+};
+
+__device__ __forceinline__ ClusterXch make_xch(unsigned char *smem, const SmemLayout &L,
+                                               int RT, int C, int crank) {
+  ClusterXch x;
+  x.slots = reinterpret_cast<float *>(smem + L.xch_off);
+  x.bars = reinterpret_cast<uint64_t *>(smem + L.xch_off + static_cast<uint32_t>(2 * RT * C * 4) * 4u);
+  x.RT = RT;
+  x.C = C;
+  x.crank = crank;
+  x.buf = 0;
+  x.phase = 0;
+  return x;
+}
+
+// Sum of NV values over the C CTAs of the cluster for row slot `r` of the
+// tile, in CTA-rank order, so every CTA gets the same bits.  One round:
+// thread 0 of the CTA posts the bytes the round expects (RT rows x C ranks
+// x 16 bytes) on the local buffer mbarrier; thread t == 0 of every row
+// group pushes its group total into slot [r][crank] of EVERY CTA of the
+// cluster (itself included) with asynchronous stores that complete on the
+// receiver's mbarrier; every thread then waits for the local mbarrier and
+// folds the C slots of its row.  No cluster barrier and no memory fence:
+// nothing orders the threads' global stores.  Every thread of the CTA must
+// make the same sequence of calls.  Two buffers suffice: a CTA can only send
+// round k+2 after receiving every CTA's round k+1, which each sends only
+// after all of its groups finished reading round k.
 template <int NV>
-__device__ __forceinline__ void cluster_sum(float (&v)[NV], int r, int RT, int t, float *xch,
-                                            int &xpar) {
-  float *slot = xch + (static_cast<size_t>(xpar) * RT + r) * 4;
+__device__ __forceinline__ void cluster_sum(float (&v)[NV], int r, int t, ClusterXch &x,
+                                            unsigned *err, volatile int *abort) {
+  const int b = x.buf;
+  float *base = x.slots + static_cast<size_t>(b) * x.RT * x.C * 4;
+  uint64_t *bar = x.bars + b;
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(x.RT * x.C * 16));
   if (t == 0) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) slot[i] = v[i];
+    const float4 val = make_float4(v[0], NV > 1 ? v[NV > 1 ? 1 : 0] : 0.f,
+                                   NV > 2 ? v[NV > 2 ? 2 : 0] : 0.f, 0.f);
+    const float *mine = base + (static_cast<size_t>(r) * x.C + x.crank) * 4;
+    for (int q = 0; q < x.C; ++q)
+      st_async_f32x4(mapa_shared(mine, q), val, mapa_shared(bar, q));
   }
-  cluster_arrive_release();
-  cluster_wait_acquire();
-  const int C = static_cast<int>(cluster_nctarank());
-  const int lane = threadIdx.x & 31;
-  float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (lane < C) f = ld_dsmem_f32x4(slot, static_cast<uint32_t>(lane));
-  const float mine[4] = {f.x, f.y, f.z, f.w};
+  mbar_wait(bar, (x.phase >> b) & 1u, err, abort);
+  x.phase ^= 1u << b;
+  const float *row = base + static_cast<size_t>(r) * x.C * 4;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    float acc = __shfl_sync(0xffffffffu, mine[i], 0);
-    for (int q = 1; q < C; ++q) acc += __shfl_sync(0xffffffffu, mine[i], q);
+    float acc = row[i];
+    for (int q = 1; q < x.C; ++q) acc += row[q * 4 + i];
     v[i] = acc;
   }
-  xpar ^= 1;
+  x.buf ^= 1;
 }
 
 // ---------------------------------------------------- ring hand-off

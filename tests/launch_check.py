@@ -16,7 +16,7 @@ def _align16(v):
     return (v + 15) & ~15
 
 
-def smem_layout(RT, NS, S, G, tpr, ntensors, stats, cluster):
+def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C):
     """Same region order as the kernels' shared-memory layout."""
     tensor = RT * NS * 2
     stage = tensor * ntensors
@@ -28,8 +28,8 @@ def smem_layout(RT, NS, S, G, tpr, ntensors, stats, cluster):
     if tpr > 32:
         off = _align16(off + 2 * G * (tpr // 32) * 4 * 4)
     L["xch"] = off
-    if cluster:
-        off = _align16(off + 2 * RT * 4 * 4)
+    if C > 1:
+        off = _align16(off + 2 * RT * C * 4 * 4 + 16)
     L["bar"] = off
     off = _align16(off + S * 8)
     L["flag"] = off
@@ -58,7 +58,7 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
     assert K * tpr >= nsc, "a chunk has no owner"
     if p["exact"]:
         assert tpr % 32 == 0 and K * tpr == nsc and nc % C == 0, "EXACT plan is not exact"
-    L = smem_layout(RT, NS, S, G, tpr, 2 if backward else 1, backward, C > 1)
+    L = smem_layout(RT, NS, S, G, tpr, 2 if backward else 1, backward, C)
     assert smem == L["total"] <= smem_optin, "shared memory over the opt-in limit"
     assert L["stage"] < TX_LIMIT
     assert L["bar"] % 8 == 0 and L["stats"] % 16 == 0 and L["red"] % 16 == 0
@@ -112,8 +112,10 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
         hi = ((1 * G + (G - 1)) * W + (W - 1)) * 4 + 4
         assert L["red"] + hi * 4 <= L["xch"]
     if C > 1:
-        hi = (1 * RT + (RT - 1)) * 4 + 4
-        assert L["xch"] + hi * 4 <= L["bar"]
+        # slot [buf][r][q] float4 for buf < 2, r < RT, q < C; then 2 mbarriers
+        hi = ((1 * RT + (RT - 1)) * C + (C - 1)) * 4 + 4
+        bars = L["xch"] + 2 * RT * C * 16
+        assert L["xch"] + hi * 4 <= bars and bars % 8 == 0 and bars + 16 <= L["bar"]
     return True
 
 
