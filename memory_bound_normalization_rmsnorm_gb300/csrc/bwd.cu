@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
       const unsigned char *xrow = stx + static_cast<size_t>(r) * a.NS * 2 + t * 16;
       // xhat and g = dy * gamma stay in registers between the two passes.
       float2 xh[K][4], gg[K][4];
-      float2 s1 = splat2(0.f), s2 = splat2(0.f);
+      float2 s1 = splat2(0.f), s2 = splat2(0.f), s1b = splat2(0.f), s2b = splat2(0.f);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const bool ok = active && (EXACT || t + k * a.tpr < nsc_me);
@@ -163,12 +163,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
         for (int p = 0; p < 4; ++p) {
           xh[k][p] = mul2(add2(xf[p], nmu), rs2);
           gg[k][p] = mul2(df[p], gf[k][p]);
-          s2 = fma2(gg[k][p], xh[k][p], s2);
-          if (MODE == kLayer) s1 = add2(s1, gg[k][p]);
+          // two independent accumulator pairs shorten the dependency chains
+          if (p & 1) {
+            s2b = fma2(gg[k][p], xh[k][p], s2b);
+            if (MODE == kLayer) s1b = add2(s1b, gg[k][p]);
+          } else {
+            s2 = fma2(gg[k][p], xh[k][p], s2);
+            if (MODE == kLayer) s1 = add2(s1, gg[k][p]);
+          }
           accg[k][p] = fma2(df[p], xh[k][p], accg[k][p]);
           if (MODE == kLayer) accb[k][p] = add2(accb[k][p], df[p]);
         }
       }
+      s1 = add2(s1, s1b);
+      s2 = add2(s2, s2b);
       float v[2] = {s1.x + s1.y, s2.x + s2.y};
       if (MODE == kLayer) {
         group_sum<2, EXACT>(v, a.tpr, g, a.G, t, red, rpar);

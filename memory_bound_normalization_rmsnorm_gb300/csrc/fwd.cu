@@ -141,8 +141,37 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
       }
       float rs;
       float2 nmu = splat2(0.f);
-      if (MODE == kLayer) {
-        // Pass 1: mean.
+      if (MODE == kLayer && EXACT) {
+        // This thread's (mean, M2) over its K*8 elements (two passes over
+        // registers), then one reduction round of equal-count merges.
+        constexpr float n_t = 8.f * K;
+        float2 a0 = splat2(0.f), a1 = splat2(0.f);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          a0 = add2(a0, add2(xf[k][0], xf[k][1]));
+          a1 = add2(a1, add2(xf[k][2], xf[k][3]));
+        }
+        const float2 at = add2(a0, a1);
+        float m = (at.x + at.y) * (1.0f / n_t);
+        const float2 nm = splat2(-m);
+        float2 q0 = splat2(0.f), q1 = splat2(0.f);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const float2 d0 = add2(xf[k][0], nm), d1 = add2(xf[k][1], nm);
+          const float2 d2 = add2(xf[k][2], nm), d3 = add2(xf[k][3], nm);
+          q0 = fma2(d0, d0, fma2(d1, d1, q0));
+          q1 = fma2(d2, d2, fma2(d3, d3, q1));
+        }
+        const float2 qt = add2(q0, q1);
+        float q = qt.x + qt.y;
+        group_meanvar(m, q, n_t, a.tpr, g, a.G, t, red, rpar);
+        if (CLUSTER) cluster_meanvar(m, q, static_cast<float>(a.NS), r, t, xch, a.err, abort_flag);
+        nmu = splat2(-m);
+        rs = rsqrtf(q * invN + a.eps);
+        if (active && t == 0 && crank == 0) a.mean[row0 + r] = m;
+      } else if (MODE == kLayer) {
+        // Ragged slices: exact two-pass, the mean first, then the sum of
+        // squared deviations over owned chunks only.
         float2 acc = splat2(0.f);
 #pragma unroll
         for (int k = 0; k < K; ++k)
@@ -153,7 +182,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         if (CLUSTER) cluster_sum<1>(v1, r, t, xch, a.err, abort_flag);
         const float mu = v1[0] * invN;
         nmu = splat2(-mu);
-        // Pass 2: sum of squared deviations, over owned chunks only.
         float2 q2 = splat2(0.f);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -168,18 +196,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         float v2[1] = {q2.x + q2.y};
         group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<1>(v2, r, t, xch, a.err, abort_flag);
-        rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
+        rs = rsqrtf(v2[0] * invN + a.eps);
         if (active && t == 0 && crank == 0) a.mean[row0 + r] = mu;
       } else {
-        float2 q2 = splat2(0.f);
+        float2 q0 = splat2(0.f), q1 = splat2(0.f);
 #pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-          for (int p = 0; p < 4; ++p) q2 = fma2(xf[k][p], xf[k][p], q2);
-        float v2[1] = {q2.x + q2.y};
+        for (int k = 0; k < K; ++k) {
+          q0 = fma2(xf[k][0], xf[k][0], fma2(xf[k][1], xf[k][1], q0));
+          q1 = fma2(xf[k][2], xf[k][2], fma2(xf[k][3], xf[k][3], q1));
+        }
+        const float2 qt = add2(q0, q1);
+        float v2[1] = {qt.x + qt.y};
         group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
         if (CLUSTER) cluster_sum<1>(v2, r, t, xch, a.err, abort_flag);
-        rs = 1.0f / sqrtf(v2[0] * invN + a.eps);
+        rs = rsqrtf(v2[0] * invN + a.eps);
       }
 
       if (active) {
