@@ -161,6 +161,41 @@ typedef struct {
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
                         int sm_count, int smem_optin_bytes, norm_plan_t *out);
 
+/*
+ * norm_bwd_noalloc -- norm_bwd for callers that cannot allocate device
+ * memory.  (An addition of this library; the normalisation pages describe
+ * no such entry point.)
+ *
+ * Some callers may not call cudaMalloc or any allocator at all: code whose
+ * device memory is owned entirely by a framework's pool or a pre-reserved
+ * arena, latency-critical paths where an allocation (which can synchronise
+ * the device) is not acceptable, and plugin interfaces that are handed only
+ * the input and output pointers.  This entry point takes exactly the
+ * arguments of norm_bwd minus the workspace and uses, as its scratch space,
+ * a fixed array of NORM_NOALLOC_WORKSPACE_BYTES (16 MiB) that the library
+ * declares in device memory; every GPU that loads the library holds that
+ * array until the process exits.  It calls no allocation routine.
+ *
+ *   - The scratch need is norm_bwd_workspace_bytes(M, N, mode) (the number
+ *     of partial rows times N times 4 bytes, twice for LAYER); a shape
+ *     whose need exceeds NORM_NOALLOC_WORKSPACE_BYTES is rejected with
+ *     NORM_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last
+ *     call's contents.  Nothing in it needs clearing (each call writes
+ *     every partial it later reads), but two calls that overlap on the GPU
+ *     (different streams, or different host threads) race on it and must
+ *     be serialised by the caller.
+ */
+#define NORM_NOALLOC_WORKSPACE_BYTES (16u << 20)
+
+norm_status_t norm_bwd_noalloc(const void *dy, const void *x, const void *gamma,
+                               const float *rstd, const float *mean,
+                               int64_t M, int64_t N, norm_mode_t mode,
+                               void *dx, float *dgamma, float *dbeta,
+                               norm_stream_t stream);
+
 /* Static, human-readable description of a status code. */
 const char *norm_strerror(norm_status_t status);
 

@@ -84,6 +84,9 @@ def lib():
             L.norm_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp,
                                    _vp, _vp, _vp, ctypes.c_size_t, _vp]
             L.norm_bwd.restype = ctypes.c_int
+            L.norm_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int,
+                                           _vp, _vp, _vp, _vp]
+            L.norm_bwd_noalloc.restype = ctypes.c_int
             L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(Plan)]
             L.norm_plan.restype = ctypes.c_int

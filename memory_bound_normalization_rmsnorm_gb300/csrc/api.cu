@@ -377,6 +377,19 @@ NormArgs base_args(const Plan &p, int64_t M, int N) {
 }  // namespace
 }  // namespace gbn
 
+// ---------------------------------------------------------------------------
+// Allocation-free backward: the scratch lives in a fixed device array of this
+// file.  Host code cannot use the array's name as a device address (on the
+// host it names a stand-in), so the address is looked up once per device
+// with cudaGetSymbolAddress, that device current, and cached.
+static __device__ __align__(256) unsigned char g_noalloc_workspace[NORM_NOALLOC_WORKSPACE_BYTES];
+
+namespace gbn {
+namespace {
+void *g_noalloc_ptr[kMaxDevices];  // guarded by g_mu
+}  // namespace
+}  // namespace gbn
+
 using namespace gbn;
 
 extern "C" {
@@ -509,6 +522,38 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   out->partials = p.P;
   out->exact = p.exact ? 1 : 0;
   return NORM_OK;
+}
+
+norm_status_t norm_bwd_noalloc(const void *dy, const void *x, const void *gamma,
+                               const float *rstd, const float *mean, int64_t M, int64_t N,
+                               norm_mode_t mode, void *dx, float *dgamma, float *dbeta,
+                               norm_stream_t stream) {
+  // Size check first: nothing is launched for a shape that does not fit.
+  size_t need = 0;
+  norm_status_t st = norm_bwd_workspace_bytes(M, N, mode, &need);
+  if (st != NORM_OK) return st;
+  if (need > NORM_NOALLOC_WORKSPACE_BYTES) return NORM_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return NORM_ERR_UNSUPPORTED;
+  void *ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = p;
+    }
+    ws = g_noalloc_ptr[dev];
+  }
+  return norm_bwd(dy, x, gamma, rstd, mean, M, N, mode, dx, dgamma, dbeta, ws,
+                  NORM_NOALLOC_WORKSPACE_BYTES, stream);
 }
 
 const char *norm_strerror(norm_status_t s) {
