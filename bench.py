@@ -141,15 +141,25 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None}
 
 
-def dist_setup():
+def dist_setup(backend="nccl"):
+    """One process per GPU under torchrun: (world, rank, local_rank).  Only
+    the timing uses the process group (a barrier and a max over ranks): the
+    replicas exchange no data."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl")
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
     return world, rank, local
+
+
+def aggregate_throughput(step_bytes, steps, ms_per_rank_max, world):
+    """Whole-job GB/s: every rank processed `steps` steps of `step_bytes`;
+    the job took the slowest rank's time."""
+    return world * step_bytes * steps / (ms_per_rank_max * 1e-3) / 1e9
 
 
 def max_over_ranks(v, world, device):
@@ -357,7 +367,7 @@ def run_ours(args):
     fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
     step_bytes = fwd_b + bwd_b
-    value = world * step_bytes * args.steps / (total_ms_max * 1e-3) / 1e9
+    value = aggregate_throughput(step_bytes, args.steps, total_ms_max, world)
 
     # end to end through the public Python API from pinned host buffers
     e2e = None
@@ -457,6 +467,55 @@ def run_e2e(gb, w, x, g, b, dy, dev, steps, step_bytes, world):
             "steps": steps}
 
 
+def run_sweep(args):
+    """One JSON line per workload: fwd and bwd timed separately (CUDA events
+    around `iters` back-to-back calls of each pass on the default stream,
+    inputs resident in HBM and larger than L2 except for the small case)."""
+    import torch
+
+    import memory_bound_normalization_rmsnorm_gb300 as gb
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = peak_hbm()
+    names = list(wl.WORKLOADS) if args.sweep == "all" else args.sweep.split(",")
+    for name in names:
+        w = wl.WORKLOADS[name]
+        x, g, b, dy = wl.make_inputs(w, "cuda")
+        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream())
+        pf = gb.norm_plan(w.M, w.N, w.mode, False)
+        pb = gb.norm_plan(w.M, w.N, w.mode, True)
+        res = {}
+        for name_, fn in (("fwd", step.fwd), ("bwd", step.bwd)):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            res[name_] = e0.elapsed_time(e1) / args.steps
+        if gb.norm_get_device_error() != 0:
+            raise RuntimeError(f"device error word set on {name}")
+        fb, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"])
+        keep = ("cluster", "threads_per_row", "chunks_per_thread", "groups", "rows_per_group",
+                "stages", "grid", "exact")
+        print(json.dumps({
+            "workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
+            "fwd_us": 1e3 * res["fwd"], "bwd_us": 1e3 * res["bwd"],
+            "fwd_GBs": fb / res["fwd"] / 1e6, "bwd_GBs": bb / res["bwd"] / 1e6,
+            "step_GBs": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6,
+            "step_frac": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6 / peak,
+            "peak": peak, "peak_kind": peak_kind, "iters": args.steps,
+            "plan_fwd": {k: pf[k] for k in keep}, "plan_bwd": {k: pb[k] for k in keep}}),
+            flush=True)
+        del step, x, g, b, dy
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -470,10 +529,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sweep", default="",
+                    help="'all' or comma-separated workload names: per-workload fwd/bwd "
+                         "timings, one JSON line each (not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
