@@ -156,6 +156,9 @@ typedef struct {
     int32_t exact;             /* 1: every CTA slice is exactly
                                   threads_per_row * chunks_per_thread chunks
                                   (kernels without ownership tests) */
+    int32_t long_rows;         /* 1: long-row kernels (the row slice is read
+                                  twice from shared memory instead of being
+                                  held in registers) */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

@@ -1,6 +1,6 @@
 """Builds the CUDA library libgbnorm.so in-tree for sm_103a.
 
-Three translation units (forward kernels, backward kernels, host ABI) are
+Four translation units (forward, backward and long-row kernels, host ABI) are
 compiled in parallel with nvcc and linked into one shared object with the
 CUDA runtime linked statically, so the library needs no CUDA library path at
 load time.  `python -m memory_bound_normalization_rmsnorm_gb300.builder -v`
@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgbnorm.so")
-SOURCES = ["fwd.cu", "bwd.cu", "api.cu"]
+SOURCES = ["fwd.cu", "bwd.cu", "long.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

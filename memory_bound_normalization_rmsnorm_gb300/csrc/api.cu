@@ -104,7 +104,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Optional plan override for tuning sweeps: GBNORM_PLAN="C=2,tpr=256,rpg=1,S=4"
 // (any subset).  Fields left out keep the heuristic's choice.
 struct Override {
-  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0;
+  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0;
   bool any = false;
 };
 
@@ -124,6 +124,8 @@ Override read_override() {
     else if (!std::strcmp(key, "S")) o.S = val;
     else if (!std::strcmp(key, "G")) o.G = val;
     else if (!std::strcmp(key, "ctas")) o.ctas = val;
+    else if (!std::strcmp(key, "long")) o.lng = val;
+    else if (!std::strcmp(key, "K")) o.K = val;
     o.any = true;
   }
   return o;
@@ -134,13 +136,95 @@ int round_k(int K, bool bwd) {
   return K == 7 ? 8 : K;
 }
 
+// Ring and tile sizing shared by both plan kinds: rows per tile and the
+// number of stages that fit in shared memory (at least two).
+norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, int64_t M) {
+  const int ntensors = bwd ? 2 : 1;
+  const int C = p.C;
+  int G = p.G;
+  const int row_bytes = p.NS * 2;
+  int rpg = 1;
+  if (C == 1) rpg = std::max(1, (32 * 1024) / (row_bytes * G));
+  if (ov.rpg) rpg = ov.rpg;
+  if (rpg < 1 || (C > 1 && rpg != 1)) return NORM_ERR_UNSUPPORTED;
+  const int budget = smem_optin - 1024;
+  int S = 0;
+  for (;;) {
+    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C);
+    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, p.tpr, ntensors, bwd, C);
+    const int per_stage = static_cast<int>(L2.total - L1.total);
+    const int fixed = static_cast<int>(L1.total) - per_stage;
+    S = (budget - fixed) / per_stage;
+    if (S >= 2 || ov.rpg || ov.G || (rpg == 1 && G == 1)) break;
+    if (rpg > 1) rpg = (rpg + 1) / 2;
+    else G = (G + 1) / 2;
+  }
+  S = std::min(S, 8);
+  if (ov.S) S = ov.S;
+  if (S < 2) return NORM_ERR_UNSUPPORTED;
+  p.G = G;
+  p.rpg = rpg;
+  p.RT = G * rpg;
+  p.S = S;
+  p.threads = G * p.tpr;
+  if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
+  const SmemLayout L = make_layout(p.RT, p.NS, S, G, p.tpr, ntensors, bwd, C);
+  if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
+  if (L.stage_bytes >= (1u << 20)) return NORM_ERR_UNSUPPORTED;
+  if (bwd && static_cast<int64_t>(2) * G * p.NS * 4 > static_cast<int64_t>(S) * L.stage_bytes)
+    return NORM_ERR_UNSUPPORTED;
+  p.smem = L.total;
+  p.ntiles = (M + p.RT - 1) / p.RT;
+  return NORM_OK;
+}
+
+// Plan for the long-row kernels: K chunks per thread (8 forward, 4
+// backward), two row groups of up to 256 threads per CTA when the slice
+// allows, and the smallest power-of-two cluster whose slices fit.
+norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, const Override &ov,
+                        Plan *out) {
+  const int nc = N / 8;
+  Plan p;
+  p.long_rows = true;
+  // 8 chunks per thread only where that fits in registers without spilling
+  // (RMSNorm forward); 4 elsewhere.
+  int K = ov.K ? ov.K : ((!bwd && mode == kRMS) ? 8 : 4);
+  if (K != 4 && K != 8) return NORM_ERR_UNSUPPORTED;
+  // Slices up to kMaxThreads threads x K chunks per CTA; clusters when the
+  // row is wider.  Without a cluster, up to two row groups per CTA overlap
+  // each other's reductions; in a cluster one group of up to kMaxThreads
+  // threads per CTA, the cross-CTA exchange being overlapped by the kernel's
+  // software pipeline instead.
+  int C = 1;
+  while (C < 16 && ceil_div(nc, C) > kMaxThreads * K) C <<= 1;
+  if (ov.C) C = ov.C;
+  if (C < 1 || C > 16) return NORM_ERR_UNSUPPORTED;
+  p.C = C;
+  p.nsc = ceil_div(nc, C);
+  p.NS = p.nsc * 8;
+  if ((C - 1) * p.nsc >= nc) return NORM_ERR_UNSUPPORTED;
+  int tpr = ov.tpr ? ov.tpr : 32 * ceil_div(ceil_div(p.nsc, K), 32);
+  if (tpr < 32 || tpr > kMaxThreads || tpr % 32) return NORM_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(tpr) * K < p.nsc) return NORM_ERR_UNSUPPORTED;
+  p.tpr = tpr;
+  p.K = K;
+  p.exact = (nc % C == 0) && (tpr * K == p.nsc);
+  p.G = ov.G ? ov.G : (C > 1 ? 1 : std::max(1, std::min(2, kMaxThreads / tpr)));
+  if (p.G * tpr > kMaxThreads || p.G > 15) return NORM_ERR_UNSUPPORTED;
+  if (C > 1 && p.G != 1) return NORM_ERR_UNSUPPORTED;  // one row per CTA per tile
+  norm_status_t st = size_ring(p, bwd, smem_optin, ov, M);
+  if (st != NORM_OK) return st;
+  if (!long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd)) return NORM_ERR_UNSUPPORTED;
+  *out = p;
+  return NORM_OK;
+}
+
 // Shape part of the plan for one pass: everything except the grid size.
 // Pure host arithmetic (no CUDA call).  `bwd` selects the backward kernel
 // (two tensors per stage, at most kMaxKBwd chunks per thread).
 norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
                          const Override &ov, Plan *out) {
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
-  const int ntensors = bwd ? 2 : 1;
   const int nc = N / 8;
   Plan p;
 
@@ -149,6 +233,11 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   // LayerNorm 2, RMSNorm 3); up to kmax only when a row needs it.
   const int kpref = bwd ? 2 : 4;
   const int klim = bwd ? (mode == kLayer ? 2 : 3) : (mode == kLayer ? 4 : 6);
+
+  // Rows wider than one CTA's register capacity (kMaxThreads x klim chunks)
+  // go to the long-row kernels, which keep the row in shared memory.
+  if (ov.lng == 1 || (ov.lng != 0 && nc > kMaxThreads * klim))
+    return long_plan(mode, bwd, M, N, smem_optin, ov, out);
 
   // Column split: the smallest power-of-two cluster (up to 8) whose per-CTA
   // slice fits kMaxThreads threads x kpref chunks, else the smallest (up to
@@ -209,47 +298,17 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   if (G < 1 || G * tpr > kMaxThreads || (tpr > 32 && G > 15))
     return NORM_ERR_UNSUPPORTED;
 
-  // Rows per tile: about 32 KB of stage per tensor, one row per group in a
-  // cluster (every row there costs a cluster barrier).
-  const int row_bytes = p.NS * 2;
-  int rpg = 1;
-  if (C == 1) rpg = std::max(1, (32 * 1024) / (row_bytes * G));
-  if (ov.rpg) rpg = ov.rpg;
-  if (rpg < 1 || (C > 1 && rpg != 1)) return NORM_ERR_UNSUPPORTED;
-
-  // Shrink the tile until at least two stages fit in shared memory.
-  const int budget = smem_optin - 1024;
-  int S = 0;
-  for (;;) {
-    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, tpr, ntensors, bwd, C);
-    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, tpr, ntensors, bwd, C);
-    const int per_stage = static_cast<int>(L2.total - L1.total);
-    const int fixed = static_cast<int>(L1.total) - per_stage;
-    S = (budget - fixed) / per_stage;
-    if (S >= 2 || ov.rpg || ov.G || (rpg == 1 && G == 1)) break;
-    if (rpg > 1) rpg = (rpg + 1) / 2;
-    else G = (G + 1) / 2;
-  }
-  S = std::min(S, 8);
-  if (ov.S) S = ov.S;
-  if (S < 2) return NORM_ERR_UNSUPPORTED;
   p.G = G;
-  p.rpg = rpg;
-  p.RT = G * rpg;
-  p.S = S;
-  p.threads = G * tpr;
-  if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
-  const SmemLayout L = make_layout(p.RT, p.NS, S, G, tpr, ntensors, bwd, C);
-  if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
-  // One stage's bytes are counted by a single mbarrier transaction count.
-  if (L.stage_bytes >= (1u << 20)) return NORM_ERR_UNSUPPORTED;
-  // The backward column-partial fold reuses the ring.
-  if (bwd && static_cast<int64_t>(2) * G * p.NS * 4 > static_cast<int64_t>(S) * L.stage_bytes)
-    return NORM_ERR_UNSUPPORTED;
-  p.smem = L.total;
-  p.ntiles = (M + p.RT - 1) / p.RT;
+  norm_status_t st = size_ring(p, bwd, smem_optin, ov, M);
+  if (st != NORM_OK) return st;
   *out = p;
   return NORM_OK;
+}
+
+const void *kernel_for(const Plan &p, int mode, bool bwd) {
+  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd);
+  return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact)
+             : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact);
 }
 
 void set_grid(Plan &p, int64_t resident_clusters) {
@@ -276,8 +335,7 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
   norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p);
   if (st != NORM_OK) return st;
 
-  const void *fn = bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact)
-                        : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact);
+  const void *fn = kernel_for(p, mode, bwd);
   if (!fn) return NORM_ERR_UNSUPPORTED;
   st = prepare_function(dev, fn, d.smem_optin);
   if (st != NORM_OK) return st;
@@ -420,7 +478,7 @@ norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64
   a.mean = mean;
   a.err = d.err;
   a.eps = eps;
-  return launch(fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact), p, a, reinterpret_cast<cudaStream_t>(stream));
+  return launch(kernel_for(p, mode, false), p, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, size_t *bytes) {
@@ -469,7 +527,7 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   a.ws = static_cast<float *>(workspace);
   a.err = d.err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch(bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact), p, a, s)) != NORM_OK) return st;
+  if ((st = launch(kernel_for(p, mode, true), p, a, s)) != NORM_OK) return st;
 
   const int nparts = (mode == NORM_LAYER && dbeta) ? 2 : 1;
   const void *rfn = reduce_kernel_ptr();
@@ -521,6 +579,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   out->grid = p.grid;
   out->partials = p.P;
   out->exact = p.exact ? 1 : 0;
+  out->long_rows = p.long_rows ? 1 : 0;
   return NORM_OK;
 }
 

@@ -15,48 +15,11 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
+#include "tiles.cuh"
 
 namespace gbn {
 
 namespace {
-
-// Issues tile `tile` into stage `s`: the rows' statistics with 4-byte
-// cp.async copies (one completion arrival per lane), then x and dy with
-// bulk copies.  Must be called by all 32 lanes of one warp.
-template <int MODE, bool CLUSTER>
-__device__ __forceinline__ void issue_bwd_tile(const NormArgs &a, const SmemLayout &L,
-                                               unsigned char *smem, int64_t tile, int s,
-                                               int col0, int nsc_me, uint64_t pol) {
-  const int lane = threadIdx.x & 31;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
-  unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
-  float *stats = reinterpret_cast<float *>(smem + L.stats_off) + static_cast<size_t>(s) * a.RT * 2;
-  const int64_t row0 = tile * a.RT;
-  const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-  for (int r = lane; r < nrows; r += 32) {
-    cp_async_4(stats + 2 * r, a.rstd + row0 + r);
-    if (MODE == kLayer) cp_async_4(stats + 2 * r + 1, a.mean + row0 + r);
-  }
-  cp_async_mbar_arrive(full);
-  __syncwarp();
-  if (lane == 0) {
-    if (!CLUSTER) {
-      const uint32_t bytes = static_cast<uint32_t>(nrows) * a.N * 2u;
-      mbar_arrive_expect_tx(full, 2u * bytes);
-      bulk_g2s(dst, a.x + row0 * a.N, bytes, full, pol);
-      bulk_g2s(dst + L.tensor_bytes, a.dy + row0 * a.N, bytes, full, pol);
-    } else {
-      const uint32_t bytes = static_cast<uint32_t>(nsc_me) * 16u;
-      const uint32_t stride = static_cast<uint32_t>(a.NS) * 2u;
-      mbar_arrive_expect_tx(full, 2u * bytes * nrows);
-      for (int r = 0; r < nrows; ++r) {
-        const int64_t off = (row0 + r) * a.N + col0;
-        bulk_g2s(dst + r * stride, a.x + off, bytes, full, pol);
-        bulk_g2s(dst + L.tensor_bytes + r * stride, a.dy + off, bytes, full, pol);
-      }
-    }
-  }
-}
 
 // EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
 // chunk needs an ownership test and the warp butterfly is full width.
@@ -87,10 +50,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
       done_cnt[s] = 0;
     }
     if (CLUSTER) {
-      uint64_t *xb = reinterpret_cast<uint64_t *>(smem + L.xch_off +
-                                                  static_cast<uint32_t>(2 * a.RT * a.C * 4) * 4u);
-      mbar_init(xb, 1);
-      mbar_init(xb + 1, 1);
+      uint64_t *xb = xch_bars(smem, L, a.RT, a.C);
+      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -223,41 +184,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
     }
   }
 
-  // Column partials: fold the G groups of this CTA in group order through
-  // shared memory (the ring is idle now: every issued tile was consumed),
-  // then write one partial row slice per CTA.
-  __syncthreads();
-  float *accs = reinterpret_cast<float *>(smem);  // [G][NS] dgamma, [G][NS] dbeta
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int c = t + k * a.tpr;
-    if (c < nsc_me) {
-      float4 *dg = reinterpret_cast<float4 *>(accs + static_cast<size_t>(g) * a.NS + c * 8);
-      dg[0] = make_float4(accg[k][0].x, accg[k][0].y, accg[k][1].x, accg[k][1].y);
-      dg[1] = make_float4(accg[k][2].x, accg[k][2].y, accg[k][3].x, accg[k][3].y);
-      if (MODE == kLayer) {
-        float4 *db = reinterpret_cast<float4 *>(accs + static_cast<size_t>(a.G + g) * a.NS + c * 8);
-        db[0] = make_float4(accb[k][0].x, accb[k][0].y, accb[k][1].x, accb[k][1].y);
-        db[1] = make_float4(accb[k][2].x, accb[k][2].y, accb[k][3].x, accb[k][3].y);
-      }
-    }
-  }
-  __syncthreads();
-  const int nq = nsc_me * 2;       // float4s of this CTA's columns
-  const int nq_stride = a.NS / 4;  // float4s per group row in shared memory
-  const int nparts = (MODE == kLayer) ? 2 : 1;
-  for (int w = 0; w < nparts; ++w) {
-    const float4 *src = reinterpret_cast<const float4 *>(accs + static_cast<size_t>(w) * a.G * a.NS);
-    float4 *dst = reinterpret_cast<float4 *>(a.ws + (static_cast<size_t>(w) * a.P + cid) * a.N + col0);
-    for (int j = tid; j < nq; j += blockDim.x) {
-      float4 acc = src[j];
-      for (int q = 1; q < a.G; ++q) {
-        const float4 v = src[static_cast<size_t>(q) * nq_stride + j];
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      dst[j] = acc;
-    }
-  }
+  write_column_partials<MODE, K, EXACT>(a, smem, accg, accb, g, t, nsc_me, cid, col0);
   if (CLUSTER) cluster_sync();
 }
 

@@ -14,6 +14,9 @@ constexpr int kMaxKBwd = 4;
 // Largest CTA (the kernels are compiled for at most this many threads, which
 // lets the compiler give each thread up to 128 registers).
 constexpr int kMaxThreads = 512;
+// Cross-CTA exchange buffers (rounds use them in turn; four allow a round to
+// be pushed before the previous one is consumed).
+constexpr int kXchBuffers = 4;
 
 // Kernel arguments.  A "tile" is RT consecutive rows restricted to the
 // column slice [col0, col0 + NS) that one CTA of a cluster owns (the whole
@@ -53,8 +56,8 @@ struct SmemLayout {
   uint32_t stats_off;     // backward: [S][RT][2] floats (rstd, mean)
   uint32_t red_off;       // [2][G][W][4] floats, cross-warp group partials
                           // (W = tpr / 32; only when tpr > 32)
-  uint32_t xch_off;       // clusters only: [2][RT][C][4] floats of cross-CTA
-                          // partials, then 2 mbarriers (one per buffer)
+  uint32_t xch_off;       // clusters only: [kXchBuffers][RT][C][4] floats of
+                          // cross-CTA partials, then one mbarrier per buffer
   uint32_t bar_off;       // [S] mbarriers
   uint32_t flag_off;      // abort flag (int), then [S] ints: warps done per stage
   uint32_t total;
@@ -81,7 +84,8 @@ __host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
   L.red_off = off;
   if (tpr > 32) off = align16(off + static_cast<uint32_t>(2 * G * (tpr / 32) * 4) * 4u);
   L.xch_off = off;
-  if (C > 1) off = align16(off + static_cast<uint32_t>(2 * RT * C * 4) * 4u + 16u);
+  if (C > 1) off = align16(off + static_cast<uint32_t>(kXchBuffers * RT * C * 4) * 4u +
+                           8u * kXchBuffers);
   L.bar_off = off;
   off = align16(off + static_cast<uint32_t>(S) * 8u);
   L.flag_off = off;
@@ -98,6 +102,7 @@ struct Plan {
   int tpr = 0;     // threads per row
   int K = 0;       // chunks per thread
   bool exact = false; // slices divide evenly into K chunks x tpr threads, tpr >= 32
+  bool long_rows = false; // long-row kernels (row re-read from the stage)
   int G = 0;       // groups per CTA
   int rpg = 1;     // rows per group per tile
   int RT = 0;      // rows per tile
@@ -114,6 +119,8 @@ struct Plan {
 const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
 const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
 const void *reduce_kernel_ptr();
+// Long-row kernels (row slice re-read from shared memory; K in {4, 8}).
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd);
 int reduce_threads();
 
 }  // namespace gbn

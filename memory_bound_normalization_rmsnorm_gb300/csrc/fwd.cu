@@ -24,32 +24,11 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
+#include "tiles.cuh"
 
 namespace gbn {
 
 namespace {
-
-template <bool CLUSTER>
-__device__ __forceinline__ void issue_fwd_tile(const NormArgs &a, const SmemLayout &L,
-                                               unsigned char *smem, int64_t tile, int s,
-                                               int col0, int nsc_me, uint64_t pol) {
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
-  unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
-  const int64_t row0 = tile * a.RT;
-  const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-  if (!CLUSTER) {
-    const uint32_t bytes = static_cast<uint32_t>(nrows) * a.N * 2u;
-    mbar_arrive_expect_tx(full, bytes);
-    bulk_g2s(dst, a.x + row0 * a.N, bytes, full, pol);
-  } else {
-    // Row r of the tile lands at r * NS * 2 (slice stride), nsc_me chunks.
-    const uint32_t bytes = static_cast<uint32_t>(nsc_me) * 16u;
-    const uint32_t stride = static_cast<uint32_t>(a.NS) * 2u;
-    mbar_arrive_expect_tx(full, bytes * nrows);
-    for (int r = 0; r < nrows; ++r)
-      bulk_g2s(dst + r * stride, a.x + (row0 + r) * a.N + col0, bytes, full, pol);
-  }
-}
 
 // EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
 // chunk needs an ownership test and the warp butterfly is full width.
@@ -79,10 +58,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
       done_cnt[s] = 0;
     }
     if (CLUSTER) {
-      uint64_t *xb = reinterpret_cast<uint64_t *>(smem + L.xch_off +
-                                                  static_cast<uint32_t>(2 * a.RT * a.C * 4) * 4u);
-      mbar_init(xb, 1);
-      mbar_init(xb + 1, 1);
+      uint64_t *xb = xch_bars(smem, L, a.RT, a.C);
+      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();

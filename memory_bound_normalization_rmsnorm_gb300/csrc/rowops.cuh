@@ -132,51 +132,56 @@ __device__ __forceinline__ void group_meanvar(float &m, float &q, float n_t, int
   }
 }
 
-// Cross-CTA exchange state of a cluster kernel.  Buffer b (two of them,
-// used alternately by successive rounds) holds [RT][C] float4 slots and has
-// one mbarrier; `phase` bit b is the parity of buffer b's current round.
+// Cross-CTA exchange state of a cluster kernel.  kXchBuffers buffers, used by
+// successive rounds in turn, each holding [RT][C] float4 slots and one
+// mbarrier; bit b of `phase` is the parity of buffer b's current round.
 struct ClusterXch {
-  float *slots;    // [2][RT][C][4]
-  uint64_t *bars;  // [2]
+  float *slots;    // [kXchBuffers][RT][C][4]
+  uint64_t *bars;  // [kXchBuffers]
   int RT;
   int C;
   int crank;
-  int buf;
+  int push_buf;    // buffer of the next round to push
+  int wait_buf;    // buffer of the oldest round not yet consumed
   uint32_t phase;
 };
+
+__device__ __forceinline__ uint64_t *xch_bars(unsigned char *smem, const SmemLayout &L, int RT,
+                                              int C) {
+  return reinterpret_cast<uint64_t *>(smem + L.xch_off +
+                                      static_cast<uint32_t>(kXchBuffers * RT * C * 4) * 4u);
+}
 
 __device__ __forceinline__ ClusterXch make_xch(unsigned char *smem, const SmemLayout &L,
                                                int RT, int C, int crank) {
   ClusterXch x;
   x.slots = reinterpret_cast<float *>(smem + L.xch_off);
-  x.bars = reinterpret_cast<uint64_t *>(smem + L.xch_off + static_cast<uint32_t>(2 * RT * C * 4) * 4u);
+  x.bars = xch_bars(smem, L, RT, C);
   x.RT = RT;
   x.C = C;
   x.crank = crank;
-  x.buf = 0;
+  x.push_buf = 0;
+  x.wait_buf = 0;
   x.phase = 0;
   return x;
 }
 
 // Cross-CTA reductions for row slot `r` of the tile, in CTA-rank order, so
-// every CTA gets the same bits.  One round: thread 0 of the CTA posts the bytes the round expects (RT rows x C ranks
-// x 16 bytes) on the local buffer mbarrier; thread t == 0 of every row
-// group pushes its group total into slot [r][crank] of EVERY CTA of the
-// cluster (itself included) with asynchronous stores that complete on the
-// receiver's mbarrier; every thread then waits for the local mbarrier and
-// folds the C slots of its row.  No cluster barrier and no memory fence:
-// nothing orders the threads' global stores.  Every thread of the CTA must
-// make the same sequence of calls.  Two buffers suffice: a CTA can only send
-// round k+2 after receiving every CTA's round k+1, which each sends only
-// after all of its groups finished reading round k.
-//
-// One exchange round: pushes (a, b, c) of row slot r to every CTA of the
-// cluster and returns this CTA's local view of the row's C slots, in rank
-// order, once all have arrived.
-__device__ __forceinline__ const float *cluster_exchange(float a, float b, float c, int r,
-                                                         int t, ClusterXch &x, unsigned *err,
-                                                         volatile int *abort) {
-  const int bsel = x.buf;
+// every CTA gets the same bits.  A round: thread 0 of the CTA posts the bytes
+// the round expects (RT rows x C ranks x 16 bytes) on the round's local
+// mbarrier; thread t == 0 of every row group pushes its group partial into
+// slot [r][crank] of EVERY CTA of the cluster (itself included) with
+// asynchronous stores that complete on the receiver's mbarrier; every thread
+// later waits on the local mbarrier and folds the C slots of its row.  No
+// cluster barrier and no memory fence: nothing orders the threads' global
+// stores.  Every thread of the CTA makes the same sequence of push and wait
+// calls, and a CTA pushes round k+1 at the earliest before it waits for
+// round k.  Then four buffers suffice: a CTA pushes round k+1 only after its
+// wait for round k-1 has seen every CTA's round k-1 push, and each CTA folds
+// round k-3 (same buffer as k+1) before it pushes round k-1.
+__device__ __forceinline__ void cluster_push(float a, float b, float c, int r, int t,
+                                             ClusterXch &x) {
+  const int bsel = x.push_buf;
   float *base = x.slots + static_cast<size_t>(bsel) * x.RT * x.C * 4;
   uint64_t *bar = x.bars + bsel;
   if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(x.RT * x.C * 16));
@@ -186,10 +191,36 @@ __device__ __forceinline__ const float *cluster_exchange(float a, float b, float
     for (int q = 0; q < x.C; ++q)
       st_async_f32x4(mapa_shared(mine, q), val, mapa_shared(bar, q));
   }
-  mbar_wait(bar, (x.phase >> bsel) & 1u, err, abort);
+  x.push_buf = (bsel + 1) % kXchBuffers;
+}
+
+// Waits for the oldest pushed round; returns this CTA's view of row r's C
+// slots (rank order).
+__device__ __forceinline__ const float *cluster_wait_row(int r, ClusterXch &x, unsigned *err,
+                                                         volatile int *abort) {
+  const int bsel = x.wait_buf;
+  mbar_wait(x.bars + bsel, (x.phase >> bsel) & 1u, err, abort);
   x.phase ^= 1u << bsel;
-  x.buf ^= 1;
-  return base + static_cast<size_t>(r) * x.C * 4;
+  x.wait_buf = (bsel + 1) % kXchBuffers;
+  return x.slots + (static_cast<size_t>(bsel) * x.RT + r) * x.C * 4;
+}
+
+__device__ __forceinline__ const float *cluster_exchange(float a, float b, float c, int r,
+                                                         int t, ClusterXch &x, unsigned *err,
+                                                         volatile int *abort) {
+  cluster_push(a, b, c, r, t, x);
+  return cluster_wait_row(r, x, err, abort);
+}
+
+// Rank-order sums of the first NV floats of the C slots of a row.
+template <int NV>
+__device__ __forceinline__ void fold_sum(const float *row, int C, float (&v)[NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float acc = row[i];
+    for (int q = 1; q < C; ++q) acc += row[q * 4 + i];
+    v[i] = acc;
+  }
 }
 
 // Sum of NV <= 3 values over the C CTAs, added in rank order.
@@ -198,12 +229,7 @@ __device__ __forceinline__ void cluster_sum(float (&v)[NV], int r, int t, Cluste
                                             unsigned *err, volatile int *abort) {
   const float *row = cluster_exchange(v[0], NV > 1 ? v[NV > 1 ? 1 : 0] : 0.f,
                                       NV > 2 ? v[NV > 2 ? 2 : 0] : 0.f, r, t, x, err, abort);
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    float acc = row[i];
-    for (int q = 1; q < x.C; ++q) acc += row[q * 4 + i];
-    v[i] = acc;
-  }
+  fold_sum<NV>(row, x.C, v);
 }
 
 // (mean, M2) over the C CTAs, each partial covering n_cta elements, merged
@@ -218,6 +244,75 @@ __device__ __forceinline__ void cluster_meanvar(float &m, float &q, float n_cta,
     const float wb = 1.0f / static_cast<float>(k + 1);
     ms_merge(m, q, row[k * 4 + 0], row[k * 4 + 1], wb, n_cta * static_cast<float>(k) * wb);
   }
+}
+
+// ------------------------------------ (count, mean, M2) of any counts
+// Chan's pairwise merge of (n, mean, M2) partials; `lo` is the partial of
+// the lower-indexed participant so that both partners of a butterfly
+// exchange compute the same bits.  Empty partials (n = 0) are neutral.
+__device__ __forceinline__ void nms_merge(float &n, float &m, float &q, float n2, float m2,
+                                          float q2) {
+  if (n2 == 0.f) return;
+  if (n == 0.f) {
+    n = n2;
+    m = m2;
+    q = q2;
+    return;
+  }
+  const float nt = n + n2;
+  const float wb = n2 / nt;
+  const float d = m2 - m;
+  q = (q + q2) + d * d * (n * wb);
+  m = fmaf(d, wb, m);
+  n = nt;
+}
+
+// (n, mean, M2) over the tpr threads of a row group (any tpr, any counts).
+__device__ __forceinline__ void group_nmeanvar(float &n, float &m, float &q, int tpr, int g,
+                                               int G, int t, float *red, int &rpar) {
+  const int lane = threadIdx.x & 31;
+  const int width = tpr < 32 ? tpr : 32;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    if (o < width) {
+      const float no = __shfl_xor_sync(0xffffffffu, n, o);
+      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+      const float qo = __shfl_xor_sync(0xffffffffu, q, o);
+      if (lane & o) {  // the partner is the lower participant
+        float n0 = no, m0 = mo, q0 = qo;
+        nms_merge(n0, m0, q0, n, m, q);
+        n = n0;
+        m = m0;
+        q = q0;
+      } else {
+        nms_merge(n, m, q, no, mo, qo);
+      }
+    }
+  }
+  if (tpr > 32) {
+    const int W = tpr >> 5;
+    float *slot = red + (static_cast<size_t>(rpar * G + g) * W) * 4;
+    if (lane == 0) {
+      slot[(t >> 5) * 4 + 0] = n;
+      slot[(t >> 5) * 4 + 1] = m;
+      slot[(t >> 5) * 4 + 2] = q;
+    }
+    named_bar_sync(1 + g, tpr);
+    n = slot[0];
+    m = slot[1];
+    q = slot[2];
+    for (int w = 1; w < W; ++w) nms_merge(n, m, q, slot[w * 4 + 0], slot[w * 4 + 1], slot[w * 4 + 2]);
+    rpar ^= 1;
+  }
+}
+
+// Rank-order (n, mean, M2) merge of a row's C slots.
+__device__ __forceinline__ void fold_nmeanvar(const float *row, int C, float &n, float &m,
+                                              float &q) {
+  m = row[0];
+  q = row[1];
+  n = row[2];
+  for (int k = 1; k < C; ++k) nms_merge(n, m, q, row[k * 4 + 2], row[k * 4 + 0], row[k * 4 + 1]);
 }
 
 // ---------------------------------------------------- ring hand-off

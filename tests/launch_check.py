@@ -9,6 +9,7 @@ reaches the GPU; uses only the plan the library reports (norm_plan).
 from __future__ import annotations
 
 MAX_THREADS = 512
+XCH_BUFFERS = 4
 TX_LIMIT = 1 << 20
 
 
@@ -29,7 +30,7 @@ def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C):
         off = _align16(off + 2 * G * (tpr // 32) * 4 * 4)
     L["xch"] = off
     if C > 1:
-        off = _align16(off + 2 * RT * C * 4 * 4 + 16)
+        off = _align16(off + XCH_BUFFERS * RT * C * 4 * 4 + 8 * XCH_BUFFERS)
     L["bar"] = off
     off = _align16(off + S * 8)
     L["flag"] = off
@@ -112,10 +113,11 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
         hi = ((1 * G + (G - 1)) * W + (W - 1)) * 4 + 4
         assert L["red"] + hi * 4 <= L["xch"]
     if C > 1:
-        # slot [buf][r][q] float4 for buf < 2, r < RT, q < C; then 2 mbarriers
-        hi = ((1 * RT + (RT - 1)) * C + (C - 1)) * 4 + 4
-        bars = L["xch"] + 2 * RT * C * 16
-        assert L["xch"] + hi * 4 <= bars and bars % 8 == 0 and bars + 16 <= L["bar"]
+        # slot [buf][r][q] float4 for buf < 4, r < RT, q < C; then 4 mbarriers
+        hi = (((XCH_BUFFERS - 1) * RT + (RT - 1)) * C + (C - 1)) * 4 + 4
+        bars = L["xch"] + XCH_BUFFERS * RT * C * 16
+        assert L["xch"] + hi * 4 <= bars and bars % 8 == 0
+        assert bars + 8 * XCH_BUFFERS <= L["bar"]
     return True
 
 
