@@ -104,7 +104,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Optional plan override for tuning sweeps: GBNORM_PLAN="C=2,tpr=256,rpg=1,S=4"
 // (any subset).  Fields left out keep the heuristic's choice.
 struct Override {
-  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0;
+  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, occ = 0;
   bool any = false;
 };
 
@@ -126,6 +126,7 @@ Override read_override() {
     else if (!std::strcmp(key, "ctas")) o.ctas = val;
     else if (!std::strcmp(key, "long")) o.lng = val;
     else if (!std::strcmp(key, "K")) o.K = val;
+    else if (!std::strcmp(key, "occ")) o.occ = val;
     o.any = true;
   }
   return o;
@@ -135,6 +136,26 @@ int round_k(int K, bool bwd) {
   if (bwd) return K;  // 1..4 all compiled
   return K == 7 ? 8 : K;
 }
+
+// Offline-tuned plans for row lengths measured on GB300 (a search over
+// threads per row, rows per group and stages, keeping changes that beat the
+// heuristic by more than ~5 %).  Like any plan they fix the reduction order,
+// so results stay bitwise reproducible; shapes not listed use the heuristic.
+struct TunedPlan {
+  int mode;  // kRMS / kLayer
+  int bwd;   // 0 forward, 1 backward
+  int N;
+  int tpr, rpg, S;  // 0 = heuristic's choice
+};
+constexpr TunedPlan kTuned[] = {
+    {kRMS, 0, 256, 32, 2, 3},     {kRMS, 0, 512, 32, 1, 3},    {kRMS, 0, 768, 32, 0, 3},
+    {kRMS, 0, 1024, 64, 1, 0},    {kRMS, 0, 2048, 128, 1, 0},  {kRMS, 0, 3072, 192, 1, 3},
+    {kRMS, 0, 5120, 160, 0, 3},   {kRMS, 0, 8192, 256, 0, 3},  {kRMS, 0, 16384, 512, 0, 3},
+    {kLayer, 0, 2048, 64, 0, 3},
+    {kRMS, 1, 256, 32, 2, 5},     {kRMS, 1, 512, 64, 0, 0},    {kRMS, 1, 768, 64, 4, 0},
+    {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 5120, 256, 2, 0},
+    {kLayer, 1, 3072, 192, 4, 0}, {kLayer, 1, 5120, 256, 2, 0},
+};
 
 // Ring and tile sizing shared by both plan kinds: rows per tile and the
 // number of stages that fit in shared memory (at least two).
@@ -147,7 +168,8 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
   if (C == 1) rpg = std::max(1, (32 * 1024) / (row_bytes * G));
   if (ov.rpg) rpg = ov.rpg;
   if (rpg < 1 || (C > 1 && rpg != 1)) return NORM_ERR_UNSUPPORTED;
-  const int budget = smem_optin - 1024;
+  // Two CTAs per SM share the SM's shared memory (opt-in limit + 1 KB).
+  const int budget = (p.occ == 2) ? (smem_optin + 1024) / 2 - 1024 : smem_optin - 1024;
   int S = 0;
   for (;;) {
     const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C);
@@ -186,10 +208,11 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
   const int nc = N / 8;
   Plan p;
   p.long_rows = true;
+  p.occ = ov.occ ? ov.occ : 1;
   // 8 chunks per thread only where that fits in registers without spilling
   // (RMSNorm forward); 4 elsewhere.
   int K = ov.K ? ov.K : ((!bwd && mode == kRMS) ? 8 : 4);
-  if (K != 4 && K != 8) return NORM_ERR_UNSUPPORTED;
+  if (K != 2 && K != 4 && K != 8) return NORM_ERR_UNSUPPORTED;
   // Slices up to kMaxThreads threads x K chunks per CTA; clusters when the
   // row is wider.  Without a cluster, up to two row groups per CTA overlap
   // each other's reductions; in a cluster one group of up to kMaxThreads
@@ -214,7 +237,7 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
   if (C > 1 && p.G != 1) return NORM_ERR_UNSUPPORTED;  // one row per CTA per tile
   norm_status_t st = size_ring(p, bwd, smem_optin, ov, M);
   if (st != NORM_OK) return st;
-  if (!long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd)) return NORM_ERR_UNSUPPORTED;
+  if (!long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ)) return NORM_ERR_UNSUPPORTED;
   *out = p;
   return NORM_OK;
 }
@@ -223,7 +246,18 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
 // Pure host arithmetic (no CUDA call).  `bwd` selects the backward kernel
 // (two tensors per stage, at most kMaxKBwd chunks per thread).
 norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
-                         const Override &ov, Plan *out) {
+                         const Override &ov_in, Plan *out) {
+  Override ov = ov_in;
+  if (!ov.any) {
+    for (const TunedPlan &tp : kTuned) {
+      if (tp.mode == mode && tp.bwd == (bwd ? 1 : 0) && tp.N == N) {
+        ov.tpr = tp.tpr;
+        ov.rpg = tp.rpg;
+        ov.S = tp.S;
+        break;
+      }
+    }
+  }
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
   const int nc = N / 8;
   Plan p;
@@ -306,7 +340,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 }
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
-  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd);
+  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact);
 }
@@ -382,8 +416,13 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
 
 norm_status_t launch(const void *fn, const Plan &p, const NormArgs &args, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int na = 0;
+  // Every kernel waits (griddepcontrol.wait) before its first global access,
+  // so it may be launched while the previous kernel of the stream drains.
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   if (p.C > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = p.C;
@@ -538,6 +577,11 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   cfg.gridDim = dim3((n + 127) / 128, nparts);
   cfg.blockDim = dim3(reduce_threads());
   cfg.stream = s;
+  cudaLaunchAttribute rattr;
+  rattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  rattr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &rattr;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelExC(&cfg, rfn, rargs) != cudaSuccess) {
     cudaGetLastError();
     return NORM_ERR_CUDA;
@@ -557,7 +601,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
     if ((st = shape_plan(mode, bwd, M, static_cast<int>(N), smem_optin_bytes, read_override(),
                          &p)) != NORM_OK)
       return st;
-    set_grid(p, sm_count / p.C);
+    set_grid(p, static_cast<int64_t>(sm_count) * p.occ / p.C);
     if (p.grid < 1) return NORM_ERR_UNSUPPORTED;
   } else {
     DeviceInfo d;

@@ -56,6 +56,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Programmatic dependent launch: let the next kernel in the stream start
+  // its prologue as our CTAs retire, and touch no global memory before the
+  // previous kernel's writes are complete and visible.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   // gamma (fp32 pairs) and the column accumulators of this thread's chunks
   // live in registers for the whole kernel.
@@ -199,6 +204,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
     const float *__restrict__ ws, int P, int N, float *__restrict__ dgamma,
     float *__restrict__ dbeta) {
   __shared__ float4 part[kReduceWarps][32];
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   const float *src = ws + static_cast<size_t>(blockIdx.y) * P * N;

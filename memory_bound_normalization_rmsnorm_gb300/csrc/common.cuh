@@ -103,6 +103,7 @@ struct Plan {
   int K = 0;       // chunks per thread
   bool exact = false; // slices divide evenly into K chunks x tpr threads, tpr >= 32
   bool long_rows = false; // long-row kernels (row re-read from the stage)
+  int occ = 1;            // CTAs per SM the kernel is compiled for
   int G = 0;       // groups per CTA
   int rpg = 1;     // rows per group per tile
   int RT = 0;      // rows per tile
@@ -119,8 +120,10 @@ struct Plan {
 const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
 const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
 const void *reduce_kernel_ptr();
-// Long-row kernels (row slice re-read from shared memory; K in {4, 8}).
-const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd);
+// Long-row kernels (row slice re-read from shared memory), K in {4, 8}.
+// occ = CTAs per SM the kernel is compiled for (only 1 is built: a
+// two-CTA-per-SM variant capped at 64 registers measured 40 % slower).
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ);
 int reduce_threads();
 
 }  // namespace gbn

@@ -64,6 +64,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Programmatic dependent launch: let the next kernel in the stream start
+  // its prologue as our CTAs retire, and touch no global memory before the
+  // previous kernel's writes are complete and visible.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   // gamma as fp32 pairs (and beta packed) for this thread's chunks stay in
   // registers for the whole kernel: the thread owns the same columns in

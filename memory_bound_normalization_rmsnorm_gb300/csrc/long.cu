@@ -39,8 +39,9 @@ struct Pending {
   float a, b, c;  // this row group's partial (also the total without a cluster)
 };
 
-template <int MODE, int K, bool CLUSTER, bool EXACT>
-__global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const NormArgs a) {
+// OCC: CTAs per SM the kernel is compiled for (2 caps registers at 64).
+template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC>
+__global__ void __launch_bounds__(kMaxThreads, OCC) norm_fwd_long_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -70,6 +71,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Programmatic dependent launch: let the next kernel in the stream start
+  // its prologue as our CTAs retire, and touch no global memory before the
+  // previous kernel's writes are complete and visible.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   // Per-column state: gamma and beta of this thread's chunks, packed bf16.
   uint4 gv[K], bv[K];
@@ -274,8 +280,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
   }
 }
 
-template <int MODE, int K, bool CLUSTER, bool EXACT>
-__global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const NormArgs a) {
+template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC>
+__global__ void __launch_bounds__(kMaxThreads, OCC) norm_bwd_long_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -305,6 +311,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Programmatic dependent launch: let the next kernel in the stream start
+  // its prologue as our CTAs retire, and touch no global memory before the
+  // previous kernel's writes are complete and visible.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   // Per-column state: gamma (packed bf16) and the fp32 column accumulators.
   uint4 gv[K];
@@ -482,31 +493,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
   if (CLUSTER) cluster_sync();
 }
 
-template <int MODE, int K, bool CLUSTER>
+template <int MODE, int K, bool CLUSTER, int OCC>
 const void *pick_long(bool bwd, bool e) {
   if (bwd)
-    return e ? reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, true>)
-             : reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, false>);
-  return e ? reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, true>)
-           : reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, false>);
+    return e ? reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, true, OCC>)
+             : reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, false, OCC>);
+  return e ? reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, true, OCC>)
+           : reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, false, OCC>);
 }
 
 template <int MODE, bool CLUSTER>
-const void *pick_long_k(int K, bool bwd, bool e) {
+const void *pick_long_k(int K, bool bwd, bool e, int occ) {
+  if (occ != 1) return nullptr;
   switch (K) {
-    case 4: return pick_long<MODE, 4, CLUSTER>(bwd, e);
-    case 8: return pick_long<MODE, 8, CLUSTER>(bwd, e);
+    case 4: return pick_long<MODE, 4, CLUSTER, 1>(bwd, e);
+    case 8: return pick_long<MODE, 8, CLUSTER, 1>(bwd, e);
     default: return nullptr;
   }
 }
 
 }  // namespace
 
-const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd) {
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ) {
   if (mode == kRMS)
-    return cluster ? pick_long_k<kRMS, true>(K, bwd, exact) : pick_long_k<kRMS, false>(K, bwd, exact);
-  return cluster ? pick_long_k<kLayer, true>(K, bwd, exact)
-                 : pick_long_k<kLayer, false>(K, bwd, exact);
+    return cluster ? pick_long_k<kRMS, true>(K, bwd, exact, occ)
+                   : pick_long_k<kRMS, false>(K, bwd, exact, occ);
+  return cluster ? pick_long_k<kLayer, true>(K, bwd, exact, occ)
+                 : pick_long_k<kLayer, false>(K, bwd, exact, occ);
 }
 
 }  // namespace gbn

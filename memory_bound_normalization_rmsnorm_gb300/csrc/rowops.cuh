@@ -99,6 +99,25 @@ __device__ __forceinline__ void ms_merge(float &m, float &q, float mo, float qo,
   m = fmaf(d, wb, m);
 }
 
+// Pairwise tree over W (mean, M2) partials of nw elements each, stored as
+// float2 at stride 4 floats: ((0,1),(2,3)),... in a fixed order.
+template <int W>
+__device__ __forceinline__ void tree_fold(const float *slot, float nw, float &m, float &q) {
+  float2 v[W];
+#pragma unroll
+  for (int w = 0; w < W; ++w) v[w] = *reinterpret_cast<const float2 *>(slot + w * 4);
+  float h = 0.5f * nw;
+#pragma unroll
+  for (int span = 1; span < W; span <<= 1) {
+#pragma unroll
+    for (int w = 0; w + span < W; w += 2 * span)
+      ms_merge_equal(v[w].x, v[w].y, v[w + span].x, v[w + span].y, h);
+    h *= 2.f;
+  }
+  m = v[0].x;
+  q = v[0].y;
+}
+
 // (mean, M2) over the tpr >= 32 threads of a row group, every thread
 // holding a partial over n_t elements.  Butterfly of equal-count merges,
 // then for tpr > 32 a fold of the per-warp partials in warp order (warp w's
@@ -116,17 +135,33 @@ __device__ __forceinline__ void group_meanvar(float &m, float &q, float n_t, int
   if (tpr > 32) {
     const int W = tpr >> 5;
     float *slot = red + (static_cast<size_t>(rpar * G + g) * W) * 4;
-    if ((threadIdx.x & 31) == 0) {
-      slot[(t >> 5) * 4 + 0] = m;
-      slot[(t >> 5) * 4 + 1] = q;
-    }
+    if ((threadIdx.x & 31) == 0)
+      *reinterpret_cast<float2 *>(slot + (t >> 5) * 4) = make_float2(m, q);
     named_bar_sync(1 + g, tpr);
     const float nw = 32.f * n_t;  // elements per warp
-    m = slot[0];
-    q = slot[1];
-    for (int w = 1; w < W; ++w) {
-      const float wb = 1.0f / static_cast<float>(w + 1);
-      ms_merge(m, q, slot[w * 4 + 0], slot[w * 4 + 1], wb, nw * static_cast<float>(w) * wb);
+    if (W == 2 || W == 4 || W == 8 || W == 16) {
+      // Power-of-two warp count: pairwise tree of equal-count merges in a
+      // fixed order, no division.
+      switch (W) {
+        case 2: tree_fold<2>(slot, nw, m, q); break;
+        case 4: tree_fold<4>(slot, nw, m, q); break;
+        case 8: tree_fold<8>(slot, nw, m, q); break;
+        default: tree_fold<16>(slot, nw, m, q); break;
+      }
+    } else {
+      // Running partial over w warps merged with warp w, in warp order
+      // (unrolled, so 1 / (w + 1) is a compile-time constant).
+      float2 f = *reinterpret_cast<const float2 *>(slot);
+      m = f.x;
+      q = f.y;
+#pragma unroll
+      for (int w = 1; w < 16; ++w) {
+        if (w < W) {
+          f = *reinterpret_cast<const float2 *>(slot + w * 4);
+          const float wb = 1.0f / static_cast<float>(w + 1);
+          ms_merge(m, q, f.x, f.y, wb, nw * static_cast<float>(w) * wb);
+        }
+      }
     }
     rpar ^= 1;
   }
@@ -240,9 +275,12 @@ __device__ __forceinline__ void cluster_meanvar(float &m, float &q, float n_cta,
   const float *row = cluster_exchange(m, q, 0.f, r, t, x, err, abort);
   m = row[0];
   q = row[1];
-  for (int k = 1; k < x.C; ++k) {
-    const float wb = 1.0f / static_cast<float>(k + 1);
-    ms_merge(m, q, row[k * 4 + 0], row[k * 4 + 1], wb, n_cta * static_cast<float>(k) * wb);
+#pragma unroll
+  for (int k = 1; k < 16; ++k) {
+    if (k < x.C) {
+      const float wb = 1.0f / static_cast<float>(k + 1);
+      ms_merge(m, q, row[k * 4 + 0], row[k * 4 + 1], wb, n_cta * static_cast<float>(k) * wb);
+    }
   }
 }
 
