@@ -199,6 +199,18 @@ norm_status_t norm_bwd_noalloc(const void *dy, const void *x, const void *gamma,
                                void *dx, float *dgamma, float *dbeta,
                                norm_stream_t stream);
 
+/*
+ * norm_selftest_wait_timeout -- exercises the failure path of the kernels'
+ * bounded waits.  Launches one CTA whose thread waits, with the same
+ * give-up logic as every wait in the library, on an mbarrier phase that
+ * nothing completes, polling at most `polls` times (1 <= polls <= 2^20).
+ * The wait gives up, the kernel records the timeout in the device error word
+ * and returns normally, so the context stays usable.  A following
+ * norm_get_device_error returns NORM_ERR_DEVICE_TIMEOUT (and clears it).
+ * Asynchronous on `stream`; returns argument or launch errors.
+ */
+norm_status_t norm_selftest_wait_timeout(uint32_t polls, norm_stream_t stream);
+
 /* Static, human-readable description of a status code. */
 const char *norm_strerror(norm_status_t status);
 

@@ -88,6 +88,8 @@ def lib():
             L.norm_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int,
                                            _vp, _vp, _vp, _vp]
             L.norm_bwd_noalloc.restype = ctypes.c_int
+            L.norm_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _vp]
+            L.norm_selftest_wait_timeout.restype = ctypes.c_int
             L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(Plan)]
             L.norm_plan.restype = ctypes.c_int

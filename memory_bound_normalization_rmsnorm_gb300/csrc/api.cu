@@ -659,6 +659,25 @@ norm_status_t norm_bwd_noalloc(const void *dy, const void *x, const void *gamma,
                   NORM_NOALLOC_WORKSPACE_BYTES, stream);
 }
 
+norm_status_t norm_selftest_wait_timeout(uint32_t polls, norm_stream_t stream) {
+  if (polls < 1 || polls > (1u << 20)) return NORM_ERR_ARG;
+  DeviceInfo d;
+  int dev = 0;
+  norm_status_t st = device_info(&d, &dev);
+  if (st != NORM_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  unsigned *err = d.err;
+  void *args[] = {&err, &polls};
+  if (cudaLaunchKernelExC(&cfg, selftest_kernel_ptr(), args) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return NORM_OK;
+}
+
 const char *norm_strerror(norm_status_t s) {
   switch (s) {
     case NORM_OK: return "success";

@@ -193,6 +193,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   if (CLUSTER) cluster_sync();
 }
 
+// Self-test of the bounded-wait failure path: waits on phase 0 of an
+// mbarrier that expects one arrival which never comes.
+__global__ void selftest_wait_kernel(unsigned *err, uint32_t polls) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, err, &abort_flag, polls);
+}
+
 constexpr int kReduceWarps = 16;
 
 // dgamma[j] = sum over p of ws[p][j] (blockIdx.y = 0) and dbeta[j] = sum
@@ -272,5 +286,9 @@ const void *reduce_kernel_ptr() {
 }
 
 int reduce_threads() { return kReduceWarps * 32; }
+
+const void *selftest_kernel_ptr() {
+  return reinterpret_cast<const void *>(&selftest_wait_kernel);
+}
 
 }  // namespace gbn

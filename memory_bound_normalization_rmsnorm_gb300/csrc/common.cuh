@@ -125,5 +125,6 @@ const void *reduce_kernel_ptr();
 // two-CTA-per-SM variant capped at 64 registers measured 40 % slower).
 const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ);
 int reduce_threads();
+const void *selftest_kernel_ptr();
 
 }  // namespace gbn

@@ -54,16 +54,17 @@ constexpr unsigned kErrWaitTimeout = 1u;
 // wait to seconds, never forever.
 constexpr uint32_t kMaxPolls = 1u << 22;
 
-// Waits for phase `parity` of `bar`.  Gives up after kMaxPolls polls (or at
+// Waits for phase `parity` of `bar`.  Gives up after max_polls polls (or at
 // once when another thread of the CTA already gave up, signalled through
 // *abort), records the failure in *err and returns false.  The caller then
 // carries on with whatever the stage holds: every address it touches stays
 // in bounds, so a lost copy yields a wrong result and an error code, never
 // a fault or a hang.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          unsigned *err, volatile int *abort) {
+                                          unsigned *err, volatile int *abort,
+                                          uint32_t max_polls = kMaxPolls) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+  for (uint32_t i = 0; i < max_polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort) return false;
   }

@@ -13,7 +13,8 @@ import memory_bound_normalization_rmsnorm_gb300 as gb
 def test_exports_every_declared_symbol():
     names = gb.declared_functions()
     assert set(names) >= {"norm_fwd", "norm_bwd", "norm_bwd_workspace_bytes",
-                          "norm_strerror", "norm_get_device_error", "norm_plan"}
+                          "norm_strerror", "norm_get_device_error", "norm_plan",
+                          "norm_bwd_noalloc", "norm_selftest_wait_timeout"}
     L = ctypes.CDLL(gb.library_path())
     for n in names:
         assert hasattr(L, n), f"{n} declared in gbnorm.h but not exported"
@@ -84,6 +85,12 @@ def test_bwd_validation_codes():
     assert call(ws=None) == 5
     assert call(ws=F + 4) == 3
     assert call(dx=F + 2) == 3
+
+
+def test_selftest_argument_checks():
+    L = gb.lib()
+    assert L.norm_selftest_wait_timeout(0, None) == 9
+    assert L.norm_selftest_wait_timeout((1 << 20) + 1, None) == 9
 
 
 def test_plan_is_pure_host_arithmetic():

@@ -121,3 +121,20 @@ def test_plan_query_matches_device():
         for bwd in (False, True):
             p = gb.norm_plan(M, N, mode, bwd)
             assert 1 <= p["grid"] <= 4 * sms and p["grid"] % p["cluster"] == 0
+
+
+def test_bounded_wait_failure_path():
+    """A wait that nothing completes gives up after its poll limit, records
+    the timeout in the device error word and lets the kernel return: the
+    status is reported once, then cleared, and the context keeps working."""
+    L = lib()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert gb.norm_get_device_error() == 0
+    assert L.norm_selftest_wait_timeout(1000, s) == 0
+    assert gb.norm_get_device_error() == 8  # NORM_ERR_DEVICE_TIMEOUT
+    assert gb.norm_get_device_error() == 0  # cleared by the read
+    x, g, b, dy = _inputs(64, 1024, 1)
+    y, r, m = gb.norm_fwd(x, g, b, 1e-5, 1)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
+    assert gb.norm_get_device_error() == 0
