@@ -101,8 +101,14 @@ class Oracle:
         lib.oracle_param_grads_bf16.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64,
                                                 ctypes.c_int64, ctypes.c_double,
                                                 ctypes.c_int, _dp, _dp, _dp, _dp]
+        lib.oracle_residual_add_bf16.argtypes = [_u16p, _u16p, ctypes.c_int64,
+                                                 ctypes.c_int64, _u16p]
+        lib.oracle_add_bwd_dx_bf16.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                               _i64p, ctypes.c_int64, _dp]
         for f in (lib.oracle_fwd_f64, lib.oracle_bwd_f64, lib.oracle_fwd_bf16,
-                  lib.oracle_bwd_dx_bf16, lib.oracle_param_grads_bf16):
+                  lib.oracle_bwd_dx_bf16, lib.oracle_param_grads_bf16,
+                  lib.oracle_residual_add_bf16, lib.oracle_add_bwd_dx_bf16):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -185,6 +191,41 @@ class Oracle:
         return tuple(out)
 
 
+    # ------------------------------------------------ fused residual add
+    def residual_add_bf16(self, x_bits, r_bits):
+        """h = bf16(x + r) (sum in binary32, round to nearest even), bits."""
+        x_bits = _u16(x_bits)
+        r_bits = _u16(r_bits)
+        assert x_bits.shape == r_bits.shape
+        M, N = x_bits.shape
+        h = np.empty((M, N), np.uint16)
+        _check(self.lib.oracle_residual_add_bf16(_ptr(x_bits, _u16p), _ptr(r_bits, _u16p),
+                                                 M, N, _ptr(h, _u16p)),
+               "oracle_residual_add_bf16")
+        return h
+
+    def add_fwd_bf16(self, x_bits, r_bits, gamma_bits, beta_bits, eps, mode, rows=None):
+        """Fused residual add + norm forward: (h bits, y, rstd, mean)."""
+        h = self.residual_add_bf16(x_bits, r_bits)
+        y, rstd, mean = self.fwd_bf16(h, gamma_bits, beta_bits, eps, mode, rows=rows)
+        return h, y, rstd, mean
+
+    def add_bwd_dx_bf16(self, dy_bits, h_bits, dh_bits, gamma_bits, eps, mode, rows=None):
+        """dx = norm backward of dy at h, plus dh (fp64)."""
+        h_bits = _u16(h_bits)
+        dy_bits = _u16(dy_bits)
+        dh_bits = _u16(dh_bits)
+        M, N = h_bits.shape
+        gamma_bits = _u16(gamma_bits)
+        r, R = _rows(rows, M)
+        dx = np.empty((R, N), np.float64)
+        _check(self.lib.oracle_add_bwd_dx_bf16(_ptr(dy_bits, _u16p), _ptr(h_bits, _u16p),
+                                               _ptr(dh_bits, _u16p), _ptr(gamma_bits, _u16p),
+                                               M, N, float(eps), int(mode), _ptr(r, _i64p), R,
+                                               _ptr(dx, _dp)), "oracle_add_bwd_dx_bf16")
+        return dx
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -211,6 +252,18 @@ def bwd_dx_bf16(*a, **k):
 
 def param_grads_bf16(*a, **k):
     return default().param_grads_bf16(*a, **k)
+
+
+def residual_add_bf16(*a, **k):
+    return default().residual_add_bf16(*a, **k)
+
+
+def add_fwd_bf16(*a, **k):
+    return default().add_fwd_bf16(*a, **k)
+
+
+def add_bwd_dx_bf16(*a, **k):
+    return default().add_bwd_dx_bf16(*a, **k)
 
 
 def bf16_bits_to_f64(bits):

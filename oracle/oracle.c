@@ -45,6 +45,18 @@
  * Every statistic is recomputed here in double from the inputs; nothing
  * saved by another implementation is reused.  bf16 inputs are widened
  * exactly (bf16 is the top half of an IEEE binary32).
+ *
+ * Fused residual add + norm (the "fusion with surrounding operations" that
+ * the same page and the kernel-fusion paragraph of "Otimizacao de
+ * Performance de GPU" credit): the residual stream is updated and
+ * normalised in one pass,
+ *   h = bf16(x + r)        (the sum is formed in binary32, then rounded to
+ *                           nearest-even bf16: h is a stored tensor, and the
+ *                           oracle takes that rounding decision exactly as
+ *                           the kernels do)
+ *   y = norm(h)            (the definitions above, on the bf16 values of h)
+ * and its backward adds the gradient dh that reaches h through the residual
+ * path:  dx = dr = (norm backward of dy at h) + dh.
  */
 #include <math.h>
 #include <stdint.h>
@@ -147,6 +159,32 @@ static void bwd_row(const double *dy, const double *x, const double *gamma,
             if (dbeta_abs)
                 dbeta_abs[j] += fabs(dy[j]);
         }
+    }
+}
+
+/* binary32 -> bf16 bit pattern, round to nearest, ties to even (NaN kept
+ * quiet).  Written from the definition: add half an ulp of bf16 (0x7FFF)
+ * plus the parity of the kept low bit, then truncate. */
+static uint16_t float_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* h = bf16(x + r) over n elements, the sum formed in binary32. */
+static void residual_add_row(const uint16_t *x, const uint16_t *r, int64_t n,
+                             uint16_t *h)
+{
+    for (int64_t j = 0; j < n; ++j) {
+        float a = (float)bf16_bits_to_double(x[j]);
+        float b = (float)bf16_bits_to_double(r[j]);
+        float s = a + b;
+        h[j] = float_to_bf16_rne(s);
     }
 }
 
@@ -299,5 +337,38 @@ int oracle_param_grads_bf16(const uint16_t *dy, const uint16_t *x,
                 dbeta_abs);
     }
     free(xr); free(dyr); free(g);
+    return 0;
+}
+
+/* ------------------------------------------------- fused residual add API */
+
+/* h = bf16(x + r) for all M rows (bit patterns). */
+int oracle_residual_add_bf16(const uint16_t *x, const uint16_t *r, int64_t M,
+                             int64_t N, uint16_t *h)
+{
+    if (!x || !r || !h || M < 0 || N < 1)
+        return -1;
+    for (int64_t i = 0; i < M; ++i)
+        residual_add_row(x + i * N, r + i * N, N, h + i * N);
+    return 0;
+}
+
+/* dx = (norm backward of dy at h) + dh for the listed rows (row convention
+ * of oracle_bwd_dx_bf16); h, dy, dh are bf16 bit patterns. */
+int oracle_add_bwd_dx_bf16(const uint16_t *dy, const uint16_t *h,
+                           const uint16_t *dh, const uint16_t *gamma,
+                           int64_t M, int64_t N, double eps, int mode,
+                           const int64_t *rows, int64_t nrows, double *dx)
+{
+    if (!dh)
+        return -1;
+    int rc = oracle_bwd_dx_bf16(dy, h, gamma, M, N, eps, mode, rows, nrows, dx);
+    if (rc != 0)
+        return rc;
+    for (int64_t k = 0; k < nrows; ++k) {
+        int64_t i = rows ? rows[k] : k;
+        for (int64_t j = 0; j < N; ++j)
+            dx[k * N + j] += bf16_bits_to_double(dh[i * N + j]);
+    }
     return 0;
 }

@@ -339,6 +339,53 @@ def pin_bf16_entry_points(orc):
         assert np.all(pga >= np.abs(pg)) and np.all(pba >= np.abs(pb)), "abs sums"
 
 
+# ------------------------------------------------- fused residual add + norm
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_residual_add_rounding(orc):
+    """h = bf16(x + r) with the sum in binary32 and round-to-nearest-even:
+    equal, bit for bit, to torch's own float32 add and bf16 conversion, on
+    values that exercise carries, cancellation, ties, overflow to inf and
+    operands many binades apart."""
+    g = torch.Generator().manual_seed(12)
+    x = torch.randn(64, 96, generator=g) * torch.exp2(torch.randint(-20, 20, (64, 96), generator=g).float())
+    r = torch.randn(64, 96, generator=g) * torch.exp2(torch.randint(-20, 20, (64, 96), generator=g).float())
+    r[:8] = -x[:8]                      # exact cancellation
+    r[8:16] = x[8:16] * 2.0 ** -8       # sums that land on bf16 ties
+    x[16, :4] = 3.0e38
+    r[16, :4] = 3.0e38                  # overflow to inf
+    xb, rb = x.to(torch.bfloat16), r.to(torch.bfloat16)
+    want = (xb.float() + rb.float()).to(torch.bfloat16)
+    got = orc.residual_add_bf16(_bits(xb), _bits(rb))
+    assert np.array_equal(got, _bits(want)), "residual add bits differ from float32 add + RNE"
+
+
+def pin_add_norm_composition(orc):
+    """The fused forward is the norm of h; the fused backward is the norm's
+    dx at h plus the residual gradient dh, added (not subtracted, not scaled)."""
+    g = torch.Generator().manual_seed(13)
+    M, N = 6, 40
+    x = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    r = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    dy = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    dh = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(N, generator=g)).to(torch.bfloat16)
+    beta = (0.1 * torch.randn(N, generator=g)).to(torch.bfloat16)
+    for mode in (RMS, LAYER):
+        bb = _bits(beta) if mode == LAYER else None
+        h, y, rs, mu = orc.add_fwd_bf16(_bits(x), _bits(r), _bits(gamma), bb, 1e-5, mode)
+        y2, rs2, mu2 = orc.fwd_bf16(h, _bits(gamma), bb, 1e-5, mode)
+        assert np.array_equal(y, y2) and np.array_equal(rs, rs2)
+        dx = orc.add_bwd_dx_bf16(_bits(dy), h, _bits(dh), _bits(gamma), 1e-5, mode)
+        dx0 = orc.bwd_dx_bf16(_bits(dy), h, _bits(gamma), 1e-5, mode)
+        assert np.array_equal(dx, dx0 + dh.double().numpy()), "dx must be norm dx + dh"
+        rows = np.array([5, 0, 2])
+        dxs = orc.add_bwd_dx_bf16(_bits(dy), h, _bits(dh), _bits(gamma), 1e-5, mode, rows=rows)
+        assert np.array_equal(dxs, dx[rows]), "row selection of the fused backward"
+
+
 ALL_PINS = [
     pin_rms_constant_row,
     pin_layer_constant_row,
@@ -351,4 +398,6 @@ ALL_PINS = [
     pin_torch_float64,
     pin_symmetries,
     pin_bf16_entry_points,
+    pin_residual_add_rounding,
+    pin_add_norm_composition,
 ]

@@ -31,6 +31,12 @@ MUTANTS = {
                     "widen_row(x + k * N, N, xr);\n        double mu, r;"),
     "param_grads_transposed": ("widen_row(x + i * N, N, xr);\n        widen_row(dy + i * N, N, dyr);\n        bwd_row(dyr, xr, g, N, eps, mode, NULL",
                                "widen_row(x + i * N, N, xr);\n        widen_row(dy + i * N, N, dyr);\n        bwd_row(xr, dyr, g, N, eps, mode, NULL"),
+    "residual_round_truncates": ("u += 0x7FFFu + lsb;", "u += 0u * lsb;"),
+    "residual_ties_away": ("u += 0x7FFFu + lsb;", "u += 0x8000u + 0u * lsb;"),
+    "residual_dh_subtracted": ("dx[k * N + j] += bf16_bits_to_double(dh[i * N + j]);",
+                               "dx[k * N + j] -= bf16_bits_to_double(dh[i * N + j]);"),
+    "residual_dh_wrong_row": ("dx[k * N + j] += bf16_bits_to_double(dh[i * N + j]);",
+                              "dx[k * N + j] += bf16_bits_to_double(dh[k * N + j]);"),
 }
 
 
