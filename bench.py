@@ -38,10 +38,13 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algo_bytes(M, N, mode, P):
+def algo_bytes(M, N, mode, P, residual=False):
+    """Minimal bytes of the forward and backward pass.  The fused residual
+    variant adds r read and h written (4MN) to the forward and dh read (2MN)
+    to the backward, which reads h where the plain one reads x."""
     k = 2 if mode == 1 else 1
-    fwd = 4 * M * N + 2 * k * N + 4 * k * M
-    bwd = 6 * M * N + 2 * N + 4 * k * M + 4 * k * P * N
+    fwd = 4 * M * N + 2 * k * N + 4 * k * M + (4 * M * N if residual else 0)
+    bwd = 6 * M * N + 2 * N + 4 * k * M + 4 * k * P * N + (2 * M * N if residual else 0)
     return fwd, bwd
 
 
@@ -273,9 +276,10 @@ def run_reference(args):
 # ------------------------------------------------------------------ GPU arm
 class DirectStep:
     """One fwd+bwd step through the C ABI with pre-marshalled arguments (no
-    per-call Python tensor checks inside the timed loop)."""
+    per-call Python tensor checks inside the timed loop).  With `r` and `dh`
+    given it runs the fused residual add variant (norm_add_fwd/norm_add_bwd)."""
 
-    def __init__(self, gb, w, x, g, b, dy, stream):
+    def __init__(self, gb, w, x, g, b, dy, stream, r=None, dh=None):
         import torch
 
         M, N = w.M, w.N
@@ -286,7 +290,9 @@ class DirectStep:
         self.mean = torch.empty(M, dtype=torch.float32, device=dev) if w.mode == 1 else None
         self.dg = torch.empty(N, dtype=torch.float32, device=dev)
         self.db = torch.empty(N, dtype=torch.float32, device=dev) if w.mode == 1 else None
-        nbytes = gb.norm_bwd_workspace_bytes(M, N, w.mode)
+        fused = r is not None
+        ws_query = gb.norm_add_bwd_workspace_bytes if fused else gb.norm_bwd_workspace_bytes
+        nbytes = ws_query(M, N, w.mode)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
         L = gb.lib()
         vp = ctypes.c_void_p
@@ -295,11 +301,21 @@ class DirectStep:
             return None if t is None else vp(t.data_ptr())
 
         s = vp(stream.cuda_stream)
-        self.fwd_args = (L.norm_fwd, [p(x), p(g), p(b), M, N, ctypes.c_float(w.eps), w.mode,
-                                      p(self.y), p(self.rstd), p(self.mean), s])
-        self.bwd_args = (L.norm_bwd, [p(dy), p(x), p(g), p(self.rstd), p(self.mean), M, N,
-                                      w.mode, p(self.dx), p(self.dg), p(self.db), p(self.ws),
-                                      ctypes.c_size_t(self.ws.numel()), s])
+        eps = ctypes.c_float(w.eps)
+        ws = [p(self.ws), ctypes.c_size_t(self.ws.numel()), s]
+        if fused:
+            self.h = torch.empty_like(x)
+            self.fwd_args = (L.norm_add_fwd, [p(x), p(r), p(g), p(b), M, N, eps, w.mode,
+                                              p(self.h), p(self.y), p(self.rstd),
+                                              p(self.mean), s])
+            self.bwd_args = (L.norm_add_bwd, [p(dy), p(dh), p(self.h), p(g), p(self.rstd),
+                                              p(self.mean), M, N, w.mode, p(self.dx),
+                                              p(self.dg), p(self.db)] + ws)
+        else:
+            self.fwd_args = (L.norm_fwd, [p(x), p(g), p(b), M, N, eps, w.mode, p(self.y),
+                                          p(self.rstd), p(self.mean), s])
+            self.bwd_args = (L.norm_bwd, [p(dy), p(x), p(g), p(self.rstd), p(self.mean), M,
+                                          N, w.mode, p(self.dx), p(self.dg), p(self.db)] + ws)
 
     def fwd(self):
         f, a = self.fwd_args
@@ -481,10 +497,14 @@ def run_sweep(args):
     names = list(wl.WORKLOADS) if args.sweep == "all" else args.sweep.split(",")
     for name in names:
         w = wl.WORKLOADS[name]
-        x, g, b, dy = wl.make_inputs(w, "cuda")
-        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream())
-        pf = gb.norm_plan(w.M, w.N, w.mode, False)
-        pb = gb.norm_plan(w.M, w.N, w.mode, True)
+        fused = args.fused_residual
+        if fused:
+            x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
+        else:
+            (x, g, b, dy), r, dh = wl.make_inputs(w, "cuda"), None, None
+        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh)
+        pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused)
+        pb = gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
         res = {}
         for name_, fn in (("fwd", step.fwd), ("bwd", step.bwd)):
             for _ in range(args.warmup):
@@ -500,19 +520,19 @@ def run_sweep(args):
             res[name_] = e0.elapsed_time(e1) / args.steps
         if gb.norm_get_device_error() != 0:
             raise RuntimeError(f"device error word set on {name}")
-        fb, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"])
+        fb, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"], residual=fused)
         keep = ("cluster", "threads_per_row", "chunks_per_thread", "groups", "rows_per_group",
                 "stages", "grid", "exact")
         print(json.dumps({
             "workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
-            "fwd_us": 1e3 * res["fwd"], "bwd_us": 1e3 * res["bwd"],
+            "fused_residual": fused, "fwd_us": 1e3 * res["fwd"], "bwd_us": 1e3 * res["bwd"],
             "fwd_GBs": fb / res["fwd"] / 1e6, "bwd_GBs": bb / res["bwd"] / 1e6,
             "step_GBs": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6,
             "step_frac": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6 / peak,
             "peak": peak, "peak_kind": peak_kind, "iters": args.steps,
             "plan_fwd": {k: pf[k] for k in keep}, "plan_bwd": {k: pb[k] for k in keep}}),
             flush=True)
-        del step, x, g, b, dy
+        del step, x, g, b, dy, r, dh
         torch.cuda.empty_cache()
 
 
@@ -532,6 +552,8 @@ def main():
     ap.add_argument("--sweep", default="",
                     help="'all' or comma-separated workload names: per-workload fwd/bwd "
                          "timings, one JSON line each (not the benchmark line)")
+    ap.add_argument("--fused-residual", action="store_true",
+                    help="with --sweep: time norm_add_fwd/norm_add_bwd (h = x + r fused in)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -128,8 +128,45 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma,
                        norm_stream_t stream);
 
 /*
+ * Fused residual add + norm.  The same page credits the normalisation
+ * kernels' automatic fusion with surrounding operations, and "Otimizacao de
+ * Performance de GPU" (introl.com, paragraph on kernel fusion) the saving of
+ * intermediate HBM traffic; the usual pre-norm transformer block adds a
+ * residual right before the norm.  One pass reads x and r and writes both
+ * the updated residual stream and the normalised output:
+ *   h = bf16(x + r)   (sum in fp32, rounded to nearest even)
+ *   y = norm(h)       (as norm_fwd, on the bf16 values of h)
+ * and the backward pass adds the gradient dh that reaches h through the
+ * residual path:  dx = (norm_bwd's dx at h) + dh  (sum in fp32, one rounding);
+ * dx is the gradient of both x and r.  dgamma / dbeta as norm_bwd.
+ * Shapes: rows that fit one CTA (N up to 16384 for LAYER, 24576 for RMS in
+ * the forward pass; 8192 / 12288 in the backward pass); longer rows return
+ * NORM_ERR_UNSUPPORTED.  Other requirements as norm_fwd / norm_bwd.
+ *
+ * norm_add_fwd:  x, r bf16 [M, N] inputs; h, y bf16 [M, N] outputs; rstd,
+ *                mean (LAYER) fp32 [M] outputs; gamma, beta as norm_fwd.
+ * norm_add_bwd:  dy, dh, h bf16 [M, N]; rstd, mean from norm_add_fwd; dx bf16
+ *                [M, N]; workspace of norm_add_bwd_workspace_bytes bytes.
+ */
+norm_status_t norm_add_fwd(const void *x, const void *r, const void *gamma,
+                           const void *beta, int64_t M, int64_t N, float eps,
+                           norm_mode_t mode, void *h, void *y, float *rstd,
+                           float *mean, norm_stream_t stream);
+
+norm_status_t norm_add_bwd_workspace_bytes(int64_t M, int64_t N,
+                                           norm_mode_t mode, size_t *bytes);
+
+norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h,
+                           const void *gamma, const float *rstd,
+                           const float *mean, int64_t M, int64_t N,
+                           norm_mode_t mode, void *dx, float *dgamma,
+                           float *dbeta, void *workspace,
+                           size_t workspace_bytes, norm_stream_t stream);
+
+/*
  * norm_plan -- the launch plan the library uses for one pass (backward = 0
- * for norm_fwd, 1 for norm_bwd) of an [M, N] problem: how rows are split
+ * for norm_fwd, 1 for norm_bwd, 2 for norm_add_fwd, 3 for norm_add_bwd) of
+ * an [M, N] problem: how rows are split
  * across threads, CTAs and clusters, and how many tiles are kept in flight.
  * With sm_count <= 0 it describes the CURRENT device (occupancy queried
  * through the CUDA runtime) and equals what norm_fwd / norm_bwd launch.

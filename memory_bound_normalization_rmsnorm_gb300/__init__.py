@@ -5,11 +5,13 @@ include/gbnorm.h (libgbnorm.so); this package is its thin Python binding plus
 the seeded synthetic workloads used by the tests and the benchmark.
 """
 from ._binding import (LAYER, RMS, NormError, declared_functions, lib, library_path,
-                       norm_bwd, norm_bwd_workspace_bytes, norm_fwd, norm_get_device_error, norm_plan,
+                       norm_add_bwd, norm_add_bwd_workspace_bytes, norm_add_fwd, norm_bwd,
+                       norm_bwd_workspace_bytes, norm_fwd, norm_get_device_error, norm_plan,
                        strerror)
 from .builder import build
 
 __all__ = [
     "RMS", "LAYER", "NormError", "norm_fwd", "norm_bwd", "norm_bwd_workspace_bytes",
-    "norm_get_device_error", "norm_plan", "strerror", "lib", "library_path", "declared_functions", "build",
+    "norm_get_device_error", "norm_plan", "norm_add_fwd", "norm_add_bwd",
+    "norm_add_bwd_workspace_bytes", "strerror", "lib", "library_path", "declared_functions", "build",
 ]

@@ -90,6 +90,15 @@ def lib():
             L.norm_bwd_noalloc.restype = ctypes.c_int
             L.norm_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _vp]
             L.norm_selftest_wait_timeout.restype = ctypes.c_int
+            L.norm_add_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
+                                       ctypes.c_int, _vp, _vp, _vp, _vp, _vp]
+            L.norm_add_fwd.restype = ctypes.c_int
+            L.norm_add_bwd_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int,
+                                                       ctypes.POINTER(ctypes.c_size_t)]
+            L.norm_add_bwd_workspace_bytes.restype = ctypes.c_int
+            L.norm_add_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int,
+                                       _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            L.norm_add_bwd.restype = ctypes.c_int
             L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(Plan)]
             L.norm_plan.restype = ctypes.c_int
@@ -222,12 +231,83 @@ def norm_bwd(dy, x, gamma, rstd, mean=None, mode=RMS, *, dx=None, dgamma=None, d
     return dx, dgamma, dbeta
 
 
-def norm_plan(M, N, mode=RMS, backward=False, sm_count=0, smem_optin=0) -> dict:
+def norm_add_fwd(x, r, gamma, beta=None, eps=1e-5, mode=RMS, *, h=None, y=None, rstd=None,
+                 mean=None, stream=None):
+    """Fused residual add + norm forward: h = bf16(x + r), y = norm(h).
+    Returns (h, y, rstd, mean)."""
+    mode = int(mode)
+    M, N = _rows(x)
+    dev = x.device
+    bf, f32 = torch.bfloat16, torch.float32
+    _check_tensor(x, "x", bf, x.shape, dev)
+    _check_tensor(r, "r", bf, x.shape, dev)
+    _check_tensor(gamma, "gamma", bf, (N,), dev)
+    _check_tensor(beta, "beta", bf, (N,), dev)
+    h = torch.empty_like(x) if h is None else h
+    y = torch.empty_like(x) if y is None else y
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=f32, device=dev)
+    if mode == LAYER and mean is None:
+        mean = torch.empty(x.shape[:-1], dtype=f32, device=dev)
+    for t, n in ((h, "h"), (y, "y")):
+        _check_tensor(t, n, bf, x.shape, dev)
+    _check_tensor(rstd, "rstd", f32, x.shape[:-1], dev)
+    _check_tensor(mean, "mean", f32, x.shape[:-1], dev)
+    st = lib().norm_add_fwd(_ptr(x), _ptr(r), _ptr(gamma), _ptr(beta), M, N, float(eps), mode,
+                            _ptr(h), _ptr(y), _ptr(rstd), _ptr(mean), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_add_fwd")
+    return h, y, rstd, mean
+
+
+def norm_add_bwd_workspace_bytes(M, N, mode=RMS) -> int:
+    out = ctypes.c_size_t(0)
+    st = lib().norm_add_bwd_workspace_bytes(int(M), int(N), int(mode), ctypes.byref(out))
+    if st != 0:
+        raise NormError(st, "norm_add_bwd_workspace_bytes")
+    return int(out.value)
+
+
+def norm_add_bwd(dy, dh, h, gamma, rstd, mean=None, mode=RMS, *, dx=None, dgamma=None,
+                 dbeta=None, want_dbeta=True, workspace=None, stream=None):
+    """Fused residual add + norm backward: dx = norm backward at h + dh (the
+    gradient of both x and r).  Returns (dx, dgamma, dbeta)."""
+    mode = int(mode)
+    M, N = _rows(h)
+    dev = h.device
+    bf, f32 = torch.bfloat16, torch.float32
+    for t, n in ((dy, "dy"), (dh, "dh"), (h, "h")):
+        _check_tensor(t, n, bf, h.shape, dev)
+    _check_tensor(gamma, "gamma", bf, (N,), dev)
+    _check_tensor(rstd, "rstd", f32, h.shape[:-1], dev)
+    _check_tensor(mean, "mean", f32, h.shape[:-1], dev)
+    dx = torch.empty_like(h) if dx is None else dx
+    dgamma = torch.empty(N, dtype=f32, device=dev) if dgamma is None else dgamma
+    if mode == LAYER and want_dbeta and dbeta is None:
+        dbeta = torch.empty(N, dtype=f32, device=dev)
+    _check_tensor(dx, "dx", bf, h.shape, dev)
+    _check_tensor(dgamma, "dgamma", f32, (N,), dev)
+    _check_tensor(dbeta, "dbeta", f32, (N,), dev)
+    if workspace is None:
+        with torch.cuda.device(dev):
+            nbytes = norm_add_bwd_workspace_bytes(M, N, mode)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    st = lib().norm_add_bwd(_ptr(dy), _ptr(dh), _ptr(h), _ptr(gamma), _ptr(rstd), _ptr(mean), M,
+                            N, mode, _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_add_bwd")
+    return dx, dgamma, dbeta
+
+
+def norm_plan(M, N, mode=RMS, backward=False, sm_count=0, smem_optin=0, residual=False) -> dict:
     """Launch plan of one pass (see norm_plan in gbnorm.h).  sm_count > 0
-    plans for a hypothetical device without touching CUDA."""
+    plans for a hypothetical device without touching CUDA; residual=True
+    plans the fused residual add variant."""
     out = Plan()
-    st = lib().norm_plan(int(M), int(N), int(mode), 1 if backward else 0, int(sm_count),
-                         int(smem_optin), ctypes.byref(out))
+    which = (1 if backward else 0) | (2 if residual else 0)
+    st = lib().norm_plan(int(M), int(N), int(mode), which, int(sm_count), int(smem_optin),
+                         ctypes.byref(out))
     if st != 0:
         raise NormError(st, "norm_plan")
     return out.as_dict()

@@ -160,7 +160,7 @@ constexpr TunedPlan kTuned[] = {
 // Ring and tile sizing shared by both plan kinds: rows per tile and the
 // number of stages that fit in shared memory (at least two).
 norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, int64_t M) {
-  const int ntensors = bwd ? 2 : 1;
+  const int ntensors = (bwd ? 2 : 1) + (p.resid ? 1 : 0);
   const int C = p.C;
   int G = p.G;
   const int row_bytes = p.NS * 2;
@@ -246,9 +246,9 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
 // Pure host arithmetic (no CUDA call).  `bwd` selects the backward kernel
 // (two tensors per stage, at most kMaxKBwd chunks per thread).
 norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
-                         const Override &ov_in, Plan *out) {
+                         const Override &ov_in, Plan *out, bool resid = false) {
   Override ov = ov_in;
-  if (!ov.any) {
+  if (!ov.any && !resid) {
     for (const TunedPlan &tp : kTuned) {
       if (tp.mode == mode && tp.bwd == (bwd ? 1 : 0) && tp.N == N) {
         ov.tpr = tp.tpr;
@@ -261,6 +261,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
   const int nc = N / 8;
   Plan p;
+  p.resid = resid;
 
   // Preferred chunks per thread, and the most that still fit in registers
   // without spilling (ptxas -v: forward LayerNorm 4, RMSNorm 6; backward
@@ -270,8 +271,10 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 
   // Rows wider than one CTA's register capacity (kMaxThreads x klim chunks)
   // go to the long-row kernels, which keep the row in shared memory.
-  if (ov.lng == 1 || (ov.lng != 0 && nc > kMaxThreads * klim))
+  if (ov.lng == 1 || (ov.lng != 0 && nc > kMaxThreads * klim)) {
+    if (resid) return NORM_ERR_UNSUPPORTED;  // fused residual: register-resident rows only
     return long_plan(mode, bwd, M, N, smem_optin, ov, out);
+  }
 
   // Column split: the smallest power-of-two cluster (up to 8) whose per-CTA
   // slice fits kMaxThreads threads x kpref chunks, else the smallest (up to
@@ -282,7 +285,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   while (C < 16 && ceil_div(nc, C) > kMaxThreads * klim) C <<= 1;
   while (C <= 16 && ceil_div(nc, C) > kMaxThreads * kmax) C <<= 1;
   if (ov.C) C = ov.C;
-  if (C < 1 || C > 16) return NORM_ERR_UNSUPPORTED;
+  if (C < 1 || C > 16 || (resid && C != 1)) return NORM_ERR_UNSUPPORTED;
   p.C = C;
   p.nsc = ceil_div(nc, C);
   p.NS = p.nsc * 8;
@@ -298,7 +301,8 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   bool exact = false;
   auto try_exact = [&](int k) {
     if (!even || p.nsc % k || (p.nsc / k) % 32 || p.nsc / k > kMaxThreads) return false;
-    if (!(bwd ? bwd_kernel_ptr(mode, k, C > 1, true) : fwd_kernel_ptr(mode, k, C > 1, true)))
+    if (!(bwd ? bwd_kernel_ptr(mode, k, C > 1, true, resid)
+              : fwd_kernel_ptr(mode, k, C > 1, true, resid)))
       return false;
     tpr = p.nsc / k;
     K = k;
@@ -341,8 +345,8 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
   if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ);
-  return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact)
-             : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact);
+  return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
+             : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid);
 }
 
 void set_grid(Plan &p, int64_t resident_clusters) {
@@ -354,9 +358,9 @@ void set_grid(Plan &p, int64_t resident_clusters) {
 // Full plan on the current device: shape part plus the occupancy-derived
 // grid (persistent: as many CTAs or clusters as can be resident at once).
 norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_t M, int N,
-                        Plan *out) {
+                        Plan *out, bool resid = false) {
   const Override ov = read_override();
-  const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, 0);
+  const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, resid ? 1 : 0);
   if (!ov.any) {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
@@ -366,7 +370,7 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
     }
   }
   Plan p;
-  norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p);
+  norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p, resid);
   if (st != NORM_OK) return st;
 
   const void *fn = kernel_for(p, mode, bwd);
@@ -439,6 +443,28 @@ norm_status_t launch(const void *fn, const Plan &p, const NormArgs &args, cudaSt
   NormArgs a = args;
   void *kargs[] = {&a};
   if (cudaLaunchKernelExC(&cfg, fn, kargs) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return NORM_OK;
+}
+
+// The fixed-order reduction of the backward partials into dgamma (and dbeta
+// when given), on `s` after the row kernel.
+norm_status_t launch_reduce(const float *ws, int P, int n, float *dgamma, float *dbeta,
+                            cudaStream_t s) {
+  const int nparts = dbeta ? 2 : 1;
+  void *rargs[] = {&ws, &P, &n, &dgamma, &dbeta};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 127) / 128, nparts);
+  cfg.blockDim = dim3(reduce_threads());
+  cfg.stream = s;
+  cudaLaunchAttribute rattr;
+  rattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  rattr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &rattr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, reduce_kernel_ptr(), rargs) != cudaSuccess) {
     cudaGetLastError();
     return NORM_ERR_CUDA;
   }
@@ -568,25 +594,95 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch(kernel_for(p, mode, true), p, a, s)) != NORM_OK) return st;
 
-  const int nparts = (mode == NORM_LAYER && dbeta) ? 2 : 1;
-  const void *rfn = reduce_kernel_ptr();
-  const float *ws = static_cast<const float *>(workspace);
-  int P = p.P, n = static_cast<int>(N);
-  void *rargs[] = {&ws, &P, &n, &dgamma, &dbeta};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((n + 127) / 128, nparts);
-  cfg.blockDim = dim3(reduce_threads());
-  cfg.stream = s;
-  cudaLaunchAttribute rattr;
-  rattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  rattr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &rattr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelExC(&cfg, rfn, rargs) != cudaSuccess) {
-    cudaGetLastError();
-    return NORM_ERR_CUDA;
-  }
+  return launch_reduce(static_cast<const float *>(workspace), p.P, static_cast<int>(N), dgamma,
+                       (mode == NORM_LAYER) ? dbeta : nullptr, s);
+}
+
+norm_status_t norm_add_fwd(const void *x, const void *r, const void *gamma, const void *beta,
+                           int64_t M, int64_t N, float eps, norm_mode_t mode, void *h, void *y,
+                           float *rstd, float *mean, norm_stream_t stream) {
+  if (!x || !r || !gamma || !h || !y || !rstd) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  if (mode == NORM_RMS && (beta || mean)) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return NORM_ERR_ARG;
+  if (!aligned16(x) || !aligned16(r) || !aligned16(gamma) || !aligned16(h) || !aligned16(y) ||
+      !aligned16(rstd) || (beta && !aligned16(beta)) || (mean && !aligned16(mean)))
+    return NORM_ERR_ALIGN;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p, true)) != NORM_OK)
+    return st;
+  NormArgs a = base_args(p, M, static_cast<int>(N));
+  a.x = static_cast<const uint16_t *>(x);
+  a.res = static_cast<const uint16_t *>(r);
+  a.gamma = static_cast<const uint16_t *>(gamma);
+  a.beta = static_cast<const uint16_t *>(beta);
+  a.h = static_cast<uint16_t *>(h);
+  a.out = static_cast<uint16_t *>(y);
+  a.rstd = rstd;
+  a.mean = mean;
+  a.err = d.err;
+  a.eps = eps;
+  return launch(kernel_for(p, mode, false), p, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+norm_status_t norm_add_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode,
+                                           size_t *bytes) {
+  if (!bytes) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p, true)) != NORM_OK)
+    return st;
+  *bytes = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
+           (mode == NORM_LAYER ? 2u : 1u);
   return NORM_OK;
+}
+
+norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h, const void *gamma,
+                           const float *rstd, const float *mean, int64_t M, int64_t N,
+                           norm_mode_t mode, void *dx, float *dgamma, float *dbeta,
+                           void *workspace, size_t workspace_bytes, norm_stream_t stream) {
+  if (!dy || !dh || !h || !gamma || !rstd || !dx || !dgamma) return NORM_ERR_NULL;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  if (mode == NORM_RMS && (mean || dbeta)) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
+  if (!aligned16(dy) || !aligned16(dh) || !aligned16(h) || !aligned16(gamma) ||
+      !aligned16(rstd) || !aligned16(dx) || !aligned16(dgamma) || (mean && !aligned16(mean)) ||
+      (dbeta && !aligned16(dbeta)) || (workspace && !aligned16(workspace)))
+    return NORM_ERR_ALIGN;
+  if (!workspace) return NORM_ERR_WORKSPACE;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p, true)) != NORM_OK)
+    return st;
+  const size_t need = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
+                      (mode == NORM_LAYER ? 2u : 1u);
+  if (workspace_bytes < need) return NORM_ERR_WORKSPACE;
+  NormArgs a = base_args(p, M, static_cast<int>(N));
+  a.x = static_cast<const uint16_t *>(h);
+  a.dy = static_cast<const uint16_t *>(dy);
+  a.res = static_cast<const uint16_t *>(dh);
+  a.gamma = static_cast<const uint16_t *>(gamma);
+  a.out = static_cast<uint16_t *>(dx);
+  a.rstd = const_cast<float *>(rstd);
+  a.mean = const_cast<float *>(mean);
+  a.ws = static_cast<float *>(workspace);
+  a.err = d.err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch(kernel_for(p, mode, true), p, a, s)) != NORM_OK) return st;
+  return launch_reduce(static_cast<const float *>(workspace), p.P, static_cast<int>(N), dgamma,
+                       (mode == NORM_LAYER) ? dbeta : nullptr, s);
 }
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, int sm_count,
@@ -594,12 +690,14 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   if (!out) return NORM_ERR_NULL;
   norm_status_t st = check_common(M, N, mode);
   if (st != NORM_OK) return st;
-  const bool bwd = backward != 0;
+  if (backward & ~3) return NORM_ERR_ARG;
+  const bool bwd = (backward & 1) != 0;
+  const bool resid = (backward & 2) != 0;
   Plan p;
   if (sm_count > 0) {
     if (smem_optin_bytes <= 0) return NORM_ERR_ARG;
     if ((st = shape_plan(mode, bwd, M, static_cast<int>(N), smem_optin_bytes, read_override(),
-                         &p)) != NORM_OK)
+                         &p, resid)) != NORM_OK)
       return st;
     set_grid(p, static_cast<int64_t>(sm_count) * p.occ / p.C);
     if (p.grid < 1) return NORM_ERR_UNSUPPORTED;
@@ -607,7 +705,8 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
     DeviceInfo d;
     int dev = 0;
     if ((st = device_info(&d, &dev)) != NORM_OK) return st;
-    if ((st = make_plan(d, dev, mode, bwd, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+    if ((st = make_plan(d, dev, mode, bwd, M, static_cast<int>(N), &p, resid)) != NORM_OK)
+      return st;
   }
   out->cluster = p.C;
   out->cols_per_cta = p.NS;

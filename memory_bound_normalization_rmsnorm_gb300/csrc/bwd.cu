@@ -23,10 +23,12 @@ namespace {
 
 // EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
 // chunk needs an ownership test and the warp butterfly is full width.
-template <int MODE, int K, bool CLUSTER, bool EXACT>
+// RESID: fused residual add -- x is h, and the stage also holds dh, added to
+// dx (in fp32, before rounding): dx = norm backward + dh.
+template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, a.C);
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 3 : 2, true, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   const float *stats_all = reinterpret_cast<const float *>(smem + L.stats_off);
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   if (tid < 32) {
     for (int j = 0; j < a.S; ++j) {
       const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_bwd_tile<MODE, CLUSTER>(a, L, smem, tile, j, col0, nsc_me, pol);
+      if (tile < a.ntiles) issue_bwd_tile<MODE, CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
     }
   }
 
@@ -169,6 +171,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
               const float2 u = fma2(xh[k][p], cv, av);
               o[p] = mul2(fma2(u, neg1, gg[k][p]), rs2);
             }
+            if (RESID) {
+              float2 dh[4];
+              chunk_to_f2(*reinterpret_cast<const uint4 *>(stx + 2 * L.tensor_bytes +
+                                                           static_cast<size_t>(r) * a.NS * 2 +
+                                                           (t + k * a.tpr) * 16),
+                          dh);
+#pragma unroll
+              for (int p = 0; p < 4; ++p) o[p] = add2(o[p], dh[p]);
+            }
             st_global_cs_v4(dxrow + k * a.tpr * 8, f2_to_chunk(o));
           }
         }
@@ -180,7 +191,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
       if (next < a.ntiles) {
         if ((tid & 31) == 0) fence_proxy_async_smem();
         __syncwarp();
-        issue_bwd_tile<MODE, CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
+        issue_bwd_tile<MODE, CLUSTER, RESID>(a, L, smem, next, s, col0, nsc_me, pol);
       }
     }
     if (++s == a.S) {
@@ -259,26 +270,40 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
 }
 
 template <int MODE, bool CLUSTER>
-const void *pick_bwd(int K, bool e) {
+const void *pick_bwd(int K, bool e, bool r) {
+  if (r && CLUSTER) return nullptr;  // fused residual: no cluster variants
   switch (K) {
-    case 1: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, false>);
-    case 2: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, false>);
-    case 3: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, false>);
-    case 4: return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, false>);
+    case 1:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, false, false>);
+    case 2:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, false, false>);
+    case 3:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, false, false>);
+    case 4:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, false, false>);
     default: return nullptr;
   }
 }
 
 }  // namespace
 
-const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact) {
+const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid) {
   if (mode == kRMS)
-    return cluster ? pick_bwd<kRMS, true>(K, exact) : pick_bwd<kRMS, false>(K, exact);
-  return cluster ? pick_bwd<kLayer, true>(K, exact) : pick_bwd<kLayer, false>(K, exact);
+    return cluster ? pick_bwd<kRMS, true>(K, exact, resid) : pick_bwd<kRMS, false>(K, exact, resid);
+  return cluster ? pick_bwd<kLayer, true>(K, exact, resid)
+                 : pick_bwd<kLayer, false>(K, exact, resid);
 }
 
 const void *reduce_kernel_ptr() {

@@ -28,6 +28,8 @@ struct NormArgs {
   const uint16_t *dy;     // bf16 [M, N] (backward)
   const uint16_t *gamma;  // bf16 [N]
   const uint16_t *beta;   // bf16 [N] or null (forward, LayerNorm)
+  const uint16_t *res;    // fused residual: r (forward) or dh (backward), bf16 [M, N]
+  uint16_t *h;            // fused residual forward: h = bf16(x + r), bf16 [M, N]
   uint16_t *out;          // y (forward) or dx (backward), bf16 [M, N]
   float *rstd;            // [M]: written by forward, read by backward
   float *mean;            // [M]: same, LayerNorm only
@@ -104,6 +106,7 @@ struct Plan {
   bool exact = false; // slices divide evenly into K chunks x tpr threads, tpr >= 32
   bool long_rows = false; // long-row kernels (row re-read from the stage)
   int occ = 1;            // CTAs per SM the kernel is compiled for
+  bool resid = false;     // fused residual add variant
   int G = 0;       // groups per CTA
   int rpg = 1;     // rows per group per tile
   int RT = 0;      // rows per tile
@@ -115,10 +118,11 @@ struct Plan {
   int P = 0;       // clusters in the grid (partial rows in backward)
 };
 
-// Kernel entry points, by (mode, K, cluster, exact).  Return nullptr when
-// that combination is not compiled.
-const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
-const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact);
+// Kernel entry points, by (mode, K, cluster, exact, fused residual).
+// Return nullptr when that combination is not compiled (the fused residual
+// variants exist without clusters only).
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
+const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
 const void *reduce_kernel_ptr();
 // Long-row kernels (row slice re-read from shared memory), K in {4, 8}.
 // occ = CTAs per SM the kernel is compiled for (only 1 is built: a

@@ -32,10 +32,12 @@ namespace {
 
 // EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
 // chunk needs an ownership test and the warp butterfly is full width.
-template <int MODE, int K, bool CLUSTER, bool EXACT>
+// RESID: fused residual add -- the stage also holds r; h = bf16(x + r) (sum
+// in binary32, round to nearest even) is written out and normalised.
+template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, a.C);
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   if (tid == 0) {
     for (int j = 0; j < a.S; ++j) {
       const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_fwd_tile<CLUSTER>(a, L, smem, tile, j, col0, nsc_me, pol);
+      if (tile < a.ntiles) issue_fwd_tile<CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
     }
   }
 
@@ -117,8 +119,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const bool ok = active && (EXACT || t + k * a.tpr < nsc_me);
-        const uint4 v = ok ? *reinterpret_cast<const uint4 *>(rowp + k * a.tpr * 16)
-                           : make_uint4(0, 0, 0, 0);
+        uint4 v = ok ? *reinterpret_cast<const uint4 *>(rowp + k * a.tpr * 16)
+                     : make_uint4(0, 0, 0, 0);
+        if (RESID) {
+          // h = bf16(x + r): add in binary32, round once, store h; the norm
+          // below works on the rounded values.
+          const uint4 rv = ok ? *reinterpret_cast<const uint4 *>(rowp + L.tensor_bytes +
+                                                                 k * a.tpr * 16)
+                              : make_uint4(0, 0, 0, 0);
+          float2 xs[4], rs_[4];
+          chunk_to_f2(v, xs);
+          chunk_to_f2(rv, rs_);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) xs[p] = add2(xs[p], rs_[p]);
+          v = f2_to_chunk(xs);
+          if (ok) st_global_cs_v4(a.h + (row0 + r) * a.N + col0 + (t + k * a.tpr) * 8, v);
+        }
         chunk_to_f2(v, xf[k]);
       }
       float rs;
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
       const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
       if (next < a.ntiles) {
         fence_proxy_async_smem();
-        issue_fwd_tile<CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
+        issue_fwd_tile<CLUSTER, RESID>(a, L, smem, next, s, col0, nsc_me, pol);
       }
     }
     if (++s == a.S) {
@@ -234,32 +250,55 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
 }
 
 template <int MODE, bool CLUSTER>
-const void *pick_fwd(int K, bool e) {
+const void *pick_fwd(int K, bool e, bool r) {
+  if (r && CLUSTER) return nullptr;  // fused residual: no cluster variants
   switch (K) {
-    case 1: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, false>);
-    case 2: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, false>);
-    case 3: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, false>);
-    case 4: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, false>);
-    case 5: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, false>);
-    case 6: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, false>);
-    case 8: return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, true>)
-                   : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, false>);
+    case 1:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, false, false>);
+    case 2:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, false, false>);
+    case 3:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, false, false>);
+    case 4:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, false, false>);
+    case 5:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, false, false>);
+    case 6:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, false, false>);
+    case 8:
+      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, false, true, true>)
+                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, false, false, true>);
+      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, true, false>)
+               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, false, false>);
     default: return nullptr;
   }
 }
 
 }  // namespace
 
-const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact) {
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid) {
   if (mode == kRMS)
-    return cluster ? pick_fwd<kRMS, true>(K, exact) : pick_fwd<kRMS, false>(K, exact);
-  return cluster ? pick_fwd<kLayer, true>(K, exact) : pick_fwd<kLayer, false>(K, exact);
+    return cluster ? pick_fwd<kRMS, true>(K, exact, resid) : pick_fwd<kRMS, false>(K, exact, resid);
+  return cluster ? pick_fwd<kLayer, true>(K, exact, resid)
+                 : pick_fwd<kLayer, false>(K, exact, resid);
 }
 
 }  // namespace gbn

@@ -7,8 +7,9 @@
 
 namespace gbn {
 
-// Forward: x only.  Called by one thread.
-template <bool CLUSTER>
+// Forward: x (and, with RESID, the residual r at the next tensor slot of
+// the stage).  Called by one thread.
+template <bool CLUSTER, bool RESID = false>
 __device__ __forceinline__ void issue_fwd_tile(const NormArgs &a, const SmemLayout &L,
                                                unsigned char *smem, int64_t tile, int s,
                                                int col0, int nsc_me, uint64_t pol) {
@@ -16,24 +17,31 @@ __device__ __forceinline__ void issue_fwd_tile(const NormArgs &a, const SmemLayo
   unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
   const int64_t row0 = tile * a.RT;
   const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
+  const uint32_t nt = RESID ? 2u : 1u;
   if (!CLUSTER) {
     const uint32_t bytes = static_cast<uint32_t>(nrows) * a.N * 2u;
-    mbar_arrive_expect_tx(full, bytes);
+    mbar_arrive_expect_tx(full, nt * bytes);
     bulk_g2s(dst, a.x + row0 * a.N, bytes, full, pol);
+    if (RESID) bulk_g2s(dst + L.tensor_bytes, a.res + row0 * a.N, bytes, full, pol);
   } else {
     // Row r of the tile lands at r * NS * 2 (slice stride), nsc_me chunks.
     const uint32_t bytes = static_cast<uint32_t>(nsc_me) * 16u;
     const uint32_t stride = static_cast<uint32_t>(a.NS) * 2u;
-    mbar_arrive_expect_tx(full, bytes * nrows);
-    for (int r = 0; r < nrows; ++r)
+    mbar_arrive_expect_tx(full, nt * bytes * nrows);
+    for (int r = 0; r < nrows; ++r) {
       bulk_g2s(dst + r * stride, a.x + (row0 + r) * a.N + col0, bytes, full, pol);
+      if (RESID)
+        bulk_g2s(dst + L.tensor_bytes + r * stride, a.res + (row0 + r) * a.N + col0, bytes,
+                 full, pol);
+    }
   }
 }
 
 // Issues tile `tile` into stage `s`: the rows' statistics with 4-byte
-// cp.async copies (one completion arrival per lane), then x and dy with
-// bulk copies.  Must be called by all 32 lanes of one warp.
-template <int MODE, bool CLUSTER>
+// cp.async copies (one completion arrival per lane), then x and dy (and,
+// with RESID, dh at the third tensor slot) with bulk copies.  Must be called
+// by all 32 lanes of one warp.
+template <int MODE, bool CLUSTER, bool RESID = false>
 __device__ __forceinline__ void issue_bwd_tile(const NormArgs &a, const SmemLayout &L,
                                                unsigned char *smem, int64_t tile, int s,
                                                int col0, int nsc_me, uint64_t pol) {
@@ -50,24 +58,26 @@ __device__ __forceinline__ void issue_bwd_tile(const NormArgs &a, const SmemLayo
   cp_async_mbar_arrive(full);
   __syncwarp();
   if (lane == 0) {
+    const uint32_t nt = RESID ? 3u : 2u;
     if (!CLUSTER) {
       const uint32_t bytes = static_cast<uint32_t>(nrows) * a.N * 2u;
-      mbar_arrive_expect_tx(full, 2u * bytes);
+      mbar_arrive_expect_tx(full, nt * bytes);
       bulk_g2s(dst, a.x + row0 * a.N, bytes, full, pol);
       bulk_g2s(dst + L.tensor_bytes, a.dy + row0 * a.N, bytes, full, pol);
+      if (RESID) bulk_g2s(dst + 2 * L.tensor_bytes, a.res + row0 * a.N, bytes, full, pol);
     } else {
       const uint32_t bytes = static_cast<uint32_t>(nsc_me) * 16u;
       const uint32_t stride = static_cast<uint32_t>(a.NS) * 2u;
-      mbar_arrive_expect_tx(full, 2u * bytes * nrows);
+      mbar_arrive_expect_tx(full, nt * bytes * nrows);
       for (int r = 0; r < nrows; ++r) {
         const int64_t off = (row0 + r) * a.N + col0;
         bulk_g2s(dst + r * stride, a.x + off, bytes, full, pol);
         bulk_g2s(dst + L.tensor_bytes + r * stride, a.dy + off, bytes, full, pol);
+        if (RESID) bulk_g2s(dst + 2 * L.tensor_bytes + r * stride, a.res + off, bytes, full, pol);
       }
     }
   }
 }
-
 
 // Backward epilogue: fold the column accumulators of the G row groups of this
 // CTA in group order through shared memory (the ring is idle: every issued

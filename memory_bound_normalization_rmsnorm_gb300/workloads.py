@@ -129,3 +129,23 @@ def bf16_bits(t: torch.Tensor):
     """uint16 numpy view of a bf16 tensor's bit patterns (copies to host)."""
     assert t.dtype == torch.bfloat16
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+def make_residual_inputs(w: Workload, device="cpu", seed=None):
+    """Inputs of the fused residual add + norm: (x, r, gamma, beta, dy, dh).
+
+    x, gamma, beta and dy as make_inputs; then, from a second generator
+    seeded with seed + 1, the residual r ~ N(0, 1) (the update added to the
+    residual stream) and the residual-path gradient dh drawn like dy.
+    """
+    x, gamma, beta, dy = make_inputs(w, device, seed=seed)
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed((w.seed if seed is None else seed) + 1)
+    f32 = dict(dtype=torch.float32, device=dev, generator=g)
+    r = torch.randn(w.M, w.N, **f32).to(torch.bfloat16)
+    dh = torch.randn(w.M, w.N, **f32)
+    if w.dy_scale != 1.0:
+        dh.mul_(w.dy_scale)
+    dh = dh.to(torch.bfloat16)
+    return x, r, gamma, beta, dy, dh

@@ -39,7 +39,7 @@ def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C):
     return L
 
 
-def check_plan(p, M, N, mode, backward, smem_optin=232448):
+def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     """Raise AssertionError if any access of the launch described by `p`
     (a norm_plan dict) would leave its buffer or break an alignment rule."""
     C, NS, tpr, K = p["cluster"], p["cols_per_cta"], p["threads_per_row"], p["chunks_per_thread"]
@@ -55,11 +55,13 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
     assert RT == G * rpg and S >= 2
     assert C >= 1 and grid % C == 0 and grid // C == P and P >= 1
     assert C == 1 or rpg == 1
+    assert not residual or (C == 1 and not p["long_rows"])
     assert ntiles == -(-M // RT) and P <= ntiles
     assert K * tpr >= nsc, "a chunk has no owner"
     if p["exact"]:
         assert tpr % 32 == 0 and K * tpr == nsc and nc % C == 0, "EXACT plan is not exact"
-    L = smem_layout(RT, NS, S, G, tpr, 2 if backward else 1, backward, C)
+    ntensors = (2 if backward else 1) + (1 if residual else 0)
+    L = smem_layout(RT, NS, S, G, tpr, ntensors, backward, C)
     assert smem == L["total"] <= smem_optin, "shared memory over the opt-in limit"
     assert L["stage"] < TX_LIMIT
     assert L["bar"] % 8 == 0 and L["stats"] % 16 == 0 and L["red"] % 16 == 0
@@ -83,6 +85,8 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448):
         if C == 1:
             max_bytes = RT * N * 2
             assert max_bytes <= L["tensor"] and max_bytes % 16 == 0
+            # every tensor of the stage lies inside the stage
+            assert ntensors * L["tensor"] == L["stage"]
         else:
             assert nsc_me * 16 <= NS * 2 and (NS * 2) % 16 == 0
         if backward:

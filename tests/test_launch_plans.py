@@ -38,6 +38,20 @@ def test_all_plans_in_bounds(backward):
     assert n > 400
 
 
+@pytest.mark.parametrize("backward", [False, True])
+def test_fused_residual_plans_in_bounds(backward):
+    n = 0
+    for M, N, mode in _cases():
+        try:
+            p = gb.norm_plan(M, N, mode, backward, SMS, OPTIN, residual=True)
+        except gb.NormError as e:
+            assert e.status == 6 and N > 8192  # only rows beyond one CTA are refused
+            continue
+        launch_check.check_plan(p, M, N, mode, backward, OPTIN, residual=True)
+        n += 1
+    assert n > 200
+
+
 def test_plan_rejects_unsupported():
     with pytest.raises(gb.NormError):
         gb.norm_plan(4, 12, 0, False, SMS, OPTIN)  # N % 8 != 0
