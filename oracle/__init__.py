@@ -32,6 +32,10 @@ _default = None
 _dp = ctypes.POINTER(ctypes.c_double)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i64p = ctypes.POINTER(ctypes.c_int64)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+FP8_ROW = 0
+FP8_MX = 1
 
 
 def compile_c(src: str, out: str) -> str:
@@ -106,9 +110,17 @@ class Oracle:
         lib.oracle_add_bwd_dx_bf16.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
                                                ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                                _i64p, ctypes.c_int64, _dp]
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_encode.argtypes = [_dp, ctypes.c_int64, _u8p]
+        lib.oracle_e4m3_decode.argtypes = [_u8p, ctypes.c_int64, _dp]
+        lib.oracle_fwd_fp8_bf16.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                            ctypes.c_int, _i64p, ctypes.c_int64, _dp, _u8p,
+                                            _dp, _dp, _u8p]
         for f in (lib.oracle_fwd_f64, lib.oracle_bwd_f64, lib.oracle_fwd_bf16,
                   lib.oracle_bwd_dx_bf16, lib.oracle_param_grads_bf16,
-                  lib.oracle_residual_add_bf16, lib.oracle_add_bwd_dx_bf16):
+                  lib.oracle_residual_add_bf16, lib.oracle_add_bwd_dx_bf16,
+                  lib.oracle_e4m3_encode, lib.oracle_e4m3_decode, lib.oracle_fwd_fp8_bf16):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -225,6 +237,51 @@ class Oracle:
                                                _ptr(dx, _dp)), "oracle_add_bwd_dx_bf16")
         return dx
 
+    # ------------------------------------------------------------ FP8 (E4M3)
+    def e4m3_encode(self, v):
+        """Nearest E4M3 codes (uint8) of fp64 values: ties to even,
+        saturating at +-448, NaN -> 0x7F."""
+        v = _f64(v)
+        out = np.empty(v.shape, np.uint8)
+        _check(self.lib.oracle_e4m3_encode(_ptr(v, _dp), v.size, _ptr(out, _u8p)),
+               "oracle_e4m3_encode")
+        return out
+
+    def e4m3_decode(self, codes):
+        """Exact fp64 values of E4M3 codes (NaN for S.1111.111)."""
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, np.float64)
+        _check(self.lib.oracle_e4m3_decode(_ptr(c, _u8p), c.size, _ptr(out, _dp)),
+               "oracle_e4m3_decode")
+        return out
+
+    def fwd_fp8_bf16(self, x_bits, r_bits, gamma_bits, beta_bits, eps, mode, scaling,
+                     rows=None):
+        """Forward with E4M3 output (scaling FP8_ROW or FP8_MX), optionally on
+        h = bf16(x + r).  Returns dict y (fp64 [R, N]), q (uint8 [R, N]),
+        amax, scale (fp64 [R] or [R, N/32]) and, for MX, ebyte (uint8)."""
+        x_bits = _u16(x_bits)
+        M, N = x_bits.shape
+        r_bits = None if r_bits is None else _u16(r_bits)
+        gamma_bits = _u16(gamma_bits)
+        beta_bits = None if beta_bits is None else _u16(beta_bits)
+        r, R = _rows(rows, M)
+        ns = (R,) if scaling == FP8_ROW else (R, N // 32)
+        y = np.empty((R, N), np.float64)
+        q = np.empty((R, N), np.uint8)
+        amax = np.empty(ns, np.float64)
+        scale = np.empty(ns, np.float64)
+        ebyte = np.zeros(ns, np.uint8)
+        _check(self.lib.oracle_fwd_fp8_bf16(
+            _ptr(x_bits, _u16p), _ptr(r_bits, _u16p), _ptr(gamma_bits, _u16p),
+            _ptr(beta_bits, _u16p), M, N, float(eps), int(mode), int(scaling), _ptr(r, _i64p), R,
+            _ptr(y, _dp), _ptr(q, _u8p), _ptr(amax, _dp), _ptr(scale, _dp), _ptr(ebyte, _u8p)),
+            "oracle_fwd_fp8_bf16")
+        out = {"y": y, "q": q, "amax": amax, "scale": scale}
+        if scaling == FP8_MX:
+            out["ebyte"] = ebyte
+        return out
+
 
 def default() -> Oracle:
     global _default
@@ -264,6 +321,18 @@ def add_fwd_bf16(*a, **k):
 
 def add_bwd_dx_bf16(*a, **k):
     return default().add_bwd_dx_bf16(*a, **k)
+
+
+def e4m3_encode(*a, **k):
+    return default().e4m3_encode(*a, **k)
+
+
+def e4m3_decode(*a, **k):
+    return default().e4m3_decode(*a, **k)
+
+
+def fwd_fp8_bf16(*a, **k):
+    return default().fwd_fp8_bf16(*a, **k)
 
 
 def bf16_bits_to_f64(bits):

@@ -57,6 +57,27 @@
  *   y = norm(h)            (the definitions above, on the bf16 values of h)
  * and its backward adds the gradient dh that reaches h through the residual
  * path:  dx = dr = (norm backward of dy at h) + dh.
+ *
+ * FP8 output (the page "Otimizacao de Performance de GPU", introl.com, in
+ * its December 2025 update, reports FP8 training as production ready on
+ * Blackwell; it gives no format or scaling, so the plainest readings are
+ * used).  y is quantised to E4M3 (the OCP 8-bit floating point format
+ * "E4M3FN": 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, largest finite 448, subnormals m/8 * 2^-6)
+ * with round to nearest, ties to even, and saturation to +-448.  Two
+ * scalings:
+ *   per row     s_i = amax_i / 448, q_ij = E4M3(y_ij / s_i), computed as
+ *               (y_ij / amax_i) * 448 so that the row maximum maps to 448
+ *               exactly; a row of zeros has s_i = 1.
+ *   MX blocks   blocks of 32 consecutive columns share a power-of-two
+ *               scale X = 2^e, e = floor(log2(amax_block)) - 8 (8 being the
+ *               largest E4M3 exponent), clamped below at -127, stored as an
+ *               E8M0 byte e + 127; q = E4M3(y / X).  This is the conversion
+ *               rule of the OCP Microscaling Formats (MX) v1.0
+ *               specification, section 6.3; the scaled block maximum lies
+ *               in [256, 512), and values from 448 up saturate.
+ * The value rounded to E4M3 is formed in fp64: exactly for MX (division by
+ * a power of two), within 2^-52 relative for per-row scaling.
  */
 #include <math.h>
 #include <stdint.h>
@@ -371,4 +392,155 @@ int oracle_add_bwd_dx_bf16(const uint16_t *dy, const uint16_t *h,
             dx[k * N + j] += bf16_bits_to_double(dh[i * N + j]);
     }
     return 0;
+}
+
+/* ----------------------------------------------------------- FP8 (E4M3) */
+
+#define ORACLE_FP8_ROW 0
+#define ORACLE_FP8_MX 1
+#define E4M3_MAX 448.0
+#define MX_BLOCK 32
+
+/* Exact value of an E4M3 code (NaN for S.1111.111). */
+static double e4m3_value(uint8_t c)
+{
+    int sign = c >> 7;
+    int e = (c >> 3) & 15;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);              /* m/8 * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10);    /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to the real value v, ties to the even mantissa,
+ * magnitudes from 448 up saturate to 448; NaN gives 0x7F.  The scaled
+ * quantities below are exact (multiplication by powers of two), and
+ * nearbyint in the default rounding mode rounds half to even. */
+static uint8_t e4m3_code(double v)
+{
+    if (isnan(v))
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= E4M3_MAX)
+        return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal binade: spacing 2^-9; m == 8 is the smallest normal,
+         * whose code is also 8 */
+        double m = nearbyint(ldexp(a, 9));
+        return sign | (uint8_t)m;
+    }
+    int e2;
+    frexp(a, &e2);               /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;              /* floor(log2 a), in [-6, 8] */
+    double m = nearbyint(ldexp(a, 3 - e));   /* in [8, 16] */
+    if (m == 16.0) {
+        m = 8.0;
+        e += 1;
+    }
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+int oracle_e4m3_encode(const double *v, int64_t n, uint8_t *out)
+{
+    if ((!v || !out) && n > 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_code(v[i]);
+    return 0;
+}
+
+int oracle_e4m3_decode(const uint8_t *c, int64_t n, double *out)
+{
+    if ((!c || !out) && n > 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_value(c[i]);
+    return 0;
+}
+
+/* Forward with E4M3 output for the listed rows (row convention of
+ * oracle_fwd_bf16).  With r non-NULL the row is first h = bf16(x + r).
+ * Outputs per listed row k:
+ *   y[k*N + j]   the exact fp64 forward output;
+ *   q[k*N + j]   its E4M3 code under the scaling;
+ *   per row:     amax[k], scale[k] = amax/448 (1 for a zero row);
+ *   MX:          amax[k*nb + b], scale[k*nb + b] = 2^e, ebyte[k*nb + b] =
+ *                e + 127, with nb = N / 32 (N must be a multiple of 32).
+ * ebyte may be NULL; it is ignored for per-row scaling. */
+int oracle_fwd_fp8_bf16(const uint16_t *x, const uint16_t *r,
+                        const uint16_t *gamma, const uint16_t *beta,
+                        int64_t M, int64_t N, double eps, int mode,
+                        int scaling, const int64_t *rows, int64_t nrows,
+                        double *y, uint8_t *q, double *amax, double *scale,
+                        uint8_t *ebyte)
+{
+    if (!x || !gamma || !y || !q || !amax || !scale || M < 0 || N < 1 ||
+        nrows < 0 || (!rows && nrows != M))
+        return -1;
+    if (scaling != ORACLE_FP8_ROW && scaling != ORACLE_FP8_MX)
+        return -1;
+    if (scaling == ORACLE_FP8_MX && N % MX_BLOCK != 0)
+        return -1;
+    int64_t nb = N / MX_BLOCK;
+    uint16_t *hrow = r ? malloc(sizeof(uint16_t) * (size_t)N) : NULL;
+    if (r && !hrow)
+        return -2;
+    int rc = 0;
+    for (int64_t k = 0; k < nrows && rc == 0; ++k) {
+        int64_t i = rows ? rows[k] : k;
+        if (i < 0 || i >= M) {
+            rc = -1;
+            break;
+        }
+        const uint16_t *src = x + i * N;
+        if (r) {
+            residual_add_row(x + i * N, r + i * N, N, hrow);
+            src = hrow;
+        }
+        double *yk = y + k * N;
+        rc = oracle_fwd_bf16(src, gamma, beta, 1, N, eps, mode, NULL, 1, yk,
+                             NULL, NULL);
+        if (rc != 0)
+            break;
+        if (scaling == ORACLE_FP8_ROW) {
+            double am = 0.0;
+            for (int64_t j = 0; j < N; ++j)
+                if (fabs(yk[j]) > am)
+                    am = fabs(yk[j]);
+            amax[k] = am;
+            scale[k] = am > 0.0 ? am / E4M3_MAX : 1.0;
+            for (int64_t j = 0; j < N; ++j)
+                q[k * N + j] = e4m3_code(am > 0.0 ? (yk[j] / am) * E4M3_MAX : yk[j]);
+        } else {
+            for (int64_t b = 0; b < nb; ++b) {
+                const double *yb = yk + b * MX_BLOCK;
+                double am = 0.0;
+                for (int j = 0; j < MX_BLOCK; ++j)
+                    if (fabs(yb[j]) > am)
+                        am = fabs(yb[j]);
+                int e = -127;
+                if (am > 0.0) {
+                    int e2;
+                    frexp(am, &e2);
+                    e = (e2 - 1) - 8;
+                    if (e < -127)
+                        e = -127;
+                }
+                amax[k * nb + b] = am;
+                scale[k * nb + b] = ldexp(1.0, e);
+                if (ebyte)
+                    ebyte[k * nb + b] = (uint8_t)(e + 127);
+                for (int j = 0; j < MX_BLOCK; ++j)
+                    q[k * N + b * MX_BLOCK + j] = e4m3_code(ldexp(yb[j], -e));
+            }
+        }
+    }
+    free(hrow);
+    return rc;
 }

@@ -10,7 +10,11 @@ AssertionError when the oracle disagrees with:
   - an independent library routine: torch CPU float64 layer_norm /
     rms_norm and autograd;
   - symmetries (column permutation, LayerNorm shift invariance, scaling);
-  - exact bf16 widening (torch's own bf16 -> float64 conversion).
+  - exact bf16 widening (torch's own bf16 -> float64 conversion);
+  - the E4M3 format's closed-form code values and torch's float8_e4m3fn
+    conversion (an independent library) for the FP8 output, and the
+    defining properties of the two scalings (row maximum maps to 448; MX
+    block maximum lands in [256, 512) after a power-of-two scale).
 The definitions these facts follow are the LayerNorm/RMSNorm and
 backward-pass paragraphs of "PyTorch atinge desempenho SOTA em normalizacao
 com torch.compile" (matsubara.tec.br); eps inside the square root, the
@@ -386,6 +390,161 @@ def pin_add_norm_composition(orc):
         assert np.array_equal(dxs, dx[rows]), "row selection of the fused backward"
 
 
+FP8_ROW, FP8_MX = 0, 1
+
+
+def _e4m3_spacing(v):
+    """Distance between adjacent E4M3 values around |v| (< 448): 2^(e-3) in
+    binade e, 2^-9 in the subnormal range."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.exp2(np.maximum(e, -6.0) - 3.0)
+
+
+def _check_nearest(codes, v, orc, what):
+    """decode(codes) is a nearest E4M3 value of v (saturating at 448), with
+    the sign of v."""
+    d = orc.e4m3_decode(codes)
+    v = np.asarray(v, np.float64)
+    sat = np.abs(v) >= 448.0
+    assert np.all(np.abs(d[sat]) == 448.0), f"{what}: saturation"
+    ok = np.abs(d - v) <= 0.5 * _e4m3_spacing(v)
+    assert np.all(ok | sat), f"{what}: {int((~(ok | sat)).sum())} codes are not nearest"
+    wrong_sign = (v != 0) & (d != 0) & ((d < 0) != (v < 0))
+    assert not wrong_sign.any(), f"{what}: sign"
+
+
+def pin_e4m3_codes(orc):
+    """E4M3 codes: every value equals the format's closed form and torch's
+    float8_e4m3fn decoding; encoding inverts decoding, breaks ties to the
+    even mantissa, saturates at +-448 and agrees with torch's float32 ->
+    float8_e4m3fn conversion on in-range values."""
+    codes = np.arange(256, dtype=np.uint8)
+    d = orc.e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(d), nan) and nan.sum() == 2, "NaN codes"
+    assert np.array_equal(d[~nan], ref[~nan]), "E4M3 decoding differs from torch"
+    assert d[0x7E] == 448.0 and d[0x01] == 2.0 ** -9 and d[0x08] == 2.0 ** -6
+    assert d[0x38] == 1.0 and d[0x80] == 0.0 and np.signbit(d[0x80])
+    fin = codes[~nan]
+    assert np.array_equal(orc.e4m3_encode(d[~nan]), fin), "encode(decode(c)) != c"
+    pos = np.arange(0x00, 0x7E, dtype=np.int64)          # adjacent pairs (c, c+1)
+    lo, hi = d[pos], d[pos + 1]
+    mid = 0.5 * (lo + hi)
+    even = np.where(pos % 2 == 0, pos, pos + 1)
+    assert np.array_equal(orc.e4m3_encode(mid), even.astype(np.uint8)), "ties to even"
+    assert np.array_equal(orc.e4m3_encode(-mid), (even | 0x80).astype(np.uint8)), "negative ties"
+    below = mid - (hi - lo) * 2.0 ** -20
+    above = mid + (hi - lo) * 2.0 ** -20
+    assert np.array_equal(orc.e4m3_encode(below), pos.astype(np.uint8)), "below midpoint"
+    assert np.array_equal(orc.e4m3_encode(above), (pos + 1).astype(np.uint8)), "above midpoint"
+    big = np.array([448.0 * (1 + 2.0 ** -20), 464.0, 480.0, 1e30, np.inf])
+    assert np.all(orc.e4m3_encode(big) == 0x7E) and np.all(orc.e4m3_encode(-big) == 0xFE)
+    assert orc.e4m3_encode(np.array([np.nan]))[0] == 0x7F
+    g = torch.Generator().manual_seed(21)
+    mag = torch.exp2(torch.empty(20000, dtype=torch.float64).uniform_(-12.0, 8.77, generator=g))
+    sgn = torch.where(torch.rand(20000, generator=g) < 0.5, -1.0, 1.0).double()
+    v32 = (mag * sgn).float()
+    want = v32.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_encode(v32.double().numpy())
+    assert np.array_equal(got, want), "E4M3 encoding differs from torch's conversion"
+
+
+def _fp8_inputs(seed, M, N, block_scales=False):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, N, generator=g)
+    x[1] *= 50.0
+    x[2, 3] = 80.0                                       # outlier
+    gamma = 1 + 0.1 * torch.randn(N, generator=g)
+    if block_scales:
+        # very different block magnitudes, one block below 2^-119 (E8M0 clamp)
+        nb = N // 32
+        mult = torch.exp2(torch.tensor([(-8.0 + 5.0 * b) for b in range(nb)]))
+        mult[-1] = 2.0 ** -128
+        gamma = gamma * mult.repeat_interleave(32)
+    beta = 0.1 * torch.randn(N, generator=g)
+    if block_scales:
+        beta = beta * mult.repeat_interleave(32)
+    x = x.to(torch.bfloat16)
+    x[3] = 0                                             # zero row
+    return x, gamma.to(torch.bfloat16), beta.to(torch.bfloat16)
+
+
+def pin_fp8_row_scaling(orc):
+    """Per-row scaling: amax is the row's max |y| of the (already pinned)
+    forward, scale = amax / 448, the row maximum gets code +-448, every code
+    is a nearest E4M3 value of y / scale; a zero row has scale 1 and codes 0."""
+    M, N = 5, 64
+    x, gamma, beta = _fp8_inputs(31, M, N)
+    for mode in (RMS, LAYER):
+        bb = _bits(beta) if mode == LAYER else None
+        # RMS: row 3 is zero -> y = 0; LayerNorm: y = beta there (nonzero)
+        o = orc.fwd_fp8_bf16(_bits(x), None, _bits(gamma), bb, 1e-5, mode, FP8_ROW)
+        y, _, _ = orc.fwd_bf16(_bits(x), _bits(gamma), bb, 1e-5, mode)
+        assert np.array_equal(o["y"], y)
+        amax = np.abs(y).max(axis=1)
+        assert np.array_equal(o["amax"], amax)
+        nz = amax > 0
+        assert mode == LAYER or not nz[3], "zero row"
+        _close(o["scale"][nz], amax[nz] / 448.0, 1e-15, what="row scale")
+        assert np.all(o["scale"][~nz] == 1.0) and np.all(o["q"][~nz] & 0x7F == 0)
+        dq = orc.e4m3_decode(o["q"])
+        assert np.all(np.abs(dq[nz]).max(axis=1) == 448.0), "row max must map to 448"
+        v = (y[nz] / amax[nz][:, None]) * 448.0
+        _check_nearest(o["q"][nz], v, orc, f"row codes mode {mode}")
+
+
+def pin_fp8_mx_scaling(orc):
+    """MX scaling: each 32-column block gets X = 2^e with the block maximum
+    in [256, 512) after scaling (e clamped at -127 for tiny blocks, E8M0
+    byte e + 127), and every code is a nearest E4M3 value of y / X,
+    saturating at 448."""
+    M, N = 5, 256
+    x, gamma, beta = _fp8_inputs(32, M, N, block_scales=True)
+    nb = N // 32
+    for mode in (RMS, LAYER):
+        bb = _bits(beta) if mode == LAYER else None
+        o = orc.fwd_fp8_bf16(_bits(x), None, _bits(gamma), bb, 1e-5, mode, FP8_MX)
+        y, _, _ = orc.fwd_bf16(_bits(x), _bits(gamma), bb, 1e-5, mode)
+        yb = y.reshape(M, nb, 32)
+        amax = np.abs(yb).max(axis=2)
+        assert np.array_equal(o["amax"], amax)
+        X = o["scale"]
+        e = np.log2(X)
+        assert np.array_equal(e, np.round(e)), "MX scale must be a power of two"
+        assert np.array_equal(o["ebyte"].astype(np.int64), e.astype(np.int64) + 127)
+        live = amax > 0
+        s = amax[live] / X[live]
+        clamped = e[live] == -127
+        assert np.all(s < 512.0) and np.all((s >= 256.0) | clamped), "block max not in [256, 512)"
+        assert np.any(clamped), "the tiny block must hit the E8M0 clamp"
+        assert np.all(e[~live] == -127)
+        assert len(np.unique(e[0])) > 3, "scales must be per block"
+        v = (yb / X[:, :, None]).reshape(M, N)
+        _check_nearest(o["q"], v, orc, f"MX codes mode {mode}")
+
+
+def pin_fp8_residual_composition(orc):
+    """FP8 output of the fused residual form is the FP8 output of h."""
+    g = torch.Generator().manual_seed(33)
+    M, N = 4, 96
+    x = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    r = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(N, generator=g)).to(torch.bfloat16)
+    h = orc.residual_add_bf16(_bits(x), _bits(r))
+    for mode in (RMS, LAYER):
+        for sc in (FP8_ROW, FP8_MX):
+            a = orc.fwd_fp8_bf16(_bits(x), _bits(r), _bits(gamma), None, 1e-5, mode, sc)
+            b = orc.fwd_fp8_bf16(h, None, _bits(gamma), None, 1e-5, mode, sc)
+            for k in a:
+                assert np.array_equal(a[k], b[k]), k
+            rows = np.array([3, 1])
+            c = orc.fwd_fp8_bf16(_bits(x), _bits(r), _bits(gamma), None, 1e-5, mode, sc,
+                                 rows=rows)
+            assert np.array_equal(c["q"], a["q"][rows]) and np.array_equal(c["scale"], a["scale"][rows])
+
+
 ALL_PINS = [
     pin_rms_constant_row,
     pin_layer_constant_row,
@@ -400,4 +559,8 @@ ALL_PINS = [
     pin_bf16_entry_points,
     pin_residual_add_rounding,
     pin_add_norm_composition,
+    pin_e4m3_codes,
+    pin_fp8_row_scaling,
+    pin_fp8_mx_scaling,
+    pin_fp8_residual_composition,
 ]

@@ -37,6 +37,24 @@ MUTANTS = {
                                "dx[k * N + j] -= bf16_bits_to_double(dh[i * N + j]);"),
     "residual_dh_wrong_row": ("dx[k * N + j] += bf16_bits_to_double(dh[i * N + j]);",
                               "dx[k * N + j] += bf16_bits_to_double(dh[k * N + j]);"),
+    "e4m3_round_toward_zero": ("double m = nearbyint(ldexp(a, 3 - e));",
+                               "double m = trunc(ldexp(a, 3 - e));"),
+    "e4m3_subnormal_spacing": ("double m = nearbyint(ldexp(a, 9));",
+                               "double m = nearbyint(ldexp(a, 8));"),
+    "e4m3_decode_bias": ("v = ldexp((double)(8 + m), e - 10);",
+                         "v = ldexp((double)(8 + m), e - 11);"),
+    "e4m3_overflow_to_nan": ("if (a >= E4M3_MAX)\n        return sign | 0x7E;",
+                             "if (a >= E4M3_MAX)\n        return sign | 0x7F;"),
+    "fp8_row_max_240": ("e4m3_code(am > 0.0 ? (yk[j] / am) * E4M3_MAX : yk[j]);",
+                        "e4m3_code(am > 0.0 ? (yk[j] / am) * 240.0 : yk[j]);"),
+    "fp8_row_scale_inverted": ("scale[k] = am > 0.0 ? am / E4M3_MAX : 1.0;",
+                               "scale[k] = am > 0.0 ? E4M3_MAX / am : 1.0;"),
+    "mx_emax_7": ("e = (e2 - 1) - 8;", "e = (e2 - 1) - 7;"),
+    "mx_no_clamp": ("if (e < -127)\n                        e = -127;",
+                    "if (e < -227)\n                        e = -127;"),
+    "mx_scale_applied_inverted": ("e4m3_code(ldexp(yb[j], -e));", "e4m3_code(ldexp(yb[j], e));"),
+    "mx_amax_half_block": ("for (int j = 0; j < MX_BLOCK; ++j)\n                    if (fabs(yb[j]) > am)",
+                           "for (int j = 0; j < MX_BLOCK / 2; ++j)\n                    if (fabs(yb[j]) > am)"),
 }
 
 
