@@ -38,12 +38,17 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algo_bytes(M, N, mode, P, residual=False):
+def algo_bytes(M, N, mode, P, residual=False, fp8=None):
     """Minimal bytes of the forward and backward pass.  The fused residual
     variant adds r read and h written (4MN) to the forward and dh read (2MN)
-    to the backward, which reads h where the plain one reads x."""
+    to the backward, which reads h where the plain one reads x.  E4M3 output
+    (fp8 = 0 per-row scale, 1 MX blocks) writes MN code bytes instead of the
+    2MN of bf16 y, plus 4M scale bytes or MN/32 exponent bytes."""
     k = 2 if mode == 1 else 1
-    fwd = 4 * M * N + 2 * k * N + 4 * k * M + (4 * M * N if residual else 0)
+    y_bytes = 2 * M * N
+    if fp8 is not None:
+        y_bytes = M * N + (4 * M if fp8 == 0 else M * N // 32)
+    fwd = 2 * M * N + y_bytes + 2 * k * N + 4 * k * M + (4 * M * N if residual else 0)
     bwd = 6 * M * N + 2 * N + 4 * k * M + 4 * k * P * N + (2 * M * N if residual else 0)
     return fwd, bwd
 
@@ -279,7 +284,7 @@ class DirectStep:
     per-call Python tensor checks inside the timed loop).  With `r` and `dh`
     given it runs the fused residual add variant (norm_add_fwd/norm_add_bwd)."""
 
-    def __init__(self, gb, w, x, g, b, dy, stream, r=None, dh=None):
+    def __init__(self, gb, w, x, g, b, dy, stream, r=None, dh=None, fp8=None):
         import torch
 
         M, N = w.M, w.N
@@ -305,6 +310,14 @@ class DirectStep:
         ws = [p(self.ws), ctypes.c_size_t(self.ws.numel()), s]
         if fused:
             self.h = torch.empty_like(x)
+        if fp8 is not None:
+            self.q = torch.empty(M, N, dtype=torch.uint8, device=dev)
+            self.scale = (torch.empty(M, dtype=torch.float32, device=dev) if fp8 == 0 else
+                          torch.empty(M, N // 32, dtype=torch.uint8, device=dev))
+            fwd_fp8 = (L.norm_fwd_fp8, [p(x), p(r), p(g), p(b), M, N, eps, w.mode, int(fp8),
+                                        p(self.h) if fused else None, p(self.q),
+                                        p(self.scale), p(self.rstd), p(self.mean), s])
+        if fused:
             self.fwd_args = (L.norm_add_fwd, [p(x), p(r), p(g), p(b), M, N, eps, w.mode,
                                               p(self.h), p(self.y), p(self.rstd),
                                               p(self.mean), s])
@@ -316,6 +329,8 @@ class DirectStep:
                                           p(self.rstd), p(self.mean), s])
             self.bwd_args = (L.norm_bwd, [p(dy), p(x), p(g), p(self.rstd), p(self.mean), M,
                                           N, w.mode, p(self.dx), p(self.dg), p(self.db)] + ws)
+        if fp8 is not None:
+            self.fwd_args = fwd_fp8
 
     def fwd(self):
         f, a = self.fwd_args
@@ -502,7 +517,8 @@ def run_sweep(args):
             x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
         else:
             (x, g, b, dy), r, dh = wl.make_inputs(w, "cuda"), None, None
-        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh)
+        fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
+        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh, fp8=fp8)
         pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused)
         pb = gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
         res = {}
@@ -520,12 +536,12 @@ def run_sweep(args):
             res[name_] = e0.elapsed_time(e1) / args.steps
         if gb.norm_get_device_error() != 0:
             raise RuntimeError(f"device error word set on {name}")
-        fb, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"], residual=fused)
+        fb, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"], residual=fused, fp8=fp8)
         keep = ("cluster", "threads_per_row", "chunks_per_thread", "groups", "rows_per_group",
                 "stages", "grid", "exact")
         print(json.dumps({
             "workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
-            "fused_residual": fused, "fwd_us": 1e3 * res["fwd"], "bwd_us": 1e3 * res["bwd"],
+            "fused_residual": fused, "fp8": args.fp8 or None, "fwd_us": 1e3 * res["fwd"], "bwd_us": 1e3 * res["bwd"],
             "fwd_GBs": fb / res["fwd"] / 1e6, "bwd_GBs": bb / res["bwd"] / 1e6,
             "step_GBs": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6,
             "step_frac": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6 / peak,
@@ -554,6 +570,9 @@ def main():
                          "timings, one JSON line each (not the benchmark line)")
     ap.add_argument("--fused-residual", action="store_true",
                     help="with --sweep: time norm_add_fwd/norm_add_bwd (h = x + r fused in)")
+    ap.add_argument("--fp8", choices=["", "row", "mx"], default="",
+                    help="with --sweep: the forward writes E4M3 (norm_fwd_fp8) with per-row "
+                         "or MX block scaling")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

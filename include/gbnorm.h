@@ -164,6 +164,44 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h,
                            size_t workspace_bytes, norm_stream_t stream);
 
 /*
+ * FP8 output.  The page "Otimizacao de Performance de GPU" (introl.com,
+ * December 2025 update) reports FP8 training as production ready on
+ * Blackwell; the next consumer of a norm's output is usually a GEMM, which
+ * on this GPU reads E4M3 operands.  norm_fwd_fp8 computes y exactly as
+ * norm_fwd (or norm_add_fwd when r is given) and writes it as E4M3 codes
+ * (OCP 8-bit floating point E4M3FN: bias 7, 3 mantissa bits, largest finite
+ * 448, no infinities) rounded to nearest even with saturation, after one of
+ * two scalings:
+ *   NORM_FP8_ROW  per row: amax = max_j |y_ij| (fp32), codes of
+ *                 y * (448 / amax); scale[i] = amax / 448 (fp32 [M]) so that
+ *                 y ~= decode(q) * scale; a row of zeros has scale 1.
+ *   NORM_FP8_MX   per 32-column block (OCP Microscaling Formats v1.0, section
+ *                 6.3): X = 2^e, e = floor(log2 amax_block) - 8, clamped
+ *                 below at -127; codes of y / X (exact); scale holds the
+ *                 E8M0 byte e + 127 per block, row-major uint8 [M, N / 32].
+ *                 N must be a multiple of 32 (else NORM_ERR_SHAPE).
+ * Arguments:
+ *   x, gamma, beta, M, N, eps, mode, rstd, mean   as norm_fwd;
+ *   r     bf16 [M, N] residual, or NULL for a plain norm; with r, h (bf16
+ *         [M, N]) receives bf16(x + r) and the norm is taken of h, as
+ *         norm_add_fwd (h must be NULL when r is);
+ *   q     uint8 [M, N] E4M3 codes of y;
+ *   scale float [M] (NORM_FP8_ROW) or uint8 [M, N / 32] (NORM_FP8_MX).
+ * All pointers are device pointers owned by the caller, 16-byte aligned.
+ * Rows that do not fit one CTA (N above 16384 for LAYER, 24576 for RMS)
+ * return NORM_ERR_UNSUPPORTED; an unknown scaling returns NORM_ERR_ARG.
+ * One kernel on `stream`.  The backward pass of an FP8-output forward is
+ * norm_bwd / norm_add_bwd (it reads x or h and the saved rstd / mean).
+ */
+typedef enum { NORM_FP8_ROW = 0, NORM_FP8_MX = 1 } norm_fp8_scaling_t;
+
+norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma,
+                           const void *beta, int64_t M, int64_t N, float eps,
+                           norm_mode_t mode, norm_fp8_scaling_t scaling,
+                           void *h, void *q, void *scale, float *rstd,
+                           float *mean, norm_stream_t stream);
+
+/*
  * norm_plan -- the launch plan the library uses for one pass (backward = 0
  * for norm_fwd, 1 for norm_bwd, 2 for norm_add_fwd, 3 for norm_add_bwd) of
  * an [M, N] problem: how rows are split

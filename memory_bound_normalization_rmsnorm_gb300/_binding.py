@@ -98,6 +98,9 @@ def lib():
             L.norm_add_bwd_workspace_bytes.restype = ctypes.c_int
             L.norm_add_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int,
                                        _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            L.norm_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
+                                       ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp]
+            L.norm_fwd_fp8.restype = ctypes.c_int
             L.norm_add_bwd.restype = ctypes.c_int
             L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(Plan)]
@@ -258,6 +261,51 @@ def norm_add_fwd(x, r, gamma, beta=None, eps=1e-5, mode=RMS, *, h=None, y=None, 
     if st != 0:
         raise NormError(st, "norm_add_fwd")
     return h, y, rstd, mean
+
+
+FP8_ROW = 0
+FP8_MX = 1
+
+
+def norm_fwd_fp8(x, gamma, beta=None, eps=1e-5, mode=RMS, scaling=FP8_ROW, *, r=None, h=None,
+                 q=None, scale=None, rstd=None, mean=None, stream=None):
+    """Forward with E4M3 output (norm_fwd_fp8 in gbnorm.h).  With r given,
+    the norm is taken of h = bf16(x + r) (written to h).  Returns
+    (q, scale, rstd, mean, h): q uint8 [..., N] E4M3 codes; scale fp32
+    [...] (FP8_ROW) or uint8 [..., N // 32] E8M0 exponents (FP8_MX)."""
+    mode = int(mode)
+    scaling = int(scaling)
+    M, N = _rows(x)
+    dev = x.device
+    bf, f32, u8 = torch.bfloat16, torch.float32, torch.uint8
+    lead = x.shape[:-1]
+    _check_tensor(x, "x", bf, x.shape, dev)
+    _check_tensor(r, "r", bf, x.shape, dev)
+    _check_tensor(gamma, "gamma", bf, (N,), dev)
+    _check_tensor(beta, "beta", bf, (N,), dev)
+    if r is not None and h is None:
+        h = torch.empty_like(x)
+    if q is None:
+        q = torch.empty(x.shape, dtype=u8, device=dev)
+    sshape = lead if scaling == FP8_ROW else (*lead, N // 32)
+    sdtype = f32 if scaling == FP8_ROW else u8
+    if scale is None:
+        scale = torch.empty(sshape, dtype=sdtype, device=dev)
+    if rstd is None:
+        rstd = torch.empty(lead, dtype=f32, device=dev)
+    if mode == LAYER and mean is None:
+        mean = torch.empty(lead, dtype=f32, device=dev)
+    _check_tensor(h, "h", bf, x.shape, dev)
+    _check_tensor(q, "q", u8, x.shape, dev)
+    _check_tensor(scale, "scale", sdtype, sshape, dev)
+    _check_tensor(rstd, "rstd", f32, lead, dev)
+    _check_tensor(mean, "mean", f32, lead, dev)
+    st = lib().norm_fwd_fp8(_ptr(x), _ptr(r), _ptr(gamma), _ptr(beta), M, N, float(eps), mode,
+                            scaling, _ptr(h), _ptr(q), _ptr(scale), _ptr(rstd), _ptr(mean),
+                            _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_fwd_fp8")
+    return q, scale, rstd, mean, h
 
 
 def norm_add_bwd_workspace_bytes(M, N, mode=RMS) -> int:

@@ -685,6 +685,54 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h, const 
                        (mode == NORM_LAYER) ? dbeta : nullptr, s);
 }
 
+norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma, const void *beta,
+                           int64_t M, int64_t N, float eps, norm_mode_t mode,
+                           norm_fp8_scaling_t scaling, void *h, void *q, void *scale,
+                           float *rstd, float *mean, norm_stream_t stream) {
+  if (!x || !gamma || !q || !scale || !rstd) return NORM_ERR_NULL;
+  if (r && !h) return NORM_ERR_NULL;
+  if (!r && h) return NORM_ERR_ARG;
+  if (scaling != NORM_FP8_ROW && scaling != NORM_FP8_MX) return NORM_ERR_ARG;
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  if (scaling == NORM_FP8_MX && N % kMxBlock != 0) return NORM_ERR_SHAPE;
+  if (mode == NORM_RMS && (beta || mean)) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return NORM_ERR_ARG;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || !aligned16(scale) ||
+      !aligned16(rstd) || (r && !aligned16(r)) || (h && !aligned16(h)) ||
+      (beta && !aligned16(beta)) || (mean && !aligned16(mean)))
+    return NORM_ERR_ALIGN;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  const bool resid = r != nullptr;
+  Plan p;
+  if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p, resid)) != NORM_OK)
+    return st;
+  // E4M3 output: register-resident rows only; MX blocks need quads of lanes.
+  if (p.C != 1 || p.long_rows) return NORM_ERR_UNSUPPORTED;
+  if (scaling == NORM_FP8_MX && p.tpr % 4 != 0) return NORM_ERR_UNSUPPORTED;
+  const int out = scaling == NORM_FP8_ROW ? kOutFp8Row : kOutFp8Mx;
+  const void *fn = fwd_fp8_kernel_ptr(mode, p.K, p.exact, resid, out);
+  if (!fn) return NORM_ERR_UNSUPPORTED;
+  if ((st = prepare_function(dev, fn, d.smem_optin)) != NORM_OK) return st;
+  NormArgs a = base_args(p, M, static_cast<int>(N));
+  a.x = static_cast<const uint16_t *>(x);
+  a.res = static_cast<const uint16_t *>(r);
+  a.gamma = static_cast<const uint16_t *>(gamma);
+  a.beta = static_cast<const uint16_t *>(beta);
+  a.h = static_cast<uint16_t *>(h);
+  a.q = static_cast<uint8_t *>(q);
+  if (scaling == NORM_FP8_ROW) a.qscale = static_cast<float *>(scale);
+  else a.qexp = static_cast<uint8_t *>(scale);
+  a.rstd = rstd;
+  a.mean = mean;
+  a.err = d.err;
+  a.eps = eps;
+  return launch(fn, p, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, int sm_count,
                         int smem_optin_bytes, norm_plan_t *out) {
   if (!out) return NORM_ERR_NULL;

@@ -31,6 +31,9 @@ struct NormArgs {
   const uint16_t *res;    // fused residual: r (forward) or dh (backward), bf16 [M, N]
   uint16_t *h;            // fused residual forward: h = bf16(x + r), bf16 [M, N]
   uint16_t *out;          // y (forward) or dx (backward), bf16 [M, N]
+  uint8_t *q;             // FP8 forward: E4M3 codes of y [M, N]
+  float *qscale;          // FP8 forward, per-row scaling: dequantisation scale [M]
+  uint8_t *qexp;          // FP8 forward, MX scaling: E8M0 block exponents [M, N / 32]
   float *rstd;            // [M]: written by forward, read by backward
   float *mean;            // [M]: same, LayerNorm only
   float *ws;              // backward partial sums [P, N] (+ [P, N] for dbeta)
@@ -121,7 +124,16 @@ struct Plan {
 // Kernel entry points, by (mode, K, cluster, exact, fused residual).
 // Return nullptr when that combination is not compiled (the fused residual
 // variants exist without clusters only).
+// Forward output kinds: bf16 y, or E4M3 codes with a per-row fp32 scale, or
+// E4M3 codes with one E8M0 exponent per 32-column block (MX).
+constexpr int kOutBf16 = 0;
+constexpr int kOutFp8Row = 1;
+constexpr int kOutFp8Mx = 2;
+constexpr int kMxBlock = 32;
+
 const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
+// E4M3 output variants (no cluster variants); nullptr if not instantiated.
+const void *fwd_fp8_kernel_ptr(int mode, int K, bool exact, bool resid, int out);
 const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
 const void *reduce_kernel_ptr();
 // Long-row kernels (row slice re-read from shared memory), K in {4, 8}.

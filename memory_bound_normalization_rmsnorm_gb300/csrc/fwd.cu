@@ -1,293 +1,34 @@
-// fwd.cu -- forward RMSNorm / LayerNorm kernel (one fused pass per row:
-// row statistics, normalisation, scale and shift).
-//
-// Follows the forward-pass paragraph of "PyTorch atinge desempenho SOTA em
-// normalizacao com torch.compile" (a reduction along the contiguous
-// dimension followed by pointwise operations), fused into one kernel so
-// that HBM sees only the input and the output ("Kernel fusion elimina
-// gargalos de memoria" on the page "Otimizacao de Performance de GPU",
-// introl.com).
-//
-// Structure: a persistent grid; each CTA (or cluster of CTAs splitting the
-// columns) walks tiles of RT consecutive rows.  S tiles are kept in flight
-// with bulk asynchronous copies into a shared-memory ring, each stage
-// guarded by an mbarrier; the last warp to finish with a stage refills it,
-// so no warp ever waits for another outside its own row group.  Row groups
-// of `tpr` threads copy their row from shared memory into registers
-// (16-byte chunks, conflict free), compute the statistics with packed FP32
-// arithmetic, reduce (warp butterfly, then the warps of the group, then
-// the CTAs of the cluster through distributed shared memory), and write y
-// with 16-byte streaming stores.
-//
-// LayerNorm statistics are two-pass on the register-resident row: the mean
-// first, then the sum of squared deviations from it.
-#include "common.cuh"
-#include "ptx.cuh"
-#include "rowops.cuh"
-#include "tiles.cuh"
+// fwd.cu -- bf16-output instantiations of the forward kernel
+// (fwd_kernel.cuh): plain and fused-residual, per mode, chunks per thread,
+// cluster and exact-split variant.
+#include "fwd_kernel.cuh"
 
 namespace gbn {
 
 namespace {
 
-// EXACT: every CTA's slice is exactly K * tpr chunks and tpr >= 32, so no
-// chunk needs an ownership test and the warp butterfly is full width.
-// RESID: fused residual add -- the stage also holds r; h = bf16(x + r) (sum
-// in binary32, round to nearest even) is written out and normalised.
-template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID>
-__global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-  float *red = reinterpret_cast<float *>(smem + L.red_off);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
-  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
+template <int MODE, int K, bool CLUSTER, bool RESID>
+const void *pick_exact(bool e) {
+  return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, K, CLUSTER, true, RESID, kOutBf16>)
+           : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, K, CLUSTER, false, RESID, kOutBf16>);
+}
 
-  const int tid = threadIdx.x;
-  const int g = tid / a.tpr;
-  const int t = tid - g * a.tpr;
-  const int nwarps = blockDim.x >> 5;
-  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
-  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
-  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
-  const int col0 = crank * a.NS;
-  // Chunks this CTA owns (the last CTA of a cluster may own fewer).
-  const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
-
-  if (tid == 0) {
-    for (int s = 0; s < a.S; ++s) {
-      mbar_init(full + s, 1);
-      done_cnt[s] = 0;
-    }
-    if (CLUSTER) {
-      uint64_t *xb = xch_bars(smem, L, a.RT, a.C);
-      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  // Programmatic dependent launch: let the next kernel in the stream start
-  // its prologue as our CTAs retire, and touch no global memory before the
-  // previous kernel's writes are complete and visible.
-  grid_launch_dependents();
-  grid_dependency_wait();
-
-  // gamma as fp32 pairs (and beta packed) for this thread's chunks stay in
-  // registers for the whole kernel: the thread owns the same columns in
-  // every row.
-  float2 gf[K][4];
-  uint4 bv[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int c = t + k * a.tpr;
-    uint4 gv = make_uint4(0, 0, 0, 0);
-    bv[k] = make_uint4(0, 0, 0, 0);
-    if (c < nsc_me) {
-      gv = ld_global_nc_v4(a.gamma + col0 + c * 8);
-      if (MODE == kLayer && a.beta != nullptr) bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
-    }
-    chunk_to_f2(gv, gf[k]);
-  }
-
-  if (CLUSTER) cluster_sync(); else __syncthreads();
-
-  const uint64_t pol = l2_evict_first_policy();
-  if (tid == 0) {
-    for (int j = 0; j < a.S; ++j) {
-      const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_fwd_tile<CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
-    }
-  }
-
-  const float invN = a.invN;
-  int rpar = 0;
-  ClusterXch xch = make_xch(smem, L, a.RT, CLUSTER ? a.C : 1, crank);
-  // Stage s and its phase parity advance with the tile count (no division).
-  int s = 0;
-  uint32_t par = 0;
-  for (int64_t tile = cid; tile < a.ntiles; tile += ncl) {
-    mbar_wait(full + s, par, a.err, abort_flag);
-    const int64_t row0 = tile * a.RT;
-    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-    const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes;
-
-    for (int q = 0; q < a.rpg; ++q) {
-      const int r = g + q * a.G;
-      const bool active = r < nrows;
-      const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2 + t * 16;
-      float2 xf[K][4];
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const bool ok = active && (EXACT || t + k * a.tpr < nsc_me);
-        uint4 v = ok ? *reinterpret_cast<const uint4 *>(rowp + k * a.tpr * 16)
-                     : make_uint4(0, 0, 0, 0);
-        if (RESID) {
-          // h = bf16(x + r): add in binary32, round once, store h; the norm
-          // below works on the rounded values.
-          const uint4 rv = ok ? *reinterpret_cast<const uint4 *>(rowp + L.tensor_bytes +
-                                                                 k * a.tpr * 16)
-                              : make_uint4(0, 0, 0, 0);
-          float2 xs[4], rs_[4];
-          chunk_to_f2(v, xs);
-          chunk_to_f2(rv, rs_);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) xs[p] = add2(xs[p], rs_[p]);
-          v = f2_to_chunk(xs);
-          if (ok) st_global_cs_v4(a.h + (row0 + r) * a.N + col0 + (t + k * a.tpr) * 8, v);
-        }
-        chunk_to_f2(v, xf[k]);
-      }
-      float rs;
-      float2 nmu = splat2(0.f);
-      if (MODE == kLayer && EXACT) {
-        // This thread's (mean, M2) over its K*8 elements (two passes over
-        // registers), then one reduction round of equal-count merges.
-        constexpr float n_t = 8.f * K;
-        float2 a0 = splat2(0.f), a1 = splat2(0.f);
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          a0 = add2(a0, add2(xf[k][0], xf[k][1]));
-          a1 = add2(a1, add2(xf[k][2], xf[k][3]));
-        }
-        const float2 at = add2(a0, a1);
-        float m = (at.x + at.y) * (1.0f / n_t);
-        const float2 nm = splat2(-m);
-        float2 q0 = splat2(0.f), q1 = splat2(0.f);
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          const float2 d0 = add2(xf[k][0], nm), d1 = add2(xf[k][1], nm);
-          const float2 d2 = add2(xf[k][2], nm), d3 = add2(xf[k][3], nm);
-          q0 = fma2(d0, d0, fma2(d1, d1, q0));
-          q1 = fma2(d2, d2, fma2(d3, d3, q1));
-        }
-        const float2 qt = add2(q0, q1);
-        float q = qt.x + qt.y;
-        group_meanvar(m, q, n_t, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_meanvar(m, q, static_cast<float>(a.NS), r, t, xch, a.err, abort_flag);
-        nmu = splat2(-m);
-        rs = rsqrtf(q * invN + a.eps);
-        if (active && t == 0 && crank == 0) a.mean[row0 + r] = m;
-      } else if (MODE == kLayer) {
-        // Ragged slices: exact two-pass, the mean first, then the sum of
-        // squared deviations over owned chunks only.
-        float2 acc = splat2(0.f);
-#pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-          for (int p = 0; p < 4; ++p) acc = add2(acc, xf[k][p]);
-        float v1[1] = {acc.x + acc.y};
-        group_sum<1, EXACT>(v1, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(v1, r, t, xch, a.err, abort_flag);
-        const float mu = v1[0] * invN;
-        nmu = splat2(-mu);
-        float2 q2 = splat2(0.f);
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          if (EXACT || t + k * a.tpr < nsc_me) {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const float2 d = add2(xf[k][p], nmu);
-              q2 = fma2(d, d, q2);
-            }
-          }
-        }
-        float v2[1] = {q2.x + q2.y};
-        group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(v2, r, t, xch, a.err, abort_flag);
-        rs = rsqrtf(v2[0] * invN + a.eps);
-        if (active && t == 0 && crank == 0) a.mean[row0 + r] = mu;
-      } else {
-        float2 q0 = splat2(0.f), q1 = splat2(0.f);
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          q0 = fma2(xf[k][0], xf[k][0], fma2(xf[k][1], xf[k][1], q0));
-          q1 = fma2(xf[k][2], xf[k][2], fma2(xf[k][3], xf[k][3], q1));
-        }
-        const float2 qt = add2(q0, q1);
-        float v2[1] = {qt.x + qt.y};
-        group_sum<1, EXACT>(v2, a.tpr, g, a.G, t, red, rpar);
-        if (CLUSTER) cluster_sum<1>(v2, r, t, xch, a.err, abort_flag);
-        rs = rsqrtf(v2[0] * invN + a.eps);
-      }
-
-      if (active) {
-        const float2 rs2 = splat2(rs);
-        uint16_t *yrow = a.out + (row0 + r) * a.N + col0 + t * 8;
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          if (EXACT || t + k * a.tpr < nsc_me) {
-            float2 o[4];
-            float2 bf[4];
-            if (MODE == kLayer) chunk_to_f2(bv[k], bf);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const float2 xh = mul2(MODE == kLayer ? add2(xf[k][p], nmu) : xf[k][p], rs2);
-              o[p] = (MODE == kLayer) ? fma2(xh, gf[k][p], bf[p]) : mul2(xh, gf[k][p]);
-            }
-            st_global_cs_v4(yrow + k * a.tpr * 8, f2_to_chunk(o));
-          }
-        }
-        if (t == 0 && crank == 0) a.rstd[row0 + r] = rs;
-      }
-    }
-
-    // This warp is done with the stage; the last warp to finish refills it
-    // with the tile S steps ahead.
-    if (last_warp_done(done_cnt, s, nwarps) && (tid & 31) == 0) {
-      const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
-      if (next < a.ntiles) {
-        fence_proxy_async_smem();
-        issue_fwd_tile<CLUSTER, RESID>(a, L, smem, next, s, col0, nsc_me, pol);
-      }
-    }
-    if (++s == a.S) {
-      s = 0;
-      par ^= 1u;
-    }
-  }
-  // No CTA may leave while a peer could still read its shared memory.
-  if (CLUSTER) cluster_sync();
+template <int MODE, int K, bool CLUSTER>
+const void *pick_variant(bool e, bool r) {
+  if (r) return CLUSTER ? nullptr : pick_exact<MODE, K, false, true>(e);  // no cluster variants
+  return pick_exact<MODE, K, CLUSTER, false>(e);
 }
 
 template <int MODE, bool CLUSTER>
 const void *pick_fwd(int K, bool e, bool r) {
-  if (r && CLUSTER) return nullptr;  // fused residual: no cluster variants
   switch (K) {
-    case 1:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 1, CLUSTER, false, false>);
-    case 2:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 2, CLUSTER, false, false>);
-    case 3:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 3, CLUSTER, false, false>);
-    case 4:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 4, CLUSTER, false, false>);
-    case 5:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 5, CLUSTER, false, false>);
-    case 6:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 6, CLUSTER, false, false>);
-    case 8:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, 8, CLUSTER, false, false>);
+    case 1: return pick_variant<MODE, 1, CLUSTER>(e, r);
+    case 2: return pick_variant<MODE, 2, CLUSTER>(e, r);
+    case 3: return pick_variant<MODE, 3, CLUSTER>(e, r);
+    case 4: return pick_variant<MODE, 4, CLUSTER>(e, r);
+    case 5: return pick_variant<MODE, 5, CLUSTER>(e, r);
+    case 6: return pick_variant<MODE, 6, CLUSTER>(e, r);
+    case 8: return pick_variant<MODE, 8, CLUSTER>(e, r);
     default: return nullptr;
   }
 }

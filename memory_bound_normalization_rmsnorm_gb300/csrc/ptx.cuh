@@ -194,6 +194,19 @@ __device__ __forceinline__ void st_global_cs_v4(void *p, uint4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ void st_global_cs_v2(void *p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y)
+               : "memory");
+}
+
+// Two fp32 values to two E4M3 codes (round to nearest even, saturating to
+// +-448), packed with `lo` in the low byte (the lower address).
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -79,6 +79,28 @@ __device__ __forceinline__ void group_sum(float (&v)[NV], int tpr, int g, int G,
   }
 }
 
+// Maximum of one non-negative value over the row group (same structure
+// and calling rule as group_sum).  max is exact, so the order is free.
+template <bool WIDE>
+__device__ __forceinline__ float group_max(float v, int tpr, int g, int G, int t, float *red,
+                                           int &rpar) {
+  const int width = WIDE ? 32 : (tpr < 32 ? tpr : 32);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    if (WIDE || o < width) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (tpr > 32) {
+    const int W = tpr >> 5;
+    float *slot = red + (static_cast<size_t>(rpar * G + g) * W) * 4;
+    if ((threadIdx.x & 31) == 0) slot[(t >> 5) * 4] = v;
+    named_bar_sync(1 + g, tpr);
+    v = slot[0];
+#pragma unroll 4
+    for (int w = 1; w < W; ++w) v = fmaxf(v, slot[w * 4]);
+    rpar ^= 1;
+  }
+  return v;
+}
+
 // ------------------------------------------- (mean, M2) of equal counts
 // Parallel variance merge of two partials that cover the same number of
 // elements n_each: mean = (ma + mb) / 2, M2 = M2a + M2b + (mb - ma)^2 *

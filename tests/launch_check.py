@@ -125,6 +125,36 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     return True
 
 
+def check_fp8_plan(p, M, N, scaling):
+    """The E4M3-output forward on plan `p` (a norm_plan dict of the plain or
+    fused-residual forward): codes and scales stay in their buffers and, for
+    MX scaling, every 32-column block is 4 consecutive chunks held by 4
+    consecutive lanes of one row group, owned (or not) together."""
+    C, tpr, K = p["cluster"], p["threads_per_row"], p["chunks_per_thread"]
+    nc = N // 8
+    assert C == 1 and not p["long_rows"], "E4M3 output is register-resident only"
+    for t in range(tpr):
+        for k in range(K):
+            c = t + k * tpr
+            if c < nc:
+                assert c * 8 + 8 <= N                   # 8 code bytes per chunk
+    assert (M - 1) * N + N <= M * N
+    if scaling == "mx":
+        assert N % 32 == 0 and tpr % 4 == 0
+        nb = N // 32
+        for t0 in range(0, tpr, 4):
+            for k in range(K):
+                cs = [t0 + i + k * tpr for i in range(4)]
+                own = [c < nc for c in cs]
+                assert all(own) or not any(own), "a block is split between owners"
+                if own[0]:
+                    assert cs[0] % 4 == 0 and cs == list(range(cs[0], cs[0] + 4))
+                    assert cs[0] // 4 < nb                # E8M0 byte inside the row
+        # a quad never straddles a group: groups start at multiples of tpr
+        assert (p["groups"] * tpr) % 4 == 0
+    return True
+
+
 def check_reduce(P, N, nparts):
     """Reduce kernel: grid (ceil(N/128), nparts), 16 warps, lane owns 4
     columns, warp w sums p in [P*w/16, P*(w+1)/16)."""

@@ -65,6 +65,34 @@ def test_fwd_validation_codes():
     assert call(mode=1, m=F + 4) == 3
 
 
+def test_fp8_validation_codes():
+    f = gb.lib().norm_fwd_fp8
+    ok = dict(x=F, res=None, g=F, b=None, M=4, N=64, eps=1e-5, mode=0, sc=0, h=None, q=F,
+              s=F, r=F, m=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["res"], a["g"], a["b"], a["M"], a["N"], a["eps"], a["mode"], a["sc"],
+                 a["h"], a["q"], a["s"], a["r"], a["m"], None)
+
+    assert call(x=None) == 1
+    assert call(q=None) == 1
+    assert call(s=None) == 1
+    assert call(r=None) == 1
+    assert call(res=F) == 1            # residual without h
+    assert call(h=F) == 9              # h without residual
+    assert call(sc=2) == 9             # unknown scaling
+    assert call(sc=1, N=48) == 2       # MX needs N % 32 == 0
+    assert call(N=12) == 2
+    assert call(mode=2) == 4
+    assert call(b=F) == 4
+    assert call(mode=1) == 4           # LayerNorm without mean
+    assert call(eps=-1.0) == 9
+    assert call(q=F + 8) == 3
+    assert call(s=F + 4) == 3
+    assert call(res=F + 2, h=F) == 3
+
+
 def test_bwd_validation_codes():
     f = gb.lib().norm_bwd
     ok = dict(dy=F, x=F, g=F, r=F, m=None, M=4, N=16, mode=0, dx=F, dg=F, db=None, ws=F,

@@ -52,6 +52,26 @@ def test_fused_residual_plans_in_bounds(backward):
     assert n > 200
 
 
+@pytest.mark.parametrize("residual", [False, True])
+def test_fp8_plans_in_bounds(residual):
+    """E4M3 output uses the forward plans: every default plan that fits one
+    CTA satisfies the MX block rule when N is a multiple of 32."""
+    n = 0
+    for M, N, mode in _cases():
+        try:
+            p = gb.norm_plan(M, N, mode, False, SMS, OPTIN, residual=residual)
+        except gb.NormError as e:
+            assert residual and e.status == 6
+            continue
+        if p["cluster"] != 1 or p["long_rows"]:
+            continue  # refused by norm_fwd_fp8 (NORM_ERR_UNSUPPORTED)
+        launch_check.check_fp8_plan(p, M, N, "row")
+        if N % 32 == 0:
+            launch_check.check_fp8_plan(p, M, N, "mx")
+        n += 1
+    assert n > 200
+
+
 def test_plan_rejects_unsupported():
     with pytest.raises(gb.NormError):
         gb.norm_plan(4, 12, 0, False, SMS, OPTIN)  # N % 8 != 0
