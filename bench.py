@@ -513,13 +513,13 @@ def run_sweep(args):
     for name in names:
         w = wl.WORKLOADS[name]
         fused = args.fused_residual
+        fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
         if fused:
             x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
         else:
             (x, g, b, dy), r, dh = wl.make_inputs(w, "cuda"), None, None
-        fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
         step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh, fp8=fp8)
-        pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused)
+        pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused, fp8=fp8 is not None)
         pb = gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
         res = {}
         for name_, fn in (("fwd", step.fwd), ("bwd", step.bwd)):

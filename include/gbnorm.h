@@ -174,7 +174,8 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h,
  * two scalings:
  *   NORM_FP8_ROW  per row: amax = max_j |y_ij| (fp32), codes of
  *                 y * (448 / amax); scale[i] = amax / 448 (fp32 [M]) so that
- *                 y ~= decode(q) * scale; a row of zeros has scale 1.
+ *                 y ~= decode(q) * scale; a row of zeros has scale 1.  Both
+ *                 quotients are formed in fp32 within 2 ulp.
  *   NORM_FP8_MX   per 32-column block (OCP Microscaling Formats v1.0, section
  *                 6.3): X = 2^e, e = floor(log2 amax_block) - 8, clamped
  *                 below at -127; codes of y / X (exact); scale holds the
@@ -203,7 +204,8 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma,
 
 /*
  * norm_plan -- the launch plan the library uses for one pass (backward = 0
- * for norm_fwd, 1 for norm_bwd, 2 for norm_add_fwd, 3 for norm_add_bwd) of
+ * for norm_fwd, 1 for norm_bwd, 2 for norm_add_fwd, 3 for norm_add_bwd, 4
+ * for norm_fwd_fp8 without and 6 with a residual) of
  * an [M, N] problem: how rows are split
  * across threads, CTAs and clusters, and how many tiles are kept in flight.
  * With sm_count <= 0 it describes the CURRENT device (occupancy queried
@@ -234,6 +236,10 @@ typedef struct {
     int32_t long_rows;         /* 1: long-row kernels (the row slice is read
                                   twice from shared memory instead of being
                                   held in registers) */
+    int32_t params_in_smem;    /* forward only: number of bf16 parameter
+                                  vectors (gamma, and beta for LAYER) staged
+                                  in shared memory and read per row instead
+                                  of being held in registers; 0 if none */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

@@ -104,7 +104,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Optional plan override for tuning sweeps: GBNORM_PLAN="C=2,tpr=256,rpg=1,S=4"
 // (any subset).  Fields left out keep the heuristic's choice.
 struct Override {
-  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, occ = 0;
+  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, occ = 0, gsm = -1;
   bool any = false;
 };
 
@@ -127,6 +127,7 @@ Override read_override() {
     else if (!std::strcmp(key, "long")) o.lng = val;
     else if (!std::strcmp(key, "K")) o.K = val;
     else if (!std::strcmp(key, "occ")) o.occ = val;
+    else if (!std::strcmp(key, "gsm")) o.gsm = val;
     o.any = true;
   }
   return o;
@@ -146,12 +147,14 @@ struct TunedPlan {
   int bwd;   // 0 forward, 1 backward
   int N;
   int tpr, rpg, S;  // 0 = heuristic's choice
+  int gsm = 0;      // forward: gamma/beta staged in shared memory, 8 chunks per thread
 };
 constexpr TunedPlan kTuned[] = {
     {kRMS, 0, 256, 32, 2, 3},     {kRMS, 0, 512, 32, 1, 3},    {kRMS, 0, 768, 32, 0, 3},
     {kRMS, 0, 1024, 64, 1, 0},    {kRMS, 0, 2048, 128, 1, 0},  {kRMS, 0, 3072, 192, 1, 3},
     {kRMS, 0, 5120, 160, 0, 3},   {kRMS, 0, 8192, 256, 0, 3},  {kRMS, 0, 16384, 512, 0, 3},
-    {kLayer, 0, 2048, 64, 0, 3},
+    {kLayer, 0, 2048, 64, 0, 3},  {kLayer, 0, 3072, 0, 0, 0, 1}, {kLayer, 0, 5120, 0, 0, 0, 1},
+    {kLayer, 0, 8192, 0, 0, 0, 1},
     {kRMS, 1, 256, 32, 2, 5},     {kRMS, 1, 512, 64, 0, 0},    {kRMS, 1, 768, 64, 4, 0},
     {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 5120, 256, 2, 0},
     {kLayer, 1, 3072, 192, 4, 0}, {kLayer, 1, 5120, 256, 2, 0},
@@ -172,8 +175,8 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
   const int budget = (p.occ == 2) ? (smem_optin + 1024) / 2 - 1024 : smem_optin - 1024;
   int S = 0;
   for (;;) {
-    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C);
-    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, p.tpr, ntensors, bwd, C);
+    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C, p.nparams);
+    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, p.tpr, ntensors, bwd, C, p.nparams);
     const int per_stage = static_cast<int>(L2.total - L1.total);
     const int fixed = static_cast<int>(L1.total) - per_stage;
     S = (budget - fixed) / per_stage;
@@ -190,7 +193,7 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
   p.S = S;
   p.threads = G * p.tpr;
   if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
-  const SmemLayout L = make_layout(p.RT, p.NS, S, G, p.tpr, ntensors, bwd, C);
+  const SmemLayout L = make_layout(p.RT, p.NS, S, G, p.tpr, ntensors, bwd, C, p.nparams);
   if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
   if (L.stage_bytes >= (1u << 20)) return NORM_ERR_UNSUPPORTED;
   if (bwd && static_cast<int64_t>(2) * G * p.NS * 4 > static_cast<int64_t>(S) * L.stage_bytes)
@@ -246,14 +249,17 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
 // Pure host arithmetic (no CUDA call).  `bwd` selects the backward kernel
 // (two tensors per stage, at most kMaxKBwd chunks per thread).
 norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
-                         const Override &ov_in, Plan *out, bool resid = false) {
+                         const Override &ov_in, Plan *out, bool resid = false,
+                         bool fp8 = false) {
   Override ov = ov_in;
-  if (!ov.any && !resid) {
+  bool tuned_gsm = false;
+  if (!ov.any && !resid && !fp8) {
     for (const TunedPlan &tp : kTuned) {
       if (tp.mode == mode && tp.bwd == (bwd ? 1 : 0) && tp.N == N) {
         ov.tpr = tp.tpr;
         ov.rpg = tp.rpg;
         ov.S = tp.S;
+        tuned_gsm = tp.gsm != 0;
         break;
       }
     }
@@ -299,24 +305,41 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   const bool even = (nc % C) == 0;
   int tpr = 0, K = 0;
   bool exact = false;
-  auto try_exact = [&](int k) {
+  auto try_exact = [&](int k, bool gsm) {
     if (!even || p.nsc % k || (p.nsc / k) % 32 || p.nsc / k > kMaxThreads) return false;
     if (!(bwd ? bwd_kernel_ptr(mode, k, C > 1, true, resid)
-              : fwd_kernel_ptr(mode, k, C > 1, true, resid)))
+              : fwd_kernel_ptr(mode, k, C > 1, true, resid, gsm)))
       return false;
     tpr = p.nsc / k;
     K = k;
     exact = true;
     return true;
   };
-  if (ov.tpr) {
+  // Forward with gamma/beta in shared memory, 8 chunks per thread, exact
+  // split: forced by the override, or preferred for E4M3 output (whose
+  // per-row amax costs a reduction round that fewer, fuller warps per row
+  // amortise) and for tuned shapes; otherwise the register-resident plan.
+  bool want_gsm = !bwd && (ov.gsm == 1 || (ov.gsm == -1 && (fp8 || tuned_gsm)));
+  if (want_gsm && !ov.tpr) {
+    bool found = false;
+    for (int k : {8, 6, 5}) {
+      if (!found) found = try_exact(k, true);
+    }
+    if (!found) {
+      if (ov.gsm == 1) return NORM_ERR_UNSUPPORTED;
+      want_gsm = false;
+    }
+  }
+  if (want_gsm && !ov.tpr) {
+    // K and tpr set by try_exact
+  } else if (ov.tpr) {
     tpr = ov.tpr;
     K = round_k(ceil_div(p.nsc, tpr), bwd);
     exact = even && tpr % 32 == 0 && K * tpr == p.nsc;
   } else {
     bool found = false;
-    for (int k = kpref; k >= 1 && !found; --k) found = try_exact(k);
-    for (int k = kpref + 1; k <= klim && !found; ++k) found = try_exact(k);
+    for (int k = kpref; k >= 1 && !found; --k) found = try_exact(k, false);
+    for (int k = kpref + 1; k <= klim && !found; ++k) found = try_exact(k, false);
     if (!found) {
       if (p.nsc <= 32) tpr = pow2ceil(p.nsc);
       else tpr = std::min(kMaxThreads, std::max(32, pow2ceil(ceil_div(p.nsc, kpref))));
@@ -329,6 +352,11 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   p.tpr = tpr;
   p.K = K;
   p.exact = exact;
+  if (want_gsm) {
+    if (!exact || (K != 8 && K != 6 && K != 5) || C != 1) return NORM_ERR_UNSUPPORTED;
+    p.gsm = true;
+    p.nparams = mode == kLayer ? 2 : 1;
+  }
 
   int G = kMaxThreads / tpr;
   if (tpr > 32) G = std::min(G, 8);
@@ -346,7 +374,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
   if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
-             : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid);
+             : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm);
 }
 
 void set_grid(Plan &p, int64_t resident_clusters) {
@@ -358,9 +386,10 @@ void set_grid(Plan &p, int64_t resident_clusters) {
 // Full plan on the current device: shape part plus the occupancy-derived
 // grid (persistent: as many CTAs or clusters as can be resident at once).
 norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_t M, int N,
-                        Plan *out, bool resid = false) {
+                        Plan *out, bool resid = false, bool fp8 = false) {
   const Override ov = read_override();
-  const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, resid ? 1 : 0);
+  const auto key =
+      std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, (resid ? 1 : 0) | (fp8 ? 2 : 0));
   if (!ov.any) {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
@@ -370,7 +399,7 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
     }
   }
   Plan p;
-  norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p, resid);
+  norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p, resid, fp8);
   if (st != NORM_OK) return st;
 
   const void *fn = kernel_for(p, mode, bwd);
@@ -708,13 +737,13 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma, cons
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
   const bool resid = r != nullptr;
   Plan p;
-  if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p, resid)) != NORM_OK)
+  if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p, resid, true)) != NORM_OK)
     return st;
   // E4M3 output: register-resident rows only; MX blocks need quads of lanes.
   if (p.C != 1 || p.long_rows) return NORM_ERR_UNSUPPORTED;
   if (scaling == NORM_FP8_MX && p.tpr % 4 != 0) return NORM_ERR_UNSUPPORTED;
   const int out = scaling == NORM_FP8_ROW ? kOutFp8Row : kOutFp8Mx;
-  const void *fn = fwd_fp8_kernel_ptr(mode, p.K, p.exact, resid, out);
+  const void *fn = fwd_fp8_kernel_ptr(mode, p.K, p.exact, resid, out, p.gsm);
   if (!fn) return NORM_ERR_UNSUPPORTED;
   if ((st = prepare_function(dev, fn, d.smem_optin)) != NORM_OK) return st;
   NormArgs a = base_args(p, M, static_cast<int>(N));
@@ -738,14 +767,16 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   if (!out) return NORM_ERR_NULL;
   norm_status_t st = check_common(M, N, mode);
   if (st != NORM_OK) return st;
-  if (backward & ~3) return NORM_ERR_ARG;
+  if (backward & ~7) return NORM_ERR_ARG;
   const bool bwd = (backward & 1) != 0;
   const bool resid = (backward & 2) != 0;
+  const bool fp8 = (backward & 4) != 0;
+  if (fp8 && bwd) return NORM_ERR_ARG;
   Plan p;
   if (sm_count > 0) {
     if (smem_optin_bytes <= 0) return NORM_ERR_ARG;
     if ((st = shape_plan(mode, bwd, M, static_cast<int>(N), smem_optin_bytes, read_override(),
-                         &p, resid)) != NORM_OK)
+                         &p, resid, fp8)) != NORM_OK)
       return st;
     set_grid(p, static_cast<int64_t>(sm_count) * p.occ / p.C);
     if (p.grid < 1) return NORM_ERR_UNSUPPORTED;
@@ -753,7 +784,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
     DeviceInfo d;
     int dev = 0;
     if ((st = device_info(&d, &dev)) != NORM_OK) return st;
-    if ((st = make_plan(d, dev, mode, bwd, M, static_cast<int>(N), &p, resid)) != NORM_OK)
+    if ((st = make_plan(d, dev, mode, bwd, M, static_cast<int>(N), &p, resid, fp8)) != NORM_OK)
       return st;
   }
   out->cluster = p.C;
@@ -771,6 +802,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   out->partials = p.P;
   out->exact = p.exact ? 1 : 0;
   out->long_rows = p.long_rows ? 1 : 0;
+  out->params_in_smem = p.nparams;
   return NORM_OK;
 }
 

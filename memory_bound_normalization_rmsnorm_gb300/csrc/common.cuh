@@ -58,6 +58,7 @@ struct NormArgs {
 struct SmemLayout {
   uint32_t tensor_bytes;  // one tensor's share of a stage: RT * NS * 2
   uint32_t stage_bytes;   // ntensors * tensor_bytes
+  uint32_t par_off;       // forward with gamma (and beta) staged: bf16 [NS] each
   uint32_t stats_off;     // backward: [S][RT][2] floats (rstd, mean)
   uint32_t red_off;       // [2][G][W][4] floats, cross-warp group partials
                           // (W = tpr / 32; only when tpr > 32)
@@ -76,14 +77,18 @@ __host__ __device__ inline uint32_t align16(uint32_t v) {
   return (v + 15u) & ~15u;
 }
 
-// C: CTAs per cluster (1: no cluster exchange region).
+// C: CTAs per cluster (1: no cluster exchange region).  nparams: bf16
+// parameter vectors of NS columns staged in shared memory (0, or 1 gamma /
+// 2 gamma and beta for the forward kernels that read them per row).
 __host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
                                                   int tpr, int ntensors,
-                                                  bool stats, int C) {
+                                                  bool stats, int C, int nparams = 0) {
   SmemLayout L;
   L.tensor_bytes = static_cast<uint32_t>(RT) * static_cast<uint32_t>(NS) * 2u;
   L.stage_bytes = L.tensor_bytes * static_cast<uint32_t>(ntensors);
   uint32_t off = L.stage_bytes * static_cast<uint32_t>(S);
+  L.par_off = off;
+  off = align16(off + static_cast<uint32_t>(nparams) * static_cast<uint32_t>(NS) * 2u);
   L.stats_off = off;
   if (stats) off = align16(off + static_cast<uint32_t>(S * RT * 2) * 4u);
   L.red_off = off;
@@ -110,6 +115,8 @@ struct Plan {
   bool long_rows = false; // long-row kernels (row re-read from the stage)
   int occ = 1;            // CTAs per SM the kernel is compiled for
   bool resid = false;     // fused residual add variant
+  bool gsm = false;       // forward: gamma/beta read per row from shared memory
+  int nparams = 0;        // bf16 vectors staged in shared memory (gsm: 1 RMS, 2 LN)
   int G = 0;       // groups per CTA
   int rpg = 1;     // rows per group per tile
   int RT = 0;      // rows per tile
@@ -131,9 +138,17 @@ constexpr int kOutFp8Row = 1;
 constexpr int kOutFp8Mx = 2;
 constexpr int kMxBlock = 32;
 
-const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
+// gsm: gamma (and beta) staged in shared memory and read per row, which frees
+// the registers that hold them otherwise (exact splits, no cluster, K in
+// {5, 6, 8}; see fwd_gsm_kernel_ptr).
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false,
+                           bool gsm = false);
 // E4M3 output variants (no cluster variants); nullptr if not instantiated.
-const void *fwd_fp8_kernel_ptr(int mode, int K, bool exact, bool resid, int out);
+const void *fwd_fp8_kernel_ptr(int mode, int K, bool exact, bool resid, int out,
+                               bool gsm = false);
+// Forward kernels with gamma/beta staged in shared memory (exact splits, no
+// cluster), K in {5, 6, 8}, any output kind; nullptr otherwise.
+const void *fwd_gsm_kernel_ptr(int mode, int K, bool resid, int out);
 const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
 const void *reduce_kernel_ptr();
 // Long-row kernels (row slice re-read from shared memory), K in {4, 8}.

@@ -9,8 +9,10 @@ namespace {
 
 template <int MODE, int K, bool CLUSTER, bool RESID>
 const void *pick_exact(bool e) {
-  return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, K, CLUSTER, true, RESID, kOutBf16>)
-           : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, K, CLUSTER, false, RESID, kOutBf16>);
+  return e ? reinterpret_cast<const void *>(
+                 &norm_fwd_kernel<MODE, K, CLUSTER, true, RESID, kOutBf16, false>)
+           : reinterpret_cast<const void *>(
+                 &norm_fwd_kernel<MODE, K, CLUSTER, false, RESID, kOutBf16, false>);
 }
 
 template <int MODE, int K, bool CLUSTER>
@@ -35,7 +37,8 @@ const void *pick_fwd(int K, bool e, bool r) {
 
 }  // namespace
 
-const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid) {
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, bool gsm) {
+  if (gsm) return (cluster || !exact) ? nullptr : fwd_gsm_kernel_ptr(mode, K, resid, kOutBf16);
   if (mode == kRMS)
     return cluster ? pick_fwd<kRMS, true>(K, exact, resid) : pick_fwd<kRMS, false>(K, exact, resid);
   return cluster ? pick_fwd<kLayer, true>(K, exact, resid)

@@ -9,8 +9,10 @@ namespace {
 
 template <int MODE, int K, bool RESID, int OUT>
 const void *pick_exact(bool e) {
-  return e ? reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, K, false, true, RESID, OUT>)
-           : reinterpret_cast<const void *>(&norm_fwd_kernel<MODE, K, false, false, RESID, OUT>);
+  return e ? reinterpret_cast<const void *>(
+                 &norm_fwd_kernel<MODE, K, false, true, RESID, OUT, false>)
+           : reinterpret_cast<const void *>(
+                 &norm_fwd_kernel<MODE, K, false, false, RESID, OUT, false>);
 }
 
 template <int MODE, int K>
@@ -46,7 +48,8 @@ const void *pick_fp8(int K, bool e, bool r, int out) {
 
 }  // namespace
 
-const void *fwd_fp8_kernel_ptr(int mode, int K, bool exact, bool resid, int out) {
+const void *fwd_fp8_kernel_ptr(int mode, int K, bool exact, bool resid, int out, bool gsm) {
+  if (gsm) return exact ? fwd_gsm_kernel_ptr(mode, K, resid, out) : nullptr;
   return mode == kRMS ? pick_fp8<kRMS>(K, exact, resid, out)
                       : pick_fp8<kLayer>(K, exact, resid, out);
 }

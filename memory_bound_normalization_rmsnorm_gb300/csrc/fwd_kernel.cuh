@@ -38,10 +38,14 @@ namespace gbn {
 // in binary32, round to nearest even) is written out and normalised.
 // OUT: kOutBf16 writes y as bf16; kOutFp8Row / kOutFp8Mx write E4M3 codes of
 // y with a per-row scale or per-32-column power-of-two (E8M0) exponents.
-template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT>
+// GSM: gamma (and beta) are staged once in shared memory and read per row
+// instead of living in registers, so a thread can hold more chunks of x.
+template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT, bool GSM>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C);
+  constexpr int kParams = GSM ? (MODE == kLayer ? 2 : 1) : 0;
+  const SmemLayout L =
+      make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C, kParams);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
@@ -79,19 +83,47 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   // gamma as fp32 pairs (and beta packed) for this thread's chunks stay in
   // registers for the whole kernel: the thread owns the same columns in
   // every row.
-  float2 gf[K][4];
-  uint4 bv[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int c = t + k * a.tpr;
-    uint4 gv = make_uint4(0, 0, 0, 0);
-    bv[k] = make_uint4(0, 0, 0, 0);
-    if (c < nsc_me) {
-      gv = ld_global_nc_v4(a.gamma + col0 + c * 8);
-      if (MODE == kLayer && a.beta != nullptr) bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
+  constexpr int KG = GSM ? 1 : K;
+  float2 gf[KG][4];
+  uint4 bv[KG];
+  const uint4 *sgam = reinterpret_cast<const uint4 *>(smem + L.par_off);
+  if (GSM) {
+    uint4 *dst = reinterpret_cast<uint4 *>(smem + L.par_off);
+    for (int c = tid; c < a.nsc; c += blockDim.x) {
+      uint4 gv = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+      if (c < nsc_me) {
+        gv = ld_global_nc_v4(a.gamma + col0 + c * 8);
+        if (MODE == kLayer && a.beta != nullptr) b = ld_global_nc_v4(a.beta + col0 + c * 8);
+      }
+      dst[c] = gv;
+      if (MODE == kLayer) dst[a.nsc + c] = b;
     }
-    chunk_to_f2(gv, gf[k]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < KG; ++k) {
+      const int c = t + k * a.tpr;
+      uint4 gv = make_uint4(0, 0, 0, 0);
+      bv[k] = make_uint4(0, 0, 0, 0);
+      if (c < nsc_me) {
+        gv = ld_global_nc_v4(a.gamma + col0 + c * 8);
+        if (MODE == kLayer && a.beta != nullptr) bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
+      }
+      chunk_to_f2(gv, gf[k]);
+    }
   }
+  // gamma (g4) and beta (b4) of chunk k of this thread, as fp32 pairs.
+  auto params = [&](int k, float2 (&g4)[4], float2 (&b4)[4]) {
+    if (GSM) {
+      const int c = t + k * a.tpr;
+      chunk_to_f2(sgam[c], g4);
+      if (MODE == kLayer) chunk_to_f2(sgam[a.nsc + c], b4);
+    } else {
+      const int kk = GSM ? 0 : k;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) g4[p] = gf[kk][p];
+      if (MODE == kLayer) chunk_to_f2(bv[kk], b4);
+    }
+  };
 
   if (CLUSTER) cluster_sync(); else __syncthreads();
 
@@ -222,12 +254,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
           for (int k = 0; k < K; ++k) {
             if (EXACT || t + k * a.tpr < nsc_me) {
               float2 o[4];
-              float2 bf[4];
-              if (MODE == kLayer) chunk_to_f2(bv[k], bf);
+              float2 gk[4], bf[4];
+              params(k, gk, bf);
 #pragma unroll
               for (int p = 0; p < 4; ++p) {
                 const float2 xh = mul2(MODE == kLayer ? add2(xf[k][p], nmu) : xf[k][p], rs2);
-                o[p] = (MODE == kLayer) ? fma2(xh, gf[k][p], bf[p]) : mul2(xh, gf[k][p]);
+                o[p] = (MODE == kLayer) ? fma2(xh, gk[p], bf[p]) : mul2(xh, gk[p]);
               }
               st_global_cs_v4(yrow + k * a.tpr * 8, f2_to_chunk(o));
             }
@@ -240,12 +272,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
         const float2 rs2 = splat2(rs);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          float2 bf[4];
-          if (MODE == kLayer) chunk_to_f2(bv[k], bf);
+          float2 gk[4], bf[4];
+          params(k, gk, bf);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const float2 xh = mul2(MODE == kLayer ? add2(xf[k][p], nmu) : xf[k][p], rs2);
-            xf[k][p] = (MODE == kLayer) ? fma2(xh, gf[k][p], bf[p]) : mul2(xh, gf[k][p]);
+            xf[k][p] = (MODE == kLayer) ? fma2(xh, gk[p], bf[p]) : mul2(xh, gk[p]);
           }
         }
         uint8_t *qrow = a.q + (row0 + r) * a.N + col0 + t * 8;
@@ -259,7 +291,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
               am = fmaxf(am, fmaxf(fabsf(xf[k][p].x), fabsf(xf[k][p].y)));
           am = group_max<EXACT>(am, a.tpr, g, a.G, t, red, rpar);
           if (active) {
-            const float2 inv = splat2(am > 0.f ? __fdiv_rn(448.f, am) : 1.f);
+            // 448 / amax within 2 ulp (the codes tolerate far more); the
+            // dequantisation scale amax / 448 within 1.5 ulp.
+            const float2 inv = splat2(am > 0.f ? __fdividef(448.f, am) : 1.f);
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               if (EXACT || t + k * a.tpr < nsc_me) {
@@ -274,7 +308,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
               }
             }
             if (t == 0) {
-              a.qscale[row0 + r] = am > 0.f ? __fdiv_rn(am, 448.f) : 1.f;
+              a.qscale[row0 + r] = am > 0.f ? am * (1.0f / 448.0f) : 1.f;
               a.rstd[row0 + r] = rs;
             }
           }
@@ -293,9 +327,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
             for (int p = 0; p < 4; ++p) m = fmaxf(m, fmaxf(fabsf(xf[k][p].x), fabsf(xf[k][p].y)));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const int eb = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu);
-            const int e = eb == 0 ? -127 : max(eb - 127 - 8, -127);
-            const float2 inv = splat2(__uint_as_float(static_cast<uint32_t>(127 - e) << 23));
+            // m >= 0, so its bits >> 23 are the biased exponent eb; e + 127 =
+            // max(eb - 8, 0) (eb < 8 covers zero and subnormal amax: e =
+            // -127), and 2^-e has the biased exponent 127 - e = min(262 - eb,
+            // 254).
+            const int eb = static_cast<int>(__float_as_uint(m) >> 23);
+            const float2 inv = splat2(__uint_as_float(static_cast<uint32_t>(min(262 - eb, 254)) << 23));
             if (own) {
               uint32_t w[4];
 #pragma unroll
@@ -305,7 +342,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
               }
               st_global_cs_v2(qrow + k * a.tpr * 8,
                               make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
-              if ((t & 3) == 0) erow[(t + k * a.tpr) >> 2] = static_cast<uint8_t>(e + 127);
+              st_global_u8_if(erow + ((t + k * a.tpr) >> 2), static_cast<uint32_t>(max(eb - 8, 0)),
+                              (t & 3) == 0);
             }
           }
           if (active && t == 0) a.rstd[row0 + r] = rs;

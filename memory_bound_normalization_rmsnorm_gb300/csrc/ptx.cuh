@@ -199,6 +199,16 @@ __device__ __forceinline__ void st_global_cs_v2(void *p, uint2 v) {
                : "memory");
 }
 
+// One byte to global memory if `pred` (a predicated store: no branch).
+__device__ __forceinline__ void st_global_u8_if(void *p, uint32_t v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %2, 0;\n\t"
+      "@q st.global.u8 [%0], %1;\n\t}" ::"l"(p),
+      "r"(v), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
 // Two fp32 values to two E4M3 codes (round to nearest even, saturating to
 // +-448), packed with `lo` in the low byte (the lower address).
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {

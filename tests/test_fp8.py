@@ -79,12 +79,19 @@ def test_fp8_full_size(name, sc):
     assert gb.norm_get_device_error() == 0
 
 
-def test_fp8_stats_match_bf16_forward_and_deterministic():
-    """rstd / mean of the E4M3 forward equal norm_fwd's bit for bit (same
-    plan, same statistics code); two runs give identical codes and scales."""
+def test_fp8_stats_match_bf16_forward_and_deterministic(monkeypatch):
+    """rstd / mean of the E4M3 forward equal norm_fwd's bit for bit when both
+    run the same plan (the E4M3 forward stages gamma/beta in shared memory at
+    this shape; the plan override makes norm_fwd do the same); two runs give
+    identical codes and scales."""
     case = wl.like(wl.WORKLOADS["layer_32768x4096"], 3001, 4096)
     x, g, b, _ = [None if t is None else t.cuda() for t in wl.make_inputs(case, "cpu")]
+    p8 = gb.norm_plan(3001, 4096, 1, False, fp8=True)
+    assert p8["params_in_smem"] == 2
+    monkeypatch.setenv("GBNORM_PLAN", "gsm=1")
+    assert gb.norm_plan(3001, 4096, 1, False) == p8
     y, rs, mu = gb.norm_fwd(x, g, b, case.eps, 1)
+    monkeypatch.delenv("GBNORM_PLAN")
     for gsc in (gb.FP8_ROW, gb.FP8_MX):
         a = gb.norm_fwd_fp8(x, g, b, case.eps, 1, gsc)
         c = gb.norm_fwd_fp8(x, g, b, case.eps, 1, gsc)
