@@ -236,10 +236,11 @@ typedef struct {
     int32_t long_rows;         /* 1: long-row kernels (the row slice is read
                                   twice from shared memory instead of being
                                   held in registers) */
-    int32_t params_in_smem;    /* forward only: number of bf16 parameter
-                                  vectors (gamma, and beta for LAYER) staged
-                                  in shared memory and read per row instead
-                                  of being held in registers; 0 if none */
+    int32_t param_smem_bytes;  /* forward only: bytes of gamma (and beta for
+                                  LAYER) staged in shared memory and read per
+                                  row instead of being held in registers
+                                  (fp32 for bf16 output, bf16 for E4M3
+                                  output); 0 if none */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

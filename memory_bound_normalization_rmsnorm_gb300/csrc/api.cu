@@ -175,8 +175,8 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
   const int budget = (p.occ == 2) ? (smem_optin + 1024) / 2 - 1024 : smem_optin - 1024;
   int S = 0;
   for (;;) {
-    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C, p.nparams);
-    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, p.tpr, ntensors, bwd, C, p.nparams);
+    const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C, p.par_bpc);
+    const SmemLayout L2 = make_layout(G * rpg, p.NS, 2, G, p.tpr, ntensors, bwd, C, p.par_bpc);
     const int per_stage = static_cast<int>(L2.total - L1.total);
     const int fixed = static_cast<int>(L1.total) - per_stage;
     S = (budget - fixed) / per_stage;
@@ -193,7 +193,7 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
   p.S = S;
   p.threads = G * p.tpr;
   if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
-  const SmemLayout L = make_layout(p.RT, p.NS, S, G, p.tpr, ntensors, bwd, C, p.nparams);
+  const SmemLayout L = make_layout(p.RT, p.NS, S, G, p.tpr, ntensors, bwd, C, p.par_bpc);
   if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
   if (L.stage_bytes >= (1u << 20)) return NORM_ERR_UNSUPPORTED;
   if (bwd && static_cast<int64_t>(2) * G * p.NS * 4 > static_cast<int64_t>(S) * L.stage_bytes)
@@ -355,7 +355,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   if (want_gsm) {
     if (!exact || (K != 8 && K != 6 && K != 5) || C != 1) return NORM_ERR_UNSUPPORTED;
     p.gsm = true;
-    p.nparams = mode == kLayer ? 2 : 1;
+    p.par_bpc = param_bytes_per_col(mode, fp8);
   }
 
   int G = kMaxThreads / tpr;
@@ -802,7 +802,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   out->partials = p.P;
   out->exact = p.exact ? 1 : 0;
   out->long_rows = p.long_rows ? 1 : 0;
-  out->params_in_smem = p.nparams;
+  out->param_smem_bytes = p.par_bpc * p.NS;
   return NORM_OK;
 }
 

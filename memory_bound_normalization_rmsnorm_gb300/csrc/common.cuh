@@ -58,7 +58,7 @@ struct NormArgs {
 struct SmemLayout {
   uint32_t tensor_bytes;  // one tensor's share of a stage: RT * NS * 2
   uint32_t stage_bytes;   // ntensors * tensor_bytes
-  uint32_t par_off;       // forward with gamma (and beta) staged: bf16 [NS] each
+  uint32_t par_off;       // forward with gamma (and beta) staged in shared memory
   uint32_t stats_off;     // backward: [S][RT][2] floats (rstd, mean)
   uint32_t red_off;       // [2][G][W][4] floats, cross-warp group partials
                           // (W = tpr / 32; only when tpr > 32)
@@ -77,18 +77,18 @@ __host__ __device__ inline uint32_t align16(uint32_t v) {
   return (v + 15u) & ~15u;
 }
 
-// C: CTAs per cluster (1: no cluster exchange region).  nparams: bf16
-// parameter vectors of NS columns staged in shared memory (0, or 1 gamma /
-// 2 gamma and beta for the forward kernels that read them per row).
+// C: CTAs per cluster (1: no cluster exchange region).  par_bpc: bytes per
+// column of the parameters staged in shared memory by the forward kernels
+// that read them per row (param_bytes_per_col; 0 for the others).
 __host__ __device__ inline SmemLayout make_layout(int RT, int NS, int S, int G,
                                                   int tpr, int ntensors,
-                                                  bool stats, int C, int nparams = 0) {
+                                                  bool stats, int C, int par_bpc = 0) {
   SmemLayout L;
   L.tensor_bytes = static_cast<uint32_t>(RT) * static_cast<uint32_t>(NS) * 2u;
   L.stage_bytes = L.tensor_bytes * static_cast<uint32_t>(ntensors);
   uint32_t off = L.stage_bytes * static_cast<uint32_t>(S);
   L.par_off = off;
-  off = align16(off + static_cast<uint32_t>(nparams) * static_cast<uint32_t>(NS) * 2u);
+  off = align16(off + static_cast<uint32_t>(par_bpc) * static_cast<uint32_t>(NS));
   L.stats_off = off;
   if (stats) off = align16(off + static_cast<uint32_t>(S * RT * 2) * 4u);
   L.red_off = off;
@@ -116,7 +116,7 @@ struct Plan {
   int occ = 1;            // CTAs per SM the kernel is compiled for
   bool resid = false;     // fused residual add variant
   bool gsm = false;       // forward: gamma/beta read per row from shared memory
-  int nparams = 0;        // bf16 vectors staged in shared memory (gsm: 1 RMS, 2 LN)
+  int par_bpc = 0;        // gsm: staged parameter bytes per column
   int G = 0;       // groups per CTA
   int rpg = 1;     // rows per group per tile
   int RT = 0;      // rows per tile
@@ -131,6 +131,14 @@ struct Plan {
 // Kernel entry points, by (mode, K, cluster, exact, fused residual).
 // Return nullptr when that combination is not compiled (the fused residual
 // variants exist without clusters only).
+// Bytes per column of the parameters a staged-parameter forward kernel keeps
+// in shared memory: gamma (and beta for LayerNorm), as fp32 for bf16 output
+// (no unpacking per row) and as bf16 for E4M3 output (less shared-memory
+// traffic next to the heavier epilogue; measured faster for each).
+__host__ __device__ constexpr int param_bytes_per_col(int mode, bool fp8_out) {
+  return (mode == 1 ? 2 : 1) * (fp8_out ? 2 : 4);
+}
+
 // Forward output kinds: bf16 y, or E4M3 codes with a per-row fp32 scale, or
 // E4M3 codes with one E8M0 exponent per 32-column block (MX).
 constexpr int kOutBf16 = 0;

@@ -38,14 +38,17 @@ namespace gbn {
 // in binary32, round to nearest even) is written out and normalised.
 // OUT: kOutBf16 writes y as bf16; kOutFp8Row / kOutFp8Mx write E4M3 codes of
 // y with a per-row scale or per-32-column power-of-two (E8M0) exponents.
-// GSM: gamma (and beta) are staged once in shared memory and read per row
-// instead of living in registers, so a thread can hold more chunks of x.
+// GSM: gamma (and beta) are staged once in shared memory (as fp32) and read
+// per row instead of living in registers, so a thread can hold more chunks
+// of x.
 template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT, bool GSM>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int kParams = GSM ? (MODE == kLayer ? 2 : 1) : 0;
+  // Staged parameters as fp32 (bf16 output) or bf16 (E4M3 output).
+  constexpr bool kParF32 = OUT == kOutBf16;
+  constexpr int kParBpc = GSM ? param_bytes_per_col(MODE, !kParF32) : 0;
   const SmemLayout L =
-      make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C, kParams);
+      make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C, kParBpc);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
@@ -86,17 +89,34 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   constexpr int KG = GSM ? 1 : K;
   float2 gf[KG][4];
   uint4 bv[KG];
-  const uint4 *sgam = reinterpret_cast<const uint4 *>(smem + L.par_off);
+  // Staged parameters.  fp32: float4 arrays [param][half][chunk]; bf16:
+  // uint4 arrays [param][chunk].  Either way consecutive threads read
+  // consecutive 16-byte words (no bank conflicts).
+  const float4 *spar = reinterpret_cast<const float4 *>(smem + L.par_off);
+  const uint4 *spar16 = reinterpret_cast<const uint4 *>(smem + L.par_off);
   if (GSM) {
-    uint4 *dst = reinterpret_cast<uint4 *>(smem + L.par_off);
     for (int c = tid; c < a.nsc; c += blockDim.x) {
       uint4 gv = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
       if (c < nsc_me) {
         gv = ld_global_nc_v4(a.gamma + col0 + c * 8);
         if (MODE == kLayer && a.beta != nullptr) b = ld_global_nc_v4(a.beta + col0 + c * 8);
       }
-      dst[c] = gv;
-      if (MODE == kLayer) dst[a.nsc + c] = b;
+      if (kParF32) {
+        float4 *dst = reinterpret_cast<float4 *>(smem + L.par_off);
+        float2 f[4];
+        chunk_to_f2(gv, f);
+        dst[c] = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+        dst[a.nsc + c] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+        if (MODE == kLayer) {
+          chunk_to_f2(b, f);
+          dst[2 * a.nsc + c] = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+          dst[3 * a.nsc + c] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+        }
+      } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(smem + L.par_off);
+        dst[c] = gv;
+        if (MODE == kLayer) dst[a.nsc + c] = b;
+      }
     }
   } else {
 #pragma unroll
@@ -113,10 +133,24 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   }
   // gamma (g4) and beta (b4) of chunk k of this thread, as fp32 pairs.
   auto params = [&](int k, float2 (&g4)[4], float2 (&b4)[4]) {
-    if (GSM) {
+    if (GSM && !kParF32) {
       const int c = t + k * a.tpr;
-      chunk_to_f2(sgam[c], g4);
-      if (MODE == kLayer) chunk_to_f2(sgam[a.nsc + c], b4);
+      chunk_to_f2(spar16[c], g4);
+      if (MODE == kLayer) chunk_to_f2(spar16[a.nsc + c], b4);
+    } else if (GSM) {
+      const int c = t + k * a.tpr;
+      const float4 g0 = spar[c], g1 = spar[a.nsc + c];
+      g4[0] = make_float2(g0.x, g0.y);
+      g4[1] = make_float2(g0.z, g0.w);
+      g4[2] = make_float2(g1.x, g1.y);
+      g4[3] = make_float2(g1.z, g1.w);
+      if (MODE == kLayer) {
+        const float4 b0 = spar[2 * a.nsc + c], b1 = spar[3 * a.nsc + c];
+        b4[0] = make_float2(b0.x, b0.y);
+        b4[1] = make_float2(b0.z, b0.w);
+        b4[2] = make_float2(b1.x, b1.y);
+        b4[3] = make_float2(b1.z, b1.w);
+      }
     } else {
       const int kk = GSM ? 0 : k;
 #pragma unroll

@@ -17,13 +17,13 @@ def _align16(v):
     return (v + 15) & ~15
 
 
-def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C, nparams=0):
+def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C, par_bytes=0):
     """Same region order as the kernels' shared-memory layout."""
     tensor = RT * NS * 2
     stage = tensor * ntensors
     off = stage * S
     L = {"tensor": tensor, "stage": stage, "params": off}
-    off = _align16(off + nparams * NS * 2)
+    off = _align16(off + par_bytes)
     L["stats"] = off
     if stats:
         off = _align16(off + S * RT * 2 * 4)
@@ -63,12 +63,16 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     if p["exact"]:
         assert tpr % 32 == 0 and K * tpr == nsc and nc % C == 0, "EXACT plan is not exact"
     ntensors = (2 if backward else 1) + (1 if residual else 0)
-    nparams = p["params_in_smem"]
-    assert nparams == 0 or (not backward and p["exact"] and K in (5, 6, 8) and C == 1
-                            and nparams == (2 if mode == 1 else 1))
-    L = smem_layout(RT, NS, S, G, tpr, ntensors, backward, C, nparams)
-    # staged parameters: chunk c of gamma at c, of beta at nsc + c (16 bytes each)
-    assert L["params"] + nparams * nsc * 16 <= L["stats"]
+    par = p["param_smem_bytes"]
+    nvec = 2 if mode == 1 else 1
+    assert par == 0 or (not backward and p["exact"] and K in (5, 6, 8) and C == 1
+                        and par in (nvec * NS * 2, nvec * NS * 4))
+    L = smem_layout(RT, NS, S, G, tpr, ntensors, backward, C, par)
+    # staged parameters: fp32 float4 [param][half][chunk] or bf16 uint4
+    # [param][chunk]; the highest 16-byte word read is inside the region
+    if par:
+        words = nvec * nsc * (2 if par == nvec * NS * 4 else 1)
+        assert L["params"] + words * 16 <= L["stats"]
     assert smem == L["total"] <= smem_optin, "shared memory over the opt-in limit"
     assert L["stage"] < TX_LIMIT
     assert L["bar"] % 8 == 0 and L["stats"] % 16 == 0 and L["red"] % 16 == 0

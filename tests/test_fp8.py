@@ -87,9 +87,11 @@ def test_fp8_stats_match_bf16_forward_and_deterministic(monkeypatch):
     case = wl.like(wl.WORKLOADS["layer_32768x4096"], 3001, 4096)
     x, g, b, _ = [None if t is None else t.cuda() for t in wl.make_inputs(case, "cpu")]
     p8 = gb.norm_plan(3001, 4096, 1, False, fp8=True)
-    assert p8["params_in_smem"] == 2
+    assert p8["param_smem_bytes"] > 0
     monkeypatch.setenv("GBNORM_PLAN", "gsm=1")
-    assert gb.norm_plan(3001, 4096, 1, False) == p8
+    pb = gb.norm_plan(3001, 4096, 1, False)
+    keys = ("threads_per_row", "chunks_per_thread", "groups", "rows_per_group")
+    assert all(pb[k] == p8[k] for k in keys), (pb, p8)
     y, rs, mu = gb.norm_fwd(x, g, b, case.eps, 1)
     monkeypatch.delenv("GBNORM_PLAN")
     for gsc in (gb.FP8_ROW, gb.FP8_MX):
