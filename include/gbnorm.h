@@ -203,6 +203,50 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma,
                            float *mean, norm_stream_t stream);
 
 /*
+ * Forward + backward on HOST tensors.  For callers whose activations live in
+ * host memory (offloaded activations, data-loader output, tests): one call
+ * copies the inputs in, runs norm_fwd and norm_bwd, and copies every output
+ * back, with the rows cut into chunks that stream through a few device
+ * buffers so that host-to-device copies, kernels and device-to-host copies
+ * of different chunks overlap on three streams (the copy engines of the two
+ * directions work at the same time).  The computation is that of norm_fwd /
+ * norm_bwd: y, rstd, mean and dx equal theirs bit for bit; dgamma / dbeta
+ * are summed per chunk and then over chunks in chunk order (bitwise
+ * reproducible for a given chunk_rows, equal to norm_bwd's within
+ * rounding).
+ *
+ * norm_host_workspace_bytes: device workspace norm_fwd_bwd_host needs for
+ *   this shape and chunk size (chunk_rows = 0: the library's default, about
+ *   16 MB of x per chunk).
+ * norm_fwd_bwd_host:
+ *   x, dy          HOST bf16 [M, N] inputs (page-locked memory, e.g. from
+ *                  cudaHostAlloc, for the copies to overlap; pageable memory
+ *                  works but serialises);
+ *   gamma, beta    HOST bf16 [N] (beta NULL: zero; RMS: NULL);
+ *   y, dx          HOST bf16 [M, N] outputs; rstd, mean HOST fp32 [M]
+ *                  (mean LAYER only); dgamma, dbeta HOST fp32 [N] (dbeta
+ *                  LAYER only, may be NULL);
+ *   chunk_rows     rows per chunk (0: default);
+ *   workspace      DEVICE memory of norm_host_workspace_bytes bytes, 256-byte
+ *                  aligned, owned by the caller (NORM_ERR_WORKSPACE if NULL or
+ *                  short, NORM_ERR_ALIGN if misaligned).
+ * Asynchronous: the call enqueues everything behind the work already on
+ * `stream` and returns; the host outputs are complete once `stream` is
+ * synchronised.  The host buffers must stay valid until then.  Calls on one
+ * device are serialised while they enqueue; the library's two internal copy
+ * streams are created on first use.
+ */
+norm_status_t norm_host_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode,
+                                        int64_t chunk_rows, size_t *bytes);
+
+norm_status_t norm_fwd_bwd_host(const void *x, const void *dy, const void *gamma,
+                                const void *beta, int64_t M, int64_t N, float eps,
+                                norm_mode_t mode, void *y, void *dx, float *rstd,
+                                float *mean, float *dgamma, float *dbeta,
+                                int64_t chunk_rows, void *workspace,
+                                size_t workspace_bytes, norm_stream_t stream);
+
+/*
  * norm_plan -- the launch plan the library uses for one pass (backward = 0
  * for norm_fwd, 1 for norm_bwd, 2 for norm_add_fwd, 3 for norm_add_bwd, 4
  * for norm_fwd_fp8 without and 6 with a residual) of

@@ -6,12 +6,14 @@ the seeded synthetic workloads used by the tests and the benchmark.
 """
 from ._binding import (FP8_MX, FP8_ROW, LAYER, RMS, NormError, declared_functions, lib,
                        library_path, norm_add_bwd, norm_add_bwd_workspace_bytes, norm_add_fwd,
-                       norm_bwd, norm_bwd_workspace_bytes, norm_fwd, norm_fwd_fp8,
-                       norm_get_device_error, norm_plan, strerror)
+                       norm_bwd, norm_bwd_workspace_bytes, norm_fwd, norm_fwd_bwd_host,
+                       norm_fwd_fp8, norm_get_device_error, norm_host_workspace_bytes,
+                       norm_plan, strerror)
 from .builder import build
 
 __all__ = [
     "RMS", "LAYER", "NormError", "norm_fwd", "norm_bwd", "norm_bwd_workspace_bytes",
     "norm_get_device_error", "norm_plan", "norm_add_fwd", "norm_add_bwd",
-    "norm_add_bwd_workspace_bytes", "norm_fwd_fp8", "FP8_ROW", "FP8_MX", "strerror", "lib", "library_path", "declared_functions", "build",
+    "norm_add_bwd_workspace_bytes", "norm_fwd_fp8", "FP8_ROW", "FP8_MX",
+    "norm_fwd_bwd_host", "norm_host_workspace_bytes", "strerror", "lib", "library_path", "declared_functions", "build",
 ]

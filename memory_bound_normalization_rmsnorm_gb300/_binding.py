@@ -101,6 +101,13 @@ def lib():
             L.norm_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp]
             L.norm_fwd_fp8.restype = ctypes.c_int
+            L.norm_host_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int, _i64,
+                                                    ctypes.POINTER(ctypes.c_size_t)]
+            L.norm_host_workspace_bytes.restype = ctypes.c_int
+            L.norm_fwd_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
+                                            ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                            _vp, ctypes.c_size_t, _vp]
+            L.norm_fwd_bwd_host.restype = ctypes.c_int
             L.norm_add_bwd.restype = ctypes.c_int
             L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(Plan)]
@@ -306,6 +313,66 @@ def norm_fwd_fp8(x, gamma, beta=None, eps=1e-5, mode=RMS, scaling=FP8_ROW, *, r=
     if st != 0:
         raise NormError(st, "norm_fwd_fp8")
     return q, scale, rstd, mean, h
+
+
+def norm_host_workspace_bytes(M, N, mode=RMS, chunk_rows=0) -> int:
+    out = ctypes.c_size_t(0)
+    st = lib().norm_host_workspace_bytes(int(M), int(N), int(mode), int(chunk_rows),
+                                         ctypes.byref(out))
+    if st != 0:
+        raise NormError(st, "norm_host_workspace_bytes")
+    return int(out.value)
+
+
+def _check_host(t, name, dtype, shape):
+    if t is None:
+        return
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}")
+
+
+def norm_fwd_bwd_host(x, dy, gamma, beta=None, eps=1e-5, mode=RMS, *, chunk_rows=0, out=None,
+                      workspace=None, stream=None, device=None):
+    """Forward + backward on host tensors (norm_fwd_bwd_host in gbnorm.h).
+    x, dy, gamma, beta are CPU tensors (pinned for overlap); returns CPU
+    tensors (y, rstd, mean, dx, dgamma, dbeta), complete once `stream`
+    (default: the current stream of `device`) is synchronised.  `out` may
+    pass preallocated (pinned) outputs in that order, `workspace` a device
+    uint8 tensor of norm_host_workspace_bytes bytes."""
+    mode = int(mode)
+    M, N = _rows(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    bf, f32 = torch.bfloat16, torch.float32
+    lead = x.shape[:-1]
+    _check_host(x, "x", bf, x.shape)
+    _check_host(dy, "dy", bf, x.shape)
+    _check_host(gamma, "gamma", bf, (N,))
+    _check_host(beta, "beta", bf, (N,))
+    if out is None:
+        pin = x.is_pinned()
+        out = (torch.empty(x.shape, dtype=bf, pin_memory=pin),
+               torch.empty(lead, dtype=f32, pin_memory=pin),
+               torch.empty(lead, dtype=f32, pin_memory=pin) if mode == LAYER else None,
+               torch.empty(x.shape, dtype=bf, pin_memory=pin),
+               torch.empty(N, dtype=f32, pin_memory=pin),
+               torch.empty(N, dtype=f32, pin_memory=pin) if mode == LAYER else None)
+    y, rstd, mean, dx, dg, db = out
+    for t, n, dt, sh in ((y, "y", bf, x.shape), (rstd, "rstd", f32, lead), (mean, "mean", f32, lead),
+                         (dx, "dx", bf, x.shape), (dg, "dgamma", f32, (N,)), (db, "dbeta", f32, (N,))):
+        _check_host(t, n, dt, sh)
+    nbytes = norm_host_workspace_bytes(M, N, mode, chunk_rows)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _check_tensor(workspace, "workspace", torch.uint8, (workspace.numel(),), dev)
+    st = lib().norm_fwd_bwd_host(_ptr(x), _ptr(dy), _ptr(gamma), _ptr(beta), M, N, float(eps),
+                                 mode, _ptr(y), _ptr(dx), _ptr(rstd), _ptr(mean), _ptr(dg),
+                                 _ptr(db), int(chunk_rows), _ptr(workspace),
+                                 workspace.numel(), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_fwd_bwd_host")
+    return y, rstd, mean, dx, dg, db
 
 
 def norm_add_bwd_workspace_bytes(M, N, mode=RMS) -> int:

@@ -527,6 +527,14 @@ NormArgs base_args(const Plan &p, int64_t M, int N) {
 }
 
 }  // namespace
+
+// Fixed-order column sum of P fp32 rows [P][n] (and, with dbeta, of the P
+// rows that follow them) into dgamma (dbeta), on `s`.
+norm_status_t reduce_rows(const float *rows, int P, int n, float *dgamma, float *dbeta,
+                          cudaStream_t s) {
+  return launch_reduce(rows, P, n, dgamma, dbeta, s);
+}
+
 }  // namespace gbn
 
 // ---------------------------------------------------------------------------

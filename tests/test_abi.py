@@ -93,6 +93,32 @@ def test_fp8_validation_codes():
     assert call(res=F + 2, h=F) == 3
 
 
+def test_host_pipeline_validation_codes():
+    f = gb.lib().norm_fwd_bwd_host
+    ok = dict(x=F, dy=F, g=F, b=None, M=4, N=64, eps=1e-5, mode=0, y=F, dx=F, r=F, m=None,
+              dg=F, db=None, cr=0, ws=F, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["dy"], a["g"], a["b"], a["M"], a["N"], a["eps"], a["mode"], a["y"],
+                 a["dx"], a["r"], a["m"], a["dg"], a["db"], a["cr"], a["ws"], a["wsb"], None)
+
+    assert call(x=None) == 1
+    assert call(dy=None) == 1
+    assert call(dg=None) == 1
+    assert call(mode=3) == 4
+    assert call(b=F) == 4              # beta with RMSNorm
+    assert call(db=F) == 4             # dbeta with RMSNorm
+    assert call(mode=1) == 4           # LayerNorm without mean
+    assert call(N=12) == 2
+    assert call(M=0) == 2
+    assert call(cr=-1) == 2
+    assert call(eps=float("nan")) == 9
+    n = ctypes.c_size_t(0)
+    assert gb.lib().norm_host_workspace_bytes(4, 12, 0, 0, ctypes.byref(n)) == 2
+    assert gb.lib().norm_host_workspace_bytes(4, 64, 0, 0, None) == 1
+
+
 def test_bwd_validation_codes():
     f = gb.lib().norm_bwd
     ok = dict(dy=F, x=F, g=F, r=F, m=None, M=4, N=16, mode=0, dx=F, dg=F, db=None, ws=F,
