@@ -63,24 +63,42 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Host-only sources: they choose and launch kernels but compile to no device
+# code; the plan they chose is recorded beside the counters instead.
+HOST_ONLY_SOURCES = ("api.cu", "host.cu")
+
+
 def source_hash():
+    """Hash of the sources that define device code."""
     csrc = os.path.join(ROOT, "memory_bound_normalization_rmsnorm_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
+        if name in HOST_ONLY_SOURCES:
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, kernel):
+def _plan_key(p):
+    """The fields of a norm_plan dict that decide which kernel a launch runs
+    and how it walks the rows."""
+    keys = ("cluster", "threads_per_row", "chunks_per_thread", "groups", "rows_per_group",
+            "stages", "grid", "exact", "long_rows", "param_smem_bytes")
+    return {k: p[k] for k in keys}
+
+
+def ncu_traffic(workload, kernel, plan=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current device code and the same launch plan (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             data = json.load(f)
         rec = data[workload][kernel]
         if rec.get("source_hash") != source_hash():
+            return None
+        if plan is not None and rec.get("plan") is not None and rec["plan"] != plan:
             return None
         return rec["bytes_per_launch"]
     except Exception:
@@ -408,7 +426,7 @@ def run_ours(args):
     peak, peak_kind = peak_hbm()
     bwd_gbs = bwd_b / (bwd_ms * 1e-3) / 1e9
     fwd_gbs = fwd_b / (fwd_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(w.name, "norm_bwd_kernel")
+    traffic = ncu_traffic(w.name, "norm_bwd_kernel", plan=_plan_key(plan_b))
     roofline = {"bound": "hbm", "achieved": bwd_gbs, "peak": peak, "unit": "GB/s",
                 "frac": bwd_gbs / peak, "traffic": traffic,
                 "kernel": "norm_bwd (fused row kernel + fixed-order partial reduce)",
