@@ -302,7 +302,7 @@ class DirectStep:
     per-call Python tensor checks inside the timed loop).  With `r` and `dh`
     given it runs the fused residual add variant (norm_add_fwd/norm_add_bwd)."""
 
-    def __init__(self, gb, w, x, g, b, dy, stream, r=None, dh=None, fp8=None):
+    def __init__(self, gb, w, x, g, b, dy, stream, r=None, dh=None, fp8=None, fwd_only=False):
         import torch
 
         M, N = w.M, w.N
@@ -315,7 +315,7 @@ class DirectStep:
         self.db = torch.empty(N, dtype=torch.float32, device=dev) if w.mode == 1 else None
         fused = r is not None
         ws_query = gb.norm_add_bwd_workspace_bytes if fused else gb.norm_bwd_workspace_bytes
-        nbytes = ws_query(M, N, w.mode)
+        nbytes = 16 if fwd_only else ws_query(M, N, w.mode)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
         L = gb.lib()
         vp = ctypes.c_void_p
@@ -529,11 +529,13 @@ def run_sweep(args):
             x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
         else:
             (x, g, b, dy), r, dh = wl.make_inputs(w, "cuda"), None, None
-        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh, fp8=fp8)
+        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh, fp8=fp8,
+                          fwd_only=args.fwd_only)
         pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused, fp8=fp8 is not None)
-        pb = gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
+        pb = None if args.fwd_only else gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
         res = {}
-        for name_, fn in (("fwd", step.fwd), ("bwd", step.bwd)):
+        passes = (("fwd", step.fwd),) if args.fwd_only else (("fwd", step.fwd), ("bwd", step.bwd))
+        for name_, fn in passes:
             for _ in range(args.warmup):
                 fn()
             torch.cuda.synchronize()
@@ -547,18 +549,20 @@ def run_sweep(args):
             res[name_] = e0.elapsed_time(e1) / args.steps
         if gb.norm_get_device_error() != 0:
             raise RuntimeError(f"device error word set on {name}")
-        fb, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"], residual=fused, fp8=fp8)
+        fb, bb = algo_bytes(w.M, w.N, w.mode, 0 if pb is None else pb["partials"],
+                            residual=fused, fp8=fp8)
         keep = ("cluster", "threads_per_row", "chunks_per_thread", "groups", "rows_per_group",
                 "stages", "grid", "exact")
-        print(json.dumps({
-            "workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
-            "fused_residual": fused, "fp8": args.fp8 or None, "fwd_us": 1e3 * res["fwd"], "bwd_us": 1e3 * res["bwd"],
-            "fwd_GBs": fb / res["fwd"] / 1e6, "bwd_GBs": bb / res["bwd"] / 1e6,
-            "step_GBs": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6,
-            "step_frac": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6 / peak,
-            "peak": peak, "peak_kind": peak_kind, "iters": args.steps,
-            "plan_fwd": {k: pf[k] for k in keep}, "plan_bwd": {k: pb[k] for k in keep}}),
-            flush=True)
+        line = {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
+                "fused_residual": fused, "fp8": args.fp8 or None, "fwd_us": 1e3 * res["fwd"],
+                "fwd_GBs": fb / res["fwd"] / 1e6, "peak": peak, "peak_kind": peak_kind,
+                "iters": args.steps, "plan_fwd": {k: pf[k] for k in keep}}
+        if pb is not None:
+            line.update({"bwd_us": 1e3 * res["bwd"], "bwd_GBs": bb / res["bwd"] / 1e6,
+                         "step_GBs": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6,
+                         "step_frac": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6 / peak,
+                         "plan_bwd": {k: pb[k] for k in keep}})
+        print(json.dumps(line), flush=True)
         del step, x, g, b, dy, r, dh
         torch.cuda.empty_cache()
 
@@ -581,6 +585,8 @@ def main():
                          "timings, one JSON line each (not the benchmark line)")
     ap.add_argument("--fused-residual", action="store_true",
                     help="with --sweep: time norm_add_fwd/norm_add_bwd (h = x + r fused in)")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="with --sweep: time the forward pass only")
     ap.add_argument("--fp8", choices=["", "row", "mx"], default="",
                     help="with --sweep: the forward writes E4M3 (norm_fwd_fp8) with per-row "
                          "or MX block scaling")

@@ -319,7 +319,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   // split: forced by the override, or preferred for E4M3 output (whose
   // per-row amax costs a reduction round that fewer, fuller warps per row
   // amortise) and for tuned shapes; otherwise the register-resident plan.
-  bool want_gsm = !bwd && (ov.gsm == 1 || (ov.gsm == -1 && (fp8 || tuned_gsm)));
+  bool want_gsm = !bwd && (ov.gsm == 1 || (ov.gsm == -1 && !ov.tpr && (fp8 || tuned_gsm)));
   if (want_gsm && !ov.tpr) {
     bool found = false;
     for (int k : {8, 6, 5}) {
@@ -338,6 +338,22 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
     exact = even && tpr % 32 == 0 && K * tpr == p.nsc;
   } else {
     bool found = false;
+    // E4M3 output of short rows: the per-row amax and scale cost the same
+    // per row whatever the row length, so give each thread as many chunks as
+    // registers allow and let sub-warp groups (down to 4 threads, the MX
+    // block width in chunks) cover the row (RMSNorm 256: 54 -> 85 % of
+    // measured, 768: 88 -> 93 %).
+    if (fp8 && !bwd && C == 1) {
+      for (int k = klim; k >= 1 && !found; --k) {
+        if (p.nsc % k) continue;
+        const int t = p.nsc / k;
+        if (t < 4 || t >= 32 || 32 % t) continue;
+        if (!fwd_fp8_kernel_ptr(mode, k, false, resid, kOutFp8Row)) continue;
+        tpr = t;
+        K = k;
+        found = true;
+      }
+    }
     for (int k = kpref; k >= 1 && !found; --k) found = try_exact(k, false);
     for (int k = kpref + 1; k <= klim && !found; ++k) found = try_exact(k, false);
     if (!found) {
