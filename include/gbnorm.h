@@ -291,6 +291,46 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
                         int sm_count, int smem_optin_bytes, norm_plan_t *out);
 
 /*
+ * Plan tuning.  The first page names the split size and the number of
+ * pipeline stages as what Inductor's autotuner searches for these kernels;
+ * the library's default plan comes from a heuristic and a table measured
+ * offline.  norm_tune_fwd / norm_tune_bwd measure, on the caller's buffers
+ * and stream, every register-resident plan of that pass (each threads-per-
+ * row value that splits the row within the compiled chunk counts, rows per
+ * group 1, 2, 4 or the heuristic's, and for the forward pass the plans with
+ * gamma/beta staged in shared memory), each `iters` times after two warm-up
+ * launches, and install the fastest in the process's plan cache for this
+ * (device, mode, pass, M, N): later norm_fwd / norm_bwd calls of that shape
+ * use it and norm_plan reports it (written to *chosen when not NULL).  Rows
+ * that need the long-row or cluster kernels keep their plan.  The outputs
+ * hold the chosen plan's results.  The call blocks until its measurements
+ * are done.
+ *
+ * A plan fixes the order of every floating-point reduction, so results are
+ * bitwise reproducible for a given plan; tuning can change the plan (and so
+ * the last bits of rstd, y, dx, dgamma, dbeta) from one process to the
+ * next.  norm_tune_reset drops every cached plan, tuned or not.
+ *
+ * Arguments as norm_fwd / norm_bwd (the backward candidates are limited to
+ * those whose partial rows fit workspace_bytes); iters in [1, 100000], else
+ * NORM_ERR_ARG; NORM_ERR_ARG also when the GBNORM_PLAN override is set
+ * (which bypasses the cache).
+ */
+norm_status_t norm_tune_fwd(const void *x, const void *gamma, const void *beta,
+                            int64_t M, int64_t N, float eps, norm_mode_t mode,
+                            void *y, float *rstd, float *mean, int iters,
+                            norm_plan_t *chosen, norm_stream_t stream);
+
+norm_status_t norm_tune_bwd(const void *dy, const void *x, const void *gamma,
+                            const float *rstd, const float *mean, int64_t M,
+                            int64_t N, norm_mode_t mode, void *dx,
+                            float *dgamma, float *dbeta, void *workspace,
+                            size_t workspace_bytes, int iters,
+                            norm_plan_t *chosen, norm_stream_t stream);
+
+norm_status_t norm_tune_reset(void);
+
+/*
  * norm_bwd_noalloc -- norm_bwd for callers that cannot allocate device
  * memory.  (An addition of this library; the normalisation pages describe
  * no such entry point.)

@@ -8,12 +8,13 @@ from ._binding import (FP8_MX, FP8_ROW, LAYER, RMS, NormError, declared_function
                        library_path, norm_add_bwd, norm_add_bwd_workspace_bytes, norm_add_fwd,
                        norm_bwd, norm_bwd_workspace_bytes, norm_fwd, norm_fwd_bwd_host,
                        norm_fwd_fp8, norm_get_device_error, norm_host_workspace_bytes,
-                       norm_plan, strerror)
+                       norm_plan, norm_tune_bwd, norm_tune_fwd, norm_tune_reset, strerror)
 from .builder import build
 
 __all__ = [
     "RMS", "LAYER", "NormError", "norm_fwd", "norm_bwd", "norm_bwd_workspace_bytes",
     "norm_get_device_error", "norm_plan", "norm_add_fwd", "norm_add_bwd",
     "norm_add_bwd_workspace_bytes", "norm_fwd_fp8", "FP8_ROW", "FP8_MX",
-    "norm_fwd_bwd_host", "norm_host_workspace_bytes", "strerror", "lib", "library_path", "declared_functions", "build",
+    "norm_fwd_bwd_host", "norm_host_workspace_bytes", "norm_tune_fwd", "norm_tune_bwd",
+    "norm_tune_reset", "strerror", "lib", "library_path", "declared_functions", "build",
 ]

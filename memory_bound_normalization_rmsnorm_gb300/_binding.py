@@ -101,6 +101,15 @@ def lib():
             L.norm_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp]
             L.norm_fwd_fp8.restype = ctypes.c_int
+            L.norm_tune_fwd.argtypes = [_vp, _vp, _vp, _i64, _i64, ctypes.c_float, ctypes.c_int,
+                                        _vp, _vp, _vp, ctypes.c_int, ctypes.POINTER(Plan), _vp]
+            L.norm_tune_fwd.restype = ctypes.c_int
+            L.norm_tune_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp,
+                                        _vp, _vp, _vp, ctypes.c_size_t, ctypes.c_int,
+                                        ctypes.POINTER(Plan), _vp]
+            L.norm_tune_bwd.restype = ctypes.c_int
+            L.norm_tune_reset.argtypes = []
+            L.norm_tune_reset.restype = ctypes.c_int
             L.norm_host_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int, _i64,
                                                     ctypes.POINTER(ctypes.c_size_t)]
             L.norm_host_workspace_bytes.restype = ctypes.c_int
@@ -313,6 +322,59 @@ def norm_fwd_fp8(x, gamma, beta=None, eps=1e-5, mode=RMS, scaling=FP8_ROW, *, r=
     if st != 0:
         raise NormError(st, "norm_fwd_fp8")
     return q, scale, rstd, mean, h
+
+
+def norm_tune_fwd(x, gamma, beta=None, eps=1e-5, mode=RMS, *, iters=20, stream=None):
+    """Measure the forward plans of this shape on these buffers and keep the
+    fastest (norm_tune_fwd in gbnorm.h).  Returns the chosen plan (dict)."""
+    mode = int(mode)
+    M, N = _rows(x)
+    dev = x.device
+    _check_tensor(x, "x", torch.bfloat16, x.shape, dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (N,), dev)
+    _check_tensor(beta, "beta", torch.bfloat16, (N,), dev)
+    y = torch.empty_like(x)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=dev)
+    mean = torch.empty_like(rstd) if mode == LAYER else None
+    out = Plan()
+    st = lib().norm_tune_fwd(_ptr(x), _ptr(gamma), _ptr(beta), M, N, float(eps), mode, _ptr(y),
+                             _ptr(rstd), _ptr(mean), int(iters), ctypes.byref(out),
+                             _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_tune_fwd")
+    return out.as_dict()
+
+
+def norm_tune_bwd(dy, x, gamma, rstd, mean=None, mode=RMS, *, iters=20, stream=None):
+    """Measure the backward plans of this shape on these buffers and keep the
+    fastest (norm_tune_bwd in gbnorm.h).  Returns the chosen plan (dict)."""
+    mode = int(mode)
+    M, N = _rows(x)
+    dev = x.device
+    for t, n in ((x, "x"), (dy, "dy")):
+        _check_tensor(t, n, torch.bfloat16, x.shape, dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (N,), dev)
+    _check_tensor(rstd, "rstd", torch.float32, x.shape[:-1], dev)
+    _check_tensor(mean, "mean", torch.float32, x.shape[:-1], dev)
+    dx = torch.empty_like(x)
+    dg = torch.empty(N, dtype=torch.float32, device=dev)
+    db = torch.empty(N, dtype=torch.float32, device=dev) if mode == LAYER else None
+    ws = torch.empty(max(norm_bwd_workspace_bytes(M, N, mode), 16), dtype=torch.uint8,
+                     device=dev)
+    out = Plan()
+    st = lib().norm_tune_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(mean), M, N, mode,
+                             _ptr(dx), _ptr(dg), _ptr(db), _ptr(ws), ws.numel(), int(iters),
+                             ctypes.byref(out), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_tune_bwd")
+    return out.as_dict()
+
+
+def norm_tune_reset():
+    """Drop every cached plan (tuned or default)."""
+    st = lib().norm_tune_reset()
+    if st != 0:
+        raise NormError(st, "norm_tune_reset")
 
 
 def norm_host_workspace_bytes(M, N, mode=RMS, chunk_rows=0) -> int:

@@ -23,6 +23,7 @@
 #include <mutex>
 #include <set>
 #include <tuple>
+#include <vector>
 
 #include "../../include/gbnorm.h"
 #include "common.cuh"
@@ -156,8 +157,8 @@ constexpr TunedPlan kTuned[] = {
     {kLayer, 0, 2048, 64, 0, 3},  {kLayer, 0, 3072, 0, 0, 0, 1}, {kLayer, 0, 5120, 0, 0, 0, 1},
     {kLayer, 0, 8192, 0, 0, 0, 1},
     {kRMS, 1, 256, 32, 2, 5},     {kRMS, 1, 512, 64, 0, 0},    {kRMS, 1, 768, 64, 4, 0},
-    {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 5120, 256, 2, 0},
-    {kLayer, 1, 3072, 192, 4, 0}, {kLayer, 1, 5120, 256, 2, 0},
+    {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 2048, 128, 1, 7},  {kRMS, 1, 5120, 256, 2, 0},
+    {kLayer, 1, 3072, 192, 4, 0}, {kLayer, 1, 5120, 320, 4, 2},
 };
 
 // Ring and tile sizing shared by both plan kinds: rows per tile and the
@@ -399,6 +400,9 @@ void set_grid(Plan &p, int64_t resident_clusters) {
   p.grid = static_cast<int>(clusters * p.C);
 }
 
+norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, const Override &ov,
+                          Plan *pp);
+
 // Full plan on the current device: shape part plus the occupancy-derived
 // grid (persistent: as many CTAs or clusters as can be resident at once).
 norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_t M, int N,
@@ -417,7 +421,23 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
   Plan p;
   norm_status_t st = shape_plan(mode, bwd, M, N, d.smem_optin, ov, &p, resid, fp8);
   if (st != NORM_OK) return st;
+  st = finish_plan(d, dev, mode, bwd, ov, &p);
+  if (st != NORM_OK) return st;
 
+  if (!ov.any) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_plans[key] = p;
+  }
+  *out = p;
+  return NORM_OK;
+}
+
+// The device-dependent part of a plan: kernel attributes and the persistent
+// grid from the occupancy of the chosen kernel.
+norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, const Override &ov,
+                          Plan *pp) {
+  Plan &p = *pp;
+  norm_status_t st;
   const void *fn = kernel_for(p, mode, bwd);
   if (!fn) return NORM_ERR_UNSUPPORTED;
   st = prepare_function(dev, fn, d.smem_optin);
@@ -454,12 +474,6 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
   }
   if (resident < 1) return NORM_ERR_UNSUPPORTED;
   set_grid(p, resident);
-
-  if (!ov.any) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_plans[key] = p;
-  }
-  *out = p;
   return NORM_OK;
 }
 
@@ -540,6 +554,147 @@ NormArgs base_args(const Plan &p, int64_t M, int N) {
   a.ntiles = p.ntiles;
   a.invN = 1.0f / static_cast<float>(N);
   return a;
+}
+
+void fill_plan(const Plan &p, norm_plan_t *out) {
+  out->cluster = p.C;
+  out->cols_per_cta = p.NS;
+  out->threads_per_row = p.tpr;
+  out->chunks_per_thread = p.K;
+  out->groups = p.G;
+  out->rows_per_group = p.rpg;
+  out->rows_per_tile = p.RT;
+  out->stages = p.S;
+  out->threads = p.threads;
+  out->smem_bytes = static_cast<int32_t>(p.smem);
+  out->tiles = p.ntiles;
+  out->grid = p.grid;
+  out->partials = p.P;
+  out->exact = p.exact ? 1 : 0;
+  out->long_rows = p.long_rows ? 1 : 0;
+  out->param_smem_bytes = p.par_bpc * p.NS;
+}
+
+// ------------------------------------------------------------ plan tuning
+// The pages name the split size and the number of pipeline stages as the
+// levers an autotuner turns for these kernels; here the candidates are the
+// register-resident plans of one pass: every threads-per-row value that
+// splits the row (exactly, or raggedly over a power of two) within the
+// compiled chunk counts, rows per group 1, 2, 4 or the heuristic's, and for
+// the forward pass the staged-parameter plans.  Rows that need the long-row
+// or cluster kernels keep their plan.
+std::vector<Override> tune_candidates(bool bwd, int N) {
+  std::vector<Override> v;
+  const int nsc = N / 8;
+  const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
+  std::vector<int> tprs;
+  for (int k = 1; k <= kmax; ++k) {
+    if (nsc % k) continue;
+    const int t = nsc / k;
+    if ((t <= 32 && 32 % t == 0) || (t % 32 == 0 && t <= kMaxThreads)) tprs.push_back(t);
+  }
+  for (int t = 1; t <= kMaxThreads; t *= 2)
+    if (ceil_div(nsc, t) <= kmax && t <= pow2ceil(nsc)) tprs.push_back(t);
+  std::sort(tprs.begin(), tprs.end());
+  tprs.erase(std::unique(tprs.begin(), tprs.end()), tprs.end());
+  for (int t : tprs) {
+    for (int rpg : {0, 1, 2, 4}) {
+      Override o;
+      o.any = true;
+      o.tpr = t;
+      o.rpg = rpg;
+      o.gsm = 0;
+      o.lng = 0;
+      o.C = 1;
+      v.push_back(o);
+    }
+  }
+  if (!bwd) {
+    for (int k : {5, 6, 8}) {
+      if (nsc % k || (nsc / k) % 32 || nsc / k > kMaxThreads) continue;
+      for (int rpg : {0, 1, 2}) {
+        Override o;
+        o.any = true;
+        o.tpr = nsc / k;
+        o.rpg = rpg;
+        o.gsm = 1;
+        o.lng = 0;
+        o.C = 1;
+        v.push_back(o);
+      }
+    }
+  }
+  return v;
+}
+
+bool same_plan(const Plan &a, const Plan &b) {
+  return a.C == b.C && a.tpr == b.tpr && a.K == b.K && a.G == b.G && a.rpg == b.rpg &&
+         a.S == b.S && a.gsm == b.gsm && a.long_rows == b.long_rows && a.grid == b.grid;
+}
+
+// Times `run` (one launch of the pass with the plan installed in the cache
+// under `key`) for every candidate and leaves the fastest installed.
+template <typename Run>
+norm_status_t tune_pass(int mode, bool bwd, int64_t M, int N, size_t ws_bytes, int iters,
+                        cudaStream_t stream, Run run, norm_plan_t *chosen) {
+  if (iters < 1 || iters > 100000) return NORM_ERR_ARG;
+  if (read_override().any) return NORM_ERR_ARG;  // a plan override bypasses the cache
+  norm_status_t st = run();                      // validates, caches the default plan
+  if (st != NORM_OK) return st;
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  Plan def;
+  if ((st = make_plan(d, dev, mode, bwd, M, N, &def)) != NORM_OK) return st;
+  const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, 0);
+  auto install = [&](const Plan &p) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_plans[key] = p;
+  };
+  std::vector<Plan> cands{def};
+  if (def.C == 1 && !def.long_rows) {
+    for (const Override &o : tune_candidates(bwd, N)) {
+      Plan p;
+      if (shape_plan(mode, bwd, M, N, d.smem_optin, o, &p) != NORM_OK) continue;
+      if (p.C != 1 || p.long_rows) continue;
+      if (finish_plan(d, dev, mode, bwd, o, &p) != NORM_OK) continue;
+      const size_t need = static_cast<size_t>(p.P) * N * 4 * (mode == kLayer ? 2 : 1);
+      if (bwd && need > ws_bytes) continue;
+      bool dup = false;
+      for (const Plan &q : cands) dup = dup || same_plan(p, q);
+      if (!dup) cands.push_back(p);
+    }
+  }
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  float best_ms = 0.f;
+  int best = -1;
+  for (size_t i = 0; i < cands.size(); ++i) {
+    install(cands[i]);
+    bool ok = run() == NORM_OK && run() == NORM_OK;  // warm-up
+    ok = ok && cudaEventRecord(e0, stream) == cudaSuccess;
+    for (int it = 0; it < iters && ok; ++it) ok = run() == NORM_OK;
+    ok = ok && cudaEventRecord(e1, stream) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
+    float ms = 0.f;
+    ok = ok && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      continue;
+    }
+    if (best < 0 || ms < best_ms) {
+      best_ms = ms;
+      best = static_cast<int>(i);
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  install(cands[best < 0 ? 0 : best]);
+  if ((st = run()) != NORM_OK) return st;  // outputs of the chosen plan
+  if (chosen) fill_plan(cands[best < 0 ? 0 : best], chosen);
+  return best < 0 ? NORM_ERR_CUDA : NORM_OK;
 }
 
 }  // namespace
@@ -811,22 +966,38 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
     if ((st = make_plan(d, dev, mode, bwd, M, static_cast<int>(N), &p, resid, fp8)) != NORM_OK)
       return st;
   }
-  out->cluster = p.C;
-  out->cols_per_cta = p.NS;
-  out->threads_per_row = p.tpr;
-  out->chunks_per_thread = p.K;
-  out->groups = p.G;
-  out->rows_per_group = p.rpg;
-  out->rows_per_tile = p.RT;
-  out->stages = p.S;
-  out->threads = p.threads;
-  out->smem_bytes = static_cast<int32_t>(p.smem);
-  out->tiles = p.ntiles;
-  out->grid = p.grid;
-  out->partials = p.P;
-  out->exact = p.exact ? 1 : 0;
-  out->long_rows = p.long_rows ? 1 : 0;
-  out->param_smem_bytes = p.par_bpc * p.NS;
+  fill_plan(p, out);
+  return NORM_OK;
+}
+
+norm_status_t norm_tune_fwd(const void *x, const void *gamma, const void *beta, int64_t M,
+                            int64_t N, float eps, norm_mode_t mode, void *y, float *rstd,
+                            float *mean, int iters, norm_plan_t *chosen, norm_stream_t stream) {
+  auto run = [&]() { return norm_fwd(x, gamma, beta, M, N, eps, mode, y, rstd, mean, stream); };
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  return tune_pass(mode, false, M, static_cast<int>(N), 0, iters,
+                   reinterpret_cast<cudaStream_t>(stream), run, chosen);
+}
+
+norm_status_t norm_tune_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
+                            const float *mean, int64_t M, int64_t N, norm_mode_t mode, void *dx,
+                            float *dgamma, float *dbeta, void *workspace,
+                            size_t workspace_bytes, int iters, norm_plan_t *chosen,
+                            norm_stream_t stream) {
+  auto run = [&]() {
+    return norm_bwd(dy, x, gamma, rstd, mean, M, N, mode, dx, dgamma, dbeta, workspace,
+                    workspace_bytes, stream);
+  };
+  norm_status_t st = check_common(M, N, mode);
+  if (st != NORM_OK) return st;
+  return tune_pass(mode, true, M, static_cast<int>(N), workspace_bytes, iters,
+                   reinterpret_cast<cudaStream_t>(stream), run, chosen);
+}
+
+norm_status_t norm_tune_reset(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_plans.clear();
   return NORM_OK;
 }
 

@@ -119,6 +119,17 @@ def test_host_pipeline_validation_codes():
     assert gb.lib().norm_host_workspace_bytes(4, 64, 0, 0, None) == 1
 
 
+def test_tune_validation_codes():
+    f = gb.lib().norm_tune_fwd
+    assert f(F, F, None, 0, 64, ctypes.c_float(1e-5), 0, F, F, None, 5, None, None) == 2
+    assert f(F, F, None, 4, 64, ctypes.c_float(1e-5), 7, F, F, None, 5, None, None) == 4
+    assert f(F, F, None, 4, 64, ctypes.c_float(1e-5), 0, F, F, None, 0, None, None) == 9
+    fb = gb.lib().norm_tune_bwd
+    assert fb(F, F, F, F, None, 4, 12, 0, F, F, None, F, 64, 5, None, None) == 2
+    assert fb(F, F, F, F, None, 4, 64, 0, F, F, None, F, 64, -1, None, None) == 9
+    assert gb.lib().norm_tune_reset() == 0
+
+
 def test_bwd_validation_codes():
     f = gb.lib().norm_bwd
     ok = dict(dy=F, x=F, g=F, r=F, m=None, M=4, N=16, mode=0, dx=F, dg=F, db=None, ws=F,
