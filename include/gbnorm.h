@@ -139,9 +139,10 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma,
  * and the backward pass adds the gradient dh that reaches h through the
  * residual path:  dx = (norm_bwd's dx at h) + dh  (sum in fp32, one rounding);
  * dx is the gradient of both x and r.  dgamma / dbeta as norm_bwd.
- * Shapes: rows that fit one CTA (N up to 16384 for LAYER, 24576 for RMS in
- * the forward pass; 8192 / 12288 in the backward pass); longer rows return
- * NORM_ERR_UNSUPPORTED.  Other requirements as norm_fwd / norm_bwd.
+ * Shapes: as norm_fwd / norm_bwd (N up to NORM_MAX_N); rows wider than one
+ * CTA's registers use the long-row kernels (and thread-block clusters) with
+ * the residual tensor in the same shared-memory stage.  Other requirements
+ * as norm_fwd / norm_bwd.
  *
  * norm_add_fwd:  x, r bf16 [M, N] inputs; h, y bf16 [M, N] outputs; rstd,
  *                mean (LAYER) fp32 [M] outputs; gamma, beta as norm_fwd.

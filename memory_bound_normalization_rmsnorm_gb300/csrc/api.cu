@@ -208,42 +208,50 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
 // backward), two row groups of up to 256 threads per CTA when the slice
 // allows, and the smallest power-of-two cluster whose slices fit.
 norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, const Override &ov,
-                        Plan *out) {
+                        Plan *out, bool resid = false) {
   const int nc = N / 8;
-  Plan p;
-  p.long_rows = true;
-  p.occ = ov.occ ? ov.occ : 1;
   // 8 chunks per thread only where that fits in registers without spilling
   // (RMSNorm forward); 4 elsewhere.
-  int K = ov.K ? ov.K : ((!bwd && mode == kRMS) ? 8 : 4);
+  const int K = ov.K ? ov.K : ((!bwd && mode == kRMS) ? 8 : 4);
   if (K != 2 && K != 4 && K != 8) return NORM_ERR_UNSUPPORTED;
   // Slices up to kMaxThreads threads x K chunks per CTA; clusters when the
-  // row is wider.  Without a cluster, up to two row groups per CTA overlap
-  // each other's reductions; in a cluster one group of up to kMaxThreads
-  // threads per CTA, the cross-CTA exchange being overlapped by the kernel's
-  // software pipeline instead.
+  // row is wider, or when a stage of the CTA's slice (x, and dy and / or the
+  // residual tensor) would not leave room for two stages.  Without a
+  // cluster, up to two row groups per CTA overlap each other's reductions;
+  // in a cluster one group of up to kMaxThreads threads per CTA, the
+  // cross-CTA exchange being overlapped by the kernel's software pipeline.
   int C = 1;
   while (C < 16 && ceil_div(nc, C) > kMaxThreads * K) C <<= 1;
   if (ov.C) C = ov.C;
-  if (C < 1 || C > 16) return NORM_ERR_UNSUPPORTED;
-  p.C = C;
-  p.nsc = ceil_div(nc, C);
-  p.NS = p.nsc * 8;
-  if ((C - 1) * p.nsc >= nc) return NORM_ERR_UNSUPPORTED;
-  int tpr = ov.tpr ? ov.tpr : 32 * ceil_div(ceil_div(p.nsc, K), 32);
-  if (tpr < 32 || tpr > kMaxThreads || tpr % 32) return NORM_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(tpr) * K < p.nsc) return NORM_ERR_UNSUPPORTED;
-  p.tpr = tpr;
-  p.K = K;
-  p.exact = (nc % C == 0) && (tpr * K == p.nsc);
-  p.G = ov.G ? ov.G : (C > 1 ? 1 : std::max(1, std::min(2, kMaxThreads / tpr)));
-  if (p.G * tpr > kMaxThreads || p.G > 15) return NORM_ERR_UNSUPPORTED;
-  if (C > 1 && p.G != 1) return NORM_ERR_UNSUPPORTED;  // one row per CTA per tile
-  norm_status_t st = size_ring(p, bwd, smem_optin, ov, M);
-  if (st != NORM_OK) return st;
-  if (!long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ)) return NORM_ERR_UNSUPPORTED;
-  *out = p;
-  return NORM_OK;
+  for (;; C <<= 1) {
+    if (C < 1 || C > 16) return NORM_ERR_UNSUPPORTED;
+    Plan p;
+    p.long_rows = true;
+    p.resid = resid;
+    p.occ = ov.occ ? ov.occ : 1;
+    p.C = C;
+    p.nsc = ceil_div(nc, C);
+    p.NS = p.nsc * 8;
+    if ((C - 1) * p.nsc >= nc) return NORM_ERR_UNSUPPORTED;
+    const int tpr = ov.tpr ? ov.tpr : 32 * ceil_div(ceil_div(p.nsc, K), 32);
+    if (tpr < 32 || tpr > kMaxThreads || tpr % 32) return NORM_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(tpr) * K < p.nsc) return NORM_ERR_UNSUPPORTED;
+    p.tpr = tpr;
+    p.K = K;
+    p.exact = (nc % C == 0) && (tpr * K == p.nsc);
+    p.G = ov.G ? ov.G : (C > 1 ? 1 : std::max(1, std::min(2, kMaxThreads / tpr)));
+    if (p.G * tpr > kMaxThreads || p.G > 15) return NORM_ERR_UNSUPPORTED;
+    if (C > 1 && p.G != 1) return NORM_ERR_UNSUPPORTED;  // one row per CTA per tile
+    norm_status_t st = size_ring(p, bwd, smem_optin, ov, M);
+    if (st != NORM_OK) {
+      if (ov.C) return st;
+      continue;  // a wider cluster halves the slice
+    }
+    if (!long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ, resid))
+      return NORM_ERR_UNSUPPORTED;
+    *out = p;
+    return NORM_OK;
+  }
 }
 
 // Shape part of the plan for one pass: everything except the grid size.
@@ -279,18 +287,23 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   // Rows wider than one CTA's register capacity (kMaxThreads x klim chunks)
   // go to the long-row kernels, which keep the row in shared memory.
   if (ov.lng == 1 || (ov.lng != 0 && nc > kMaxThreads * klim)) {
-    if (resid) return NORM_ERR_UNSUPPORTED;  // fused residual: register-resident rows only
-    return long_plan(mode, bwd, M, N, smem_optin, ov, out);
+    if (fp8) return NORM_ERR_UNSUPPORTED;  // E4M3 output: register-resident rows only
+    return long_plan(mode, bwd, M, N, smem_optin, ov, out, resid);
   }
 
   // Column split: the smallest power-of-two cluster (up to 8) whose per-CTA
   // slice fits kMaxThreads threads x kpref chunks, else the smallest (up to
   // 16) that fits klim, else kmax chunks.  Slices are ceil(nc / C) chunks;
   // the last CTA of a cluster takes the remainder.
+  // (The fused residual add has no register-resident cluster variants: it
+  // keeps C = 1 up to klim chunks per thread; wider rows took the long-row
+  // path above.)
   int C = 1;
-  while (C < 8 && ceil_div(nc, C) > kMaxThreads * kpref) C <<= 1;
-  while (C < 16 && ceil_div(nc, C) > kMaxThreads * klim) C <<= 1;
-  while (C <= 16 && ceil_div(nc, C) > kMaxThreads * kmax) C <<= 1;
+  if (!resid) {
+    while (C < 8 && ceil_div(nc, C) > kMaxThreads * kpref) C <<= 1;
+    while (C < 16 && ceil_div(nc, C) > kMaxThreads * klim) C <<= 1;
+    while (C <= 16 && ceil_div(nc, C) > kMaxThreads * kmax) C <<= 1;
+  }
   if (ov.C) C = ov.C;
   if (C < 1 || C > 16 || (resid && C != 1)) return NORM_ERR_UNSUPPORTED;
   p.C = C;
@@ -389,7 +402,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 }
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
-  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ);
+  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ, p.resid);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm);
 }

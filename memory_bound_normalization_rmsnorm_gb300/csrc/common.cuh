@@ -162,7 +162,9 @@ const void *reduce_kernel_ptr();
 // Long-row kernels (row slice re-read from shared memory), K in {4, 8}.
 // occ = CTAs per SM the kernel is compiled for (only 1 is built: a
 // two-CTA-per-SM variant capped at 64 registers measured 40 % slower).
-const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ);
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ,
+                            bool resid = false);
+const void *long_resid_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd);
 int reduce_threads();
 const void *selftest_kernel_ptr();
 

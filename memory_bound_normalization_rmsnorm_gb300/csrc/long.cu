@@ -1,525 +1,41 @@
-// long.cu -- forward and backward kernels for long rows.
-//
-// Same pipeline as fwd.cu / bwd.cu (persistent grid, bulk-copy ring of S
-// stages, last-warp refill, fixed-order reductions, cluster column split
-// with DSMEM pushes), with two differences:
-//   - the row slice is NOT copied into registers: it is read from the
-//     shared-memory stage twice (statistics or dot products, then outputs),
-//     so registers hold only per-column state (gamma, beta, the dgamma/dbeta
-//     accumulators) and a CTA can own a wide slice (up to 8 chunks of 8
-//     columns per thread);
-//   - in a cluster the cross-CTA exchange is software-pipelined: the partial
-//     of the current tile's row is pushed to the peers, and only then is the
-//     previous tile finished (wait for its exchange, outputs, stage
-//     release), so the DSMEM round trip overlaps a full statistics pass.
-// LayerNorm statistics use one exchange round of (count, mean, M2) merges.
-//
-// What is computed follows the same page paragraphs as fwd.cu and bwd.cu
-// ("PyTorch atinge desempenho SOTA em normalizacao com torch.compile":
-// LayerNorm/RMSNorm definitions, forward reduction + pointwise pass, fused
-// backward with split column reduction).
-#include "common.cuh"
-#include "ptx.cuh"
-#include "rowops.cuh"
-#include "tiles.cuh"
+// long.cu -- instantiations of the long-row kernels (long_kernel.cuh)
+// without the fused residual add.
+#include "long_kernel.cuh"
 
 namespace gbn {
 
 namespace {
 
-__device__ __forceinline__ uint4 lds_chunk(const unsigned char *p) {
-  return *reinterpret_cast<const uint4 *>(p);
-}
-
-// State of a tile whose statistics are pushed but whose outputs are not
-// written yet.
-struct Pending {
-  int64_t tile;
-  int s;
-  float a, b, c;  // this row group's partial (also the total without a cluster)
-};
-
-// OCC: CTAs per SM the kernel is compiled for (2 caps registers at 64).
-template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC>
-__global__ void __launch_bounds__(kMaxThreads, OCC) norm_fwd_long_kernel(const NormArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 1, false, a.C);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-  float *red = reinterpret_cast<float *>(smem + L.red_off);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
-  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
-
-  const int tid = threadIdx.x;
-  const int g = tid / a.tpr;
-  const int t = tid - g * a.tpr;
-  const int nwarps = blockDim.x >> 5;
-  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
-  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
-  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
-  const int col0 = crank * a.NS;
-  const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
-
-  if (tid == 0) {
-    for (int s = 0; s < a.S; ++s) {
-      mbar_init(full + s, 1);
-      done_cnt[s] = 0;
-    }
-    if (CLUSTER) {
-      uint64_t *xb = xch_bars(smem, L, a.RT, a.C);
-      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  // Programmatic dependent launch: let the next kernel in the stream start
-  // its prologue as our CTAs retire, and touch no global memory before the
-  // previous kernel's writes are complete and visible.
-  grid_launch_dependents();
-  grid_dependency_wait();
-
-  // Per-column state: gamma and beta of this thread's chunks, packed bf16.
-  uint4 gv[K], bv[K];
-  int nown = 0;  // chunks this thread owns
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int c = t + k * a.tpr;
-    gv[k] = make_uint4(0, 0, 0, 0);
-    bv[k] = make_uint4(0, 0, 0, 0);
-    if (c < nsc_me) {
-      ++nown;
-      gv[k] = ld_global_nc_v4(a.gamma + col0 + c * 8);
-      if (MODE == kLayer && a.beta != nullptr) bv[k] = ld_global_nc_v4(a.beta + col0 + c * 8);
-    }
-  }
-
-  if (CLUSTER) cluster_sync(); else __syncthreads();
-
-  const uint64_t pol = l2_evict_first_policy();
-  if (tid == 0) {
-    for (int j = 0; j < a.S; ++j) {
-      const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_fwd_tile<CLUSTER>(a, L, smem, tile, j, col0, nsc_me, pol);
-    }
-  }
-
-  const float invN = a.invN;
-  const int cstep = a.tpr * 16;
-  int rpar = 0;
-  ClusterXch xch = make_xch(smem, L, a.RT, CLUSTER ? a.C : 1, crank);
-
-  // Statistics pass of row slot r of the stage at `st`: this row group's
-  // partial, (n, mean, M2) for LayerNorm or (sum x^2) for RMSNorm.
-  auto stats_pass = [&](const unsigned char *st, int r, bool active, float &pa, float &pb,
-                        float &pc) {
-    const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2 + t * 16;
-    if (MODE == kLayer) {
-      float2 a0 = splat2(0.f), a1 = splat2(0.f);
-      if (active) {
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          if (EXACT || t + k * a.tpr < nsc_me) {
-            float2 xf[4];
-            chunk_to_f2(lds_chunk(rowp + k * cstep), xf);
-            a0 = add2(a0, add2(xf[0], xf[1]));
-            a1 = add2(a1, add2(xf[2], xf[3]));
-          }
-        }
-      }
-      const float2 at = add2(a0, a1);
-      float n = active ? 8.f * static_cast<float>(nown) : 0.f;
-      float m = n > 0.f ? (at.x + at.y) / n : 0.f;
-      const float2 nm = splat2(-m);
-      float2 q0 = splat2(0.f), q1 = splat2(0.f);
-      if (active) {
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          if (EXACT || t + k * a.tpr < nsc_me) {
-            float2 xf[4];
-            chunk_to_f2(lds_chunk(rowp + k * cstep), xf);
-            const float2 d0 = add2(xf[0], nm), d1 = add2(xf[1], nm);
-            const float2 d2 = add2(xf[2], nm), d3 = add2(xf[3], nm);
-            q0 = fma2(d0, d0, fma2(d1, d1, q0));
-            q1 = fma2(d2, d2, fma2(d3, d3, q1));
-          }
-        }
-      }
-      const float2 qt = add2(q0, q1);
-      float q = qt.x + qt.y;
-      group_nmeanvar(n, m, q, a.tpr, g, a.G, t, red, rpar);
-      pa = m;
-      pb = q;
-      pc = n;
-    } else {
-      float2 q0 = splat2(0.f), q1 = splat2(0.f);
-      if (active) {
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          if (EXACT || t + k * a.tpr < nsc_me) {
-            float2 xf[4];
-            chunk_to_f2(lds_chunk(rowp + k * cstep), xf);
-            q0 = fma2(xf[0], xf[0], fma2(xf[1], xf[1], q0));
-            q1 = fma2(xf[2], xf[2], fma2(xf[3], xf[3], q1));
-          }
-        }
-      }
-      const float2 qt = add2(q0, q1);
-      float v[1] = {qt.x + qt.y};
-      group_sum<1, EXACT>(v, a.tpr, g, a.G, t, red, rpar);
-      pa = v[0];
-      pb = 0.f;
-      pc = 0.f;
-    }
-  };
-
-  // Output pass of row slot r given the row totals; writes y and the
-  // statistics.
-  auto output_pass = [&](const unsigned char *st, int64_t row0, int r, float ta, float tb) {
-    float rs, mu = 0.f;
-    if (MODE == kLayer) {
-      mu = ta;
-      rs = rsqrtf(tb * invN + a.eps);
-    } else {
-      rs = rsqrtf(ta * invN + a.eps);
-    }
-    const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2 + t * 16;
-    const float2 rs2 = splat2(rs), nmu = splat2(-mu);
-    uint16_t *yrow = a.out + (row0 + r) * a.N + col0 + t * 8;
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      if (EXACT || t + k * a.tpr < nsc_me) {
-        float2 xf[4], gf[4], bf[4], o[4];
-        chunk_to_f2(lds_chunk(rowp + k * cstep), xf);
-        chunk_to_f2(gv[k], gf);
-        if (MODE == kLayer) chunk_to_f2(bv[k], bf);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const float2 xh = mul2(MODE == kLayer ? add2(xf[p], nmu) : xf[p], rs2);
-          o[p] = (MODE == kLayer) ? fma2(xh, gf[p], bf[p]) : mul2(xh, gf[p]);
-        }
-        st_global_cs_v4(yrow + k * a.tpr * 8, f2_to_chunk(o));
-      }
-    }
-    if (t == 0 && crank == 0) {
-      a.rstd[row0 + r] = rs;
-      if (MODE == kLayer) a.mean[row0 + r] = mu;
-    }
-  };
-
-  // Stage s is consumed: the last warp refills it with the tile S ahead.
-  auto release = [&](int64_t tile, int s) {
-    if (last_warp_done(done_cnt, s, nwarps) && (tid & 31) == 0) {
-      const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
-      if (next < a.ntiles) {
-        fence_proxy_async_smem();
-        issue_fwd_tile<CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
-      }
-    }
-  };
-
-  // Finish a pending cluster tile: wait for its exchange, fold in rank
-  // order, write outputs, release the stage.  (Cluster tiles hold one row
-  // per group: rows_per_group is 1.)
-  auto finish = [&](const Pending &p) {
-    const int64_t row0 = p.tile * a.RT;
-    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-    const int r = g;
-    const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
-    float ta, tb;
-    if (MODE == kLayer) {
-      float n, m, q;
-      fold_nmeanvar(row, xch.C, n, m, q);
-      ta = m;
-      tb = q;
-    } else {
-      float v[1];
-      fold_sum<1>(row, xch.C, v);
-      ta = v[0];
-      tb = 0.f;
-    }
-    if (r < nrows) output_pass(smem + static_cast<size_t>(p.s) * L.stage_bytes, row0, r, ta, tb);
-    release(p.tile, p.s);
-  };
-
-  int s = 0;
-  uint32_t par = 0;
-  Pending pend;
-  bool have_pend = false;
-  for (int64_t tile = cid; tile < a.ntiles; tile += ncl) {
-    mbar_wait(full + s, par, a.err, abort_flag);
-    const int64_t row0 = tile * a.RT;
-    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-    const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes;
-    if (CLUSTER) {
-      const int r = g;
-      Pending cur;
-      cur.tile = tile;
-      cur.s = s;
-      stats_pass(st, r, r < nrows, cur.a, cur.b, cur.c);
-      cluster_push(cur.a, cur.b, cur.c, r, t, xch);
-      if (have_pend) finish(pend);
-      pend = cur;
-      have_pend = true;
-    } else {
-      for (int q = 0; q < a.rpg; ++q) {
-        const int r = g + q * a.G;
-        const bool active = r < nrows;
-        float pa, pb, pc;
-        stats_pass(st, r, active, pa, pb, pc);
-        if (active) output_pass(st, row0, r, pa, pb);
-      }
-      release(tile, s);
-    }
-    if (++s == a.S) {
-      s = 0;
-      par ^= 1u;
-    }
-  }
-  if (CLUSTER) {
-    if (have_pend) finish(pend);
-    cluster_sync();
-  }
-}
-
-template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC>
-__global__ void __launch_bounds__(kMaxThreads, OCC) norm_bwd_long_kernel(const NormArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, a.C);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-  float *red = reinterpret_cast<float *>(smem + L.red_off);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
-  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
-
-  const int tid = threadIdx.x;
-  const int g = tid / a.tpr;
-  const int t = tid - g * a.tpr;
-  const int nwarps = blockDim.x >> 5;
-  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
-  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
-  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
-  const int col0 = crank * a.NS;
-  const int nsc_me = min(a.nsc, a.N / 8 - crank * a.nsc);
-
-  if (tid == 0) {
-    for (int s = 0; s < a.S; ++s) {
-      mbar_init(full + s, 1);
-      done_cnt[s] = 0;
-    }
-    if (CLUSTER) {
-      uint64_t *xb = xch_bars(smem, L, a.RT, a.C);
-      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  // Programmatic dependent launch: let the next kernel in the stream start
-  // its prologue as our CTAs retire, and touch no global memory before the
-  // previous kernel's writes are complete and visible.
-  grid_launch_dependents();
-  grid_dependency_wait();
-
-  // Per-column state: gamma (packed bf16) and the fp32 column accumulators.
-  uint4 gv[K];
-  float2 accg[K][4], accb[K][4];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int c = t + k * a.tpr;
-    gv[k] = (c < nsc_me) ? ld_global_nc_v4(a.gamma + col0 + c * 8) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      accg[k][p] = splat2(0.f);
-      accb[k][p] = splat2(0.f);
-    }
-  }
-
-  if (CLUSTER) cluster_sync(); else __syncthreads();
-
-  const uint64_t pol = l2_evict_first_policy();
-  if (tid < 32) {
-    for (int j = 0; j < a.S; ++j) {
-      const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_bwd_tile<MODE, CLUSTER>(a, L, smem, tile, j, col0, nsc_me, pol);
-    }
-  }
-
-  const float invN = a.invN;
-  const int cstep = a.tpr * 16;
-  int rpar = 0;
-  ClusterXch xch = make_xch(smem, L, a.RT, CLUSTER ? a.C : 1, crank);
-  const float *stats_all = reinterpret_cast<const float *>(smem + L.stats_off);
-
-  // Dot-product pass of row slot r of stage s: sum(g) and sum(g * xhat) of
-  // this row group (group totals), and the column accumulators.
-  auto dot_pass = [&](int s, int r, bool active, float &pa, float &pb) {
-    const unsigned char *xrow = smem + static_cast<size_t>(s) * L.stage_bytes +
-                                static_cast<size_t>(r) * a.NS * 2 + t * 16;
-    const float *stats = stats_all + static_cast<size_t>(s) * a.RT * 2;
-    float rs = 0.f, mu = 0.f;
-    if (active) {
-      rs = stats[2 * r];
-      if (MODE == kLayer) mu = stats[2 * r + 1];
-    }
-    const float2 rs2 = splat2(rs), nmu = splat2(-mu);
-    float2 s1 = splat2(0.f), s2 = splat2(0.f), s1b = splat2(0.f), s2b = splat2(0.f);
-    if (active) {
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        if (EXACT || t + k * a.tpr < nsc_me) {
-          float2 xf[4], df[4], gf[4];
-          chunk_to_f2(lds_chunk(xrow + k * cstep), xf);
-          chunk_to_f2(lds_chunk(xrow + L.tensor_bytes + k * cstep), df);
-          chunk_to_f2(gv[k], gf);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const float2 xh = mul2(add2(xf[p], nmu), rs2);
-            const float2 gg = mul2(df[p], gf[p]);
-            if (p & 1) {
-              s2b = fma2(gg, xh, s2b);
-              if (MODE == kLayer) s1b = add2(s1b, gg);
-            } else {
-              s2 = fma2(gg, xh, s2);
-              if (MODE == kLayer) s1 = add2(s1, gg);
-            }
-            accg[k][p] = fma2(df[p], xh, accg[k][p]);
-            if (MODE == kLayer) accb[k][p] = add2(accb[k][p], df[p]);
-          }
-        }
-      }
-    }
-    s1 = add2(s1, s1b);
-    s2 = add2(s2, s2b);
-    float v[2] = {s1.x + s1.y, s2.x + s2.y};
-    if (MODE == kLayer) {
-      group_sum<2, EXACT>(v, a.tpr, g, a.G, t, red, rpar);
-    } else {
-      float w1[1] = {v[1]};
-      group_sum<1, EXACT>(w1, a.tpr, g, a.G, t, red, rpar);
-      v[1] = w1[0];
-    }
-    pa = v[0];
-    pb = v[1];
-  };
-
-  // dx pass of row slot r of stage s given the row totals.
-  auto dx_pass = [&](int s, int64_t row0, int r, float tsum_g, float tsum_gx) {
-    const unsigned char *xrow = smem + static_cast<size_t>(s) * L.stage_bytes +
-                                static_cast<size_t>(r) * a.NS * 2 + t * 16;
-    const float *stats = stats_all + static_cast<size_t>(s) * a.RT * 2;
-    const float rs = stats[2 * r];
-    const float mu = (MODE == kLayer) ? stats[2 * r + 1] : 0.f;
-    const float2 rs2 = splat2(rs), nmu = splat2(-mu);
-    const float2 av = splat2((MODE == kLayer) ? tsum_g * invN : 0.f);
-    const float2 cv = splat2(tsum_gx * invN);
-    const float2 neg1 = splat2(-1.f);
-    uint16_t *dxrow = a.out + (row0 + r) * a.N + col0 + t * 8;
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      if (EXACT || t + k * a.tpr < nsc_me) {
-        float2 xf[4], df[4], gf[4], o[4];
-        chunk_to_f2(lds_chunk(xrow + k * cstep), xf);
-        chunk_to_f2(lds_chunk(xrow + L.tensor_bytes + k * cstep), df);
-        chunk_to_f2(gv[k], gf);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          // dx = rstd * (g - (xhat * c + a))
-          const float2 xh = mul2(add2(xf[p], nmu), rs2);
-          const float2 gg = mul2(df[p], gf[p]);
-          const float2 u = fma2(xh, cv, av);
-          o[p] = mul2(fma2(u, neg1, gg), rs2);
-        }
-        st_global_cs_v4(dxrow + k * a.tpr * 8, f2_to_chunk(o));
-      }
-    }
-  };
-
-  auto release = [&](int64_t tile, int s) {
-    if (last_warp_done(done_cnt, s, nwarps)) {
-      const int64_t next = tile + static_cast<int64_t>(a.S) * ncl;
-      if (next < a.ntiles) {
-        if ((tid & 31) == 0) fence_proxy_async_smem();
-        __syncwarp();
-        issue_bwd_tile<MODE, CLUSTER>(a, L, smem, next, s, col0, nsc_me, pol);
-      }
-    }
-  };
-
-  auto finish = [&](const Pending &p) {
-    const int64_t row0 = p.tile * a.RT;
-    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-    const int r = g;
-    const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
-    float v[2];
-    fold_sum<2>(row, xch.C, v);
-    if (r < nrows) dx_pass(p.s, row0, r, v[0], v[1]);
-    release(p.tile, p.s);
-  };
-
-  int s = 0;
-  uint32_t par = 0;
-  Pending pend;
-  bool have_pend = false;
-  for (int64_t tile = cid; tile < a.ntiles; tile += ncl) {
-    mbar_wait(full + s, par, a.err, abort_flag);
-    const int64_t row0 = tile * a.RT;
-    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-    if (CLUSTER) {
-      const int r = g;
-      Pending cur;
-      cur.tile = tile;
-      cur.s = s;
-      cur.c = 0.f;
-      dot_pass(s, r, r < nrows, cur.a, cur.b);
-      cluster_push(cur.a, cur.b, 0.f, r, t, xch);
-      if (have_pend) finish(pend);
-      pend = cur;
-      have_pend = true;
-    } else {
-      for (int q = 0; q < a.rpg; ++q) {
-        const int r = g + q * a.G;
-        const bool active = r < nrows;
-        float pa, pb;
-        dot_pass(s, r, active, pa, pb);
-        if (active) dx_pass(s, row0, r, pa, pb);
-      }
-      release(tile, s);
-    }
-    if (++s == a.S) {
-      s = 0;
-      par ^= 1u;
-    }
-  }
-  if (CLUSTER && have_pend) finish(pend);
-
-  write_column_partials<MODE, K, EXACT>(a, smem, accg, accb, g, t, nsc_me, cid, col0);
-  if (CLUSTER) cluster_sync();
-}
-
-template <int MODE, int K, bool CLUSTER, int OCC>
+template <int MODE, int K, bool CLUSTER>
 const void *pick_long(bool bwd, bool e) {
   if (bwd)
-    return e ? reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, true, OCC>)
-             : reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, false, OCC>);
-  return e ? reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, true, OCC>)
-           : reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, false, OCC>);
+    return e ? reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, true, 1, false>)
+             : reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, false, 1, false>);
+  return e ? reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, true, 1, false>)
+           : reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, false, 1, false>);
 }
 
 template <int MODE, bool CLUSTER>
-const void *pick_long_k(int K, bool bwd, bool e, int occ) {
-  if (occ != 1) return nullptr;
+const void *pick_long_k(int K, bool bwd, bool e) {
   switch (K) {
-    case 4: return pick_long<MODE, 4, CLUSTER, 1>(bwd, e);
-    case 8: return pick_long<MODE, 8, CLUSTER, 1>(bwd, e);
+    case 4: return pick_long<MODE, 4, CLUSTER>(bwd, e);
+    case 8: return pick_long<MODE, 8, CLUSTER>(bwd, e);
     default: return nullptr;
   }
 }
 
+template <bool CLUSTER>
+const void *pick_mode(int mode, int K, bool bwd, bool e) {
+  return mode == kRMS ? pick_long_k<kRMS, CLUSTER>(K, bwd, e) : pick_long_k<kLayer, CLUSTER>(K, bwd, e);
+}
+
 }  // namespace
 
-const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ) {
-  if (mode == kRMS)
-    return cluster ? pick_long_k<kRMS, true>(K, bwd, exact, occ)
-                   : pick_long_k<kRMS, false>(K, bwd, exact, occ);
-  return cluster ? pick_long_k<kLayer, true>(K, bwd, exact, occ)
-                 : pick_long_k<kLayer, false>(K, bwd, exact, occ);
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ,
+                            bool resid) {
+  if (occ != 1) return nullptr;
+  if (resid) return long_resid_kernel_ptr(mode, K, cluster, exact, bwd);
+  return cluster ? pick_mode<true>(mode, K, bwd, exact) : pick_mode<false>(mode, K, bwd, exact);
 }
 
 }  // namespace gbn

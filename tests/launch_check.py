@@ -57,7 +57,7 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     assert RT == G * rpg and S >= 2
     assert C >= 1 and grid % C == 0 and grid // C == P and P >= 1
     assert C == 1 or rpg == 1
-    assert not residual or (C == 1 and not p["long_rows"])
+    assert not residual or C == 1 or p["long_rows"]  # no register-path cluster variants
     assert ntiles == -(-M // RT) and P <= ntiles
     assert K * tpr >= nsc, "a chunk has no owner"
     if p["exact"]:

@@ -62,7 +62,7 @@ def test_fused_residual_parity(mode, M, N):
 
 
 @pytest.mark.parametrize("name", ["layer_32768x4096", "rms_32768x8192_resid",
-                                  "layer_32768x2048_resid"])
+                                  "layer_32768x2048_resid", "rms_4096x65536"])
 def test_fused_residual_full_size(name):
     w = wl.WORKLOADS[name]
     x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
@@ -104,12 +104,21 @@ def test_fused_residual_deterministic_and_matches_unfused():
     assert ((fused - unfused).abs() <= bound).all()
 
 
-def test_fused_residual_refuses_rows_beyond_one_cta():
-    M, N = 4, 16384
-    x = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
-    g = torch.ones(N, dtype=torch.bfloat16, device="cuda")
-    b = torch.zeros(N, dtype=torch.bfloat16, device="cuda")
-    h, y, rs, mu = gb.norm_add_fwd(x, x, g, b, 1e-5, 1)  # LN forward fits one CTA
-    with pytest.raises(gb.NormError) as e:
-        gb.norm_add_bwd(x, x, h, g, rs, mu, 1)  # LN backward at 16384 does not
-    assert e.value.status == 6
+@pytest.mark.parametrize("mode,M,N", [(1, 67, 16384), (0, 45, 16384), (1, 33, 24576),
+                                      (0, 21, 32768), (1, 19, 65536), (0, 9, 131072),
+                                      (0, 5, 262144)])
+def test_fused_residual_long_rows(mode, M, N):
+    """Rows wider than one CTA's registers: the long-row kernels (shared-
+    memory-resident slices, clusters beyond 16384 / 32768 columns) with the
+    residual tensor in the same stage."""
+    base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
+    case = wl.like(base, M, N)
+    for bwd in (False, True):
+        p = gb.norm_plan(M, N, mode, bwd, residual=True)
+        assert p["long_rows"] == 1 or p["chunks_per_thread"] * p["threads_per_row"] * 8 >= N
+    ins = [None if t is None else t.cuda()
+           for t in wl.make_residual_inputs(case, "cpu", seed=M + N)]
+    x, r, g, b, dy, dh = ins
+    outs = _run(x, r, g, b, dy, dh, case.eps, mode)
+    _compare(mode, case.eps, x, r, g, b, dy, dh, outs, label=f"long {mode}:{M}x{N}")
+    assert gb.norm_get_device_error() == 0
