@@ -218,13 +218,15 @@ __global__ void selftest_wait_kernel(unsigned *err, uint32_t polls) {
   if (threadIdx.x == 0) mbar_wait(&bar, 0, err, &abort_flag, polls);
 }
 
-constexpr int kReduceWarps = 16;
+constexpr int kReduceWarps = 32;
+constexpr int kReduceBatch = 8;  // partial rows a lane loads before adding
 
 // dgamma[j] = sum over p of ws[p][j] (blockIdx.y = 0) and dbeta[j] = sum
 // over p of ws[P + p][j] (blockIdx.y = 1).  Warp w of the block sums the
-// contiguous range p in [P*w/16, P*(w+1)/16) in increasing p; the 16 warp
-// sums are then added in warp order: a fixed order for a given P, so the
-// result is bitwise reproducible.  Each lane owns 4 consecutive columns.
+// contiguous range p in [P*w/32, P*(w+1)/32) in increasing p (loads of a
+// batch issued together, then added in order); the 32 warp sums are then
+// added in warp order: a fixed order for a given P, so the result is bitwise
+// reproducible.  Each lane owns 4 consecutive columns.
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
     const float *__restrict__ ws, int P, int N, float *__restrict__ dgamma,
     float *__restrict__ dbeta) {
@@ -240,20 +242,19 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
   if (col < N) {
     const int p0 = static_cast<int>((static_cast<int64_t>(P) * w) / kReduceWarps);
     const int p1 = static_cast<int>((static_cast<int64_t>(P) * (w + 1)) / kReduceWarps);
-    int p = p0;
-    for (; p + 4 <= p1; p += 4) {
-      float4 v[4];
+    for (int p = p0; p < p1; p += kReduceBatch) {
+      float4 v[kReduceBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        v[u] = __ldcg(reinterpret_cast<const float4 *>(src + static_cast<size_t>(p + u) * N + col));
+      for (int u = 0; u < kReduceBatch; ++u)
+        v[u] = (p + u < p1) ? __ldcg(reinterpret_cast<const float4 *>(
+                                  src + static_cast<size_t>(p + u) * N + col))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+      for (int u = 0; u < kReduceBatch; ++u) {
+        if (p + u < p1) {
+          acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+        }
       }
-    }
-    for (; p < p1; ++p) {
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + static_cast<size_t>(p) * N + col));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
   }
   part[w][lane] = acc;

@@ -166,9 +166,14 @@ def check_fp8_plan(p, M, N, scaling):
     return True
 
 
+REDUCE_WARPS = 32
+REDUCE_BATCH = 8
+
+
 def check_reduce(P, N, nparts):
-    """Reduce kernel: grid (ceil(N/128), nparts), 16 warps, lane owns 4
-    columns, warp w sums p in [P*w/16, P*(w+1)/16)."""
+    """Reduce kernel: grid (ceil(N/128), nparts), 32 warps, lane owns 4
+    columns, warp w sums p in [P*w/32, P*(w+1)/32) in batches of 8 loads,
+    each guarded by p < the range end."""
     assert N % 4 == 0
     gx = -(-N // 128)
     for bx in (0, gx - 1):
@@ -177,7 +182,10 @@ def check_reduce(P, N, nparts):
             if col < N:
                 assert col + 4 <= N
                 assert ((nparts - 1) * P + (P - 1)) * N + col + 4 <= nparts * P * N
-    ranges = [(P * w // 16, P * (w + 1) // 16) for w in range(16)]
-    covered = [p for a, b in ranges for p in range(a, b)]
+    ranges = [(P * w // REDUCE_WARPS, P * (w + 1) // REDUCE_WARPS) for w in range(REDUCE_WARPS)]
+    covered = []
+    for a, b in ranges:
+        for p in range(a, b, REDUCE_BATCH):
+            covered += [p + u for u in range(REDUCE_BATCH) if p + u < b]
     assert covered == list(range(P))
     return True
