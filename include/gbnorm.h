@@ -190,8 +190,10 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h,
  *   q     uint8 [M, N] E4M3 codes of y;
  *   scale float [M] (NORM_FP8_ROW) or uint8 [M, N / 32] (NORM_FP8_MX).
  * All pointers are device pointers owned by the caller, 16-byte aligned.
- * Rows that do not fit one CTA (N above 16384 for LAYER, 24576 for RMS)
- * return NORM_ERR_UNSUPPORTED; an unknown scaling returns NORM_ERR_ARG.
+ * Every N up to NORM_MAX_N is supported with MX scaling; per-row scaling
+ * needs the row in one CTA (N up to 32768 for RMS, 16384 for LAYER, less
+ * with a residual) and returns NORM_ERR_UNSUPPORTED beyond; an unknown
+ * scaling returns NORM_ERR_ARG.
  * One kernel on `stream`.  The backward pass of an FP8-output forward is
  * norm_bwd / norm_add_bwd (it reads x or h and the saved rstd / mean).
  */

@@ -208,7 +208,7 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
 // backward), two row groups of up to 256 threads per CTA when the slice
 // allows, and the smallest power-of-two cluster whose slices fit.
 norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, const Override &ov,
-                        Plan *out, bool resid = false) {
+                        Plan *out, bool resid = false, bool fp8 = false) {
   const int nc = N / 8;
   // 8 chunks per thread only where that fits in registers without spilling
   // (RMSNorm forward); 4 elsewhere.
@@ -230,7 +230,8 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
     p.resid = resid;
     p.occ = ov.occ ? ov.occ : 1;
     p.C = C;
-    p.nsc = ceil_div(nc, C);
+    // E4M3 output: slices start on a 32-column MX block (4 chunks)
+    p.nsc = fp8 ? 4 * ceil_div(nc, 4 * C) : ceil_div(nc, C);
     p.NS = p.nsc * 8;
     if ((C - 1) * p.nsc >= nc) return NORM_ERR_UNSUPPORTED;
     const int tpr = ov.tpr ? ov.tpr : 32 * ceil_div(ceil_div(p.nsc, K), 32);
@@ -247,7 +248,8 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
       if (ov.C) return st;
       continue;  // a wider cluster halves the slice
     }
-    if (!long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ, resid))
+    if (fp8 ? !long_fp8_kernel_ptr(mode, p.K, p.C > 1, p.exact, resid, kOutFp8Mx)
+            : !long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ, resid))
       return NORM_ERR_UNSUPPORTED;
     *out = p;
     return NORM_OK;
@@ -287,8 +289,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
   // Rows wider than one CTA's register capacity (kMaxThreads x klim chunks)
   // go to the long-row kernels, which keep the row in shared memory.
   if (ov.lng == 1 || (ov.lng != 0 && nc > kMaxThreads * klim)) {
-    if (fp8) return NORM_ERR_UNSUPPORTED;  // E4M3 output: register-resident rows only
-    return long_plan(mode, bwd, M, N, smem_optin, ov, out, resid);
+    return long_plan(mode, bwd, M, N, smem_optin, ov, out, resid, fp8 && !bwd);
   }
 
   // Column split: the smallest power-of-two cluster (up to 8) whose per-CTA
@@ -931,11 +932,13 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma, cons
   Plan p;
   if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p, resid, true)) != NORM_OK)
     return st;
-  // E4M3 output: register-resident rows only; MX blocks need quads of lanes.
-  if (p.C != 1 || p.long_rows) return NORM_ERR_UNSUPPORTED;
+  // MX blocks need quads of lanes; per-row scaling needs one CTA per row
+  // (the row amax is a CTA-local reduction).
   if (scaling == NORM_FP8_MX && p.tpr % 4 != 0) return NORM_ERR_UNSUPPORTED;
   const int out = scaling == NORM_FP8_ROW ? kOutFp8Row : kOutFp8Mx;
-  const void *fn = fwd_fp8_kernel_ptr(mode, p.K, p.exact, resid, out, p.gsm);
+  if (p.C != 1 && out == kOutFp8Row) return NORM_ERR_UNSUPPORTED;
+  const void *fn = p.long_rows ? long_fp8_kernel_ptr(mode, p.K, p.C > 1, p.exact, resid, out)
+                               : fwd_fp8_kernel_ptr(mode, p.K, p.exact, resid, out, p.gsm);
   if (!fn) return NORM_ERR_UNSUPPORTED;
   if ((st = prepare_function(dev, fn, d.smem_optin)) != NORM_OK) return st;
   NormArgs a = base_args(p, M, static_cast<int>(N));

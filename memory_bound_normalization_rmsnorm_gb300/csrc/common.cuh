@@ -165,6 +165,9 @@ const void *reduce_kernel_ptr();
 const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ,
                             bool resid = false);
 const void *long_resid_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd);
+// Long-row forward with E4M3 output (out = kOutFp8Row without a cluster, or
+// kOutFp8Mx); nullptr if not instantiated.
+const void *long_fp8_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, int out);
 int reduce_threads();
 const void *selftest_kernel_ptr();
 

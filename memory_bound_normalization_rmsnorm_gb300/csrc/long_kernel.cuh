@@ -46,8 +46,12 @@ struct Pending {
 // RESID: fused residual add -- the stage also holds r; the statistics pass
 // forms h = bf16(x + r) (sum in binary32, round to nearest even), writes it
 // over x in the stage, and the output pass writes h out beside y.
-template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC, bool RESID>
+// OUT: bf16 y (kOutBf16), or E4M3 codes with a per-row scale (kOutFp8Row;
+// clusters excluded: the row amax would need a second exchange round) or
+// with per-32-column E8M0 exponents (kOutFp8Mx; slices start on a block).
+template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC, bool RESID, int OUT = kOutBf16>
 __global__ void __launch_bounds__(kMaxThreads, OCC) norm_fwd_long_kernel(const NormArgs a) {
+  static_assert(!(CLUSTER && OUT == kOutFp8Row), "per-row E4M3 scaling needs one CTA per row");
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -205,23 +209,93 @@ __global__ void __launch_bounds__(kMaxThreads, OCC) norm_fwd_long_kernel(const N
     }
     const unsigned char *rowp = st + static_cast<size_t>(r) * a.NS * 2 + t * 16;
     const float2 rs2 = splat2(rs), nmu = splat2(-mu);
-    uint16_t *yrow = a.out + (row0 + r) * a.N + col0 + t * 8;
     uint16_t *hrow = RESID ? a.h + (row0 + r) * a.N + col0 + t * 8 : nullptr;
+    // y of chunk k (owned chunks only); with `store_h` also streams h out.
+    auto ychunk = [&](int k, float2 (&o)[4], bool store_h) {
+      float2 xf[4], gf[4], bf[4];
+      const uint4 hv = lds_chunk(rowp + k * cstep);
+      if (RESID && store_h) st_global_cs_v4(hrow + k * a.tpr * 8, hv);
+      chunk_to_f2(hv, xf);
+      chunk_to_f2(gv[k], gf);
+      if (MODE == kLayer) chunk_to_f2(bv[k], bf);
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      if (EXACT || t + k * a.tpr < nsc_me) {
-        float2 xf[4], gf[4], bf[4], o[4];
-        const uint4 hv = lds_chunk(rowp + k * cstep);
-        if (RESID) st_global_cs_v4(hrow + k * a.tpr * 8, hv);
-        chunk_to_f2(hv, xf);
-        chunk_to_f2(gv[k], gf);
-        if (MODE == kLayer) chunk_to_f2(bv[k], bf);
+      for (int p = 0; p < 4; ++p) {
+        const float2 xh = mul2(MODE == kLayer ? add2(xf[p], nmu) : xf[p], rs2);
+        o[p] = (MODE == kLayer) ? fma2(xh, gf[p], bf[p]) : mul2(xh, gf[p]);
+      }
+    };
+    if (OUT == kOutBf16) {
+      uint16_t *yrow = a.out + (row0 + r) * a.N + col0 + t * 8;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const float2 xh = mul2(MODE == kLayer ? add2(xf[p], nmu) : xf[p], rs2);
-          o[p] = (MODE == kLayer) ? fma2(xh, gf[p], bf[p]) : mul2(xh, gf[p]);
+      for (int k = 0; k < K; ++k) {
+        if (EXACT || t + k * a.tpr < nsc_me) {
+          float2 o[4];
+          ychunk(k, o, true);
+          st_global_cs_v4(yrow + k * a.tpr * 8, f2_to_chunk(o));
         }
-        st_global_cs_v4(yrow + k * a.tpr * 8, f2_to_chunk(o));
+      }
+    } else if (OUT == kOutFp8Row) {
+      // amax of the row (one CTA per row here), then the codes
+      uint8_t *qrow = a.q + (row0 + r) * a.N + col0 + t * 8;
+      float am = 0.f;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        if (EXACT || t + k * a.tpr < nsc_me) {
+          float2 o[4];
+          ychunk(k, o, false);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) am = fmaxf(am, fmaxf(fabsf(o[p].x), fabsf(o[p].y)));
+        }
+      }
+      am = group_max<true>(am, a.tpr, g, a.G, t, red, rpar);
+      const float2 inv = splat2(am > 0.f ? __fdividef(448.f, am) : 1.f);
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        if (EXACT || t + k * a.tpr < nsc_me) {
+          float2 o[4];
+          ychunk(k, o, true);
+          uint32_t w[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float2 v = mul2(o[p], inv);
+            w[p] = cvt_e4m3x2(v.x, v.y);
+          }
+          st_global_cs_v2(qrow + k * a.tpr * 8,
+                          make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
+        }
+      }
+      if (t == 0) a.qscale[row0 + r] = am > 0.f ? am * (1.0f / 448.0f) : 1.f;
+    } else {
+      // MX: a block is 4 consecutive chunks of 4 consecutive lanes (tpr is a
+      // multiple of 32 and the slice starts on a block), so its amax is two
+      // butterfly steps; every lane takes part in the shuffles.
+      uint8_t *qrow = a.q + (row0 + r) * a.N + col0 + t * 8;
+      uint8_t *erow = a.qexp + (row0 + r) * (a.N / kMxBlock) + col0 / kMxBlock;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const bool own = EXACT || t + k * a.tpr < nsc_me;
+        float2 o[4] = {splat2(0.f), splat2(0.f), splat2(0.f), splat2(0.f)};
+        if (own) ychunk(k, o, true);
+        float m = 0.f;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) m = fmaxf(m, fmaxf(fabsf(o[p].x), fabsf(o[p].y)));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int eb = static_cast<int>(__float_as_uint(m) >> 23);
+        const float2 inv =
+            splat2(__uint_as_float(static_cast<uint32_t>(min(262 - eb, 254)) << 23));
+        if (own) {
+          uint32_t w[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float2 v = mul2(o[p], inv);
+            w[p] = cvt_e4m3x2(v.x, v.y);
+          }
+          st_global_cs_v2(qrow + k * a.tpr * 8,
+                          make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
+          st_global_u8_if(erow + ((t + k * a.tpr) >> 2), static_cast<uint32_t>(max(eb - 8, 0)),
+                          (t & 3) == 0);
+        }
       }
     }
     if (t == 0 && crank == 0) {

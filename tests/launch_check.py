@@ -143,7 +143,17 @@ def check_fp8_plan(p, M, N, scaling):
     consecutive lanes of one row group, owned (or not) together."""
     C, tpr, K = p["cluster"], p["threads_per_row"], p["chunks_per_thread"]
     nc = N // 8
-    assert C == 1 and not p["long_rows"], "E4M3 output is register-resident only"
+    if C > 1 or p["long_rows"]:
+        # long-row kernels: slices start on a 32-column block, tpr % 32 == 0
+        nsc = p["cols_per_cta"] // 8
+        assert nsc % 4 == 0 and tpr % 32 == 0 and (C - 1) * nsc < nc
+        assert scaling == "mx" or C == 1, "per-row scaling needs one CTA per row"
+        for crank in range(C):
+            nsc_me = min(nsc, nc - crank * nsc)
+            for c in range(0, nsc_me, 4):
+                blk = (crank * nsc + c) // 4
+                assert blk < N // 32 or scaling != "mx"
+        return True
     for t in range(tpr):
         for k in range(K):
             c = t + k * tpr

@@ -122,9 +122,29 @@ def test_fp8_zero_rows_and_tiny_blocks():
     fp8_check.check_fp8(q.cpu().numpy(), e.cpu().numpy(), ref, oracle.FP8_MX, 0, "tiny")
 
 
-def test_fp8_refuses_rows_beyond_one_cta():
-    x = torch.zeros(2, 32768, dtype=torch.bfloat16, device="cuda")
-    g = torch.ones(32768, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(gb.NormError) as e:
-        gb.norm_fwd_fp8(x, g, None, 1e-6, 0, gb.FP8_ROW)
-    assert e.value.status == 6
+@pytest.mark.parametrize("residual", [False, True], ids=["plain", "resid"])
+@pytest.mark.parametrize("mode,M,N", [(0, 37, 32768), (0, 21, 40000), (1, 29, 18432),
+                                      (1, 17, 24576), (0, 9, 65536), (0, 5, 131072)])
+def test_fp8_long_rows(mode, M, N, residual):
+    """Rows wider than one CTA's registers (long-row kernels, clusters):
+    MX scaling everywhere; per-row scaling where one CTA holds the row, and
+    NORM_ERR_UNSUPPORTED where a cluster would (the amax would need a second
+    exchange round)."""
+    base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
+    case = wl.like(base, M, N)
+    x, r, g, b, _, _ = [None if t is None else t.cuda()
+                        for t in wl.make_residual_inputs(case, "cpu", seed=M * 3 + N)]
+    if not residual:
+        r = None
+    plan = gb.norm_plan(M, N, mode, False, residual=residual, fp8=True)
+    assert plan["long_rows"] == 1
+    for gsc, osc in SCALINGS:
+        if gsc == gb.FP8_ROW and plan["cluster"] > 1:
+            with pytest.raises(gb.NormError) as e:
+                gb.norm_fwd_fp8(x, g, b, case.eps, mode, gsc, r=r)
+            assert e.value.status == 6
+            continue
+        outs = gb.norm_fwd_fp8(x, g, b, case.eps, mode, gsc, r=r)
+        torch.cuda.synchronize()
+        _compare(case, x, r, g, b, outs, osc, label=f"long {mode}:{M}x{N}:{gsc}:{residual}")
+    assert gb.norm_get_device_error() == 0

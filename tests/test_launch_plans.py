@@ -50,8 +50,8 @@ def test_fused_residual_plans_in_bounds(backward):
 
 @pytest.mark.parametrize("residual", [False, True])
 def test_fp8_plans_in_bounds(residual):
-    """E4M3 output uses the forward plans: every default plan that fits one
-    CTA satisfies the MX block rule when N is a multiple of 32."""
+    """Every E4M3-output plan is in bounds, and satisfies the MX block rule
+    when N is a multiple of 32 (register-resident and long-row plans)."""
     n = 0
     for M, N, mode in _cases():
         try:
@@ -59,11 +59,12 @@ def test_fp8_plans_in_bounds(residual):
         except gb.NormError as e:
             assert residual and e.status == 6
             continue
-        if p["cluster"] != 1 or p["long_rows"]:
-            continue  # refused by norm_fwd_fp8 (NORM_ERR_UNSUPPORTED)
-        launch_check.check_fp8_plan(p, M, N, "row")
+        p8 = gb.norm_plan(M, N, mode, False, SMS, OPTIN, residual=residual, fp8=True)
+        launch_check.check_plan(p8, M, N, mode, False, OPTIN, residual=residual)
+        if p8["cluster"] == 1:
+            launch_check.check_fp8_plan(p8, M, N, "row")
         if N % 32 == 0:
-            launch_check.check_fp8_plan(p, M, N, "mx")
+            launch_check.check_fp8_plan(p8, M, N, "mx")
         n += 1
     assert n > 400
 
