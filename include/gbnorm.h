@@ -298,14 +298,15 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
  * pipeline stages as what Inductor's autotuner searches for these kernels;
  * the library's default plan comes from a heuristic and a table measured
  * offline.  norm_tune_fwd / norm_tune_bwd measure, on the caller's buffers
- * and stream, every register-resident plan of that pass (each threads-per-
- * row value that splits the row within the compiled chunk counts, rows per
- * group 1, 2, 4 or the heuristic's, and for the forward pass the plans with
- * gamma/beta staged in shared memory), each `iters` times after two warm-up
+ * and stream, every single-CTA plan of that pass (each threads-per-row
+ * value that splits the row within the compiled chunk counts, rows per
+ * group 1, 2, 4 or the heuristic's, the long-row kernels with 1 to 8 row
+ * groups, and for the forward pass the plans with gamma/beta staged in
+ * shared memory), each `iters` times after two warm-up
  * launches, and install the fastest in the process's plan cache for this
  * (device, mode, pass, M, N): later norm_fwd / norm_bwd calls of that shape
  * use it and norm_plan reports it (written to *chosen when not NULL).  Rows
- * that need the long-row or cluster kernels keep their plan.  The outputs
+ * that need a cluster keep their plan.  The outputs
  * hold the chosen plan's results.  The call blocks until its measurements
  * are done.
  *

@@ -149,6 +149,8 @@ struct TunedPlan {
   int N;
   int tpr, rpg, S;  // 0 = heuristic's choice
   int gsm = 0;      // forward: gamma/beta staged in shared memory, 8 chunks per thread
+  int lng = 0;      // 1: the long-row kernels (slice re-read from the stage)
+  int G = 0;        // row groups per CTA (0 = heuristic's choice)
 };
 constexpr TunedPlan kTuned[] = {
     {kRMS, 0, 256, 32, 2, 3},     {kRMS, 0, 512, 32, 1, 3},    {kRMS, 0, 768, 32, 0, 3},
@@ -158,7 +160,12 @@ constexpr TunedPlan kTuned[] = {
     {kLayer, 0, 8192, 0, 0, 0, 1},
     {kRMS, 1, 256, 32, 2, 5},     {kRMS, 1, 512, 64, 0, 0},    {kRMS, 1, 768, 64, 4, 0},
     {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 2048, 128, 1, 7},  {kRMS, 1, 5120, 256, 2, 0},
-    {kLayer, 1, 3072, 192, 4, 0}, {kLayer, 1, 5120, 320, 4, 2},
+    {kLayer, 1, 3072, 192, 4, 0},
+    // LayerNorm backward at 5120 / 8192: the long-row kernel with 4 chunks
+    // per thread and 3 / 2 row groups (15 / 16 warps) beats the register
+    // kernel's 2 chunks per thread (10 / 16 warps, 8 / 16 warps per row):
+    // 195 -> 173 us and 274 -> 265 us at 32768 rows.
+    {kLayer, 1, 5120, 0, 0, 0, 0, 1, 3}, {kLayer, 1, 8192, 0, 0, 0, 0, 1, 2},
 };
 
 // Ring and tile sizing shared by both plan kinds: rows per tile and the
@@ -270,6 +277,8 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
         ov.tpr = tp.tpr;
         ov.rpg = tp.rpg;
         ov.S = tp.S;
+        ov.G = tp.G;
+        if (tp.lng) ov.lng = 1;
         tuned_gsm = tp.gsm != 0;
         break;
       }
@@ -592,11 +601,11 @@ void fill_plan(const Plan &p, norm_plan_t *out) {
 // ------------------------------------------------------------ plan tuning
 // The pages name the split size and the number of pipeline stages as the
 // levers an autotuner turns for these kernels; here the candidates are the
-// register-resident plans of one pass: every threads-per-row value that
-// splits the row (exactly, or raggedly over a power of two) within the
-// compiled chunk counts, rows per group 1, 2, 4 or the heuristic's, and for
-// the forward pass the staged-parameter plans.  Rows that need the long-row
-// or cluster kernels keep their plan.
+// single-CTA plans of one pass: every threads-per-row value that splits the
+// row (exactly, or raggedly over a power of two) within the compiled chunk
+// counts, rows per group 1, 2, 4 or the heuristic's, the long-row kernels
+// with 1 to 8 row groups, and for the forward pass the staged-parameter
+// plans.  Rows that need a cluster keep their plan.
 std::vector<Override> tune_candidates(bool bwd, int N) {
   std::vector<Override> v;
   const int nsc = N / 8;
@@ -622,6 +631,16 @@ std::vector<Override> tune_candidates(bool bwd, int N) {
       o.C = 1;
       v.push_back(o);
     }
+  }
+  // the long-row kernels at this width (slice re-read from the stage):
+  // 1 to 8 row groups per CTA
+  for (int G = 1; G <= 8; ++G) {
+    Override o;
+    o.any = true;
+    o.lng = 1;
+    o.C = 1;
+    o.G = G;
+    v.push_back(o);
   }
   if (!bwd) {
     for (int k : {5, 6, 8}) {
@@ -666,11 +685,11 @@ norm_status_t tune_pass(int mode, bool bwd, int64_t M, int N, size_t ws_bytes, i
     g_plans[key] = p;
   };
   std::vector<Plan> cands{def};
-  if (def.C == 1 && !def.long_rows) {
+  if (def.C == 1) {
     for (const Override &o : tune_candidates(bwd, N)) {
       Plan p;
       if (shape_plan(mode, bwd, M, N, d.smem_optin, o, &p) != NORM_OK) continue;
-      if (p.C != 1 || p.long_rows) continue;
+      if (p.C != 1) continue;
       if (finish_plan(d, dev, mode, bwd, o, &p) != NORM_OK) continue;
       const size_t need = static_cast<size_t>(p.P) * N * 4 * (mode == kLayer ? 2 : 1);
       if (bwd && need > ws_bytes) continue;
