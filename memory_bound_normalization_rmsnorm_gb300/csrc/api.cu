@@ -105,7 +105,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Optional plan override for tuning sweeps: GBNORM_PLAN="C=2,tpr=256,rpg=1,S=4"
 // (any subset).  Fields left out keep the heuristic's choice.
 struct Override {
-  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, occ = 0, gsm = -1;
+  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, gsm = -1;
   bool any = false;
 };
 
@@ -127,7 +127,6 @@ Override read_override() {
     else if (!std::strcmp(key, "ctas")) o.ctas = val;
     else if (!std::strcmp(key, "long")) o.lng = val;
     else if (!std::strcmp(key, "K")) o.K = val;
-    else if (!std::strcmp(key, "occ")) o.occ = val;
     else if (!std::strcmp(key, "gsm")) o.gsm = val;
     o.any = true;
   }
@@ -179,8 +178,7 @@ norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, i
   if (C == 1) rpg = std::max(1, (32 * 1024) / (row_bytes * G));
   if (ov.rpg) rpg = ov.rpg;
   if (rpg < 1 || (C > 1 && rpg != 1)) return NORM_ERR_UNSUPPORTED;
-  // Two CTAs per SM share the SM's shared memory (opt-in limit + 1 KB).
-  const int budget = (p.occ == 2) ? (smem_optin + 1024) / 2 - 1024 : smem_optin - 1024;
+  const int budget = smem_optin - 1024;
   int S = 0;
   for (;;) {
     const SmemLayout L1 = make_layout(G * rpg, p.NS, 1, G, p.tpr, ntensors, bwd, C, p.par_bpc);
@@ -235,7 +233,6 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
     Plan p;
     p.long_rows = true;
     p.resid = resid;
-    p.occ = ov.occ ? ov.occ : 1;
     p.C = C;
     // E4M3 output: slices start on a 32-column MX block (4 chunks)
     p.nsc = fp8 ? 4 * ceil_div(nc, 4 * C) : ceil_div(nc, C);
@@ -256,7 +253,7 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
       continue;  // a wider cluster halves the slice
     }
     if (fp8 ? !long_fp8_kernel_ptr(mode, p.K, p.C > 1, p.exact, resid, kOutFp8Mx)
-            : !long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ, resid))
+            : !long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, resid))
       return NORM_ERR_UNSUPPORTED;
     *out = p;
     return NORM_OK;
@@ -412,7 +409,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 }
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
-  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.occ, p.resid);
+  if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.resid);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm);
 }
@@ -992,7 +989,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
     if ((st = shape_plan(mode, bwd, M, static_cast<int>(N), smem_optin_bytes, read_override(),
                          &p, resid, fp8)) != NORM_OK)
       return st;
-    set_grid(p, static_cast<int64_t>(sm_count) * p.occ / p.C);
+    set_grid(p, static_cast<int64_t>(sm_count) / p.C);
     if (p.grid < 1) return NORM_ERR_UNSUPPORTED;
   } else {
     DeviceInfo d;

@@ -270,30 +270,25 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(
   }
 }
 
+template <int MODE, int K, bool CLUSTER, bool RESID>
+const void *pick_exact(bool e) {
+  return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, K, CLUSTER, true, RESID>)
+           : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, K, CLUSTER, false, RESID>);
+}
+
+template <int MODE, int K, bool CLUSTER>
+const void *pick_variant(bool e, bool r) {
+  if (r) return CLUSTER ? nullptr : pick_exact<MODE, K, false, true>(e);  // no cluster variants
+  return pick_exact<MODE, K, CLUSTER, false>(e);
+}
+
 template <int MODE, bool CLUSTER>
 const void *pick_bwd(int K, bool e, bool r) {
-  if (r && CLUSTER) return nullptr;  // fused residual: no cluster variants
   switch (K) {
-    case 1:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 1, CLUSTER, false, false>);
-    case 2:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 2, CLUSTER, false, false>);
-    case 3:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 3, CLUSTER, false, false>);
-    case 4:
-      if (r) return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, false, true, true>)
-                      : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, false, false, true>);
-      return e ? reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, true, false>)
-               : reinterpret_cast<const void *>(&norm_bwd_kernel<MODE, 4, CLUSTER, false, false>);
+    case 1: return pick_variant<MODE, 1, CLUSTER>(e, r);
+    case 2: return pick_variant<MODE, 2, CLUSTER>(e, r);
+    case 3: return pick_variant<MODE, 3, CLUSTER>(e, r);
+    case 4: return pick_variant<MODE, 4, CLUSTER>(e, r);
     default: return nullptr;
   }
 }

@@ -113,7 +113,6 @@ struct Plan {
   int K = 0;       // chunks per thread
   bool exact = false; // slices divide evenly into K chunks x tpr threads, tpr >= 32
   bool long_rows = false; // long-row kernels (row re-read from the stage)
-  int occ = 1;            // CTAs per SM the kernel is compiled for
   bool resid = false;     // fused residual add variant
   bool gsm = false;       // forward: gamma/beta read per row from shared memory
   int par_bpc = 0;        // gsm: staged parameter bytes per column
@@ -160,9 +159,7 @@ const void *fwd_gsm_kernel_ptr(int mode, int K, bool resid, int out);
 const void *bwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false);
 const void *reduce_kernel_ptr();
 // Long-row kernels (row slice re-read from shared memory), K in {4, 8}.
-// occ = CTAs per SM the kernel is compiled for (only 1 is built: a
-// two-CTA-per-SM variant capped at 64 registers measured 40 % slower).
-const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ,
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd,
                             bool resid = false);
 const void *long_resid_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd);
 // Long-row forward with E4M3 output (out = kOutFp8Row without a cluster, or

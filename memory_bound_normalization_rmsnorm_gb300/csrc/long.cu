@@ -9,10 +9,10 @@ namespace {
 template <int MODE, int K, bool CLUSTER>
 const void *pick_long(bool bwd, bool e) {
   if (bwd)
-    return e ? reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, true, 1, false>)
-             : reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, false, 1, false>);
-  return e ? reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, true, 1, false>)
-           : reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, false, 1, false>);
+    return e ? reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, true, false>)
+             : reinterpret_cast<const void *>(&norm_bwd_long_kernel<MODE, K, CLUSTER, false, false>);
+  return e ? reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, true, false>)
+           : reinterpret_cast<const void *>(&norm_fwd_long_kernel<MODE, K, CLUSTER, false, false>);
 }
 
 template <int MODE, bool CLUSTER>
@@ -31,9 +31,7 @@ const void *pick_mode(int mode, int K, bool bwd, bool e) {
 
 }  // namespace
 
-const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, int occ,
-                            bool resid) {
-  if (occ != 1) return nullptr;
+const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd, bool resid) {
   if (resid) return long_resid_kernel_ptr(mode, K, cluster, exact, bwd);
   return cluster ? pick_mode<true>(mode, K, bwd, exact) : pick_mode<false>(mode, K, bwd, exact);
 }

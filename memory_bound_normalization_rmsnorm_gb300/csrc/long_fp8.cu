@@ -11,9 +11,9 @@ namespace {
 template <int MODE, int K, bool CLUSTER, bool RESID, int OUT>
 const void *pick_exact(bool e) {
   return e ? reinterpret_cast<const void *>(
-                 &norm_fwd_long_kernel<MODE, K, CLUSTER, true, 1, RESID, OUT>)
+                 &norm_fwd_long_kernel<MODE, K, CLUSTER, true, RESID, OUT>)
            : reinterpret_cast<const void *>(
-                 &norm_fwd_long_kernel<MODE, K, CLUSTER, false, 1, RESID, OUT>);
+                 &norm_fwd_long_kernel<MODE, K, CLUSTER, false, RESID, OUT>);
 }
 
 template <int MODE, int K>

@@ -42,15 +42,14 @@ struct Pending {
   float a, b, c;  // this row group's partial (also the total without a cluster)
 };
 
-// OCC: CTAs per SM the kernel is compiled for (2 caps registers at 64).
 // RESID: fused residual add -- the stage also holds r; the statistics pass
 // forms h = bf16(x + r) (sum in binary32, round to nearest even), writes it
 // over x in the stage, and the output pass writes h out beside y.
 // OUT: bf16 y (kOutBf16), or E4M3 codes with a per-row scale (kOutFp8Row;
 // clusters excluded: the row amax would need a second exchange round) or
 // with per-32-column E8M0 exponents (kOutFp8Mx; slices start on a block).
-template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC, bool RESID, int OUT = kOutBf16>
-__global__ void __launch_bounds__(kMaxThreads, OCC) norm_fwd_long_kernel(const NormArgs a) {
+template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT = kOutBf16>
+__global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const NormArgs a) {
   static_assert(!(CLUSTER && OUT == kOutFp8Row), "per-row E4M3 scaling needs one CTA per row");
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C);
@@ -381,8 +380,8 @@ __global__ void __launch_bounds__(kMaxThreads, OCC) norm_fwd_long_kernel(const N
 
 // RESID: fused residual add -- the stage also holds dh (third tensor) and
 // dx = (norm backward at h) + dh, summed in fp32 and rounded once.
-template <int MODE, int K, bool CLUSTER, bool EXACT, int OCC, bool RESID>
-__global__ void __launch_bounds__(kMaxThreads, OCC) norm_bwd_long_kernel(const NormArgs a) {
+template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID>
+__global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 3 : 2, true, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
