@@ -190,10 +190,9 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h,
  *   q     uint8 [M, N] E4M3 codes of y;
  *   scale float [M] (NORM_FP8_ROW) or uint8 [M, N / 32] (NORM_FP8_MX).
  * All pointers are device pointers owned by the caller, 16-byte aligned.
- * Every N up to NORM_MAX_N is supported with MX scaling; per-row scaling
- * needs the row in one CTA (N up to 32768 for RMS, 16384 for LAYER, less
- * with a residual) and returns NORM_ERR_UNSUPPORTED beyond; an unknown
- * scaling returns NORM_ERR_ARG.
+ * Every N up to NORM_MAX_N is supported (rows wider than one CTA use the
+ * long-row kernels and clusters; with per-row scaling the CTAs of a cluster
+ * exchange their slice maxima); an unknown scaling returns NORM_ERR_ARG.
  * One kernel on `stream`.  The backward pass of an FP8-output forward is
  * norm_bwd / norm_add_bwd (it reads x or h and the saved rstd / mean).
  */

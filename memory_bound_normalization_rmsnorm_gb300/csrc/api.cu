@@ -948,11 +948,9 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma, cons
   Plan p;
   if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p, resid, true)) != NORM_OK)
     return st;
-  // MX blocks need quads of lanes; per-row scaling needs one CTA per row
-  // (the row amax is a CTA-local reduction).
+  // MX blocks need quads of lanes.
   if (scaling == NORM_FP8_MX && p.tpr % 4 != 0) return NORM_ERR_UNSUPPORTED;
   const int out = scaling == NORM_FP8_ROW ? kOutFp8Row : kOutFp8Mx;
-  if (p.C != 1 && out == kOutFp8Row) return NORM_ERR_UNSUPPORTED;
   const void *fn = p.long_rows ? long_fp8_kernel_ptr(mode, p.K, p.C > 1, p.exact, resid, out)
                                : fwd_fp8_kernel_ptr(mode, p.K, p.exact, resid, out, p.gsm);
   if (!fn) return NORM_ERR_UNSUPPORTED;

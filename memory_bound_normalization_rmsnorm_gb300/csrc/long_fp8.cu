@@ -1,6 +1,6 @@
 // long_fp8.cu -- E4M3-output instantiations of the long-row forward kernel
-// (long_kernel.cuh): MX block scaling with or without a cluster, per-row
-// scaling with one CTA per row; plain or fused-residual.  One chunk count
+// (long_kernel.cuh): MX block or per-row scaling, with or without a
+// cluster; plain or fused-residual.  One chunk count
 // per mode (8 for RMSNorm, 4 for LayerNorm: the long-row planner's choice).
 #include "long_kernel.cuh"
 
@@ -24,9 +24,12 @@ const void *pick(bool cluster, bool e, bool r, int out) {
     return r ? pick_exact<MODE, K, false, true, kOutFp8Mx>(e)
              : pick_exact<MODE, K, false, false, kOutFp8Mx>(e);
   }
-  if (out == kOutFp8Row && !cluster)
+  if (out == kOutFp8Row) {
+    if (cluster) return r ? pick_exact<MODE, K, true, true, kOutFp8Row>(e)
+                          : pick_exact<MODE, K, true, false, kOutFp8Row>(e);
     return r ? pick_exact<MODE, K, false, true, kOutFp8Row>(e)
              : pick_exact<MODE, K, false, false, kOutFp8Row>(e);
+  }
   return nullptr;
 }
 

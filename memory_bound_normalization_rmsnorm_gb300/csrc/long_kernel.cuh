@@ -46,11 +46,11 @@ struct Pending {
 // forms h = bf16(x + r) (sum in binary32, round to nearest even), writes it
 // over x in the stage, and the output pass writes h out beside y.
 // OUT: bf16 y (kOutBf16), or E4M3 codes with a per-row scale (kOutFp8Row;
-// clusters excluded: the row amax would need a second exchange round) or
-// with per-32-column E8M0 exponents (kOutFp8Mx; slices start on a block).
+// in a cluster the row amax takes a second exchange round, and the tiles are
+// not software-pipelined) or with per-32-column E8M0 exponents (kOutFp8Mx;
+// slices start on a block).
 template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT = kOutBf16>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const NormArgs a) {
-  static_assert(!(CLUSTER && OUT == kOutFp8Row), "per-row E4M3 scaling needs one CTA per row");
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 2 : 1, false, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -247,6 +247,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
         }
       }
       am = group_max<true>(am, a.tpr, g, a.G, t, red, rpar);
+      if (CLUSTER) {
+        // second exchange round: the CTAs' slice maxima, folded (max is
+        // exact, so every CTA gets the same amax)
+        cluster_push(am, 0.f, 0.f, r, t, xch);
+        const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
+        am = row[0];
+        for (int q = 1; q < xch.C; ++q) am = fmaxf(am, row[q * 4]);
+      }
       const float2 inv = splat2(am > 0.f ? __fdividef(448.f, am) : 1.f);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
                           make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
         }
       }
-      if (t == 0) a.qscale[row0 + r] = am > 0.f ? am * (1.0f / 448.0f) : 1.f;
+      if (t == 0 && crank == 0) a.qscale[row0 + r] = am > 0.f ? am * (1.0f / 448.0f) : 1.f;
     } else {
       // MX: a block is 4 consecutive chunks of 4 consecutive lanes (tpr is a
       // multiple of 32 and the slice starts on a block), so its amax is two
@@ -354,9 +362,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       cur.s = s;
       stats_pass(st, r, r < nrows, cur.a, cur.b, cur.c);
       cluster_push(cur.a, cur.b, cur.c, r, t, xch);
-      if (have_pend) finish(pend);
-      pend = cur;
-      have_pend = true;
+      if (OUT == kOutFp8Row) {
+        // the output pass pushes and waits for the amax round itself, so a
+        // tile is finished before the next one's statistics are pushed
+        // (exchange rounds are consumed in the order they were pushed)
+        finish(cur);
+      } else {
+        if (have_pend) finish(pend);
+        pend = cur;
+        have_pend = true;
+      }
     } else {
       for (int q = 0; q < a.rpg; ++q) {
         const int r = g + q * a.G;

@@ -127,9 +127,8 @@ def test_fp8_zero_rows_and_tiny_blocks():
                                       (1, 17, 24576), (0, 9, 65536), (0, 5, 131072)])
 def test_fp8_long_rows(mode, M, N, residual):
     """Rows wider than one CTA's registers (long-row kernels, clusters):
-    MX scaling everywhere; per-row scaling where one CTA holds the row, and
-    NORM_ERR_UNSUPPORTED where a cluster would (the amax would need a second
-    exchange round)."""
+    both scalings; with a cluster, per-row scaling exchanges the CTAs'
+    slice maxima in a second round."""
     base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
     case = wl.like(base, M, N)
     x, r, g, b, _, _ = [None if t is None else t.cuda()
@@ -139,11 +138,6 @@ def test_fp8_long_rows(mode, M, N, residual):
     plan = gb.norm_plan(M, N, mode, False, residual=residual, fp8=True)
     assert plan["long_rows"] == 1
     for gsc, osc in SCALINGS:
-        if gsc == gb.FP8_ROW and plan["cluster"] > 1:
-            with pytest.raises(gb.NormError) as e:
-                gb.norm_fwd_fp8(x, g, b, case.eps, mode, gsc, r=r)
-            assert e.value.status == 6
-            continue
         outs = gb.norm_fwd_fp8(x, g, b, case.eps, mode, gsc, r=r)
         torch.cuda.synchronize()
         _compare(case, x, r, g, b, outs, osc, label=f"long {mode}:{M}x{N}:{gsc}:{residual}")
