@@ -64,6 +64,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   grid_launch_dependents();
   grid_dependency_wait();
 
+  // The first S tiles are requested before anything else, so that their
+  // DRAM round trip overlaps the parameter loads below (warp 0, whose lane 0
+  // initialised the barriers, issues them after a warp sync).
+  const uint64_t pol = l2_evict_first_policy();
+  if (tid < 32) {
+    __syncwarp();
+    for (int j = 0; j < a.S; ++j) {
+      const int64_t tile = cid + j * ncl;
+      if (tile < a.ntiles) issue_bwd_tile<MODE, CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
+    }
+  }
+
   // gamma (fp32 pairs) and the column accumulators of this thread's chunks
   // live in registers for the whole kernel.
   float2 gf[K][4], accg[K][4], accb[K][4];
@@ -80,14 +92,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
   }
 
   if (CLUSTER) cluster_sync(); else __syncthreads();
-
-  const uint64_t pol = l2_evict_first_policy();
-  if (tid < 32) {
-    for (int j = 0; j < a.S; ++j) {
-      const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_bwd_tile<MODE, CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
-    }
-  }
 
   const float invN = a.invN;
   int rpar = 0;

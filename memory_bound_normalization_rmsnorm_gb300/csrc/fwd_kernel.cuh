@@ -83,6 +83,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   grid_launch_dependents();
   grid_dependency_wait();
 
+  // The first S tiles are requested before anything else, so that their
+  // DRAM round trip overlaps the parameter loads below (the thread that
+  // initialised the barriers issues them; the others wait on the barriers
+  // only after the block-wide sync that follows).
+  const uint64_t pol = l2_evict_first_policy();
+  if (tid == 0) {
+    for (int j = 0; j < a.S; ++j) {
+      const int64_t tile = cid + j * ncl;
+      if (tile < a.ntiles) issue_fwd_tile<CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
+    }
+  }
+
   // gamma as fp32 pairs (and beta packed) for this thread's chunks stay in
   // registers for the whole kernel: the thread owns the same columns in
   // every row.
@@ -160,14 +172,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   };
 
   if (CLUSTER) cluster_sync(); else __syncthreads();
-
-  const uint64_t pol = l2_evict_first_policy();
-  if (tid == 0) {
-    for (int j = 0; j < a.S; ++j) {
-      const int64_t tile = cid + j * ncl;
-      if (tile < a.ntiles) issue_fwd_tile<CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
-    }
-  }
 
   const float invN = a.invN;
   int rpar = 0;
