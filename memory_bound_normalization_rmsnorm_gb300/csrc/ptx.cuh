@@ -142,22 +142,6 @@ __device__ __forceinline__ void cluster_sync() {
   cluster_arrive_release();
   cluster_wait_acquire();
 }
-// Loads 4 floats from the shared memory of CTA `rank` of this cluster, at
-// the offset that `local` has in this CTA's shared memory.
-__device__ __forceinline__ float4 ld_dsmem_f32x4(const void *local,
-                                                 uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(smem_addr(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
-               : "memory");
-  return v;
-}
-
 // Shared::cluster address of `local` (this CTA's shared memory) in CTA
 // `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(const void *local, uint32_t rank) {
