@@ -91,3 +91,30 @@ def test_regimes_by_row_length():
     assert p["cluster"] > 1
     p = gb.norm_plan(4096, 131072, 0, True, SMS, OPTIN)
     assert p["cluster"] > 1
+
+
+def test_random_shapes_every_plan_kind():
+    """Seeded random (M, N) for every pass and variant: each plan the library
+    would launch on a GB300 is in bounds (plain, fused residual, E4M3)."""
+    import numpy as np
+
+    rng = np.random.default_rng(7)
+    n = 0
+    for _ in range(150):
+        N = int(rng.integers(1, 262144 // 8 + 1)) * 8
+        M = int(rng.choice([1, 3, 17, 1000, 4099, 65537]))
+        mode = int(rng.integers(0, 2))
+        for backward in (False, True):
+            for residual in (False, True):
+                p = gb.norm_plan(M, N, mode, backward, SMS, OPTIN, residual=residual)
+                launch_check.check_plan(p, M, N, mode, backward, OPTIN, residual=residual)
+                if backward:
+                    launch_check.check_reduce(p["partials"], N, 2 if mode == 1 else 1)
+                n += 1
+            if not backward:
+                p8 = gb.norm_plan(M, N, mode, False, SMS, OPTIN, fp8=True)
+                launch_check.check_plan(p8, M, N, mode, False, OPTIN)
+                launch_check.check_fp8_plan(p8, M, N, "row")
+                if N % 32 == 0:
+                    launch_check.check_fp8_plan(p8, M, N, "mx")
+    assert n == 600
