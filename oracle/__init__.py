@@ -117,10 +117,15 @@ class Oracle:
                                             ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                             ctypes.c_int, _i64p, ctypes.c_int64, _dp, _u8p,
                                             _dp, _dp, _u8p]
+        lib.oracle_norm_gemm_bf16.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
+                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+                                              ctypes.c_int, _i64p, ctypes.c_int64, _dp, _dp,
+                                              _dp]
         for f in (lib.oracle_fwd_f64, lib.oracle_bwd_f64, lib.oracle_fwd_bf16,
                   lib.oracle_bwd_dx_bf16, lib.oracle_param_grads_bf16,
                   lib.oracle_residual_add_bf16, lib.oracle_add_bwd_dx_bf16,
-                  lib.oracle_e4m3_encode, lib.oracle_e4m3_decode, lib.oracle_fwd_fp8_bf16):
+                  lib.oracle_e4m3_encode, lib.oracle_e4m3_decode, lib.oracle_fwd_fp8_bf16,
+                  lib.oracle_norm_gemm_bf16):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -283,6 +288,30 @@ class Oracle:
         return out
 
 
+    # ------------------------------------------- norm feeding a GEMM
+    def norm_gemm_bf16(self, x_bits, gamma_bits, beta_bits, w_bits, eps, mode, rows=None):
+        """out = norm(x) @ W^T in fp64, W [Nout, K] (one row per output
+        feature), for all rows of x or the listed ones.  y = norm(x) is the
+        unrounded fp64 forward.  Returns (out [R, Nout], rstd [R], mean [R])."""
+        x_bits = _u16(x_bits)
+        M, K = x_bits.shape
+        w_bits = _u16(w_bits)
+        Nout, K2 = w_bits.shape
+        if K2 != K:
+            raise ValueError("W must be [Nout, K]")
+        gamma_bits = _u16(gamma_bits)
+        beta_bits = None if beta_bits is None else _u16(beta_bits)
+        r, R = _rows(rows, M)
+        out = np.empty((R, Nout), np.float64)
+        rstd = np.empty(R, np.float64)
+        mean = np.empty(R, np.float64)
+        _check(self.lib.oracle_norm_gemm_bf16(
+            _ptr(x_bits, _u16p), _ptr(gamma_bits, _u16p), _ptr(beta_bits, _u16p),
+            _ptr(w_bits, _u16p), M, K, Nout, float(eps), int(mode), _ptr(r, _i64p), R,
+            _ptr(out, _dp), _ptr(rstd, _dp), _ptr(mean, _dp)), "oracle_norm_gemm_bf16")
+        return out, rstd, mean
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -333,6 +362,10 @@ def e4m3_decode(*a, **k):
 
 def fwd_fp8_bf16(*a, **k):
     return default().fwd_fp8_bf16(*a, **k)
+
+
+def norm_gemm_bf16(*a, **k):
+    return default().norm_gemm_bf16(*a, **k)
 
 
 def bf16_bits_to_f64(bits):

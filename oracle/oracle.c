@@ -544,3 +544,69 @@ int oracle_fwd_fp8_bf16(const uint16_t *x, const uint16_t *r,
     free(hrow);
     return rc;
 }
+
+/*
+ * Normalisation feeding a GEMM (the "Lazy Pre-Norm" fusion named in item 4,
+ * "Lazy Pre-Norm and Multi-CTA Norm Fusion", of the page "Towards Free
+ * Normalization: Fusing Normalization into GEMM and Attention Kernels"; its
+ * items 9 and 10 describe the GEMM that consumes the normalised rows).  The
+ * page gives no formula; the plainest reading is a pre-norm linear layer:
+ *
+ *   y   = norm(x)                (the forward definition above, in double,
+ *                                 with gamma and beta; y is NOT rounded)
+ *   out_ik = sum_j y_ij * W_kj   (W is [Nout, K] row-major: one row per
+ *                                 output feature, K = the normalised width)
+ *
+ * Written as the definition: the normalised row in double, then one dot
+ * product per output feature in increasing j.  How a fused kernel
+ * rearranges the arithmetic (folding gamma into W, applying rstd and the
+ * mean after the contraction) is its own business; the result here is the
+ * composition itself.  `rows` selects output rows as in oracle_fwd_bf16.
+ */
+int oracle_norm_gemm_bf16(const uint16_t *x, const uint16_t *gamma,
+                          const uint16_t *beta, const uint16_t *w, int64_t M,
+                          int64_t K, int64_t Nout, double eps, int mode,
+                          const int64_t *rows, int64_t nrows, double *out,
+                          double *rstd, double *mean)
+{
+    if (!x || !gamma || !w || !out || M < 0 || K < 1 || Nout < 1 || nrows < 0)
+        return -1;
+    if (!rows && nrows != M)
+        return -1;
+    double *xr = malloc(sizeof(double) * (size_t)K);
+    double *g = malloc(sizeof(double) * (size_t)K);
+    double *b = beta ? malloc(sizeof(double) * (size_t)K) : NULL;
+    double *yr = malloc(sizeof(double) * (size_t)K);
+    double *wr = malloc(sizeof(double) * (size_t)K);
+    if (!xr || !g || (beta && !b) || !yr || !wr) {
+        free(xr); free(g); free(b); free(yr); free(wr);
+        return -2;
+    }
+    widen_row(gamma, K, g);
+    if (beta)
+        widen_row(beta, K, b);
+    int rc = 0;
+    for (int64_t k = 0; k < nrows && rc == 0; ++k) {
+        int64_t i = rows ? rows[k] : k;
+        if (i < 0 || i >= M) {
+            rc = -1;
+            break;
+        }
+        widen_row(x + i * K, K, xr);
+        double mu, r;
+        fwd_row(xr, g, b, K, eps, mode, yr, &mu, &r);
+        if (rstd)
+            rstd[k] = r;
+        if (mean)
+            mean[k] = mu;
+        for (int64_t o = 0; o < Nout; ++o) {
+            widen_row(w + o * K, K, wr);
+            double s = 0.0;
+            for (int64_t j = 0; j < K; ++j)
+                s += yr[j] * wr[j];
+            out[k * Nout + o] = s;
+        }
+    }
+    free(xr); free(g); free(b); free(yr); free(wr);
+    return rc;
+}

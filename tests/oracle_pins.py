@@ -545,6 +545,99 @@ def pin_fp8_residual_composition(orc):
             assert np.array_equal(c["q"], a["q"][rows]) and np.array_equal(c["scale"], a["scale"][rows])
 
 
+# ------------------------------------------------ norm feeding a GEMM
+def _gemm_case(seed, M, K, Nout, offset=0.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(M, K, generator=g) + offset).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(K, generator=g)).to(torch.bfloat16)
+    beta = (0.1 * torch.randn(K, generator=g)).to(torch.bfloat16)
+    w = (torch.randn(Nout, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+    return x, gamma, beta, w
+
+
+def pin_norm_gemm_selection(orc):
+    """W whose row o holds one power of two s_o at column p(o) picks out
+    column p(o) of the normalised rows: out[:, o] = s_o * y[:, p(o)] exactly.
+    Pins the operand order (W is [Nout, K], one row per output feature) with
+    a non-square W and a permutation that is not its own inverse."""
+    K, Nout = 16, 24
+    x, gamma, beta, _ = _gemm_case(21, 5, K, Nout)
+    p = np.array([(3 * o + 1) % K for o in range(Nout)])
+    s = 2.0 ** np.array([(o % 5) - 2 for o in range(Nout)])
+    w = torch.zeros(Nout, K, dtype=torch.float64)
+    w[np.arange(Nout), p] = torch.tensor(s)
+    wb = _bits(w.to(torch.bfloat16))
+    for mode in (RMS, LAYER):
+        bb = _bits(beta) if mode == LAYER else None
+        y, rs, mu = orc.fwd_bf16(_bits(x), _bits(gamma), bb, 1e-5, mode)
+        out, rs2, mu2 = orc.norm_gemm_bf16(_bits(x), _bits(gamma), bb, wb, 1e-5, mode)
+        assert out.shape == (5, Nout)
+        assert np.array_equal(out, y[:, p] * s), f"selection W, mode {mode}"
+        assert np.array_equal(rs, rs2) and np.array_equal(mu, mu2), "saved stats"
+        rows = np.array([4, 0, 2])
+        o2, _, _ = orc.norm_gemm_bf16(_bits(x), _bits(gamma), bb, wb, 1e-5, mode, rows=rows)
+        assert np.array_equal(o2, out[rows]), "row selection"
+
+
+def pin_norm_gemm_torch(orc):
+    """torch CPU float64 layer_norm / rms_norm followed by F.linear (a library
+    implementation independent of the oracle) gives the same output."""
+    for M, K, Nout, off in ((3, 8, 5, 0.0), (7, 64, 40, 0.0), (9, 200, 33, 2.0),
+                            (4, 1024, 96, 0.5)):
+        x, gamma, beta, w = _gemm_case(22 + K, M, K, Nout, off)
+        xt, gt, bt, wt = (t.double() for t in (x, gamma, beta, w))
+        for mode in (RMS, LAYER):
+            if mode == LAYER:
+                yt = F.layer_norm(xt, (K,), gt, bt, 1e-5)
+            else:
+                yt = F.rms_norm(xt, (K,), gt, 1e-5)
+            want = F.linear(yt, wt).numpy()
+            scale = (yt.abs() @ wt.abs().T).numpy()
+            bb = _bits(beta) if mode == LAYER else None
+            out, _, _ = orc.norm_gemm_bf16(_bits(x), _bits(gamma), bb, _bits(w), 1e-5, mode)
+            _close(out, want, 0, 1e-13 * scale.max(), what=f"torch norm+linear {mode} {K}")
+
+
+def pin_norm_gemm_factorisation(orc):
+    """The lazy pre-norm identity that lets a GEMM normalise after the
+    contraction: with W' = W * gamma (per column), u = W' 1 and v = W beta,
+    out = rstd * (x W'^T - mean * u) + v, each term formed separately in
+    float64 from the raw x (row statistics taken with numpy)."""
+    for off in (0.0, 3.0):
+        x, gamma, beta, w = _gemm_case(31, 6, 48, 20, off)
+        X, G, B, W = (t.double().numpy() for t in (x, gamma, beta, w))
+        Wg = W * G[None, :]
+        u = Wg.sum(axis=1)
+        v = W @ B
+        for mode in (RMS, LAYER):
+            mu = X.mean(axis=1) if mode == LAYER else np.zeros(X.shape[0])
+            var = ((X - mu[:, None]) ** 2).mean(axis=1) if mode == LAYER else (X ** 2).mean(axis=1)
+            r = 1.0 / np.sqrt(var + 1e-5)
+            want = r[:, None] * (X @ Wg.T - mu[:, None] * u[None, :])
+            if mode == LAYER:
+                want = want + v[None, :]
+            bb = _bits(beta) if mode == LAYER else None
+            out, rs, mean = orc.norm_gemm_bf16(_bits(x), _bits(gamma), bb, _bits(w), 1e-5, mode)
+            scale = np.abs(r)[:, None] * (np.abs(X) @ np.abs(Wg).T) + np.abs(v)[None, :]
+            _close(out, want, 0, 1e-12 * scale.max(), what=f"factorisation {mode} off={off}")
+            _close(rs, r, 1e-13, what="rstd")
+
+
+def pin_norm_gemm_layer_constant_weights(orc):
+    """LayerNorm with gamma = 1: a constant weight row c sums the normalised
+    row, sum_j xhat_j = 0, so out = c * sum_j beta_j (and 0 with beta = 0)."""
+    K, Nout = 40, 6
+    x, _, beta, _ = _gemm_case(41, 7, K, Nout, 1.5)
+    ones = _bits(torch.ones(K, dtype=torch.bfloat16))
+    c = torch.tensor([1.0, -2.0, 0.5, 3.0, 0.25, -1.0], dtype=torch.float64)
+    wb = _bits(c[:, None].expand(Nout, K).to(torch.bfloat16).contiguous())
+    out, _, _ = orc.norm_gemm_bf16(_bits(x), ones, None, wb, 1e-5, LAYER)
+    _close(out, np.zeros_like(out), 0, 1e-12 * K, what="sum of xhat")
+    out, _, _ = orc.norm_gemm_bf16(_bits(x), ones, _bits(beta), wb, 1e-5, LAYER)
+    want = np.broadcast_to(c.numpy()[None, :] * beta.double().sum().item(), out.shape)
+    _close(out, want, 0, 1e-12 * K, what="c * sum beta")
+
+
 ALL_PINS = [
     pin_rms_constant_row,
     pin_layer_constant_row,
@@ -563,4 +656,8 @@ ALL_PINS = [
     pin_fp8_row_scaling,
     pin_fp8_mx_scaling,
     pin_fp8_residual_composition,
+    pin_norm_gemm_selection,
+    pin_norm_gemm_torch,
+    pin_norm_gemm_factorisation,
+    pin_norm_gemm_layer_constant_weights,
 ]

@@ -55,6 +55,11 @@ MUTANTS = {
     "mx_scale_applied_inverted": ("e4m3_code(ldexp(yb[j], -e));", "e4m3_code(ldexp(yb[j], e));"),
     "mx_amax_half_block": ("for (int j = 0; j < MX_BLOCK; ++j)\n                    if (fabs(yb[j]) > am)",
                            "for (int j = 0; j < MX_BLOCK / 2; ++j)\n                    if (fabs(yb[j]) > am)"),
+    "gemm_w_transposed": ("s += yr[j] * wr[j];",
+                          "s += yr[j] * bf16_bits_to_double(w[j * Nout + o]);"),
+    "gemm_x_not_y": ("s += yr[j] * wr[j];", "s += xr[j] * wr[j];"),
+    "gemm_one_w_row": ("widen_row(w + o * K, K, wr);", "widen_row(w, K, wr);"),
+    "gemm_gamma_twice": ("s += yr[j] * wr[j];", "s += yr[j] * wr[j] * g[j];"),
 }
 
 
