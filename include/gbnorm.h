@@ -293,6 +293,58 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
                         int sm_count, int smem_optin_bytes, norm_plan_t *out);
 
 /*
+ * Normalisation fused into a GEMM.  Item 4 of the page "Towards Free
+ * Normalization: Fusing Normalization into GEMM and Attention Kernels"
+ * names the Lazy Pre-Norm fusion; its items 9 and 10 give the obstacle it
+ * removes (the normalisation needs whole rows, a GEMM tiles rows and
+ * columns).  The operation is a pre-norm linear layer:
+ *
+ *   out = norm(x) W^T    x bf16 [M, K]; W bf16 [Nout, K], one row per
+ *                        output feature; out bf16 [M, Nout], row-major
+ *
+ * with norm the forward definition at the top of this file over the K
+ * columns of x (gamma, beta bf16 [K]).  The library applies the
+ * normalisation after the contraction, which is linear in the normalised
+ * row:
+ *
+ *   out_ik = rstd_i * (sum_j x_ij W'_kj - mean_i * u_k) + v_k
+ *   W'_kj = bf16(W_kj * gamma_j) (nearest even), u_k = sum_j W'_kj,
+ *   v_k = sum_j W_kj * beta_j    (mean = 0 and v = 0 for RMSNorm)
+ *
+ * norm_gemm_prepare makes W', u and v from the weights (once per weight
+ * update).  norm_gemm_fwd is one tcgen05 tensor-core GEMM on the raw x that
+ * takes each row's statistics from the tiles it streams and applies rstd
+ * and the mean correction in its epilogue; the normalised rows are never
+ * written.  Accumulation is fp32; out is rounded to nearest even.  Numerics
+ * differ from rounding norm(x) to bf16 before a bf16 GEMM: here x enters
+ * exactly and W * gamma is rounded once.  Results are bitwise reproducible
+ * for a given shape and device.
+ *
+ * norm_gemm_prepare: w [Nout, K]; gamma [K]; beta [K] or NULL (LAYER only,
+ *   NULL = 0; non-NULL with RMS is NORM_ERR_MODE); wg [Nout, K] bf16 out
+ *   (W'); u, v [Nout] fp32 out, required for LAYER (else NORM_ERR_MODE),
+ *   optional for RMS.
+ * norm_gemm_fwd: x [M, K]; wg, u, v from norm_gemm_prepare (u and v are
+ *   not read for RMS; required for LAYER); out [M, Nout]; rstd [M] fp32 out
+ *   (required); mean [M] fp32 out, required for LAYER and NULL for RMS
+ *   (else NORM_ERR_MODE); eps finite and >= 0 (else NORM_ERR_ARG).
+ * Both: device pointers owned by the caller, 16-byte aligned (else
+ *   NORM_ERR_ALIGN); outputs must not alias inputs; K % 64 == 0 with
+ *   64 <= K <= NORM_MAX_N, Nout % 32 == 0 with 32 <= Nout <= 2^24, and
+ *   1 <= M <= 8388480 (65535 tiles of 128 rows), else NORM_ERR_SHAPE.
+ *   Asynchronous on `stream`; a lost asynchronous copy or MMA surfaces
+ *   through norm_get_device_error.
+ */
+norm_status_t norm_gemm_prepare(const void *w, const void *gamma, const void *beta,
+                                int64_t K, int64_t Nout, norm_mode_t mode, void *wg,
+                                float *u, float *v, norm_stream_t stream);
+
+norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u,
+                            const float *v, int64_t M, int64_t K, int64_t Nout,
+                            float eps, norm_mode_t mode, void *out, float *rstd,
+                            float *mean, norm_stream_t stream);
+
+/*
  * Plan tuning.  The first page names the split size and the number of
  * pipeline stages as what Inductor's autotuner searches for these kernels;
  * the library's default plan comes from a heuristic and a table measured

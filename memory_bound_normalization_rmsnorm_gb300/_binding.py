@@ -118,6 +118,12 @@ def lib():
                                             _vp, ctypes.c_size_t, _vp]
             L.norm_fwd_bwd_host.restype = ctypes.c_int
             L.norm_add_bwd.restype = ctypes.c_int
+            L.norm_gemm_prepare.argtypes = [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp,
+                                            _vp, _vp]
+            L.norm_gemm_prepare.restype = ctypes.c_int
+            L.norm_gemm_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
+                                        ctypes.c_int, _vp, _vp, _vp, _vp]
+            L.norm_gemm_fwd.restype = ctypes.c_int
             L.norm_plan.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(Plan)]
             L.norm_plan.restype = ctypes.c_int
@@ -475,6 +481,70 @@ def norm_add_bwd(dy, dh, h, gamma, rstd, mean=None, mode=RMS, *, dx=None, dgamma
     if st != 0:
         raise NormError(st, "norm_add_bwd")
     return dx, dgamma, dbeta
+
+
+def norm_gemm_prepare(w, gamma, beta=None, mode=RMS, *, wg=None, u=None, v=None,
+                      stream=None):
+    """Weights of the normalisation-GEMM: W' = bf16(W * gamma) (gamma scales
+    the columns of W [Nout, K]), u = row sums of W' and v = W beta (fp32).
+    Returns (wg, u, v); u and v are None for RMSNorm unless given."""
+    mode = int(mode)
+    if w.dim() != 2:
+        raise ValueError("w must be [Nout, K]")
+    Nout, K = w.shape
+    dev = w.device
+    bf, f32 = torch.bfloat16, torch.float32
+    _check_tensor(w, "w", bf, (Nout, K), dev)
+    _check_tensor(gamma, "gamma", bf, (K,), dev)
+    _check_tensor(beta, "beta", bf, (K,), dev)
+    if wg is None:
+        wg = torch.empty_like(w)
+    if mode == LAYER:
+        if u is None:
+            u = torch.empty(Nout, dtype=f32, device=dev)
+        if v is None:
+            v = torch.empty(Nout, dtype=f32, device=dev)
+    _check_tensor(wg, "wg", bf, (Nout, K), dev)
+    _check_tensor(u, "u", f32, (Nout,), dev)
+    _check_tensor(v, "v", f32, (Nout,), dev)
+    st = lib().norm_gemm_prepare(_ptr(w), _ptr(gamma), _ptr(beta), K, Nout, mode, _ptr(wg),
+                                 _ptr(u), _ptr(v), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_gemm_prepare")
+    return wg, u, v
+
+
+def norm_gemm_fwd(x, wg, u=None, v=None, eps=1e-5, mode=RMS, *, out=None, rstd=None,
+                  mean=None, stream=None):
+    """out = norm(x) W^T through the fused tensor-core GEMM, with (wg, u, v)
+    from norm_gemm_prepare.  x is [..., K]; returns (out [..., Nout], rstd,
+    mean), mean None for RMSNorm."""
+    mode = int(mode)
+    M, K = _rows(x)
+    if wg.dim() != 2 or wg.shape[1] != K:
+        raise ValueError("wg must be [Nout, K]")
+    Nout = wg.shape[0]
+    dev = x.device
+    bf, f32 = torch.bfloat16, torch.float32
+    _check_tensor(x, "x", bf, x.shape, dev)
+    _check_tensor(wg, "wg", bf, (Nout, K), dev)
+    _check_tensor(u, "u", f32, (Nout,), dev)
+    _check_tensor(v, "v", f32, (Nout,), dev)
+    oshape = tuple(x.shape[:-1]) + (Nout,)
+    if out is None:
+        out = torch.empty(oshape, dtype=bf, device=dev)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=f32, device=dev)
+    if mode == LAYER and mean is None:
+        mean = torch.empty(x.shape[:-1], dtype=f32, device=dev)
+    _check_tensor(out, "out", bf, oshape, dev)
+    _check_tensor(rstd, "rstd", f32, x.shape[:-1], dev)
+    _check_tensor(mean, "mean", f32, x.shape[:-1], dev)
+    st = lib().norm_gemm_fwd(_ptr(x), _ptr(wg), _ptr(u), _ptr(v), M, K, Nout, float(eps), mode,
+                             _ptr(out), _ptr(rstd), _ptr(mean), _stream(stream, dev))
+    if st != 0:
+        raise NormError(st, "norm_gemm_fwd")
+    return out, rstd, mean
 
 
 def norm_plan(M, N, mode=RMS, backward=False, sm_count=0, smem_optin=0, residual=False,

@@ -736,6 +736,20 @@ norm_status_t reduce_rows(const float *rows, int P, int n, float *dgamma, float 
   return launch_reduce(rows, P, n, dgamma, dbeta, s);
 }
 
+// Ordinal, SM count, opt-in shared memory per block and device error word
+// of the current device (cached per device).
+norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err) {
+  DeviceInfo d;
+  int dv = 0;
+  norm_status_t st = device_info(&d, &dv);
+  if (st != NORM_OK) return st;
+  *dev = dv;
+  *sms = d.sms;
+  *smem_optin = d.smem_optin;
+  *err = d.err;
+  return NORM_OK;
+}
+
 }  // namespace gbn
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,451 @@
+// gemm.cu -- normalisation fused into the prologue of a tcgen05 GEMM
+// (norm_gemm_prepare / norm_gemm_fwd in include/gbnorm.h).
+//
+// out = norm(x) W^T with x [M, K] and W [Nout, K] in bf16 (one W row per
+// output feature), out bf16 [M, Nout].  Item 4 of the page "Towards Free
+// Normalization: Fusing Normalization into GEMM and Attention Kernels" names
+// the Lazy Pre-Norm fusion, and its items 9 and 10 the obstacle: the
+// normalisation wants whole rows while a GEMM tiles rows and columns.  Here
+// the normalisation is moved past the contraction, which is linear in the
+// normalised row:
+//
+//   out_ik = rstd_i * (sum_j x_ij W'_kj - mean_i * u_k) + v_k
+//   W' = bf16(W * gamma) (gamma scales the columns j), u = W' 1, v = W beta
+//
+// (mean = 0 and v = 0 for RMSNorm).  W', u and v depend on the weights only
+// and are made once by norm_gemm_prepare.  The GEMM then streams raw x
+// tiles through shared memory; four warps take each row's statistics from
+// the same tiles the tensor cores read, and the epilogue applies rstd and
+// the mean correction while it drains the fp32 accumulator from tensor
+// memory.  x is read from HBM once per output tile column (mostly hitting
+// L2), and the normalised rows are never written.
+//
+// One CTA computes one 128 x 256 output tile (6 warps, one CTA per SM):
+//   warp 4      allocates 256 TMEM columns, then (lane 0) issues the tiled
+//               TMA loads of the x and W' tiles into a 4-stage ring;
+//   warp 5      (lane 0) issues the tcgen05.mma instructions, 4 per 64-wide
+//               K block, and commits each stage back to the producer;
+//   warps 0-3   thread t owns row t of the tile: its statistics during the
+//               main loop (a Chan merge of per-block means and squared
+//               deviations for LayerNorm, a sum of squares for RMSNorm),
+//               then the epilogue on TMEM lane t.
+// Every wait is bounded: a lost copy or MMA sets the device error word, the
+// CTA still waits (bounded) for its own copies and MMAs in flight, frees its
+// tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "../../include/gbnorm.h"
+#include "common.cuh"
+#include "rowops.cuh"
+#include "tcgen05.cuh"
+
+namespace gbn {
+
+// Device error word and shape of the current device (api.cu).
+norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err);
+
+namespace {
+
+constexpr int kBM = 128;       // tile rows (TMEM lanes)
+constexpr int kBN = 256;       // tile columns (TMEM fp32 columns)
+constexpr int kBK = 64;        // K block: one 128-byte swizzle row of bf16
+constexpr int kUK = 16;        // K per tcgen05.mma of kind::f16
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kATile = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBTile = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kStageBytes = kATile + kBTile;
+constexpr uint32_t kTmemCols = 256;
+// Ring, then 2 * kStages + 1 mbarriers, the TMEM address slot and the abort
+// flag; plus slack to align the ring to 1024 bytes (128-byte swizzle atoms).
+constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+static_assert(kBK * 2 == 128, "one K block is one 128-byte swizzled row");
+static_assert(kBN % 32 == 0 && kBN <= 256 && kBM == 128, "tcgen05 tile shape");
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    norm_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ u,
+                     const float *__restrict__ v, uint16_t *__restrict__ out,
+                     float *__restrict__ rstd, float *__restrict__ mean, int M, int K, int Nout,
+                     float eps, uint32_t tx_bytes, unsigned *err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  uint8_t *ring = smem_raw + pad;
+  uint8_t *a_tiles = ring;
+  uint8_t *b_tiles = ring + kStages * kATile;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + kStages * kStageBytes);
+  uint64_t *empty = full + kStages;
+  uint64_t *done = empty + kStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int n0 = blockIdx.x * kBN;
+  const int m0 = blockIdx.y * kBM;
+  const int nk = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 4);  // the MMA commit and one arrival per statistics warp
+    }
+    mbar_init(done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages && !mbar_wait(&empty[s], (kb / kStages - 1) & 1, err, abort)) break;
+        mbar_arrive_expect_tx(&full[s], tx_bytes);
+        tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
+        tma_load_2d(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s]);
+        issued = kb + 1;
+      }
+      // No copy may still be landing in shared memory when the CTA exits.
+      volatile int never = 0;
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int loads = (issued - s + kStages - 1) / kStages;
+        mbar_wait(&full[s], (loads - 1) & 1, err, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (!mbar_wait(&full[s], (kb / kStages) & 1, err, abort)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(a_tiles + s * kATile);
+        const uint32_t b0 = smem_addr(b_tiles + s * kBTile);
+#pragma unroll
+        for (int k = 0; k < kBK / kUK; ++k)
+          mma_bf16_ss(tmem, desc_sw128(a0 + k * kUK * 2), desc_sw128(b0 + k * kUK * 2), idesc,
+                      (kb | k) != 0);
+        mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+      }
+      mma_commit(done);  // the accumulator is complete (or, after an abort, idle)
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------- row statistics, then the epilogue
+    const int t = threadIdx.x;  // row of the tile = TMEM lane
+    float run_mean = 0.f, run_m2 = 0.f, sumsq = 0.f;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (kb / kStages) & 1, err, abort));
+      if (ok) {
+        // Row t's 128 bytes; the 128-byte swizzle stores 16-byte chunk q at
+        // position q ^ (t % 8), which also spreads a quarter-warp over all
+        // banks.
+        const uint8_t *row = a_tiles + s * kATile + t * 128;
+        float2 xv[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 c = *reinterpret_cast<const uint4 *>(row + ((q ^ (t & 7)) << 4));
+          float2 f[4];
+          chunk_to_f2(c, f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) xv[q * 4 + e] = f[e];
+        }
+        if (MODE == kRMS) {
+          float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a = fma2(xv[e], xv[e], a);
+          sumsq += a.x + a.y;
+        } else {
+          float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a = add2(a, xv[e]);
+          const float mb = (a.x + a.y) * (1.f / kBK);
+          float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 d = add2(xv[e], splat2(-mb));
+            d2 = fma2(d, d, d2);
+          }
+          // Merge the block (kBK values, mean mb, squared deviations d2)
+          // into the running (kb * kBK values) statistics.
+          const float na = float(kb) * kBK;
+          const float n = na + kBK;
+          const float delta = mb - run_mean;
+          run_mean += delta * (kBK / n);
+          run_m2 += (d2.x + d2.y) + delta * delta * (na * kBK / n);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (!ok) break;
+    }
+    const float invK = 1.f / float(K);
+    const float mu = MODE == kRMS ? 0.f : run_mean;
+    const float r = rsqrtf((MODE == kRMS ? sumsq : run_m2) * invK + eps);
+    const int row = m0 + t;
+    if (blockIdx.x == 0 && row < M) {
+      rstd[row] = r;
+      if (MODE == kLayer) mean[row] = mu;
+    }
+
+    mbar_wait(done, 0, err, abort);
+    tc_fence_after();
+    const uint32_t t_lane = tmem + (uint32_t(warp * 32) << 16);
+    uint16_t *orow = out + size_t(row) * Nout;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int n = n0 + c * 32;
+      if (n >= Nout) break;  // the same for the whole warp
+      uint32_t acc[32];
+      tmem_ld32(t_lane + c * 32, acc);
+      tmem_wait_ld(acc);
+      if (row < M) {
+        uint32_t pk[16];
+        if (MODE == kRMS) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = f2_to_bf2(mul2(splat2(r), make_float2(__uint_as_float(acc[2 * e]),
+                                                          __uint_as_float(acc[2 * e + 1]))));
+        } else {
+          const float4 *u4 = reinterpret_cast<const float4 *>(u + n);
+          const float4 *v4 = reinterpret_cast<const float4 *>(v + n);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 uu = __ldg(u4 + q);
+            const float4 vv = __ldg(v4 + q);
+            const float2 a0 = make_float2(__uint_as_float(acc[4 * q]),
+                                          __uint_as_float(acc[4 * q + 1]));
+            const float2 a1 = make_float2(__uint_as_float(acc[4 * q + 2]),
+                                          __uint_as_float(acc[4 * q + 3]));
+            const float2 o0 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.x, uu.y), a0),
+                                   make_float2(vv.x, vv.y));
+            const float2 o1 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.z, uu.w), a1),
+                                   make_float2(vv.z, vv.w));
+            pk[2 * q] = f2_to_bf2(o0);
+            pk[2 * q + 1] = f2_to_bf2(o1);
+          }
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+
+  // Teardown: every MMA has finished before the tensor memory is freed.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    if (lane == 0) {
+      volatile int never = 0;
+      mbar_wait(done, 0, err, &never);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// W' = bf16(W * gamma) per column, u = row sums of W' and v = W beta (fp32,
+// fixed order: each lane strides the row in 8-element chunks, then a
+// butterfly over the warp).  One warp per W row.
+__global__ void __launch_bounds__(256)
+    norm_gemm_prepare_kernel(const uint16_t *__restrict__ w, const uint16_t *__restrict__ gamma,
+                             const uint16_t *__restrict__ beta, int K, int Nout,
+                             uint16_t *__restrict__ wg, float *__restrict__ u,
+                             float *__restrict__ v) {
+  const int o = blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (o >= Nout) return;
+  const uint16_t *wr = w + size_t(o) * K;
+  uint16_t *gr = wg + size_t(o) * K;
+  float su = 0.f, sv = 0.f;
+  for (int j = lane * 8; j < K; j += 256) {
+    float2 wv[4], gv[4], p[4], pr[4];
+    chunk_to_f2(ld_global_nc_v4(wr + j), wv);
+    chunk_to_f2(ld_global_nc_v4(gamma + j), gv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = mul2(wv[e], gv[e]);  // exact: 8-bit x 8-bit significands
+    const uint4 pc = f2_to_chunk(p);
+    *reinterpret_cast<uint4 *>(gr + j) = pc;
+    chunk_to_f2(pc, pr);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) su = (su + pr[e].x) + pr[e].y;
+    if (beta) {
+      float2 bv[4];
+      chunk_to_f2(ld_global_nc_v4(beta + j), bv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sv = fmaf(wv[e].y, bv[e].y, fmaf(wv[e].x, bv[e].x, sv));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    su += __shfl_xor_sync(0xffffffffu, su, off);
+    sv += __shfl_xor_sync(0xffffffffu, sv, off);
+  }
+  if (lane == 0) {
+    if (u) u[o] = su;
+    if (v) v[o] = sv;
+  }
+}
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::set<std::pair<int, const void *>> g_attr_done;
+
+norm_status_t encoder(PFN_cuTensorMapEncodeTiled_v12000 *out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      return NORM_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return NORM_OK;
+}
+
+// Row-major bf16 [rows, cols] with boxes of box_rows x 64 columns, 128-byte
+// swizzle, zero fill outside the tensor.
+norm_status_t make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                       uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  norm_status_t st = encoder(&enc);
+  if (st != NORM_OK) return st;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {cuuint32_t(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NORM_OK : NORM_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
+  if (M < 1 || M > int64_t(65535) * kBM) return NORM_ERR_SHAPE;
+  if (K < kBK || K > NORM_MAX_N || K % kBK != 0) return NORM_ERR_SHAPE;
+  if (Nout < 32 || Nout > (int64_t(1) << 24) || Nout % 32 != 0) return NORM_ERR_SHAPE;
+  return NORM_OK;
+}
+
+}  // namespace
+
+const void *norm_gemm_kernel_ptr(int mode) {
+  return mode == kRMS ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS>)
+                      : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer>);
+}
+
+}  // namespace gbn
+
+using namespace gbn;
+
+extern "C" {
+
+norm_status_t norm_gemm_prepare(const void *w, const void *gamma, const void *beta, int64_t K,
+                                int64_t Nout, norm_mode_t mode, void *wg, float *u, float *v,
+                                norm_stream_t stream) {
+  if (mode != NORM_RMS && mode != NORM_LAYER) return NORM_ERR_MODE;
+  if (!w || !gamma || !wg) return NORM_ERR_NULL;
+  if (mode == NORM_RMS && beta) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && (!u || !v)) return NORM_ERR_MODE;
+  norm_status_t st = check_shape(1, K, Nout);
+  if (st != NORM_OK) return st;
+  const void *ptrs[] = {w, gamma, beta, wg, u, v};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return NORM_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  norm_gemm_prepare_kernel<<<unsigned((Nout + 7) / 8), 256, 0, s>>>(
+      static_cast<const uint16_t *>(w), static_cast<const uint16_t *>(gamma),
+      static_cast<const uint16_t *>(beta), int(K), int(Nout), static_cast<uint16_t *>(wg), u,
+      v);
+  if (cudaGetLastError() != cudaSuccess) return NORM_ERR_CUDA;
+  return NORM_OK;
+}
+
+norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const float *v,
+                            int64_t M, int64_t K, int64_t Nout, float eps, norm_mode_t mode,
+                            void *out, float *rstd, float *mean, norm_stream_t stream) {
+  if (mode != NORM_RMS && mode != NORM_LAYER) return NORM_ERR_MODE;
+  if (!x || !wg || !out || !rstd) return NORM_ERR_NULL;
+  if (mode == NORM_RMS && mean) return NORM_ERR_MODE;
+  if (mode == NORM_LAYER && (!mean || !u || !v)) return NORM_ERR_MODE;
+  norm_status_t st = check_shape(M, K, Nout);
+  if (st != NORM_OK) return st;
+  if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+  const void *ptrs[] = {x, wg, u, v, out, rstd, mean};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return NORM_ERR_ALIGN;
+
+  int dev = 0, sms = 0, optin = 0;
+  unsigned *err = nullptr;
+  if ((st = device_context(&dev, &sms, &optin, &err)) != NORM_OK) return st;
+  if (optin < int(kSmemBytes)) return NORM_ERR_UNSUPPORTED;
+  const void *fn = norm_gemm_kernel_ptr(mode);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_attr_done.count({dev, fn})) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(kSmemBytes)) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+      }
+      g_attr_done.insert({dev, fn});
+    }
+  }
+  // Boxes no taller than the tensor: a tile's rows beyond M (or Nout) are
+  // then left as they were in shared memory; they only reach accumulator
+  // rows (columns) that are never stored.
+  const uint32_t box_x = uint32_t(M < kBM ? M : kBM);
+  const uint32_t box_w = uint32_t(Nout < kBN ? Nout : kBN);
+  uint32_t tx = (box_x + box_w) * kBK * 2;
+  CUtensorMap tm_x, tm_w;
+  if ((st = make_map(&tm_x, x, M, K, box_x)) != NORM_OK) return st;
+  if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((Nout + kBN - 1) / kBN), unsigned((M + kBM - 1) / kBM));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  int Mi = int(M), Ki = int(K), Ni = int(Nout);
+  uint16_t *o = static_cast<uint16_t *>(out);
+  void *args[] = {&tm_x, &tm_w, &u, &v, &o, &rstd, &mean, &Mi, &Ki, &Ni, &eps, &tx, &err};
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return NORM_OK;
+}
+
+}  // extern "C"

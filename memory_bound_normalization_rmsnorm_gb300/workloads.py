@@ -149,3 +149,15 @@ def make_residual_inputs(w: Workload, device="cpu", seed=None):
         dh.mul_(w.dy_scale)
     dh = dh.to(torch.bfloat16)
     return x, r, gamma, beta, dy, dh
+
+
+def make_gemm_weight(w: Workload, Nout: int, device="cpu", seed=None):
+    """Weight [Nout, K = w.N] of the linear layer that consumes the
+    normalised rows: N(0, 1/K) entries (the usual fan-in scaled
+    initialisation), drawn in fp32 from a generator seeded with seed + 2 and
+    rounded to bf16."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed((w.seed if seed is None else seed) + 2)
+    wt = torch.randn(Nout, w.N, dtype=torch.float32, device=dev, generator=g)
+    return (wt * (1.0 / w.N ** 0.5)).to(torch.bfloat16)

@@ -152,6 +152,58 @@ def test_bwd_validation_codes():
     assert call(dx=F + 2) == 3
 
 
+def test_norm_gemm_validation_codes():
+    L = gb.lib()
+    pf = L.norm_gemm_prepare
+    okp = dict(w=F, g=F, b=None, K=128, Nout=64, mode=0, wg=F, u=None, v=None)
+
+    def prep(**kw):
+        a = dict(okp, **kw)
+        return pf(a["w"], a["g"], a["b"], a["K"], a["Nout"], a["mode"], a["wg"], a["u"], a["v"],
+                  None)
+
+    assert prep(w=None) == 1
+    assert prep(wg=None) == 1
+    assert prep(mode=3) == 4
+    assert prep(b=F) == 4                       # beta with RMSNorm
+    assert prep(mode=1) == 4                    # LayerNorm without u, v
+    assert prep(mode=1, u=F) == 4
+    assert prep(K=96) == 2                      # K % 64
+    assert prep(K=0) == 2
+    assert prep(Nout=48) == 2                   # Nout % 32
+    assert prep(g=F + 8) == 3
+    assert prep(mode=1, u=F, v=F + 4) == 3
+
+    ff = L.norm_gemm_fwd
+    okf = dict(x=F, wg=F, u=None, v=None, M=5, K=128, Nout=64, eps=1e-5, mode=0, out=F, r=F,
+               m=None)
+
+    def fwd(**kw):
+        a = dict(okf, **kw)
+        return ff(a["x"], a["wg"], a["u"], a["v"], a["M"], a["K"], a["Nout"], a["eps"],
+                  a["mode"], a["out"], a["r"], a["m"], None)
+
+    assert fwd(x=None) == 1
+    assert fwd(out=None) == 1
+    assert fwd(r=None) == 1
+    assert fwd(mode=2) == 4
+    assert fwd(m=F) == 4                        # mean with RMSNorm
+    assert fwd(mode=1, m=F) == 4                # LayerNorm without u, v
+    assert fwd(mode=1, u=F, v=F) == 4           # LayerNorm without mean
+    assert fwd(M=0) == 2
+    assert fwd(M=65535 * 128 + 1) == 2
+    assert fwd(K=100) == 2
+    assert fwd(K=262144 + 64) == 2
+    assert fwd(Nout=16) == 2
+    assert fwd(Nout=80) == 2
+    assert fwd(eps=float("nan")) == 9
+    assert fwd(eps=-1.0) == 9
+    assert fwd(x=F + 2) == 3
+    assert fwd(out=F + 8) == 3
+    if not torch.cuda.is_available():
+        assert fwd() == 7                       # valid arguments, no device
+
+
 def test_selftest_argument_checks():
     L = gb.lib()
     assert L.norm_selftest_wait_timeout(0, None) == 9

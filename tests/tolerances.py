@@ -62,3 +62,53 @@ def check_t2(gpu, ref, scale=None, name=""):
         g, r, b = gpu.reshape(-1), ref.reshape(-1), np.broadcast_to(bound, ref.shape).reshape(-1)
         msg = "; ".join(f"[{i}] gpu={g[i]!r} ref={r[i]!r} bound={b[i]:.3g}" for i in idx)
         raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} out of tolerance: {msg}")
+
+
+def check_t4(gpu, ref, x, gamma, beta, w, rstd, mean, name=""):
+    """T4, the normalisation-GEMM out = norm(x) W^T (bf16 out [R, Nout]).
+
+    The kernel computes rstd * (x W'^T - mean * u) + v with W' = bf16(W *
+    gamma), fp32 accumulation, and rounds the result to bf16.  With
+    tau_j = xhat_j * gamma_j * W_kj (the exact terms) and u_b = 2^-8 (bf16
+    unit roundoff), each element obeys the worst-case bound
+        |gpu - ref| <= (u_b + 2^-20) |ref| + u_b * sum_j |tau_j|
+                       + K 2^-23 * (rstd (sum_j |x_j gamma_j W_kj|
+                                          + |mean| sum_j |gamma_j W_kj|)
+                                    + sum_j |beta_j W_kj| + |ref - v_k|)
+    (output rounding; W' rounding, at most u_b per term; fp32 sums of K
+    terms, in the contraction, in u, v and the row statistics).  The bound is
+    loose for random signs, so the RMS error over all elements is also held
+    to 1.5x its expected size, sqrt(u_b^2 / 3 * mean(sum_j tau_j^2 + ref^2))
+    (independent rounding errors, each at most u_b relative).
+
+    x: float64 [R, K] (the bf16 rows), gamma/beta float64 [K] (beta may be
+    None), w float64 [Nout, K]; rstd/mean: the oracle's fp64 statistics [R].
+    """
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    K = x.shape[1]
+    ub = 2.0 ** -8
+    mu = np.zeros(x.shape[0]) if mean is None else np.asarray(mean, np.float64)
+    r = np.asarray(rstd, np.float64)
+    xhat = (x - mu[:, None]) * r[:, None]
+    gw = np.abs(w * gamma[None, :])                      # |gamma_j W_kj|
+    A = np.abs(xhat) @ gw.T
+    Q = (xhat ** 2) @ (gw ** 2).T
+    B = r[:, None] * (np.abs(x) @ gw.T + np.abs(mu)[:, None] * gw.sum(axis=1)[None, :])
+    v = np.zeros(w.shape[0]) if beta is None else w @ beta
+    V = np.zeros(w.shape[0]) if beta is None else np.abs(w) @ np.abs(beta)
+    bound = ((ub + 2.0 ** -20) * np.abs(ref) + ub * A
+             + K * 2.0 ** -23 * (B + V[None, :] + np.abs(ref - v[None, :])))
+    err = np.abs(gpu - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        msg = "; ".join(f"[{i},{j}] gpu={gpu[i, j]!r} ref={ref[i, j]!r} bound={bound[i, j]:.3g}"
+                        for i, j in idx)
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements out of "
+                             f"tolerance: {msg}")
+    rms = float(np.sqrt(np.mean(err ** 2)))
+    expect = float(np.sqrt(ub ** 2 / 3.0 * np.mean(Q + ref ** 2)))
+    assert rms <= 1.5 * expect, f"{name}: RMS error {rms:.3g} above 1.5 x expected {expect:.3g}"
+    return rms / expect
