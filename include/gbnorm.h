@@ -330,7 +330,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
  *   (else NORM_ERR_MODE); eps finite and >= 0 (else NORM_ERR_ARG).
  * Both: device pointers owned by the caller, 16-byte aligned (else
  *   NORM_ERR_ALIGN); outputs must not alias inputs; K % 64 == 0 with
- *   64 <= K <= NORM_MAX_N, Nout % 32 == 0 with 32 <= Nout <= 2^24, and
+ *   64 <= K <= NORM_MAX_N, Nout % 32 == 0 with 32 <= Nout <= 2^20, and
  *   1 <= M <= 8388480 (65535 tiles of 128 rows), else NORM_ERR_SHAPE.
  *   Asynchronous on `stream`; a lost asynchronous copy or MMA surfaces
  *   through norm_get_device_error.

@@ -20,15 +20,23 @@
 // memory.  x is read from HBM once per output tile column (mostly hitting
 // L2), and the normalised rows are never written.
 //
-// One CTA computes one 128 x 256 output tile (6 warps, one CTA per SM):
-//   warp 4      allocates 256 TMEM columns, then (lane 0) issues the tiled
-//               TMA loads of the x and W' tiles into a 4-stage ring;
-//   warp 5      (lane 0) issues the tcgen05.mma instructions, 4 per 64-wide
-//               K block, and commits each stage back to the producer;
-//   warps 0-3   thread t owns row t of the tile: its statistics during the
-//               main loop (a Chan merge of per-block means and squared
-//               deviations for LayerNorm, a sum of squares for RMSNorm),
-//               then the epilogue on TMEM lane t.
+// A persistent grid (one CTA per SM, 12 warps) walks the 128 x 256 output
+// tiles in row-major tile order (tile j of CTA c is c + j * gridDim.x):
+//   warp 0      (lane 0) issues the tiled TMA loads of the x and W' tiles
+//               into a 4-stage ring (128-byte swizzle);
+//   warp 1      (lane 0) issues the tcgen05.mma instructions, 4 per 64-wide
+//               K block, into one of two 256-column fp32 accumulators in
+//               tensor memory, and commits each stage back to the producer;
+//   warp 2      allocates (and at the end frees) the 512 TMEM columns;
+//   warps 8-11  thread t owns row t of the current tile: its statistics,
+//               from the x tiles in the ring, handed to the epilogue
+//               through shared memory (two slots);
+//   warps 4-7   the epilogue of the previous tile, on TMEM lane t, while
+//               the tensor cores fill the other accumulator.
+// Row statistics use shifted sums: the mean of the row's first 64 values,
+// rounded to bf16, is the shift c, and sum(x - c), sum((x - c)^2) give the
+// mean and the population variance without the cancellation of raw power
+// sums.
 // Every wait is bounded: a lost copy or MMA sets the device error word, the
 // CTA still waits (bounded) for its own copies and MMAs in flight, frees its
 // tensor memory and exits.
@@ -54,21 +62,26 @@ norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err
 namespace {
 
 constexpr int kBM = 128;       // tile rows (TMEM lanes)
-constexpr int kBN = 256;       // tile columns (TMEM fp32 columns)
+constexpr int kBN = 256;       // tile columns (fp32 TMEM columns per accumulator)
 constexpr int kBK = 64;        // K block: one 128-byte swizzle row of bf16
 constexpr int kUK = 16;        // K per tcgen05.mma of kind::f16
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;   // warps 4-7: TMEM lane quarters 0-3
+constexpr int kStatWarp0 = 8;  // warps 8-11
 constexpr uint32_t kATile = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBTile = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kStageBytes = kATile + kBTile;
-constexpr uint32_t kTmemCols = 256;
-// Ring, then 2 * kStages + 1 mbarriers, the TMEM address slot and the abort
-// flag; plus slack to align the ring to 1024 bytes (128-byte swizzle atoms).
-constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+constexpr uint32_t kTmemCols = 2 * kBN;     // two accumulators: all 512 columns
+constexpr int kNumBars = 2 * kStages + 8 + 1;
+// Ring, mbarriers, TMEM address slot and abort flag, two slots of per-row
+// (rstd, mean); plus slack to align the ring to 1024 bytes (the 128-byte
+// swizzle atom is 8 rows of 128 bytes).
+constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256 + 2 * kBM * 8;
 
 static_assert(kBK * 2 == 128, "one K block is one 128-byte swizzled row");
 static_assert(kBN % 32 == 0 && kBN <= 256 && kBM == 128, "tcgen05 tile shape");
+static_assert(kNumBars * 8 + 8 <= 256, "barrier region");
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -83,27 +96,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *a_tiles = ring;
   uint8_t *b_tiles = ring + kStages * kATile;
   uint64_t *full = reinterpret_cast<uint64_t *>(ring + kStages * kStageBytes);
-  uint64_t *empty = full + kStages;
-  uint64_t *done = empty + kStages;
+  uint64_t *empty = full + kStages;      // [kStages]
+  uint64_t *acc_full = empty + kStages;  // [2] accumulator complete
+  uint64_t *acc_empty = acc_full + 2;    // [2] accumulator drained
+  uint64_t *st_full = acc_empty + 2;     // [2] row statistics written
+  uint64_t *st_empty = st_full + 2;      // [2] row statistics read
+  uint64_t *done = st_empty + 2;         // every MMA of the CTA finished
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float2 *stats = reinterpret_cast<float2 *>(ring + kStages * kStageBytes + 256);  // [2][kBM]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int n0 = blockIdx.x * kBN;
-  const int m0 = blockIdx.y * kBM;
   const int nk = K / kBK;
+  const int n_tiles = (Nout + kBN - 1) / kBN;
+  const int ntiles = ((M + kBM - 1) / kBM) * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1 + 4);  // the MMA commit and one arrival per statistics warp
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+      mbar_init(&st_full[b], 128);
+      mbar_init(&st_empty[b], 128);
+    }
     mbar_init(done, 1);
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 2) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -112,153 +136,214 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(&empty[s], (kb / kStages - 1) & 1, err, abort)) break;
-        mbar_arrive_expect_tx(&full[s], tx_bytes);
-        tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
-        tma_load_2d(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s]);
-        issued = kb + 1;
+      int g = 0;  // K blocks issued by this CTA (all tiles)
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles) * kBM;
+        const int n0 = (tile % n_tiles) * kBN;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages) {
+            if (!mbar_wait(&empty[s], (g / kStages - 1) & 1, err, abort)) {
+              ok = false;
+              break;
+            }
+            // The statistics warps read the stage through the generic
+            // proxy; order those reads before the asynchronous-proxy refill.
+            fence_proxy_async_smem();
+          }
+          mbar_arrive_expect_tx(&full[s], tx_bytes);
+          tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
+          tma_load_2d(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s]);
+        }
       }
       // No copy may still be landing in shared memory when the CTA exits.
       volatile int never = 0;
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int loads = (issued - s + kStages - 1) / kStages;
+      for (int s = 0; s < kStages && s < g; ++s) {
+        const int loads = (g - s + kStages - 1) / kStages;
         mbar_wait(&full[s], (loads - 1) & 1, err, &never);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&full[s], (kb / kStages) & 1, err, abort)) break;
+      int g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x, j = 0; ok && tile < ntiles; tile += gridDim.x, ++j) {
+        const int b = j & 1;
+        if (j >= 2 && !mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, err, abort)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_addr(a_tiles + s * kATile);
-        const uint32_t b0 = smem_addr(b_tiles + s * kBTile);
+        const uint32_t d = tmem + uint32_t(b * kBN);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!mbar_wait(&full[s], (g / kStages) & 1, err, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(a_tiles + s * kATile);
+          const uint32_t b0 = smem_addr(b_tiles + s * kBTile);
 #pragma unroll
-        for (int k = 0; k < kBK / kUK; ++k)
-          mma_bf16_ss(tmem, desc_sw128(a0 + k * kUK * 2), desc_sw128(b0 + k * kUK * 2), idesc,
-                      (kb | k) != 0);
-        mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+          for (int k = 0; k < kBK / kUK; ++k)
+            mma_bf16_ss(d, desc_sw128(a0 + k * kUK * 2), desc_sw128(b0 + k * kUK * 2), idesc,
+                        (kb | k) != 0);
+          mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        if (ok) mma_commit(&acc_full[b]);
       }
-      mma_commit(done);  // the accumulator is complete (or, after an abort, idle)
+      mma_commit(done);  // arrives when every MMA issued above has completed
     }
     __syncwarp();
-  } else {
-    // ------------------------------- row statistics, then the epilogue
-    const int t = threadIdx.x;  // row of the tile = TMEM lane
-    float run_mean = 0.f, run_m2 = 0.f, sumsq = 0.f;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (kb / kStages) & 1, err, abort));
-      if (ok) {
+  } else if (warp >= kStatWarp0) {
+    // ------------------------------------------------ row statistics
+    const int t = threadIdx.x - kStatWarp0 * 32;  // row of the tile
+    int g = 0;
+    for (int tile = blockIdx.x, j = 0; tile < ntiles; tile += gridDim.x, ++j) {
+      const int b = j & 1;
+      float2 s1[4], s2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
+      float c = 0.f;  // shift (LayerNorm): mean of the row's first 64 values
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int s = g % kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, err, abort));
+        if (!ok) break;
         // Row t's 128 bytes; the 128-byte swizzle stores 16-byte chunk q at
         // position q ^ (t % 8), which also spreads a quarter-warp over all
-        // banks.
+        // 32 banks.
         const uint8_t *row = a_tiles + s * kATile + t * 128;
         float2 xv[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 c = *reinterpret_cast<const uint4 *>(row + ((q ^ (t & 7)) << 4));
+          const uint4 cq = *reinterpret_cast<const uint4 *>(row + ((q ^ (t & 7)) << 4));
           float2 f[4];
-          chunk_to_f2(c, f);
+          chunk_to_f2(cq, f);
 #pragma unroll
           for (int e = 0; e < 4; ++e) xv[q * 4 + e] = f[e];
         }
         if (MODE == kRMS) {
-          float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a = fma2(xv[e], xv[e], a);
-          sumsq += a.x + a.y;
+          for (int e = 0; e < 32; ++e) s2[e & 3] = fma2(xv[e], xv[e], s2[e & 3]);
         } else {
-          float2 a = make_float2(0.f, 0.f);
+          if (kb == 0) {
+            float2 a[4] = {xv[0], xv[1], xv[2], xv[3]};
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a = add2(a, xv[e]);
-          const float mb = (a.x + a.y) * (1.f / kBK);
-          float2 d2 = make_float2(0.f, 0.f);
+            for (int e = 4; e < 32; ++e) a[e & 3] = add2(a[e & 3], xv[e]);
+            const float2 a01 = add2(add2(a[0], a[1]), add2(a[2], a[3]));
+            // Rounded to bf16, so that x - c is exact in fp32 (two 8-bit
+            // significands less than 2^16 apart in magnitude); an fp32
+            // shift would round every difference the same way and bias the
+            // sum.
+            c = __bfloat162float(__float2bfloat16_rn((a01.x + a01.y) * (1.f / kBK)));
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float2 d = add2(xv[e], splat2(-mb));
-            d2 = fma2(d, d, d2);
+            const float2 dv = add2(xv[e], splat2(-c));
+            s1[e & 3] = add2(s1[e & 3], dv);
+            s2[e & 3] = fma2(dv, dv, s2[e & 3]);
           }
-          // Merge the block (kBK values, mean mb, squared deviations d2)
-          // into the running (kb * kBK values) statistics.
-          const float na = float(kb) * kBK;
-          const float n = na + kBK;
-          const float delta = mb - run_mean;
-          run_mean += delta * (kBK / n);
-          run_m2 += (d2.x + d2.y) + delta * delta * (na * kBK / n);
         }
+        // The stage is released only after its values have been consumed:
+        // an arrival right after the loads were issued let the refill land
+        // under loads still in flight.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
       if (!ok) break;
-    }
-    const float invK = 1.f / float(K);
-    const float mu = MODE == kRMS ? 0.f : run_mean;
-    const float r = rsqrtf((MODE == kRMS ? sumsq : run_m2) * invK + eps);
-    const int row = m0 + t;
-    if (blockIdx.x == 0 && row < M) {
-      rstd[row] = r;
-      if (MODE == kLayer) mean[row] = mu;
-    }
-
-    mbar_wait(done, 0, err, abort);
-    tc_fence_after();
-    const uint32_t t_lane = tmem + (uint32_t(warp * 32) << 16);
-    uint16_t *orow = out + size_t(row) * Nout;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int n = n0 + c * 32;
-      if (n >= Nout) break;  // the same for the whole warp
-      uint32_t acc[32];
-      tmem_ld32(t_lane + c * 32, acc);
-      tmem_wait_ld(acc);
-      if (row < M) {
-        uint32_t pk[16];
-        if (MODE == kRMS) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = f2_to_bf2(mul2(splat2(r), make_float2(__uint_as_float(acc[2 * e]),
-                                                          __uint_as_float(acc[2 * e + 1]))));
-        } else {
-          const float4 *u4 = reinterpret_cast<const float4 *>(u + n);
-          const float4 *v4 = reinterpret_cast<const float4 *>(v + n);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 uu = __ldg(u4 + q);
-            const float4 vv = __ldg(v4 + q);
-            const float2 a0 = make_float2(__uint_as_float(acc[4 * q]),
-                                          __uint_as_float(acc[4 * q + 1]));
-            const float2 a1 = make_float2(__uint_as_float(acc[4 * q + 2]),
-                                          __uint_as_float(acc[4 * q + 3]));
-            const float2 o0 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.x, uu.y), a0),
-                                   make_float2(vv.x, vv.y));
-            const float2 o1 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.z, uu.w), a1),
-                                   make_float2(vv.z, vv.w));
-            pk[2 * q] = f2_to_bf2(o0);
-            pk[2 * q + 1] = f2_to_bf2(o1);
-          }
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + n);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      const float invK = 1.f / float(K);
+      const float2 q2 = add2(add2(s2[0], s2[1]), add2(s2[2], s2[3]));
+      float mu = 0.f, var;
+      if (MODE == kRMS) {
+        var = (q2.x + q2.y) * invK;
+      } else {
+        const float2 q1 = add2(add2(s1[0], s1[1]), add2(s1[2], s1[3]));
+        const float d1 = (q1.x + q1.y) * invK;  // mean - c
+        var = fmaxf(fmaf(-d1, d1, (q2.x + q2.y) * invK), 0.f);
+        mu = c + d1;
       }
+      const float r = rsqrtf(var + eps);
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&st_empty[b], ((j >> 1) - 1) & 1, err, abort)))
+        break;
+      stats[b * kBM + t] = make_float2(r, mu);
+      mbar_arrive(&st_full[b]);
+      const int row = (tile / n_tiles) * kBM + t;
+      if (tile % n_tiles == 0 && row < M) {
+        rstd[row] = r;
+        if (MODE == kLayer) mean[row] = mu;
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------ epilogue
+    const int t = threadIdx.x - kEpiWarp0 * 32;  // row of the tile = TMEM lane
+    const int quarter = warp - kEpiWarp0;        // == warp % 4: TMEM lanes 32q .. 32q + 31
+    for (int tile = blockIdx.x, j = 0; tile < ntiles; tile += gridDim.x, ++j) {
+      const int b = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[b], ph, err, abort))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&st_full[b], ph, err, abort))) break;
+      tc_fence_after();
+      const float2 rm = stats[b * kBM + t];
+      mbar_arrive(&st_empty[b]);
+      const float r = rm.x, mu = rm.y;
+      const int row = (tile / n_tiles) * kBM + t;
+      const int n0 = (tile % n_tiles) * kBN;
+      const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * kBN);
+      uint16_t *orow = out + size_t(row) * Nout;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int n = n0 + c * 32;
+        if (n >= Nout) break;  // the same for the whole warp
+        uint32_t acc[32];
+        tmem_ld32(t_lane + c * 32, acc);
+        tmem_wait_ld(acc);
+        if (row < M) {
+          uint32_t pk[16];
+          if (MODE == kRMS) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = f2_to_bf2(mul2(splat2(r), make_float2(__uint_as_float(acc[2 * e]),
+                                                            __uint_as_float(acc[2 * e + 1]))));
+          } else {
+            const float4 *u4 = reinterpret_cast<const float4 *>(u + n);
+            const float4 *v4 = reinterpret_cast<const float4 *>(v + n);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 uu = __ldg(u4 + q);
+              const float4 vv = __ldg(v4 + q);
+              const float2 a0 = make_float2(__uint_as_float(acc[4 * q]),
+                                            __uint_as_float(acc[4 * q + 1]));
+              const float2 a1 = make_float2(__uint_as_float(acc[4 * q + 2]),
+                                            __uint_as_float(acc[4 * q + 3]));
+              const float2 o0 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.x, uu.y), a0),
+                                     make_float2(vv.x, vv.y));
+              const float2 o1 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.z, uu.w), a1),
+                                     make_float2(vv.z, vv.w));
+              pk[2 * q] = f2_to_bf2(o0);
+              pk[2 * q + 1] = f2_to_bf2(o1);
+            }
+          }
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + n);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);  // this lane's accumulator columns are read
     }
   }
 
   // Teardown: every MMA has finished before the tensor memory is freed.
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 2) {
     if (lane == 0) {
       volatile int never = 0;
       mbar_wait(done, 0, err, &never);
@@ -355,7 +440,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
   if (M < 1 || M > int64_t(65535) * kBM) return NORM_ERR_SHAPE;
   if (K < kBK || K > NORM_MAX_N || K % kBK != 0) return NORM_ERR_SHAPE;
-  if (Nout < 32 || Nout > (int64_t(1) << 24) || Nout % 32 != 0) return NORM_ERR_SHAPE;
+  if (Nout < 32 || Nout > (int64_t(1) << 20) || Nout % 32 != 0) return NORM_ERR_SHAPE;
   return NORM_OK;
 }
 
@@ -434,7 +519,8 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((Nout + kBN - 1) / kBN), unsigned((M + kBM - 1) / kBM));
+  const int64_t ntiles = ((M + kBM - 1) / kBM) * ((Nout + kBN - 1) / kBN);
+  cfg.gridDim = dim3(unsigned(ntiles < sms ? ntiles : sms));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
