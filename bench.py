@@ -66,14 +66,21 @@ def peak_hbm():
 # Host-only sources: they choose and launch kernels but compile to no device
 # code; the plan they chose is recorded beside the counters instead.
 HOST_ONLY_SOURCES = ("api.cu", "host.cu")
+# The normalisation-GEMM's own sources (its kernels are in gemm.cu alone),
+# and the shared headers that gemm.cu also includes.
+NORM_GEMM_SOURCES = ("gemm.cu", "tcgen05.cuh")
+NORM_GEMM_HEADERS = ("common.cuh", "ptx.cuh", "rowops.cuh")
 
 
-def source_hash():
-    """Hash of the sources that define device code."""
+def source_hash(kind="norm"):
+    """Hash of the sources that define the device code of the normalisation
+    kernels (kind "norm") or of the normalisation-GEMM kernel ("gemm")."""
     csrc = os.path.join(ROOT, "memory_bound_normalization_rmsnorm_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
-        if name in HOST_ONLY_SOURCES:
+        if kind == "norm" and (name in HOST_ONLY_SOURCES or name in NORM_GEMM_SOURCES):
+            continue
+        if kind == "gemm" and name not in NORM_GEMM_SOURCES + NORM_GEMM_HEADERS:
             continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
@@ -88,7 +95,7 @@ def _plan_key(p):
     return {k: p[k] for k in keys}
 
 
-def ncu_traffic(workload, kernel, plan=None):
+def ncu_traffic(workload, kernel, plan=None, kind="norm"):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current device code and the same launch plan (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -96,7 +103,7 @@ def ncu_traffic(workload, kernel, plan=None):
         with open(path) as f:
             data = json.load(f)
         rec = data[workload][kernel]
-        if rec.get("source_hash") != source_hash():
+        if rec.get("source_hash") != source_hash(kind):
             return None
         if plan is not None and rec.get("plan") is not None and rec["plan"] != plan:
             return None
@@ -580,6 +587,100 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def peak_bf16():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+NORM_GEMM_CASES = [(mode, 32768, k, k) for mode in (0, 1) for k in (2048, 3072, 4096, 5120, 8192)]
+
+
+def run_norm_gemm(args):
+    """One JSON line per (mode, M, K, Nout): the fused normalisation-GEMM
+    (norm_gemm_fwd, weights prepared once) against the unfused sequence
+    norm_fwd + cuBLAS bf16 GEMM (torch.matmul) on the same inputs, each timed
+    with CUDA events around back-to-back calls on the current stream.  The
+    roofline is the tensor-core one: 2 M K Nout flops per call against the
+    measured cuBLAS bf16 burst peak."""
+    import torch
+
+    import memory_bound_normalization_rmsnorm_gb300 as gb
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = peak_bf16()
+    cases = NORM_GEMM_CASES
+    if args.norm_gemm != "all":
+        k = int(args.norm_gemm)
+        cases = [c for c in cases if c[2] == k]
+
+    def timed(fn):
+        # About 0.3 s of calls (at most --steps), so that the clock samples
+        # fall inside the timed region.
+        t0 = time.perf_counter()
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / args.warmup
+        iters = max(1, min(args.steps, int(0.3 / max(per, 1e-6))))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters, iters
+
+    for mode, M, K, Nout in cases:
+        w0 = wl.Workload(f"norm_gemm_{'rms' if mode == 0 else 'layer'}_{M}x{K}x{Nout}", mode, M,
+                         K, 1e-5, "normal_offset", "one_plus_0.1n")
+        x, g, b, _ = wl.make_inputs(w0, "cuda", with_dy=False)
+        b = b if mode == 1 else None
+        w = wl.make_gemm_weight(w0, Nout, "cuda")
+        wg, u, v = gb.norm_gemm_prepare(w, g, b, mode)
+        out, rstd, mean = gb.norm_gemm_fwd(x, wg, u, v, 1e-5, mode)
+        y, r2, m2 = gb.norm_fwd(x, g, b, 1e-5, mode)
+        prod = torch.empty(M, Nout, dtype=torch.bfloat16, device="cuda")
+        wt = w.t()
+        clk = ClockSampler(0)
+        clk.start()
+        t_fused, iters = timed(lambda: gb.norm_gemm_fwd(x, wg, u, v, 1e-5, mode, out=out,
+                                                        rstd=rstd, mean=mean))
+        clocks = clk.stop()
+        t_norm, _ = timed(lambda: gb.norm_fwd(x, g, b, 1e-5, mode, y=y, rstd=r2, mean=m2))
+        t_gemm, _ = timed(lambda: torch.matmul(y, wt, out=prod))
+
+        def unfused():
+            gb.norm_fwd(x, g, b, 1e-5, mode, y=y, rstd=r2, mean=m2)
+            torch.matmul(y, wt, out=prod)
+
+        t_unfused, _ = timed(unfused)
+        if gb.norm_get_device_error() != 0:
+            raise RuntimeError(f"device error word set on {w0.name}")
+        flops = 2.0 * M * K * Nout
+        achieved = flops / (t_fused * 1e-3) / 1e12
+        line = {"workload": w0.name, "mode": w0.mode_name, "M": M, "K": K, "Nout": Nout,
+                "dtype": "bf16 in, fp32 accumulate, bf16 out", "iters": iters,
+                "fused_us": 1e3 * t_fused, "fused_tflops": achieved,
+                "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                             "unit": "TFLOP/s", "frac": achieved / peak,
+                             "peak_kind": f"cuBLAS bf16 burst, {peak_kind}",
+                             "traffic": ncu_traffic(w0.name, "norm_gemm_kernel", kind="gemm")},
+                "unfused_us": 1e3 * t_unfused, "norm_fwd_us": 1e3 * t_norm,
+                "cublas_us": 1e3 * t_gemm, "cublas_tflops": flops / (t_gemm * 1e-3) / 1e12,
+                "speedup_vs_unfused": t_unfused / t_fused,
+                "norm_time_hidden_frac": (t_unfused - t_fused) / t_norm,
+                "clocks": clocks}
+        print(json.dumps(line), flush=True)
+        del x, g, b, w, wg, u, v, out, rstd, mean, y, r2, m2, prod
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -603,10 +704,15 @@ def main():
     ap.add_argument("--fp8", choices=["", "row", "mx"], default="",
                     help="with --sweep: the forward writes E4M3 (norm_fwd_fp8) with per-row "
                          "or MX block scaling")
+    ap.add_argument("--norm-gemm", default="",
+                    help="'all' or one K: the normalisation fused into the tcgen05 GEMM "
+                         "against norm_fwd + cuBLAS, one JSON line per case")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.sweep:
+    if args.norm_gemm:
+        run_norm_gemm(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -21,7 +21,8 @@
 // L2), and the normalised rows are never written.
 //
 // A persistent grid (one CTA per SM, 12 warps) walks the 128 x 256 output
-// tiles in row-major tile order (tile j of CTA c is c + j * gridDim.x):
+// tiles (tile j of CTA c is c + j * gridDim.x, in the grouped order of
+// tile_coords):
 //   warp 0      (lane 0) issues the tiled TMA loads of the x and W' tiles
 //               into a 4-stage ring (128-byte swizzle);
 //   warp 1      (lane 0) issues the tcgen05.mma instructions, 4 per 64-wide
@@ -73,21 +74,42 @@ constexpr uint32_t kATile = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBTile = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr uint32_t kTmemCols = 2 * kBN;     // two accumulators: all 512 columns
+constexpr int kOutCols = 64;                  // output columns per TMA store box
+constexpr uint32_t kOutTile = kBM * kOutCols * 2;  // 16 KB staging buffer
 constexpr int kNumBars = 2 * kStages + 8 + 1;
-// Ring, mbarriers, TMEM address slot and abort flag, two slots of per-row
-// (rstd, mean); plus slack to align the ring to 1024 bytes (the 128-byte
-// swizzle atom is 8 rows of 128 bytes).
-constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 256 + 2 * kBM * 8;
+// Ring, output staging buffer, mbarriers, TMEM address slot and abort flag,
+// two slots of per-row (rstd, mean); plus slack to align the ring to 1024
+// bytes (the 128-byte swizzle atom is 8 rows of 128 bytes).
+constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kOutTile + 256 + 2 * kBM * 8;
 
 static_assert(kBK * 2 == 128, "one K block is one 128-byte swizzled row");
 static_assert(kBN % 32 == 0 && kBN <= 256 && kBM == 128, "tcgen05 tile shape");
 static_assert(kNumBars * 8 + 8 <= 256, "barrier region");
 
+// Tile walk: groups of kGroupM row blocks, each group taken column by
+// column (row block fastest).  The ~one tile per SM in flight at a time then
+// covers about 16 row blocks x 9 column blocks instead of a few whole row
+// blocks, so the x and W' tiles they read stay in L2 even when W' is larger
+// than L2.
+constexpr int kGroupM = 16;
+
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &m_blk,
+                                            int &n_blk) {
+  const int per_group = kGroupM * n_tiles;
+  const int group = tile / per_group;
+  const int first = group * kGroupM;
+  const int rows = min(kGroupM, m_tiles - first);
+  const int idx = tile - group * per_group;
+  m_blk = first + idx % rows;
+  n_blk = idx / rows;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     norm_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
-                     const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ u,
-                     const float *__restrict__ v, uint16_t *__restrict__ out,
+                     const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_out, const float *__restrict__ u,
+                     const float *__restrict__ v,
                      float *__restrict__ rstd, float *__restrict__ mean, int M, int K, int Nout,
                      float eps, uint32_t tx_bytes, unsigned *err) {
   extern __shared__ uint8_t smem_raw[];
@@ -95,7 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *ring = smem_raw + pad;
   uint8_t *a_tiles = ring;
   uint8_t *b_tiles = ring + kStages * kATile;
-  uint64_t *full = reinterpret_cast<uint64_t *>(ring + kStages * kStageBytes);
+  uint8_t *staging = ring + kStages * kStageBytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(staging + kOutTile);
   uint64_t *empty = full + kStages;      // [kStages]
   uint64_t *acc_full = empty + kStages;  // [2] accumulator complete
   uint64_t *acc_empty = acc_full + 2;    // [2] accumulator drained
@@ -104,13 +127,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *done = st_empty + 2;         // every MMA of the CTA finished
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  float2 *stats = reinterpret_cast<float2 *>(ring + kStages * kStageBytes + 256);  // [2][kBM]
+  float2 *stats = reinterpret_cast<float2 *>(staging + kOutTile + 256);  // [2][kBM]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int nk = K / kBK;
   const int n_tiles = (Nout + kBN - 1) / kBN;
-  const int ntiles = ((M + kBM - 1) / kBM) * n_tiles;
+  const int m_tiles = (M + kBM - 1) / kBM;
+  const int ntiles = m_tiles * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -142,8 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;  // K blocks issued by this CTA (all tiles)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles) * kBM;
-        const int n0 = (tile % n_tiles) * kBN;
+        int mb, nb;
+        tile_coords(tile, m_tiles, n_tiles, mb, nb);
+        const int m0 = mb * kBM;
+        const int n0 = nb * kBN;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
           if (g >= kStages) {
@@ -201,52 +227,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kStatWarp0) {
     // ------------------------------------------------ row statistics
-    const int t = threadIdx.x - kStatWarp0 * 32;  // row of the tile
+    // Warp w of the four takes rows 32w .. 32w + 31.  In each 64-wide K
+    // block, load i (0..7) has lane l read 16-byte chunk l % 8 of row
+    // 32w + 4i + l / 8: eight lanes read one whole 128-byte row line, so the
+    // lanes of a load never share a bank, whatever the swizzle.  Each lane
+    // keeps partial sums of its chunk for its eight rows; the eight lanes of
+    // a row combine them once per tile (and once for the LayerNorm shift).
+    // The chunk order within a row does not matter to a sum.
+    const int sw = warp - kStatWarp0;
+    const int sub = lane >> 3;  // row within each group of four
+    const int part = lane & 7;  // chunk of the row line
     int g = 0;
     for (int tile = blockIdx.x, j = 0; tile < ntiles; tile += gridDim.x, ++j) {
       const int b = j & 1;
-      float2 s1[4], s2[4];
+      float2 s1[8], s2[8];
+      float c[8];  // shift (LayerNorm): mean of the row's first 64 values
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
-      float c = 0.f;  // shift (LayerNorm): mean of the row's first 64 values
+      for (int i = 0; i < 8; ++i) {
+        s1[i] = s2[i] = make_float2(0.f, 0.f);
+        c[i] = 0.f;
+      }
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb, ++g) {
         const int s = g % kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, err, abort));
         if (!ok) break;
-        // Row t's 128 bytes; the 128-byte swizzle stores 16-byte chunk q at
-        // position q ^ (t % 8), which also spreads a quarter-warp over all
-        // 32 banks.
-        const uint8_t *row = a_tiles + s * kATile + t * 128;
-        float2 xv[32];
+        const uint8_t *base = a_tiles + s * kATile + (32 * sw + sub) * 128 + part * 16;
+        uint4 q[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 cq = *reinterpret_cast<const uint4 *>(row + ((q ^ (t & 7)) << 4));
-          float2 f[4];
-          chunk_to_f2(cq, f);
+        for (int i = 0; i < 8; ++i) q[i] = *reinterpret_cast<const uint4 *>(base + i * 4 * 128);
+        if (MODE == kLayer && kb == 0) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) xv[q * 4 + e] = f[e];
-        }
-        if (MODE == kRMS) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s2[e & 3] = fma2(xv[e], xv[e], s2[e & 3]);
-        } else {
-          if (kb == 0) {
-            float2 a[4] = {xv[0], xv[1], xv[2], xv[3]};
-#pragma unroll
-            for (int e = 4; e < 32; ++e) a[e & 3] = add2(a[e & 3], xv[e]);
-            const float2 a01 = add2(add2(a[0], a[1]), add2(a[2], a[3]));
+          for (int i = 0; i < 8; ++i) {
+            float2 f[4];
+            chunk_to_f2(q[i], f);
+            const float2 a2 = add2(add2(f[0], f[1]), add2(f[2], f[3]));
+            float a = a2.x + a2.y;
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
             // Rounded to bf16, so that x - c is exact in fp32 (two 8-bit
             // significands less than 2^16 apart in magnitude); an fp32
             // shift would round every difference the same way and bias the
             // sum.
-            c = __bfloat162float(__float2bfloat16_rn((a01.x + a01.y) * (1.f / kBK)));
+            c[i] = __bfloat162float(__float2bfloat16_rn(a * (1.f / kBK)));
           }
+        }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float2 dv = add2(xv[e], splat2(-c));
-            s1[e & 3] = add2(s1[e & 3], dv);
-            s2[e & 3] = fma2(dv, dv, s2[e & 3]);
+        for (int i = 0; i < 8; ++i) {
+          float2 f[4];
+          chunk_to_f2(q[i], f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (MODE == kRMS) {
+              s2[i] = fma2(f[e], f[e], s2[i]);
+            } else {
+              const float2 dv = add2(f[e], splat2(-c[i]));
+              s1[i] = add2(s1[i], dv);
+              s2[i] = fma2(dv, dv, s2[i]);
+            }
           }
         }
         // The stage is released only after its values have been consumed:
@@ -257,62 +296,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       const float invK = 1.f / float(K);
-      const float2 q2 = add2(add2(s2[0], s2[1]), add2(s2[2], s2[3]));
-      float mu = 0.f, var;
-      if (MODE == kRMS) {
-        var = (q2.x + q2.y) * invK;
-      } else {
-        const float2 q1 = add2(add2(s1[0], s1[1]), add2(s1[2], s1[3]));
-        const float d1 = (q1.x + q1.y) * invK;  // mean - c
-        var = fmaxf(fmaf(-d1, d1, (q2.x + q2.y) * invK), 0.f);
-        mu = c + d1;
+      float r[8], mu[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float q2 = s2[i].x + s2[i].y;
+        q2 += __shfl_xor_sync(0xffffffffu, q2, 1);
+        q2 += __shfl_xor_sync(0xffffffffu, q2, 2);
+        q2 += __shfl_xor_sync(0xffffffffu, q2, 4);
+        float var;
+        mu[i] = 0.f;
+        if (MODE == kRMS) {
+          var = q2 * invK;
+        } else {
+          float q1 = s1[i].x + s1[i].y;
+          q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+          q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+          q1 += __shfl_xor_sync(0xffffffffu, q1, 4);
+          const float d1 = q1 * invK;  // mean - c
+          var = fmaxf(fmaf(-d1, d1, q2 * invK), 0.f);
+          mu[i] = c[i] + d1;
+        }
+        r[i] = rsqrtf(var + eps);
       }
-      const float r = rsqrtf(var + eps);
       if (j >= 2 &&
           !__all_sync(0xffffffffu, mbar_wait(&st_empty[b], ((j >> 1) - 1) & 1, err, abort)))
         break;
-      stats[b * kBM + t] = make_float2(r, mu);
-      mbar_arrive(&st_full[b]);
-      const int row = (tile / n_tiles) * kBM + t;
-      if (tile % n_tiles == 0 && row < M) {
-        rstd[row] = r;
-        if (MODE == kLayer) mean[row] = mu;
+      int mb, nb;
+      tile_coords(tile, m_tiles, n_tiles, mb, nb);
+      const int m0 = mb * kBM;
+      if (part == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = 32 * sw + 4 * i + sub;
+          stats[b * kBM + t] = make_float2(r[i], mu[i]);
+          if (nb == 0 && m0 + t < M) {
+            rstd[m0 + t] = r[i];
+            if (MODE == kLayer) mean[m0 + t] = mu[i];
+          }
+        }
       }
+      mbar_arrive(&st_full[b]);
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------ epilogue
+    // Thread t drains TMEM lane t (row t of the tile) 64 columns at a time
+    // into a 128-byte-swizzled staging buffer (chunk q of row t at position
+    // q ^ (t % 8)), from which one thread writes the 128 x 64 box with a TMA
+    // store; rows beyond M and columns beyond Nout are clipped by the store.
     const int t = threadIdx.x - kEpiWarp0 * 32;  // row of the tile = TMEM lane
     const int quarter = warp - kEpiWarp0;        // == warp % 4: TMEM lanes 32q .. 32q + 31
     for (int tile = blockIdx.x, j = 0; tile < ntiles; tile += gridDim.x, ++j) {
       const int b = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[b], ph, err, abort))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&st_full[b], ph, err, abort))) break;
+      // The four epilogue warps meet at named barriers below, so they never
+      // leave the loop early: after a lost wait (error recorded, abort
+      // raised, later waits give up at once) they carry on with whatever
+      // the accumulator holds.
+      mbar_wait(&acc_full[b], ph, err, abort);
+      mbar_wait(&st_full[b], ph, err, abort);
+      __syncwarp();
       tc_fence_after();
       const float2 rm = stats[b * kBM + t];
       mbar_arrive(&st_empty[b]);
       const float r = rm.x, mu = rm.y;
-      const int row = (tile / n_tiles) * kBM + t;
-      const int n0 = (tile % n_tiles) * kBN;
+      int mb, nb;
+      tile_coords(tile, m_tiles, n_tiles, mb, nb);
+      const int m0 = mb * kBM;
+      const int n0 = nb * kBN;
       const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * kBN);
-      uint16_t *orow = out + size_t(row) * Nout;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        const int n = n0 + c * 32;
-        if (n >= Nout) break;  // the same for the whole warp
-        uint32_t acc[32];
-        tmem_ld32(t_lane + c * 32, acc);
-        tmem_wait_ld(acc);
-        if (row < M) {
-          uint32_t pk[16];
-          if (MODE == kRMS) {
+      for (int h = 0; h < kBN / kOutCols; ++h) {
+        const int n = n0 + h * kOutCols;
+        if (n >= Nout) break;  // the same for the whole CTA
+        uint32_t pk[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t acc[32];
+          tmem_ld32(t_lane + h * kOutCols + half * 32, acc);
+          tmem_wait_ld(acc);
+          if (n + half * 32 >= Nout) {  // Nout % 64 == 32: nothing to read or store here
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[half * 16 + e] = 0u;
+          } else if (MODE == kRMS) {
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              pk[e] = f2_to_bf2(mul2(splat2(r), make_float2(__uint_as_float(acc[2 * e]),
-                                                            __uint_as_float(acc[2 * e + 1]))));
+              pk[half * 16 + e] = f2_to_bf2(mul2(
+                  splat2(r), make_float2(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]))));
           } else {
-            const float4 *u4 = reinterpret_cast<const float4 *>(u + n);
-            const float4 *v4 = reinterpret_cast<const float4 *>(v + n);
+            const float4 *u4 = reinterpret_cast<const float4 *>(u + n + half * 32);
+            const float4 *v4 = reinterpret_cast<const float4 *>(v + n + half * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const float4 uu = __ldg(u4 + q);
@@ -325,19 +397,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      make_float2(vv.x, vv.y));
               const float2 o1 = fma2(splat2(r), fma2(splat2(-mu), make_float2(uu.z, uu.w), a1),
                                      make_float2(vv.z, vv.w));
-              pk[2 * q] = f2_to_bf2(o0);
-              pk[2 * q + 1] = f2_to_bf2(o1);
+              pk[half * 16 + 2 * q] = f2_to_bf2(o0);
+              pk[half * 16 + 2 * q + 1] = f2_to_bf2(o1);
             }
           }
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + n);
+        }
+        if (h == kBN / kOutCols - 1 || n + kOutCols >= Nout) {
+          tc_fence_before();
+          mbar_arrive(&acc_empty[b]);  // this lane's accumulator columns are all read
+        }
+        // The staging buffer is free once the previous store has read it.
+        if (t == 0) bulk_wait_read_all();
+        named_bar_sync(1, 128);
+        uint8_t *srow = staging + t * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4 *>(srow + ((q ^ (t & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        fence_proxy_async_smem();  // generic writes -> the store's async-proxy reads
+        named_bar_sync(1, 128);
+        if (t == 0) {
+          tma_store_2d(&tm_out, n, m0, staging);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[b]);  // this lane's accumulator columns are read
     }
+    if (t == 0) bulk_wait_all();  // every output store is complete before exit
   }
 
   // Teardown: every MMA has finished before the tensor memory is freed.
@@ -514,9 +599,11 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   const uint32_t box_x = uint32_t(M < kBM ? M : kBM);
   const uint32_t box_w = uint32_t(Nout < kBN ? Nout : kBN);
   uint32_t tx = (box_x + box_w) * kBK * 2;
-  CUtensorMap tm_x, tm_w;
+  const uint32_t box_o = uint32_t(M < kBM ? M : kBM);
+  CUtensorMap tm_x, tm_w, tm_o;
   if ((st = make_map(&tm_x, x, M, K, box_x)) != NORM_OK) return st;
   if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;
+  if ((st = make_map(&tm_o, out, M, Nout, box_o)) != NORM_OK) return st;
 
   cudaLaunchConfig_t cfg = {};
   const int64_t ntiles = ((M + kBM - 1) / kBM) * ((Nout + kBN - 1) / kBN);
@@ -525,8 +612,7 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   int Mi = int(M), Ki = int(K), Ni = int(Nout);
-  uint16_t *o = static_cast<uint16_t *>(out);
-  void *args[] = {&tm_x, &tm_w, &u, &v, &o, &rstd, &mean, &Mi, &Ki, &Ni, &eps, &tx, &err};
+  void *args[] = {&tm_x, &tm_w, &tm_o, &u, &v, &rstd, &mean, &Mi, &Ki, &Ni, &eps, &tx, &err};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
     cudaGetLastError();
     return NORM_ERR_CUDA;

@@ -2,7 +2,8 @@
 // normalisation-GEMM kernel: tensor memory (TMEM) allocation, the
 // tcgen05.mma instruction with shared-memory operand descriptors, completion
 // tracking through an mbarrier, TMEM -> register loads, and the tiled TMA
-// load (cp.async.bulk.tensor) that fills the operand tiles.
+// load and store (cp.async.bulk.tensor) that fill the operand tiles and
+// write the output tiles.
 #pragma once
 #include <cstdint>
 
@@ -26,6 +27,28 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int c0,
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Stores the box at (c0, c1) of the tensor described by `tmap` from shared
+// memory at `src` (a bulk-group operation: commit, then wait).  Elements of
+// the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int c0, int c1, const void *src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(smem_addr(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMEM
