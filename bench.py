@@ -263,6 +263,31 @@ def cpu_baseline(w, seconds=12.0):
                       f"sums, fp64, single thread, {total_t:.1f} s"}
 
 
+def gemm_cpu_baseline(w0, Nout, seconds=3.0):
+    """The fp64 oracle's norm(x) W^T on a bounded sample of rows of the same
+    workload (single thread), as TF/s of the same 2 K Nout flops per row."""
+    import oracle
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    oracle.default()
+    x, g, b, _ = wl.make_inputs(wl.like(w0, 64, w0.N), "cpu", with_dy=False)
+    wt = wl.make_gemm_weight(w0, Nout, "cpu")
+    xb, gb_, wb = wl.bf16_bits(x), wl.bf16_bits(g), wl.bf16_bits(wt)
+    bb = None if b is None or w0.mode == 0 else wl.bf16_bits(b)
+    rows, total_t, done = 1, 0.0, 0
+    while total_t < seconds and done < 64:
+        sel = list(range(done, min(64, done + rows)))
+        t0 = time.perf_counter()
+        oracle.norm_gemm_bf16(xb, gb_, bb, wb, float(w0.eps), w0.mode, rows=sel)
+        total_t += time.perf_counter() - t0
+        done += len(sel)
+        rows *= 2
+    flops = 2.0 * done * w0.N * Nout
+    return {"value": flops / total_t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} rows x K={w0.N} x Nout={Nout} ({w0.mode_name}), fp64 norm then "
+                      f"dot products, single thread, {total_t:.1f} s"}
+
+
 def run_reference(args):
     world, rank, local = dist_setup()
     from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
@@ -676,6 +701,8 @@ def run_norm_gemm(args):
                 "speedup_vs_unfused": t_unfused / t_fused,
                 "norm_time_hidden_frac": (t_unfused - t_fused) / t_norm,
                 "clocks": clocks}
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = gemm_cpu_baseline(w0, Nout)
         print(json.dumps(line), flush=True)
         del x, g, b, w, wg, u, v, out, rstd, mean, y, r2, m2, prod
         torch.cuda.empty_cache()
