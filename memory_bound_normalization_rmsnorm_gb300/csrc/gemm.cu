@@ -46,6 +46,8 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
+#include <map>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -62,29 +64,38 @@ norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err
 
 namespace {
 
-constexpr int kBM = 128;       // tile rows (TMEM lanes)
+constexpr int kBM = 128;       // rows per CTA (TMEM lanes)
 constexpr int kBN = 256;       // tile columns (fp32 TMEM columns per accumulator)
 constexpr int kBK = 64;        // K block: one 128-byte swizzle row of bf16
 constexpr int kUK = 16;        // K per tcgen05.mma of kind::f16
-constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;   // warps 4-7: TMEM lane quarters 0-3
 constexpr int kStatWarp0 = 8;  // warps 8-11
 constexpr uint32_t kATile = kBM * kBK * 2;  // 16 KB
-constexpr uint32_t kBTile = kBN * kBK * 2;  // 32 KB
-constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr uint32_t kTmemCols = 2 * kBN;     // two accumulators: all 512 columns
 constexpr int kOutCols = 64;                  // output columns per TMA store box
 constexpr uint32_t kOutTile = kBM * kOutCols * 2;  // 16 KB staging buffer
-constexpr int kNumBars = 2 * kStages + 8 + 1;
-// Ring, output staging buffer, mbarriers, TMEM address slot and abort flag,
-// two slots of per-row (rstd, mean); plus slack to align the ring to 1024
-// bytes (the 128-byte swizzle atom is 8 rows of 128 bytes).
-constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kOutTile + 256 + 2 * kBM * 8;
+
+// Per-CTA geometry.  One CTA holds all 256 W' rows of its tile (4 stages of
+// 48 KB); in a CTA pair each holds 128 of them (6 stages of 32 KB).  Shared
+// memory: ring, output staging buffer, mbarriers, TMEM address slot and
+// abort flag, two slots of per-row (rstd, mean); plus slack to align the
+// ring to 1024 bytes (the 128-byte swizzle atom is 8 rows of 128 bytes).
+template <bool PAIR>
+struct Geo {
+  static constexpr int kCtas = PAIR ? 2 : 1;
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBRows = kBN / kCtas;  // W' rows per CTA and stage
+  static constexpr uint32_t kBTile = kBRows * kBK * 2;
+  static constexpr uint32_t kStageBytes = kATile + kBTile;
+  static constexpr int kNumBars = 2 * kStages + 8 + 1;
+  static constexpr uint32_t kSmemBytes =
+      1024 + kStages * kStageBytes + kOutTile + 256 + 2 * kBM * 8;
+  static_assert(kNumBars * 8 + 8 <= 256, "barrier region");
+};
 
 static_assert(kBK * 2 == 128, "one K block is one 128-byte swizzled row");
 static_assert(kBN % 32 == 0 && kBN <= 256 && kBM == 128, "tcgen05 tile shape");
-static_assert(kNumBars * 8 + 8 <= 256, "barrier region");
 
 // Tile walk: groups of kGroupM row blocks, each group taken column by
 // column (row block fastest).  The ~one tile per SM in flight at a time then
@@ -104,7 +115,14 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
   n_blk = idx / rows;
 }
 
-template <int MODE>
+// PAIR: the grid is made of 2-CTA clusters; each pair computes 256 x 256
+// tiles with cta_group::2 MMAs issued by rank 0 (M = 256: 128 rows and 128
+// W' rows per CTA).  All four loads of a stage count on rank 0's full
+// barrier; the MMA commit frees the stage in both CTAs and also completes
+// rank 1's full barrier, after which rank 1's statistics warps read its x
+// tile (the MMA has read it, so it has landed).  Rank 1's epilogue warps
+// release the accumulator on rank 0.
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     norm_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_w,
@@ -112,6 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const float *__restrict__ v,
                      float *__restrict__ rstd, float *__restrict__ mean, int M, int K, int Nout,
                      float eps, uint32_t tx_bytes, unsigned *err) {
+  using G = Geo<PAIR>;
+  constexpr int kStages = G::kStages;
+  constexpr uint32_t kBTile = G::kBTile;
+  constexpr uint32_t kStageBytes = G::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t *ring = smem_raw + pad;
@@ -131,19 +153,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit0 = blockIdx.x / G::kCtas;  // this CTA's (pair's) first tile
+  const int nunits = gridDim.x / G::kCtas;  // tile stride
   const int nk = K / kBK;
   const int n_tiles = (Nout + kBN - 1) / kBN;
-  const int m_tiles = (M + kBM - 1) / kBM;
+  const int m_tiles = (M + kBM * G::kCtas - 1) / (kBM * G::kCtas);
   const int ntiles = m_tiles * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
+      // rank 0 (or a single CTA): its producer's arrival with the byte count
+      // of the stage; rank 1 of a pair: the MMA commit
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1 + 4);  // the MMA commit and one arrival per statistics warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      // rank 1's four epilogue warps also release rank 0's accumulator slot
+      mbar_init(&acc_empty[b], PAIR ? 128 + 4 : 128);
       mbar_init(&st_full[b], 128);
       mbar_init(&st_empty[b], 128);
     }
@@ -152,11 +180,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -165,11 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int g = 0;  // K blocks issued by this CTA (all tiles)
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      const uint32_t full_rank0 = PAIR ? mapa_shared(full, 0) : 0u;
+      for (int tile = unit0; ok && tile < ntiles; tile += nunits) {
         int mb, nb;
         tile_coords(tile, m_tiles, n_tiles, mb, nb);
-        const int m0 = mb * kBM;
-        const int n0 = nb * kBN;
+        const int m0 = (mb * G::kCtas + int(rank)) * kBM;
+        const int n0 = nb * kBN + int(rank) * G::kBRows;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
           if (g >= kStages) {
@@ -181,9 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // proxy; order those reads before the asynchronous-proxy refill.
             fence_proxy_async_smem();
           }
-          mbar_arrive_expect_tx(&full[s], tx_bytes);
-          tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
-          tma_load_2d(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s]);
+          if (PAIR && rank != 0) {  // counted on rank 0's barrier, where the MMA waits
+            tma_load_2d_pair(a_tiles + s * kATile, &tm_x, kb * kBK, m0,
+                             full_rank0 + uint32_t(s * 8));
+            tma_load_2d_pair(b_tiles + s * kBTile, &tm_w, kb * kBK, n0,
+                             full_rank0 + uint32_t(s * 8));
+          } else {
+            mbar_arrive_expect_tx(&full[s], tx_bytes);
+            tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
+            tma_load_2d(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s]);
+          }
         }
       }
       // No copy may still be landing in shared memory when the CTA exits.
@@ -196,13 +240,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * G::kCtas, kBN);
+      auto commit = [&](uint64_t *bar) {
+        if (PAIR)
+          mma_commit_pair(bar, 0x3);
+        else
+          mma_commit(bar);
+      };
       int g = 0;
       bool ok = true;
-      for (int tile = blockIdx.x, j = 0; ok && tile < ntiles; tile += gridDim.x, ++j) {
+      for (int tile = unit0, j = 0; ok && tile < ntiles; tile += nunits, ++j) {
         const int b = j & 1;
-        if (j >= 2 && !mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, err, abort)) break;
+        // rank 1's epilogue also releases this slot (a generic arrival from
+        // the other CTA: acquired at cluster scope)
+        if (j >= 2 && !(PAIR ? mbar_wait_cluster(&acc_empty[b], ((j >> 1) - 1) & 1, err, abort)
+                             : mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, err, abort)))
+          break;
         tc_fence_after();
         const uint32_t d = tmem + uint32_t(b * kBN);
         for (int kb = 0; kb < nk; ++kb, ++g) {
@@ -215,14 +269,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a0 = smem_addr(a_tiles + s * kATile);
           const uint32_t b0 = smem_addr(b_tiles + s * kBTile);
 #pragma unroll
-          for (int k = 0; k < kBK / kUK; ++k)
-            mma_bf16_ss(d, desc_sw128(a0 + k * kUK * 2), desc_sw128(b0 + k * kUK * 2), idesc,
-                        (kb | k) != 0);
-          mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+          for (int k = 0; k < kBK / kUK; ++k) {
+            const uint64_t ad = desc_sw128(a0 + k * kUK * 2), bd = desc_sw128(b0 + k * kUK * 2);
+            if (PAIR)
+              mma_bf16_ss_pair(d, ad, bd, idesc, (kb | k) != 0);
+            else
+              mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0);
+          }
+          commit(&empty[s]);  // the stage is free once these MMAs have read it
+          if (PAIR) mma_commit_pair(&full[s], 0x2);  // rank 1's x tile: readable now
         }
-        if (ok) mma_commit(&acc_full[b]);
+        if (ok) commit(&acc_full[b]);
       }
-      mma_commit(done);  // arrives when every MMA issued above has completed
+      commit(done);  // arrives when every MMA issued above has completed
     }
     __syncwarp();
   } else if (warp >= kStatWarp0) {
@@ -238,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = lane >> 3;  // row within each group of four
     const int part = lane & 7;  // chunk of the row line
     int g = 0;
-    for (int tile = blockIdx.x, j = 0; tile < ntiles; tile += gridDim.x, ++j) {
+    for (int tile = unit0, j = 0; tile < ntiles; tile += nunits, ++j) {
       const int b = j & 1;
       float2 s1[8], s2[8];
       float c[8];  // shift (LayerNorm): mean of the row's first 64 values
@@ -323,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       int mb, nb;
       tile_coords(tile, m_tiles, n_tiles, mb, nb);
-      const int m0 = mb * kBM;
+      const int m0 = (mb * G::kCtas + int(rank)) * kBM;
       if (part == 0) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -345,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // store; rows beyond M and columns beyond Nout are clipped by the store.
     const int t = threadIdx.x - kEpiWarp0 * 32;  // row of the tile = TMEM lane
     const int quarter = warp - kEpiWarp0;        // == warp % 4: TMEM lanes 32q .. 32q + 31
-    for (int tile = blockIdx.x, j = 0; tile < ntiles; tile += gridDim.x, ++j) {
+    const uint32_t acc_empty_rank0 = PAIR ? mapa_shared(acc_empty, 0) : 0u;
+    for (int tile = unit0, j = 0; tile < ntiles; tile += nunits, ++j) {
       const int b = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       // The four epilogue warps meet at named barriers below, so they never
@@ -361,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float r = rm.x, mu = rm.y;
       int mb, nb;
       tile_coords(tile, m_tiles, n_tiles, mb, nb);
-      const int m0 = mb * kBM;
+      const int m0 = (mb * G::kCtas + int(rank)) * kBM;
       const int n0 = nb * kBN;
       const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * kBN);
 #pragma unroll 1
@@ -403,8 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (h == kBN / kOutCols - 1 || n + kOutCols >= Nout) {
+          // this lane's accumulator columns are all read
           tc_fence_before();
-          mbar_arrive(&acc_empty[b]);  // this lane's accumulator columns are all read
+          if (PAIR && rank != 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acc_empty_rank0 + uint32_t(b * 8));
+          } else {
+            mbar_arrive(&acc_empty[b]);
+          }
         }
         // The staging buffer is free once the previous store has read it.
         if (t == 0) bulk_wait_read_all();
@@ -416,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         fence_proxy_async_smem();  // generic writes -> the store's async-proxy reads
         named_bar_sync(1, 128);
-        if (t == 0) {
+        if (t == 0 && m0 < M) {  // rank 1 of a pair may own no row of a short last tile
           tma_store_2d(&tm_out, n, m0, staging);
           bulk_commit();
         }
@@ -425,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t == 0) bulk_wait_all();  // every output store is complete before exit
   }
 
-  // Teardown: every MMA has finished before the tensor memory is freed.
+  // Teardown: every MMA has finished before the tensor memory is freed, and
+  // (pair) neither CTA exits while the other may still signal it.
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
@@ -435,8 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
+  if (PAIR) cluster_sync();
 }
 
 // W' = bf16(W * gamma) per column, u = row sums of W' and v = W beta (fp32,
@@ -522,6 +593,21 @@ norm_status_t make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t c
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The single-CTA kernel by default; GBNORM_GEMM_CTAS=2 selects the
+// CTA-pair kernel.  Measured on GB300 at 32768 x 4096 x 4096 the pair
+// matched the single CTA for RMSNorm (1665 vs 1673 TF/s) and was slower
+// for LayerNorm (1398 vs 1465): rank 1's statistics can only read its x
+// tile once the MMA commit says it has landed, which delays the release of
+// its stages, and halving the W' traffic per CTA bought nothing.
+bool want_pair() {
+  const char *s = std::getenv("GBNORM_GEMM_CTAS");
+  return s && std::atoi(s) == 2;
+}
+
+// Co-resident 2-CTA clusters of the pair kernel, per (device, mode)
+// (GBNORM_GEMM_PAIRS=n launches n pairs instead, for sweeps).
+std::map<std::pair<int, int>, int> g_pairs;
+
 norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
   if (M < 1 || M > int64_t(65535) * kBM) return NORM_ERR_SHAPE;
   if (K < kBK || K > NORM_MAX_N || K % kBK != 0) return NORM_ERR_SHAPE;
@@ -531,9 +617,12 @@ norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
 
 }  // namespace
 
-const void *norm_gemm_kernel_ptr(int mode) {
-  return mode == kRMS ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS>)
-                      : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer>);
+const void *norm_gemm_kernel_ptr(int mode, bool pair) {
+  if (pair)
+    return mode == kRMS ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, true>)
+                        : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, true>);
+  return mode == kRMS ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, false>)
+                      : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, false>);
 }
 
 }  // namespace gbn
@@ -580,13 +669,15 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   int dev = 0, sms = 0, optin = 0;
   unsigned *err = nullptr;
   if ((st = device_context(&dev, &sms, &optin, &err)) != NORM_OK) return st;
-  if (optin < int(kSmemBytes)) return NORM_ERR_UNSUPPORTED;
-  const void *fn = norm_gemm_kernel_ptr(mode);
+  bool pair = want_pair();
+  const uint32_t smem = pair ? Geo<true>::kSmemBytes : Geo<false>::kSmemBytes;
+  if (optin < int(smem)) return NORM_ERR_UNSUPPORTED;
+  const void *fn = norm_gemm_kernel_ptr(mode, pair);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_attr_done.count({dev, fn})) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(kSmemBytes)) != cudaSuccess) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+          cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
       }
@@ -595,22 +686,53 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   }
   // Boxes no taller than the tensor: a tile's rows beyond M (or Nout) are
   // then left as they were in shared memory; they only reach accumulator
-  // rows (columns) that are never stored.
+  // rows (columns) that are never stored.  Per K block, rank 0 (or the
+  // single CTA) expects the x and W' boxes of every CTA of the pair.
+  const int ctas = pair ? 2 : 1;
+  const int brows = kBN / ctas;
   const uint32_t box_x = uint32_t(M < kBM ? M : kBM);
-  const uint32_t box_w = uint32_t(Nout < kBN ? Nout : kBN);
-  uint32_t tx = (box_x + box_w) * kBK * 2;
-  const uint32_t box_o = uint32_t(M < kBM ? M : kBM);
+  const uint32_t box_w = uint32_t(Nout < brows ? Nout : brows);
+  uint32_t tx = uint32_t(ctas) * (box_x + box_w) * kBK * 2;
   CUtensorMap tm_x, tm_w, tm_o;
   if ((st = make_map(&tm_x, x, M, K, box_x)) != NORM_OK) return st;
   if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;
-  if ((st = make_map(&tm_o, out, M, Nout, box_o)) != NORM_OK) return st;
+  if ((st = make_map(&tm_o, out, M, Nout, box_x)) != NORM_OK) return st;
 
+  const int64_t units =
+      ((M + int64_t(kBM) * ctas - 1) / (int64_t(kBM) * ctas)) * ((Nout + kBN - 1) / kBN);
   cudaLaunchConfig_t cfg = {};
-  const int64_t ntiles = ((M + kBM - 1) / kBM) * ((Nout + kBN - 1) / kBN);
-  cfg.gridDim = dim3(unsigned(ntiles < sms ? ntiles : sms));
+  cudaLaunchAttribute attr;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (pair) {
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int pairs = 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      auto it = g_pairs.find({dev, int(mode)});
+      if (it != g_pairs.end()) pairs = it->second;
+    }
+    if (const char *ov = std::getenv("GBNORM_GEMM_PAIRS")) pairs = std::atoi(ov);
+    if (pairs == 0) {
+      cfg.gridDim = dim3(unsigned(sms - sms % 2));
+      if (cudaOccupancyMaxActiveClusters(&pairs, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+      }
+      if (pairs < 1) return NORM_ERR_UNSUPPORTED;
+      std::lock_guard<std::mutex> lk(g_mu);
+      g_pairs[{dev, int(mode)}] = pairs;
+    }
+    cfg.gridDim = dim3(unsigned(2 * (units < pairs ? units : pairs)));
+  } else {
+    cfg.gridDim = dim3(unsigned(units < sms ? units : sms));
+  }
   int Mi = int(M), Ki = int(K), Ni = int(Nout);
   void *args[] = {&tm_x, &tm_w, &tm_o, &u, &v, &rstd, &mean, &Mi, &Ki, &Ni, &eps, &tx, &err};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {

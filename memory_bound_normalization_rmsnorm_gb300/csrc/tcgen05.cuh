@@ -117,6 +117,86 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// ------------------------------------------- CTA-pair (cta_group::2) forms
+// A pair of CTAs (ranks 0 and 1 of a 2-CTA cluster) shares one MMA of
+// M = 256: each CTA holds 128 rows of A and half of the N rows of B in its
+// own shared memory at the same offsets, and receives its 128 rows of the
+// accumulator in its own tensor memory.  Allocation, release and
+// relinquishing are done by one warp in EACH CTA of the pair; the MMA is
+// issued by one thread of rank 0.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One arrival on the mbarrier at `bar`'s offset in every CTA of `mask` once
+// every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+// Tiled TMA load into this CTA's shared memory whose byte count lands on
+// an mbarrier of either CTA of the pair (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, int c0, int c1,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+// Arrival on an mbarrier of another CTA of the cluster (release, cluster
+// scope), at shared::cluster address `bar`.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait with cluster-scope acquire, for phases that other CTAs of the
+// cluster help complete.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                  volatile int *abort,
+                                                  uint32_t max_polls = kMaxPolls) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  for (uint32_t i = 0; i < max_polls; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+  }
+  *abort = 1;
+  atomicOr(err, kErrWaitTimeout);
+  return false;
+}
+
 // ------------------------------------------------------ TMEM -> registers
 // 32 consecutive fp32 columns of this thread's lane (warp w of a warpgroup
 // reaches lanes 32w .. 32w + 31).  The values are valid after tmem_wait_ld,

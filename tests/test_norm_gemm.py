@@ -56,8 +56,8 @@ def _compare(x, gamma, beta, w, outs, mode, rows=None, label=""):
     return ratio
 
 
-SMALL = [(1, 64, 32), (7, 128, 96), (128, 256, 256), (129, 512, 288), (300, 1024, 544),
-         (1000, 2048, 1024), (257, 4096, 512)]
+SMALL = [(1, 64, 32), (7, 128, 96), (128, 256, 256), (129, 512, 288), (255, 256, 128),
+         (256, 128, 512), (300, 1024, 544), (1000, 2048, 1024), (257, 4096, 512)]
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
@@ -68,6 +68,39 @@ def test_parity_small(mode, M, K, Nout):
     x, gamma, beta, w = _inputs(mode, M, K, Nout, seed=M + K)
     outs = _run(x, gamma, beta, w, mode)
     _compare(x, gamma, beta, w, outs, mode, label=f"{M}x{K}x{Nout}")
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
+@pytest.mark.parametrize("M,K,Nout", [(1, 64, 32), (129, 512, 288), (300, 1024, 544),
+                                      (1000, 2048, 1024), (200, 256, 96)])
+def test_cta_pair_kernel(mode, M, K, Nout, monkeypatch):
+    """The CTA-pair kernel (cta_group::2 MMAs over 256-row tiles, selected
+    with GBNORM_GEMM_CTAS=2; the default is the single-CTA kernel) on ragged
+    shapes, including a last 256-row tile whose second CTA owns no row."""
+    monkeypatch.setenv("GBNORM_GEMM_CTAS", "2")
+    x, gamma, beta, w = _inputs(mode, M, K, Nout, seed=M + 3 * K)
+    outs = _run(x, gamma, beta, w, mode)
+    _compare(x, gamma, beta, w, outs, mode, label=f"pair {M}x{K}x{Nout}")
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
+def test_cta_pair_full_size(mode, monkeypatch):
+    """The CTA-pair kernel at 32768 x 4096 x 4096: sampled rows against the
+    oracle (both CTAs of a pair: rows of either half of 256-row tiles) and
+    every row's rstd against float64 statistics."""
+    monkeypatch.setenv("GBNORM_GEMM_CTAS", "2")
+    M, K = 32768, 4096
+    x, gamma, beta, w = _inputs(mode, M, K, K, seed=12)
+    outs = _run(x, gamma, beta, w, mode)
+    rows = pu.sample_rows(M, n=64, seed=3)
+    _compare(x, gamma, beta, w, outs, mode, rows=rows, label="pair full size")
+    xd = x.double()
+    if mode == wl.LAYER:
+        var = ((xd - xd.mean(dim=1, keepdim=True)) ** 2).mean(dim=1)
+    else:
+        var = (xd ** 2).mean(dim=1)
+    r64 = 1.0 / torch.sqrt(var + float(np.float32(EPS)))
+    assert (outs[4].double() / r64 - 1).abs().max().item() < 1e-5
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
