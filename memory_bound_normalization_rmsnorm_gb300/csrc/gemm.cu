@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_out, const float *__restrict__ u,
                      const float *__restrict__ v,
                      float *__restrict__ rstd, float *__restrict__ mean, int M, int K, int Nout,
-                     float eps, uint32_t tx_bytes, unsigned *err) {
+                     float eps, uint32_t tx_bytes, int rgrp, unsigned *err) {
   using G = Geo<PAIR>;
   constexpr int kStages = G::kStages;
   constexpr uint32_t kBTile = G::kBTile;
@@ -159,7 +159,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = K / kBK;
   const int n_tiles = (Nout + kBN - 1) / kBN;
   const int m_tiles = (M + kBM * G::kCtas - 1) / (kBM * G::kCtas);
-  const int ntiles = m_tiles * n_tiles;
+  // A unit is rgrp consecutive column tiles of one row block (rgrp divides
+  // n_tiles); units are dealt to the CTAs (pairs) round-robin in the
+  // grouped order of tile_coords, and each takes its unit's tiles in turn,
+  // so the row statistics are computed once per unit.  tile_at gives the
+  // j-th tile of this CTA (false past the last one).
+  const int n_groups = n_tiles / rgrp;
+  const int nunits_all = m_tiles * n_groups;
+  auto tile_at = [&](int j, int &mb, int &nb) {
+    const int unit = unit0 + (j / rgrp) * nunits;
+    if (unit >= nunits_all) return false;
+    int ngb;
+    tile_coords(unit, m_tiles, n_groups, mb, ngb);
+    nb = ngb * rgrp + j % rgrp;
+    return true;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -202,9 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;  // K blocks issued by this CTA (all tiles)
       bool ok = true;
       const uint32_t full_rank0 = PAIR ? mapa_shared(full, 0) : 0u;
-      for (int tile = unit0; ok && tile < ntiles; tile += nunits) {
-        int mb, nb;
-        tile_coords(tile, m_tiles, n_tiles, mb, nb);
+      int mb, nb;
+      for (int j = 0; ok && tile_at(j, mb, nb); ++j) {
         const int m0 = (mb * G::kCtas + int(rank)) * kBM;
         const int n0 = nb * kBN + int(rank) * G::kBRows;
         for (int kb = 0; kb < nk; ++kb, ++g) {
@@ -250,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int g = 0;
       bool ok = true;
-      for (int tile = unit0, j = 0; ok && tile < ntiles; tile += nunits, ++j) {
+      int mb, nb;
+      for (int j = 0; ok && tile_at(j, mb, nb); ++j) {
         const int b = j & 1;
         // rank 1's epilogue also releases this slot (a generic arrival from
         // the other CTA: acquired at cluster scope)
@@ -297,8 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = lane >> 3;  // row within each group of four
     const int part = lane & 7;  // chunk of the row line
     int g = 0;
-    for (int tile = unit0, j = 0; tile < ntiles; tile += nunits, ++j) {
+    int mb, nb;
+    float r[8], mu[8];  // statistics of the current unit's rows
+    for (int j = 0; tile_at(j, mb, nb); ++j) {
       const int b = j & 1;
+      const bool fresh = (j % rgrp) == 0;  // first tile of a unit: take the statistics
       float2 s1[8], s2[8];
       float c[8];  // shift (LayerNorm): mean of the row's first 64 values
 #pragma unroll
@@ -311,6 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = g % kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1, err, abort));
         if (!ok) break;
+        if (!fresh) {  // statistics already known: just hand the stage back
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          continue;
+        }
         const uint8_t *base = a_tiles + s * kATile + (32 * sw + sub) * 128 + part * 16;
         uint4 q[8];
 #pragma unroll
@@ -355,9 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       const float invK = 1.f / float(K);
-      float r[8], mu[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 8 && fresh; ++i) {
         float q2 = s2[i].x + s2[i].y;
         q2 += __shfl_xor_sync(0xffffffffu, q2, 1);
         q2 += __shfl_xor_sync(0xffffffffu, q2, 2);
@@ -380,8 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j >= 2 &&
           !__all_sync(0xffffffffu, mbar_wait(&st_empty[b], ((j >> 1) - 1) & 1, err, abort)))
         break;
-      int mb, nb;
-      tile_coords(tile, m_tiles, n_tiles, mb, nb);
       const int m0 = (mb * G::kCtas + int(rank)) * kBM;
       if (part == 0) {
 #pragma unroll
@@ -405,7 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = threadIdx.x - kEpiWarp0 * 32;  // row of the tile = TMEM lane
     const int quarter = warp - kEpiWarp0;        // == warp % 4: TMEM lanes 32q .. 32q + 31
     const uint32_t acc_empty_rank0 = PAIR ? mapa_shared(acc_empty, 0) : 0u;
-    for (int tile = unit0, j = 0; tile < ntiles; tile += nunits, ++j) {
+    int mb, nb;
+    for (int j = 0; tile_at(j, mb, nb); ++j) {
       const int b = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       // The four epilogue warps meet at named barriers below, so they never
@@ -419,8 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 rm = stats[b * kBM + t];
       mbar_arrive(&st_empty[b]);
       const float r = rm.x, mu = rm.y;
-      int mb, nb;
-      tile_coords(tile, m_tiles, n_tiles, mb, nb);
       const int m0 = (mb * G::kCtas + int(rank)) * kBM;
       const int n0 = nb * kBN;
       const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * kBN);
@@ -698,10 +716,11 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;
   if ((st = make_map(&tm_o, out, M, Nout, box_x)) != NORM_OK) return st;
 
-  const int64_t units =
-      ((M + int64_t(kBM) * ctas - 1) / (int64_t(kBM) * ctas)) * ((Nout + kBN - 1) / kBN);
+  const int64_t m_blocks = (M + int64_t(kBM) * ctas - 1) / (int64_t(kBM) * ctas);
+  const int64_t n_tiles = (Nout + kBN - 1) / kBN;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr;
+  int pairs = 0;  // co-resident 2-CTA clusters (pair kernel)
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -712,7 +731,6 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    int pairs = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
       auto it = g_pairs.find({dev, int(mode)});
@@ -729,12 +747,36 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
       std::lock_guard<std::mutex> lk(g_mu);
       g_pairs[{dev, int(mode)}] = pairs;
     }
-    cfg.gridDim = dim3(unsigned(2 * (units < pairs ? units : pairs)));
-  } else {
-    cfg.gridDim = dim3(unsigned(units < sms ? units : sms));
   }
+  // Column tiles per unit (statistics computed once per unit): LayerNorm's
+  // statistics cost ~12 % of the kernel, RMSNorm's a few percent, so
+  // LayerNorm takes the largest of 4 / 2 that divides the column tiles and
+  // adds at most 5 % to the most tiles any CTA (pair) runs; RMSNorm takes 1.
+  // GBNORM_GEMM_GROUP=r forces r (for sweeps; r must divide the column tiles).
+  const int64_t slots = pair ? pairs : sms;
+  auto most = [&](int64_t r) {  // tiles of the busiest CTA (pair)
+    const int64_t u = m_blocks * (n_tiles / r);
+    return ((u + slots - 1) / slots) * r;
+  };
+  int rgrp = 1;
+  if (mode == NORM_LAYER)
+    for (int r : {4, 2})
+      if (n_tiles % r == 0 && most(r) * 100 <= most(1) * 105) {
+        rgrp = r;
+        break;
+      }
+  if (const char *ov = std::getenv("GBNORM_GEMM_GROUP")) {
+    const int r = std::atoi(ov);
+    if (r >= 1 && n_tiles % r == 0) rgrp = r;
+  }
+  const int64_t units = m_blocks * (n_tiles / rgrp);
+  if (pair)
+    cfg.gridDim = dim3(unsigned(2 * (units < pairs ? units : pairs)));
+  else
+    cfg.gridDim = dim3(unsigned(units < sms ? units : sms));
   int Mi = int(M), Ki = int(K), Ni = int(Nout);
-  void *args[] = {&tm_x, &tm_w, &tm_o, &u, &v, &rstd, &mean, &Mi, &Ki, &Ni, &eps, &tx, &err};
+  void *args[] = {&tm_x, &tm_w, &tm_o, &u,  &v,  &rstd, &mean,
+                  &Mi,   &Ki,   &Ni,   &eps, &tx, &rgrp, &err};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
     cudaGetLastError();
     return NORM_ERR_CUDA;

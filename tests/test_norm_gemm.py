@@ -104,6 +104,20 @@ def test_cta_pair_full_size(mode, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
+@pytest.mark.parametrize("group", ["2", "4"])
+@pytest.mark.parametrize("pair", ["1", "2"])
+def test_statistics_shared_by_column_tiles(mode, group, pair, monkeypatch):
+    """A CTA (pair) taking 2 or 4 consecutive column tiles of a row block
+    computes the row statistics once and reuses them (forced with
+    GBNORM_GEMM_GROUP; LayerNorm chooses it by itself at full size)."""
+    monkeypatch.setenv("GBNORM_GEMM_GROUP", group)
+    monkeypatch.setenv("GBNORM_GEMM_CTAS", pair)
+    x, gamma, beta, w = _inputs(mode, 700, 1024, 1024, seed=5, row_offset=1.0)
+    outs = _run(x, gamma, beta, w, mode)
+    _compare(x, gamma, beta, w, outs, mode, label=f"group {group} ctas {pair}")
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
 def test_large_row_offset(mode):
     """Rows offset by 3 (mean far from 0): the mean correction after the
     contraction, and the one-pass block statistics, hold up."""
