@@ -17,23 +17,26 @@
 // tiles through shared memory; four warps take each row's statistics from
 // the same tiles the tensor cores read, and the epilogue applies rstd and
 // the mean correction while it drains the fp32 accumulator from tensor
-// memory.  x is read from HBM once per output tile column (mostly hitting
-// L2), and the normalised rows are never written.
+// memory.  x reaches the SM once per output tile column (mostly from L2),
+// and the normalised rows are never written.
 //
 // A persistent grid (one CTA per SM, 12 warps) walks the 128 x 256 output
-// tiles (tile j of CTA c is c + j * gridDim.x, in the grouped order of
-// tile_coords):
+// tiles in units of 1, 2 or 4 consecutive column tiles of one row block,
+// dealt round-robin in the grouped order of tile_coords:
 //   warp 0      (lane 0) issues the tiled TMA loads of the x and W' tiles
 //               into a 4-stage ring (128-byte swizzle);
 //   warp 1      (lane 0) issues the tcgen05.mma instructions, 4 per 64-wide
 //               K block, into one of two 256-column fp32 accumulators in
 //               tensor memory, and commits each stage back to the producer;
 //   warp 2      allocates (and at the end frees) the 512 TMEM columns;
-//   warps 8-11  thread t owns row t of the current tile: its statistics,
-//               from the x tiles in the ring, handed to the epilogue
-//               through shared memory (two slots);
-//   warps 4-7   the epilogue of the previous tile, on TMEM lane t, while
-//               the tensor cores fill the other accumulator.
+//   warps 8-11  the statistics of the current unit's 128 rows, from the x
+//               tiles of its first tile, handed to the epilogue through
+//               shared memory (two slots);
+//   warps 4-7   the epilogue of the previous tile, on TMEM lane t = row t,
+//               while the tensor cores fill the other accumulator; output
+//               through a swizzled staging buffer and TMA tensor stores.
+// The PAIR variant runs 2-CTA clusters over 256-row tiles with
+// cta_group::2 MMAs (see the kernel).
 // Row statistics use shifted sums: the mean of the row's first 64 values,
 // rounded to bf16, is the shift c, and sum(x - c), sum((x - c)^2) give the
 // mean and the population variance without the cancellation of raw power
