@@ -35,8 +35,8 @@
 //   warps 4-7   the epilogue of the previous tile, on TMEM lane t = row t,
 //               while the tensor cores fill the other accumulator; output
 //               through a swizzled staging buffer and TMA tensor stores.
-// The PAIR variant runs 2-CTA clusters over 256-row tiles with
-// cta_group::2 MMAs (see the kernel).
+// Two cluster forms run 2-CTA clusters over 256-row blocks: cta_group::2
+// MMAs (PAIR), or single-CTA MMAs with the W' tile multicast (MCAST).
 // Row statistics use shifted sums: the mean of the row's first 64 values,
 // rounded to bf16, is the shift c, and sum(x - c), sum((x - c)^2) give the
 // mean and the population variance without the cancellation of raw power
@@ -50,6 +50,8 @@
 
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
+#include <tuple>
 #include <map>
 #include <mutex>
 #include <set>
@@ -84,11 +86,20 @@ constexpr uint32_t kOutTile = kBM * kOutCols * 2;  // 16 KB staging buffer
 // memory: ring, output staging buffer, mbarriers, TMEM address slot and
 // abort flag, two slots of per-row (rstd, mean); plus slack to align the
 // ring to 1024 bytes (the 128-byte swizzle atom is 8 rows of 128 bytes).
-template <bool PAIR>
+// Kernel forms: one CTA per 128 x 256 tile; a CTA pair sharing one
+// cta_group::2 MMA per 256 x 256 tile; or a 2-CTA cluster of two 128 x 256
+// tiles of the same columns whose W' tile is loaded half by each CTA and
+// multicast to both.
+constexpr int kFormSingle = 0;
+constexpr int kFormPair = 1;
+constexpr int kFormMcast = 2;
+
+template <int FORM>
 struct Geo {
-  static constexpr int kCtas = PAIR ? 2 : 1;
-  static constexpr int kStages = PAIR ? 6 : 4;
-  static constexpr int kBRows = kBN / kCtas;  // W' rows per CTA and stage
+  static constexpr int kCtas = FORM == kFormSingle ? 1 : 2;  // CTAs per cluster
+  static constexpr int kStages = FORM == kFormPair ? 6 : 4;
+  // W' rows held per CTA and stage (the pair splits the tile's 256 rows)
+  static constexpr int kBRows = FORM == kFormPair ? kBN / 2 : kBN;
   static constexpr uint32_t kBTile = kBRows * kBK * 2;
   static constexpr uint32_t kStageBytes = kATile + kBTile;
   static constexpr int kNumBars = 2 * kStages + 8 + 1;
@@ -125,7 +136,11 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // rank 1's full barrier, after which rank 1's statistics warps read its x
 // tile (the MMA has read it, so it has landed).  Rank 1's epilogue warps
 // release the accumulator on rank 0.
-template <int MODE, bool PAIR>
+// MCAST: 2-CTA clusters over 256-row blocks; each CTA computes its own
+// 128 x 256 tile with single-CTA MMAs, loads its x tile and one half of the
+// shared W' tile, multicast into both CTAs; both MMA commits free a stage
+// in both CTAs (the halves one CTA loads land in the other's stage too).
+template <int MODE, int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
     norm_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_w,
@@ -133,7 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const float *__restrict__ v,
                      float *__restrict__ rstd, float *__restrict__ mean, int M, int K, int Nout,
                      float eps, uint32_t tx_bytes, int rgrp, unsigned *err) {
-  using G = Geo<PAIR>;
+  constexpr bool PAIR = FORM == kFormPair;
+  constexpr bool MCAST = FORM == kFormMcast;
+  constexpr bool CLUSTER = FORM != kFormSingle;
+  using G = Geo<FORM>;
   constexpr int kStages = G::kStages;
   constexpr uint32_t kBTile = G::kBTile;
   constexpr uint32_t kStageBytes = G::kStageBytes;
@@ -156,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
   const int unit0 = blockIdx.x / G::kCtas;  // this CTA's (pair's) first tile
   const int nunits = gridDim.x / G::kCtas;  // tile stride
   const int nk = K / kBK;
@@ -183,7 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rank 0 (or a single CTA): its producer's arrival with the byte count
       // of the stage; rank 1 of a pair: the MMA commit
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);  // the MMA commit and one arrival per statistics warp
+      // the MMA commit (MCAST: both CTAs' commits) and one arrival per
+      // statistics warp
+      mbar_init(&empty[s], (MCAST ? 2 : 1) + 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -206,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   tc_fence_before();
-  if (PAIR)
+  if (CLUSTER)
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   else
     __syncthreads();
@@ -222,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mb, nb;
       for (int j = 0; ok && tile_at(j, mb, nb); ++j) {
         const int m0 = (mb * G::kCtas + int(rank)) * kBM;
-        const int n0 = nb * kBN + int(rank) * G::kBRows;
+        // this CTA's W' rows: all 256 (single), or its half (pair, multicast)
+        const int n0 = nb * kBN + (CLUSTER ? int(rank) * (kBN / 2) : 0);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
           if (g >= kStages) {
@@ -239,6 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                              full_rank0 + uint32_t(s * 8));
             tma_load_2d_pair(b_tiles + s * kBTile, &tm_w, kb * kBK, n0,
                              full_rank0 + uint32_t(s * 8));
+          } else if (MCAST) {  // own x tile; own half of W' into both CTAs
+            mbar_arrive_expect_tx(&full[s], tx_bytes);
+            tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
+            tma_load_2d_mcast(b_tiles + s * kBTile + rank * (kBTile / 2), &tm_w, kb * kBK, n0,
+                              &full[s], 0x3);
           } else {
             mbar_arrive_expect_tx(&full[s], tx_bytes);
             tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
@@ -256,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM * G::kCtas, kBN);
+    if (lane == 0 && (!PAIR || rank == 0)) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * (PAIR ? 2 : 1), kBN);
       auto commit = [&](uint64_t *bar) {
         if (PAIR)
           mma_commit_pair(bar, 0x3);
@@ -293,7 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0);
           }
-          commit(&empty[s]);  // the stage is free once these MMAs have read it
+          // the stage is free once these MMAs have read it (MCAST: in both
+          // CTAs, since this CTA's W' half also lands in the other's stage)
+          if (MCAST)
+            mma_commit_mcast(&empty[s], 0x3);
+          else
+            commit(&empty[s]);
           if (PAIR) mma_commit_pair(&full[s], 0x2);  // rank 1's x tile: readable now
         }
         if (ok) commit(&acc_full[b]);
@@ -528,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       tmem_dealloc(tmem, kTmemCols);
   }
-  if (PAIR) cluster_sync();
+  if (CLUSTER) cluster_sync();
 }
 
 // W' = bf16(W * gamma) per column, u = row sums of W' and v = W beta (fp32,
@@ -614,20 +645,30 @@ norm_status_t make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t c
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The single-CTA kernel by default; GBNORM_GEMM_CTAS=2 selects the
-// CTA-pair kernel.  Measured on GB300 at 32768 x 4096 x 4096 the pair
-// matched the single CTA for RMSNorm (1665 vs 1673 TF/s) and was slower
-// for LayerNorm (1398 vs 1465): rank 1's statistics can only read its x
-// tile once the MMA commit says it has landed, which delays the release of
-// its stages, and halving the W' traffic per CTA bought nothing.
-bool want_pair() {
+// Kernel form: the single-CTA kernel by default; GBNORM_GEMM_CTAS=2
+// selects the CTA pair (cta_group::2) and GBNORM_GEMM_CTAS=2m the 2-CTA
+// cluster with multicast W'.  Measured on GB300 at 32768 x 4096 x 4096
+// (RMSNorm / LayerNorm TF/s on one box): single 1696 / 1563, pair
+// 1659 / 1563, multicast 1611 / 1522.  In the pair, rank 1's statistics
+// can only read its x tile once the MMA commit says it has landed, which
+// delays the release of its stages.
+int gemm_form() {
   const char *s = std::getenv("GBNORM_GEMM_CTAS");
-  return s && std::atoi(s) == 2;
+  if (!s) return kFormSingle;
+  if (std::strcmp(s, "2") == 0) return kFormPair;
+  if (std::strcmp(s, "2m") == 0) return kFormMcast;
+  return kFormSingle;
 }
 
-// Co-resident 2-CTA clusters of the pair kernel, per (device, mode)
-// (GBNORM_GEMM_PAIRS=n launches n pairs instead, for sweeps).
-std::map<std::pair<int, int>, int> g_pairs;
+uint32_t form_smem(int form) {
+  return form == kFormPair ? Geo<kFormPair>::kSmemBytes
+                           : (form == kFormMcast ? Geo<kFormMcast>::kSmemBytes
+                                                 : Geo<kFormSingle>::kSmemBytes);
+}
+
+// Co-resident 2-CTA clusters of a cluster form, per (device, mode, form)
+// (GBNORM_GEMM_PAIRS=n launches n clusters instead, for sweeps).
+std::map<std::tuple<int, int, int>, int> g_pairs;
 
 norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
   if (M < 1 || M > int64_t(65535) * kBM) return NORM_ERR_SHAPE;
@@ -638,12 +679,19 @@ norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
 
 }  // namespace
 
-const void *norm_gemm_kernel_ptr(int mode, bool pair) {
-  if (pair)
-    return mode == kRMS ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, true>)
-                        : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, true>);
-  return mode == kRMS ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, false>)
-                      : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, false>);
+const void *norm_gemm_kernel_ptr(int mode, int form) {
+  const bool rms = mode == kRMS;
+  switch (form) {
+    case kFormPair:
+      return rms ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, kFormPair>)
+                 : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, kFormPair>);
+    case kFormMcast:
+      return rms ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, kFormMcast>)
+                 : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, kFormMcast>);
+    default:
+      return rms ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, kFormSingle>)
+                 : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, kFormSingle>);
+  }
 }
 
 }  // namespace gbn
@@ -690,10 +738,11 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   int dev = 0, sms = 0, optin = 0;
   unsigned *err = nullptr;
   if ((st = device_context(&dev, &sms, &optin, &err)) != NORM_OK) return st;
-  bool pair = want_pair();
-  const uint32_t smem = pair ? Geo<true>::kSmemBytes : Geo<false>::kSmemBytes;
+  const int form = gemm_form();
+  const bool cluster = form != kFormSingle;
+  const uint32_t smem = form_smem(form);
   if (optin < int(smem)) return NORM_ERR_UNSUPPORTED;
-  const void *fn = norm_gemm_kernel_ptr(mode, pair);
+  const void *fn = norm_gemm_kernel_ptr(mode, form);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_attr_done.count({dev, fn})) {
@@ -707,13 +756,17 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   }
   // Boxes no taller than the tensor: a tile's rows beyond M (or Nout) are
   // then left as they were in shared memory; they only reach accumulator
-  // rows (columns) that are never stored.  Per K block, rank 0 (or the
-  // single CTA) expects the x and W' boxes of every CTA of the pair.
-  const int ctas = pair ? 2 : 1;
-  const int brows = kBN / ctas;
+  // rows (columns) that are never stored.  Per K block: the single CTA
+  // expects its x box and its 256-row W' box; rank 0 of a pair the x and
+  // W' boxes of both CTAs; each CTA of the multicast form its x box and
+  // both 128-row W' halves.
+  const int ctas = cluster ? 2 : 1;
+  const int brows = cluster ? kBN / 2 : kBN;
   const uint32_t box_x = uint32_t(M < kBM ? M : kBM);
   const uint32_t box_w = uint32_t(Nout < brows ? Nout : brows);
-  uint32_t tx = uint32_t(ctas) * (box_x + box_w) * kBK * 2;
+  uint32_t tx = form == kFormPair    ? 2 * (box_x + box_w) * kBK * 2
+                : form == kFormMcast ? (box_x + 2 * box_w) * kBK * 2
+                                     : (box_x + box_w) * kBK * 2;
   CUtensorMap tm_x, tm_w, tm_o;
   if ((st = make_map(&tm_x, x, M, K, box_x)) != NORM_OK) return st;
   if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;
@@ -723,11 +776,11 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   const int64_t n_tiles = (Nout + kBN - 1) / kBN;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr;
-  int pairs = 0;  // co-resident 2-CTA clusters (pair kernel)
+  int pairs = 0;  // co-resident 2-CTA clusters (cluster forms)
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  if (pair) {
+  if (cluster) {
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
     attr.val.clusterDim.y = 1;
@@ -736,7 +789,7 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
     cfg.numAttrs = 1;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      auto it = g_pairs.find({dev, int(mode)});
+      auto it = g_pairs.find({dev, int(mode), form});
       if (it != g_pairs.end()) pairs = it->second;
     }
     if (const char *ov = std::getenv("GBNORM_GEMM_PAIRS")) pairs = std::atoi(ov);
@@ -748,7 +801,7 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
       }
       if (pairs < 1) return NORM_ERR_UNSUPPORTED;
       std::lock_guard<std::mutex> lk(g_mu);
-      g_pairs[{dev, int(mode)}] = pairs;
+      g_pairs[{dev, int(mode), form}] = pairs;
     }
   }
   // Column tiles per unit (statistics computed once per unit): LayerNorm's
@@ -756,7 +809,7 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   // LayerNorm takes the largest of 4 / 2 that divides the column tiles and
   // adds at most 5 % to the most tiles any CTA (pair) runs; RMSNorm takes 1.
   // GBNORM_GEMM_GROUP=r forces r (for sweeps; r must divide the column tiles).
-  const int64_t slots = pair ? pairs : sms;
+  const int64_t slots = cluster ? pairs : sms;
   auto most = [&](int64_t r) {  // tiles of the busiest CTA (pair)
     const int64_t u = m_blocks * (n_tiles / r);
     return ((u + slots - 1) / slots) * r;
@@ -773,7 +826,7 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
     if (r >= 1 && n_tiles % r == 0) rgrp = r;
   }
   const int64_t units = m_blocks * (n_tiles / rgrp);
-  if (pair)
+  if (cluster)
     cfg.gridDim = dim3(unsigned(2 * (units < pairs ? units : pairs)));
   else
     cfg.gridDim = dim3(unsigned(units < sms ? units : sms));
