@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
-  const int unit0 = blockIdx.x / G::kCtas;  // this CTA's (pair's) first tile
-  const int nunits = gridDim.x / G::kCtas;  // tile stride
+  const int unit0 = blockIdx.x / G::kCtas;  // this CTA's (cluster's) first unit
+  const int nunits = gridDim.x / G::kCtas;  // unit stride
   const int nk = K / kBK;
   const int n_tiles = (Nout + kBN - 1) / kBN;
   const int m_tiles = (M + kBM * G::kCtas - 1) / (kBM * G::kCtas);
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // rank 0 (or a single CTA): its producer's arrival with the byte count
-      // of the stage; rank 1 of a pair: the MMA commit
+      // its producer's arrival with the byte count of the stage (rank 1 of
+      // a pair: rank 0's MMA commit instead)
       mbar_init(&full[s], 1);
       // the MMA commit (MCAST: both CTAs' commits) and one arrival per
       // statistics warp
