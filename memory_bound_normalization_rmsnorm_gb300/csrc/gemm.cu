@@ -30,11 +30,11 @@
 //               tensor memory, and commits each stage back to the producer;
 //   warp 2      allocates (and at the end frees) the 512 TMEM columns;
 //   warps 8-11  the statistics of the current unit's 128 rows, from the x
-//               tiles of its first tile, handed to the epilogue through
-//               shared memory (two slots);
+//               tiles of its first tile, handed to the epilogue through a
+//               shared-memory slot;
 //   warps 4-7   the epilogue of the previous tile, on TMEM lane t = row t,
 //               while the tensor cores fill the other accumulator; output
-//               through a swizzled staging buffer and TMA tensor stores.
+//               through two swizzled staging buffers and TMA tensor stores.
 // Two cluster forms run 2-CTA clusters over 256-row blocks: cta_group::2
 // MMAs (PAIR), or single-CTA MMAs with the W' tile multicast (MCAST).
 // Row statistics use shifted sums: the mean of the row's first 64 values,
@@ -79,12 +79,12 @@ constexpr int kStatWarp0 = 8;  // warps 8-11
 constexpr uint32_t kATile = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 2 * kBN;     // two accumulators: all 512 columns
 constexpr int kOutCols = 64;                  // output columns per TMA store box
-constexpr uint32_t kOutTile = kBM * kOutCols * 2;  // 16 KB staging buffer
+constexpr uint32_t kOutTile = kBM * kOutCols * 2;  // 16 KB per staging buffer (two)
 
 // Per-CTA geometry.  One CTA holds all 256 W' rows of its tile (4 stages of
 // 48 KB); in a CTA pair each holds 128 of them (6 stages of 32 KB).  Shared
-// memory: ring, output staging buffer, mbarriers, TMEM address slot and
-// abort flag, two slots of per-row (rstd, mean); plus slack to align the
+// memory: ring, two output staging buffers, mbarriers, TMEM address slot
+// and abort flag, one slot of per-row (rstd, mean); plus slack to align the
 // ring to 1024 bytes (the 128-byte swizzle atom is 8 rows of 128 bytes).
 // Kernel forms: one CTA per 128 x 256 tile; a CTA pair sharing one
 // cta_group::2 MMA per 256 x 256 tile; or a 2-CTA cluster of two 128 x 256
@@ -104,7 +104,7 @@ struct Geo {
   static constexpr uint32_t kStageBytes = kATile + kBTile;
   static constexpr int kNumBars = 2 * kStages + 8 + 1;
   static constexpr uint32_t kSmemBytes =
-      1024 + kStages * kStageBytes + kOutTile + 256 + 2 * kBM * 8;
+      1024 + kStages * kStageBytes + 2 * kOutTile + 256 + kBM * 8;
   static_assert(kNumBars * 8 + 8 <= 256, "barrier region");
 };
 
@@ -160,17 +160,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *ring = smem_raw + pad;
   uint8_t *a_tiles = ring;
   uint8_t *b_tiles = ring + kStages * kATile;
-  uint8_t *staging = ring + kStages * kStageBytes;
-  uint64_t *full = reinterpret_cast<uint64_t *>(staging + kOutTile);
+  uint8_t *staging = ring + kStages * kStageBytes;  // [2][kOutTile]
+  uint64_t *full = reinterpret_cast<uint64_t *>(staging + 2 * kOutTile);
   uint64_t *empty = full + kStages;      // [kStages]
   uint64_t *acc_full = empty + kStages;  // [2] accumulator complete
   uint64_t *acc_empty = acc_full + 2;    // [2] accumulator drained
-  uint64_t *st_full = acc_empty + 2;     // [2] row statistics written
-  uint64_t *st_empty = st_full + 2;      // [2] row statistics read
-  uint64_t *done = st_empty + 2;         // every MMA of the CTA finished
+  uint64_t *st_full = acc_empty + 2;     // row statistics of a tile written
+  uint64_t *st_empty = st_full + 1;      // ... and read by the epilogue
+  uint64_t *done = st_empty + 1;         // every MMA of the CTA finished
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  float2 *stats = reinterpret_cast<float2 *>(staging + kOutTile + 256);  // [2][kBM]
+  float2 *stats = reinterpret_cast<float2 *>(staging + 2 * kOutTile + 256);  // [kBM]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -209,9 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[b], 1);
       // rank 1's four epilogue warps also release rank 0's accumulator slot
       mbar_init(&acc_empty[b], PAIR ? 128 + 4 : 128);
-      mbar_init(&st_full[b], 128);
-      mbar_init(&st_empty[b], 128);
     }
+    mbar_init(st_full, 128);
+    mbar_init(st_empty, 128);
     mbar_init(done, 1);
     *abort = 0;
     fence_mbar_init();
@@ -348,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int mb, nb;
     float r[8], mu[8];  // statistics of the current unit's rows
     for (int j = 0; tile_at(j, mb, nb); ++j) {
-      const int b = j & 1;
       const bool fresh = (j % rgrp) == 0;  // first tile of a unit: take the statistics
       float2 s1[8], s2[8];
       float c[8];  // shift (LayerNorm): mean of the row's first 64 values
@@ -432,22 +431,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         r[i] = rsqrtf(var + eps);
       }
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait(&st_empty[b], ((j >> 1) - 1) & 1, err, abort)))
+      // one slot: the epilogue has read the previous tile's statistics
+      if (j >= 1 &&
+          !__all_sync(0xffffffffu, mbar_wait(st_empty, (j - 1) & 1, err, abort)))
         break;
       const int m0 = (mb * G::kCtas + int(rank)) * kBM;
       if (part == 0) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int t = 32 * sw + 4 * i + sub;
-          stats[b * kBM + t] = make_float2(r[i], mu[i]);
+          stats[t] = make_float2(r[i], mu[i]);
           if (nb == 0 && m0 + t < M) {
             rstd[m0 + t] = r[i];
             if (MODE == kLayer) mean[m0 + t] = mu[i];
           }
         }
       }
-      mbar_arrive(&st_full[b]);
+      mbar_arrive(st_full);
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------ epilogue
@@ -459,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp - kEpiWarp0;        // == warp % 4: TMEM lanes 32q .. 32q + 31
     const uint32_t acc_empty_rank0 = PAIR ? mapa_shared(acc_empty, 0) : 0u;
     int mb, nb;
+    int slice = 0;  // 64-column slices stored so far (staging buffer slice % 2)
     for (int j = 0; tile_at(j, mb, nb); ++j) {
       const int b = j & 1;
       const uint32_t ph = (j >> 1) & 1;
@@ -467,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // raised, later waits give up at once) they carry on with whatever
       // the accumulator holds.
       mbar_wait(&acc_full[b], ph, err, abort);
-      mbar_wait(&st_full[b], ph, err, abort);
+      mbar_wait(st_full, j & 1, err, abort);
       __syncwarp();
       tc_fence_after();
-      const float2 rm = stats[b * kBM + t];
-      mbar_arrive(&st_empty[b]);
+      const float2 rm = stats[t];
+      mbar_arrive(st_empty);
       const float r = rm.x, mu = rm.y;
       const int m0 = (mb * G::kCtas + int(rank)) * kBM;
       const int n0 = nb * kBN;
@@ -524,10 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&acc_empty[b]);
           }
         }
-        // The staging buffer is free once the previous store has read it.
-        if (t == 0) bulk_wait_read_all();
+        // Two staging buffers in turn: the one about to be written is free
+        // once the store issued from it two slices ago has read it.
+        uint8_t *sbuf = staging + (slice & 1) * kOutTile;
+        ++slice;
+        if (t == 0) bulk_wait_read_but_one();
         named_bar_sync(1, 128);
-        uint8_t *srow = staging + t * 128;
+        uint8_t *srow = sbuf + t * 128;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4 *>(srow + ((q ^ (t & 7)) << 4)) =
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();  // generic writes -> the store's async-proxy reads
         named_bar_sync(1, 128);
         if (t == 0 && m0 < M) {  // rank 1 of a pair may own no row of a short last tile
-          tma_store_2d(&tm_out, n, m0, staging);
+          tma_store_2d(&tm_out, n, m0, sbuf);
           bulk_commit();
         }
       }
