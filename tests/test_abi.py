@@ -196,6 +196,7 @@ def test_norm_gemm_validation_codes():
     assert fwd(K=262144 + 64) == 2
     assert fwd(Nout=16) == 2
     assert fwd(Nout=80) == 2
+    assert fwd(Nout=(1 << 20) + 32) == 2       # Nout <= 2^20
     assert fwd(eps=float("nan")) == 9
     assert fwd(eps=-1.0) == 9
     assert fwd(x=F + 2) == 3
