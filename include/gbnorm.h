@@ -34,10 +34,15 @@
  * slow path for other shapes: they are rejected with a status code.
  *
  * Execution.  Calls are asynchronous on `stream` (NULL = the legacy default
- * stream) and thread-safe.  The return value reports argument validation
- * and launch errors.  Execution errors surface at the caller's next
- * synchronisation, or, for the library's own bounded waits, through
- * norm_get_device_error.  Results are bitwise reproducible run to run for a
+ * stream) and thread-safe.  The library caches per device and per CUDA
+ * context what it looks up once (SM count, kernel attributes, launch plans,
+ * the addresses of its device error word and scratch array, its internal
+ * copy streams); after the context is destroyed (cudaDeviceReset) the next
+ * call on that device sees a new context and sets it up again, dropping
+ * the plans of the old one (tuned plans included).  The return value
+ * reports argument validation and launch errors.  Execution errors surface
+ * at the caller's next synchronisation, or, for the library's own bounded
+ * waits, through norm_get_device_error.  Results are bitwise reproducible run to run for a
  * given shape and device: every reduction, including the dgamma/dbeta
  * column sums, is done in a fixed order without atomics.
  */
@@ -76,7 +81,11 @@ typedef enum {
     NORM_ERR_UNSUPPORTED = 6,    /* shape cannot be scheduled on this device */
     NORM_ERR_CUDA = 7,           /* a CUDA runtime call failed */
     NORM_ERR_DEVICE_TIMEOUT = 8, /* a kernel gave up a bounded wait */
-    NORM_ERR_ARG = 9             /* eps is negative or not finite */
+    NORM_ERR_ARG = 9,            /* eps is negative or not finite (or
+                                    another numeric argument out of range) */
+    NORM_ERR_MEMORY = 10         /* a pointer that a tensor copy reads or
+                                    writes is not device memory of the
+                                    current device (norm_gemm_fwd) */
 } norm_status_t;
 
 /*
@@ -332,6 +341,10 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
  *   NORM_ERR_ALIGN); outputs must not alias inputs; K % 64 == 0 with
  *   64 <= K <= NORM_MAX_N, Nout % 32 == 0 with 32 <= Nout <= 2^20, and
  *   1 <= M <= 8388480 (65535 tiles of 128 rows), else NORM_ERR_SHAPE.
+ *   norm_gemm_fwd moves x, wg and out with tiled tensor copies, whose
+ *   descriptors take addresses this GPU reaches directly: each must be
+ *   device memory of the current device (or managed memory), else
+ *   NORM_ERR_MEMORY before anything is built or launched.
  *   Asynchronous on `stream`; a lost asynchronous copy or MMA surfaces
  *   through norm_get_device_error.
  */

@@ -31,6 +31,7 @@ STATUS = {
     7: "NORM_ERR_CUDA",
     8: "NORM_ERR_DEVICE_TIMEOUT",
     9: "NORM_ERR_ARG",
+    10: "NORM_ERR_MEMORY",
 }
 
 _lock = threading.Lock()

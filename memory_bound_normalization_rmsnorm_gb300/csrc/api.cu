@@ -12,6 +12,8 @@
 // atinge desempenho SOTA em normalizacao com torch.compile" (paragraph on
 // Inductor) is where the warp-per-row regime ends here as well
 // (N <= 2048 for the forward pass, whose rows sit in registers).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -39,12 +41,48 @@ struct DeviceInfo {
   int sms = 0;
   int smem_optin = 0;
   unsigned *err = nullptr;
+  unsigned long long ctx = 0;  // context the cached addresses belong to
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 std::set<std::pair<int, const void *>> g_attr_done;
 std::map<std::tuple<int, int, int64_t, int, int>, Plan> g_plans;
+void *g_noalloc_ptr[kMaxDevices];  // scratch array address per device, guarded by g_mu
+
+// Unique identity (for the life of the process) of the calling thread's
+// current CUDA context -- the device's primary context for runtime-API
+// callers -- or 0 when there is none yet.  Every per-device cache of this
+// library (device error word and scratch addresses, kernel attributes,
+// plans) belongs to one context; cudaDeviceReset destroys it, and the next
+// call sees a new identity and sets the device up again.  `*ok` is false
+// when the driver offers no context identities (the caches are then kept
+// for the life of the process).
+unsigned long long current_context_id(bool *ok) {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    cudaGetLastError();
+  });
+  *ok = get_cur && get_id;
+  if (!*ok) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 norm_status_t device_info(DeviceInfo *out, int *dev_out) {
   int dev = 0;
@@ -53,9 +91,11 @@ norm_status_t device_info(DeviceInfo *out, int *dev_out) {
     return NORM_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return NORM_ERR_UNSUPPORTED;
+  bool ids = false;
+  const unsigned long long ctx = current_context_id(&ids);
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceInfo &d = g_dev[dev];
-  if (d.sms == 0) {
+  if (d.sms == 0 || (ids && ctx != d.ctx)) {
     int sms = 0, optin = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
@@ -63,14 +103,23 @@ norm_status_t device_info(DeviceInfo *out, int *dev_out) {
       cudaGetLastError();
       return NORM_ERR_CUDA;
     }
+    // (makes the device's primary context current if none was)
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
       cudaGetLastError();
       return NORM_ERR_CUDA;
     }
+    // Kernel attributes, plans (which were made with them) and the scratch
+    // address of an earlier context of this device are void.
+    for (auto it = g_attr_done.begin(); it != g_attr_done.end();)
+      it = it->first == dev ? g_attr_done.erase(it) : std::next(it);
+    for (auto it = g_plans.begin(); it != g_plans.end();)
+      it = std::get<0>(it->first) == dev ? g_plans.erase(it) : std::next(it);
+    g_noalloc_ptr[dev] = nullptr;
     d.err = static_cast<unsigned *>(p);
     d.smem_optin = optin;
     d.sms = sms;
+    d.ctx = ids ? current_context_id(&ids) : 0;
   }
   *out = d;
   *dev_out = dev;
@@ -115,10 +164,16 @@ Override read_override() {
   if (!s || !*s) return o;
   char buf[256];
   std::snprintf(buf, sizeof buf, "%s", s);
-  for (char *tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
+  // Fields separated by commas, walked with a local cursor (no hidden state:
+  // several host threads may plan at once).
+  for (char *tok = buf; tok && *tok;) {
+    char *comma = std::strchr(tok, ',');
+    if (comma) *comma = '\0';
+    char *cur = tok;
+    tok = comma ? comma + 1 : nullptr;
     char key[32];
     int val = 0;
-    if (std::sscanf(tok, "%31[^=]=%d", key, &val) != 2) continue;
+    if (std::sscanf(cur, "%31[^=]=%d", key, &val) != 2) continue;
     if (!std::strcmp(key, "C")) o.C = val;
     else if (!std::strcmp(key, "tpr")) o.tpr = val;
     else if (!std::strcmp(key, "rpg")) o.rpg = val;
@@ -736,9 +791,11 @@ norm_status_t reduce_rows(const float *rows, int P, int n, float *dgamma, float 
   return launch_reduce(rows, P, n, dgamma, dbeta, s);
 }
 
-// Ordinal, SM count, opt-in shared memory per block and device error word
-// of the current device (cached per device).
-norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err) {
+// Ordinal, SM count, opt-in shared memory per block, device error word and
+// context identity (0 if unknown) of the current device (cached per device
+// and context).
+norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err,
+                             unsigned long long *ctx) {
   DeviceInfo d;
   int dv = 0;
   norm_status_t st = device_info(&d, &dv);
@@ -747,6 +804,7 @@ norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err
   *sms = d.sms;
   *smem_optin = d.smem_optin;
   *err = d.err;
+  if (ctx) *ctx = d.ctx;
   return NORM_OK;
 }
 
@@ -756,14 +814,9 @@ norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err
 // Allocation-free backward: the scratch lives in a fixed device array of this
 // file.  Host code cannot use the array's name as a device address (on the
 // host it names a stand-in), so the address is looked up once per device
-// with cudaGetSymbolAddress, that device current, and cached.
+// with cudaGetSymbolAddress, that device current, and cached (until the
+// device's context is destroyed: see device_info).
 static __device__ __align__(256) unsigned char g_noalloc_workspace[NORM_NOALLOC_WORKSPACE_BYTES];
-
-namespace gbn {
-namespace {
-void *g_noalloc_ptr[kMaxDevices];  // guarded by g_mu
-}  // namespace
-}  // namespace gbn
 
 using namespace gbn;
 
@@ -1107,7 +1160,8 @@ const char *norm_strerror(norm_status_t s) {
     case NORM_ERR_UNSUPPORTED: return "shape cannot be scheduled on this device";
     case NORM_ERR_CUDA: return "CUDA runtime error";
     case NORM_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait on an asynchronous copy";
-    case NORM_ERR_ARG: return "eps must be finite and >= 0";
+    case NORM_ERR_ARG: return "eps must be finite and >= 0 (or a numeric argument is out of range)";
+    case NORM_ERR_MEMORY: return "a pointer is not device memory of the current device";
   }
   return "unknown status";
 }

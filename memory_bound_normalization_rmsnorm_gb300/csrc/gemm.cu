@@ -35,8 +35,8 @@
 //   warps 4-7   the epilogue of the previous tile, on TMEM lane t = row t,
 //               while the tensor cores fill the other accumulator; output
 //               through two swizzled staging buffers and TMA tensor stores.
-// Two cluster forms run 2-CTA clusters over 256-row blocks: cta_group::2
-// MMAs (PAIR), or single-CTA MMAs with the W' tile multicast (MCAST).
+// A cluster form (PAIR) runs 2-CTA clusters over 256-row blocks with
+// cta_group::2 MMAs.
 // Row statistics use shifted sums: the mean of the row's first 64 values,
 // rounded to bf16, is the shift c, and sum(x - c), sum((x - c)^2) give the
 // mean and the population variance without the cancellation of raw power
@@ -65,7 +65,8 @@
 namespace gbn {
 
 // Device error word and shape of the current device (api.cu).
-norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err);
+norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err,
+                             unsigned long long *ctx);
 
 namespace {
 
@@ -86,13 +87,10 @@ constexpr uint32_t kOutTile = kBM * kOutCols * 2;  // 16 KB per staging buffer (
 // memory: ring, two output staging buffers, mbarriers, TMEM address slot
 // and abort flag, one slot of per-row (rstd, mean); plus slack to align the
 // ring to 1024 bytes (the 128-byte swizzle atom is 8 rows of 128 bytes).
-// Kernel forms: one CTA per 128 x 256 tile; a CTA pair sharing one
-// cta_group::2 MMA per 256 x 256 tile; or a 2-CTA cluster of two 128 x 256
-// tiles of the same columns whose W' tile is loaded half by each CTA and
-// multicast to both.
+// Kernel forms: one CTA per 128 x 256 tile, or a CTA pair sharing one
+// cta_group::2 MMA per 256 x 256 tile.
 constexpr int kFormSingle = 0;
 constexpr int kFormPair = 1;
-constexpr int kFormMcast = 2;
 
 template <int FORM>
 struct Geo {
@@ -136,10 +134,6 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // rank 1's full barrier, after which rank 1's statistics warps read its x
 // tile (the MMA has read it, so it has landed).  Rank 1's epilogue warps
 // release the accumulator on rank 0.
-// MCAST: 2-CTA clusters over 256-row blocks; each CTA computes its own
-// 128 x 256 tile with single-CTA MMAs, loads its x tile and one half of the
-// shared W' tile, multicast into both CTAs; both MMA commits free a stage
-// in both CTAs (the halves one CTA loads land in the other's stage too).
 template <int MODE, int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
     norm_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -149,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      float *__restrict__ rstd, float *__restrict__ mean, int M, int K, int Nout,
                      float eps, uint32_t tx_bytes, int rgrp, unsigned *err) {
   constexpr bool PAIR = FORM == kFormPair;
-  constexpr bool MCAST = FORM == kFormMcast;
   constexpr bool CLUSTER = FORM != kFormSingle;
   using G = Geo<FORM>;
   constexpr int kStages = G::kStages;
@@ -201,9 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // its producer's arrival with the byte count of the stage (rank 1 of
       // a pair: rank 0's MMA commit instead)
       mbar_init(&full[s], 1);
-      // the MMA commit (MCAST: both CTAs' commits) and one arrival per
-      // statistics warp
-      mbar_init(&empty[s], (MCAST ? 2 : 1) + 4);
+      // the MMA commit and one arrival per statistics warp
+      mbar_init(&empty[s], 1 + 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -242,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mb, nb;
       for (int j = 0; ok && tile_at(j, mb, nb); ++j) {
         const int m0 = (mb * G::kCtas + int(rank)) * kBM;
-        // this CTA's W' rows: all 256 (single), or its half (pair, multicast)
+        // this CTA's W' rows: all 256 (single), or its half (pair)
         const int n0 = nb * kBN + (CLUSTER ? int(rank) * (kBN / 2) : 0);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
@@ -260,11 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                              full_rank0 + uint32_t(s * 8));
             tma_load_2d_pair(b_tiles + s * kBTile, &tm_w, kb * kBK, n0,
                              full_rank0 + uint32_t(s * 8));
-          } else if (MCAST) {  // own x tile; own half of W' into both CTAs
-            mbar_arrive_expect_tx(&full[s], tx_bytes);
-            tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
-            tma_load_2d_mcast(b_tiles + s * kBTile + rank * (kBTile / 2), &tm_w, kb * kBK, n0,
-                              &full[s], 0x3);
           } else {
             mbar_arrive_expect_tx(&full[s], tx_bytes);
             tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
@@ -319,12 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0);
           }
-          // the stage is free once these MMAs have read it (MCAST: in both
-          // CTAs, since this CTA's W' half also lands in the other's stage)
-          if (MCAST)
-            mma_commit_mcast(&empty[s], 0x3);
-          else
-            commit(&empty[s]);
+          // the stage is free once these MMAs have read it
+          commit(&empty[s]);
           if (PAIR) mma_commit_pair(&full[s], 0x2);  // rank 1's x tile: readable now
         }
         if (ok) commit(&acc_full[b]);
@@ -611,7 +594,7 @@ __global__ void __launch_bounds__(256)
 
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::set<std::pair<int, const void *>> g_attr_done;
+std::set<std::pair<unsigned long long, const void *>> g_attr_done;  // (context, kernel)
 
 norm_status_t encoder(PFN_cuTensorMapEncodeTiled_v12000 *out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -649,25 +632,34 @@ norm_status_t make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t c
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// x, W' and out are moved by tiled tensor copies, whose tensor maps take a
+// global address this GPU can reach: device memory of the current device
+// (or managed memory).  Host memory, another device's memory and addresses
+// unknown to CUDA are refused before a map is built.
+norm_status_t check_device_memory(const void *p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_MEMORY;
+  }
+  if (a.type == cudaMemoryTypeManaged) return NORM_OK;
+  return (a.type == cudaMemoryTypeDevice && a.device == dev) ? NORM_OK : NORM_ERR_MEMORY;
+}
+
 // Kernel form: the single-CTA kernel by default; GBNORM_GEMM_CTAS=2
-// selects the CTA pair (cta_group::2) and GBNORM_GEMM_CTAS=2m the 2-CTA
-// cluster with multicast W'.  Measured on GB300 at 32768 x 4096 x 4096
-// (RMSNorm / LayerNorm TF/s on one box): single 1696 / 1563, pair
-// 1659 / 1563, multicast 1611 / 1522.  In the pair, rank 1's statistics
-// can only read its x tile once the MMA commit says it has landed, which
-// delays the release of its stages.
+// selects the CTA pair (cta_group::2).  Measured on GB300 at
+// 32768 x 4096 x 4096 (RMSNorm / LayerNorm TF/s on one box): single
+// 1696 / 1563, pair 1659 / 1563.  In the pair, rank 1's statistics can only
+// read its x tile once the MMA commit says it has landed, which delays the
+// release of its stages.
 int gemm_form() {
   const char *s = std::getenv("GBNORM_GEMM_CTAS");
-  if (!s) return kFormSingle;
-  if (std::strcmp(s, "2") == 0) return kFormPair;
-  if (std::strcmp(s, "2m") == 0) return kFormMcast;
+  if (s && std::strcmp(s, "2") == 0) return kFormPair;
   return kFormSingle;
 }
 
 uint32_t form_smem(int form) {
-  return form == kFormPair ? Geo<kFormPair>::kSmemBytes
-                           : (form == kFormMcast ? Geo<kFormMcast>::kSmemBytes
-                                                 : Geo<kFormSingle>::kSmemBytes);
+  return form == kFormPair ? Geo<kFormPair>::kSmemBytes : Geo<kFormSingle>::kSmemBytes;
 }
 
 // Co-resident 2-CTA clusters of a cluster form, per (device, mode, form)
@@ -689,9 +681,6 @@ const void *norm_gemm_kernel_ptr(int mode, int form) {
     case kFormPair:
       return rms ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, kFormPair>)
                  : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, kFormPair>);
-    case kFormMcast:
-      return rms ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, kFormMcast>)
-                 : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, kFormMcast>);
     default:
       return rms ? reinterpret_cast<const void *>(&norm_gemm_kernel<kRMS, kFormSingle>)
                  : reinterpret_cast<const void *>(&norm_gemm_kernel<kLayer, kFormSingle>);
@@ -741,7 +730,11 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
 
   int dev = 0, sms = 0, optin = 0;
   unsigned *err = nullptr;
-  if ((st = device_context(&dev, &sms, &optin, &err)) != NORM_OK) return st;
+  unsigned long long ctx = 0;
+  if ((st = device_context(&dev, &sms, &optin, &err, &ctx)) != NORM_OK) return st;
+  const void *moved[] = {x, wg, out};
+  for (const void *p : moved)
+    if ((st = check_device_memory(p, dev)) != NORM_OK) return st;
   const int form = gemm_form();
   const bool cluster = form != kFormSingle;
   const uint32_t smem = form_smem(form);
@@ -749,28 +742,25 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
   const void *fn = norm_gemm_kernel_ptr(mode, form);
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_attr_done.count({dev, fn})) {
+    if (!g_attr_done.count({ctx, fn})) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
           cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
       }
-      g_attr_done.insert({dev, fn});
+      g_attr_done.insert({ctx, fn});
     }
   }
   // Boxes no taller than the tensor: a tile's rows beyond M (or Nout) are
   // then left as they were in shared memory; they only reach accumulator
   // rows (columns) that are never stored.  Per K block: the single CTA
   // expects its x box and its 256-row W' box; rank 0 of a pair the x and
-  // W' boxes of both CTAs; each CTA of the multicast form its x box and
-  // both 128-row W' halves.
+  // W' boxes of both CTAs.
   const int ctas = cluster ? 2 : 1;
   const int brows = cluster ? kBN / 2 : kBN;
   const uint32_t box_x = uint32_t(M < kBM ? M : kBM);
   const uint32_t box_w = uint32_t(Nout < brows ? Nout : brows);
-  uint32_t tx = form == kFormPair    ? 2 * (box_x + box_w) * kBK * 2
-                : form == kFormMcast ? (box_x + 2 * box_w) * kBK * 2
-                                     : (box_x + box_w) * kBK * 2;
+  uint32_t tx = form == kFormPair ? 2 * (box_x + box_w) * kBK * 2 : (box_x + box_w) * kBK * 2;
   CUtensorMap tm_x, tm_w, tm_o;
   if ((st = make_map(&tm_x, x, M, K, box_x)) != NORM_OK) return st;
   if ((st = make_map(&tm_w, wg, Nout, K, box_w)) != NORM_OK) return st;

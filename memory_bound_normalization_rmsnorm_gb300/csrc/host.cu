@@ -22,6 +22,8 @@
 namespace gbn {
 norm_status_t reduce_rows(const float *rows, int P, int n, float *dgamma, float *dbeta,
                           cudaStream_t s);
+norm_status_t device_context(int *dev, int *sms, int *smem_optin, unsigned **err,
+                             unsigned long long *ctx);
 }
 
 namespace {
@@ -35,6 +37,7 @@ size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Pipe {
   bool ready = false;
+  unsigned long long ctx = 0;  // the context its streams and events belong to
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t start, fin, end;
   cudaEvent_t in_done[kDepth], comp_done[kDepth], out_done[kDepth];
@@ -130,13 +133,17 @@ norm_status_t norm_fwd_bwd_host(const void *x, const void *dy, const void *gamma
   if (st != NORM_OK) return st;
   if (!workspace || workspace_bytes < L.total) return NORM_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return NORM_ERR_ALIGN;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
-    cudaGetLastError();
-    return NORM_ERR_CUDA;
-  }
+  int dev = 0, sms = 0, optin = 0;
+  unsigned *err = nullptr;
+  unsigned long long ctx = 0;
+  if ((st = gbn::device_context(&dev, &sms, &optin, &err, &ctx)) != NORM_OK) return st;
+  if (dev >= kMaxDev) return NORM_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_pipe_mu[dev]);
   Pipe &P = g_pipe[dev];
+  // Streams and events of a destroyed context (cudaDeviceReset) went with
+  // it: make new ones.
+  if (P.ready && P.ctx != ctx) P = Pipe();
+  P.ctx = ctx;
   if (!make_pipe(P)) {
     cudaGetLastError();
     return NORM_ERR_CUDA;

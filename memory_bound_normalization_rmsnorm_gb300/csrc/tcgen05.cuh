@@ -202,27 +202,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
   return false;
 }
 
-// ------------------------------------------- cluster multicast (cta_group::1)
-// Tiled TMA load written to the same shared-memory offset in every CTA of
-// `mask`, each counting the bytes on its mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mcast(void *dst, const void *tmap, int c0, int c1,
-                                                  uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-// One arrival on the mbarrier at `bar`'s offset in every CTA of `mask` once
-// the single-CTA tcgen05 operations this thread issued have completed.
-__device__ __forceinline__ void mma_commit_mcast(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // ------------------------------------------------------ TMEM -> registers
 // 32 consecutive fp32 columns of this thread's lane (warp w of a warpgroup
 // reaches lanes 32w .. 32w + 31).  The values are valid after tmem_wait_ld,

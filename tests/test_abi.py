@@ -27,11 +27,11 @@ def test_library_is_in_tree():
 
 def test_strerror_covers_all_codes():
     seen = set()
-    for code in range(10):
+    for code in range(11):
         s = gb.strerror(code)
         assert s and s != "unknown status"
         seen.add(s)
-    assert len(seen) == 10
+    assert len(seen) == 11
     assert gb.strerror(1234) == "unknown status"
 
 

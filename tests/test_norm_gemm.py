@@ -71,14 +71,13 @@ def test_parity_small(mode, M, K, Nout):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
-@pytest.mark.parametrize("form", ["2", "2m"])
+@pytest.mark.parametrize("form", ["2"])
 @pytest.mark.parametrize("M,K,Nout", [(1, 64, 32), (129, 512, 288), (300, 1024, 544),
                                       (1000, 2048, 1024), (200, 256, 96)])
 def test_cluster_kernels(mode, form, M, K, Nout, monkeypatch):
-    """The 2-CTA cluster kernels (GBNORM_GEMM_CTAS=2: cta_group::2 MMAs over
-    256-row tiles; =2m: single-CTA MMAs with the W' tile multicast to both
-    CTAs; the default is the single-CTA kernel) on ragged shapes, including
-    a last 256-row block whose second CTA owns no row."""
+    """The 2-CTA cluster kernel (GBNORM_GEMM_CTAS=2: cta_group::2 MMAs over
+    256-row tiles; the default is the single-CTA kernel) on ragged shapes,
+    including a last 256-row block whose second CTA owns no row."""
     monkeypatch.setenv("GBNORM_GEMM_CTAS", form)
     x, gamma, beta, w = _inputs(mode, M, K, Nout, seed=M + 3 * K)
     outs = _run(x, gamma, beta, w, mode)
@@ -86,7 +85,7 @@ def test_cluster_kernels(mode, form, M, K, Nout, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
-@pytest.mark.parametrize("form", ["2", "2m"])
+@pytest.mark.parametrize("form", ["2"])
 def test_cluster_kernels_full_size(mode, form, monkeypatch):
     """The cluster kernels at 32768 x 4096 x 4096: sampled rows against the
     oracle (rows of either CTA of the cluster) and every row's rstd against
@@ -108,7 +107,7 @@ def test_cluster_kernels_full_size(mode, form, monkeypatch):
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
 @pytest.mark.parametrize("group", ["2", "4"])
-@pytest.mark.parametrize("pair", ["1", "2", "2m"])
+@pytest.mark.parametrize("pair", ["1", "2"])
 def test_statistics_shared_by_column_tiles(mode, group, pair, monkeypatch):
     """A CTA (pair) taking 2 or 4 consecutive column tiles of a row block
     computes the row statistics once and reuses them (forced with
