@@ -117,7 +117,8 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "timestamp")
 
     def __init__(self, gpu_index):
         self.gpu_index = gpu_index
@@ -138,6 +139,7 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            self.rows = []
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
         self.proc.terminate()
@@ -153,6 +155,29 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.path)
+        self.rows = rows
+        return self.summary(rows)
+
+    @staticmethod
+    def _epoch(stamp):
+        import datetime
+
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def window(self, t0, t1):
+        """Summary of the samples taken between wall-clock times t0 and t1
+        (time.time()); None when no sample fell inside."""
+        sel = [r for r in getattr(self, "rows", [])
+               if len(r) >= 10 and (e := self._epoch(r[9])) is not None and t0 <= e <= t1]
+        return self.summary(sel) if sel else None
+
+    @staticmethod
+    def summary(rows):
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
@@ -223,27 +248,73 @@ def gpu_index(local):
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_sample(w, rows, seed=0):
-    """Oracle fwd + dx + column sums on the first `rows` rows of the workload
-    distribution; returns (seconds, bytes by the same minimal-byte formula)."""
-    import oracle
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_inputs(w, rows, seed=0):
+    """bf16 bits of `rows` rows of the workload's distribution (CPU draw)."""
     from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
 
     case = wl.like(w, rows, w.N)
     x, g, b, dy = wl.make_inputs(case, "cpu", seed=seed)
-    xb, gb_, dyb = wl.bf16_bits(x), wl.bf16_bits(g), wl.bf16_bits(dy)
     bb = None if b is None else wl.bf16_bits(b)
+    return wl.bf16_bits(x), wl.bf16_bits(g), bb, wl.bf16_bits(dy)
+
+
+def oracle_pass(w, xb, gb_, bb, dyb):
+    """The oracle's forward, dx and column sums over the given rows."""
+    import oracle
+
     eps = float(w.eps)
-    t0 = time.perf_counter()
     oracle.fwd_bf16(xb, gb_, bb, eps, w.mode)
     oracle.bwd_dx_bf16(dyb, xb, gb_, eps, w.mode)
     oracle.param_grads_bf16(dyb, xb, gb_, eps, w.mode)
+
+
+def oracle_sample(w, rows, seed=0):
+    """Oracle fwd + dx + column sums on `rows` rows of the workload
+    distribution, one thread; returns (seconds, bytes by the same minimal-byte
+    formula)."""
+    xb, gb_, bb, dyb = oracle_inputs(w, rows, seed)
+    t0 = time.perf_counter()
+    oracle_pass(w, xb, gb_, bb, dyb)
     dt = time.perf_counter() - t0
     f, bw = algo_bytes(rows, w.N, w.mode, 1)
     return dt, f + bw
 
 
-def cpu_baseline(w, seconds=12.0):
+def oracle_threads(w, rows, threads, seconds, seed=0):
+    """The oracle on every host core: `rows` rows drawn once, cut into one
+    block of consecutive rows per thread, each thread running the oracle's
+    forward, dx and column sums over its block (the C calls release the
+    interpreter lock, so the blocks run in parallel), repeated until about
+    `seconds` have passed.  Returns (seconds, bytes, passes)."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    xb, gb_, bb, dyb = oracle_inputs(w, rows, seed)
+    cuts = np.linspace(0, rows, threads + 1).astype(int)
+    blocks = [(np.ascontiguousarray(xb[a:b]), np.ascontiguousarray(dyb[a:b]))
+              for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+    f, bw = algo_bytes(rows, w.N, w.mode, 1)
+    total, passes = 0.0, 0
+    with cf.ThreadPoolExecutor(len(blocks)) as ex:
+        while total < seconds or passes == 0:
+            t0 = time.perf_counter()
+            list(ex.map(lambda blk: oracle_pass(w, blk[0], gb_, bb, blk[1]), blocks))
+            total += time.perf_counter() - t0
+            passes += 1
+    return total, passes * (f + bw), passes
+
+
+def cpu_baseline(w, seconds=12.0, threaded_seconds=8.0):
+    """The fp64 oracle as it stands, timed on this host: on every core
+    (threads over row blocks; the line's value) and on one thread."""
     import oracle
 
     oracle.default()
@@ -258,9 +329,19 @@ def cpu_baseline(w, seconds=12.0):
         total_t += dt
         total_b += nb
         done += r
-    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} of {w.M} rows x N={w.N} ({w.mode_name}), fwd + dx + column "
-                      f"sums, fp64, single thread, {total_t:.1f} s"}
+    single = {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1,
+              "sample": f"{done} of {w.M} rows x N={w.N} ({w.mode_name}), fwd + dx + column "
+                        f"sums, fp64, single thread, {total_t:.1f} s"}
+    n = host_cores()
+    # rows for the threaded sample: the whole workload, or what ~2 s of the
+    # all-core pass covers if that is less (and at least one row per thread)
+    per_row = total_t / max(done, 1)
+    trows = int(min(w.M, max(n, 2.0 * n / max(per_row, 1e-9))))
+    tt, tb, passes = oracle_threads(w, trows, n, threaded_seconds, seed=7)
+    return {"value": tb / tt / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{trows} of {w.M} rows x N={w.N} ({w.mode_name}) x {passes} passes, "
+                      f"fwd + dx + column sums, fp64, {n} threads over row blocks, {tt:.1f} s",
+            "single_thread": single}
 
 
 def gemm_cpu_baseline(w0, Nout, seconds=3.0):
@@ -289,6 +370,9 @@ def gemm_cpu_baseline(w0, Nout, seconds=3.0):
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on every host core
+    (threads over row blocks); each step one pass over a bounded sample of
+    the workload's rows, sized so the whole run takes about two minutes."""
     world, rank, local = dist_setup()
     from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
 
@@ -299,16 +383,16 @@ def run_reference(args):
     import oracle
 
     oracle.default()
-    # size one step so that warmup + steps take about two minutes in all
+    n = host_cores()
     dt, _ = oracle_sample(w, 8)
-    per_row = dt / 8
+    per_row = dt / 8 / n  # all cores
     budget = 120.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(w.M, budget / max(per_row, 1e-9))))
+    rows = int(max(n, min(w.M, budget / max(per_row, 1e-9))))
     for i in range(args.warmup):
-        oracle_sample(w, rows, seed=1000 + i)
+        oracle_threads(w, rows, n, 0.0, seed=1000 + i)
     tt, tb = 0.0, 0
     for i in range(args.steps):
-        dt, nb = oracle_sample(w, rows, seed=i)
+        dt, nb, _ = oracle_threads(w, rows, n, 0.0, seed=i)
         tt += dt
         tb += nb
     value = tb / tt / 1e9
@@ -318,9 +402,9 @@ def run_reference(args):
         "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N, "eps": w.eps},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle",
                          "sample": f"{rows} of {w.M} rows per step, fwd + dx + column sums, "
-                                   f"fp64, single thread"},
+                                   f"fp64, {n} threads over row blocks"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -395,6 +479,101 @@ class DirectStep:
             raise RuntimeError(f"norm_bwd status {st}")
 
 
+def timed_loop(fn, iters, stream):
+    """Milliseconds per call of `iters` back-to-back calls of fn, CUDA events
+    on `stream` around the whole loop (nothing between the calls)."""
+    import torch
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def auto_iters(fn, stream, seconds, lo=10, hi=2000):
+    """Calls of fn that take about `seconds` (after three warm-up calls)."""
+    for _ in range(3):
+        fn()
+    ms = timed_loop(fn, 5, stream)
+    return int(max(lo, min(hi, seconds * 1e3 / max(ms, 1e-4))))
+
+
+def plan_str(p):
+    """Compact text of a norm_plan dict."""
+    if p is None:
+        return None
+    s = (f"C{p['cluster']} tpr{p['threads_per_row']} K{p['chunks_per_thread']} "
+         f"G{p['groups']} rpg{p['rows_per_group']} S{p['stages']} grid{p['grid']}")
+    if p.get("long_rows"):
+        s += " long"
+    if p.get("param_smem_bytes"):
+        s += " gsm"
+    if p.get("split_segments"):
+        s += f" split{p['split_segments']}"
+    return s
+
+
+def measure_workload(gb, w, peak, seconds=0.15, warmup=3, steps=0, fused=False, fp8=None,
+                     fwd_only=False, sampler=None):
+    """Forward, backward and whole-step (forward then backward) throughput of
+    one workload: CUDA events around back-to-back calls of each on the
+    current stream, inputs resident in HBM (larger than L2 except for the
+    1 MB case).  `steps` > 0 fixes the call count, else about `seconds` of
+    calls per measurement."""
+    import torch
+
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    if fused:
+        x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
+    else:
+        (x, g, b, dy), r, dh = wl.make_inputs(w, "cuda"), None, None
+    stream = torch.cuda.current_stream()
+    step = DirectStep(gb, w, x, g, b, dy, stream, r=r, dh=dh, fp8=fp8, fwd_only=fwd_only)
+    pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused, fp8=fp8 is not None)
+    pb = None if fwd_only else gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
+
+    def both():
+        step.fwd()
+        step.bwd()
+
+    passes = [("fwd", step.fwd)] if fwd_only else [("fwd", step.fwd), ("bwd", step.bwd),
+                                                    ("step", both)]
+    res = {}
+    t0 = time.time()
+    for name, fn in passes:
+        for _ in range(warmup):
+            fn()
+        n = steps if steps > 0 else auto_iters(fn, stream, seconds)
+        res[name] = timed_loop(fn, n, stream)
+        res[name + "_iters"] = n
+    t1 = time.time()
+    if gb.norm_get_device_error() != 0:
+        raise RuntimeError(f"device error word set on {w.name}")
+    fb, bb = algo_bytes(w.M, w.N, w.mode, 0 if pb is None else pb["partials"],
+                        residual=fused, fp8=fp8)
+    out = {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
+           "fwd_us": 1e3 * res["fwd"], "fwd_GBs": fb / res["fwd"] / 1e6,
+           "fwd_frac": fb / res["fwd"] / 1e6 / peak, "plan_fwd": plan_str(pf)}
+    if pb is not None:
+        out.update({"bwd_us": 1e3 * res["bwd"], "bwd_GBs": bb / res["bwd"] / 1e6,
+                    "bwd_frac": bb / res["bwd"] / 1e6 / peak,
+                    "step_us": 1e3 * res["step"], "step_GBs": (fb + bb) / res["step"] / 1e6,
+                    "step_frac": (fb + bb) / res["step"] / 1e6 / peak,
+                    "plan_bwd": plan_str(pb), "partials": pb["partials"]})
+    out["iters"] = {k[:-6]: v for k, v in res.items() if k.endswith("_iters")}
+    if sampler is not None:
+        out["window"] = (t0, t1)
+    del step, x, g, b, dy, r, dh
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -414,9 +593,11 @@ def run_ours(args):
     plan_b = gb.norm_plan(w.M, w.N, w.mode, True)
     P = plan_b["partials"]
     fwd_b, bwd_b = algo_bytes(w.M, w.N, w.mode, P)
+    peak, peak_kind = peak_hbm()
 
     sampler = ClockSampler(gpu_index(local))
     sampler.start()
+    busy0 = time.time()
     for _ in range(args.warmup):
         step.fwd()
         step.bwd()
@@ -424,49 +605,82 @@ def run_ours(args):
     if gb.norm_get_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    # Per-kernel durations (for the roofline) come from CUDA events around the
-    # forward and the backward call of the first `nev` timed steps.  An event
-    # recorded between two kernels makes the second wait for the first to
-    # finish (no programmatic overlap of its launch with the first's tail),
-    # which on every step would slow the step by ~5 %; the remaining steps
-    # run back to back, as a training loop runs them.
-    nev = min(args.steps, 50)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nev)]
+    # The timed region: K steps back to back, CUDA events only at its two
+    # ends, so each kernel's launch overlaps the previous one's tail as it
+    # does in a training loop.
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
-    for i in range(args.steps):
-        if i < nev:
-            ev[i][0].record(stream)
-            step.fwd()
-            ev[i][1].record(stream)
-            step.bwd()
-            ev[i][2].record(stream)
-        else:
-            step.fwd()
-            step.bwd()
+    for _ in range(args.steps):
+        step.fwd()
+        step.bwd()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = sampler.stop()
     if gb.norm_get_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
-
     total_ms = t0.elapsed_time(t1)
     total_ms_max = max_over_ranks(total_ms, world, dev)
-    fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
-    bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
     step_bytes = fwd_b + bwd_b
     value = aggregate_throughput(step_bytes, args.steps, total_ms_max, world)
+
+    # Per-pass durations for the roofline, AFTER the timed region: the
+    # forward and the backward call each timed over back-to-back calls of
+    # that pass alone (an event between two kernels would hold the second
+    # one's launch until the first ends).
+    nk = max(20, min(200, args.steps))
+    fwd_ms = timed_loop(step.fwd, nk, stream)
+    bwd_ms = timed_loop(step.bwd, nk, stream)
+
+    # Cold figure: a 512 MB buffer written before every step evicts the
+    # inputs and outputs from L2 (129 MB); events around each step alone.
+    cold = None
+    if not args.no_cold:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        times = []
+        for i in range(max(5, min(20, args.steps))):
+            flush.fill_(i & 0xff)
+            a_ = torch.cuda.Event(enable_timing=True)
+            b_ = torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            step.fwd()
+            step.bwd()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            times.append(a_.elapsed_time(b_))
+        del flush
+        cms = statistics.median(times)
+        cold = {"ms_per_step": cms, "GB/s": step_bytes / cms / 1e6,
+                "frac": step_bytes / cms / 1e6 / peak, "reps": len(times),
+                "how": "512 MB buffer written before each step; events around that step"}
+    busy1 = time.time()
+    if gb.norm_get_device_error() != 0:
+        raise RuntimeError("device error word set after the per-kernel passes")
 
     # end to end through the public Python API from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(gb, w, x, g, b, dy, dev, args.e2e_steps, fwd_b + bwd_b, world)
+        e2e = run_e2e(gb, w, x, g, b, dy, dev, args.e2e_steps, step_bytes, world, local,
+                      fwd_ms + bwd_ms)
+    del step, x, g, b, dy
+    torch.cuda.empty_cache()
 
-    peak, peak_kind = peak_hbm()
+    # Every benchmark workload, one after the other, same process (rank 0 of
+    # a single-GPU run only).
+    sweep = None
+    if world == 1 and not args.no_sweep:
+        sweep = []
+        for name in wl.WORKLOADS:
+            sweep.append(measure_workload(gb, wl.WORKLOADS[name], peak, sampler=sampler))
+    clocks_all = sampler.stop()
+    clocks = sampler.window(busy0, busy1) or clocks_all
+    if sweep is not None:
+        for e in sweep:
+            c = sampler.window(*e.pop("window"))
+            e["sm_mhz"] = None if c is None else c["sm_mhz"]
+
     bwd_gbs = bwd_b / (bwd_ms * 1e-3) / 1e9
     fwd_gbs = fwd_b / (fwd_ms * 1e-3) / 1e9
     traffic = ncu_traffic(w.name, "norm_bwd_kernel", plan=_plan_key(plan_b))
@@ -475,7 +689,8 @@ def run_ours(args):
                 "kernel": "norm_bwd (fused row kernel + fixed-order partial reduce)",
                 "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "bytes_per_launch": bwd_b, "launch_ms": bwd_ms}
+                "bytes_per_launch": bwd_b, "launch_ms": bwd_ms,
+                "timing": f"{nk} back-to-back norm_bwd calls after the timed region"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -489,20 +704,24 @@ def run_ours(args):
                        "eps": w.eps, "io_dtype": "bf16", "accumulate": "fp32",
                        "parallelism": f"replicas x{world} (rows independent)",
                        "l2": "inputs larger than L2 (each of x, dy, y, dx is "
-                             f"{w.M * w.N * 2 / 1e6:.0f} MB > 129 MB); no flush",
-                       "kernel_timing": f"CUDA events around the forward and the backward "
-                                        f"call of the first {nev} of the {args.steps} timed steps",
+                             f"{w.M * w.N * 2 / 1e6:.0f} MB > 129 MB); no flush in the timed "
+                             "region (a flushed figure is under 'cold')",
+                       "kernel_timing": f"timed region: {args.steps} back-to-back steps, "
+                                        "events at its ends only; per-pass times from "
+                                        f"{nk} back-to-back calls of each pass afterwards",
                        "plan_fwd": plan_f, "plan_bwd": plan_b},
             "pct_of_nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
             "pct_of_measured_peak": 100.0 * value / world / peak,
             "fwd": {"ms": fwd_ms, "GB/s": fwd_gbs, "frac": fwd_gbs / peak, "bytes": fwd_b},
             "bwd": {"ms": bwd_ms, "GB/s": bwd_gbs, "frac": bwd_gbs / peak, "bytes": bwd_b,
                     "partials": P},
+            "cold": cold,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 3 * args.steps,
             "clocks": clocks,
+            "sweep": sweep,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -511,53 +730,188 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(gb, w, x, g, b, dy, dev, steps, step_bytes, world):
+def gpu_host_locality(local):
+    """The GPU's PCI address and, from sysfs, the NUMA node and CPU list the
+    kernel reports as local to it (None where unknown)."""
+    import torch
+
+    info = {"pci": None, "numa_node": None, "local_cpus": None}
+    try:
+        pr = torch.cuda.get_device_properties(local)
+        info["pci"] = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+    except Exception:
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                                  "-i", str(gpu_index(local))], capture_output=True, text=True,
+                                 timeout=20).stdout.strip()
+            dom, rest = out.split(":", 1)
+            info["pci"] = f"{int(dom, 16):04x}:{rest.lower()}"
+        except Exception:
+            return info
+    base = f"/sys/bus/pci/devices/{info['pci']}"
+    try:
+        with open(base + "/numa_node") as f:
+            info["numa_node"] = int(f.read().strip())
+    except Exception:
+        pass
+    try:
+        with open(base + "/local_cpulist") as f:
+            cpus = set()
+            for part in f.read().strip().split(","):
+                if "-" in part:
+                    a, b = part.split("-")
+                    cpus.update(range(int(a), int(b) + 1))
+                elif part:
+                    cpus.add(int(part))
+            info["local_cpus"] = sorted(cpus)
+    except Exception:
+        pass
+    return info
+
+
+def pages_by_node(addr):
+    """NUMA node -> pages of the mapping that holds host address `addr`,
+    from /proc/self/numa_maps (None where the kernel does not say)."""
+    try:
+        start = None
+        with open("/proc/self/maps") as f:
+            for line in f:
+                a, b = line.split()[0].split("-")
+                if int(a, 16) <= addr < int(b, 16):
+                    start = a
+                    break
+        if start is None:
+            return None
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                if line.split()[0].lstrip("0") == start.lstrip("0"):
+                    nodes = {}
+                    for tok in line.split()[1:]:
+                        if tok.startswith("N") and "=" in tok:
+                            k, v = tok[1:].split("=")
+                            if k.isdigit():
+                                nodes[int(k)] = int(v)
+                    return nodes or None
+    except Exception:
+        return None
+    return None
+
+
+def run_e2e(gb, w, x, g, b, dy, dev, steps, step_bytes, world, local, kernel_ms):
     """Per step one norm_fwd_bwd_host call: host (pinned) x, dy, gamma(,
     beta) in; y, rstd(, mean), dx, dgamma(, dbeta) back in pinned host
     buffers.  The library streams the rows through device buffers in chunks
     with both copy directions and the kernels overlapped; timed with CUDA
-    events on the calling stream around the whole step."""
+    events on the calling stream around the whole step.  The pinned buffers
+    are allocated from a thread bound to the CPUs local to the GPU (when
+    sysfs names them), so their pages sit on the GPU's side of the host;
+    the line records where they landed and what single copies of the same
+    buffers achieve, and from those the copy-bound time of a step."""
     import torch
 
-    hx = x.cpu().pin_memory()
-    hdy = dy.cpu().pin_memory()
-    hg = g.cpu().pin_memory()
-    hb = None if b is None else b.cpu().pin_memory()
-    M, N = w.M, w.N
-    ln = w.mode == 1
-    out = (torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True),
-           torch.empty(M, dtype=torch.float32, pin_memory=True),
-           torch.empty(M, dtype=torch.float32, pin_memory=True) if ln else None,
-           torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True),
-           torch.empty(N, dtype=torch.float32, pin_memory=True),
-           torch.empty(N, dtype=torch.float32, pin_memory=True) if ln else None)
-    ws = torch.empty(gb.norm_host_workspace_bytes(M, N, w.mode), dtype=torch.uint8, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hg, hb) if t is not None)
-    d2h = sum(t.numel() * t.element_size() for t in out if t is not None)
+    loc = gpu_host_locality(local)
+    old_aff = None
+    bound = False
+    if loc["local_cpus"]:
+        try:
+            old_aff = os.sched_getaffinity(0)
+            use = set(loc["local_cpus"]) & set(old_aff)
+            if use:
+                os.sched_setaffinity(0, use)
+                bound = True
+        except Exception:
+            old_aff = None
+    try:
+        hx = x.cpu().pin_memory()
+        hdy = dy.cpu().pin_memory()
+        hg = g.cpu().pin_memory()
+        hb = None if b is None else b.cpu().pin_memory()
+        M, N = w.M, w.N
+        ln = w.mode == 1
+        out = (torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True),
+               torch.empty(M, dtype=torch.float32, pin_memory=True),
+               torch.empty(M, dtype=torch.float32, pin_memory=True) if ln else None,
+               torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True),
+               torch.empty(N, dtype=torch.float32, pin_memory=True),
+               torch.empty(N, dtype=torch.float32, pin_memory=True) if ln else None)
+        ws = torch.empty(gb.norm_host_workspace_bytes(M, N, w.mode), dtype=torch.uint8,
+                         device=dev)
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hdy, hg, hb) if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in out if t is not None)
 
-    def one():
-        gb.norm_fwd_bwd_host(hx, hdy, hg, hb, w.eps, w.mode, out=out, workspace=ws)
+        def one():
+            gb.norm_fwd_bwd_host(hx, hdy, hg, hb, w.eps, w.mode, out=out, workspace=ws)
 
-    one()
-    torch.cuda.synchronize()
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
-    s0.record()
-    for _ in range(steps):
         one()
-    s1.record()
-    torch.cuda.synchronize()
-    ms = s0.elapsed_time(s1)
-    ms = max_over_ranks(ms, world, dev)
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(steps):
+            one()
+        s1.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1)
+        ms = max_over_ranks(ms, world, dev)
+
+        # single copies of the same pinned buffers: x in, dx out, and both at
+        # once on two streams
+        dbuf = torch.empty_like(x)
+        dbuf2 = torch.empty_like(x)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def copy_ms(fns, reps=3):
+            best = None
+            for _ in range(reps):
+                torch.cuda.synchronize()
+                t = time.perf_counter()
+                for st, fn in fns:
+                    with torch.cuda.stream(st):
+                        fn()
+                torch.cuda.synchronize()
+                dt = (time.perf_counter() - t) * 1e3
+                best = dt if best is None else min(best, dt)
+            return best
+
+        nbytes = hx.numel() * 2
+        h2d_ms = copy_ms([(s_in, lambda: dbuf.copy_(hx, non_blocking=True))])
+        d2h_ms = copy_ms([(s_out, lambda: out[3].copy_(dbuf2, non_blocking=True))])
+        both_ms = copy_ms([(s_in, lambda: dbuf.copy_(hx, non_blocking=True)),
+                           (s_out, lambda: out[3].copy_(dbuf2, non_blocking=True))])
+        h2d_gbs = nbytes / h2d_ms / 1e6
+        d2h_gbs = nbytes / d2h_ms / 1e6
+        both_gbs = 2 * nbytes / both_ms / 1e6
+        # copy-bound model of one step: the bytes of both directions at the
+        # rate the two directions reach together, or the kernels, whichever
+        # is longer
+        model_ms = max((h2d + d2h) / both_gbs / 1e6, kernel_ms)
+        placement = {"x_pages_by_node": pages_by_node(hx.data_ptr()),
+                     "dx_pages_by_node": pages_by_node(out[3].data_ptr())}
+        del dbuf, dbuf2
+    finally:
+        if old_aff is not None:
+            try:
+                os.sched_setaffinity(0, old_aff)
+            except Exception:
+                pass
     return {"value": world * step_bytes * steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
-            "steps": steps, "api": "norm_fwd_bwd_host (host tensors, chunked, copies overlapped)"}
+            "steps": steps, "api": "norm_fwd_bwd_host (host tensors, chunked, copies overlapped)",
+            "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "both_directions_gbs": both_gbs,
+            "copy_bound_model_ms": model_ms,
+            "vs_model": model_ms / (ms / steps),
+            "gpu_locality": {"pci": loc["pci"], "numa_node": loc["numa_node"],
+                             "local_cpus": (f"{loc['local_cpus'][0]}-{loc['local_cpus'][-1]}"
+                                            if loc["local_cpus"] else None),
+                             "pinned_from_local_cpus": bound},
+            "placement": placement}
 
 
 def run_sweep(args):
-    """One JSON line per workload: fwd and bwd timed separately (CUDA events
-    around `iters` back-to-back calls of each pass on the default stream,
-    inputs resident in HBM and larger than L2 except for the small case)."""
+    """One JSON line per workload: fwd and bwd timed separately and the whole
+    step (CUDA events around back-to-back calls of each on the default
+    stream, inputs resident in HBM and larger than L2 except for the small
+    case)."""
     import torch
 
     import memory_bound_normalization_rmsnorm_gb300 as gb
@@ -566,49 +920,61 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     peak, peak_kind = peak_hbm()
     names = list(wl.WORKLOADS) if args.sweep == "all" else args.sweep.split(",")
+    fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
     for name in names:
         w = wl.WORKLOADS[name]
-        fused = args.fused_residual
-        fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
-        if fused:
-            x, r, g, b, dy, dh = wl.make_residual_inputs(w, "cuda")
-        else:
-            (x, g, b, dy), r, dh = wl.make_inputs(w, "cuda"), None, None
-        step = DirectStep(gb, w, x, g, b, dy, torch.cuda.current_stream(), r=r, dh=dh, fp8=fp8,
-                          fwd_only=args.fwd_only)
-        pf = gb.norm_plan(w.M, w.N, w.mode, False, residual=fused, fp8=fp8 is not None)
-        pb = None if args.fwd_only else gb.norm_plan(w.M, w.N, w.mode, True, residual=fused)
-        res = {}
-        passes = (("fwd", step.fwd),) if args.fwd_only else (("fwd", step.fwd), ("bwd", step.bwd))
-        for name_, fn in passes:
-            for _ in range(args.warmup):
-                fn()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(args.steps):
-                fn()
-            e1.record()
-            torch.cuda.synchronize()
-            res[name_] = e0.elapsed_time(e1) / args.steps
-        if gb.norm_get_device_error() != 0:
-            raise RuntimeError(f"device error word set on {name}")
-        fb, bb = algo_bytes(w.M, w.N, w.mode, 0 if pb is None else pb["partials"],
-                            residual=fused, fp8=fp8)
-        keep = ("cluster", "threads_per_row", "chunks_per_thread", "groups", "rows_per_group",
-                "stages", "grid", "exact")
-        line = {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
-                "fused_residual": fused, "fp8": args.fp8 or None, "fwd_us": 1e3 * res["fwd"],
-                "fwd_GBs": fb / res["fwd"] / 1e6, "peak": peak, "peak_kind": peak_kind,
-                "iters": args.steps, "plan_fwd": {k: pf[k] for k in keep}}
-        if pb is not None:
-            line.update({"bwd_us": 1e3 * res["bwd"], "bwd_GBs": bb / res["bwd"] / 1e6,
-                         "step_GBs": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6,
-                         "step_frac": (fb + bb) / (res["fwd"] + res["bwd"]) / 1e6 / peak,
-                         "plan_bwd": {k: pb[k] for k in keep}})
+        line = measure_workload(gb, w, peak, warmup=args.warmup, steps=args.steps,
+                                fused=args.fused_residual, fp8=fp8, fwd_only=args.fwd_only)
+        line.update({"fused_residual": args.fused_residual, "fp8": args.fp8 or None,
+                     "peak": peak, "peak_kind": peak_kind})
         print(json.dumps(line), flush=True)
-        del step, x, g, b, dy, r, dh
+
+
+def run_ablate(args):
+    """The two knobs the first page tunes for the backward pass, on one
+    workload's backward call: the number of partial rows (split size; the
+    persistent grid is capped with GBNORM_PLAN grid=P) and the number of
+    pipeline stages (GBNORM_PLAN S=n).  One JSON line per setting."""
+    import torch
+
+    import memory_bound_normalization_rmsnorm_gb300 as gb
+    from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    peak, _ = peak_hbm()
+    w = wl.WORKLOADS[args.workload]
+    x, g, b, dy = wl.make_inputs(w, "cuda")
+    stream = torch.cuda.current_stream()
+    settings = [("grid", f"grid={p}") for p in (19, 38, 76, 114, 152)]
+    settings += [("grid", f"grid={p},G=1") for p in (152, 304)]
+    settings += [("stages", f"S={k}") for k in range(2, 9)]
+    for kind, ov in settings:
+        os.environ["GBNORM_PLAN"] = ov
+        try:
+            step = DirectStep(gb, w, x, g, b, dy, stream)
+            pb = gb.norm_plan(w.M, w.N, w.mode, True)
+        except Exception as e:  # a setting the planner cannot schedule
+            print(json.dumps({"workload": w.name, "knob": kind, "override": ov,
+                              "error": str(e)}), flush=True)
+            continue
+        finally:
+            os.environ.pop("GBNORM_PLAN", None)
+        os.environ["GBNORM_PLAN"] = ov
+        try:
+            for _ in range(args.warmup):
+                step.bwd()
+            ms = timed_loop(step.bwd, max(20, args.steps), stream)
+        finally:
+            os.environ.pop("GBNORM_PLAN", None)
+        if gb.norm_get_device_error() != 0:
+            raise RuntimeError(f"device error word set under {ov}")
+        _, bb = algo_bytes(w.M, w.N, w.mode, pb["partials"])
+        print(json.dumps({"workload": w.name, "knob": kind, "override": ov,
+                          "partials": pb["partials"], "rows_per_partial": w.M / pb["partials"],
+                          "stages": pb["stages"], "plan": plan_str(pb), "bwd_us": 1e3 * ms,
+                          "bwd_GBs": bb / ms / 1e6, "bwd_frac": bb / ms / 1e6 / peak}),
+              flush=True)
+        del step
         torch.cuda.empty_cache()
 
 
@@ -719,6 +1085,13 @@ def main():
                     help="override M (smaller cases for profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cold", action="store_true",
+                    help="skip the L2-flushed per-step figure")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload sweep in the benchmark line")
+    ap.add_argument("--ablate", action="store_true",
+                    help="partial-row count and stage count of the backward pass on "
+                         "--workload, one JSON line per setting (not the benchmark line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", default="",
@@ -737,7 +1110,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.norm_gemm:
+    if args.ablate:
+        run_ablate(args)
+    elif args.norm_gemm:
         run_norm_gemm(args)
     elif args.sweep:
         run_sweep(args)

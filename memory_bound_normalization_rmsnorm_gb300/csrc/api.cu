@@ -152,9 +152,10 @@ int pow2ceil(int v) {
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Optional plan override for tuning sweeps: GBNORM_PLAN="C=2,tpr=256,rpg=1,S=4"
-// (any subset).  Fields left out keep the heuristic's choice.
+// (any subset).  Fields left out keep the heuristic's choice.  grid=P caps
+// the persistent grid at P CTAs (clusters), i.e. the backward's partial rows.
 struct Override {
-  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, gsm = -1;
+  int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, gsm = -1, grid = 0;
   bool any = false;
 };
 
@@ -183,6 +184,7 @@ Override read_override() {
     else if (!std::strcmp(key, "long")) o.lng = val;
     else if (!std::strcmp(key, "K")) o.K = val;
     else if (!std::strcmp(key, "gsm")) o.gsm = val;
+    else if (!std::strcmp(key, "grid")) o.grid = val;
     o.any = true;
   }
   return o;
@@ -547,6 +549,7 @@ norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, cons
     }
     resident = nclusters;
   }
+  if (ov.grid > 0) resident = std::min<int64_t>(resident, ov.grid);
   if (resident < 1) return NORM_ERR_UNSUPPORTED;
   set_grid(p, resident);
   return NORM_OK;

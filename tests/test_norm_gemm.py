@@ -210,3 +210,31 @@ def test_every_row_statistics_repeatable(mode):
             for a, b in zip(first, [t for t in outs[3:] if t is not None]):
                 assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                                    b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+def test_memory_not_on_this_device_is_refused():
+    """x, W' and out are moved by tiled tensor copies, which need memory this
+    GPU reaches directly: pinned host memory and pageable host memory given
+    as any of them are refused with NORM_ERR_MEMORY before anything is
+    launched, and the device path still works afterwards."""
+    import ctypes
+
+    M, K, Nout = 256, 512, 288
+    x, gamma, beta, w = _inputs(wl.LAYER, M, K, Nout, seed=21)
+    wg, u, v, out, rstd, mean = _run(x, gamma, beta, w, wl.LAYER)
+    pinned = torch.empty(M * max(K, Nout), dtype=torch.bfloat16).pin_memory()
+    pageable = torch.empty(M * max(K, Nout), dtype=torch.bfloat16)
+    L = gb.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call(xp, wp, op):
+        return L.norm_gemm_fwd(xp, wp, u.data_ptr(), v.data_ptr(), M, K, Nout, EPS, wl.LAYER,
+                               op, rstd.data_ptr(), mean.data_ptr(), stream)
+
+    for host in (pinned, pageable):
+        assert call(host.data_ptr(), wg.data_ptr(), out.data_ptr()) == 10
+        assert call(x.data_ptr(), host.data_ptr(), out.data_ptr()) == 10
+        assert call(x.data_ptr(), wg.data_ptr(), host.data_ptr()) == 10
+    assert call(x.data_ptr(), wg.data_ptr(), out.data_ptr()) == 0
+    torch.cuda.synchronize()
+    assert gb.norm_get_device_error() == 0
