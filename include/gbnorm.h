@@ -61,8 +61,17 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *norm_stream_t;
 
-/* Largest supported row length (columns). */
-#define NORM_MAX_N 262144
+/* Largest row length (columns) of norm_fwd / norm_bwd and of their
+ * allocation-free and host-tensor variants.  Rows of up to
+ * NORM_MAX_N_ONEPASS columns are normalised in one pass over HBM (rows held
+ * in registers, or in the shared memory of one CTA or of a thread-block
+ * cluster of up to 16 CTAs); wider rows take a two-pass path that cuts each
+ * row into 4096-column segments and reads x (and dy) twice. */
+#define NORM_MAX_N (1 << 24)
+#define NORM_MAX_N_ONEPASS 262144
+/* Largest row length of the fused variants (norm_add_fwd / norm_add_bwd,
+ * norm_fwd_fp8) and of the normalisation-GEMM's K: the one-pass limit. */
+#define NORM_MAX_N_FUSED NORM_MAX_N_ONEPASS
 
 typedef enum {
     NORM_RMS = 0,   /* RMSNorm: no mean, no beta */
@@ -72,7 +81,9 @@ typedef enum {
 typedef enum {
     NORM_OK = 0,
     NORM_ERR_NULL = 1,           /* a required pointer is NULL */
-    NORM_ERR_SHAPE = 2,          /* M < 1, N < 8, N > NORM_MAX_N or N % 8 != 0 */
+    NORM_ERR_SHAPE = 2,          /* M < 1, N < 8, N % 8 != 0, or N above the
+                                    entry point's limit (NORM_MAX_N, or
+                                    NORM_MAX_N_FUSED for the fused variants) */
     NORM_ERR_ALIGN = 3,          /* a pointer is not 16-byte aligned */
     NORM_ERR_MODE = 4,           /* unknown mode, or a pointer given that the
                                     mode forbids (beta/mean/dbeta for RMS) or
@@ -98,6 +109,9 @@ typedef enum {
  *   y      bf16 [M, N] output
  *   rstd   fp32 [M] output, 1/sqrt(var + eps) or 1/sqrt(meansq + eps)
  *   mean   fp32 [M] output; required for LAYER, must be NULL for RMS
+ * One kernel for N <= NORM_MAX_N_ONEPASS.  Wider rows take three: the
+ * per-segment statistics (written into y as scratch, 8 bytes per segment of
+ * each row), their fixed-order fold into rstd / mean, and the output.
  */
 norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta,
                        int64_t M, int64_t N, float eps, norm_mode_t mode,
@@ -128,7 +142,10 @@ norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode,
  *           must not share a workspace.
  * Two kernels run on `stream`: the fused row pass (dx plus per-CTA partial
  * column sums written to the workspace) and a fixed-order reduction of the
- * partials into dgamma/dbeta.
+ * partials into dgamma/dbeta.  Rows wider than NORM_MAX_N_ONEPASS take four:
+ * the per-(row, segment) dot products (into the workspace), their per-row
+ * fold, dx with the dgamma/dbeta sums of each CTA's segments (into the
+ * workspace), and a fixed-order reduction of those.
  */
 norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma,
                        const float *rstd, const float *mean, int64_t M,
@@ -148,7 +165,7 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma,
  * and the backward pass adds the gradient dh that reaches h through the
  * residual path:  dx = (norm_bwd's dx at h) + dh  (sum in fp32, one rounding);
  * dx is the gradient of both x and r.  dgamma / dbeta as norm_bwd.
- * Shapes: as norm_fwd / norm_bwd (N up to NORM_MAX_N); rows wider than one
+ * Shapes: as norm_fwd / norm_bwd but N up to NORM_MAX_N_FUSED; rows wider than one
  * CTA's registers use the long-row kernels (and thread-block clusters) with
  * the residual tensor in the same shared-memory stage.  Other requirements
  * as norm_fwd / norm_bwd.
@@ -199,7 +216,7 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h,
  *   q     uint8 [M, N] E4M3 codes of y;
  *   scale float [M] (NORM_FP8_ROW) or uint8 [M, N / 32] (NORM_FP8_MX).
  * All pointers are device pointers owned by the caller, 16-byte aligned.
- * Every N up to NORM_MAX_N is supported (rows wider than one CTA use the
+ * Every N up to NORM_MAX_N_FUSED is supported (rows wider than one CTA use the
  * long-row kernels and clusters; with per-row scaling the CTAs of a cluster
  * exchange their slice maxima); an unknown scaling returns NORM_ERR_ARG.
  * One kernel on `stream`.  The backward pass of an FP8-output forward is
@@ -260,8 +277,9 @@ norm_status_t norm_fwd_bwd_host(const void *x, const void *dy, const void *gamma
 /*
  * norm_plan -- the launch plan the library uses for one pass (backward = 0
  * for norm_fwd, 1 for norm_bwd, 2 for norm_add_fwd, 3 for norm_add_bwd, 4
- * for norm_fwd_fp8 without and 6 with a residual) of
- * an [M, N] problem: how rows are split
+ * for norm_fwd_fp8 without and 6 with a residual; for rows on the two-pass
+ * path, 0 / 1 report its statistics / dx pass and 8 / 9 its output /
+ * dot-product pass) of an [M, N] problem: how rows are split
  * across threads, CTAs and clusters, and how many tiles are kept in flight.
  * With sm_count <= 0 it describes the CURRENT device (occupancy queried
  * through the CUDA runtime) and equals what norm_fwd / norm_bwd launch.
@@ -296,6 +314,13 @@ typedef struct {
                                   row instead of being held in registers
                                   (fp32 for bf16 output, bf16 for E4M3
                                   output); 0 if none */
+    int32_t split_segments;    /* two-pass path (rows wider than
+                                  NORM_MAX_N_ONEPASS): segments of
+                                  cols_per_cta columns per row; the fields
+                                  above describe its statistics (forward) or
+                                  dx (backward) pass, whose rows_per_tile
+                                  rows of one segment make a unit, `tiles`
+                                  counting the row tiles; 0 otherwise */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
@@ -339,7 +364,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,
  *   (else NORM_ERR_MODE); eps finite and >= 0 (else NORM_ERR_ARG).
  * Both: device pointers owned by the caller, 16-byte aligned (else
  *   NORM_ERR_ALIGN); outputs must not alias inputs; K % 64 == 0 with
- *   64 <= K <= NORM_MAX_N, Nout % 32 == 0 with 32 <= Nout <= 2^20, and
+ *   64 <= K <= NORM_MAX_N_FUSED, Nout % 32 == 0 with 32 <= Nout <= 2^20, and
  *   1 <= M <= 8388480 (65535 tiles of 128 rows), else NORM_ERR_SHAPE.
  *   norm_gemm_fwd moves x, wg and out with tiled tensor copies, whose
  *   descriptors take addresses this GPU reaches directly: each must be

@@ -50,7 +50,8 @@ class Plan(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("partials", ctypes.c_int32), ("exact", ctypes.c_int32),
-                ("long_rows", ctypes.c_int32), ("param_smem_bytes", ctypes.c_int32)]
+                ("long_rows", ctypes.c_int32), ("param_smem_bytes", ctypes.c_int32),
+                ("split_segments", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -549,12 +550,15 @@ def norm_gemm_fwd(x, wg, u=None, v=None, eps=1e-5, mode=RMS, *, out=None, rstd=N
 
 
 def norm_plan(M, N, mode=RMS, backward=False, sm_count=0, smem_optin=0, residual=False,
-              fp8=False) -> dict:
+              fp8=False, other_pass=False) -> dict:
     """Launch plan of one pass (see norm_plan in gbnorm.h).  sm_count > 0
     plans for a hypothetical device without touching CUDA; residual=True
-    plans the fused residual add variant, fp8=True the E4M3-output forward."""
+    plans the fused residual add variant, fp8=True the E4M3-output forward;
+    other_pass=True gives, for rows on the two-pass path, the forward's
+    output pass or the backward's dot-product pass."""
     out = Plan()
-    which = (1 if backward else 0) | (2 if residual else 0) | (4 if fp8 else 0)
+    which = ((1 if backward else 0) | (2 if residual else 0) | (4 if fp8 else 0)
+             | (8 if other_pass else 0))
     st = lib().norm_plan(int(M), int(N), int(mode), which, int(sm_count), int(smem_optin),
                          ctypes.byref(out))
     if st != 0:

@@ -1,9 +1,9 @@
 """Builds the CUDA library libgbnorm.so in-tree for sm_103a.
 
-Ten translation units (bf16- and E4M3-output forward, forward with staged
+Eleven translation units (bf16- and E4M3-output forward, forward with staged
 parameters, backward, long-row kernels plain, with the fused residual add and
-with E4M3 output, host ABI, host-tensor pipeline, and the normalisation fused
-into a tcgen05 GEMM) are
+with E4M3 output, the two-pass path for the longest rows, host ABI,
+host-tensor pipeline, and the normalisation fused into a tcgen05 GEMM) are
 compiled in parallel with nvcc and linked into one shared object with the
 CUDA runtime linked statically, so the library needs no CUDA library path at
 load time.  `python -m memory_bound_normalization_rmsnorm_gb300.builder -v`
@@ -25,7 +25,7 @@ OUT_DIR = os.path.join(PKG, "lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgbnorm.so")
 SOURCES = ["fwd.cu", "fwd_fp8.cu", "fwd_gsm.cu", "bwd.cu", "long.cu", "long_resid.cu",
-           "long_fp8.cu", "api.cu", "host.cu", "gemm.cu"]
+           "long_fp8.cu", "split.cu", "api.cu", "host.cu", "gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -156,6 +156,8 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // the persistent grid at P CTAs (clusters), i.e. the backward's partial rows.
 struct Override {
   int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, gsm = -1, grid = 0;
+  int split = -1;  // 1: the two-pass path at any N; 0: never
+  int W = 0;       // two-pass path: segment width (a multiple of 1024)
   bool any = false;
 };
 
@@ -185,6 +187,8 @@ Override read_override() {
     else if (!std::strcmp(key, "K")) o.K = val;
     else if (!std::strcmp(key, "gsm")) o.gsm = val;
     else if (!std::strcmp(key, "grid")) o.grid = val;
+    else if (!std::strcmp(key, "split")) o.split = val;
+    else if (!std::strcmp(key, "W")) o.W = val;
     o.any = true;
   }
   return o;
@@ -466,6 +470,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 }
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
+  if (p.split) return split_kernel_ptr(mode, p.phase, p.K);
   if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.resid);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm);
@@ -555,6 +560,141 @@ norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, cons
   return NORM_OK;
 }
 
+// ------------------------------------------------------ two-pass path
+// Rows wider than NORM_MAX_N_ONEPASS (or any row, with the plan override
+// split=1) are cut into segments of kSplitW columns (override W=); see
+// split.cu.  Each pass has its own plan: rows of RT = G * rpg per unit, S
+// units in flight, and a persistent grid of at most one CTA per unit.
+constexpr int kSplitW = 4096;
+
+bool use_split(int N, const Override &ov) {
+  return ov.split == 1 || (ov.split != 0 && N > NORM_MAX_N_ONEPASS);
+}
+
+// Shape part of a pass's plan (no CUDA call): threads per row and chunks per
+// thread from the segment width (K = 4, or 2 for the dx pass, which holds
+// the column sums), G row groups of up to 512 threads, and the stages that
+// fit in `smem_optin` bytes.
+norm_status_t split_shape(int mode, int phase, int64_t M, int N, int smem_optin,
+                          const Override &ov, Plan *out) {
+  const int W = ov.W ? ov.W : kSplitW;
+  const int K = phase == kSplitBwdDx ? 2 : 4;
+  const int nc = W / 8;
+  if (W < 1024 || W % 1024 || nc % K) return NORM_ERR_UNSUPPORTED;
+  const int tpr = nc / K;
+  if (tpr < 32 || tpr > kMaxThreads || tpr % 32) return NORM_ERR_UNSUPPORTED;
+  if (!split_kernel_ptr(mode, phase, K)) return NORM_ERR_UNSUPPORTED;
+  Plan p;
+  p.split = true;
+  p.phase = phase;
+  p.C = 1;
+  p.NS = W;
+  p.nsc = nc;
+  p.tpr = tpr;
+  p.K = K;
+  p.exact = false;
+  p.nseg = (N + W - 1) / W;
+  int G = kMaxThreads / tpr;
+  if (tpr > 32) G = std::min(G, 8);
+  if (ov.G) G = ov.G;
+  if (G < 1 || G * tpr > kMaxThreads || (tpr > 32 && G > 15)) return NORM_ERR_UNSUPPORTED;
+  const int nt = phase >= kSplitBwdDots ? 2 : 1;
+  int rpg = ov.rpg ? ov.rpg : std::max(1, 4 / G);
+  const int budget = smem_optin - 1024;
+  int S = 0;
+  for (;;) {
+    const SmemLayout L1 = split_smem_layout(G * rpg, W, 1, G, tpr, nt);
+    const SmemLayout L2 = split_smem_layout(G * rpg, W, 2, G, tpr, nt);
+    const int per_stage = static_cast<int>(L2.total - L1.total);
+    const int fixed = static_cast<int>(L1.total) - per_stage;
+    S = (budget - fixed) / per_stage;
+    if (S >= 2 || rpg == 1 || ov.rpg) break;
+    rpg = (rpg + 1) / 2;
+  }
+  S = std::min(S, 8);
+  if (ov.S) S = ov.S;
+  if (S < 2) return NORM_ERR_UNSUPPORTED;
+  const SmemLayout L = split_smem_layout(G * rpg, W, S, G, tpr, nt);
+  if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;
+  p.G = G;
+  p.rpg = rpg;
+  p.RT = G * rpg;
+  p.S = S;
+  p.threads = G * tpr;
+  if (p.threads % 32) return NORM_ERR_UNSUPPORTED;
+  p.smem = L.total;
+  p.ntiles = (M + p.RT - 1) / p.RT;
+  *out = p;
+  return NORM_OK;
+}
+
+// Units of a pass: row tiles x segments.  The grid never exceeds them, so
+// every CTA owns at least one unit (the dgamma/dbeta reduction relies on it).
+void split_grid(Plan &p, int64_t resident) {
+  const int64_t units = p.ntiles * p.nseg;
+  p.grid = static_cast<int>(std::min<int64_t>(resident, units));
+  p.P = p.grid;
+}
+
+// Plans of the two passes of the two-pass path: [0] statistics (forward) or
+// dot products (backward), [1] output or dx.  Cached like the one-pass plans.
+norm_status_t make_split_plans(const DeviceInfo &d, int dev, int mode, bool bwd, int64_t M,
+                               int N, Plan out[2]) {
+  const Override ov = read_override();
+  for (int i = 0; i < 2; ++i) {
+    const int phase = (bwd ? kSplitBwdDots : kSplitFwdStats) + i;
+    const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, 8 + phase);
+    if (!ov.any) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      auto it = g_plans.find(key);
+      if (it != g_plans.end()) {
+        out[i] = it->second;
+        continue;
+      }
+    }
+    Plan p;
+    norm_status_t st = split_shape(mode, phase, M, N, d.smem_optin, ov, &p);
+    if (st != NORM_OK) return st;
+    const void *fn = split_kernel_ptr(mode, phase, p.K);
+    if ((st = prepare_function(dev, fn, d.smem_optin)) != NORM_OK) return st;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, p.threads, p.smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return NORM_ERR_CUDA;
+    }
+    if (ov.ctas) per_sm = std::min(per_sm, ov.ctas);
+    int64_t resident = static_cast<int64_t>(per_sm) * d.sms;
+    if (ov.grid > 0) resident = std::min<int64_t>(resident, ov.grid);
+    if (resident < 1) return NORM_ERR_UNSUPPORTED;
+    split_grid(p, resident);
+    if (!ov.any) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      g_plans[key] = p;
+    }
+    out[i] = p;
+  }
+  return NORM_OK;
+}
+
+// Workspace of the two-pass backward: the dgamma (and dbeta) slots, one
+// segment wide, for every (CTA, segment) pair of the dx pass (CTA b's slot
+// of segment s is b + s, since a CTA's units cover consecutive segments),
+// then the per-(row, segment) dot products and the per-row totals.
+struct SplitWs {
+  size_t slots = 0, rowp = 0, rowt = 0, total = 0;
+};
+SplitWs split_ws(const Plan &dx, int64_t M, int mode) {
+  SplitWs w;
+  const size_t k = mode == kLayer ? 2 : 1;
+  const size_t nslots = static_cast<size_t>(dx.grid) + static_cast<size_t>(dx.nseg);
+  w.slots = 0;
+  w.rowp = k * nslots * static_cast<size_t>(dx.NS) * sizeof(float);
+  w.rowt = w.rowp + ((static_cast<size_t>(M) * dx.nseg * 2 * sizeof(float) + 15) & ~size_t(15));
+  w.total = w.rowt + ((static_cast<size_t>(M) * 2 * sizeof(float) + 15) & ~size_t(15));
+  return w;
+}
+
 norm_status_t launch(const void *fn, const Plan &p, const NormArgs &args, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -608,9 +748,50 @@ norm_status_t launch_reduce(const float *ws, int P, int n, float *dgamma, float 
   return NORM_OK;
 }
 
-norm_status_t check_common(int64_t M, int64_t N, norm_mode_t mode) {
+// A launch with programmatic stream serialisation allowed (the kernel waits
+// for its predecessor before touching global memory).
+norm_status_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return NORM_ERR_CUDA;
+  }
+  return NORM_OK;
+}
+
+// The per-row fold of the two-pass path: one warp per row, 8 rows per block.
+norm_status_t launch_fold(int mode, bool bwd, const NormArgs &args, cudaStream_t s) {
+  NormArgs a = args;
+  void *kargs[] = {&a};
+  const int64_t blocks = (a.M + 7) / 8;
+  if (blocks > 0x7fffffff) return NORM_ERR_SHAPE;
+  return launch_pdl(split_fold_kernel_ptr(mode, bwd), dim3(static_cast<unsigned>(blocks)),
+                    dim3(256), kargs, s);
+}
+
+// dgamma (and dbeta) from the two-pass dx pass's slots.
+norm_status_t launch_split_reduce(const NormArgs &args, int grid, float *dgamma, float *dbeta,
+                                  cudaStream_t s) {
+  NormArgs a = args;
+  void *kargs[] = {&a, &grid, &dgamma, &dbeta};
+  const int64_t threads = (static_cast<int64_t>(a.N) + 3) / 4;
+  return launch_pdl(split_reduce_kernel_ptr(),
+                    dim3(static_cast<unsigned>((threads + 255) / 256), dbeta ? 2 : 1), dim3(256),
+                    kargs, s);
+}
+
+norm_status_t check_common(int64_t M, int64_t N, norm_mode_t mode,
+                           int64_t max_n = NORM_MAX_N) {
   if (mode != NORM_RMS && mode != NORM_LAYER) return NORM_ERR_MODE;
-  if (M < 1 || N < 8 || N > NORM_MAX_N || (N % 8) != 0) return NORM_ERR_SHAPE;
+  if (M < 1 || N < 8 || N > max_n || (N % 8) != 0) return NORM_ERR_SHAPE;
   if (M > (int64_t(1) << 40)) return NORM_ERR_SHAPE;
   return NORM_OK;
 }
@@ -630,6 +811,7 @@ NormArgs base_args(const Plan &p, int64_t M, int N) {
   a.P = p.P;
   a.C = p.C;
   a.ntiles = p.ntiles;
+  a.nseg = p.nseg;
   a.invN = 1.0f / static_cast<float>(N);
   return a;
 }
@@ -651,6 +833,7 @@ void fill_plan(const Plan &p, norm_plan_t *out) {
   out->exact = p.exact ? 1 : 0;
   out->long_rows = p.long_rows ? 1 : 0;
   out->param_smem_bytes = p.par_bpc * p.NS;
+  out->split_segments = p.split ? p.nseg : 0;
 }
 
 // ------------------------------------------------------------ plan tuning
@@ -729,6 +912,16 @@ norm_status_t tune_pass(int mode, bool bwd, int64_t M, int N, size_t ws_bytes, i
   if (read_override().any) return NORM_ERR_ARG;  // a plan override bypasses the cache
   norm_status_t st = run();                      // validates, caches the default plan
   if (st != NORM_OK) return st;
+  if (use_split(N, Override())) {  // the two-pass path keeps its plan
+    if (chosen) {
+      norm_plan_t pl;
+      if ((st = norm_plan(M, N, static_cast<norm_mode_t>(mode), bwd ? 1 : 0, 0, 0, &pl)) !=
+          NORM_OK)
+        return st;
+      *chosen = pl;
+    }
+    return NORM_OK;
+  }
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
@@ -840,8 +1033,15 @@ norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
-  Plan p;
-  if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  const bool split = use_split(static_cast<int>(N), read_override());
+  Plan sp[2];
+  Plan &p = sp[0];
+  if (split) {
+    if ((st = make_split_plans(d, dev, mode, false, M, static_cast<int>(N), sp)) != NORM_OK)
+      return st;
+  } else if ((st = make_plan(d, dev, mode, false, M, static_cast<int>(N), &p)) != NORM_OK) {
+    return st;
+  }
   NormArgs a = base_args(p, M, static_cast<int>(N));
   a.x = static_cast<const uint16_t *>(x);
   a.gamma = static_cast<const uint16_t *>(gamma);
@@ -851,7 +1051,21 @@ norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64
   a.mean = mean;
   a.err = d.err;
   a.eps = eps;
-  return launch(kernel_for(p, mode, false), p, a, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!split) return launch(kernel_for(p, mode, false), p, a, s);
+  // statistics into y, their fold into rstd / mean, then y
+  if ((st = launch(kernel_for(sp[0], mode, false), sp[0], a, s)) != NORM_OK) return st;
+  if ((st = launch_fold(mode, false, a, s)) != NORM_OK) return st;
+  NormArgs b = base_args(sp[1], M, static_cast<int>(N));
+  b.x = a.x;
+  b.gamma = a.gamma;
+  b.beta = a.beta;
+  b.out = a.out;
+  b.rstd = rstd;
+  b.mean = mean;
+  b.err = d.err;
+  b.eps = eps;
+  return launch(kernel_for(sp[1], mode, false), sp[1], b, s);
 }
 
 norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, size_t *bytes) {
@@ -861,6 +1075,13 @@ norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, s
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  if (use_split(static_cast<int>(N), read_override())) {
+    Plan sp[2];
+    if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
+      return st;
+    *bytes = split_ws(sp[1], M, mode).total;
+    return NORM_OK;
+  }
   Plan p;
   if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p)) != NORM_OK) return st;
   *bytes = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
@@ -885,6 +1106,36 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_split(static_cast<int>(N), read_override())) {
+    Plan sp[2];
+    if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
+      return st;
+    const SplitWs w = split_ws(sp[1], M, mode);
+    if (workspace_bytes < w.total) return NORM_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    NormArgs a[2];
+    for (int i = 0; i < 2; ++i) {
+      a[i] = base_args(sp[i], M, static_cast<int>(N));
+      a[i].x = static_cast<const uint16_t *>(x);
+      a[i].dy = static_cast<const uint16_t *>(dy);
+      a[i].gamma = static_cast<const uint16_t *>(gamma);
+      a[i].out = static_cast<uint16_t *>(dx);
+      a[i].rstd = const_cast<float *>(rstd);
+      a[i].mean = const_cast<float *>(mean);
+      a[i].ws = reinterpret_cast<float *>(ws + w.slots);
+      a[i].rowp = reinterpret_cast<float *>(ws + w.rowp);
+      a[i].rowt = reinterpret_cast<float *>(ws + w.rowt);
+      a[i].err = d.err;
+    }
+    // dot products per (row, segment), their per-row fold, dx with the
+    // dgamma / dbeta slots, and the slots' fixed-order reduction
+    if ((st = launch(kernel_for(sp[0], mode, true), sp[0], a[0], s)) != NORM_OK) return st;
+    if ((st = launch_fold(mode, true, a[0], s)) != NORM_OK) return st;
+    if ((st = launch(kernel_for(sp[1], mode, true), sp[1], a[1], s)) != NORM_OK) return st;
+    return launch_split_reduce(a[1], sp[1].grid, dgamma, mode == NORM_LAYER ? dbeta : nullptr,
+                               s);
+  }
   Plan p;
   if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p)) != NORM_OK) return st;
   const size_t need = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
@@ -899,7 +1150,6 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   a.mean = const_cast<float *>(mean);
   a.ws = static_cast<float *>(workspace);
   a.err = d.err;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch(kernel_for(p, mode, true), p, a, s)) != NORM_OK) return st;
 
   return launch_reduce(static_cast<const float *>(workspace), p.P, static_cast<int>(N), dgamma,
@@ -910,7 +1160,7 @@ norm_status_t norm_add_fwd(const void *x, const void *r, const void *gamma, cons
                            int64_t M, int64_t N, float eps, norm_mode_t mode, void *h, void *y,
                            float *rstd, float *mean, norm_stream_t stream) {
   if (!x || !r || !gamma || !h || !y || !rstd) return NORM_ERR_NULL;
-  norm_status_t st = check_common(M, N, mode);
+  norm_status_t st = check_common(M, N, mode, NORM_MAX_N_FUSED);
   if (st != NORM_OK) return st;
   if (mode == NORM_RMS && (beta || mean)) return NORM_ERR_MODE;
   if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
@@ -941,7 +1191,7 @@ norm_status_t norm_add_fwd(const void *x, const void *r, const void *gamma, cons
 norm_status_t norm_add_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode,
                                            size_t *bytes) {
   if (!bytes) return NORM_ERR_NULL;
-  norm_status_t st = check_common(M, N, mode);
+  norm_status_t st = check_common(M, N, mode, NORM_MAX_N_FUSED);
   if (st != NORM_OK) return st;
   DeviceInfo d;
   int dev = 0;
@@ -959,7 +1209,7 @@ norm_status_t norm_add_bwd(const void *dy, const void *dh, const void *h, const 
                            norm_mode_t mode, void *dx, float *dgamma, float *dbeta,
                            void *workspace, size_t workspace_bytes, norm_stream_t stream) {
   if (!dy || !dh || !h || !gamma || !rstd || !dx || !dgamma) return NORM_ERR_NULL;
-  norm_status_t st = check_common(M, N, mode);
+  norm_status_t st = check_common(M, N, mode, NORM_MAX_N_FUSED);
   if (st != NORM_OK) return st;
   if (mode == NORM_RMS && (mean || dbeta)) return NORM_ERR_MODE;
   if (mode == NORM_LAYER && !mean) return NORM_ERR_MODE;
@@ -1001,7 +1251,7 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma, cons
   if (r && !h) return NORM_ERR_NULL;
   if (!r && h) return NORM_ERR_ARG;
   if (scaling != NORM_FP8_ROW && scaling != NORM_FP8_MX) return NORM_ERR_ARG;
-  norm_status_t st = check_common(M, N, mode);
+  norm_status_t st = check_common(M, N, mode, NORM_MAX_N_FUSED);
   if (st != NORM_OK) return st;
   if (scaling == NORM_FP8_MX && N % kMxBlock != 0) return NORM_ERR_SHAPE;
   if (mode == NORM_RMS && (beta || mean)) return NORM_ERR_MODE;
@@ -1046,12 +1296,39 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   if (!out) return NORM_ERR_NULL;
   norm_status_t st = check_common(M, N, mode);
   if (st != NORM_OK) return st;
-  if (backward & ~7) return NORM_ERR_ARG;
+  if (backward & ~15) return NORM_ERR_ARG;
   const bool bwd = (backward & 1) != 0;
   const bool resid = (backward & 2) != 0;
   const bool fp8 = (backward & 4) != 0;
+  const bool other = (backward & 8) != 0;  // two-pass path: its other pass
   if (fp8 && bwd) return NORM_ERR_ARG;
+  if ((resid || fp8) && N > NORM_MAX_N_FUSED) return NORM_ERR_SHAPE;
   Plan p;
+  const Override ov = read_override();
+  if (!resid && !fp8 && use_split(static_cast<int>(N), ov)) {
+    // the two-pass path: its statistics (forward) or dx (backward) pass,
+    // or with bit 3 the output (forward) or dot-product (backward) pass
+    const int phase = bwd ? (other ? kSplitBwdDots : kSplitBwdDx)
+                          : (other ? kSplitFwdOut : kSplitFwdStats);
+    if (sm_count > 0) {
+      if (smem_optin_bytes <= 0) return NORM_ERR_ARG;
+      if ((st = split_shape(mode, phase, M, static_cast<int>(N), smem_optin_bytes, ov, &p)) !=
+          NORM_OK)
+        return st;
+      split_grid(p, sm_count);
+    } else {
+      DeviceInfo d;
+      int dev = 0;
+      if ((st = device_info(&d, &dev)) != NORM_OK) return st;
+      Plan sp[2];
+      if ((st = make_split_plans(d, dev, mode, bwd, M, static_cast<int>(N), sp)) != NORM_OK)
+        return st;
+      p = sp[(phase == kSplitBwdDx || phase == kSplitFwdOut) ? 1 : 0];
+    }
+    fill_plan(p, out);
+    if (phase == kSplitBwdDx) out->partials = p.grid + p.nseg;  // slots, one segment wide
+    return NORM_OK;
+  }
   if (sm_count > 0) {
     if (smem_optin_bytes <= 0) return NORM_ERR_ARG;
     if ((st = shape_plan(mode, bwd, M, static_cast<int>(N), smem_optin_bytes, read_override(),

@@ -36,7 +36,10 @@ struct NormArgs {
   uint8_t *qexp;          // FP8 forward, MX scaling: E8M0 block exponents [M, N / 32]
   float *rstd;            // [M]: written by forward, read by backward
   float *mean;            // [M]: same, LayerNorm only
-  float *ws;              // backward partial sums [P, N] (+ [P, N] for dbeta)
+  float *ws;              // backward partial sums [P, N] (+ [P, N] for dbeta); on the
+                          // two-pass path the per-(CTA, segment) slots
+  float *rowp;            // two-pass backward: per-(row, segment) dot products [M, nseg, 2]
+  float *rowt;            // two-pass backward: per-row dot-product totals [M, 2]
   unsigned *err;          // device error word
   int64_t M;
   int64_t ntiles;
@@ -50,6 +53,7 @@ struct NormArgs {
   int S;    // pipeline stages
   int P;    // partial rows (backward) = number of clusters in the grid
   int C;    // CTAs per cluster
+  int nseg; // two-pass path: segments of NS columns per row (the last one ragged)
   float eps;
   float invN;
 };
@@ -125,6 +129,9 @@ struct Plan {
   int64_t ntiles = 0;
   int grid = 0;    // CTAs
   int P = 0;       // clusters in the grid (partial rows in backward)
+  bool split = false;  // two-pass path: rows cut into nseg segments of NS columns
+  int nseg = 0;
+  int phase = 0;       // two-pass path: which of its passes (kSplit*)
 };
 
 // Kernel entry points, by (mode, K, cluster, exact, fused residual).
@@ -167,5 +174,17 @@ const void *long_resid_kernel_ptr(int mode, int K, bool cluster, bool exact, boo
 const void *long_fp8_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, int out);
 int reduce_threads();
 const void *selftest_kernel_ptr();
+
+// The two-pass path for rows longer than one cluster holds (split.cu).
+constexpr int kSplitFwdStats = 0;  // per-(row, segment) statistics into y
+constexpr int kSplitFwdOut = 1;    // y from the folded statistics
+constexpr int kSplitBwdDots = 2;   // per-(row, segment) dot products
+constexpr int kSplitBwdDx = 3;     // dx and the dgamma / dbeta slots
+// Kernels by (mode, pass, chunks per thread); nullptr if not instantiated
+// (K = 4 for the first three passes, 2 for the dx pass).
+const void *split_kernel_ptr(int mode, int phase, int K);
+const void *split_fold_kernel_ptr(int mode, bool bwd);
+const void *split_reduce_kernel_ptr();
+SmemLayout split_smem_layout(int RT, int NS, int S, int G, int tpr, int ntensors);
 
 }  // namespace gbn

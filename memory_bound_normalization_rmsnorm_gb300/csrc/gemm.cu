@@ -668,7 +668,7 @@ std::map<std::tuple<int, int, int>, int> g_pairs;
 
 norm_status_t check_shape(int64_t M, int64_t K, int64_t Nout) {
   if (M < 1 || M > int64_t(65535) * kBM) return NORM_ERR_SHAPE;
-  if (K < kBK || K > NORM_MAX_N || K % kBK != 0) return NORM_ERR_SHAPE;
+  if (K < kBK || K > NORM_MAX_N_FUSED || K % kBK != 0) return NORM_ERR_SHAPE;
   if (Nout < 32 || Nout > (int64_t(1) << 20) || Nout % 32 != 0) return NORM_ERR_SHAPE;
   return NORM_OK;
 }

@@ -198,3 +198,95 @@ def check_reduce(P, N, nparts):
             covered += [p + u for u in range(REDUCE_BATCH) if p + u < b]
     assert covered == list(range(P))
     return True
+
+
+SPLIT_FWD_STATS, SPLIT_FWD_OUT, SPLIT_BWD_DOTS, SPLIT_BWD_DX = range(4)
+
+
+def split_layout(RT, NS, S, G, tpr, ntensors):
+    """Same region order as the two-pass kernels' shared-memory layout."""
+    tensor = RT * NS * 2
+    stage = tensor * ntensors
+    off = stage * S
+    L = {"tensor": tensor, "stage": stage, "stats": off}
+    off = _align16(off + S * RT * 4 * 4)
+    L["red"] = off
+    if tpr > 32:
+        off = _align16(off + 2 * G * (tpr // 32) * 4 * 4)
+    L["bar"] = off
+    off = _align16(off + S * 8)
+    L["flag"] = off
+    off = _align16(off + 4 + 4 * S)
+    L["total"] = off
+    return L
+
+
+def unit_ranges(U, grid):
+    """[begin, end) of the units of each CTA: [U b / grid, U (b+1) / grid)."""
+    return [(U * b // grid, U * (b + 1) // grid) for b in range(grid)]
+
+
+def check_split_plan(p, M, N, mode, phase, smem_optin=232448):
+    """The two-pass kernels on plan `p` (a norm_plan dict with
+    split_segments > 0): every unit visited once, every bulk copy, shared
+    memory slot, scratch and workspace index in bounds; for the dx pass,
+    each (CTA, segment) slot is distinct and the reduction reads exactly
+    the slots that the CTAs touching each segment wrote."""
+    NS, tpr, K = p["cols_per_cta"], p["threads_per_row"], p["chunks_per_thread"]
+    G, rpg, RT, S = p["groups"], p["rows_per_group"], p["rows_per_tile"], p["stages"]
+    threads, smem, T, grid = p["threads"], p["smem_bytes"], p["tiles"], p["grid"]
+    nseg = p["split_segments"]
+    nc, nsc = N // 8, NS // 8
+    assert p["cluster"] == 1 and nseg == -(-N // NS) and NS % 1024 == 0
+    assert tpr * K * 8 == NS and tpr % 32 == 0 and threads == G * tpr <= MAX_THREADS
+    assert G <= 16 and (tpr == 32 or G <= 15)
+    assert RT == G * rpg and S >= 2 and T == -(-M // RT)
+    ntensors = 2 if phase >= SPLIT_BWD_DOTS else 1
+    L = split_layout(RT, NS, S, G, tpr, ntensors)
+    assert smem == L["total"] <= smem_optin and L["stage"] < TX_LIMIT
+    if tpr > 32:
+        W = tpr // 32
+        hi = ((1 * G + (G - 1)) * W + (W - 1)) * 4 + 4
+        assert L["red"] + hi * 4 <= L["bar"]
+    # stats slots [S][RT][4]
+    assert L["stats"] + ((S - 1) * RT + RT - 1) * 16 + 16 <= L["red"]
+    U = T * nseg
+    assert 1 <= grid <= U
+    ranges = unit_ranges(U, grid)
+    assert ranges[0][0] == 0 and ranges[-1][1] == U
+    assert all(a < b for a, b in ranges), "a CTA with no unit"
+    assert all(ranges[i][1] == ranges[i + 1][0] for i in range(grid - 1))
+    # per segment: chunks and copies
+    for seg in {0, nseg - 1, nseg // 2}:
+        nsc_me = min(nsc, nc - seg * nsc)
+        assert 1 <= nsc_me <= nsc
+        col0 = seg * NS
+        assert col0 + nsc_me * 8 <= N and (col0 * 2) % 16 == 0
+        owned = sorted(t + k * tpr for t in range(tpr) for k in range(K) if t + k * tpr < nsc_me)
+        assert owned == list(range(nsc_me))
+        assert (RT - 1) * NS * 2 + nsc_me * 16 <= L["tensor"]
+        if phase == SPLIT_FWD_STATS:
+            # partial of (row, seg) in y's row: float (RMS) or float2 (LN)
+            assert (seg + 1) * (8 if mode == 1 else 4) <= 2 * N
+    for rt in {0, T - 1}:
+        row0 = rt * RT
+        nrows = min(RT, M - row0)
+        assert 1 <= nrows and (row0 + nrows - 1) * N + N <= M * N
+    if phase == SPLIT_BWD_DOTS:
+        assert (M - 1) * nseg + nseg - 1 < M * nseg      # rowp float2 index
+    if phase == SPLIT_BWD_DX:
+        nslots = grid + nseg
+        slots = set()
+        touch = [[] for _ in range(nseg)]
+        for b, (u0, u1) in enumerate(ranges):
+            for seg in range(u0 // T, (u1 - 1) // T + 1):
+                assert 0 <= b + seg < nslots
+                assert (b, seg) not in slots
+                slots.add((b, seg))
+                touch[seg].append(b)
+        assert len({b + s for b, s in slots}) == len(slots), "two pairs share a slot"
+        for seg in range(nseg):
+            lo = ((seg * T + 1) * grid - 1) // U
+            hi = ((seg + 1) * T * grid - 1) // U
+            assert touch[seg] == list(range(lo, hi + 1)), "reduce reads other slots"
+    return True

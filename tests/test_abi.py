@@ -53,7 +53,7 @@ def test_fwd_validation_codes():
     assert call(M=0) == 2
     assert call(N=12) == 2
     assert call(N=0) == 2
-    assert call(N=262152) == 2
+    assert call(N=(1 << 24) + 8) == 2   # N > NORM_MAX_N
     assert call(mode=2) == 4
     assert call(b=F) == 4              # beta with RMSNorm
     assert call(m=F) == 4              # mean with RMSNorm
@@ -83,6 +83,7 @@ def test_fp8_validation_codes():
     assert call(h=F) == 9              # h without residual
     assert call(sc=2) == 9             # unknown scaling
     assert call(sc=1, N=48) == 2       # MX needs N % 32 == 0
+    assert call(N=262144 + 32) == 2    # above NORM_MAX_N_FUSED
     assert call(N=12) == 2
     assert call(mode=2) == 4
     assert call(b=F) == 4

@@ -75,7 +75,12 @@ def test_plan_rejects_unsupported():
     with pytest.raises(gb.NormError):
         gb.norm_plan(0, 16, 0, False, SMS, OPTIN)  # M < 1
     with pytest.raises(gb.NormError):
-        gb.norm_plan(4, 262152, 0, False, SMS, OPTIN)  # N > NORM_MAX_N
+        gb.norm_plan(4, (1 << 24) + 8, 0, False, SMS, OPTIN)  # N > NORM_MAX_N
+    for which in (dict(residual=True), dict(fp8=True)):  # fused variants stop earlier
+        with pytest.raises(gb.NormError):
+            gb.norm_plan(4, 262152, 0, False, SMS, OPTIN, **which)
+    with pytest.raises(gb.NormError):
+        gb.norm_plan(4, 262152, 0, True, SMS, OPTIN, residual=True)
 
 
 def test_regimes_by_row_length():
@@ -118,3 +123,55 @@ def test_random_shapes_every_plan_kind():
                 if N % 32 == 0:
                     launch_check.check_fp8_plan(p8, M, N, "mx")
     assert n == 600
+
+
+SPLIT_SHAPES = [(6, 524288), (33, 1048576), (4096, 524288), (1, 262152), (4097, 300008),
+                (5, 1 << 24), (2, 262144 + 4096 * 3 + 8)]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("backward", [False, True])
+@pytest.mark.parametrize("other", [False, True])
+def test_split_plans_in_bounds(mode, backward, other):
+    """Rows wider than one cluster holds take the two-pass path: both passes
+    of the forward and of the backward stay in bounds, and the dx pass's
+    dgamma / dbeta slots are distinct and read back exactly."""
+    phase = (2 if backward else 0) + (1 if other else 0)
+    for M, N in SPLIT_SHAPES:
+        p = gb.norm_plan(M, N, mode, backward, SMS, OPTIN, other_pass=other)
+        assert p["split_segments"] == -(-N // 4096)
+        launch_check.check_split_plan(p, M, N, mode, phase, OPTIN)
+
+
+@pytest.mark.parametrize("backward", [False, True])
+def test_split_forced_small_rows(backward, monkeypatch):
+    """The plan override split=1 (with W=1024 segments) puts short rows on
+    the two-pass path, which the GPU parity tests use for ragged and
+    many-segment cases at sizes the oracle checks in full."""
+    monkeypatch.setenv("GBNORM_PLAN", "split=1,W=1024")
+    for mode in (0, 1):
+        for M, N in ((37, 1024), (130, 3000), (70, 4104), (9, 8200), (1, 8), (3, 1016)):
+            for other in (False, True):
+                p = gb.norm_plan(M, N, mode, backward, SMS, OPTIN, other_pass=other)
+                assert p["split_segments"] == -(-N // 1024)
+                launch_check.check_split_plan(p, M, N, mode,
+                                              (2 if backward else 0) + (1 if other else 0), OPTIN)
+
+
+def test_split_random_shapes():
+    import numpy as np
+
+    rng = np.random.default_rng(7)
+    for _ in range(60):
+        N = int(rng.integers(262152 // 8, (1 << 24) // 8 + 1)) * 8
+        M = int(rng.integers(1, 5000))
+        mode = int(rng.integers(0, 2))
+        for phase in range(4):
+            p = gb.norm_plan(M, N, mode, phase >= 2, SMS, OPTIN, other_pass=bool(phase & 1))
+            launch_check.check_split_plan(p, M, N, mode, phase, OPTIN)
+
+
+def test_one_pass_up_to_its_limit():
+    for bwd in (False, True):
+        assert gb.norm_plan(4096, 262144, 0, bwd, SMS, OPTIN)["split_segments"] == 0
+        assert gb.norm_plan(4096, 262152, 0, bwd, SMS, OPTIN)["split_segments"] > 0

@@ -28,6 +28,7 @@ CASES = [
     ("rms_262144x768_outliers", 20001, 768),
     ("rms_4096x131072", 37, 131072),
     ("layer_32768x5120_resid", 1001, 5120),
+    ("layer_32768x4096", 6, 524288),  # rows wide enough for the two-pass path
 ]
 
 
