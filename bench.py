@@ -555,8 +555,10 @@ def measure_workload(gb, w, peak, seconds=0.15, warmup=3, steps=0, fused=False, 
     t1 = time.time()
     if gb.norm_get_device_error() != 0:
         raise RuntimeError(f"device error word set on {w.name}")
-    fb, bb = algo_bytes(w.M, w.N, w.mode, 0 if pb is None else pb["partials"],
-                        residual=fused, fp8=fp8)
+    P = 0 if pb is None else pb["partials"]
+    if pb is not None and pb.get("split_segments"):
+        P = P * pb["cols_per_cta"] / w.N  # slots are one segment wide
+    fb, bb = algo_bytes(w.M, w.N, w.mode, P, residual=fused, fp8=fp8)
     out = {"workload": w.name, "mode": w.mode_name, "M": w.M, "N": w.N,
            "fwd_us": 1e3 * res["fwd"], "fwd_GBs": fb / res["fwd"] / 1e6,
            "fwd_frac": fb / res["fwd"] / 1e6 / peak, "plan_fwd": plan_str(pf)}
@@ -672,8 +674,11 @@ def run_ours(args):
     sweep = None
     if world == 1 and not args.no_sweep:
         sweep = []
-        for name in wl.WORKLOADS:
-            sweep.append(measure_workload(gb, wl.WORKLOADS[name], peak, sampler=sampler))
+        for name in wl.ALL:
+            e = measure_workload(gb, wl.ALL[name], peak, sampler=sampler)
+            if name in wl.WIDE:
+                e["beyond_configs"] = "rows wider than one cluster holds (two-pass path)"
+            sweep.append(e)
     clocks_all = sampler.stop()
     clocks = sampler.window(busy0, busy1) or clocks_all
     if sweep is not None:
@@ -919,10 +924,13 @@ def run_sweep(args):
 
     torch.cuda.set_device(0)
     peak, peak_kind = peak_hbm()
-    names = list(wl.WORKLOADS) if args.sweep == "all" else args.sweep.split(",")
+    names = (list(wl.WORKLOADS) if args.sweep == "all" else
+             list(wl.WIDE) if args.sweep == "wide" else args.sweep.split(","))
     fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
     for name in names:
-        w = wl.WORKLOADS[name]
+        w = wl.ALL[name]
+        if args.rows:
+            w = wl.like(w, args.rows, w.N)
         line = measure_workload(gb, w, peak, warmup=args.warmup, steps=args.steps,
                                 fused=args.fused_residual, fp8=fp8, fwd_only=args.fwd_only)
         line.update({"fused_residual": args.fused_residual, "fp8": args.fp8 or None,
@@ -945,25 +953,26 @@ def run_ablate(args):
     w = wl.WORKLOADS[args.workload]
     x, g, b, dy = wl.make_inputs(w, "cuda")
     stream = torch.cuda.current_stream()
-    settings = [("grid", f"grid={p}") for p in (19, 38, 76, 114, 152)]
-    settings += [("grid", f"grid={p},G=1") for p in (152, 304)]
-    settings += [("stages", f"S={k}") for k in range(2, 9)]
+    # partial rows: the persistent grid capped below one CTA per SM, the
+    # default, and two smaller CTAs (one row group) per SM; stages: tiles of
+    # one row per group (half the default tile) so that up to 6 fit
+    settings = [("grid", f"grid={p}") for p in (19, 38, 76, 114)]
+    settings += [("grid", ""), ("grid", "G=1,rpg=1,S=3,ctas=2")]
+    settings += [("stages", f"rpg=1,S={k}") for k in range(2, 8)]
     for kind, ov in settings:
-        os.environ["GBNORM_PLAN"] = ov
+        if ov:
+            os.environ["GBNORM_PLAN"] = ov
         try:
             step = DirectStep(gb, w, x, g, b, dy, stream)
             pb = gb.norm_plan(w.M, w.N, w.mode, True)
+            step.fwd()
+            for _ in range(args.warmup):
+                step.bwd()
+            ms = timed_loop(step.bwd, max(20, args.steps), stream)
         except Exception as e:  # a setting the planner cannot schedule
             print(json.dumps({"workload": w.name, "knob": kind, "override": ov,
                               "error": str(e)}), flush=True)
             continue
-        finally:
-            os.environ.pop("GBNORM_PLAN", None)
-        os.environ["GBNORM_PLAN"] = ov
-        try:
-            for _ in range(args.warmup):
-                step.bwd()
-            ms = timed_loop(step.bwd, max(20, args.steps), stream)
         finally:
             os.environ.pop("GBNORM_PLAN", None)
         if gb.norm_get_device_error() != 0:
@@ -1082,7 +1091,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="layer_32768x4096")
     ap.add_argument("--rows", type=int, default=0,
-                    help="override M (smaller cases for profiling captures only)")
+                    help="override M (smaller cases for profiling captures only; also "
+                         "with --sweep)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cold", action="store_true",
@@ -1095,8 +1105,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", default="",
-                    help="'all' or comma-separated workload names: per-workload fwd/bwd "
-                         "timings, one JSON line each (not the benchmark line)")
+                    help="'all', 'wide' or comma-separated workload names: per-workload "
+                         "fwd/bwd timings, one JSON line each (not the benchmark line)")
     ap.add_argument("--fused-residual", action="store_true",
                     help="with --sweep: time norm_add_fwd/norm_add_bwd (h = x + r fused in)")
     ap.add_argument("--fwd-only", action="store_true",
