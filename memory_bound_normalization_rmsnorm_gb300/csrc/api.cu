@@ -506,27 +506,6 @@ norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_
   st = finish_plan(d, dev, mode, bwd, ov, &p);
   if (st != NORM_OK) return st;
 
-  // Long rows in clusters: the smallest cluster whose slices fit is not
-  // always the one that keeps the most SMs busy -- a cluster must sit
-  // inside one GPC, and on GB300 clusters of 8 occupy 120 of the 152 SMs
-  // where clusters of 9 occupy 135.  Every cluster size up to 16 whose
-  // slices fit is tried; the one launching the most CTAs wins (ties: the
-  // smaller cluster, which exchanges less).
-  if (p.long_rows && p.C > 1 && !ov.C) {
-    Plan best = p;
-    for (int c = 2; c <= 16; ++c) {
-      if (c == p.C) continue;
-      Override o = ov;
-      o.C = c;
-      Plan q;
-      if (long_plan(mode, bwd, M, N, d.smem_optin, o, &q, resid, fp8 && !bwd) != NORM_OK)
-        continue;
-      if (finish_plan(d, dev, mode, bwd, o, &q) != NORM_OK) continue;
-      if (q.grid > best.grid || (q.grid == best.grid && q.C < best.C)) best = q;
-    }
-    p = best;
-  }
-
   if (!ov.any) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_plans[key] = p;
