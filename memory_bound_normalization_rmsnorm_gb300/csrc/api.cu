@@ -201,8 +201,10 @@ int round_k(int K, bool bwd) {
 
 // Offline-tuned plans for row lengths measured on GB300 (a search over
 // threads per row, rows per group and stages, keeping changes that beat the
-// heuristic by more than ~5 %).  Like any plan they fix the reduction order,
-// so results stay bitwise reproducible; shapes not listed use the heuristic.
+// heuristic by more than ~5 %; then a search over the stage count alone,
+// keeping gains above 1 %: fewer tiles in flight than fit -- 2 to 5 -- are
+// often faster).  Like any plan they fix the reduction order, so results
+// stay bitwise reproducible; shapes not listed use the heuristic.
 struct TunedPlan {
   int mode;  // kRMS / kLayer
   int bwd;   // 0 forward, 1 backward
@@ -213,19 +215,22 @@ struct TunedPlan {
   int G = 0;        // row groups per CTA (0 = heuristic's choice)
 };
 constexpr TunedPlan kTuned[] = {
-    {kRMS, 0, 256, 32, 2, 3},     {kRMS, 0, 512, 32, 1, 3},    {kRMS, 0, 768, 32, 0, 3},
-    {kRMS, 0, 1024, 64, 1, 0},    {kRMS, 0, 2048, 128, 1, 0},  {kRMS, 0, 3072, 192, 1, 3},
-    {kRMS, 0, 5120, 160, 0, 3},   {kRMS, 0, 8192, 256, 0, 3},  {kRMS, 0, 16384, 512, 0, 3},
-    {kLayer, 0, 2048, 64, 0, 3},  {kLayer, 0, 3072, 0, 0, 0, 1}, {kLayer, 0, 5120, 0, 0, 0, 1},
-    {kLayer, 0, 8192, 0, 0, 0, 1},
+    {kRMS, 0, 256, 32, 2, 2},     {kRMS, 0, 512, 32, 1, 2},    {kRMS, 0, 768, 32, 0, 3},
+    {kRMS, 0, 1024, 64, 1, 0},    {kRMS, 0, 2048, 128, 1, 2},  {kRMS, 0, 3072, 192, 1, 3},
+    {kRMS, 0, 5120, 160, 0, 3},   {kRMS, 0, 8192, 256, 0, 3},  {kRMS, 0, 16384, 512, 0, 4},
+    {kRMS, 0, 32768, 0, 0, 2},
+    {kLayer, 0, 2048, 64, 0, 5},  {kLayer, 0, 3072, 0, 0, 0, 1}, {kLayer, 0, 4096, 0, 0, 4},
+    {kLayer, 0, 5120, 0, 0, 3, 1}, {kLayer, 0, 8192, 0, 0, 0, 1},
     {kRMS, 1, 256, 32, 2, 5},     {kRMS, 1, 512, 64, 0, 0},    {kRMS, 1, 768, 64, 4, 0},
-    {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 2048, 128, 1, 7},  {kRMS, 1, 5120, 256, 2, 0},
+    {kRMS, 1, 1024, 64, 1, 5},    {kRMS, 1, 2048, 128, 1, 5},  {kRMS, 1, 5120, 256, 2, 0},
+    {kRMS, 1, 16384, 0, 0, 2},
     {kLayer, 1, 3072, 192, 4, 0},
     // LayerNorm backward at 5120 / 8192: the long-row kernel with 4 chunks
     // per thread and 3 / 2 row groups (15 / 16 warps) beats the register
     // kernel's 2 chunks per thread (10 / 16 warps, 8 / 16 warps per row):
-    // 195 -> 173 us and 274 -> 265 us at 32768 rows.
-    {kLayer, 1, 5120, 0, 0, 0, 0, 1, 3}, {kLayer, 1, 8192, 0, 0, 0, 0, 1, 2},
+    // 195 -> 173 us and 274 -> 265 us at 32768 rows; two stages instead of
+    // three gain another 2-3 %.
+    {kLayer, 1, 5120, 0, 0, 2, 0, 1, 3}, {kLayer, 1, 8192, 0, 0, 2, 0, 1, 2},
 };
 
 // Ring and tile sizing shared by both plan kinds: rows per tile and the
@@ -611,7 +616,8 @@ norm_status_t split_shape(int mode, int phase, int64_t M, int N, int smem_optin,
     if (S >= 2 || rpg == 1 || ov.rpg) break;
     rpg = (rpg + 1) / 2;
   }
-  S = std::min(S, 8);
+  // three units in flight: measured the fastest of 2 to 8 for every pass
+  S = std::min(S, 3);
   if (ov.S) S = ov.S;
   if (S < 2) return NORM_ERR_UNSUPPORTED;
   const SmemLayout L = split_smem_layout(G * rpg, W, S, G, tpr, nt);
