@@ -63,25 +63,23 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# Host-only sources: they choose and launch kernels but compile to no device
-# code; the plan they chose is recorded beside the counters instead.
-HOST_ONLY_SOURCES = ("api.cu", "host.cu")
-# The normalisation-GEMM's own sources (its kernels are in gemm.cu alone),
-# and the shared headers that gemm.cu also includes.
-NORM_GEMM_SOURCES = ("gemm.cu", "tcgen05.cuh")
-NORM_GEMM_HEADERS = ("common.cuh", "ptx.cuh", "rowops.cuh")
+# The sources each recorded kernel is built from (its translation unit and
+# the headers it includes); a traffic record is valid while they are
+# unchanged.  Host sources choose and launch kernels but compile to no device
+# code: the plan a record was taken with is kept beside its counters instead.
+_SHARED = ("common.cuh", "ptx.cuh", "rowops.cuh")
+KERNEL_SOURCES = {
+    "norm_fwd_kernel": ("fwd.cu", "fwd_kernel.cuh", "tiles.cuh") + _SHARED,
+    "norm_bwd_kernel": ("bwd.cu", "tiles.cuh") + _SHARED,
+    "norm_gemm_kernel": ("gemm.cu", "tcgen05.cuh") + _SHARED,
+}
 
 
-def source_hash(kind="norm"):
-    """Hash of the sources that define the device code of the normalisation
-    kernels (kind "norm") or of the normalisation-GEMM kernel ("gemm")."""
+def source_hash(kernel="norm_bwd_kernel"):
+    """Hash of the sources that define `kernel`'s device code."""
     csrc = os.path.join(ROOT, "memory_bound_normalization_rmsnorm_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if kind == "norm" and (name in HOST_ONLY_SOURCES or name in NORM_GEMM_SOURCES):
-            continue
-        if kind == "gemm" and name not in NORM_GEMM_SOURCES + NORM_GEMM_HEADERS:
-            continue
+    for name in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -95,7 +93,7 @@ def _plan_key(p):
     return {k: p[k] for k in keys}
 
 
-def ncu_traffic(workload, kernel, plan=None, kind="norm"):
+def ncu_traffic(workload, kernel, plan=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current device code and the same launch plan (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -103,7 +101,7 @@ def ncu_traffic(workload, kernel, plan=None, kind="norm"):
         with open(path) as f:
             data = json.load(f)
         rec = data[workload][kernel]
-        if rec.get("source_hash") != source_hash(kind):
+        if rec.get("source_hash") != source_hash(kernel):
             return None
         if plan is not None and rec.get("plan") is not None and rec["plan"] != plan:
             return None
@@ -1070,7 +1068,7 @@ def run_norm_gemm(args):
                 "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                              "unit": "TFLOP/s", "frac": achieved / peak,
                              "peak_kind": f"cuBLAS bf16 burst, {peak_kind}",
-                             "traffic": ncu_traffic(w0.name, "norm_gemm_kernel", kind="gemm")},
+                             "traffic": ncu_traffic(w0.name, "norm_gemm_kernel")},
                 "unfused_us": 1e3 * t_unfused, "norm_fwd_us": 1e3 * t_norm,
                 "cublas_us": 1e3 * t_gemm, "cublas_tflops": flops / (t_gemm * 1e-3) / 1e12,
                 "speedup_vs_unfused": t_unfused / t_fused,
