@@ -158,6 +158,7 @@ struct Override {
   int C = 0, tpr = 0, rpg = 0, S = 0, G = 0, ctas = 0, lng = -1, K = 0, gsm = -1, grid = 0;
   int split = -1;  // 1: the two-pass path at any N; 0: never
   int W = 0;       // two-pass path: segment width (a multiple of 1024)
+  int S1 = 0, S2 = 0;  // two-pass path: stages of its first / second pass
   bool any = false;
 };
 
@@ -189,6 +190,8 @@ Override read_override() {
     else if (!std::strcmp(key, "grid")) o.grid = val;
     else if (!std::strcmp(key, "split")) o.split = val;
     else if (!std::strcmp(key, "W")) o.W = val;
+    else if (!std::strcmp(key, "S1")) o.S1 = val;
+    else if (!std::strcmp(key, "S2")) o.S2 = val;
     o.any = true;
   }
   return o;
@@ -618,7 +621,10 @@ norm_status_t split_shape(int mode, int phase, int64_t M, int N, int smem_optin,
   }
   // three units in flight: measured the fastest of 2 to 8 for every pass
   S = std::min(S, 3);
+  const bool first = phase == kSplitFwdStats || phase == kSplitBwdDots;
   if (ov.S) S = ov.S;
+  if (first && ov.S1) S = ov.S1;
+  if (!first && ov.S2) S = ov.S2;
   if (S < 2) return NORM_ERR_UNSUPPORTED;
   const SmemLayout L = split_smem_layout(G * rpg, W, S, G, tpr, nt);
   if (static_cast<int64_t>(L.total) > budget) return NORM_ERR_UNSUPPORTED;

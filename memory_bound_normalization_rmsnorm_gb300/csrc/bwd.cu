@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
         chunk_to_f2(dv, df);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          xh[k][p] = mul2(add2(xf[p], nmu), rs2);
+          xh[k][p] = mul2(MODE == kLayer ? add2(xf[p], nmu) : xf[p], rs2);
           gg[k][p] = mul2(df[p], gf[k][p]);
           // two independent accumulator pairs shorten the dependency chains
           if (p & 1) {
@@ -159,9 +159,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
         if (CLUSTER) cluster_sum<1>(w1, r, t, xch, a.err, abort_flag);
         v[1] = w1[0];
       }
-      const float2 av = splat2((MODE == kLayer) ? v[0] * invN : 0.f);
-      const float2 cv = splat2(v[1] * invN);
-      const float2 neg1 = splat2(-1.f);
+      // dx = rstd (g - a - xhat c) = rstd g - rstd a - (rstd c) xhat
+      const float2 nra = splat2((MODE == kLayer) ? -rs * (v[0] * invN) : 0.f);
+      const float2 nrc = splat2(-rs * (v[1] * invN));
 
       if (active) {
         uint16_t *dxrow = a.out + (row0 + r) * a.N + col0 + t * 8;
@@ -170,11 +170,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_kernel(const NormArgs
           if (EXACT || t + k * a.tpr < nsc_me) {
             float2 o[4];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              // dx = rstd * (g - (xhat * c + a))
-              const float2 u = fma2(xh[k][p], cv, av);
-              o[p] = mul2(fma2(u, neg1, gg[k][p]), rs2);
-            }
+            for (int p = 0; p < 4; ++p)
+              o[p] = fma2(xh[k][p], nrc,
+                          MODE == kLayer ? fma2(gg[k][p], rs2, nra) : mul2(gg[k][p], rs2));
             if (RESID) {
               float2 dh[4];
               chunk_to_f2(*reinterpret_cast<const uint4 *>(stx + 2 * L.tensor_bytes +

@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
           chunk_to_f2(gv[k], gf);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            const float2 xh = mul2(add2(xf[p], nmu), rs2);
+            const float2 xh = mul2(MODE == kLayer ? add2(xf[p], nmu) : xf[p], rs2);
             const float2 gg = mul2(df[p], gf[p]);
             if (p & 1) {
               s2b = fma2(gg, xh, s2b);
@@ -523,9 +523,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
     const float rs = stats[2 * r];
     const float mu = (MODE == kLayer) ? stats[2 * r + 1] : 0.f;
     const float2 rs2 = splat2(rs), nmu = splat2(-mu);
-    const float2 av = splat2((MODE == kLayer) ? tsum_g * invN : 0.f);
-    const float2 cv = splat2(tsum_gx * invN);
-    const float2 neg1 = splat2(-1.f);
+    // dx = rstd (g - a - xhat c) = rstd g - rstd a - rstd^2 c (x - mean):
+    // the row constants -rstd a and -rstd^2 c leave three (RMSNorm) or four
+    // (LayerNorm) packed operations per pair
+    const float2 nra = splat2((MODE == kLayer) ? -rs * (tsum_g * invN) : 0.f);
+    const float2 nk1 = splat2(-rs * rs * (tsum_gx * invN));
     uint16_t *dxrow = a.out + (row0 + r) * a.N + col0 + t * 8;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -536,11 +538,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
         chunk_to_f2(gv[k], gf);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          // dx = rstd * (g - (xhat * c + a))
-          const float2 xh = mul2(add2(xf[p], nmu), rs2);
           const float2 gg = mul2(df[p], gf[p]);
-          const float2 u = fma2(xh, cv, av);
-          o[p] = mul2(fma2(u, neg1, gg), rs2);
+          const float2 xc = MODE == kLayer ? add2(xf[p], nmu) : xf[p];
+          o[p] = fma2(xc, nk1, MODE == kLayer ? fma2(gg, rs2, nra) : mul2(gg, rs2));
         }
         if (RESID) {
           float2 hf[4];

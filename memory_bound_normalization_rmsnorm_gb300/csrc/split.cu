@@ -79,19 +79,32 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   return pol;
 }
 
-// Issues unit u into stage s: the tile's row slices of x (and dy), each one
-// bulk copy, and for the passes that need them the rows' saved statistics
-// (and the backward's dot-product totals) by 4-byte copies.  Called by all
-// 32 lanes of one warp.
+// Segment and row tile of a unit, advanced without division.
+struct UnitPos {
+  int64_t seg, rt;
+};
+__device__ __forceinline__ void unit_advance(UnitPos &p, int64_t by, int64_t T) {
+  p.rt += by;
+  while (p.rt >= T) {
+    p.rt -= T;
+    ++p.seg;
+  }
+}
+
+// Issues the unit at `pos` into stage s: the tile's row slices of x (and
+// dy), each one bulk copy, and for the passes that need them the rows' saved
+// statistics (and the backward's dot-product totals) by 4-byte copies.
+// Called by all 32 lanes of one warp.
 template <int MODE, int PHASE>
 __device__ __forceinline__ void issue_unit(const NormArgs &a, const SmemLayout &L,
-                                           unsigned char *smem, int64_t u, int s, uint64_t pol) {
+                                           unsigned char *smem, UnitPos pos, int s,
+                                           uint64_t pol) {
   constexpr int NT = PHASE >= kSplitBwdDots ? 2 : 1;
   const int lane = threadIdx.x & 31;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off) + s;
   unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
-  const int64_t seg = u / a.ntiles;
-  const int64_t row0 = (u - seg * a.ntiles) * a.RT;
+  const int64_t seg = pos.seg;
+  const int64_t row0 = pos.rt * a.RT;
   const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
   const int64_t col0 = seg * a.NS;
   const int nsc_me = static_cast<int>(min64(a.nsc, a.N / 8 - seg * a.nsc));
@@ -157,10 +170,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
   const uint64_t pol = (PHASE == kSplitFwdStats || PHASE == kSplitBwdDots)
                            ? l2_evict_normal_policy()
                            : l2_evict_first_policy();
+  // position of the first unit (one division per CTA), then advanced
+  UnitPos first;
+  first.seg = u0 / T;
+  first.rt = u0 - first.seg * T;
   if (tid < 32) {
     __syncwarp();
-    for (int j = 0; j < a.S; ++j)
-      if (u0 + j < u1) issue_unit<MODE, PHASE>(a, L, smem, u0 + j, j, pol);
+    UnitPos ip = first;
+    for (int j = 0; j < a.S; ++j) {
+      if (u0 + j < u1) issue_unit<MODE, PHASE>(a, L, smem, ip, j, pol);
+      unit_advance(ip, 1, T);
+    }
   }
 
   // Per-segment state: gamma (fp32 pairs) and beta (packed) of this
@@ -219,8 +239,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
   int rpar = 0;
   int s = 0;
   uint32_t par = 0;
-  for (int64_t u = u0; u < u1; ++u) {
-    const int64_t seg = u / T;
+  UnitPos pos = first;
+  for (int64_t u = u0; u < u1; ++u, unit_advance(pos, 1, T)) {
+    const int64_t seg = pos.seg;
     if (seg != cur) {
       if (PHASE == kSplitBwdDx && cur >= 0) flush(cur);
       cur = seg;
@@ -244,7 +265,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
       }
     }
     mbar_wait(full + s, par, a.err, abort_flag);
-    const int64_t row0 = (u - seg * T) * a.RT;
+    const int64_t row0 = pos.rt * a.RT;
     const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
     const unsigned char *stx = smem + static_cast<size_t>(s) * L.stage_bytes;
     const float *stats = reinterpret_cast<const float *>(smem + L.stats_off) +
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
           chunk_to_f2(dv, df[k]);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            xh[k][p] = mul2(add2(xf[k][p], nmu), rs2);
+            xh[k][p] = mul2(MODE == kLayer ? add2(xf[k][p], nmu) : xf[k][p], rs2);
             gg[k][p] = mul2(df[k][p], gf[k][p]);
           }
         }
@@ -358,9 +379,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
           if (active && t == 0)
             reinterpret_cast<float2 *>(a.rowp)[(row0 + r) * a.nseg + seg] = make_float2(v[0], v[1]);
         } else if (active) {
-          const float2 av = splat2(MODE == kLayer ? stats[4 * r + 2] * invN : 0.f);
-          const float2 cv = splat2(stats[4 * r + 3] * invN);
-          const float2 neg1 = splat2(-1.f);
+          // dx = rstd (g - a - xhat c) = rstd g - rstd a - (rstd c) xhat
+          const float2 nra = splat2(MODE == kLayer ? -rs * (stats[4 * r + 2] * invN) : 0.f);
+          const float2 nrc = splat2(-rs * (stats[4 * r + 3] * invN));
           uint16_t *dxrow = a.out + (row0 + r) * a.N + seg * a.NS + t * 8;
 #pragma unroll
           for (int k = 0; k < K; ++k) {
@@ -368,9 +389,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
               float2 o[4];
 #pragma unroll
               for (int p = 0; p < 4; ++p) {
-                // dx = rstd * (g - (xhat * c + a))
-                const float2 uu = fma2(xh[k][p], cv, av);
-                o[p] = mul2(fma2(uu, neg1, gg[k][p]), rs2);
+                o[p] = fma2(xh[k][p], nrc,
+                            MODE == kLayer ? fma2(gg[k][p], rs2, nra) : mul2(gg[k][p], rs2));
                 accg[k][p] = fma2(df[k][p], xh[k][p], accg[k][p]);
                 if (MODE == kLayer) accb[k][p] = add2(accb[k][p], df[k][p]);
               }
@@ -387,7 +407,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_split_kernel(const NormAr
       if (next < u1) {
         if ((tid & 31) == 0) fence_proxy_async_smem();
         __syncwarp();
-        issue_unit<MODE, PHASE>(a, L, smem, next, s, pol);
+        UnitPos np = pos;
+        unit_advance(np, a.S, T);
+        issue_unit<MODE, PHASE>(a, L, smem, np, s, pol);
       }
     }
     if (++s == a.S) {
