@@ -619,8 +619,9 @@ norm_status_t split_shape(int mode, int phase, int64_t M, int N, int smem_optin,
     if (S >= 2 || rpg == 1 || ov.rpg) break;
     rpg = (rpg + 1) / 2;
   }
-  // three units in flight: measured the fastest of 2 to 8 for every pass
-  S = std::min(S, 3);
+  // units in flight: three (two for the dx pass, whose units hold x and dy
+  // and write dx), measured the fastest of 2 to 8 per pass
+  S = std::min(S, phase == kSplitBwdDx ? 2 : 3);
   const bool first = phase == kSplitFwdStats || phase == kSplitBwdDots;
   if (ov.S) S = ov.S;
   if (first && ov.S1) S = ov.S1;
