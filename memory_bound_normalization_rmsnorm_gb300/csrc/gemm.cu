@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint64_t pol_w = l2_evict_last_policy();
       int g = 0;  // K blocks issued by this CTA (all tiles)
       bool ok = true;
       const uint32_t full_rank0 = PAIR ? mapa_shared(full, 0) : 0u;
@@ -253,9 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(b_tiles + s * kBTile, &tm_w, kb * kBK, n0,
                              full_rank0 + uint32_t(s * 8));
           } else {
+            // W' tiles are read again by every row block: kept in L2 ahead
+            // of the x stream and of the output (written once, evict-first)
             mbar_arrive_expect_tx(&full[s], tx_bytes);
             tma_load_2d(a_tiles + s * kATile, &tm_x, kb * kBK, m0, &full[s]);
-            tma_load_2d(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s]);
+            tma_load_2d_hint(b_tiles + s * kBTile, &tm_w, kb * kBK, n0, &full[s], pol_w);
           }
         }
       }
@@ -439,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // q ^ (t % 8)), from which one thread writes the 128 x 64 box with a TMA
     // store; rows beyond M and columns beyond Nout are clipped by the store.
     const int t = threadIdx.x - kEpiWarp0 * 32;  // row of the tile = TMEM lane
+    const uint64_t pol_out = l2_evict_first_policy();
     const int quarter = warp - kEpiWarp0;        // == warp % 4: TMEM lanes 32q .. 32q + 31
     const uint32_t acc_empty_rank0 = PAIR ? mapa_shared(acc_empty, 0) : 0u;
     int mb, nb;
@@ -522,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();  // generic writes -> the store's async-proxy reads
         named_bar_sync(1, 128);
         if (t == 0 && m0 < M) {  // rank 1 of a pair may own no row of a short last tile
-          tma_store_2d(&tm_out, n, m0, sbuf);
+          tma_store_2d_hint(&tm_out, n, m0, sbuf, pol_out);
           bulk_commit();
         }
       }

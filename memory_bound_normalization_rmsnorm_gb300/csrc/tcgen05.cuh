@@ -29,6 +29,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int c0,
       : "memory");
 }
 
+// The same load with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const void *tmap, int c0, int c1,
+                                                 uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Stores the box at (c0, c1) of the tensor described by `tmap` from shared
 // memory at `src` (a bulk-group operation: commit, then wait).  Elements of
 // the box outside the tensor are not written.
@@ -38,6 +48,20 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, int c0, int c1, c
           reinterpret_cast<uint64_t>(tmap)),
       "r"(c0), "r"(c1), "r"(smem_addr(src))
       : "memory");
+}
+// The same store with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, int c0, int c1,
+                                                  const void *src, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(smem_addr(src)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
