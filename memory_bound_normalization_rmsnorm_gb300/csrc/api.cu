@@ -240,7 +240,8 @@ constexpr TunedPlan kTuned[] = {
 // number of stages that fit in shared memory (at least two).
 norm_status_t size_ring(Plan &p, bool bwd, int smem_optin, const Override &ov, int64_t M,
                         int s_cap = 0) {
-  const int ntensors = (bwd ? 2 : 1) + (p.resid ? 1 : 0);
+  // (the long-row fused residual backward reads dh into registers: not staged)
+  const int ntensors = (bwd ? 2 : 1) + (p.resid && !(bwd && p.long_rows) ? 1 : 0);
   const int C = p.C;
   int G = p.G;
   const int row_bytes = p.NS * 2;

@@ -393,12 +393,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
   }
 }
 
-// RESID: fused residual add -- the stage also holds dh (third tensor) and
-// dx = (norm backward at h) + dh, summed in fp32 and rounded once.
+// RESID: fused residual add -- dx = (norm backward at h) + dh, summed in
+// fp32 and rounded once.  dh is needed by the dx pass only, so it is not
+// staged: each thread loads its chunks of a row's dh into registers one step
+// ahead of that row's dx pass (before the dot pass without a cluster; after
+// the previous tile's push in a cluster), so the stage holds h and dy like
+// the plain backward and takes the same (narrower) clusters.
 template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, RESID ? 3 : 2, true, a.C);
+  const SmemLayout L = make_layout(a.RT, a.NS, a.S, a.G, a.tpr, 2, true, a.C);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
     for (int j = 0; j < a.S; ++j) {
       const int64_t tile = cid + j * ncl;
       if (tile < a.ntiles)
-        issue_bwd_tile<MODE, CLUSTER, RESID>(a, L, smem, tile, j, col0, nsc_me, pol);
+        issue_bwd_tile<MODE, CLUSTER, false>(a, L, smem, tile, j, col0, nsc_me, pol);
     }
   }
 
@@ -515,6 +519,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
     pb = v[1];
   };
 
+  // RESID: this thread's chunks of dh for the row whose dx pass comes next.
+  uint4 dhr[RESID ? K : 1];
+  auto load_dh = [&](int64_t row0, int r, bool active) {
+#pragma unroll
+    for (int k = 0; k < (RESID ? K : 0); ++k) {
+      const int c = t + k * a.tpr;
+      dhr[k] = (active && (EXACT || c < nsc_me))
+                   ? ld_global_nc_v4(a.res + (row0 + r) * a.N + col0 + c * 8)
+                   : make_uint4(0, 0, 0, 0);
+    }
+  };
+
   // dx pass of row slot r of stage s given the row totals.
   auto dx_pass = [&](int s, int64_t row0, int r, float tsum_g, float tsum_gx) {
     const unsigned char *xrow = smem + static_cast<size_t>(s) * L.stage_bytes +
@@ -544,7 +560,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
         }
         if (RESID) {
           float2 hf[4];
-          chunk_to_f2(lds_chunk(xrow + 2 * L.tensor_bytes + k * cstep), hf);
+          chunk_to_f2(dhr[RESID ? k : 0], hf);
 #pragma unroll
           for (int p = 0; p < 4; ++p) o[p] = add2(o[p], hf[p]);
         }
@@ -559,7 +575,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
       if (next < a.ntiles) {
         if ((tid & 31) == 0) fence_proxy_async_smem();
         __syncwarp();
-        issue_bwd_tile<MODE, CLUSTER, RESID>(a, L, smem, next, s, col0, nsc_me, pol);
+        issue_bwd_tile<MODE, CLUSTER, false>(a, L, smem, next, s, col0, nsc_me, pol);
       }
     }
   };
@@ -591,7 +607,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
       cur.c = 0.f;
       dot_pass(s, r, r < nrows, cur.a, cur.b);
       cluster_push(cur.a, cur.b, 0.f, r, t, xch);
-      if (have_pend) finish(pend);
+      if (have_pend) finish(pend);  // its dh arrived during this tile's dot pass
+      if (RESID) load_dh(row0, r, r < nrows);
       pend = cur;
       have_pend = true;
     } else {
@@ -599,6 +616,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_bwd_long_kernel(const Nor
         const int r = g + q * a.G;
         const bool active = r < nrows;
         float pa, pb;
+        if (RESID) load_dh(row0, r, active);  // in flight during the dot pass
         dot_pass(s, r, active, pa, pb);
         if (active) dx_pass(s, row0, r, pa, pb);
       }

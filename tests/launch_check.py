@@ -62,7 +62,8 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     assert K * tpr >= nsc, "a chunk has no owner"
     if p["exact"]:
         assert tpr % 32 == 0 and K * tpr == nsc and nc % C == 0, "EXACT plan is not exact"
-    ntensors = (2 if backward else 1) + (1 if residual else 0)
+    # the long-row fused residual backward keeps dh out of the stage
+    ntensors = (2 if backward else 1) + (1 if residual and not (backward and p["long_rows"]) else 0)
     par = p["param_smem_bytes"]
     nvec = 2 if mode == 1 else 1
     assert par == 0 or (not backward and p["exact"] and K in (5, 6, 8) and C == 1
