@@ -516,13 +516,32 @@ def plan_str(p):
     return s
 
 
+def cold_ms(fn, flush, stream, reps):
+    """Median time of one call with L2 flushed before it: a buffer larger
+    than L2 is written, then CUDA events bracket the call alone."""
+    import torch
+
+    times = []
+    for i in range(reps):
+        flush.fill_(i & 0xff)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
 def measure_workload(gb, w, peak, seconds=0.15, warmup=3, steps=0, fused=False, fp8=None,
-                     fwd_only=False, sampler=None):
+                     fwd_only=False, sampler=None, flush=None, cold_reps=15):
     """Forward, backward and whole-step (forward then backward) throughput of
     one workload: CUDA events around back-to-back calls of each on the
     current stream, inputs resident in HBM (larger than L2 except for the
     1 MB case).  `steps` > 0 fixes the call count, else about `seconds` of
-    calls per measurement."""
+    calls per measurement.  With `flush` (a buffer larger than L2) also the
+    median of `cold_reps` calls each run after L2 was flushed."""
     import torch
 
     from memory_bound_normalization_rmsnorm_gb300 import workloads as wl
@@ -542,7 +561,7 @@ def measure_workload(gb, w, peak, seconds=0.15, warmup=3, steps=0, fused=False, 
 
     passes = [("fwd", step.fwd)] if fwd_only else [("fwd", step.fwd), ("bwd", step.bwd),
                                                     ("step", both)]
-    res = {}
+    res, cold = {}, {}
     t0 = time.time()
     for name, fn in passes:
         for _ in range(warmup):
@@ -551,6 +570,9 @@ def measure_workload(gb, w, peak, seconds=0.15, warmup=3, steps=0, fused=False, 
         res[name] = timed_loop(fn, n, stream)
         res[name + "_iters"] = n
     t1 = time.time()
+    if flush is not None:
+        for name, fn in passes:
+            cold[name] = cold_ms(fn, flush, stream, cold_reps)
     if gb.norm_get_device_error() != 0:
         raise RuntimeError(f"device error word set on {w.name}")
     P = 0 if pb is None else pb["partials"]
@@ -567,6 +589,10 @@ def measure_workload(gb, w, peak, seconds=0.15, warmup=3, steps=0, fused=False, 
                     "step_frac": (fb + bb) / res["step"] / 1e6 / peak,
                     "plan_bwd": plan_str(pb), "partials": pb["partials"]})
     out["iters"] = {k[:-6]: v for k, v in res.items() if k.endswith("_iters")}
+    if cold:
+        nb = {"fwd": fb, "bwd": bb, "step": fb + bb}
+        out["cold"] = {f"{k}_frac": nb[k] / ms / 1e6 / peak for k, ms in cold.items()}
+        out["cold"]["reps"] = cold_reps
     if sampler is not None:
         out["window"] = (t0, t1)
     del step, x, g, b, dy, r, dh
@@ -672,8 +698,9 @@ def run_ours(args):
     sweep = None
     if world == 1 and not args.no_sweep:
         sweep = []
+        flush = None if args.no_cold else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         for name in wl.ALL:
-            e = measure_workload(gb, wl.ALL[name], peak, sampler=sampler)
+            e = measure_workload(gb, wl.ALL[name], peak, sampler=sampler, flush=flush)
             if name in wl.WIDE:
                 e["beyond_configs"] = "rows wider than one cluster holds (two-pass path)"
             sweep.append(e)
