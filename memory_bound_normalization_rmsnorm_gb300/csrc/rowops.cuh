@@ -63,67 +63,17 @@ __device__ __forceinline__ void group_sum(float (&v)[NV], int tpr, int g, int G,
   if (tpr > 32) {
     const int W = tpr >> 5;
     float *slot = red + (static_cast<size_t>(rpar * G + g) * W) * 4;
-    if (NV <= 2) {
-      // Warp w's values packed at slot[w * NV + i] and read back four at a
-      // time, still added in warp order (same bits as one load per value).
-      if ((threadIdx.x & 31) == 0) {
+    if ((threadIdx.x & 31) == 0) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) slot[(t >> 5) * NV + i] = v[i];
-      }
-      named_bar_sync(1 + g, tpr);
-      const float4 *s4 = reinterpret_cast<const float4 *>(slot);
-      float4 c = s4[0];
-      if (NV == 1) {
-        float a = c.x;
-        if (W > 1) a += c.y;
-        if (W > 2) a += c.z;
-        if (W > 3) a += c.w;
-        for (int q = 1; q < (W >> 2); ++q) {
-          c = s4[q];
-          a += c.x;
-          a += c.y;
-          a += c.z;
-          a += c.w;
-        }
-        if (W > 4 && (W & 3)) {
-          c = s4[W >> 2];
-          a += c.x;
-          if ((W & 3) > 1) a += c.y;
-          if ((W & 3) > 2) a += c.z;
-        }
-        v[0] = a;
-      } else {
-        float a0 = c.x, a1 = c.y;
-        a0 += c.z;  // W >= 2
-        a1 += c.w;
-        for (int q = 1; q < (W >> 1); ++q) {
-          c = s4[q];
-          a0 += c.x;
-          a1 += c.y;
-          a0 += c.z;
-          a1 += c.w;
-        }
-        if (W & 1) {
-          c = s4[W >> 1];
-          a0 += c.x;
-          a1 += c.y;
-        }
-        v[0] = a0;
-        v[NV > 1 ? 1 : 0] = a1;
-      }
-    } else {
-      if ((threadIdx.x & 31) == 0) {
+      for (int i = 0; i < NV; ++i) slot[(t >> 5) * 4 + i] = v[i];
+    }
+    named_bar_sync(1 + g, tpr);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) slot[(t >> 5) * 4 + i] = v[i];
-      }
-      named_bar_sync(1 + g, tpr);
-#pragma unroll
-      for (int i = 0; i < NV; ++i) v[i] = slot[i];
+    for (int i = 0; i < NV; ++i) v[i] = slot[i];
 #pragma unroll 4
-      for (int w = 1; w < W; ++w) {
+    for (int w = 1; w < W; ++w) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] += slot[w * 4 + i];
-      }
+      for (int i = 0; i < NV; ++i) v[i] += slot[w * 4 + i];
     }
     rpar ^= 1;
   }
@@ -319,21 +269,15 @@ __device__ __forceinline__ const float *cluster_exchange(float a, float b, float
   return cluster_wait_row(r, x, err, abort);
 }
 
-// Rank-order sums of the first NV floats of the C slots of a row (each
-// slot one 16-byte word, read whole).
+// Rank-order sums of the first NV floats of the C slots of a row.
 template <int NV>
 __device__ __forceinline__ void fold_sum(const float *row, int C, float (&v)[NV]) {
-  const float4 *r4 = reinterpret_cast<const float4 *>(row);
-  float4 c = r4[0];
-  float acc[3] = {c.x, c.y, c.z};
-  for (int q = 1; q < C; ++q) {
-    c = r4[q];
-    acc[0] += c.x;
-    if (NV > 1) acc[1] += c.y;
-    if (NV > 2) acc[2] += c.z;
-  }
 #pragma unroll
-  for (int i = 0; i < NV; ++i) v[i] = acc[i];
+  for (int i = 0; i < NV; ++i) {
+    float acc = row[i];
+    for (int q = 1; q < C; ++q) acc += row[q * 4 + i];
+    v[i] = acc;
+  }
 }
 
 // Sum of NV <= 3 values over the C CTAs, added in rank order.
