@@ -44,7 +44,8 @@ def test_forced_two_pass_small(mode, M, N, monkeypatch):
     pu.compare(mode, case.eps, x, g, b, dy, outs, label=f"split {mode}:{M}x{N}")
 
 
-WIDE = [(3, 262152), (6, 524288), (5, 1048576), (2, 300008), (4, 262144 + 4096 * 3 + 8)]
+WIDE = [(3, 262152), (6, 524288), (5, 1048576), (2, 300008), (4, 262144 + 4096 * 3 + 8),
+        (2, 1 << 24)]  # the widest row the library takes (NORM_MAX_N): 4096 segments
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
