@@ -513,6 +513,8 @@ def plan_str(p):
         s += " gsm"
     if p.get("split_segments"):
         s += f" split{p['split_segments']}"
+    if p.get("streamed"):
+        s += " stream"
     return s
 
 

@@ -321,6 +321,12 @@ typedef struct {
                                   dx (backward) pass, whose rows_per_tile
                                   rows of one segment make a unit, `tiles`
                                   counting the row tiles; 0 otherwise */
+    int32_t streamed;          /* backward only: 1 when the row slices
+                                  (cols_per_cta columns each) are streamed
+                                  twice through shared memory -- dot
+                                  products, then dx, the second read served
+                                  from L2 -- with the dgamma / dbeta column
+                                  sums held in tensor memory; 0 otherwise */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

@@ -25,7 +25,7 @@ OUT_DIR = os.path.join(PKG, "lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgbnorm.so")
 SOURCES = ["fwd.cu", "fwd_fp8.cu", "fwd_gsm.cu", "bwd.cu", "long.cu", "long_resid.cu",
-           "long_fp8.cu", "split.cu", "api.cu", "host.cu", "gemm.cu"]
+           "long_fp8.cu", "split.cu", "stream.cu", "api.cu", "host.cu", "gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -159,6 +159,7 @@ struct Override {
   int split = -1;  // 1: the two-pass path at any N; 0: never
   int W = 0;       // two-pass path: segment width (a multiple of 1024)
   int S1 = 0, S2 = 0;  // two-pass path: stages of its first / second pass
+  int stream = -1;     // backward: 1 the streaming long-row kernel where it applies, 0 never
   bool any = false;
 };
 
@@ -192,6 +193,7 @@ Override read_override() {
     else if (!std::strcmp(key, "W")) o.W = val;
     else if (!std::strcmp(key, "S1")) o.S1 = val;
     else if (!std::strcmp(key, "S2")) o.S2 = val;
+    else if (!std::strcmp(key, "stream")) o.stream = val;
     o.any = true;
   }
   return o;
@@ -332,6 +334,46 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
   }
 }
 
+// Plan for the streaming long-row backward (stream.cu): rows of N = C x
+// kStreamSlice columns, a cluster of C CTAs per row (one CTA when C = 1),
+// one row group of kStreamThreads threads per CTA and S pieces in flight.
+constexpr int kStreamStages = 6;
+
+bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <= 16; }
+
+// Whether the backward of rows of N columns takes the streaming kernel.
+bool use_stream(int N, const Override &ov) {
+  return stream_applies(N) && ov.stream == 1;
+}
+
+norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, Plan *out) {
+  if (!stream_applies(N)) return NORM_ERR_UNSUPPORTED;
+  const int C = N / kStreamSlice;
+  if (ov.C && ov.C != C) return NORM_ERR_UNSUPPORTED;
+  Plan p;
+  p.stream = true;
+  p.C = C;
+  p.NS = kStreamSlice;
+  p.nsc = kStreamSlice / 8;
+  p.tpr = kStreamThreads;
+  p.K = p.nsc / kStreamThreads;
+  p.exact = true;
+  p.G = 1;
+  p.rpg = 1;
+  p.RT = 1;
+  p.threads = kStreamThreads;
+  const int64_t budget = smem_optin - 1024;
+  int S = ov.S ? ov.S : kStreamStages;
+  while (!ov.S && S > 2 && static_cast<int64_t>(stream_layout(S, C).total) > budget) --S;
+  if (S < 2 || static_cast<int64_t>(stream_layout(S, C).total) > budget)
+    return NORM_ERR_UNSUPPORTED;
+  p.S = S;
+  p.smem = stream_layout(S, C).total;
+  p.ntiles = M;
+  *out = p;
+  return NORM_OK;
+}
+
 // Shape part of the plan for one pass: everything except the grid size.
 // Pure host arithmetic (no CUDA call).  `bwd` selects the backward kernel
 // (two tensors per stage, at most kMaxKBwd chunks per thread).
@@ -353,6 +395,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
       }
     }
   }
+  if (bwd && !resid && use_stream(N, ov)) return stream_plan(M, N, smem_optin, ov, out);
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
   const int nc = N / 8;
   Plan p;
@@ -487,6 +530,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
   if (p.split) return split_kernel_ptr(mode, p.phase, p.K);
+  if (p.stream) return stream_kernel_ptr(mode, p.C > 1);
   if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.resid);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm);
@@ -583,7 +627,8 @@ norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, cons
 // units in flight, and a persistent grid of at most one CTA per unit.
 constexpr int kSplitW = 4096;
 
-bool use_split(int N, const Override &ov) {
+bool use_split(int N, const Override &ov, bool bwd = false) {
+  if (bwd && use_stream(N, ov)) return false;
   return ov.split == 1 || (ov.split != 0 && N > NORM_MAX_N_ONEPASS);
 }
 
@@ -855,6 +900,7 @@ void fill_plan(const Plan &p, norm_plan_t *out) {
   out->long_rows = p.long_rows ? 1 : 0;
   out->param_smem_bytes = p.par_bpc * p.NS;
   out->split_segments = p.split ? p.nseg : 0;
+  out->streamed = p.stream ? 1 : 0;
 }
 
 // ------------------------------------------------------------ plan tuning
@@ -921,7 +967,8 @@ std::vector<Override> tune_candidates(bool bwd, int N) {
 
 bool same_plan(const Plan &a, const Plan &b) {
   return a.C == b.C && a.tpr == b.tpr && a.K == b.K && a.G == b.G && a.rpg == b.rpg &&
-         a.S == b.S && a.gsm == b.gsm && a.long_rows == b.long_rows && a.grid == b.grid;
+         a.S == b.S && a.gsm == b.gsm && a.long_rows == b.long_rows && a.grid == b.grid &&
+         a.stream == b.stream;
 }
 
 // Times `run` (one launch of the pass with the plan installed in the cache
@@ -933,7 +980,7 @@ norm_status_t tune_pass(int mode, bool bwd, int64_t M, int N, size_t ws_bytes, i
   if (read_override().any) return NORM_ERR_ARG;  // a plan override bypasses the cache
   norm_status_t st = run();                      // validates, caches the default plan
   if (st != NORM_OK) return st;
-  if (use_split(N, Override())) {  // the two-pass path keeps its plan
+  if (use_split(N, Override(), bwd)) {  // the two-pass path keeps its plan
     if (chosen) {
       norm_plan_t pl;
       if ((st = norm_plan(M, N, static_cast<norm_mode_t>(mode), bwd ? 1 : 0, 0, 0, &pl)) !=
@@ -1096,7 +1143,7 @@ norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, s
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
-  if (use_split(static_cast<int>(N), read_override())) {
+  if (use_split(static_cast<int>(N), read_override(), true)) {
     Plan sp[2];
     if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
       return st;
@@ -1128,7 +1175,7 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (use_split(static_cast<int>(N), read_override())) {
+  if (use_split(static_cast<int>(N), read_override(), true)) {
     Plan sp[2];
     if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
       return st;
@@ -1326,7 +1373,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   if ((resid || fp8) && N > NORM_MAX_N_FUSED) return NORM_ERR_SHAPE;
   Plan p;
   const Override ov = read_override();
-  if (!resid && !fp8 && use_split(static_cast<int>(N), ov)) {
+  if (!resid && !fp8 && use_split(static_cast<int>(N), ov, bwd)) {
     // the two-pass path: its statistics (forward) or dx (backward) pass,
     // or with bit 3 the output (forward) or dot-product (backward) pass
     const int phase = bwd ? (other ? kSplitBwdDots : kSplitBwdDx)

@@ -132,6 +132,7 @@ struct Plan {
   bool split = false;  // two-pass path: rows cut into nseg segments of NS columns
   int nseg = 0;
   int phase = 0;       // two-pass path: which of its passes (kSplit*)
+  bool stream = false; // backward: the streaming long-row kernel (stream.cu)
 };
 
 // Kernel entry points, by (mode, K, cluster, exact, fused residual).
@@ -186,5 +187,39 @@ const void *split_kernel_ptr(int mode, int phase, int K);
 const void *split_fold_kernel_ptr(int mode, bool bwd);
 const void *split_reduce_kernel_ptr();
 SmemLayout split_smem_layout(int RT, int NS, int S, int G, int tpr, int ntensors);
+
+// The streaming long-row backward (stream.cu): one row group of
+// kStreamThreads threads per CTA, each CTA owning kStreamSlice columns of a
+// row (a cluster of N / kStreamSlice CTAs), streamed twice through a ring of
+// pieces of kStreamPiece columns (kStreamKP chunks per thread).
+constexpr int kStreamThreads = 512;
+constexpr int kStreamKP = 2;
+constexpr int kStreamPiece = kStreamThreads * kStreamKP * 8;
+constexpr int kStreamSlice = 4 * kStreamPiece;
+// Its shared memory: S stages of one piece of x and dy, the cross-warp
+// scratch of the row sums, the cluster exchange slots (C > 1), the stage
+// mbarriers, then the abort flag, the per-stage warp counters and the
+// tensor-memory address slot.
+__host__ __device__ inline SmemLayout stream_layout(int S, int C) {
+  SmemLayout L;
+  L.tensor_bytes = static_cast<uint32_t>(kStreamPiece) * 2u;
+  L.stage_bytes = 2u * L.tensor_bytes;
+  uint32_t off = L.stage_bytes * static_cast<uint32_t>(S);
+  L.par_off = off;
+  L.stats_off = off;
+  L.red_off = off;
+  off = align16(off + static_cast<uint32_t>(2 * (kStreamThreads / 32) * 4) * 4u);
+  L.xch_off = off;
+  if (C > 1)
+    off = align16(off + static_cast<uint32_t>(kXchBuffers * C * 4) * 4u + 8u * kXchBuffers);
+  L.bar_off = off;
+  off = align16(off + static_cast<uint32_t>(S) * 8u);
+  L.flag_off = off;
+  off = align16(off + 4u + 4u * static_cast<uint32_t>(S) + 4u);
+  L.total = off;
+  return L;
+}
+// Kernel by (mode, cluster or single CTA).
+const void *stream_kernel_ptr(int mode, bool cluster);
 
 }  // namespace gbn

@@ -1,0 +1,394 @@
+// stream.cu -- the streaming long-row backward: rows of 32768 columns per
+// CTA (a cluster of C = N / 32768 CTAs per row), each row slice streamed
+// through a shared-memory ring twice -- once for the per-row dot products,
+// once for dx -- instead of being held in shared memory, with the dgamma /
+// dbeta column sums accumulated in tensor memory (TMEM).
+//
+// "PyTorch atinge desempenho SOTA em normalizacao com torch.compile"
+// (matsubara.tec.br) places the backward's difficulty at very large
+// dimensions: a row no longer fits on chip, and a kernel that keeps its
+// slice resident needs so many CTAs per row that whole clusters stop
+// fitting on the GPU's processor clusters (at 131072 columns the resident
+// long-row backward needs clusters of 8 CTAs, of which 15 fit: 120 of 152
+// SMs).  Here a CTA keeps on chip only what a row does not need twice: the
+// packed gamma of its slice (registers) and the column accumulators (TMEM,
+// 128 KB for RMSNorm, 256 KB with dbeta).  Its 32768-column slice of x and
+// dy passes through a ring of 8192-column pieces:
+//
+//   pass 1 (row j)    sum g and sum g (x - mean) over the slice (g = dy *
+//                     gamma), summed over the CTA, then over the cluster
+//                     (DSMEM exchange, the same rank-order fold as the
+//                     resident long-row kernel); x and dy come from HBM;
+//   pass 2 (row j-1)  dx = rstd g - rstd a - rstd^2 c (x - mean) with the
+//                     row totals, and dgamma += dy xhat, dbeta += dy read,
+//                     updated and written back in TMEM; x and dy come again
+//                     -- from L2, where pass 1 left them one row earlier.
+//
+// The pieces are issued in the order pass 1 of row j, pass 2 of row j-1, so
+// the cross-CTA exchange of row j-1 completes while row j streams in, and
+// the L2 holds about two slices per CTA between their two reads (~40 MB on
+// the whole GPU at 131072 columns).  The column sums leave TMEM once, at the
+// end, as this cluster's partial row of the workspace; the fixed-order
+// reduce kernel adds the partial rows as for the other backward kernels, so
+// results stay bitwise reproducible.
+#include "common.cuh"
+#include "ptx.cuh"
+#include "rowops.cuh"
+#include "tcgen05.cuh"
+
+namespace gbn {
+
+namespace {
+
+constexpr int kKP = kStreamKP;   // 16-byte chunks per thread per piece
+constexpr int kW = kStreamPiece;  // piece width (columns)
+static_assert(kW == kStreamThreads * kKP * 8, "piece = threads x chunks x 8 columns");
+
+// L2 policy of pass 1's reads (their data is read again by pass 2).
+__device__ __forceinline__ uint64_t l2_normal_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint4 lds_v4(const unsigned char *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+// Piece q of a CTA's sequence over its nr rows (np pieces per slice):
+// pass 1 of row 0, then for j = 1 .. nr-1 pass 1 of row j and pass 2 of
+// row j-1, then pass 2 of row nr-1.
+__device__ __forceinline__ void piece_at(int64_t q, int np, int64_t nr, int &pass, int64_t &j,
+                                         int &p) {
+  if (q < np) {
+    pass = 0;
+    j = 0;
+    p = static_cast<int>(q);
+    return;
+  }
+  const int64_t q2 = q - np;
+  const int64_t b = q2 / (2 * np);
+  const int w = static_cast<int>(q2 - b * 2 * np);
+  if (b < nr - 1) {
+    if (w < np) {
+      pass = 0;
+      j = b + 1;
+      p = w;
+    } else {
+      pass = 1;
+      j = b;
+      p = w - np;
+    }
+  } else {
+    pass = 1;
+    j = nr - 1;
+    p = w;
+  }
+}
+
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// One CTA per (row, 32768-column slice); NP pieces of kW columns per slice.
+template <int MODE, int NP, bool CLUSTER>
+__global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(const NormArgs a) {
+  constexpr int NACC = MODE == kLayer ? 2 : 1;          // dgamma (and dbeta)
+  constexpr int CPC = 8 * NACC;                          // TMEM columns per chunk
+  constexpr int TCW = NP * kKP * CPC;                    // columns per warp quarter group
+  constexpr uint32_t kCols = pow2_at_least(4 * TCW);     // 16 warps: 4 per lane quarter
+  static_assert(4 * TCW <= 512, "accumulators exceed tensor memory");
+  constexpr int kNW = kStreamThreads / 32;
+  constexpr int kStride = kStreamThreads * 16;           // bytes between a thread's chunks
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+  float *red = reinterpret_cast<float *>(smem + L.red_off);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.flag_off) + 1 + a.S;
+
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
+  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
+  const int64_t col0 = static_cast<int64_t>(crank) * a.NS;
+  const int64_t nr = cid < a.M ? (a.M - cid + ncl - 1) / ncl : 0;  // rows of this cluster
+  const int64_t total = 2 * NP * nr;                                 // pieces
+
+  if (t == 0) {
+    for (int s = 0; s < a.S; ++s) {
+      mbar_init(full + s, 1);
+      done_cnt[s] = 0;
+    }
+    if (CLUSTER) {
+      uint64_t *xb = xch_bars(smem, L, 1, a.C);
+      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  // Programmatic dependent launch: no global access before the previous
+  // kernel's writes are visible.
+  grid_launch_dependents();
+  grid_dependency_wait();
+
+  // This thread's chunks of gamma: piece p, chunk k at column
+  // col0 + p * kW + (k * threads + t) * 8.
+  uint4 gv[NP][kKP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p)
+#pragma unroll
+    for (int k = 0; k < kKP; ++k)
+      gv[p][k] = ld_global_nc_v4(a.gamma + col0 + p * kW + (k * kStreamThreads + t) * 8);
+
+  tc_fence_before();
+  if (CLUSTER) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  // Warp w reaches TMEM lanes 32 (w % 4) ..; the four warps sharing them
+  // take consecutive groups of TCW columns.
+  const uint32_t tq = *tmem_slot + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                      static_cast<uint32_t>((warp >> 2) * TCW);
+  {
+    uint32_t z[CPC];
+#pragma unroll
+    for (int i = 0; i < CPC; ++i) z[i] = 0u;
+#pragma unroll
+    for (int c = 0; c < NP * kKP; ++c) tmem_st_n<CPC>(tq + c * CPC, z);
+  }
+
+  const uint64_t pol1 = l2_normal_policy();
+  const uint64_t pol2 = l2_evict_first_policy();
+  // Issues piece q of the sequence into stage s (one thread).
+  auto issue = [&](int64_t q, int s) {
+    int pass, p;
+    int64_t j;
+    piece_at(q, NP, nr, pass, j, p);
+    const int64_t off = (cid + j * ncl) * a.N + col0 + static_cast<int64_t>(p) * kW;
+    uint64_t *bar = full + s;
+    unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
+    const uint64_t pol = pass ? pol2 : pol1;
+    mbar_arrive_expect_tx(bar, L.stage_bytes);
+    bulk_g2s(dst, a.x + off, L.tensor_bytes, bar, pol);
+    bulk_g2s(dst + L.tensor_bytes, a.dy + off, L.tensor_bytes, bar, pol);
+  };
+  if (t == 0) {
+    for (int64_t q = 0; q < total && q < a.S; ++q) issue(q, static_cast<int>(q));
+  }
+  // After every warp has read stage s for piece q, the last one refills it
+  // with piece q + S.
+  auto release = [&](int64_t q, int s) {
+    if (last_warp_done(done_cnt, s, kNW)) {
+      const int64_t next = q + a.S;
+      if (next < total && (t & 31) == 0) {
+        fence_proxy_async_smem();
+        issue(next, s);
+      }
+    }
+  };
+
+  auto load_stats = [&](int64_t j, float &rs, float &mu) {
+    rs = 0.f;
+    mu = 0.f;
+    if (j < nr) {
+      const int64_t row = cid + j * ncl;
+      rs = __ldg(a.rstd + row);
+      if (MODE == kLayer) mu = __ldg(a.mean + row);
+    }
+  };
+
+  ClusterXch xch = make_xch(smem, L, 1, CLUSTER ? a.C : 1, crank);
+  const float invN = a.invN;
+  int rpar = 0;
+  int s = 0;
+  uint32_t par = 0;
+  int64_t q = 0;
+  auto advance = [&]() {
+    ++q;
+    if (++s == a.S) {
+      s = 0;
+      par ^= 1u;
+    }
+  };
+  float rs_prev = 0.f, mu_prev = 0.f, rs_cur, mu_cur, rs_next, mu_next;
+  load_stats(0, rs_cur, mu_cur);
+  load_stats(1, rs_next, mu_next);
+  float tot_a = 0.f, tot_b = 0.f;  // without a cluster: row j's totals for its pass 2
+
+  for (int64_t j = 0; j <= nr; ++j) {
+    float cur_a = 0.f, cur_b = 0.f;
+    if (j < nr) {
+      // ---- pass 1 of row j: sum g and sum g (x - mean) over the slice
+      const float2 nmu = splat2(-mu_cur);
+      float2 s1 = splat2(0.f), s2 = splat2(0.f), s1b = splat2(0.f), s2b = splat2(0.f);
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        mbar_wait(full + s, par, a.err, abort_flag);
+        const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes + t * 16;
+#pragma unroll
+        for (int k = 0; k < kKP; ++k) {
+          float2 xf[4], df[4], gf[4];
+          chunk_to_f2(lds_v4(st + k * kStride), xf);
+          chunk_to_f2(lds_v4(st + L.tensor_bytes + k * kStride), df);
+          chunk_to_f2(gv[p][k], gf);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 gg = mul2(df[e], gf[e]);
+            const float2 xc = MODE == kLayer ? add2(xf[e], nmu) : xf[e];
+            if (e & 1) {
+              s2b = fma2(gg, xc, s2b);
+              if (MODE == kLayer) s1b = add2(s1b, gg);
+            } else {
+              s2 = fma2(gg, xc, s2);
+              if (MODE == kLayer) s1 = add2(s1, gg);
+            }
+          }
+        }
+        release(q, s);
+        advance();
+      }
+      s1 = add2(s1, s1b);
+      s2 = add2(s2, s2b);
+      float v[2] = {s1.x + s1.y, s2.x + s2.y};
+      if (MODE == kLayer) {
+        group_sum<2, true>(v, kStreamThreads, 0, 1, t, red, rpar);
+      } else {
+        float w1[1] = {v[1]};
+        group_sum<1, true>(w1, kStreamThreads, 0, 1, t, red, rpar);
+        v[1] = w1[0];
+      }
+      if (CLUSTER) cluster_push(v[0], v[1], 0.f, 0, t, xch);
+      cur_a = v[0];
+      cur_b = v[1];
+    }
+    if (j >= 1) {
+      // ---- pass 2 of row j - 1: dx and the column sums
+      float A = tot_a, U = tot_b;
+      if (CLUSTER) {
+        const float *row = cluster_wait_row(0, xch, a.err, abort_flag);
+        float v[2];
+        fold_sum<2>(row, xch.C, v);
+        A = v[0];
+        U = v[1];
+      }
+      const float rs = rs_prev;
+      // c = mean(g xhat) = rstd U / N; dx = rstd g - rstd a - rstd^2 c (x - mean)
+      const float chat = rs * (U * invN);
+      const float2 nk1 = splat2(-(rs * rs) * chat);
+      const float2 nra = splat2(MODE == kLayer ? -rs * (A * invN) : 0.f);
+      const float2 rs2 = splat2(rs), nmu = splat2(-mu_prev);
+      uint16_t *dxrow = a.out + (cid + (j - 1) * ncl) * a.N + col0 + t * 8;
+      __syncwarp();
+      tmem_wait_st();  // the previous pass 2's accumulator stores are complete
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        uint32_t acc[kKP * CPC];
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < kKP; ++k)
+          tmem_ld_n<CPC>(tq + (p * kKP + k) * CPC,
+                         *reinterpret_cast<uint32_t(*)[CPC]>(acc + k * CPC));
+        mbar_wait(full + s, par, a.err, abort_flag);
+        __syncwarp();
+        if constexpr (kKP * CPC == 16) {
+          tmem_wait_ld_n<16>(*reinterpret_cast<uint32_t(*)[16]>(acc));
+        } else {
+          tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(acc));
+        }
+        const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes + t * 16;
+#pragma unroll
+        for (int k = 0; k < kKP; ++k) {
+          float2 xf[4], df[4], gf[4], o[4];
+          chunk_to_f2(lds_v4(st + k * kStride), xf);
+          chunk_to_f2(lds_v4(st + L.tensor_bytes + k * kStride), df);
+          chunk_to_f2(gv[p][k], gf);
+          uint32_t *ak = acc + k * CPC;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 gg = mul2(df[e], gf[e]);
+            const float2 xc = MODE == kLayer ? add2(xf[e], nmu) : xf[e];
+            o[e] = fma2(xc, nk1, MODE == kLayer ? fma2(gg, rs2, nra) : mul2(gg, rs2));
+            const float2 xh = mul2(xc, rs2);
+            float2 ag = make_float2(__uint_as_float(ak[2 * e]), __uint_as_float(ak[2 * e + 1]));
+            ag = fma2(df[e], xh, ag);
+            ak[2 * e] = __float_as_uint(ag.x);
+            ak[2 * e + 1] = __float_as_uint(ag.y);
+            if (MODE == kLayer) {
+              float2 ab = make_float2(__uint_as_float(ak[8 + 2 * e]),
+                                      __uint_as_float(ak[8 + 2 * e + 1]));
+              ab = add2(ab, df[e]);
+              ak[8 + 2 * e] = __float_as_uint(ab.x);
+              ak[8 + 2 * e + 1] = __float_as_uint(ab.y);
+            }
+          }
+          st_global_cs_v4(dxrow + p * kW + k * kStreamThreads * 8, f2_to_chunk(o));
+        }
+#pragma unroll
+        for (int k = 0; k < kKP; ++k)
+          tmem_st_n<CPC>(tq + (p * kKP + k) * CPC,
+                         *reinterpret_cast<const uint32_t(*)[CPC]>(acc + k * CPC));
+        release(q, s);
+        advance();
+      }
+    }
+    tot_a = cur_a;
+    tot_b = cur_b;
+    rs_prev = rs_cur;
+    mu_prev = mu_cur;
+    rs_cur = rs_next;
+    mu_cur = mu_next;
+    load_stats(j + 2, rs_next, mu_next);
+  }
+
+  // This cluster's partial row of the workspace: [P][N] dgamma, then
+  // [P][N] dbeta (LayerNorm).
+  __syncwarp();
+  tmem_wait_st();
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+#pragma unroll
+    for (int k = 0; k < kKP; ++k) {
+      uint32_t acc[CPC];
+      __syncwarp();
+      tmem_ld_n<CPC>(tq + (p * kKP + k) * CPC, acc);
+      tmem_wait_ld_n<CPC>(acc);
+      const int64_t col = col0 + p * kW + (k * kStreamThreads + t) * 8;
+#pragma unroll
+      for (int w = 0; w < NACC; ++w) {
+        float4 *dst = reinterpret_cast<float4 *>(a.ws + (w * a.P + cid) * a.N + col);
+        dst[0] = make_float4(__uint_as_float(acc[8 * w + 0]), __uint_as_float(acc[8 * w + 1]),
+                             __uint_as_float(acc[8 * w + 2]), __uint_as_float(acc[8 * w + 3]));
+        dst[1] = make_float4(__uint_as_float(acc[8 * w + 4]), __uint_as_float(acc[8 * w + 5]),
+                             __uint_as_float(acc[8 * w + 6]), __uint_as_float(acc[8 * w + 7]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*tmem_slot, kCols);
+  }
+  if (CLUSTER) cluster_sync();
+}
+
+}  // namespace
+
+const void *stream_kernel_ptr(int mode, bool cluster) {
+  constexpr int NP = kStreamSlice / kW;
+  if (mode == kLayer)
+    return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kLayer, NP, true>)
+                   : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kLayer, NP, false>);
+  return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kRMS, NP, true>)
+                 : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kRMS, NP, false>);
+}
+
+}  // namespace gbn
