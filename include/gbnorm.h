@@ -445,8 +445,12 @@ norm_status_t norm_tune_reset(void);
  * array until the process exits.  It calls no allocation routine.
  *
  *   - The scratch need is norm_bwd_workspace_bytes(M, N, mode) (the number
- *     of partial rows times N times 4 bytes, twice for LAYER); a shape
- *     whose need exceeds NORM_NOALLOC_WORKSPACE_BYTES is rejected with
+ *     of partial rows times N times 4 bytes, twice for LAYER).  Where the
+ *     plan norm_bwd takes is the streaming long-row kernel (norm_plan's
+ *     `streamed`, one partial row per cluster) and its need exceeds the
+ *     array, this entry point runs the resident long-row plan instead (the
+ *     plan norm_bwd takes under GBNORM_PLAN=stream=0); a shape whose need
+ *     still exceeds NORM_NOALLOC_WORKSPACE_BYTES is rejected with
  *     NORM_ERR_WORKSPACE before anything is launched.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.

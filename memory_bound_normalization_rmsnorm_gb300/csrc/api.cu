@@ -159,7 +159,8 @@ struct Override {
   int split = -1;  // 1: the two-pass path at any N; 0: never
   int W = 0;       // two-pass path: segment width (a multiple of 1024)
   int S1 = 0, S2 = 0;  // two-pass path: stages of its first / second pass
-  int stream = -1;     // backward: 1 the streaming long-row kernel where it applies, 0 never
+  int stream = -1;     // backward: 1 the streaming long-row kernel where it applies, 0 never,
+                       // -1 where it measured faster (stream_default)
   bool any = false;
 };
 
@@ -341,9 +342,28 @@ constexpr int kStreamStages = 6;
 
 bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <= 16; }
 
-// Whether the backward of rows of N columns takes the streaming kernel.
-bool use_stream(int N, const Override &ov) {
-  return stream_applies(N) && ov.stream == 1;
+// Row widths, in slices of kStreamSlice columns, where the streaming
+// backward measured faster on GB300 (1024 to 4096 rows) than the resident
+// long-row kernel or, beyond NORM_MAX_N_ONEPASS, the two-pass path:
+// 4 and 8 slices (the resident kernel's clusters of 8 and 16 occupy 120 and
+// 112 SMs; RMSNorm 74 -> 81 % and 66 -> 68 %, LayerNorm 62 -> 71 % and
+// 53 -> 59 % of measured), RMSNorm at 1 and 16 slices (87 -> 89.5 %,
+// 58.7 -> 59.9 %), LayerNorm at 2 (72.5 -> 73.5 %).  Elsewhere (RMSNorm at
+// 2 slices: 86.6 against 82.8 %; LayerNorm at 16: 58.0 against 52.6 %;
+// slice counts that are not powers of two) the other kernels stay.
+bool stream_default(int mode, int C) {
+  if (C == 4 || C == 8) return true;
+  if (mode == kRMS) return C == 1 || C == 16;
+  return C == 2;
+}
+
+// Whether the backward of rows of N columns takes the streaming kernel:
+// forced by the override stream=1, or by default where it measured faster
+// (not under other override fields, which pin the plan they describe).
+bool use_stream(int N, int mode, const Override &ov) {
+  if (!stream_applies(N) || ov.stream == 0) return false;
+  if (ov.stream == 1) return true;
+  return !ov.any && stream_default(mode, N / kStreamSlice);
 }
 
 norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, Plan *out) {
@@ -395,7 +415,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
       }
     }
   }
-  if (bwd && !resid && use_stream(N, ov)) return stream_plan(M, N, smem_optin, ov, out);
+  if (bwd && !resid && use_stream(N, mode, ov)) return stream_plan(M, N, smem_optin, ov, out);
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
   const int nc = N / 8;
   Plan p;
@@ -547,11 +567,15 @@ norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, cons
 
 // Full plan on the current device: shape part plus the occupancy-derived
 // grid (persistent: as many CTAs or clusters as can be resident at once).
+// `no_stream`: a backward plan without the streaming kernel (the resident
+// long-row kernel or the two-pass path instead; fewer partial rows).
 norm_status_t make_plan(const DeviceInfo &d, int dev, int mode, bool bwd, int64_t M, int N,
-                        Plan *out, bool resid = false, bool fp8 = false) {
-  const Override ov = read_override();
-  const auto key =
-      std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N, (resid ? 1 : 0) | (fp8 ? 2 : 0));
+                        Plan *out, bool resid = false, bool fp8 = false,
+                        bool no_stream = false) {
+  Override ov = read_override();
+  if (no_stream) ov.stream = 0;
+  const auto key = std::make_tuple(dev, mode * 2 + (bwd ? 1 : 0), M, N,
+                                   (resid ? 1 : 0) | (fp8 ? 2 : 0) | (no_stream ? 4 : 0));
   if (!ov.any) {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
@@ -627,8 +651,10 @@ norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, cons
 // units in flight, and a persistent grid of at most one CTA per unit.
 constexpr int kSplitW = 4096;
 
-bool use_split(int N, const Override &ov, bool bwd = false) {
-  if (bwd && use_stream(N, ov)) return false;
+// (`bwd_mode`: the mode of a backward pass, whose rows may take the
+// streaming kernel instead; -1 for a forward pass)
+bool use_split(int N, const Override &ov, int bwd_mode = -1) {
+  if (bwd_mode >= 0 && use_stream(N, bwd_mode, ov)) return false;
   return ov.split == 1 || (ov.split != 0 && N > NORM_MAX_N_ONEPASS);
 }
 
@@ -980,7 +1006,7 @@ norm_status_t tune_pass(int mode, bool bwd, int64_t M, int N, size_t ws_bytes, i
   if (read_override().any) return NORM_ERR_ARG;  // a plan override bypasses the cache
   norm_status_t st = run();                      // validates, caches the default plan
   if (st != NORM_OK) return st;
-  if (use_split(N, Override(), bwd)) {  // the two-pass path keeps its plan
+  if (use_split(N, Override(), bwd ? mode : -1)) {  // the two-pass path keeps its plan
     if (chosen) {
       norm_plan_t pl;
       if ((st = norm_plan(M, N, static_cast<norm_mode_t>(mode), bwd ? 1 : 0, 0, 0, &pl)) !=
@@ -1136,14 +1162,19 @@ norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64
   return launch(kernel_for(sp[1], mode, false), sp[1], b, s);
 }
 
-norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, size_t *bytes) {
+// Workspace of the backward's plan (`no_stream`: the plan without the
+// streaming kernel).
+static norm_status_t bwd_workspace(int64_t M, int64_t N, norm_mode_t mode, bool no_stream,
+                                   size_t *bytes) {
   if (!bytes) return NORM_ERR_NULL;
   norm_status_t st = check_common(M, N, mode);
   if (st != NORM_OK) return st;
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
-  if (use_split(static_cast<int>(N), read_override(), true)) {
+  Override ov = read_override();
+  if (no_stream) ov.stream = 0;
+  if (use_split(static_cast<int>(N), ov, mode)) {
     Plan sp[2];
     if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
       return st;
@@ -1151,16 +1182,22 @@ norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, s
     return NORM_OK;
   }
   Plan p;
-  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p, false, false,
+                      no_stream)) != NORM_OK)
+    return st;
   *bytes = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
            (mode == NORM_LAYER ? 2u : 1u);
   return NORM_OK;
 }
 
-norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
-                       const float *mean, int64_t M, int64_t N, norm_mode_t mode, void *dx,
-                       float *dgamma, float *dbeta, void *workspace, size_t workspace_bytes,
-                       norm_stream_t stream) {
+norm_status_t norm_bwd_workspace_bytes(int64_t M, int64_t N, norm_mode_t mode, size_t *bytes) {
+  return bwd_workspace(M, N, mode, false, bytes);
+}
+
+static norm_status_t bwd_run(const void *dy, const void *x, const void *gamma, const float *rstd,
+                             const float *mean, int64_t M, int64_t N, norm_mode_t mode,
+                             void *dx, float *dgamma, float *dbeta, void *workspace,
+                             size_t workspace_bytes, norm_stream_t stream, bool no_stream) {
   if (!dy || !x || !gamma || !rstd || !dx || !dgamma) return NORM_ERR_NULL;
   norm_status_t st = check_common(M, N, mode);
   if (st != NORM_OK) return st;
@@ -1175,7 +1212,9 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (use_split(static_cast<int>(N), read_override(), true)) {
+  Override ov = read_override();
+  if (no_stream) ov.stream = 0;
+  if (use_split(static_cast<int>(N), ov, mode)) {
     Plan sp[2];
     if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
       return st;
@@ -1205,7 +1244,9 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
                                s);
   }
   Plan p;
-  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p)) != NORM_OK) return st;
+  if ((st = make_plan(d, dev, mode, true, M, static_cast<int>(N), &p, false, false,
+                      no_stream)) != NORM_OK)
+    return st;
   const size_t need = static_cast<size_t>(p.P) * static_cast<size_t>(N) * sizeof(float) *
                       (mode == NORM_LAYER ? 2u : 1u);
   if (workspace_bytes < need) return NORM_ERR_WORKSPACE;
@@ -1222,6 +1263,14 @@ norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const f
 
   return launch_reduce(static_cast<const float *>(workspace), p.P, static_cast<int>(N), dgamma,
                        (mode == NORM_LAYER) ? dbeta : nullptr, s);
+}
+
+norm_status_t norm_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
+                       const float *mean, int64_t M, int64_t N, norm_mode_t mode, void *dx,
+                       float *dgamma, float *dbeta, void *workspace, size_t workspace_bytes,
+                       norm_stream_t stream) {
+  return bwd_run(dy, x, gamma, rstd, mean, M, N, mode, dx, dgamma, dbeta, workspace,
+                 workspace_bytes, stream, false);
 }
 
 norm_status_t norm_add_fwd(const void *x, const void *r, const void *gamma, const void *beta,
@@ -1373,7 +1422,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   if ((resid || fp8) && N > NORM_MAX_N_FUSED) return NORM_ERR_SHAPE;
   Plan p;
   const Override ov = read_override();
-  if (!resid && !fp8 && use_split(static_cast<int>(N), ov, bwd)) {
+  if (!resid && !fp8 && use_split(static_cast<int>(N), ov, bwd ? mode : -1)) {
     // the two-pass path: its statistics (forward) or dx (backward) pass,
     // or with bit 3 the output (forward) or dot-product (backward) pass
     const int phase = bwd ? (other ? kSplitBwdDots : kSplitBwdDx)
@@ -1451,10 +1500,18 @@ norm_status_t norm_bwd_noalloc(const void *dy, const void *x, const void *gamma,
                                norm_mode_t mode, void *dx, float *dgamma, float *dbeta,
                                norm_stream_t stream) {
   // Size check first: nothing is launched for a shape that does not fit.
+  // The streaming backward writes a partial row per cluster (up to 152);
+  // where that exceeds the array, the resident long-row kernel's plan (fewer
+  // partial rows) runs instead.
   size_t need = 0;
-  norm_status_t st = norm_bwd_workspace_bytes(M, N, mode, &need);
+  norm_status_t st = bwd_workspace(M, N, mode, false, &need);
   if (st != NORM_OK) return st;
-  if (need > NORM_NOALLOC_WORKSPACE_BYTES) return NORM_ERR_WORKSPACE;
+  bool no_stream = false;
+  if (need > NORM_NOALLOC_WORKSPACE_BYTES) {
+    if ((st = bwd_workspace(M, N, mode, true, &need)) != NORM_OK) return st;
+    if (need > NORM_NOALLOC_WORKSPACE_BYTES) return NORM_ERR_WORKSPACE;
+    no_stream = true;
+  }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -1474,8 +1531,8 @@ norm_status_t norm_bwd_noalloc(const void *dy, const void *x, const void *gamma,
     }
     ws = g_noalloc_ptr[dev];
   }
-  return norm_bwd(dy, x, gamma, rstd, mean, M, N, mode, dx, dgamma, dbeta, ws,
-                  NORM_NOALLOC_WORKSPACE_BYTES, stream);
+  return bwd_run(dy, x, gamma, rstd, mean, M, N, mode, dx, dgamma, dbeta, ws,
+                 NORM_NOALLOC_WORKSPACE_BYTES, stream, no_stream);
 }
 
 norm_status_t norm_selftest_wait_timeout(uint32_t polls, norm_stream_t stream) {

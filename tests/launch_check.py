@@ -41,9 +41,107 @@ def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C, par_bytes=0):
     return L
 
 
+STREAM_THREADS = 512
+STREAM_KP = 2                                  # chunks per thread per piece
+STREAM_PIECE = STREAM_THREADS * STREAM_KP * 8  # columns per piece
+STREAM_NP = 4                                  # pieces per slice
+STREAM_SLICE = STREAM_NP * STREAM_PIECE
+
+
+def stream_layout(S, C):
+    """Shared memory of the streaming backward, in the kernel's order."""
+    tensor = STREAM_PIECE * 2
+    stage = 2 * tensor
+    off = stage * S
+    L = {"tensor": tensor, "stage": stage, "red": off}
+    off = _align16(off + 2 * (STREAM_THREADS // 32) * 4 * 4)
+    L["xch"] = off
+    if C > 1:
+        off = _align16(off + XCH_BUFFERS * C * 4 * 4 + 8 * XCH_BUFFERS)
+    L["bar"] = off
+    off = _align16(off + S * 8)
+    L["flag"] = off
+    off = _align16(off + 4 + 4 * S + 4)  # abort flag, S warp counters, TMEM slot
+    L["total"] = off
+    return L
+
+
+def stream_piece_at(q, np_, nr):
+    """(pass, row index j, piece p) of piece q of a cluster's sequence: pass 1
+    of row 0, then pass 1 of row j and pass 2 of row j - 1, then pass 2 of
+    the last row."""
+    if q < np_:
+        return 0, 0, q
+    q2 = q - np_
+    b, w = divmod(q2, 2 * np_)
+    if b < nr - 1:
+        return (0, b + 1, w) if w < np_ else (1, b, w - np_)
+    return 1, nr - 1, w
+
+
+def check_stream_plan(p, M, N, mode, smem_optin=232448):
+    """The streaming backward's accesses for plan `p`: every (row, pass,
+    piece) issued once per cluster in pipeline order, each bulk copy inside
+    x / dy and 16-byte aligned, the shared-memory regions in bounds, the
+    tensor-memory columns within 512 and the partial rows inside the
+    workspace."""
+    C, NS, S, grid, P = p["cluster"], p["cols_per_cta"], p["stages"], p["grid"], p["partials"]
+    assert p["streamed"] == 1 and p["threads"] == STREAM_THREADS and p["exact"] == 1
+    assert NS == STREAM_SLICE and N == C * NS and 1 <= C <= 16
+    assert p["chunks_per_thread"] * STREAM_THREADS * 8 == NS
+    assert p["tiles"] == M and grid % C == 0 and grid // C == P and 1 <= P <= M
+    L = stream_layout(S, C)
+    assert p["smem_bytes"] == L["total"] <= smem_optin - 1024 and S >= 2
+    assert L["stage"] < TX_LIMIT and L["bar"] % 8 == 0 and L["flag"] % 4 == 0
+    # named-barrier scratch (rpar in {0, 1}, 16 warps) and exchange slots
+    assert L["red"] + ((1 * 16) + 15) * 4 * 4 + 16 <= L["xch"]
+    if C > 1:
+        bars = L["xch"] + XCH_BUFFERS * C * 16
+        assert bars % 8 == 0 and bars + 8 * XCH_BUFFERS <= L["bar"]
+    # thread t, chunk k of a piece: smem byte t*16 + k*threads*16 (+16) in the
+    # tensor; global column piece*W + (k*threads + t)*8 (+8) in the slice
+    assert (STREAM_THREADS - 1) * 16 + (STREAM_KP - 1) * STREAM_THREADS * 16 + 16 <= L["tensor"]
+    assert (STREAM_NP - 1) * STREAM_PIECE + ((STREAM_KP - 1) * STREAM_THREADS
+                                               + STREAM_THREADS - 1) * 8 + 8 <= NS
+    nacc = 2 if mode == 1 else 1
+    groups = STREAM_THREADS // 32 // 4
+    assert groups * STREAM_NP * STREAM_KP * 8 * nacc <= 512, "accumulators exceed TMEM"
+    seen = 0
+    for cid in range(P):
+        nr = -(-(M - cid) // P)
+        order = []
+        for q in range(2 * STREAM_NP * nr):
+            ps, j, pc = stream_piece_at(q, STREAM_NP, nr)
+            assert 0 <= j < nr and 0 <= pc < STREAM_NP
+            row = cid + j * P
+            assert row < M
+            for crank in range(C):
+                off = row * N + crank * NS + pc * STREAM_PIECE
+                assert (off * 2) % 16 == 0 and off + STREAM_PIECE <= M * N
+            order.append((ps, j, pc))
+        assert len(set(order)) == len(order) == 2 * STREAM_NP * nr
+        # consumed in this order by the kernel's loop: pass 1 of row j, then
+        # pass 2 of row j - 1, each piece in increasing order
+        want = []
+        for j in range(nr + 1):
+            if j < nr:
+                want += [(0, j, pc) for pc in range(STREAM_NP)]
+            if j >= 1:
+                want += [(1, j - 1, pc) for pc in range(STREAM_NP)]
+        assert order == want
+        seen += nr
+        last = ((nacc - 1) * P + cid) * N + (C - 1) * NS + NS
+        assert last <= nacc * P * N, "partial row write out of the workspace"
+    assert seen == M
+    return True
+
+
 def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     """Raise AssertionError if any access of the launch described by `p`
     (a norm_plan dict) would leave its buffer or break an alignment rule."""
+    if p.get("streamed"):
+        assert backward and not residual
+        return check_stream_plan(p, M, N, mode, smem_optin)
     C, NS, tpr, K = p["cluster"], p["cols_per_cta"], p["threads_per_row"], p["chunks_per_thread"]
     G, rpg, RT, S = p["groups"], p["rows_per_group"], p["rows_per_tile"], p["stages"]
     threads, smem, ntiles, grid, P = p["threads"], p["smem_bytes"], p["tiles"], p["grid"], p["partials"]

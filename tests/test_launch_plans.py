@@ -132,10 +132,13 @@ SPLIT_SHAPES = [(6, 524288), (33, 1048576), (4096, 524288), (1, 262152), (4097, 
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("backward", [False, True])
 @pytest.mark.parametrize("other", [False, True])
-def test_split_plans_in_bounds(mode, backward, other):
+def test_split_plans_in_bounds(mode, backward, other, monkeypatch):
     """Rows wider than one cluster holds take the two-pass path: both passes
     of the forward and of the backward stay in bounds, and the dx pass's
-    dgamma / dbeta slots are distinct and read back exactly."""
+    dgamma / dbeta slots are distinct and read back exactly.  (stream=0
+    keeps the RMSNorm backward at 524288 columns, which streams by default,
+    on the two-pass path.)"""
+    monkeypatch.setenv("GBNORM_PLAN", "stream=0")
     phase = (2 if backward else 0) + (1 if other else 0)
     for M, N in SPLIT_SHAPES:
         p = gb.norm_plan(M, N, mode, backward, SMS, OPTIN, other_pass=other)
@@ -158,8 +161,10 @@ def test_split_forced_small_rows(backward, monkeypatch):
                                               (2 if backward else 0) + (1 if other else 0), OPTIN)
 
 
-def test_split_random_shapes():
+def test_split_random_shapes(monkeypatch):
     import numpy as np
+
+    monkeypatch.setenv("GBNORM_PLAN", "stream=0")
 
     rng = np.random.default_rng(7)
     for _ in range(60):
@@ -175,3 +180,41 @@ def test_one_pass_up_to_its_limit():
     for bwd in (False, True):
         assert gb.norm_plan(4096, 262144, 0, bwd, SMS, OPTIN)["split_segments"] == 0
         assert gb.norm_plan(4096, 262152, 0, bwd, SMS, OPTIN)["split_segments"] > 0
+
+
+STREAM_SHAPES = [(1, 32768), (5, 32768), (4096, 32768), (3, 65536), (4099, 65536),
+                 (2, 131072), (4096, 131072), (45, 131072), (7, 262144), (2048, 262144),
+                 (3, 524288), (1024, 524288), (11, 98304)]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_stream_plans_in_bounds(mode, monkeypatch):
+    """The streaming backward (forced at every width it takes, and where it
+    is the default): pieces, copies, shared and tensor memory, partials."""
+    for M, N in STREAM_SHAPES:
+        monkeypatch.setenv("GBNORM_PLAN", "stream=1")
+        p = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
+        launch_check.check_plan(p, M, N, mode, True, OPTIN)
+        launch_check.check_reduce(p["partials"], N, 2 if mode == 1 else 1)
+        monkeypatch.delenv("GBNORM_PLAN")
+        p = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
+        if p["streamed"]:
+            launch_check.check_plan(p, M, N, mode, True, OPTIN)
+
+
+def test_stream_default_widths():
+    """Where the backward streams by default (the widths it measured faster
+    at) and where it keeps the resident long-row kernel or the two-pass
+    path."""
+    want = {(0, 32768): 1, (0, 65536): 0, (0, 131072): 1, (0, 262144): 1, (0, 524288): 1,
+            (1, 32768): 0, (1, 65536): 1, (1, 131072): 1, (1, 262144): 1, (1, 524288): 0,
+            (0, 98304): 0, (0, 16384): 0, (1, 1048576): 0}
+    for (mode, N), s in want.items():
+        p = gb.norm_plan(4096, N, mode, True, SMS, OPTIN)
+        assert p["streamed"] == s, (mode, N)
+        if N > 262144 and not s:
+            assert p["split_segments"] > 0
+        # the forward and the fused residual backward never stream
+        assert gb.norm_plan(4096, N, mode, False, SMS, OPTIN)["streamed"] == 0
+        if N <= 262144:
+            assert gb.norm_plan(4096, N, mode, True, SMS, OPTIN, residual=True)["streamed"] == 0

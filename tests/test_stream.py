@@ -6,7 +6,9 @@ The path is forced with the plan override stream=1 at every width it takes
 (N = C x 32768, C = 1 .. 16): a single CTA per row, clusters of 2 to 16, few
 rows (clusters with one row and with none beyond the first) and more rows
 than clusters (each cluster streams several rows, the software pipeline of
-pass 1 of row j with pass 2 of row j - 1 runs through).
+pass 1 of row j with pass 2 of row j - 1 runs through).  Where it is the
+default backward, the resident long-row kernel it replaces stays covered
+here with stream=0.
 """
 import numpy as np
 import pytest
@@ -105,3 +107,19 @@ def test_stream_not_taken_where_it_does_not_apply(monkeypatch):
         assert gb.norm_plan(64, N, wl.RMS, True)["streamed"] == 0
     p = gb.norm_plan(64, 98304, wl.RMS, True)  # three slices: a cluster of 3
     assert p["streamed"] == 1 and p["cluster"] == 3
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
+@pytest.mark.parametrize("M,N", [(45, 131072), (7, 262144), (300, 32768)])
+def test_resident_long_rows_where_streaming_is_default(mode, M, N, monkeypatch):
+    """stream=0: the resident long-row backward (slice held in shared
+    memory, clusters of up to 16) at widths that stream by default."""
+    monkeypatch.setenv("GBNORM_PLAN", "stream=0")
+    plan = gb.norm_plan(M, N, mode, True)
+    assert plan["streamed"] == 0 and plan["long_rows"] == 1
+    case = wl.like(_base(mode), M, N)
+    x, g, b, dy = [None if t is None else t.cuda()
+                   for t in wl.make_inputs(case, "cpu", seed=N % 991 + M)]
+    outs = pu.run_gpu(x, g, b, dy, case.eps, mode)
+    assert gb.norm_get_device_error() == 0
+    pu.compare(mode, case.eps, x, g, b, dy, outs, label=f"resident {mode}:{M}x{N}")

@@ -37,14 +37,20 @@ def _p(t):
 
 
 @pytest.mark.parametrize("name,M,N", CASES)
-def test_noalloc_matches_workspace_entry_point(name, M, N):
+def test_noalloc_matches_workspace_entry_point(name, M, N, monkeypatch):
     case = wl.like(wl.WORKLOADS[name], M, N)
     x, g, b, dy = [None if t is None else t.cuda() for t in wl.make_inputs(case, "cpu")]
     mode = case.mode
     y, rstd, mean = gb.norm_fwd(x, g, b, case.eps, mode)
+    if gb.norm_bwd_workspace_bytes(M, N, mode) > 16 << 20:
+        # the streaming backward's partial rows do not fit the array: the
+        # entry point runs the resident long-row plan, as stream=0 does
+        assert gb.norm_plan(M, N, mode, True)["streamed"] == 1
+        monkeypatch.setenv("GBNORM_PLAN", "stream=0")
     dx_ref, dg_ref, db_ref = gb.norm_bwd(dy, x, g, rstd, mean, mode)
     torch.cuda.synchronize()
     assert gb.norm_bwd_workspace_bytes(M, N, mode) <= 16 << 20
+    monkeypatch.delenv("GBNORM_PLAN", raising=False)
     L = gb.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
@@ -69,9 +75,9 @@ def test_noalloc_matches_workspace_entry_point(name, M, N):
 def test_noalloc_rejects_shapes_beyond_its_array(monkeypatch):
     """A launch plan whose scratch need exceeds 16 MiB is refused with
     NORM_ERR_WORKSPACE before anything is launched.  (With the library's
-    default plans every supported shape needs less; a plan override with one
-    CTA per row and 152+ partial rows makes LayerNorm 4096 x 16384 need
-    about 20 MB.)"""
+    default plans every supported shape fits, the streaming backward through
+    its fallback; a plan override with one CTA per row and 152+ partial rows
+    makes LayerNorm 4096 x 16384 need about 20 MB.)"""
     M, N = 4096, 16384
     monkeypatch.setenv("GBNORM_PLAN", "C=1,tpr=512")
     need = gb.norm_bwd_workspace_bytes(M, N, wl.LAYER)
