@@ -327,6 +327,10 @@ typedef struct {
                                   products, then dx, the second read served
                                   from L2 -- with the dgamma / dbeta column
                                   sums held in tensor memory; 0 otherwise */
+    int32_t wait_hint_ns;      /* forward, register-resident rows: suspend
+                                  hint (ns) of the waits for a stage, so that
+                                  a waiting row group issues nothing; 0: the
+                                  hardware's default interval */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

@@ -51,7 +51,8 @@ class Plan(ctypes.Structure):
                 ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("partials", ctypes.c_int32), ("exact", ctypes.c_int32),
                 ("long_rows", ctypes.c_int32), ("param_smem_bytes", ctypes.c_int32),
-                ("split_segments", ctypes.c_int32), ("streamed", ctypes.c_int32)]
+                ("split_segments", ctypes.c_int32), ("streamed", ctypes.c_int32),
+                ("wait_hint_ns", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -56,6 +56,7 @@ struct NormArgs {
   int nseg; // two-pass path: segments of NS columns per row (the last one ragged)
   float eps;
   float invN;
+  unsigned wait_ns;  // register-resident forward: suspend hint of its stage waits (0: none)
 };
 
 // Byte offsets of the dynamic shared memory regions (all 16-byte aligned).
@@ -133,6 +134,7 @@ struct Plan {
   int nseg = 0;
   int phase = 0;       // two-pass path: which of its passes (kSplit*)
   bool stream = false; // backward: the streaming long-row kernel (stream.cu)
+  int wait_ns = 0;     // register-resident forward: suspend hint of its stage waits
 };
 
 // Kernel entry points, by (mode, K, cluster, exact, fused residual).
@@ -156,8 +158,10 @@ constexpr int kMxBlock = 32;
 // gsm: gamma (and beta) staged in shared memory and read per row, which frees
 // the registers that hold them otherwise (exact splits, no cluster, K in
 // {5, 6, 8}; see fwd_gsm_kernel_ptr).
+// sleep: the variant whose stage waits carry the plan's suspend hint (exact,
+// no cluster, no residual, no staged parameters, K in {2, 4}).
 const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid = false,
-                           bool gsm = false);
+                           bool gsm = false, bool sleep = false);
 // E4M3 output variants (no cluster variants); nullptr if not instantiated.
 const void *fwd_fp8_kernel_ptr(int mode, int K, bool exact, bool resid, int out,
                                bool gsm = false);

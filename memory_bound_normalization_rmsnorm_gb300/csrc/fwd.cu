@@ -35,9 +35,27 @@ const void *pick_fwd(int K, bool e, bool r) {
   }
 }
 
+// Variants whose stage waits sleep (the plan's suspend hint): exact,
+// single-CTA, plain, 2 or 4 chunks per thread.
+template <int MODE>
+const void *pick_sleep(int K) {
+  switch (K) {
+    case 2: return reinterpret_cast<const void *>(
+        &norm_fwd_kernel<MODE, 2, false, true, false, kOutBf16, false, true>);
+    case 4: return reinterpret_cast<const void *>(
+        &norm_fwd_kernel<MODE, 4, false, true, false, kOutBf16, false, true>);
+    default: return nullptr;
+  }
+}
+
 }  // namespace
 
-const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, bool gsm) {
+const void *fwd_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, bool gsm,
+                           bool sleep) {
+  if (sleep) {
+    if (cluster || !exact || resid || gsm) return nullptr;
+    return mode == kRMS ? pick_sleep<kRMS>(K) : pick_sleep<kLayer>(K);
+  }
   if (gsm) return (cluster || !exact) ? nullptr : fwd_gsm_kernel_ptr(mode, K, resid, kOutBf16);
   if (mode == kRMS)
     return cluster ? pick_fwd<kRMS, true>(K, exact, resid) : pick_fwd<kRMS, false>(K, exact, resid);

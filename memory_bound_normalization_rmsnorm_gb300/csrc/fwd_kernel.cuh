@@ -41,7 +41,9 @@ namespace gbn {
 // GSM: gamma (and beta) are staged once in shared memory (as fp32) and read
 // per row instead of living in registers, so a thread can hold more chunks
 // of x.
-template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT, bool GSM>
+// SLEEP: the stage waits carry the plan's suspend hint (a.wait_ns).
+template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT, bool GSM,
+          bool SLEEP = false>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   // Staged parameters as fp32 (bf16 output) or bf16 (E4M3 output).
@@ -180,7 +182,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_kernel(const NormArgs
   int s = 0;
   uint32_t par = 0;
   for (int64_t tile = cid; tile < a.ntiles; tile += ncl) {
-    mbar_wait(full + s, par, a.err, abort_flag);
+    if constexpr (SLEEP)
+      mbar_wait_sleep(full + s, par, a.err, abort_flag, a.wait_ns);
+    else
+      mbar_wait(full + s, par, a.err, abort_flag);
     const int64_t row0 = tile * a.RT;
     const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
     const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes;

@@ -47,6 +47,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with a suspend-time hint: a thread whose phase is not yet
+// complete may sleep up to `ns` nanoseconds (or until the phase completes)
+// instead of the hardware's default interval, issuing nothing meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Error bits a kernel may set in the library's device error word.
 constexpr unsigned kErrWaitTimeout = 1u;
 // Number of try_wait polls before a wait is declared lost.  Each poll may
@@ -66,6 +82,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < max_polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+  }
+  *abort = 1;
+  atomicOr(err, kErrWaitTimeout);
+  return false;
+}
+
+// mbar_wait whose polls may each sleep up to `ns` nanoseconds: warps that
+// wait for a stage leave the issue slots to the row groups that compute.
+// Same bound in polls (so at most kMaxPolls x ns when every poll sleeps in
+// full: seconds for the hints the plans use).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                volatile int *abort, uint32_t ns) {
+  if (mbar_try_wait_sleep(bar, parity, ns)) return true;
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    if (mbar_try_wait_sleep(bar, parity, ns)) return true;
     if ((i & 255u) == 255u && *abort) return false;
   }
   *abort = 1;
