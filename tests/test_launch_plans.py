@@ -218,3 +218,18 @@ def test_stream_default_widths():
         assert gb.norm_plan(4096, N, mode, False, SMS, OPTIN)["streamed"] == 0
         if N <= 262144:
             assert gb.norm_plan(4096, N, mode, True, SMS, OPTIN, residual=True)["streamed"] == 0
+
+
+def test_wait_hint_only_where_tuned(monkeypatch):
+    """The register-resident LayerNorm 4096 forward waits with a suspend
+    hint; no other default plan does, and the override hint= applies only to
+    the plans that have a hinted variant (exact, single CTA, plain, 2 or 4
+    chunks per thread)."""
+    assert gb.norm_plan(32768, 4096, 1, False, SMS, OPTIN)["wait_hint_ns"] == 2000
+    for mode, N in ((1, 2048), (0, 4096), (0, 1024), (1, 8192), (0, 131072)):
+        assert gb.norm_plan(32768, N, mode, False, SMS, OPTIN)["wait_hint_ns"] == 0
+    assert gb.norm_plan(32768, 4096, 1, True, SMS, OPTIN)["wait_hint_ns"] == 0
+    monkeypatch.setenv("GBNORM_PLAN", "hint=1500")
+    p = gb.norm_plan(32768, 2048, 0, False, SMS, OPTIN)
+    assert p["wait_hint_ns"] == (1500 if p["chunks_per_thread"] in (2, 4) and p["exact"] else 0)
+    assert gb.norm_plan(4096, 131072, 0, False, SMS, OPTIN)["wait_hint_ns"] == 0  # long rows

@@ -113,3 +113,20 @@ def test_rows_are_independent():
     dx2, _, _ = gb.norm_bwd(dy[sub].contiguous(), x[sub].contiguous(), g, r2, m2, 1)
     torch.cuda.synchronize()
     assert torch.equal(y[sub], y2) and torch.equal(r[sub], r2) and torch.equal(dx[sub], dx2)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode,M,N", [(wl.LAYER, 9001, 4096), (wl.RMS, 3001, 2048),
+                                      (wl.LAYER, 777, 1024)])
+def test_forward_with_wait_hint(mode, M, N, monkeypatch):
+    """Forward plans whose stage waits sleep (the LayerNorm 4096 default,
+    and others forced with hint=): same results as the oracle."""
+    monkeypatch.setenv("GBNORM_PLAN", "hint=2000")
+    assert gb.norm_plan(M, N, mode, False)["wait_hint_ns"] == 2000
+    base = wl.WORKLOADS["layer_32768x4096" if mode == wl.LAYER else "rms_262144x1024_outliers"]
+    case = wl.like(base, M, N)
+    x, g, b, dy = [None if t is None else t.cuda()
+                   for t in wl.make_inputs(case, "cpu", seed=M + N)]
+    outs = pu.run_gpu(x, g, b, dy, case.eps, mode)
+    assert gb.norm_get_device_error() == 0
+    pu.compare(mode, case.eps, x, g, b, dy, outs, label=f"hint {mode}:{M}x{N}")
