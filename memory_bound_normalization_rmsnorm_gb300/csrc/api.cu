@@ -352,17 +352,17 @@ bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <=
 
 // Row widths, in slices of kStreamSlice columns, where the streaming
 // backward measured faster on GB300 (1024 to 4096 rows) than the resident
-// long-row kernel or, beyond NORM_MAX_N_ONEPASS, the two-pass path:
-// 4 and 8 slices (the resident kernel's clusters of 8 and 16 occupy 120 and
-// 112 SMs; RMSNorm 74 -> 81 % and 66 -> 68 %, LayerNorm 62 -> 71 % and
-// 53 -> 59 % of measured), RMSNorm at 1 and 16 slices (87 -> 89.5 %,
-// 58.7 -> 59.9 %), LayerNorm at 2 (72.5 -> 73.5 %).  Elsewhere (RMSNorm at
-// 2 slices: 86.6 against 82.8 %; LayerNorm at 16: 58.0 against 52.6 %;
-// slice counts that are not powers of two) the other kernels stay.
+// long-row kernel or, beyond NORM_MAX_N_ONEPASS, the two-pass path, in % of
+// the measured copy bandwidth: 1, 2, 4 and 8 slices (RMSNorm 87.2 -> 87.5,
+// 86.9 -> 89.0, 74.3 -> 85.9, 66.1 -> 70.6; LayerNorm 74.8 -> 79.9,
+// 72.7 -> 77.1, 61.7 -> 74.4, 53.0 -> 60.7: the resident kernel's clusters
+// of 8 and 16 occupy only 120 and 112 SMs) and RMSNorm at 16 (two-pass
+// 58.4 -> 63.7).  LayerNorm at 16 slices keeps the two-pass path (57.8
+// against 53.9), and slice counts that are not powers of two keep the
+// resident kernel (clusters of 3 measured ~40 %).
 bool stream_default(int mode, int C) {
-  if (C == 4 || C == 8) return true;
-  if (mode == kRMS) return C == 1 || C == 16;
-  return C == 2;
+  if (C == 1 || C == 2 || C == 4 || C == 8) return true;
+  return C == 16 && mode == kRMS;
 }
 
 // Whether the backward of rows of N columns takes the streaming kernel:

@@ -200,10 +200,11 @@ constexpr int kStreamThreads = 512;
 constexpr int kStreamKP = 2;
 constexpr int kStreamPiece = kStreamThreads * kStreamKP * 8;
 constexpr int kStreamSlice = 4 * kStreamPiece;
-// Its shared memory: S stages of one piece of x and dy, the cross-warp
-// scratch of the row sums, the cluster exchange slots (C > 1), the stage
-// mbarriers, then the abort flag, the per-stage warp counters and the
-// tensor-memory address slot.
+// Its shared memory: S stages of one piece of x and dy, the per-warp row
+// partials ([kXchBuffers][warps][2] floats, then kXchBuffers arrival
+// counters), the exchange slots and their mbarriers ([kXchBuffers][C] float4,
+// also for C = 1), the stage mbarriers, then the abort flag, the per-stage
+// warp counters and the tensor-memory address slot.
 __host__ __device__ inline SmemLayout stream_layout(int S, int C) {
   SmemLayout L;
   L.tensor_bytes = static_cast<uint32_t>(kStreamPiece) * 2u;
@@ -212,10 +213,10 @@ __host__ __device__ inline SmemLayout stream_layout(int S, int C) {
   L.par_off = off;
   L.stats_off = off;
   L.red_off = off;
-  off = align16(off + static_cast<uint32_t>(2 * (kStreamThreads / 32) * 4) * 4u);
+  off = align16(off + static_cast<uint32_t>(kXchBuffers * (kStreamThreads / 32) * 2) * 4u +
+                4u * kXchBuffers);
   L.xch_off = off;
-  if (C > 1)
-    off = align16(off + static_cast<uint32_t>(kXchBuffers * C * 4) * 4u + 8u * kXchBuffers);
+  off = align16(off + static_cast<uint32_t>(kXchBuffers * C * 4) * 4u + 8u * kXchBuffers);
   L.bar_off = off;
   off = align16(off + static_cast<uint32_t>(S) * 8u);
   L.flag_off = off;

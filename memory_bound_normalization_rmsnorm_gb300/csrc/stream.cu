@@ -86,6 +86,25 @@ __device__ __forceinline__ void piece_at(int64_t q, int np, int64_t nr, int &pas
   }
 }
 
+// Publishes a CTA's row totals (a, b) into exchange round x.push_buf, by one
+// thread: with a cluster, the round's expected bytes on this CTA's mbarrier
+// and an asynchronous store into slot [crank] of every CTA of the cluster;
+// alone, a store into its own slot and an arrival (release) on its mbarrier.
+template <bool CLUSTER>
+__device__ __forceinline__ void xch_publish(float a, float b, const ClusterXch &x) {
+  const int bsel = x.push_buf;
+  float *mine = x.slots + (static_cast<size_t>(bsel) * x.C + x.crank) * 4;
+  uint64_t *bar = x.bars + bsel;
+  const float4 val = make_float4(a, b, 0.f, 0.f);
+  if (CLUSTER) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(x.C * 16));
+    for (int q = 0; q < x.C; ++q) st_async_f32x4(mapa_shared(mine, q), val, mapa_shared(bar, q));
+  } else {
+    *reinterpret_cast<float4 *>(mine) = val;
+    mbar_arrive(bar);
+  }
+}
+
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   uint32_t p = 32;
   while (p < v) p <<= 1;
@@ -106,7 +125,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-  float *red = reinterpret_cast<float *>(smem + L.red_off);
+  float *wred = reinterpret_cast<float *>(smem + L.red_off);  // [buffer][warp][2]
+  int *wcnt = reinterpret_cast<int *>(wred + kXchBuffers * kNW * 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
   int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.flag_off) + 1 + a.S;
@@ -125,9 +145,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
       mbar_init(full + s, 1);
       done_cnt[s] = 0;
     }
-    if (CLUSTER) {
-      uint64_t *xb = xch_bars(smem, L, 1, a.C);
-      for (int b = 0; b < kXchBuffers; ++b) mbar_init(xb + b, 1);
+    uint64_t *xb = xch_bars(smem, L, 1, CLUSTER ? a.C : 1);
+    for (int b = 0; b < kXchBuffers; ++b) {
+      mbar_init(xb + b, 1);
+      wcnt[b] = 0;
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -207,7 +228,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
 
   ClusterXch xch = make_xch(smem, L, 1, CLUSTER ? a.C : 1, crank);
   const float invN = a.invN;
-  int rpar = 0;
   int s = 0;
   uint32_t par = 0;
   int64_t q = 0;
@@ -221,10 +241,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
   float rs_prev = 0.f, mu_prev = 0.f, rs_cur, mu_cur, rs_next, mu_next;
   load_stats(0, rs_cur, mu_cur);
   load_stats(1, rs_next, mu_next);
-  float tot_a = 0.f, tot_b = 0.f;  // without a cluster: row j's totals for its pass 2
 
   for (int64_t j = 0; j <= nr; ++j) {
-    float cur_a = 0.f, cur_b = 0.f;
     if (j < nr) {
       // ---- pass 1 of row j: sum g and sum g (x - mean) over the slice
       const float2 nmu = splat2(-mu_cur);
@@ -257,22 +275,38 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
       }
       s1 = add2(s1, s1b);
       s2 = add2(s2, s2b);
-      float v[2] = {s1.x + s1.y, s2.x + s2.y};
-      if (MODE == kLayer) {
-        group_sum<2, true>(v, kStreamThreads, 0, 1, t, red, rpar);
-      } else {
-        float w1[1] = {v[1]};
-        group_sum<1, true>(w1, kStreamThreads, 0, 1, t, red, rpar);
-        v[1] = w1[0];
+      // The row's totals without a CTA-wide barrier: each warp posts its
+      // butterfly-summed partial; the last warp to post adds the partials
+      // in warp order and publishes the CTA total (to every CTA of the
+      // cluster, or to this CTA's own exchange slot) while the other warps
+      // go on to the next pass.  Same additions in the same order as a
+      // barrier-synchronised group sum.
+      float v0 = s1.x + s1.y, v1 = s2.x + s2.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (MODE == kLayer) v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, o);
       }
-      if (CLUSTER) cluster_push(v[0], v[1], 0.f, 0, t, xch);
-      cur_a = v[0];
-      cur_b = v[1];
+      const int rb = xch.push_buf;
+      float *slots = wred + rb * kNW * 2;
+      if ((t & 31) == 0) {
+        slots[2 * warp] = v0;
+        slots[2 * warp + 1] = v1;
+      }
+      if (last_warp_done(wcnt, rb, kNW) && (t & 31) == 0) {
+        float A = slots[0], U = slots[1];
+        for (int w = 1; w < kNW; ++w) {
+          A += slots[2 * w];
+          U += slots[2 * w + 1];
+        }
+        xch_publish<CLUSTER>(A, U, xch);
+      }
+      xch.push_buf = (rb + 1) % kXchBuffers;
     }
     if (j >= 1) {
       // ---- pass 2 of row j - 1: dx and the column sums
-      float A = tot_a, U = tot_b;
-      if (CLUSTER) {
+      float A, U;
+      {
         const float *row = cluster_wait_row(0, xch, a.err, abort_flag);
         float v[2];
         fold_sum<2>(row, xch.C, v);
@@ -339,8 +373,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
         advance();
       }
     }
-    tot_a = cur_a;
-    tot_b = cur_b;
     rs_prev = rs_cur;
     mu_prev = mu_cur;
     rs_cur = rs_next;

@@ -54,10 +54,10 @@ def stream_layout(S, C):
     stage = 2 * tensor
     off = stage * S
     L = {"tensor": tensor, "stage": stage, "red": off}
-    off = _align16(off + 2 * (STREAM_THREADS // 32) * 4 * 4)
+    # per-warp row partials [buffer][warp][2] floats, then one counter per buffer
+    off = _align16(off + XCH_BUFFERS * (STREAM_THREADS // 32) * 2 * 4 + 4 * XCH_BUFFERS)
     L["xch"] = off
-    if C > 1:
-        off = _align16(off + XCH_BUFFERS * C * 4 * 4 + 8 * XCH_BUFFERS)
+    off = _align16(off + XCH_BUFFERS * C * 4 * 4 + 8 * XCH_BUFFERS)  # also for C = 1
     L["bar"] = off
     off = _align16(off + S * 8)
     L["flag"] = off
@@ -93,11 +93,14 @@ def check_stream_plan(p, M, N, mode, smem_optin=232448):
     L = stream_layout(S, C)
     assert p["smem_bytes"] == L["total"] <= smem_optin - 1024 and S >= 2
     assert L["stage"] < TX_LIMIT and L["bar"] % 8 == 0 and L["flag"] % 4 == 0
-    # named-barrier scratch (rpar in {0, 1}, 16 warps) and exchange slots
-    assert L["red"] + ((1 * 16) + 15) * 4 * 4 + 16 <= L["xch"]
-    if C > 1:
-        bars = L["xch"] + XCH_BUFFERS * C * 16
-        assert bars % 8 == 0 and bars + 8 * XCH_BUFFERS <= L["bar"]
+    # per-warp partials (buffer < 4, warp < 16, 2 floats), the 4 counters,
+    # then the exchange slots [buffer][rank] and their 4 mbarriers
+    warps = STREAM_THREADS // 32
+    hi = ((XCH_BUFFERS - 1) * warps + (warps - 1)) * 2 + 2
+    assert L["red"] + hi * 4 <= L["red"] + XCH_BUFFERS * warps * 2 * 4
+    assert L["red"] + XCH_BUFFERS * warps * 2 * 4 + 4 * XCH_BUFFERS <= L["xch"]
+    bars = L["xch"] + XCH_BUFFERS * C * 16
+    assert bars % 8 == 0 and bars + 8 * XCH_BUFFERS <= L["bar"]
     # thread t, chunk k of a piece: smem byte t*16 + k*threads*16 (+16) in the
     # tensor; global column piece*W + (k*threads + t)*8 (+8) in the slice
     assert (STREAM_THREADS - 1) * 16 + (STREAM_KP - 1) * STREAM_THREADS * 16 + 16 <= L["tensor"]

@@ -206,8 +206,8 @@ def test_stream_default_widths():
     """Where the backward streams by default (the widths it measured faster
     at) and where it keeps the resident long-row kernel or the two-pass
     path."""
-    want = {(0, 32768): 1, (0, 65536): 0, (0, 131072): 1, (0, 262144): 1, (0, 524288): 1,
-            (1, 32768): 0, (1, 65536): 1, (1, 131072): 1, (1, 262144): 1, (1, 524288): 0,
+    want = {(0, 32768): 1, (0, 65536): 1, (0, 131072): 1, (0, 262144): 1, (0, 524288): 1,
+            (1, 32768): 1, (1, 65536): 1, (1, 131072): 1, (1, 262144): 1, (1, 524288): 0,
             (0, 98304): 0, (0, 16384): 0, (1, 1048576): 0}
     for (mode, N), s in want.items():
         p = gb.norm_plan(4096, N, mode, True, SMS, OPTIN)
