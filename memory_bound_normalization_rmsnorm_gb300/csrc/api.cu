@@ -359,7 +359,11 @@ bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <=
 // of 8 and 16 occupy only 120 and 112 SMs) and RMSNorm at 16 (two-pass
 // 58.4 -> 63.7).  LayerNorm at 16 slices keeps the two-pass path (57.8
 // against 53.9), and slice counts that are not powers of two keep the
-// resident kernel (clusters of 3 measured ~40 %).
+// resident kernel (clusters of 3 measured ~40 %).  The fused residual
+// backward (dh streamed once with the dx pass) takes it at the same widths
+// (1, 2, 4 and 8 slices; the fused entry points stop at 262144 columns):
+// RMSNorm 80.9 -> 95.9, 80.2 -> 98.5, 70.3 -> 98.6, 64.7 -> 86.3 %,
+// LayerNorm 63.6 -> 90.6, 57.8 -> 90.1, 48.2 -> 88.8, 45.0 -> 74.0 %.
 bool stream_default(int mode, int C) {
   if (C == 1 || C == 2 || C == 4 || C == 8) return true;
   return C == 16 && mode == kRMS;
@@ -374,12 +378,14 @@ bool use_stream(int N, int mode, const Override &ov) {
   return !ov.any && stream_default(mode, N / kStreamSlice);
 }
 
-norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, Plan *out) {
+norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, Plan *out,
+                          bool resid = false) {
   if (!stream_applies(N)) return NORM_ERR_UNSUPPORTED;
   const int C = N / kStreamSlice;
   if (ov.C && ov.C != C) return NORM_ERR_UNSUPPORTED;
   Plan p;
   p.stream = true;
+  p.resid = resid;
   p.C = C;
   p.NS = kStreamSlice;
   p.nsc = kStreamSlice / 8;
@@ -392,11 +398,11 @@ norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, 
   p.threads = kStreamThreads;
   const int64_t budget = smem_optin - 1024;
   int S = ov.S ? ov.S : kStreamStages;
-  while (!ov.S && S > 2 && static_cast<int64_t>(stream_layout(S, C).total) > budget) --S;
-  if (S < 2 || static_cast<int64_t>(stream_layout(S, C).total) > budget)
+  while (!ov.S && S > 2 && static_cast<int64_t>(stream_layout(S, C, resid).total) > budget) --S;
+  if (S < 2 || static_cast<int64_t>(stream_layout(S, C, resid).total) > budget)
     return NORM_ERR_UNSUPPORTED;
   p.S = S;
-  p.smem = stream_layout(S, C).total;
+  p.smem = stream_layout(S, C, resid).total;
   p.ntiles = M;
   *out = p;
   return NORM_OK;
@@ -424,7 +430,8 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
       }
     }
   }
-  if (bwd && !resid && use_stream(N, mode, ov)) return stream_plan(M, N, smem_optin, ov, out);
+  if (bwd && !fp8 && use_stream(N, mode, ov))
+    return stream_plan(M, N, smem_optin, ov, out, resid);
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
   const int nc = N / 8;
   Plan p;
@@ -561,7 +568,7 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
   if (p.split) return split_kernel_ptr(mode, p.phase, p.K);
-  if (p.stream) return stream_kernel_ptr(mode, p.C > 1);
+  if (p.stream) return stream_kernel_ptr(mode, p.C > 1, p.resid);
   if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.resid);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm, p.wait_ns > 0);

@@ -200,15 +200,16 @@ constexpr int kStreamThreads = 512;
 constexpr int kStreamKP = 2;
 constexpr int kStreamPiece = kStreamThreads * kStreamKP * 8;
 constexpr int kStreamSlice = 4 * kStreamPiece;
-// Its shared memory: S stages of one piece of x and dy, the per-warp row
+// Its shared memory: S stages of one piece of x and dy (and, for the fused
+// residual backward, of dh, which only the dx pass loads), the per-warp row
 // partials ([kXchBuffers][warps][2] floats, then kXchBuffers arrival
 // counters), the exchange slots and their mbarriers ([kXchBuffers][C] float4,
 // also for C = 1), the stage mbarriers, then the abort flag, the per-stage
 // warp counters and the tensor-memory address slot.
-__host__ __device__ inline SmemLayout stream_layout(int S, int C) {
+__host__ __device__ inline SmemLayout stream_layout(int S, int C, bool resid = false) {
   SmemLayout L;
   L.tensor_bytes = static_cast<uint32_t>(kStreamPiece) * 2u;
-  L.stage_bytes = 2u * L.tensor_bytes;
+  L.stage_bytes = (resid ? 3u : 2u) * L.tensor_bytes;
   uint32_t off = L.stage_bytes * static_cast<uint32_t>(S);
   L.par_off = off;
   L.stats_off = off;
@@ -224,7 +225,7 @@ __host__ __device__ inline SmemLayout stream_layout(int S, int C) {
   L.total = off;
   return L;
 }
-// Kernel by (mode, cluster or single CTA).
-const void *stream_kernel_ptr(int mode, bool cluster);
+// Kernel by (mode, cluster or single CTA, fused residual).
+const void *stream_kernel_ptr(int mode, bool cluster, bool resid = false);
 
 }  // namespace gbn

@@ -112,7 +112,9 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 }
 
 // One CTA per (row, 32768-column slice); NP pieces of kW columns per slice.
-template <int MODE, int NP, bool CLUSTER>
+// RESID: the fused residual backward, dx = (norm backward at h) + dh, dh
+// streamed once with the dx pass's pieces (a.x holds h, a.res dh).
+template <int MODE, int NP, bool CLUSTER, bool RESID>
 __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(const NormArgs a) {
   constexpr int NACC = MODE == kLayer ? 2 : 1;          // dgamma (and dbeta)
   constexpr int CPC = 8 * NACC;                          // TMEM columns per chunk
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
   constexpr int kStride = kStreamThreads * 16;           // bytes between a thread's chunks
 
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1);
+  const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1, RESID);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *wred = reinterpret_cast<float *>(smem + L.red_off);  // [buffer][warp][2]
   int *wcnt = reinterpret_cast<int *>(wred + kXchBuffers * kNW * 2);
@@ -197,9 +199,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
     uint64_t *bar = full + s;
     unsigned char *dst = smem + static_cast<size_t>(s) * L.stage_bytes;
     const uint64_t pol = pass ? pol2 : pol1;
-    mbar_arrive_expect_tx(bar, L.stage_bytes);
+    const bool with_dh = RESID && pass == 1;
+    mbar_arrive_expect_tx(bar, (with_dh ? 3u : 2u) * L.tensor_bytes);
     bulk_g2s(dst, a.x + off, L.tensor_bytes, bar, pol);
     bulk_g2s(dst + L.tensor_bytes, a.dy + off, L.tensor_bytes, bar, pol);
+    if (with_dh) bulk_g2s(dst + 2 * L.tensor_bytes, a.res + off, L.tensor_bytes, bar, pol2);
   };
   if (t == 0) {
     for (int64_t q = 0; q < total && q < a.S; ++q) issue(q, static_cast<int>(q));
@@ -363,6 +367,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
               ak[8 + 2 * e + 1] = __float_as_uint(ab.y);
             }
           }
+          if (RESID) {
+            float2 hf[4];
+            chunk_to_f2(lds_v4(st + 2 * L.tensor_bytes + k * kStride), hf);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = add2(o[e], hf[e]);
+          }
           st_global_cs_v4(dxrow + p * kW + k * kStreamThreads * 8, f2_to_chunk(o));
         }
 #pragma unroll
@@ -412,15 +422,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
   if (CLUSTER) cluster_sync();
 }
 
+template <int MODE, int NP, bool RESID>
+const void *stream_ptr(bool cluster) {
+  return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<MODE, NP, true, RESID>)
+                 : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<MODE, NP, false, RESID>);
+}
+
 }  // namespace
 
-const void *stream_kernel_ptr(int mode, bool cluster) {
+const void *stream_kernel_ptr(int mode, bool cluster, bool resid) {
   constexpr int NP = kStreamSlice / kW;
   if (mode == kLayer)
-    return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kLayer, NP, true>)
-                   : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kLayer, NP, false>);
-  return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kRMS, NP, true>)
-                 : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<kRMS, NP, false>);
+    return resid ? stream_ptr<kLayer, NP, true>(cluster) : stream_ptr<kLayer, NP, false>(cluster);
+  return resid ? stream_ptr<kRMS, NP, true>(cluster) : stream_ptr<kRMS, NP, false>(cluster);
 }
 
 }  // namespace gbn

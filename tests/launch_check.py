@@ -48,10 +48,11 @@ STREAM_NP = 4                                  # pieces per slice
 STREAM_SLICE = STREAM_NP * STREAM_PIECE
 
 
-def stream_layout(S, C):
-    """Shared memory of the streaming backward, in the kernel's order."""
+def stream_layout(S, C, resid=False):
+    """Shared memory of the streaming backward, in the kernel's order (a
+    third tensor per stage, dh, for the fused residual backward)."""
     tensor = STREAM_PIECE * 2
-    stage = 2 * tensor
+    stage = (3 if resid else 2) * tensor
     off = stage * S
     L = {"tensor": tensor, "stage": stage, "red": off}
     # per-warp row partials [buffer][warp][2] floats, then one counter per buffer
@@ -79,7 +80,7 @@ def stream_piece_at(q, np_, nr):
     return 1, nr - 1, w
 
 
-def check_stream_plan(p, M, N, mode, smem_optin=232448):
+def check_stream_plan(p, M, N, mode, smem_optin=232448, residual=False):
     """The streaming backward's accesses for plan `p`: every (row, pass,
     piece) issued once per cluster in pipeline order, each bulk copy inside
     x / dy and 16-byte aligned, the shared-memory regions in bounds, the
@@ -90,8 +91,10 @@ def check_stream_plan(p, M, N, mode, smem_optin=232448):
     assert NS == STREAM_SLICE and N == C * NS and 1 <= C <= 16
     assert p["chunks_per_thread"] * STREAM_THREADS * 8 == NS
     assert p["tiles"] == M and grid % C == 0 and grid // C == P and 1 <= P <= M
-    L = stream_layout(S, C)
+    L = stream_layout(S, C, residual)
     assert p["smem_bytes"] == L["total"] <= smem_optin - 1024 and S >= 2
+    # pass 1 pieces land x and dy, pass 2 pieces also dh: inside the stage
+    assert (3 if residual else 2) * L["tensor"] == L["stage"]
     assert L["stage"] < TX_LIMIT and L["bar"] % 8 == 0 and L["flag"] % 4 == 0
     # per-warp partials (buffer < 4, warp < 16, 2 floats), the 4 counters,
     # then the exchange slots [buffer][rank] and their 4 mbarriers
@@ -143,8 +146,8 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     """Raise AssertionError if any access of the launch described by `p`
     (a norm_plan dict) would leave its buffer or break an alignment rule."""
     if p.get("streamed"):
-        assert backward and not residual
-        return check_stream_plan(p, M, N, mode, smem_optin)
+        assert backward
+        return check_stream_plan(p, M, N, mode, smem_optin, residual)
     C, NS, tpr, K = p["cluster"], p["cols_per_cta"], p["threads_per_row"], p["chunks_per_thread"]
     G, rpg, RT, S = p["groups"], p["rows_per_group"], p["rows_per_tile"], p["stages"]
     threads, smem, ntiles, grid, P = p["threads"], p["smem_bytes"], p["tiles"], p["grid"], p["partials"]

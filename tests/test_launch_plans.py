@@ -196,6 +196,10 @@ def test_stream_plans_in_bounds(mode, monkeypatch):
         p = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
         launch_check.check_plan(p, M, N, mode, True, OPTIN)
         launch_check.check_reduce(p["partials"], N, 2 if mode == 1 else 1)
+        if N <= 262144:  # the fused residual variant (dh in the dx pass's pieces)
+            p = gb.norm_plan(M, N, mode, True, SMS, OPTIN, residual=True)
+            assert p["streamed"] == 1
+            launch_check.check_plan(p, M, N, mode, True, OPTIN, residual=True)
         monkeypatch.delenv("GBNORM_PLAN")
         p = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
         if p["streamed"]:
@@ -214,10 +218,14 @@ def test_stream_default_widths():
         assert p["streamed"] == s, (mode, N)
         if N > 262144 and not s:
             assert p["split_segments"] > 0
-        # the forward and the fused residual backward never stream
+        # the forward never streams; the fused residual backward streams
+        # where the plain one does (its entry points stop at 262144 columns)
         assert gb.norm_plan(4096, N, mode, False, SMS, OPTIN)["streamed"] == 0
         if N <= 262144:
-            assert gb.norm_plan(4096, N, mode, True, SMS, OPTIN, residual=True)["streamed"] == 0
+            pr = gb.norm_plan(4096, N, mode, True, SMS, OPTIN, residual=True)
+            assert pr["streamed"] == s
+            if s:
+                launch_check.check_plan(pr, 4096, N, mode, True, OPTIN, residual=True)
 
 
 def test_wait_hint_only_where_tuned(monkeypatch):

@@ -107,18 +107,43 @@ def test_fused_residual_deterministic_and_matches_unfused():
 @pytest.mark.parametrize("mode,M,N", [(1, 67, 16384), (0, 45, 16384), (1, 33, 24576),
                                       (0, 21, 32768), (1, 19, 65536), (0, 9, 131072),
                                       (0, 5, 262144)])
-def test_fused_residual_long_rows(mode, M, N):
+@pytest.mark.parametrize("stream", ["", "stream=0"], ids=["default", "resident"])
+def test_fused_residual_long_rows(mode, M, N, stream, monkeypatch):
     """Rows wider than one CTA's registers: the long-row kernels (shared-
     memory-resident slices, clusters beyond 16384 / 32768 columns) with the
-    residual tensor in the same stage."""
+    residual tensor in the same stage, and the backward that streams its
+    slices where that is the default (rows of 32768 x 2^k columns); with
+    stream=0 the resident long-row backward at those widths too."""
+    if stream:
+        monkeypatch.setenv("GBNORM_PLAN", stream)
     base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
     case = wl.like(base, M, N)
     for bwd in (False, True):
         p = gb.norm_plan(M, N, mode, bwd, residual=True)
-        assert p["long_rows"] == 1 or p["chunks_per_thread"] * p["threads_per_row"] * 8 >= N
+        assert (p["long_rows"] == 1 or p["streamed"] == 1
+                or p["chunks_per_thread"] * p["threads_per_row"] * 8 >= N)
+        if stream:
+            assert p["streamed"] == 0
     ins = [None if t is None else t.cuda()
            for t in wl.make_residual_inputs(case, "cpu", seed=M + N)]
     x, r, g, b, dy, dh = ins
     outs = _run(x, r, g, b, dy, dh, case.eps, mode)
     _compare(mode, case.eps, x, r, g, b, dy, dh, outs, label=f"long {mode}:{M}x{N}")
+    assert gb.norm_get_device_error() == 0
+
+
+@pytest.mark.parametrize("mode,M,N", [(1, 45, 32768), (0, 81, 65536), (1, 7, 131072),
+                                      (0, 40, 131072), (0, 12, 262144), (1, 5, 262144)])
+def test_fused_residual_streamed_backward(mode, M, N, monkeypatch):
+    """The streamed long-row backward with the residual gradient (stream=1:
+    h and dy read twice, the second time from L2, dh once with the dx
+    pass's pieces)."""
+    monkeypatch.setenv("GBNORM_PLAN", "stream=1")
+    assert gb.norm_plan(M, N, mode, True, residual=True)["streamed"] == 1
+    base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
+    case = wl.like(base, M, N)
+    x, r, g, b, dy, dh = [None if t is None else t.cuda()
+                          for t in wl.make_residual_inputs(case, "cpu", seed=M + N + 1)]
+    outs = _run(x, r, g, b, dy, dh, case.eps, mode)
+    _compare(mode, case.eps, x, r, g, b, dy, dh, outs, label=f"stream resid {mode}:{M}x{N}")
     assert gb.norm_get_device_error() == 0
