@@ -321,16 +321,19 @@ typedef struct {
                                   dx (backward) pass, whose rows_per_tile
                                   rows of one segment make a unit, `tiles`
                                   counting the row tiles; 0 otherwise */
-    int32_t streamed;          /* backward only: 1 when the row slices
-                                  (cols_per_cta columns each) are streamed
-                                  twice through shared memory -- dot
-                                  products, then dx, the second read served
-                                  from L2 -- with the dgamma / dbeta column
-                                  sums held in tensor memory; 0 otherwise */
+    int32_t streamed;          /* 1 when the row slices (cols_per_cta
+                                  columns each) are streamed twice through
+                                  shared memory, the second read served from
+                                  L2: statistics then y (forward), dot
+                                  products then dx with the dgamma / dbeta
+                                  column sums held in tensor memory
+                                  (backward); 0 otherwise */
     int32_t wait_hint_ns;      /* forward, register-resident rows: suspend
                                   hint (ns) of the waits for a stage, so that
                                   a waiting row group issues nothing; 0: the
                                   hardware's default interval */
+    int32_t piece_cols;        /* streamed plans: columns of a slice moved
+                                  per shared-memory stage; 0 otherwise */
 } norm_plan_t;
 
 norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward,

@@ -52,7 +52,7 @@ class Plan(ctypes.Structure):
                 ("partials", ctypes.c_int32), ("exact", ctypes.c_int32),
                 ("long_rows", ctypes.c_int32), ("param_smem_bytes", ctypes.c_int32),
                 ("split_segments", ctypes.c_int32), ("streamed", ctypes.c_int32),
-                ("wait_hint_ns", ctypes.c_int32)]
+                ("wait_hint_ns", ctypes.c_int32), ("piece_cols", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -343,21 +343,36 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
   }
 }
 
-// Plan for the streaming long-row backward (stream.cu): rows of N = C x
-// kStreamSlice columns, a cluster of C CTAs per row (one CTA when C = 1),
-// one row group of kStreamThreads threads per CTA and S pieces in flight.
-constexpr int kStreamStages = 6;
+// Plans of the streaming long-row kernels (stream.cu): rows of C slices, a
+// cluster of C CTAs per row (one CTA when C = 1), one row group of
+// kStreamThreads threads per CTA, slices streamed as pieces of
+// stream_piece_cols(kp) columns with as many pieces in flight as fit (up to
+// kStreamMaxStages).  Pieces of 16384 columns (kp = 4) for RMSNorm, of 8192
+// (kp = 2) for LayerNorm, whose larger per-chunk state spills at 4 chunks,
+// and for the fused residual backward, whose third tensor would leave only
+// two 96 KB stages: from 8192- to 16384-column pieces the RMSNorm backward
+// at 131072 columns went from 85.9 to 93.0 % of measured (fewer waits and
+// refills per byte), LayerNorm's from 74.4 to 69.6 %, the fused residual
+// RMSNorm backward's from 98.7 to 92.8 %.  The override W= sets the piece
+// width (8192 or 16384).
+constexpr int kStreamMaxStages = 12;
+
+int stream_kp(int mode, const Override &ov, bool resid = false) {
+  if (ov.W == stream_piece_cols(2)) return 2;
+  if (ov.W == stream_piece_cols(4)) return 4;
+  return (mode == kRMS && !resid) ? 4 : 2;
+}
 
 bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <= 16; }
 
 // Row widths, in slices of kStreamSlice columns, where the streaming
 // backward measured faster on GB300 (1024 to 4096 rows) than the resident
 // long-row kernel or, beyond NORM_MAX_N_ONEPASS, the two-pass path, in % of
-// the measured copy bandwidth: 1, 2, 4 and 8 slices (RMSNorm 87.2 -> 87.5,
-// 86.9 -> 89.0, 74.3 -> 85.9, 66.1 -> 70.6; LayerNorm 74.8 -> 79.9,
+// the measured copy bandwidth: 1, 2, 4 and 8 slices (RMSNorm 87.2 -> 91.9,
+// 86.9 -> 93.6, 74.3 -> 93.5, 66.1 -> 83.0; LayerNorm 74.8 -> 79.9,
 // 72.7 -> 77.1, 61.7 -> 74.4, 53.0 -> 60.7: the resident kernel's clusters
 // of 8 and 16 occupy only 120 and 112 SMs) and RMSNorm at 16 (two-pass
-// 58.4 -> 63.7).  LayerNorm at 16 slices keeps the two-pass path (57.8
+// 58.4 -> 77.1).  LayerNorm at 16 slices keeps the two-pass path (57.8
 // against 53.9), and slice counts that are not powers of two keep the
 // resident kernel (clusters of 3 measured ~40 %).  The fused residual
 // backward (dh streamed once with the dx pass) takes it at the same widths
@@ -378,17 +393,16 @@ bool use_stream(int N, int mode, const Override &ov) {
   return !ov.any && stream_default(mode, N / kStreamSlice);
 }
 
-norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, Plan *out,
-                          bool resid = false) {
-  if (!stream_applies(N)) return NORM_ERR_UNSUPPORTED;
-  const int C = N / kStreamSlice;
-  if (ov.C && ov.C != C) return NORM_ERR_UNSUPPORTED;
+// The part of a streaming plan both passes share.
+norm_status_t stream_common(int64_t M, int N, int slice, int kp, int ntensors, int smem_optin,
+                            const Override &ov, Plan *out) {
   Plan p;
   p.stream = true;
-  p.resid = resid;
-  p.C = C;
-  p.NS = kStreamSlice;
-  p.nsc = kStreamSlice / 8;
+  p.piece_kp = kp;
+  p.C = N / slice;
+  if (ov.C && ov.C != p.C) return NORM_ERR_UNSUPPORTED;
+  p.NS = slice;
+  p.nsc = slice / 8;
   p.tpr = kStreamThreads;
   p.K = p.nsc / kStreamThreads;
   p.exact = true;
@@ -397,15 +411,61 @@ norm_status_t stream_plan(int64_t M, int N, int smem_optin, const Override &ov, 
   p.RT = 1;
   p.threads = kStreamThreads;
   const int64_t budget = smem_optin - 1024;
-  int S = ov.S ? ov.S : kStreamStages;
-  while (!ov.S && S > 2 && static_cast<int64_t>(stream_layout(S, C, resid).total) > budget) --S;
-  if (S < 2 || static_cast<int64_t>(stream_layout(S, C, resid).total) > budget)
-    return NORM_ERR_UNSUPPORTED;
+  auto bytes = [&](int S) {
+    return static_cast<int64_t>(stream_layout(S, p.C, ntensors, kp).total);
+  };
+  int S = ov.S ? ov.S : kStreamMaxStages;
+  while (!ov.S && S > 2 && bytes(S) > budget) --S;
+  if (S < 2 || bytes(S) > budget) return NORM_ERR_UNSUPPORTED;
   p.S = S;
-  p.smem = stream_layout(S, C, resid).total;
+  p.smem = stream_layout(S, p.C, ntensors, kp).total;
   p.ntiles = M;
   *out = p;
   return NORM_OK;
+}
+
+norm_status_t stream_plan(int64_t M, int N, int mode, int smem_optin, const Override &ov,
+                          Plan *out, bool resid = false) {
+  if (!stream_applies(N)) return NORM_ERR_UNSUPPORTED;
+  const int kp = stream_kp(mode, ov, resid);
+  if (!stream_kernel_ptr(mode, kp, N > kStreamSlice, resid)) return NORM_ERR_UNSUPPORTED;
+  const norm_status_t st =
+      stream_common(M, N, kStreamSlice, kp, resid ? 3 : 2, smem_optin, ov, out);
+  if (st == NORM_OK) out->resid = resid;
+  return st;
+}
+
+// The streaming forward: by default for RMSNorm rows wider than
+// NORM_MAX_N_ONEPASS, in place of the two-pass path (which reads x twice
+// from HBM), with 65536-column slices where at most 16 make a row, else
+// 32768 (RMSNorm 4096 x 524288: two-pass 63.3 %, 32768-column slices in
+// clusters of 16 72.1 %, 65536-column slices in clusters of 8 78.2 %;
+// 1024 x 1048576: 63.4 -> 70.3 %).  The LayerNorm forward keeps the
+// two-pass path there (42.6 against 60.4 % at 2048 x 524288).  Forced by
+// stream=1 at any width it takes (K=8: 32768-column slices, K=16: 65536).
+int stream_fwd_np(int N, int mode, const Override &ov) {
+  if (ov.stream == 0) return 0;
+  const bool forced = ov.stream == 1;
+  if (!forced && (ov.any || N <= NORM_MAX_N_ONEPASS || mode != kRMS)) return 0;
+  const int kp = stream_kp(mode, ov);
+  auto fits = [&](int np) {
+    const int slice = np * stream_piece_cols(kp);
+    const int C = N / slice;
+    return np >= 1 && N % slice == 0 && C >= 1 && C <= 16 && (forced || (C & (C - 1)) == 0) &&
+           stream_fwd_kernel_ptr(mode, kp, np, C > 1) != nullptr;
+  };
+  const int np1 = kStreamSlice / stream_piece_cols(kp);  // 32768-column slices
+  if (ov.K == 8) return fits(np1) ? np1 : 0;
+  if (ov.K == 16) return fits(2 * np1) ? 2 * np1 : 0;
+  if (!forced && fits(2 * np1)) return 2 * np1;
+  if (fits(np1)) return np1;
+  return fits(2 * np1) ? 2 * np1 : 0;
+}
+
+norm_status_t stream_fwd_plan(int64_t M, int N, int mode, int np, int smem_optin,
+                              const Override &ov, Plan *out) {
+  const int kp = stream_kp(mode, ov);
+  return stream_common(M, N, np * stream_piece_cols(kp), kp, 1, smem_optin, ov, out);
 }
 
 // Shape part of the plan for one pass: everything except the grid size.
@@ -431,7 +491,11 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
     }
   }
   if (bwd && !fp8 && use_stream(N, mode, ov))
-    return stream_plan(M, N, smem_optin, ov, out, resid);
+    return stream_plan(M, N, mode, smem_optin, ov, out, resid);
+  if (!bwd && !resid && !fp8) {
+    const int np = stream_fwd_np(N, mode, ov);
+    if (np) return stream_fwd_plan(M, N, mode, np, smem_optin, ov, out);
+  }
   const int kmax = bwd ? kMaxKBwd : kMaxKFwd;
   const int nc = N / 8;
   Plan p;
@@ -568,7 +632,10 @@ norm_status_t shape_plan(int mode, bool bwd, int64_t M, int N, int smem_optin,
 
 const void *kernel_for(const Plan &p, int mode, bool bwd) {
   if (p.split) return split_kernel_ptr(mode, p.phase, p.K);
-  if (p.stream) return stream_kernel_ptr(mode, p.C > 1, p.resid);
+  if (p.stream)
+    return bwd ? stream_kernel_ptr(mode, p.piece_kp, p.C > 1, p.resid)
+               : stream_fwd_kernel_ptr(mode, p.piece_kp, p.NS / stream_piece_cols(p.piece_kp),
+                                       p.C > 1);
   if (p.long_rows) return long_kernel_ptr(mode, p.K, p.C > 1, p.exact, bwd, p.resid);
   return bwd ? bwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid)
              : fwd_kernel_ptr(mode, p.K, p.C > 1, p.exact, p.resid, p.gsm, p.wait_ns > 0);
@@ -669,10 +736,10 @@ norm_status_t finish_plan(const DeviceInfo &d, int dev, int mode, bool bwd, cons
 // units in flight, and a persistent grid of at most one CTA per unit.
 constexpr int kSplitW = 4096;
 
-// (`bwd_mode`: the mode of a backward pass, whose rows may take the
-// streaming kernel instead; -1 for a forward pass)
-bool use_split(int N, const Override &ov, int bwd_mode = -1) {
-  if (bwd_mode >= 0 && use_stream(N, bwd_mode, ov)) return false;
+// (rows the streaming kernels take do not: the backward's, and the
+// forward's beyond NORM_MAX_N_ONEPASS)
+bool use_split(int N, const Override &ov, int mode, bool bwd) {
+  if (bwd ? use_stream(N, mode, ov) : stream_fwd_np(N, mode, ov) != 0) return false;
   return ov.split == 1 || (ov.split != 0 && N > NORM_MAX_N_ONEPASS);
 }
 
@@ -946,6 +1013,7 @@ void fill_plan(const Plan &p, norm_plan_t *out) {
   out->param_smem_bytes = p.par_bpc * p.NS;
   out->split_segments = p.split ? p.nseg : 0;
   out->streamed = p.stream ? 1 : 0;
+  out->piece_cols = p.stream ? stream_piece_cols(p.piece_kp) : 0;
   out->wait_hint_ns = p.wait_ns;
 }
 
@@ -1014,7 +1082,7 @@ std::vector<Override> tune_candidates(bool bwd, int N) {
 bool same_plan(const Plan &a, const Plan &b) {
   return a.C == b.C && a.tpr == b.tpr && a.K == b.K && a.G == b.G && a.rpg == b.rpg &&
          a.S == b.S && a.gsm == b.gsm && a.long_rows == b.long_rows && a.grid == b.grid &&
-         a.stream == b.stream && a.wait_ns == b.wait_ns;
+         a.stream == b.stream && a.piece_kp == b.piece_kp && a.wait_ns == b.wait_ns;
 }
 
 // Times `run` (one launch of the pass with the plan installed in the cache
@@ -1026,7 +1094,7 @@ norm_status_t tune_pass(int mode, bool bwd, int64_t M, int N, size_t ws_bytes, i
   if (read_override().any) return NORM_ERR_ARG;  // a plan override bypasses the cache
   norm_status_t st = run();                      // validates, caches the default plan
   if (st != NORM_OK) return st;
-  if (use_split(N, Override(), bwd ? mode : -1)) {  // the two-pass path keeps its plan
+  if (use_split(N, Override(), mode, bwd)) {  // the two-pass path keeps its plan
     if (chosen) {
       norm_plan_t pl;
       if ((st = norm_plan(M, N, static_cast<norm_mode_t>(mode), bwd ? 1 : 0, 0, 0, &pl)) !=
@@ -1147,7 +1215,7 @@ norm_status_t norm_fwd(const void *x, const void *gamma, const void *beta, int64
   DeviceInfo d;
   int dev = 0;
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
-  const bool split = use_split(static_cast<int>(N), read_override());
+  const bool split = use_split(static_cast<int>(N), read_override(), mode, false);
   Plan sp[2];
   Plan &p = sp[0];
   if (split) {
@@ -1194,7 +1262,7 @@ static norm_status_t bwd_workspace(int64_t M, int64_t N, norm_mode_t mode, bool 
   if ((st = device_info(&d, &dev)) != NORM_OK) return st;
   Override ov = read_override();
   if (no_stream) ov.stream = 0;
-  if (use_split(static_cast<int>(N), ov, mode)) {
+  if (use_split(static_cast<int>(N), ov, mode, true)) {
     Plan sp[2];
     if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
       return st;
@@ -1234,7 +1302,7 @@ static norm_status_t bwd_run(const void *dy, const void *x, const void *gamma, c
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Override ov = read_override();
   if (no_stream) ov.stream = 0;
-  if (use_split(static_cast<int>(N), ov, mode)) {
+  if (use_split(static_cast<int>(N), ov, mode, true)) {
     Plan sp[2];
     if ((st = make_split_plans(d, dev, mode, true, M, static_cast<int>(N), sp)) != NORM_OK)
       return st;
@@ -1442,7 +1510,7 @@ norm_status_t norm_plan(int64_t M, int64_t N, norm_mode_t mode, int backward, in
   if ((resid || fp8) && N > NORM_MAX_N_FUSED) return NORM_ERR_SHAPE;
   Plan p;
   const Override ov = read_override();
-  if (!resid && !fp8 && use_split(static_cast<int>(N), ov, bwd ? mode : -1)) {
+  if (!resid && !fp8 && use_split(static_cast<int>(N), ov, mode, bwd)) {
     // the two-pass path: its statistics (forward) or dx (backward) pass,
     // or with bit 3 the output (forward) or dot-product (backward) pass
     const int phase = bwd ? (other ? kSplitBwdDots : kSplitBwdDx)

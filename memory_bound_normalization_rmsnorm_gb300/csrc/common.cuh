@@ -133,7 +133,8 @@ struct Plan {
   bool split = false;  // two-pass path: rows cut into nseg segments of NS columns
   int nseg = 0;
   int phase = 0;       // two-pass path: which of its passes (kSplit*)
-  bool stream = false; // backward: the streaming long-row kernel (stream.cu)
+  bool stream = false; // the streaming long-row kernels (stream.cu)
+  int piece_kp = 0;    // streaming: chunks per thread per piece
   int wait_ns = 0;     // register-resident forward: suspend hint of its stage waits
 };
 
@@ -192,29 +193,31 @@ const void *split_fold_kernel_ptr(int mode, bool bwd);
 const void *split_reduce_kernel_ptr();
 SmemLayout split_smem_layout(int RT, int NS, int S, int G, int tpr, int ntensors);
 
-// The streaming long-row backward (stream.cu): one row group of
-// kStreamThreads threads per CTA, each CTA owning kStreamSlice columns of a
-// row (a cluster of N / kStreamSlice CTAs), streamed twice through a ring of
-// pieces of kStreamPiece columns (kStreamKP chunks per thread).
+// The streaming long-row kernels (stream.cu): one row group of
+// kStreamThreads threads per CTA, each CTA owning a slice of a row
+// (kStreamSlice columns in the backward, a cluster of N / kStreamSlice CTAs;
+// that or twice as many in the forward), streamed twice through a ring of
+// pieces of kStreamThreads x kp x 8 columns (kp 16-byte chunks per thread).
 constexpr int kStreamThreads = 512;
-constexpr int kStreamKP = 2;
-constexpr int kStreamPiece = kStreamThreads * kStreamKP * 8;
-constexpr int kStreamSlice = 4 * kStreamPiece;
-// Its shared memory: S stages of one piece of x and dy (and, for the fused
-// residual backward, of dh, which only the dx pass loads), the per-warp row
-// partials ([kXchBuffers][warps][2] floats, then kXchBuffers arrival
-// counters), the exchange slots and their mbarriers ([kXchBuffers][C] float4,
-// also for C = 1), the stage mbarriers, then the abort flag, the per-stage
-// warp counters and the tensor-memory address slot.
-__host__ __device__ inline SmemLayout stream_layout(int S, int C, bool resid = false) {
+constexpr int kStreamSlice = 32768;
+__host__ __device__ constexpr int stream_piece_cols(int kp) { return kStreamThreads * kp * 8; }
+// Their shared memory: S stages of `ntensors` pieces -- x (forward), x and dy
+// (backward), x, dy and dh (fused residual backward; only the dx pass loads
+// dh) -- the per-warp row partials ([kXchBuffers][warps][2] floats for the
+// backward's two sums, [..][4] for the forward's (mean, M2) pairs, then
+// kXchBuffers arrival counters), the exchange slots and their mbarriers
+// ([kXchBuffers][C] float4, also for C = 1), the stage mbarriers, then the
+// abort flag, the per-stage warp counters and the tensor-memory address slot.
+__host__ __device__ inline SmemLayout stream_layout(int S, int C, int ntensors, int kp) {
   SmemLayout L;
-  L.tensor_bytes = static_cast<uint32_t>(kStreamPiece) * 2u;
-  L.stage_bytes = (resid ? 3u : 2u) * L.tensor_bytes;
+  L.tensor_bytes = static_cast<uint32_t>(stream_piece_cols(kp)) * 2u;
+  L.stage_bytes = static_cast<uint32_t>(ntensors) * L.tensor_bytes;
   uint32_t off = L.stage_bytes * static_cast<uint32_t>(S);
   L.par_off = off;
   L.stats_off = off;
   L.red_off = off;
-  off = align16(off + static_cast<uint32_t>(kXchBuffers * (kStreamThreads / 32) * 2) * 4u +
+  const int per_warp = ntensors == 1 ? 4 : 2;
+  off = align16(off + static_cast<uint32_t>(kXchBuffers * (kStreamThreads / 32) * per_warp) * 4u +
                 4u * kXchBuffers);
   L.xch_off = off;
   off = align16(off + static_cast<uint32_t>(kXchBuffers * C * 4) * 4u + 8u * kXchBuffers);
@@ -225,7 +228,11 @@ __host__ __device__ inline SmemLayout stream_layout(int S, int C, bool resid = f
   L.total = off;
   return L;
 }
-// Kernel by (mode, cluster or single CTA, fused residual).
-const void *stream_kernel_ptr(int mode, bool cluster, bool resid = false);
+// Backward kernel by (mode, chunks per thread per piece: 2 or 4, cluster or
+// single CTA, fused residual); nullptr if not instantiated.
+const void *stream_kernel_ptr(int mode, int kp, bool cluster, bool resid = false);
+// Forward kernel by (mode, kp, pieces per slice, cluster); nullptr if not
+// instantiated.
+const void *stream_fwd_kernel_ptr(int mode, int kp, int np, bool cluster);
 
 }  // namespace gbn

@@ -40,9 +40,6 @@ namespace gbn {
 
 namespace {
 
-constexpr int kKP = kStreamKP;   // 16-byte chunks per thread per piece
-constexpr int kW = kStreamPiece;  // piece width (columns)
-static_assert(kW == kStreamThreads * kKP * 8, "piece = threads x chunks x 8 columns");
 
 // L2 policy of pass 1's reads (their data is read again by pass 2).
 __device__ __forceinline__ uint64_t l2_normal_policy() {
@@ -114,8 +111,11 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 // One CTA per (row, 32768-column slice); NP pieces of kW columns per slice.
 // RESID: the fused residual backward, dx = (norm backward at h) + dh, dh
 // streamed once with the dx pass's pieces (a.x holds h, a.res dh).
-template <int MODE, int NP, bool CLUSTER, bool RESID>
+template <int MODE, int KP, bool CLUSTER, bool RESID>
 __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(const NormArgs a) {
+  constexpr int kKP = KP;                          // 16-byte chunks per thread per piece
+  constexpr int kW = stream_piece_cols(KP);        // piece width (columns)
+  constexpr int NP = kStreamSlice / kW;            // pieces per slice
   constexpr int NACC = MODE == kLayer ? 2 : 1;          // dgamma (and dbeta)
   constexpr int CPC = 8 * NACC;                          // TMEM columns per chunk
   constexpr int TCW = NP * kKP * CPC;                    // columns per warp quarter group
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
   constexpr int kStride = kStreamThreads * 16;           // bytes between a thread's chunks
 
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1, RESID);
+  const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1, RESID ? 3 : 2, KP);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *wred = reinterpret_cast<float *>(smem + L.red_off);  // [buffer][warp][2]
   int *wcnt = reinterpret_cast<int *>(wred + kXchBuffers * kNW * 2);
@@ -422,19 +422,276 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
   if (CLUSTER) cluster_sync();
 }
 
-template <int MODE, int NP, bool RESID>
+// Streaming forward for rows too wide for a resident slice: the same piece
+// sequence over 32768-column slices (65536 for RMSNorm's 8-piece variant),
+// pass 1 the row statistics from HBM, pass 2 y from the L2 copy pass 1 left.
+// Statistics per thread: sum x^2 (RMSNorm), or per piece (16 values in
+// registers) its mean and sum of squared deviations, merged into a running
+// (mean, M2) weighted by counts (LayerNorm); then an equal-count butterfly
+// over the warp, the last warp to finish the row folds the 16 warp partials
+// pairwise and publishes the CTA's, and the cluster merges its CTAs' in rank
+// order.  gamma (and beta) stay in registers.
+template <int MODE, int KP, int NP, bool CLUSTER>
+__global__ void __launch_bounds__(kStreamThreads, 1) norm_fwd_stream_kernel(const NormArgs a) {
+  constexpr int kKP = KP;
+  constexpr int kW = stream_piece_cols(KP);
+  constexpr int kNW = kStreamThreads / 32;
+  constexpr int kStride = kStreamThreads * 16;
+  constexpr int kPW = 4;  // floats per warp partial
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemLayout L = stream_layout(a.S, CLUSTER ? a.C : 1, 1, KP);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+  float *wred = reinterpret_cast<float *>(smem + L.red_off);  // [buffer][warp][4]
+  int *wcnt = reinterpret_cast<int *>(wred + kXchBuffers * kNW * kPW);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag_off);
+  int *done_cnt = reinterpret_cast<int *>(smem + L.flag_off) + 1;
+
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : blockIdx.x;
+  const int64_t ncl = CLUSTER ? static_cast<int64_t>(ncluster_x()) : gridDim.x;
+  const int64_t col0 = static_cast<int64_t>(crank) * a.NS;
+  const int64_t nr = cid < a.M ? (a.M - cid + ncl - 1) / ncl : 0;
+  const int64_t total = 2 * NP * nr;
+
+  if (t == 0) {
+    for (int s = 0; s < a.S; ++s) {
+      mbar_init(full + s, 1);
+      done_cnt[s] = 0;
+    }
+    uint64_t *xb = xch_bars(smem, L, 1, CLUSTER ? a.C : 1);
+    for (int b = 0; b < kXchBuffers; ++b) {
+      mbar_init(xb + b, 1);
+      wcnt[b] = 0;
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  grid_launch_dependents();
+  grid_dependency_wait();
+
+  uint4 gv[NP][kKP], bv[NP][kKP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p)
+#pragma unroll
+    for (int k = 0; k < kKP; ++k) {
+      const int64_t c = col0 + p * kW + (k * kStreamThreads + t) * 8;
+      gv[p][k] = ld_global_nc_v4(a.gamma + c);
+      bv[p][k] = (MODE == kLayer && a.beta != nullptr) ? ld_global_nc_v4(a.beta + c)
+                                                      : make_uint4(0, 0, 0, 0);
+    }
+
+  if (CLUSTER) cluster_sync(); else __syncthreads();
+
+  const uint64_t pol1 = l2_normal_policy();
+  const uint64_t pol2 = l2_evict_first_policy();
+  auto issue = [&](int64_t q, int s) {
+    int pass, p;
+    int64_t j;
+    piece_at(q, NP, nr, pass, j, p);
+    const int64_t off = (cid + j * ncl) * a.N + col0 + static_cast<int64_t>(p) * kW;
+    uint64_t *bar = full + s;
+    mbar_arrive_expect_tx(bar, L.tensor_bytes);
+    bulk_g2s(smem + static_cast<size_t>(s) * L.stage_bytes, a.x + off, L.tensor_bytes, bar,
+             pass ? pol2 : pol1);
+  };
+  if (t == 0) {
+    for (int64_t q = 0; q < total && q < a.S; ++q) issue(q, static_cast<int>(q));
+  }
+  auto release = [&](int64_t q, int s) {
+    if (last_warp_done(done_cnt, s, kNW)) {
+      const int64_t next = q + a.S;
+      if (next < total && (t & 31) == 0) {
+        fence_proxy_async_smem();
+        issue(next, s);
+      }
+    }
+  };
+
+  ClusterXch xch = make_xch(smem, L, 1, CLUSTER ? a.C : 1, crank);
+  const float invN = a.invN;
+  constexpr float kPerThread = 8.f * kKP * NP;  // elements of a row slice per thread
+  int s = 0;
+  uint32_t par = 0;
+  int64_t q = 0;
+  auto advance = [&]() {
+    ++q;
+    if (++s == a.S) {
+      s = 0;
+      par ^= 1u;
+    }
+  };
+
+  for (int64_t j = 0; j <= nr; ++j) {
+    if (j < nr) {
+      // ---- pass 1 of row j: this thread's statistics, then the CTA's
+      float m = 0.f, m2 = 0.f;
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        mbar_wait(full + s, par, a.err, abort_flag);
+        const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes + t * 16;
+        float2 xf[kKP][4];
+#pragma unroll
+        for (int k = 0; k < kKP; ++k) chunk_to_f2(lds_v4(st + k * kStride), xf[k]);
+        release(q, s);
+        advance();
+        if (MODE == kLayer) {
+          float2 s0 = splat2(0.f), s1 = splat2(0.f);
+#pragma unroll
+          for (int k = 0; k < kKP; ++k) {
+            s0 = add2(s0, add2(xf[k][0], xf[k][1]));
+            s1 = add2(s1, add2(xf[k][2], xf[k][3]));
+          }
+          const float2 st2 = add2(s0, s1);
+          const float mp = (st2.x + st2.y) * (1.f / (8.f * kKP));
+          const float2 nm = splat2(-mp);
+          float2 q0 = splat2(0.f), q1 = splat2(0.f);
+#pragma unroll
+          for (int k = 0; k < kKP; ++k) {
+            const float2 d0 = add2(xf[k][0], nm), d1 = add2(xf[k][1], nm);
+            const float2 d2 = add2(xf[k][2], nm), d3 = add2(xf[k][3], nm);
+            q0 = fma2(d0, d0, fma2(d1, d1, q0));
+            q1 = fma2(d2, d2, fma2(d3, d3, q1));
+          }
+          const float2 qt = add2(q0, q1);
+          const float qp = qt.x + qt.y;
+          if (p == 0) {
+            m = mp;
+            m2 = qp;
+          } else {
+            // running partial over p pieces merged with piece p (counts 16p, 16)
+            ms_merge(m, m2, mp, qp, 1.f / static_cast<float>(p + 1),
+                     8.f * kKP * static_cast<float>(p) / static_cast<float>(p + 1));
+          }
+        } else {
+          float2 q0 = splat2(0.f), q1 = splat2(0.f);
+#pragma unroll
+          for (int k = 0; k < kKP; ++k) {
+            q0 = fma2(xf[k][0], xf[k][0], fma2(xf[k][1], xf[k][1], q0));
+            q1 = fma2(xf[k][2], xf[k][2], fma2(xf[k][3], xf[k][3], q1));
+          }
+          const float2 qt = add2(q0, q1);
+          m2 += qt.x + qt.y;
+        }
+      }
+      // warp: butterfly (equal counts for LayerNorm's merges)
+      float h = 0.5f * kPerThread;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float qo = __shfl_xor_sync(0xffffffffu, m2, o);
+        if (MODE == kLayer) {
+          const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+          ms_merge_equal(m, m2, mo, qo, h);
+          h *= 2.f;
+        } else {
+          m2 += qo;
+        }
+      }
+      const int rb = xch.push_buf;
+      float *slots = wred + rb * kNW * kPW;
+      if ((t & 31) == 0) {
+        slots[kPW * warp] = m;
+        slots[kPW * warp + 1] = m2;
+      }
+      if (last_warp_done(wcnt, rb, kNW) && (t & 31) == 0) {
+        float M = 0.f, Q = 0.f;
+        if (MODE == kLayer) {
+          tree_fold<kNW>(slots, 32.f * kPerThread, M, Q);
+        } else {
+          Q = slots[1];
+          for (int w = 1; w < kNW; ++w) Q += slots[kPW * w + 1];
+        }
+        xch_publish<CLUSTER>(M, Q, xch);
+      }
+      xch.push_buf = (rb + 1) % kXchBuffers;
+    }
+    if (j >= 1) {
+      // ---- pass 2 of row j - 1: y
+      const float *rowx = cluster_wait_row(0, xch, a.err, abort_flag);
+      float mu = 0.f, rs;
+      if (MODE == kLayer) {
+        float mm = rowx[0], qq = rowx[1];
+        const float ncta = static_cast<float>(a.NS);
+        for (int k = 1; k < xch.C; ++k) {
+          const float wb = 1.0f / static_cast<float>(k + 1);
+          ms_merge(mm, qq, rowx[k * 4], rowx[k * 4 + 1], wb, ncta * static_cast<float>(k) * wb);
+        }
+        mu = mm;
+        rs = rsqrtf(qq * invN + a.eps);
+      } else {
+        float v[1];
+        fold_sum<1>(rowx + 1, xch.C, v);
+        rs = rsqrtf(v[0] * invN + a.eps);
+      }
+      const int64_t row = cid + (j - 1) * ncl;
+      if (t == 0 && crank == 0) {
+        a.rstd[row] = rs;
+        if (MODE == kLayer) a.mean[row] = mu;
+      }
+      const float2 rs2 = splat2(rs), nmu = splat2(-mu);
+      uint16_t *yrow = a.out + row * a.N + col0 + t * 8;
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        mbar_wait(full + s, par, a.err, abort_flag);
+        const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes + t * 16;
+#pragma unroll
+        for (int k = 0; k < kKP; ++k) {
+          float2 xf[4], gf[4], bf[4], o[4];
+          chunk_to_f2(lds_v4(st + k * kStride), xf);
+          chunk_to_f2(gv[p][k], gf);
+          if (MODE == kLayer) chunk_to_f2(bv[p][k], bf);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 xh = mul2(MODE == kLayer ? add2(xf[e], nmu) : xf[e], rs2);
+            o[e] = (MODE == kLayer) ? fma2(xh, gf[e], bf[e]) : mul2(xh, gf[e]);
+          }
+          st_global_cs_v4(yrow + p * kW + k * kStreamThreads * 8, f2_to_chunk(o));
+        }
+        release(q, s);
+        advance();
+      }
+    }
+  }
+  if (CLUSTER) cluster_sync();
+}
+
+template <int MODE, int KP, int NP>
+const void *stream_fwd_ptr(bool cluster) {
+  return cluster ? reinterpret_cast<const void *>(&norm_fwd_stream_kernel<MODE, KP, NP, true>)
+                 : reinterpret_cast<const void *>(&norm_fwd_stream_kernel<MODE, KP, NP, false>);
+}
+
+template <int MODE, int KP, bool RESID>
 const void *stream_ptr(bool cluster) {
-  return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<MODE, NP, true, RESID>)
-                 : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<MODE, NP, false, RESID>);
+  return cluster ? reinterpret_cast<const void *>(&norm_bwd_stream_kernel<MODE, KP, true, RESID>)
+                 : reinterpret_cast<const void *>(&norm_bwd_stream_kernel<MODE, KP, false, RESID>);
 }
 
 }  // namespace
 
-const void *stream_kernel_ptr(int mode, bool cluster, bool resid) {
-  constexpr int NP = kStreamSlice / kW;
-  if (mode == kLayer)
-    return resid ? stream_ptr<kLayer, NP, true>(cluster) : stream_ptr<kLayer, NP, false>(cluster);
-  return resid ? stream_ptr<kRMS, NP, true>(cluster) : stream_ptr<kRMS, NP, false>(cluster);
+// Instantiated: 2 chunks per thread per piece (8192-column pieces) for both
+// modes, and 4 (16384) for RMSNorm, whose dx pass keeps half the
+// accumulator registers per chunk of LayerNorm's (dgamma only).
+const void *stream_kernel_ptr(int mode, int kp, bool cluster, bool resid) {
+  if (mode == kLayer) {
+    if (kp != 2) return nullptr;
+    return resid ? stream_ptr<kLayer, 2, true>(cluster) : stream_ptr<kLayer, 2, false>(cluster);
+  }
+  if (kp == 4) return resid ? stream_ptr<kRMS, 4, true>(cluster) : stream_ptr<kRMS, 4, false>(cluster);
+  if (kp == 2) return resid ? stream_ptr<kRMS, 2, true>(cluster) : stream_ptr<kRMS, 2, false>(cluster);
+  return nullptr;
+}
+
+// Forward: RMSNorm with 16384-column pieces, two or four per slice (32768 or
+// 65536 columns); LayerNorm with four 8192-column pieces.
+const void *stream_fwd_kernel_ptr(int mode, int kp, int np, bool cluster) {
+  if (mode == kLayer) return (kp == 2 && np == 4) ? stream_fwd_ptr<kLayer, 2, 4>(cluster) : nullptr;
+  if (kp != 4) return nullptr;
+  if (np == 2) return stream_fwd_ptr<kRMS, 4, 2>(cluster);
+  if (np == 4) return stream_fwd_ptr<kRMS, 4, 4>(cluster);
+  return nullptr;
 }
 
 }  // namespace gbn

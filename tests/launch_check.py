@@ -42,21 +42,21 @@ def smem_layout(RT, NS, S, G, tpr, ntensors, stats, C, par_bytes=0):
 
 
 STREAM_THREADS = 512
-STREAM_KP = 2                                  # chunks per thread per piece
-STREAM_PIECE = STREAM_THREADS * STREAM_KP * 8  # columns per piece
-STREAM_NP = 4                                  # pieces per slice
-STREAM_SLICE = STREAM_NP * STREAM_PIECE
+STREAM_SLICE = 32768  # backward slice; the forward's is this or twice it
 
 
-def stream_layout(S, C, resid=False):
-    """Shared memory of the streaming backward, in the kernel's order (a
-    third tensor per stage, dh, for the fused residual backward)."""
-    tensor = STREAM_PIECE * 2
-    stage = (3 if resid else 2) * tensor
+def stream_layout(S, C, ntensors, piece):
+    """Shared memory of the streaming kernels, in their order: stages of
+    `piece` columns of x (forward), x and dy (backward) or x, dy and dh
+    (fused residual backward)."""
+    tensor = piece * 2
+    stage = ntensors * tensor
     off = stage * S
     L = {"tensor": tensor, "stage": stage, "red": off}
-    # per-warp row partials [buffer][warp][2] floats, then one counter per buffer
-    off = _align16(off + XCH_BUFFERS * (STREAM_THREADS // 32) * 2 * 4 + 4 * XCH_BUFFERS)
+    # per-warp row partials [buffer][warp][2 or 4] floats, then one counter per buffer
+    per_warp = 4 if ntensors == 1 else 2
+    L["per_warp"] = per_warp
+    off = _align16(off + XCH_BUFFERS * (STREAM_THREADS // 32) * per_warp * 4 + 4 * XCH_BUFFERS)
     L["xch"] = off
     off = _align16(off + XCH_BUFFERS * C * 4 * 4 + 8 * XCH_BUFFERS)  # also for C = 1
     L["bar"] = off
@@ -80,64 +80,71 @@ def stream_piece_at(q, np_, nr):
     return 1, nr - 1, w
 
 
-def check_stream_plan(p, M, N, mode, smem_optin=232448, residual=False):
-    """The streaming backward's accesses for plan `p`: every (row, pass,
+def check_stream_plan(p, M, N, mode, smem_optin=232448, residual=False, backward=True):
+    """The streaming kernels' accesses for plan `p`: every (row, pass,
     piece) issued once per cluster in pipeline order, each bulk copy inside
-    x / dy and 16-byte aligned, the shared-memory regions in bounds, the
-    tensor-memory columns within 512 and the partial rows inside the
-    workspace."""
+    its tensor and 16-byte aligned, the shared-memory regions in bounds, the
+    backward's tensor-memory columns within 512 and its partial rows inside
+    the workspace."""
     C, NS, S, grid, P = p["cluster"], p["cols_per_cta"], p["stages"], p["grid"], p["partials"]
     assert p["streamed"] == 1 and p["threads"] == STREAM_THREADS and p["exact"] == 1
-    assert NS == STREAM_SLICE and N == C * NS and 1 <= C <= 16
+    piece = p["piece_cols"]
+    kp = piece // (STREAM_THREADS * 8)  # chunks per thread per piece
+    assert kp in (2, 4) and piece == STREAM_THREADS * kp * 8
+    np_ = NS // piece
+    assert NS % piece == 0 and N == C * NS and 1 <= C <= 16
+    assert NS == STREAM_SLICE or (not backward and NS == 2 * STREAM_SLICE)
     assert p["chunks_per_thread"] * STREAM_THREADS * 8 == NS
     assert p["tiles"] == M and grid % C == 0 and grid // C == P and 1 <= P <= M
-    L = stream_layout(S, C, residual)
+    nt = (3 if residual else 2) if backward else 1
+    L = stream_layout(S, C, nt, piece)
     assert p["smem_bytes"] == L["total"] <= smem_optin - 1024 and S >= 2
-    # pass 1 pieces land x and dy, pass 2 pieces also dh: inside the stage
-    assert (3 if residual else 2) * L["tensor"] == L["stage"]
+    # pass 1 pieces land x (and dy), pass 2 pieces also dh: inside the stage
+    assert nt * L["tensor"] == L["stage"]
     assert L["stage"] < TX_LIMIT and L["bar"] % 8 == 0 and L["flag"] % 4 == 0
-    # per-warp partials (buffer < 4, warp < 16, 2 floats), the 4 counters,
-    # then the exchange slots [buffer][rank] and their 4 mbarriers
-    warps = STREAM_THREADS // 32
-    hi = ((XCH_BUFFERS - 1) * warps + (warps - 1)) * 2 + 2
-    assert L["red"] + hi * 4 <= L["red"] + XCH_BUFFERS * warps * 2 * 4
-    assert L["red"] + XCH_BUFFERS * warps * 2 * 4 + 4 * XCH_BUFFERS <= L["xch"]
+    # per-warp partials (buffer < 4, warp < 16, 2 or 4 floats), the 4
+    # counters, then the exchange slots [buffer][rank] and their 4 mbarriers
+    warps, pw = STREAM_THREADS // 32, L["per_warp"]
+    hi = ((XCH_BUFFERS - 1) * warps + (warps - 1)) * pw + pw
+    assert L["red"] + hi * 4 <= L["red"] + XCH_BUFFERS * warps * pw * 4
+    assert L["red"] + XCH_BUFFERS * warps * pw * 4 + 4 * XCH_BUFFERS <= L["xch"]
     bars = L["xch"] + XCH_BUFFERS * C * 16
     assert bars % 8 == 0 and bars + 8 * XCH_BUFFERS <= L["bar"]
     # thread t, chunk k of a piece: smem byte t*16 + k*threads*16 (+16) in the
     # tensor; global column piece*W + (k*threads + t)*8 (+8) in the slice
-    assert (STREAM_THREADS - 1) * 16 + (STREAM_KP - 1) * STREAM_THREADS * 16 + 16 <= L["tensor"]
-    assert (STREAM_NP - 1) * STREAM_PIECE + ((STREAM_KP - 1) * STREAM_THREADS
-                                               + STREAM_THREADS - 1) * 8 + 8 <= NS
+    assert (STREAM_THREADS - 1) * 16 + (kp - 1) * STREAM_THREADS * 16 + 16 <= L["tensor"]
+    assert (np_ - 1) * piece + ((kp - 1) * STREAM_THREADS + STREAM_THREADS - 1) * 8 + 8 <= NS
     nacc = 2 if mode == 1 else 1
     groups = STREAM_THREADS // 32 // 4
-    assert groups * STREAM_NP * STREAM_KP * 8 * nacc <= 512, "accumulators exceed TMEM"
+    if backward:
+        assert groups * np_ * kp * 8 * nacc <= 512, "accumulators exceed TMEM"
     seen = 0
     for cid in range(P):
         nr = -(-(M - cid) // P)
         order = []
-        for q in range(2 * STREAM_NP * nr):
-            ps, j, pc = stream_piece_at(q, STREAM_NP, nr)
-            assert 0 <= j < nr and 0 <= pc < STREAM_NP
+        for q in range(2 * np_ * nr):
+            ps, j, pc = stream_piece_at(q, np_, nr)
+            assert 0 <= j < nr and 0 <= pc < np_
             row = cid + j * P
             assert row < M
             for crank in range(C):
-                off = row * N + crank * NS + pc * STREAM_PIECE
-                assert (off * 2) % 16 == 0 and off + STREAM_PIECE <= M * N
+                off = row * N + crank * NS + pc * piece
+                assert (off * 2) % 16 == 0 and off + piece <= M * N
             order.append((ps, j, pc))
-        assert len(set(order)) == len(order) == 2 * STREAM_NP * nr
+        assert len(set(order)) == len(order) == 2 * np_ * nr
         # consumed in this order by the kernel's loop: pass 1 of row j, then
         # pass 2 of row j - 1, each piece in increasing order
         want = []
         for j in range(nr + 1):
             if j < nr:
-                want += [(0, j, pc) for pc in range(STREAM_NP)]
+                want += [(0, j, pc) for pc in range(np_)]
             if j >= 1:
-                want += [(1, j - 1, pc) for pc in range(STREAM_NP)]
+                want += [(1, j - 1, pc) for pc in range(np_)]
         assert order == want
         seen += nr
-        last = ((nacc - 1) * P + cid) * N + (C - 1) * NS + NS
-        assert last <= nacc * P * N, "partial row write out of the workspace"
+        if backward:
+            last = ((nacc - 1) * P + cid) * N + (C - 1) * NS + NS
+            assert last <= nacc * P * N, "partial row write out of the workspace"
     assert seen == M
     return True
 
@@ -146,8 +153,8 @@ def check_plan(p, M, N, mode, backward, smem_optin=232448, residual=False):
     """Raise AssertionError if any access of the launch described by `p`
     (a norm_plan dict) would leave its buffer or break an alignment rule."""
     if p.get("streamed"):
-        assert backward
-        return check_stream_plan(p, M, N, mode, smem_optin, residual)
+        assert not (residual and not backward)
+        return check_stream_plan(p, M, N, mode, smem_optin, residual, backward)
     C, NS, tpr, K = p["cluster"], p["cols_per_cta"], p["threads_per_row"], p["chunks_per_thread"]
     G, rpg, RT, S = p["groups"], p["rows_per_group"], p["rows_per_tile"], p["stages"]
     threads, smem, ntiles, grid, P = p["threads"], p["smem_bytes"], p["tiles"], p["grid"], p["partials"]

@@ -196,6 +196,12 @@ def test_stream_plans_in_bounds(mode, monkeypatch):
         p = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
         launch_check.check_plan(p, M, N, mode, True, OPTIN)
         launch_check.check_reduce(p["partials"], N, 2 if mode == 1 else 1)
+        assert p["piece_cols"] == (16384 if mode == 0 else 8192)
+        monkeypatch.setenv("GBNORM_PLAN", "stream=1,W=8192")  # RMSNorm's 8192-column pieces
+        p8 = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
+        assert p8["piece_cols"] == 8192
+        launch_check.check_plan(p8, M, N, mode, True, OPTIN)
+        monkeypatch.setenv("GBNORM_PLAN", "stream=1")
         if N <= 262144:  # the fused residual variant (dh in the dx pass's pieces)
             p = gb.norm_plan(M, N, mode, True, SMS, OPTIN, residual=True)
             assert p["streamed"] == 1
@@ -218,9 +224,17 @@ def test_stream_default_widths():
         assert p["streamed"] == s, (mode, N)
         if N > 262144 and not s:
             assert p["split_segments"] > 0
-        # the forward never streams; the fused residual backward streams
-        # where the plain one does (its entry points stop at 262144 columns)
-        assert gb.norm_plan(4096, N, mode, False, SMS, OPTIN)["streamed"] == 0
+        # the forward streams only RMSNorm rows beyond 262144 columns
+        # (slices of 65536, else 32768, in clusters of up to 16); the fused
+        # residual backward streams where the plain one does (its entry
+        # points stop at 262144 columns)
+        pf = gb.norm_plan(4096, N, mode, False, SMS, OPTIN)
+        fwd_streams = mode == 0 and N > 262144 and N // 65536 <= 16
+        if fwd_streams:
+            assert pf["cols_per_cta"] == 65536 and pf["piece_cols"] == 16384
+        assert pf["streamed"] == int(fwd_streams), (mode, N, pf)
+        if fwd_streams:
+            launch_check.check_plan(pf, 4096, N, mode, False, OPTIN)
         if N <= 262144:
             pr = gb.norm_plan(4096, N, mode, True, SMS, OPTIN, residual=True)
             assert pr["streamed"] == s
@@ -241,3 +255,26 @@ def test_wait_hint_only_where_tuned(monkeypatch):
     p = gb.norm_plan(32768, 2048, 0, False, SMS, OPTIN)
     assert p["wait_hint_ns"] == (1500 if p["chunks_per_thread"] in (2, 4) and p["exact"] else 0)
     assert gb.norm_plan(4096, 131072, 0, False, SMS, OPTIN)["wait_hint_ns"] == 0  # long rows
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_stream_forward_plans_in_bounds(mode, monkeypatch):
+    """The streaming forward, forced (stream=1) at every width it takes and
+    with 8-piece slices (K=16, RMSNorm), and where it is the default."""
+    shapes = [(1, 32768), (7, 65536), (300, 131072), (5, 262144), (3, 524288), (4099, 524288)]
+    for M, N in shapes:
+        monkeypatch.setenv("GBNORM_PLAN", "stream=1")
+        p = gb.norm_plan(M, N, mode, False, SMS, OPTIN)
+        assert p["streamed"] == 1 and p["cols_per_cta"] == 32768
+        assert p["piece_cols"] == (16384 if mode == 0 else 8192)
+        launch_check.check_plan(p, M, N, mode, False, OPTIN)
+        if mode == 0 and N >= 65536:
+            monkeypatch.setenv("GBNORM_PLAN", "stream=1,K=16")
+            p = gb.norm_plan(M, N, mode, False, SMS, OPTIN)
+            assert p["streamed"] == 1 and p["cols_per_cta"] == 65536
+            launch_check.check_plan(p, M, N, mode, False, OPTIN)
+    monkeypatch.delenv("GBNORM_PLAN")
+    for M, N in ((2048, 524288), (1024, 1048576)):
+        p = gb.norm_plan(M, N, mode, False, SMS, OPTIN)
+        if p["streamed"]:
+            launch_check.check_plan(p, M, N, mode, False, OPTIN)

@@ -50,7 +50,10 @@ WIDE = [(3, 262152), (6, 524288), (5, 1048576), (2, 300008), (4, 262144 + 4096 *
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
 @pytest.mark.parametrize("M,N", WIDE)
-def test_wide_rows_every_row(mode, M, N):
+def test_wide_rows_every_row(mode, M, N, monkeypatch):
+    # stream=0: the two-pass path also at the widths the streaming kernels
+    # take by default (test_stream.py covers those)
+    monkeypatch.setenv("GBNORM_PLAN", "stream=0")
     case = wl.like(_base(mode, wide=True), M, N)
     x, g, b, dy = [None if t is None else t.cuda()
                    for t in wl.make_inputs(case, "cpu", seed=N % 1000 + M)]
@@ -65,7 +68,8 @@ def test_wide_rows_every_row(mode, M, N):
                                       (wl.RMS, 1024, 1048576)])
 def test_wide_rows_many(mode, M, N):
     """Thousands of wide rows (the very-long-row workload family extended
-    past the cluster limit): sampled rows against the oracle, dgamma /
+    past the cluster limit), with the default plans (streamed where they
+    stream, else two-pass): sampled rows against the oracle, dgamma /
     dbeta over every row, and every row's LayerNorm identity sum(dx) = 0."""
     case = wl.like(_base(mode, wide=True), M, N)
     x, g, b, dy = wl.make_inputs(case, "cuda")
@@ -84,7 +88,8 @@ def test_wide_rows_many(mode, M, N):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
-def test_two_pass_bitwise_reproducible(mode):
+def test_two_pass_bitwise_reproducible(mode, monkeypatch):
+    monkeypatch.setenv("GBNORM_PLAN", "stream=0")
     M, N = 300, 524288
     case = wl.like(_base(mode, wide=True), M, N)
     x, g, b, dy = wl.make_inputs(case, "cuda")

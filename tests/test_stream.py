@@ -32,8 +32,11 @@ CASES = [(1, 32768), (5, 32768), (300, 32768), (3, 65536), (81, 65536), (2, 1310
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
 @pytest.mark.parametrize("M,N", CASES)
-def test_stream_every_row(mode, M, N, monkeypatch):
-    monkeypatch.setenv("GBNORM_PLAN", "stream=1")
+@pytest.mark.parametrize("piece", ["", ",W=8192"], ids=["default-piece", "8192-piece"])
+def test_stream_every_row(mode, M, N, piece, monkeypatch):
+    if piece and mode == wl.LAYER:
+        pytest.skip("LayerNorm streams 8192-column pieces by default")
+    monkeypatch.setenv("GBNORM_PLAN", "stream=1" + piece)
     plan = gb.norm_plan(M, N, mode, True)
     assert plan["streamed"] == 1 and plan["cluster"] == N // 32768
     case = wl.like(_base(mode), M, N)
@@ -123,3 +126,44 @@ def test_resident_long_rows_where_streaming_is_default(mode, M, N, monkeypatch):
     outs = pu.run_gpu(x, g, b, dy, case.eps, mode)
     assert gb.norm_get_device_error() == 0
     pu.compare(mode, case.eps, x, g, b, dy, outs, label=f"resident {mode}:{M}x{N}")
+
+
+@pytest.mark.parametrize("mode,M,N,ov", [(wl.RMS, 5, 65536, "stream=1,K=16"),
+                                         (wl.RMS, 40, 262144, "stream=1,K=16"),
+                                         (wl.RMS, 7, 131072, "stream=1,K=8"),
+                                         (wl.RMS, 3, 1048576, ""), (wl.RMS, 9, 524288, ""),
+                                         (wl.LAYER, 6, 524288, "stream=1")])
+def test_stream_forward_wide_and_wide_slices(mode, M, N, ov, monkeypatch):
+    """The streaming forward where it is the default (RMSNorm rows of 524288
+    and 1048576 columns, 65536-column slices) and forced (65536- and
+    32768-column slices at narrower rows, LayerNorm): every row against the
+    oracle."""
+    if ov:
+        monkeypatch.setenv("GBNORM_PLAN", ov)
+    p = gb.norm_plan(M, N, mode, False)
+    assert p["streamed"] == 1
+    if "K=16" in ov or not ov:
+        assert p["cols_per_cta"] == 65536
+    case = wl.like(_base(mode), M, N)
+    x, g, b, dy = [None if t is None else t.cuda()
+                   for t in wl.make_inputs(case, "cpu", seed=N % 983 + M)]
+    outs = pu.run_gpu(x, g, b, dy, case.eps, mode)
+    assert gb.norm_get_device_error() == 0
+    pu.compare(mode, case.eps, x, g, b, dy, outs, label=f"stream fwd {mode}:{M}x{N}")
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
+def test_stream_forward_bitwise_reproducible(mode, monkeypatch):
+    monkeypatch.setenv("GBNORM_PLAN", "stream=1")
+    M, N = 100, 524288
+    case = wl.like(_base(mode), M, N)
+    x, g, b, dy = wl.make_inputs(case, "cuda")
+    assert gb.norm_plan(M, N, mode, False)["streamed"] == 1
+    first = gb.norm_fwd(x, g, b, case.eps, mode)
+    for _ in range(3):
+        again = gb.norm_fwd(x, g, b, case.eps, mode)
+        assert torch.equal(first[0].view(torch.int16), again[0].view(torch.int16))
+        assert torch.equal(first[1], again[1])
+        if mode == wl.LAYER:
+            assert torch.equal(first[2], again[2])
+    assert gb.norm_get_device_error() == 0
