@@ -24,6 +24,8 @@ def _small_cases():
     out.append((W["rms_262144x256_outliers"], 70001, 256))  # ring wraps, RT = 64
     for n in (16384, 32768, 65536, 131072):
         out.append((W[f"rms_4096x{n}"], 37, n))
+    for n in (24576, 32768, 65536, 131072):  # LayerNorm long rows, exact slices
+        out.append((W["layer_32768x4096"], 37, n))
     for mode in ("rms", "layer"):
         for n in (2048, 3072, 5120, 8192):
             out.append((W[f"{mode}_32768x{n}_resid"], 605, n))
