@@ -299,11 +299,12 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
                         Plan *out, bool resid = false, bool fp8 = false) {
   const int nc = N / 8;
   // 8 chunks per thread for the forward (RMSNorm without spilling;
-  // plain LayerNorm with a few spilled registers when one CTA owns the row
-  // and none in clusters, and still faster than 4: 60 -> 73 % of measured
-  // at 32768 columns, 58 -> 86 % at 65536, 48 -> 83 % at 131072); 4 for the
-  // backward and the fused LayerNorm forwards.
-  const int K = ov.K ? ov.K : ((!bwd && (mode == kRMS || (!resid && !fp8))) ? 8 : 4);
+  // LayerNorm with a few spilled registers when one CTA owns the row and
+  // none in clusters, and still faster than 4: 60 -> 73 % of measured at
+  // 32768 columns, 58 -> 86 % at 65536, 48 -> 83 % at 131072; with the fused
+  // residual add 94 -> 96, 91 -> 98, 76 -> 83 %); 4 for the backward and the
+  // LayerNorm E4M3 forward (no 8-chunk variant).
+  const int K = ov.K ? ov.K : ((!bwd && (mode == kRMS || !fp8)) ? 8 : 4);
   if (K != 2 && K != 4 && K != 8) return NORM_ERR_UNSUPPORTED;
   // Slices up to kMaxThreads threads x K chunks per CTA; clusters when the
   // row is wider, or when a stage of the CTA's slice (x, and dy and / or the
