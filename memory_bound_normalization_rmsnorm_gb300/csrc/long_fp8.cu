@@ -1,7 +1,7 @@
 // long_fp8.cu -- E4M3-output instantiations of the long-row forward kernel
 // (long_kernel.cuh): MX block or per-row scaling, with or without a
-// cluster; plain or fused-residual.  One chunk count
-// per mode (8 for RMSNorm, 4 for LayerNorm: the long-row planner's choice).
+// cluster; plain or fused-residual.  8 chunks per thread (the long-row
+// planner's choice for the forward).
 #include "long_kernel.cuh"
 
 namespace gbn {
@@ -36,8 +36,9 @@ const void *pick(bool cluster, bool e, bool r, int out) {
 }  // namespace
 
 const void *long_fp8_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, int out) {
-  if (mode == kRMS) return K == 8 ? pick<kRMS, 8>(cluster, exact, resid, out) : nullptr;
-  return K == 4 ? pick<kLayer, 4>(cluster, exact, resid, out) : nullptr;
+  if (K != 8) return nullptr;
+  return mode == kRMS ? pick<kRMS, 8>(cluster, exact, resid, out)
+                      : pick<kLayer, 8>(cluster, exact, resid, out);
 }
 
 }  // namespace gbn
