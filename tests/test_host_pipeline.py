@@ -30,7 +30,10 @@ def _device_ref(case, x, g, b, dy):
 
 @pytest.mark.parametrize("mode", [0, 1], ids=["rms", "layer"])
 @pytest.mark.parametrize("M,N,chunk", [(1031, 1024, 100), (257, 4096, 0), (3000, 2048, 1000),
-                                       (5, 512, 2), (64, 8192, 64)])
+                                       (5, 512, 2), (64, 8192, 64),
+                                       # streamed long rows (backward; and the
+                                       # RMSNorm forward beyond 262144 columns)
+                                       (40, 131072, 16), (10, 524288, 4)])
 @pytest.mark.parametrize("pin", [True, False], ids=["pinned", "pageable"])
 def test_host_pipeline_matches_device_path(M, N, chunk, mode, pin):
     base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_262144x1024_outliers"]
