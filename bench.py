@@ -962,8 +962,8 @@ def run_sweep(args):
     fp8 = {"": None, "row": 0, "mx": 1}[args.fp8]
     for name in names:
         w = wl.ALL[name]
-        if args.rows:
-            w = wl.like(w, args.rows, w.N)
+        if args.rows or args.cols:
+            w = wl.like(w, args.rows or w.M, args.cols or w.N)
         line = measure_workload(gb, w, peak, warmup=args.warmup, steps=args.steps,
                                 fused=args.fused_residual, fp8=fp8, fwd_only=args.fwd_only)
         line.update({"fused_residual": args.fused_residual, "fp8": args.fp8 or None,
@@ -1137,6 +1137,8 @@ def main():
                          "--workload, one JSON line per setting (not the benchmark line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cols", type=int, default=0,
+                    help="with --sweep: row length of the workload (same distributions)")
     ap.add_argument("--sweep", default="",
                     help="'all', 'wide' or comma-separated workload names: per-workload "
                          "fwd/bwd timings, one JSON line each (not the benchmark line)")
