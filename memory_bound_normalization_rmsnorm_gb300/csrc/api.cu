@@ -352,20 +352,28 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
 // cluster of C CTAs per row (one CTA when C = 1), one row group of
 // kStreamThreads threads per CTA, slices streamed as pieces of
 // stream_piece_cols(kp) columns with as many pieces in flight as fit (up to
-// kStreamMaxStages).  Pieces of 16384 columns (kp = 4) for RMSNorm, of 8192
-// (kp = 2) for LayerNorm, whose larger per-chunk state spills at 4 chunks,
-// and for the fused residual backward, whose third tensor would leave only
-// two 96 KB stages: from 8192- to 16384-column pieces the RMSNorm backward
-// at 131072 columns went from 85.9 to 93.0 % of measured (fewer waits and
-// refills per byte), LayerNorm's from 74.4 to 69.6 %, the fused residual
-// RMSNorm backward's from 98.7 to 92.8 %.  The override W= sets the piece
-// width (8192 or 16384).
+// kStreamMaxStages).  Pieces of 16384 columns (kp = 4), or of 8192 (kp =
+// 2) for the fused residual backward, whose third tensor would leave only
+// two 96 KB stages: from 8192- to 16384-column pieces (fewer waits and
+// refills per byte) the RMSNorm backward at 131072 columns went from 85.9 to
+// 93.0 % of measured, LayerNorm's from 74.0 to 83.0 % (its dx pass moves the
+// dgamma / dbeta accumulators through registers in two batches of two
+// chunks), the fused residual RMSNorm backward's from 98.8 down to 96.0 %.
+// The override W= sets the piece width (8192 or 16384).
 constexpr int kStreamMaxStages = 12;
 
-int stream_kp(int mode, const Override &ov, bool resid = false) {
+int stream_kp(const Override &ov, bool resid) {
   if (ov.W == stream_piece_cols(2)) return 2;
   if (ov.W == stream_piece_cols(4)) return 4;
-  return (mode == kRMS && !resid) ? 4 : 2;
+  return resid ? 2 : 4;
+}
+
+// The streaming forward's pieces: 16384 columns for RMSNorm, 8192 for
+// LayerNorm (the instantiated variants).
+int stream_fwd_kp(int mode, const Override &ov) {
+  if (ov.W == stream_piece_cols(2)) return 2;
+  if (ov.W == stream_piece_cols(4)) return 4;
+  return mode == kRMS ? 4 : 2;
 }
 
 bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <= 16; }
@@ -374,19 +382,18 @@ bool stream_applies(int N) { return N % kStreamSlice == 0 && N / kStreamSlice <=
 // backward measured faster on GB300 (1024 to 4096 rows) than the resident
 // long-row kernel or, beyond NORM_MAX_N_ONEPASS, the two-pass path, in % of
 // the measured copy bandwidth: 1, 2, 4 and 8 slices (RMSNorm 87.2 -> 91.9,
-// 86.9 -> 93.6, 74.3 -> 93.5, 66.1 -> 83.0; LayerNorm 74.8 -> 79.9,
-// 72.7 -> 77.1, 61.7 -> 74.4, 53.0 -> 60.7: the resident kernel's clusters
-// of 8 and 16 occupy only 120 and 112 SMs) and RMSNorm at 16 (two-pass
-// 58.4 -> 77.1).  LayerNorm at 16 slices keeps the two-pass path (57.8
-// against 53.9), and slice counts that are not powers of two keep the
-// resident kernel (clusters of 3 measured ~40 %).  The fused residual
+// 86.9 -> 93.6, 74.3 -> 93.5, 66.1 -> 83.0; LayerNorm 75.0 -> 82.5,
+// 72.7 -> 83.4, 61.7 -> 83.0, 53.0 -> 72.2: the resident kernel's clusters
+// of 8 and 16 occupy only 120 and 112 SMs) and 16 (two-pass RMSNorm
+// 58.4 -> 77.1, LayerNorm 57.8 -> 64.1).  Slice counts that are not powers
+// of two keep the resident kernel (clusters of 3 measured ~40 %).  The fused residual
 // backward (dh streamed once with the dx pass) takes it at the same widths
 // (1, 2, 4 and 8 slices; the fused entry points stop at 262144 columns):
 // RMSNorm 80.9 -> 95.9, 80.2 -> 98.5, 70.3 -> 98.6, 64.7 -> 86.3 %,
 // LayerNorm 63.6 -> 90.6, 57.8 -> 90.1, 48.2 -> 88.8, 45.0 -> 74.0 %.
 bool stream_default(int mode, int C) {
-  if (C == 1 || C == 2 || C == 4 || C == 8) return true;
-  return C == 16 && mode == kRMS;
+  (void)mode;
+  return C == 1 || C == 2 || C == 4 || C == 8 || C == 16;
 }
 
 // Whether the backward of rows of N columns takes the streaming kernel:
@@ -432,7 +439,7 @@ norm_status_t stream_common(int64_t M, int N, int slice, int kp, int ntensors, i
 norm_status_t stream_plan(int64_t M, int N, int mode, int smem_optin, const Override &ov,
                           Plan *out, bool resid = false) {
   if (!stream_applies(N)) return NORM_ERR_UNSUPPORTED;
-  const int kp = stream_kp(mode, ov, resid);
+  const int kp = stream_kp(ov, resid);
   if (!stream_kernel_ptr(mode, kp, N > kStreamSlice, resid)) return NORM_ERR_UNSUPPORTED;
   const norm_status_t st =
       stream_common(M, N, kStreamSlice, kp, resid ? 3 : 2, smem_optin, ov, out);
@@ -452,7 +459,7 @@ int stream_fwd_np(int N, int mode, const Override &ov) {
   if (ov.stream == 0) return 0;
   const bool forced = ov.stream == 1;
   if (!forced && (ov.any || N <= NORM_MAX_N_ONEPASS || mode != kRMS)) return 0;
-  const int kp = stream_kp(mode, ov);
+  const int kp = stream_fwd_kp(mode, ov);
   auto fits = [&](int np) {
     const int slice = np * stream_piece_cols(kp);
     const int C = N / slice;
@@ -469,7 +476,7 @@ int stream_fwd_np(int N, int mode, const Override &ov) {
 
 norm_status_t stream_fwd_plan(int64_t M, int N, int mode, int np, int smem_optin,
                               const Override &ov, Plan *out) {
-  const int kp = stream_kp(mode, ov);
+  const int kp = stream_fwd_kp(mode, ov);
   return stream_common(M, N, np * stream_piece_cols(kp), kp, 1, smem_optin, ov, out);
 }
 

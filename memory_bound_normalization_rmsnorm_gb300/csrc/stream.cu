@@ -326,59 +326,75 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_bwd_stream_kernel(cons
       uint16_t *dxrow = a.out + (cid + (j - 1) * ncl) * a.N + col0 + t * 8;
       __syncwarp();
       tmem_wait_st();  // the previous pass 2's accumulator stores are complete
+      // The accumulators of a piece go through registers in batches of KB
+      // chunks (32 registers at most): LayerNorm's dgamma and dbeta take 16
+      // TMEM columns per chunk, so its 16384-column pieces take two batches.
+      constexpr int KB = (kKP * CPC <= 32) ? kKP : 32 / CPC;
+      constexpr int NBAT = kKP / KB;
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
-        uint32_t acc[kKP * CPC];
+        uint32_t acc[KB * CPC];
         __syncwarp();
 #pragma unroll
-        for (int k = 0; k < kKP; ++k)
+        for (int k = 0; k < KB; ++k)
           tmem_ld_n<CPC>(tq + (p * kKP + k) * CPC,
                          *reinterpret_cast<uint32_t(*)[CPC]>(acc + k * CPC));
         mbar_wait(full + s, par, a.err, abort_flag);
-        __syncwarp();
-        if constexpr (kKP * CPC == 16) {
-          tmem_wait_ld_n<16>(*reinterpret_cast<uint32_t(*)[16]>(acc));
-        } else {
-          tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(acc));
-        }
         const unsigned char *st = smem + static_cast<size_t>(s) * L.stage_bytes + t * 16;
 #pragma unroll
-        for (int k = 0; k < kKP; ++k) {
-          float2 xf[4], df[4], gf[4], o[4];
-          chunk_to_f2(lds_v4(st + k * kStride), xf);
-          chunk_to_f2(lds_v4(st + L.tensor_bytes + k * kStride), df);
-          chunk_to_f2(gv[p][k], gf);
-          uint32_t *ak = acc + k * CPC;
+        for (int b = 0; b < NBAT; ++b) {
+          __syncwarp();
+          if (b > 0) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 gg = mul2(df[e], gf[e]);
-            const float2 xc = MODE == kLayer ? add2(xf[e], nmu) : xf[e];
-            o[e] = fma2(xc, nk1, MODE == kLayer ? fma2(gg, rs2, nra) : mul2(gg, rs2));
-            const float2 xh = mul2(xc, rs2);
-            float2 ag = make_float2(__uint_as_float(ak[2 * e]), __uint_as_float(ak[2 * e + 1]));
-            ag = fma2(df[e], xh, ag);
-            ak[2 * e] = __float_as_uint(ag.x);
-            ak[2 * e + 1] = __float_as_uint(ag.y);
-            if (MODE == kLayer) {
-              float2 ab = make_float2(__uint_as_float(ak[8 + 2 * e]),
-                                      __uint_as_float(ak[8 + 2 * e + 1]));
-              ab = add2(ab, df[e]);
-              ak[8 + 2 * e] = __float_as_uint(ab.x);
-              ak[8 + 2 * e + 1] = __float_as_uint(ab.y);
+            for (int k = 0; k < KB; ++k)
+              tmem_ld_n<CPC>(tq + (p * kKP + b * KB + k) * CPC,
+                             *reinterpret_cast<uint32_t(*)[CPC]>(acc + k * CPC));
+          }
+          if constexpr (KB * CPC == 16) {
+            tmem_wait_ld_n<16>(*reinterpret_cast<uint32_t(*)[16]>(acc));
+          } else {
+            tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(acc));
+          }
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb) {
+            const int k = b * KB + kb;
+            float2 xf[4], df[4], gf[4], o[4];
+            chunk_to_f2(lds_v4(st + k * kStride), xf);
+            chunk_to_f2(lds_v4(st + L.tensor_bytes + k * kStride), df);
+            chunk_to_f2(gv[p][k], gf);
+            uint32_t *ak = acc + kb * CPC;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 gg = mul2(df[e], gf[e]);
+              const float2 xc = MODE == kLayer ? add2(xf[e], nmu) : xf[e];
+              o[e] = fma2(xc, nk1, MODE == kLayer ? fma2(gg, rs2, nra) : mul2(gg, rs2));
+              const float2 xh = mul2(xc, rs2);
+              float2 ag = make_float2(__uint_as_float(ak[2 * e]), __uint_as_float(ak[2 * e + 1]));
+              ag = fma2(df[e], xh, ag);
+              ak[2 * e] = __float_as_uint(ag.x);
+              ak[2 * e + 1] = __float_as_uint(ag.y);
+              if (MODE == kLayer) {
+                float2 ab = make_float2(__uint_as_float(ak[8 + 2 * e]),
+                                        __uint_as_float(ak[8 + 2 * e + 1]));
+                ab = add2(ab, df[e]);
+                ak[8 + 2 * e] = __float_as_uint(ab.x);
+                ak[8 + 2 * e + 1] = __float_as_uint(ab.y);
+              }
             }
-          }
-          if (RESID) {
-            float2 hf[4];
-            chunk_to_f2(lds_v4(st + 2 * L.tensor_bytes + k * kStride), hf);
+            if (RESID) {
+              float2 hf[4];
+              chunk_to_f2(lds_v4(st + 2 * L.tensor_bytes + k * kStride), hf);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[e] = add2(o[e], hf[e]);
+              for (int e = 0; e < 4; ++e) o[e] = add2(o[e], hf[e]);
+            }
+            st_global_cs_v4(dxrow + p * kW + k * kStreamThreads * 8, f2_to_chunk(o));
           }
-          st_global_cs_v4(dxrow + p * kW + k * kStreamThreads * 8, f2_to_chunk(o));
+          __syncwarp();
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb)
+            tmem_st_n<CPC>(tq + (p * kKP + b * KB + kb) * CPC,
+                           *reinterpret_cast<const uint32_t(*)[CPC]>(acc + kb * CPC));
         }
-#pragma unroll
-        for (int k = 0; k < kKP; ++k)
-          tmem_st_n<CPC>(tq + (p * kKP + k) * CPC,
-                         *reinterpret_cast<const uint32_t(*)[CPC]>(acc + k * CPC));
         release(q, s);
         advance();
       }
@@ -676,8 +692,9 @@ const void *stream_ptr(bool cluster) {
 // accumulator registers per chunk of LayerNorm's (dgamma only).
 const void *stream_kernel_ptr(int mode, int kp, bool cluster, bool resid) {
   if (mode == kLayer) {
-    if (kp != 2) return nullptr;
-    return resid ? stream_ptr<kLayer, 2, true>(cluster) : stream_ptr<kLayer, 2, false>(cluster);
+    if (kp == 4) return resid ? stream_ptr<kLayer, 4, true>(cluster) : stream_ptr<kLayer, 4, false>(cluster);
+    if (kp == 2) return resid ? stream_ptr<kLayer, 2, true>(cluster) : stream_ptr<kLayer, 2, false>(cluster);
+    return nullptr;
   }
   if (kp == 4) return resid ? stream_ptr<kRMS, 4, true>(cluster) : stream_ptr<kRMS, 4, false>(cluster);
   if (kp == 2) return resid ? stream_ptr<kRMS, 2, true>(cluster) : stream_ptr<kRMS, 2, false>(cluster);

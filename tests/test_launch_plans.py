@@ -196,8 +196,8 @@ def test_stream_plans_in_bounds(mode, monkeypatch):
         p = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
         launch_check.check_plan(p, M, N, mode, True, OPTIN)
         launch_check.check_reduce(p["partials"], N, 2 if mode == 1 else 1)
-        assert p["piece_cols"] == (16384 if mode == 0 else 8192)
-        monkeypatch.setenv("GBNORM_PLAN", "stream=1,W=8192")  # RMSNorm's 8192-column pieces
+        assert p["piece_cols"] == 16384
+        monkeypatch.setenv("GBNORM_PLAN", "stream=1,W=8192")  # the fused variant's pieces
         p8 = gb.norm_plan(M, N, mode, True, SMS, OPTIN)
         assert p8["piece_cols"] == 8192
         launch_check.check_plan(p8, M, N, mode, True, OPTIN)
@@ -217,7 +217,7 @@ def test_stream_default_widths():
     at) and where it keeps the resident long-row kernel or the two-pass
     path."""
     want = {(0, 32768): 1, (0, 65536): 1, (0, 131072): 1, (0, 262144): 1, (0, 524288): 1,
-            (1, 32768): 1, (1, 65536): 1, (1, 131072): 1, (1, 262144): 1, (1, 524288): 0,
+            (1, 32768): 1, (1, 65536): 1, (1, 131072): 1, (1, 262144): 1, (1, 524288): 1,
             (0, 98304): 0, (0, 16384): 0, (1, 1048576): 0}
     for (mode, N), s in want.items():
         p = gb.norm_plan(4096, N, mode, True, SMS, OPTIN)

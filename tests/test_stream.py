@@ -32,10 +32,12 @@ CASES = [(1, 32768), (5, 32768), (300, 32768), (3, 65536), (81, 65536), (2, 1310
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER], ids=["rms", "layer"])
 @pytest.mark.parametrize("M,N", CASES)
-@pytest.mark.parametrize("piece", ["", ",W=8192"], ids=["default-piece", "8192-piece"])
+@pytest.mark.parametrize("piece", ["", "other"], ids=["default-piece", "other-piece"])
 def test_stream_every_row(mode, M, N, piece, monkeypatch):
-    if piece and mode == wl.LAYER:
-        pytest.skip("LayerNorm streams 8192-column pieces by default")
+    # the piece width the mode does not take by default: 8192 columns for
+    # RMSNorm, 16384 for LayerNorm (two register batches of accumulators)
+    if piece:
+        piece = ",W=8192" if mode == wl.RMS else ",W=16384"
     monkeypatch.setenv("GBNORM_PLAN", "stream=1" + piece)
     plan = gb.norm_plan(M, N, mode, True)
     assert plan["streamed"] == 1 and plan["cluster"] == N // 32768
