@@ -704,7 +704,7 @@ def run_ours(args):
         for name in wl.ALL:
             e = measure_workload(gb, wl.ALL[name], peak, sampler=sampler, flush=flush)
             if name in wl.WIDE:
-                e["beyond_configs"] = "rows wider than one cluster holds (two-pass path)"
+                e["beyond_configs"] = "rows wider than one cluster holds in shared memory (streamed or two-pass)"
             sweep.append(e)
     clocks_all = sampler.stop()
     clocks = sampler.window(busy0, busy1) or clocks_all

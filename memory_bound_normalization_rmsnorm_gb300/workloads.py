@@ -70,9 +70,10 @@ HEADLINE = "layer_32768x4096"
 
 
 def _wide():
-    """Rows wider than one thread-block cluster holds (the two-pass path):
-    the very-long-row family carried past 262144 columns, RMSNorm with its
-    distributions and LayerNorm with the headline's."""
+    """Rows wider than one thread-block cluster holds in shared memory
+    (streamed row slices or the two-pass path): the very-long-row family
+    carried past 262144 columns, RMSNorm with its distributions and
+    LayerNorm with the headline's."""
     w = [Workload("rms_4096x524288", RMS, 4096, 524288, 1e-6, "normal2", "uniform_0.5_1.5"),
          Workload("rms_1024x1048576", RMS, 1024, 1048576, 1e-6, "normal2", "uniform_0.5_1.5"),
          Workload("layer_2048x524288", LAYER, 2048, 524288, 1e-5, "normal", "one_plus_0.1n")]
