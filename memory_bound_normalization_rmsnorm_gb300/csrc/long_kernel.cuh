@@ -344,16 +344,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       float n, m, q;
       if (EXACT) {
         // equal counts (NS columns per CTA), merged in rank order
-        m = row[0];
-        q = row[1];
-        const float ncta = static_cast<float>(a.NS);
-#pragma unroll
-        for (int k = 1; k < 16; ++k) {
-          if (k < xch.C) {
-            const float wb = 1.0f / static_cast<float>(k + 1);
-            ms_merge(m, q, row[k * 4], row[k * 4 + 1], wb, ncta * static_cast<float>(k) * wb);
-          }
-        }
+        rank_fold_meanvar(row, xch.C, static_cast<float>(a.NS), m, q);
       } else {
         fold_nmeanvar(row, xch.C, n, m, q);
       }

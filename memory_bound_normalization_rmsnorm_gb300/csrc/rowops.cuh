@@ -289,21 +289,29 @@ __device__ __forceinline__ void cluster_sum(float (&v)[NV], int r, int t, Cluste
   fold_sum<NV>(row, x.C, v);
 }
 
+// (mean, M2) of C <= 16 partials of n_cta elements each (row[4k], row[4k+1]),
+// the running partial over k CTAs merged with CTA k in rank order.  Unrolled,
+// so every 1 / (k + 1) is a compile-time constant, not a division per row.
+__device__ __forceinline__ void rank_fold_meanvar(const float *row, int C, float n_cta, float &m,
+                                                  float &q) {
+  m = row[0];
+  q = row[1];
+#pragma unroll
+  for (int k = 1; k < 16; ++k) {
+    if (k < C) {
+      const float wb = 1.0f / static_cast<float>(k + 1);
+      ms_merge(m, q, row[k * 4 + 0], row[k * 4 + 1], wb, n_cta * static_cast<float>(k) * wb);
+    }
+  }
+}
+
 // (mean, M2) over the C CTAs, each partial covering n_cta elements, merged
 // in rank order.
 __device__ __forceinline__ void cluster_meanvar(float &m, float &q, float n_cta, int r, int t,
                                                 ClusterXch &x, unsigned *err,
                                                 volatile int *abort) {
   const float *row = cluster_exchange(m, q, 0.f, r, t, x, err, abort);
-  m = row[0];
-  q = row[1];
-#pragma unroll
-  for (int k = 1; k < 16; ++k) {
-    if (k < x.C) {
-      const float wb = 1.0f / static_cast<float>(k + 1);
-      ms_merge(m, q, row[k * 4 + 0], row[k * 4 + 1], wb, n_cta * static_cast<float>(k) * wb);
-    }
-  }
+  rank_fold_meanvar(row, x.C, n_cta, m, q);
 }
 
 // ------------------------------------ (count, mean, M2) of any counts

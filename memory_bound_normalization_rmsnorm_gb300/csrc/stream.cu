@@ -628,12 +628,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) norm_fwd_stream_kernel(cons
       const float *rowx = cluster_wait_row(0, xch, a.err, abort_flag);
       float mu = 0.f, rs;
       if (MODE == kLayer) {
-        float mm = rowx[0], qq = rowx[1];
-        const float ncta = static_cast<float>(a.NS);
-        for (int k = 1; k < xch.C; ++k) {
-          const float wb = 1.0f / static_cast<float>(k + 1);
-          ms_merge(mm, qq, rowx[k * 4], rowx[k * 4 + 1], wb, ncta * static_cast<float>(k) * wb);
-        }
+        float mm, qq;
+        rank_fold_meanvar(rowx, xch.C, static_cast<float>(a.NS), mm, qq);
         mu = mm;
         rs = rsqrtf(qq * invN + a.eps);
       } else {
