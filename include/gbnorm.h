@@ -245,7 +245,9 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma,
  *
  * norm_host_workspace_bytes: device workspace norm_fwd_bwd_host needs for
  *   this shape and chunk size (chunk_rows = 0: the library's default, about
- *   16 MB of x per chunk).
+ *   16 MB of x per chunk): three chunks of x, dy, y and dx, plus rstd (and
+ *   mean) of all M rows, which go back to the host in one copy each after
+ *   the last chunk.
  * norm_fwd_bwd_host:
  *   x, dy          HOST bf16 [M, N] inputs (page-locked memory, e.g. from
  *                  cudaHostAlloc, for the copies to overlap; pageable memory
@@ -254,7 +256,8 @@ norm_status_t norm_fwd_fp8(const void *x, const void *r, const void *gamma,
  *   y, dx          HOST bf16 [M, N] outputs; rstd, mean HOST fp32 [M]
  *                  (mean LAYER only); dgamma, dbeta HOST fp32 [N] (dbeta
  *                  LAYER only, may be NULL);
- *   chunk_rows     rows per chunk (0: default);
+ *   chunk_rows     rows per chunk (0: default; rounded up to a multiple of
+ *                  4 when smaller than M);
  *   workspace      DEVICE memory of norm_host_workspace_bytes bytes, 256-byte
  *                  aligned, owned by the caller (NORM_ERR_WORKSPACE if NULL or
  *                  short, NORM_ERR_ALIGN if misaligned).

@@ -10,6 +10,11 @@
 // [2][chunks][N] array (its own fixed-order partial sum), and a last
 // reduction sums those rows in chunk order, so the result is bitwise
 // reproducible for a given chunk size.
+//
+// rstd and mean of every row stay on the device until the last chunk is
+// done and go back in one copy each: a copy has a fixed cost of several
+// microseconds on the host link, which per chunk added up to more than the
+// statistics' own bytes.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -73,23 +78,28 @@ struct Layout {
   int64_t R = 0, nch = 0;
   size_t gamma = 0, beta = 0, slot0 = 0, slot_bytes = 0, x = 0, dy = 0, y = 0, dx = 0,
          rstd = 0, mean = 0, bws = 0, bws_bytes = 0, rows = 0, dg = 0, db = 0, total = 0;
+  // rstd / mean: [M] fp32 arrays of the whole call (not per slot)
 };
 
 norm_status_t layout(int64_t M, int64_t N, norm_mode_t mode, int64_t chunk_rows, Layout *L) {
   Layout l;
   l.R = chunk_rows > 0 ? std::min(chunk_rows, M) : default_chunk_rows(M, N);
+  // a chunk's first row indexes the [M] statistics arrays, whose pointers the
+  // kernels take 16-byte aligned: chunks start at multiples of 4 rows
+  if (l.R < M) l.R = std::min(M, (l.R + 3) / 4 * 4);
   l.nch = (M + l.R - 1) / l.R;
   if (l.nch > (int64_t(1) << 20)) return NORM_ERR_SHAPE;
   size_t bws = 0;
   norm_status_t st = norm_bwd_workspace_bytes(l.R, N, mode, &bws);
   if (st != NORM_OK) return st;
-  const size_t t = static_cast<size_t>(l.R) * N * 2, s = static_cast<size_t>(l.R) * 4;
+  const size_t t = static_cast<size_t>(l.R) * N * 2, s = static_cast<size_t>(M) * 4;
   size_t off = 0;
   l.gamma = off; off = up(off + N * 2);
   l.beta = off; off = up(off + N * 2);
-  l.x = 0; l.dy = up(t); l.y = l.dy + up(t); l.dx = l.y + up(t); l.rstd = l.dx + up(t);
-  l.mean = l.rstd + up(s);
-  l.slot_bytes = l.mean + up(s);
+  l.rstd = off; off = up(off + s);
+  l.mean = off; off = up(off + (mode == NORM_LAYER ? s : 0));
+  l.x = 0; l.dy = up(t); l.y = l.dy + up(t); l.dx = l.y + up(t);
+  l.slot_bytes = l.dx + up(t);
   l.slot0 = off; off += kDepth * l.slot_bytes;
   l.bws = off; l.bws_bytes = std::max<size_t>(bws, 16); off = up(off + l.bws_bytes);
   l.rows = off; off = up(off + size_t(2) * l.nch * N * 4);
@@ -182,8 +192,8 @@ norm_status_t norm_fwd_bwd_host(const void *x, const void *dy, const void *gamma
     // compute: inputs in, and the slot's previous outputs copied out
     chk(cudaStreamWaitEvent(cs, P.in_done[s], 0));
     if (c >= kDepth) chk(cudaStreamWaitEvent(cs, P.out_done[s], 0));
-    float *rs = reinterpret_cast<float *>(slot + L.rstd);
-    float *mu = ln ? reinterpret_cast<float *>(slot + L.mean) : nullptr;
+    float *rs = reinterpret_cast<float *>(ws + L.rstd) + r0;
+    float *mu = ln ? reinterpret_cast<float *>(ws + L.mean) + r0 : nullptr;
     st = norm_fwd(slot + L.x, ws + L.gamma, dbeta_dev, nr, N, eps, mode, slot + L.y, rs, mu,
                   stream);
     if (st != NORM_OK) return st;
@@ -196,8 +206,6 @@ norm_status_t norm_fwd_bwd_host(const void *x, const void *dy, const void *gamma
     chk(cudaStreamWaitEvent(P.d2h, P.comp_done[s], 0));
     chk(cudaMemcpyAsync(hy + off, slot + L.y, bytes, d2h, P.d2h));
     chk(cudaMemcpyAsync(hdx + off, slot + L.dx, bytes, d2h, P.d2h));
-    chk(cudaMemcpyAsync(rstd + r0, rs, nr * 4, d2h, P.d2h));
-    if (ln) chk(cudaMemcpyAsync(mean + r0, mu, nr * 4, d2h, P.d2h));
     chk(cudaEventRecord(P.out_done[s], P.d2h));
   }
   if (!ok) {
@@ -213,6 +221,8 @@ norm_status_t norm_fwd_bwd_host(const void *x, const void *dy, const void *gamma
   chk(cudaStreamWaitEvent(P.d2h, P.fin, 0));
   chk(cudaMemcpyAsync(dgamma, dg, N * 4, d2h, P.d2h));
   if (ln && dbeta) chk(cudaMemcpyAsync(dbeta, db, N * 4, d2h, P.d2h));
+  chk(cudaMemcpyAsync(rstd, ws + L.rstd, M * 4, d2h, P.d2h));
+  if (ln) chk(cudaMemcpyAsync(mean, ws + L.mean, M * 4, d2h, P.d2h));
   // `stream` ends after the last copy
   chk(cudaEventRecord(P.end, P.d2h));
   chk(cudaStreamWaitEvent(cs, P.end, 0));
