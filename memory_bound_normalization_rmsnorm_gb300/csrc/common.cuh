@@ -155,6 +155,12 @@ constexpr int kOutBf16 = 0;
 constexpr int kOutFp8Row = 1;
 constexpr int kOutFp8Mx = 2;
 constexpr int kMxBlock = 32;
+// Phases of the long-row forward's per-row E4M3 output pass: amax then codes
+// (one CTA per row), or in a cluster this CTA's slice amax alone, and later
+// the codes with the row amax the exchange returned.
+constexpr int kFp8Whole = 0;
+constexpr int kFp8Amax = 1;
+constexpr int kFp8Codes = 2;
 
 // gsm: gamma (and beta) staged in shared memory and read per row, which frees
 // the registers that hold them otherwise (exact splits, no cluster, K in
@@ -175,8 +181,8 @@ const void *reduce_kernel_ptr();
 const void *long_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd,
                             bool resid = false);
 const void *long_resid_kernel_ptr(int mode, int K, bool cluster, bool exact, bool bwd);
-// Long-row forward with E4M3 output (out = kOutFp8Row without a cluster, or
-// kOutFp8Mx); nullptr if not instantiated.
+// Long-row forward with E4M3 output (kOutFp8Row or kOutFp8Mx, with or
+// without a cluster); nullptr if not instantiated.
 const void *long_fp8_kernel_ptr(int mode, int K, bool cluster, bool exact, bool resid, int out);
 int reduce_threads();
 const void *selftest_kernel_ptr();

@@ -46,9 +46,9 @@ struct Pending {
 // forms h = bf16(x + r) (sum in binary32, round to nearest even), writes it
 // over x in the stage, and the output pass writes h out beside y.
 // OUT: bf16 y (kOutBf16), or E4M3 codes with a per-row scale (kOutFp8Row;
-// in a cluster the row amax takes a second exchange round, and the tiles are
-// not software-pipelined) or with per-32-column E8M0 exponents (kOutFp8Mx;
-// slices start on a block).
+// in a cluster the CTAs' slice maxima of a row travel in the next row's
+// exchange round, so a row's codes are written one round later) or with
+// per-32-column E8M0 exponents (kOutFp8Mx; slices start on a block).
 template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT = kOutBf16>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -206,8 +206,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
   };
 
   // Output pass of row slot r given the row totals; writes y and the
-  // statistics.
-  auto output_pass = [&](const unsigned char *st, int64_t row0, int r, float ta, float tb) {
+  // statistics.  Per-row E4M3 runs in one of three phases: kFp8Whole (no
+  // cluster: the row amax, then the codes), kFp8Amax (cluster: returns this
+  // CTA's slice amax, stores nothing) or kFp8Codes (cluster: the codes with
+  // the row amax `am_row`, then the statistics).
+  auto output_pass = [&](const unsigned char *st, int64_t row0, int r, float ta, float tb,
+                         int phase = kFp8Whole, float am_row = 0.f) -> float {
     float rs, mu = 0.f;
     if (MODE == kLayer) {
       mu = ta;
@@ -243,26 +247,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
         }
       }
     } else if (OUT == kOutFp8Row) {
-      // amax of the row (one CTA per row here), then the codes
+      // amax of the row (of this CTA's slice in a cluster), then the codes
       uint8_t *qrow = a.q + (row0 + r) * a.N + col0 + t * 8;
-      float am = 0.f;
+      float am = am_row;
+      if (phase != kFp8Codes) {
+        am = 0.f;
 #pragma unroll
-      for (int k = 0; k < K; ++k) {
-        if (EXACT || t + k * a.tpr < nsc_me) {
-          float2 o[4];
-          ychunk(k, o, false);
+        for (int k = 0; k < K; ++k) {
+          if (EXACT || t + k * a.tpr < nsc_me) {
+            float2 o[4];
+            ychunk(k, o, false);
 #pragma unroll
-          for (int p = 0; p < 4; ++p) am = fmaxf(am, fmaxf(fabsf(o[p].x), fabsf(o[p].y)));
+            for (int p = 0; p < 4; ++p) am = fmaxf(am, fmaxf(fabsf(o[p].x), fabsf(o[p].y)));
+          }
         }
-      }
-      am = group_max<true>(am, a.tpr, g, a.G, t, red, rpar);
-      if (CLUSTER) {
-        // second exchange round: the CTAs' slice maxima, folded (max is
-        // exact, so every CTA gets the same amax)
-        cluster_push(am, 0.f, 0.f, r, t, xch);
-        const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
-        am = row[0];
-        for (int q = 1; q < xch.C; ++q) am = fmaxf(am, row[q * 4]);
+        am = group_max<true>(am, a.tpr, g, a.G, t, red, rpar);
+        if (phase == kFp8Amax) return am;
       }
       const float2 inv = splat2(am > 0.f ? __fdividef(448.f, am) : 1.f);
 #pragma unroll
@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       a.rstd[row0 + r] = rs;
       if (MODE == kLayer) a.mean[row0 + r] = mu;
     }
+    return 0.f;
   };
 
   // Stage s is consumed: the last warp refills it with the tile S ahead.
@@ -334,12 +335,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
   // Finish a pending cluster tile: wait for its exchange, fold in rank
   // order, write outputs, release the stage.  (Cluster tiles hold one row
   // per group: rows_per_group is 1.)
-  auto finish = [&](const Pending &p) {
-    const int64_t row0 = p.tile * a.RT;
-    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
-    const int r = g;
-    const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
-    float ta, tb;
+  // Row totals of an exchange round's C slots, folded in rank order.
+  auto fold_totals = [&](const float *row, float &ta, float &tb) {
     if (MODE == kLayer) {
       float n, m, q;
       if (EXACT) {
@@ -356,7 +353,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       ta = v[0];
       tb = 0.f;
     }
+  };
+  auto finish = [&](const Pending &p) {
+    const int64_t row0 = p.tile * a.RT;
+    const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
+    const int r = g;
+    float ta, tb;
+    fold_totals(cluster_wait_row(r, xch, a.err, abort_flag), ta, tb);
     if (r < nrows) output_pass(smem + static_cast<size_t>(p.s) * L.stage_bytes, row0, r, ta, tb);
+    release(p.tile, p.s);
+  };
+  // Per-row E4M3 in a cluster: one exchange round per tile carries the
+  // tile's statistics partial and, in its fourth float, this CTA's slice
+  // amax of the previous tile, whose codes are written once the round is
+  // in.  (Two rounds per tile -- statistics, then amax -- cannot overlap the
+  // next tile's statistics, since rounds are consumed in push order.)
+  float pend_ta = 0.f, pend_tb = 0.f, pend_am = 0.f;
+  auto fp8_codes = [&](const Pending &p, const float *row) {
+    const int64_t row0 = p.tile * a.RT;
+    const int r = g;
+    float am = row[3];
+    for (int q = 1; q < xch.C; ++q) am = fmaxf(am, row[q * 4 + 3]);
+    if (r < static_cast<int>(min64(a.RT, a.M - row0)))
+      output_pass(smem + static_cast<size_t>(p.s) * L.stage_bytes, row0, r, pend_ta, pend_tb,
+                  kFp8Codes, am);
     release(p.tile, p.s);
   };
 
@@ -375,13 +395,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       cur.tile = tile;
       cur.s = s;
       stats_pass(st, r, r < nrows, cur.a, cur.b, cur.c);
-      cluster_push(cur.a, cur.b, cur.c, r, t, xch);
       if (OUT == kOutFp8Row) {
-        // the output pass pushes and waits for the amax round itself, so a
-        // tile is finished before the next one's statistics are pushed
-        // (exchange rounds are consumed in the order they were pushed)
-        finish(cur);
+        cluster_push(cur.a, cur.b, cur.c, r, t, xch, have_pend ? pend_am : 0.f);
+        const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
+        float ta, tb;
+        fold_totals(row, ta, tb);
+        if (have_pend) fp8_codes(pend, row);
+        pend = cur;
+        pend_ta = ta;
+        pend_tb = tb;
+        pend_am = r < nrows ? output_pass(st, row0, r, ta, tb, kFp8Amax) : 0.f;
+        have_pend = true;
       } else {
+        cluster_push(cur.a, cur.b, cur.c, r, t, xch);
         if (have_pend) finish(pend);
         pend = cur;
         have_pend = true;
@@ -402,7 +428,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
     }
   }
   if (CLUSTER) {
-    if (have_pend) finish(pend);
+    if (have_pend) {
+      if (OUT == kOutFp8Row) {
+        // a last round with the last tile's slice maxima only
+        cluster_push(0.f, 0.f, 0.f, g, t, xch, pend_am);
+        fp8_codes(pend, cluster_wait_row(g, xch, a.err, abort_flag));
+      } else {
+        finish(pend);
+      }
+    }
     cluster_sync();
   }
 }

@@ -237,13 +237,13 @@ __device__ __forceinline__ ClusterXch make_xch(unsigned char *smem, const SmemLa
 // wait for round k-1 has seen every CTA's round k-1 push, and each CTA folds
 // round k-3 (same buffer as k+1) before it pushes round k-1.
 __device__ __forceinline__ void cluster_push(float a, float b, float c, int r, int t,
-                                             ClusterXch &x) {
+                                             ClusterXch &x, float d = 0.f) {
   const int bsel = x.push_buf;
   float *base = x.slots + static_cast<size_t>(bsel) * x.RT * x.C * 4;
   uint64_t *bar = x.bars + bsel;
   if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(x.RT * x.C * 16));
   if (t == 0) {
-    const float4 val = make_float4(a, b, c, 0.f);
+    const float4 val = make_float4(a, b, c, d);
     const float *mine = base + (static_cast<size_t>(r) * x.C + x.crank) * 4;
     for (int q = 0; q < x.C; ++q)
       st_async_f32x4(mapa_shared(mine, q), val, mapa_shared(bar, q));

@@ -124,11 +124,15 @@ def test_fp8_zero_rows_and_tiny_blocks():
 
 @pytest.mark.parametrize("residual", [False, True], ids=["plain", "resid"])
 @pytest.mark.parametrize("mode,M,N", [(0, 37, 32768), (0, 21, 40000), (1, 29, 18432),
-                                      (1, 17, 24576), (0, 9, 65536), (0, 5, 131072)])
+                                      (1, 17, 24576), (0, 9, 65536), (0, 5, 131072),
+                                      (1, 7, 65536), (1, 3, 131072), (1, 11, 40000),
+                                      (0, 301, 65536)])
 def test_fp8_long_rows(mode, M, N, residual):
     """Rows wider than one CTA's registers (long-row kernels, clusters):
-    both scalings; with a cluster, per-row scaling exchanges the CTAs'
-    slice maxima in a second round."""
+    both scalings; with a cluster, per-row scaling sends the CTAs' slice
+    maxima of a row in the next row's exchange round (and one last round
+    after the last row), so every cluster case here has rows that finish in
+    a later round, and the 301-row case gives each cluster several."""
     base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
     case = wl.like(base, M, N)
     x, r, g, b, _, _ = [None if t is None else t.cuda()
