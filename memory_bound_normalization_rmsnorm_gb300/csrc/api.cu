@@ -304,7 +304,8 @@ norm_status_t long_plan(int mode, bool bwd, int64_t M, int N, int smem_optin, co
   // 32768 columns, 58 -> 86 % at 65536, 48 -> 83 % at 131072; with the fused
   // residual add 94 -> 96, 91 -> 98, 76 -> 83 %; with E4M3 output, of its
   // minimal bytes, MX 42 -> 44, 41 -> 60, 33 -> 58 %, per-row 34 -> 40,
-  // 32 -> 33, 26 -> 32 %); 4 for the backward.
+  // 32 -> 33, 26 -> 32 %, the last two now 47 and 45 % with one exchange
+  // round per row); 4 for the backward.
   const int K = ov.K ? ov.K : (!bwd ? 8 : 4);
   if (K != 2 && K != 4 && K != 8) return NORM_ERR_UNSUPPORTED;
   // Slices up to kMaxThreads threads x K chunks per CTA; clusters when the
