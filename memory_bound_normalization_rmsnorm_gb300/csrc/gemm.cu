@@ -20,14 +20,18 @@
 // memory.  x reaches the SM once per output tile column (mostly from L2),
 // and the normalised rows are never written.
 //
-// A persistent grid (one CTA per SM, 12 warps) walks the 128 x 256 output
-// tiles in units of 1, 2 or 4 consecutive column tiles of one row block,
-// dealt round-robin in the grouped order of tile_coords:
+// A persistent grid (one CTA per SM, 12 warps) walks the output tiles in
+// units of 1, 2 or 4 consecutive column tiles of one row block, dealt
+// round-robin in the grouped order of tile_coords.  By default 2-CTA
+// clusters (PAIR) share 256 x 256 tiles with cta_group::2 MMAs, each CTA
+// holding 128 x rows and 128 W' rows per stage (6 stages); the single-CTA
+// form takes 128 x 256 tiles (4 stages).  Per CTA:
 //   warp 0      (lane 0) issues the tiled TMA loads of the x and W' tiles
-//               into a 4-stage ring (128-byte swizzle);
-//   warp 1      (lane 0) issues the tcgen05.mma instructions, 4 per 64-wide
-//               K block, into one of two 256-column fp32 accumulators in
-//               tensor memory, and commits each stage back to the producer;
+//               into the stage ring (128-byte swizzle);
+//   warp 1      (lane 0; rank 0 of a pair) issues the tcgen05.mma
+//               instructions, 4 per 64-wide K block, into one of two
+//               256-column fp32 accumulators in tensor memory, and commits
+//               each stage back to the producers;
 //   warp 2      allocates (and at the end frees) the 512 TMEM columns;
 //   warps 8-11  the statistics of the current unit's 128 rows, from the x
 //               tiles of its first tile, handed to the epilogue through a
@@ -35,8 +39,6 @@
 //   warps 4-7   the epilogue of the previous tile, on TMEM lane t = row t,
 //               while the tensor cores fill the other accumulator; output
 //               through two swizzled staging buffers and TMA tensor stores.
-// A cluster form (PAIR) runs 2-CTA clusters over 256-row blocks with
-// cta_group::2 MMAs.
 // Row statistics use shifted sums: the mean of the row's first 64 values,
 // rounded to bf16, is the shift c, and sum(x - c), sum((x - c)^2) give the
 // mean and the population variance without the cancellation of raw power
@@ -280,9 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           mma_commit(bar);
       };
-      int g = 0;
       bool ok = true;
       int mb, nb;
+      // One thread issues every MMA and the tensor pipe holds only a few
+      // queued instructions, so the per-K-block bookkeeping of this loop is
+      // on the critical path: descriptors and barrier addresses are formed
+      // by one add each from values taken once.
+      const uint64_t adesc0 = desc_sw128(smem_addr(a_tiles));
+      const uint64_t bdesc0 = desc_sw128(smem_addr(b_tiles));
+      const uint32_t full0 = smem_addr(full), empty0 = smem_addr(empty);
+      int s = 0;
+      uint32_t ph = 0;
       for (int j = 0; ok && tile_at(j, mb, nb); ++j) {
         const int b = j & 1;
         // rank 1's epilogue also releases this slot (a generic arrival from
@@ -292,26 +302,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d = tmem + uint32_t(b * kBN);
-        for (int kb = 0; kb < nk; ++kb, ++g) {
-          const int s = g % kStages;
-          if (!mbar_wait(&full[s], (g / kStages) & 1, err, abort)) {
+        for (int kb = 0; kb < nk; ++kb) {
+          const uint32_t fb = full0 + 8u * uint32_t(s);
+          if (!mbar_try_wait_sa(fb, ph) && !mbar_wait_sa(fb, ph, err, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(a_tiles + s * kATile);
-          const uint32_t b0 = smem_addr(b_tiles + s * kBTile);
+          // start address field (bits 0-13, address / 16): + stage offset,
+          // + 2 per 16-element K step (32 bytes)
+          const uint64_t ad = adesc0 + uint32_t(s * int(kATile >> 4));
+          const uint64_t bd = bdesc0 + uint32_t(s * int(kBTile >> 4));
 #pragma unroll
           for (int k = 0; k < kBK / kUK; ++k) {
-            const uint64_t ad = desc_sw128(a0 + k * kUK * 2), bd = desc_sw128(b0 + k * kUK * 2);
             if (PAIR)
-              mma_bf16_ss_pair(d, ad, bd, idesc, (kb | k) != 0);
+              mma_bf16_ss_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
             else
-              mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0);
+              mma_bf16_ss(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
           }
           // the stage is free once these MMAs have read it
-          commit(&empty[s]);
-          if (PAIR) mma_commit_pair(&full[s], 0x2);  // rank 1's x tile: readable now
+          if (PAIR) {
+            mma_commit_pair_sa(empty0 + 8u * uint32_t(s), 0x3);
+            mma_commit_pair_sa(fb, 0x2);  // rank 1's x tile: readable now
+          } else {
+            mma_commit_sa(empty0 + 8u * uint32_t(s));
+          }
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (ok) commit(&acc_full[b]);
       }
@@ -650,16 +669,17 @@ norm_status_t check_device_memory(const void *p, int dev) {
   return (a.type == cudaMemoryTypeDevice && a.device == dev) ? NORM_OK : NORM_ERR_MEMORY;
 }
 
-// Kernel form: the single-CTA kernel by default; GBNORM_GEMM_CTAS=2
-// selects the CTA pair (cta_group::2).  Measured on GB300 at
-// 32768 x 4096 x 4096 (RMSNorm / LayerNorm TF/s on one box): single
-// 1696 / 1563, pair 1659 / 1563.  In the pair, rank 1's statistics can only
-// read its x tile once the MMA commit says it has landed, which delays the
-// release of its stages.
+// Kernel form: the CTA pair (cta_group::2) by default, GBNORM_GEMM_CTAS=1
+// the single-CTA kernel.  Measured on GB300 at M = 32768, K = Nout from 2048
+// to 8192 (one box, TF/s): RMSNorm pair 1498-1578 against single 1453-1497,
+// LayerNorm 1407-1528 against 1364-1462.  The pair's per-SM operand traffic
+// (shared-memory writes by TMA and reads by the tensor core) is two thirds
+// of the single CTA's, and once the MMA issuer's per-K-block bookkeeping was
+// cut (it is one thread on the critical path) that is what showed.
 int gemm_form() {
   const char *s = std::getenv("GBNORM_GEMM_CTAS");
-  if (s && std::strcmp(s, "2") == 0) return kFormPair;
-  return kFormSingle;
+  if (s && std::strcmp(s, "1") == 0) return kFormSingle;
+  return kFormPair;
 }
 
 uint32_t form_smem(int form) {

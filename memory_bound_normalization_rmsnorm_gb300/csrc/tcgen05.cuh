@@ -146,6 +146,35 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// The same operations on shared-memory addresses already converted (the
+// MMA issuer's loop forms them with one add).
+__device__ __forceinline__ bool mbar_try_wait_sa(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sa(uint32_t bar, uint32_t parity, unsigned *err,
+                                             volatile int *abort) {
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    if (mbar_try_wait_sa(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+  }
+  *abort = 1;
+  atomicOr(err, kErrWaitTimeout);
+  return false;
+}
+__device__ __forceinline__ void mma_commit_sa(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------- CTA-pair (cta_group::2) forms
 // A pair of CTAs (ranks 0 and 1 of a 2-CTA cluster) shares one MMA of
 // M = 256: each CTA holds 128 rows of A and half of the N rows of B in its
@@ -181,6 +210,13 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_sa(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
 }

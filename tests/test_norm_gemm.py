@@ -71,13 +71,15 @@ def test_parity_small(mode, M, K, Nout):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
-@pytest.mark.parametrize("form", ["2"])
+@pytest.mark.parametrize("form", ["1", "2"])
 @pytest.mark.parametrize("M,K,Nout", [(1, 64, 32), (129, 512, 288), (300, 1024, 544),
                                       (1000, 2048, 1024), (200, 256, 96)])
 def test_cluster_kernels(mode, form, M, K, Nout, monkeypatch):
-    """The 2-CTA cluster kernel (GBNORM_GEMM_CTAS=2: cta_group::2 MMAs over
-    256-row tiles; the default is the single-CTA kernel) on ragged shapes,
-    including a last 256-row block whose second CTA owns no row."""
+    """Both kernel forms on ragged shapes: the single-CTA kernel
+    (GBNORM_GEMM_CTAS=1, 128 x 256 tiles) and the 2-CTA cluster kernel (the
+    default, also selected with GBNORM_GEMM_CTAS=2: cta_group::2 MMAs over
+    256-row tiles), including a last 256-row block whose second CTA owns no
+    row."""
     monkeypatch.setenv("GBNORM_GEMM_CTAS", form)
     x, gamma, beta, w = _inputs(mode, M, K, Nout, seed=M + 3 * K)
     outs = _run(x, gamma, beta, w, mode)
@@ -85,10 +87,10 @@ def test_cluster_kernels(mode, form, M, K, Nout, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
-@pytest.mark.parametrize("form", ["2"])
+@pytest.mark.parametrize("form", ["1", "2"])
 def test_cluster_kernels_full_size(mode, form, monkeypatch):
-    """The cluster kernels at 32768 x 4096 x 4096: sampled rows against the
-    oracle (rows of either CTA of the cluster) and every row's rstd against
+    """Both kernel forms at 32768 x 4096 x 4096: sampled rows against the
+    oracle (rows of either CTA of a cluster) and every row's rstd against
     float64 statistics."""
     monkeypatch.setenv("GBNORM_GEMM_CTAS", form)
     M, K = 32768, 4096
