@@ -822,10 +822,13 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
       g_pairs[{dev, int(mode), form}] = pairs;
     }
   }
-  // Column tiles per unit (statistics computed once per unit): LayerNorm's
-  // statistics cost ~12 % of the kernel, RMSNorm's a few percent, so
-  // LayerNorm takes the largest of 4 / 2 that divides the column tiles and
-  // adds at most 5 % to the most tiles any CTA (pair) runs; RMSNorm takes 1.
+  // Column tiles per unit (statistics computed once per unit): the largest
+  // candidate that divides the column tiles and adds at most 5 % to the most
+  // tiles any CTA (pair) runs -- 4 or 2 for LayerNorm, whose statistics
+  // cost ~12 % of the kernel, 2 for RMSNorm (CTA pairs, TF/s at K = Nout =
+  // 2048 / 3072 / 4096 / 5120 / 8192: one tile per unit 1605 / 1590 / 1611
+  // / 1536 / 1526, two 1678 / 1614 / 1618 / 1578 / 1573, four 1556 / 1559 /
+  // 1619 / 1515 / 1558).
   // GBNORM_GEMM_GROUP=r forces r (for sweeps; r must divide the column tiles).
   const int64_t slots = cluster ? pairs : sms;
   auto most = [&](int64_t r) {  // tiles of the busiest CTA (pair)
@@ -833,12 +836,11 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
     return ((u + slots - 1) / slots) * r;
   };
   int rgrp = 1;
-  if (mode == NORM_LAYER)
-    for (int r : {4, 2})
-      if (n_tiles % r == 0 && most(r) * 100 <= most(1) * 105) {
-        rgrp = r;
-        break;
-      }
+  for (int r : {4, 2})
+    if ((mode == NORM_LAYER || r == 2) && n_tiles % r == 0 && most(r) * 100 <= most(1) * 105) {
+      rgrp = r;
+      break;
+    }
   if (const char *ov = std::getenv("GBNORM_GEMM_GROUP")) {
     const int r = std::atoi(ov);
     if (r >= 1 && n_tiles % r == 0) rgrp = r;
