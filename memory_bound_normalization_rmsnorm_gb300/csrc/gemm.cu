@@ -825,12 +825,13 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
     }
   }
   // Column tiles per unit (statistics computed once per unit): the largest
-  // candidate that divides the column tiles and adds at most 5 % to the most
-  // tiles any CTA (pair) runs -- 4 or 2 for LayerNorm, whose statistics
-  // cost ~12 % of the kernel, 2 for RMSNorm (CTA pairs, TF/s at K = Nout =
-  // 2048 / 3072 / 4096 / 5120 / 8192: one tile per unit 1605 / 1590 / 1611
-  // / 1536 / 1526, two 1678 / 1614 / 1618 / 1578 / 1573, four 1556 / 1559 /
-  // 1619 / 1515 / 1558).
+  // of 8, 5, 4, 2 that divides the column tiles and adds at most 5 % to the
+  // most tiles any CTA (pair) runs.  CTA pairs, TF/s at K = Nout = 2048 /
+  // 3072 / 4096 / 5120 / 8192, RMSNorm: one tile per unit 1605 / 1590 /
+  // 1611 / 1536 / 1526, two 1678 / 1614 / 1618 / 1578 / 1573; on another
+  // box at 5120 four 1637, five 1675, at 8192 four 1614, eight 1644;
+  // LayerNorm at 5120 four 1546, five 1590, ten 1449 (10 % more tiles on
+  // the busiest pair), at 8192 four 1504, eight 1550.
   // GBNORM_GEMM_GROUP=r forces r (for sweeps; r must divide the column tiles).
   const int64_t slots = cluster ? pairs : sms;
   auto most = [&](int64_t r) {  // tiles of the busiest CTA (pair)
@@ -838,8 +839,8 @@ norm_status_t norm_gemm_fwd(const void *x, const void *wg, const float *u, const
     return ((u + slots - 1) / slots) * r;
   };
   int rgrp = 1;
-  for (int r : {4, 2})
-    if ((mode == NORM_LAYER || r == 2) && n_tiles % r == 0 && most(r) * 100 <= most(1) * 105) {
+  for (int r : {8, 5, 4, 2})
+    if (n_tiles % r == 0 && most(r) * 100 <= most(1) * 105) {
       rgrp = r;
       break;
     }

@@ -122,6 +122,19 @@ def test_statistics_shared_by_column_tiles(mode, group, pair, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
+@pytest.mark.parametrize("group,Nout", [("5", 2560), ("8", 2048)])
+@pytest.mark.parametrize("pair", ["1", "2"])
+def test_statistics_shared_by_wide_units(mode, group, Nout, pair, monkeypatch):
+    """Units of 5 and 8 column tiles (the planner's choice at 5120 and 8192
+    output columns), forced on smaller shapes whose tile counts they divide."""
+    monkeypatch.setenv("GBNORM_GEMM_GROUP", group)
+    monkeypatch.setenv("GBNORM_GEMM_CTAS", pair)
+    x, gamma, beta, w = _inputs(mode, 900, 512, Nout, seed=7, row_offset=0.5)
+    outs = _run(x, gamma, beta, w, mode)
+    _compare(x, gamma, beta, w, outs, mode, label=f"group {group} Nout {Nout} ctas {pair}")
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
 def test_large_row_offset(mode):
     """Rows offset by 3 (mean far from 0): the mean correction after the
     contraction, and the one-pass block statistics, hold up."""
