@@ -21,7 +21,7 @@
 // and the normalised rows are never written.
 //
 // A persistent grid (one CTA per SM, 12 warps) walks the output tiles in
-// units of 1, 2 or 4 consecutive column tiles of one row block, dealt
+// units of 1 to 8 consecutive column tiles of one row block, dealt
 // round-robin in the grouped order of tile_coords.  By default 2-CTA
 // clusters (PAIR) share 256 x 256 tiles with cta_group::2 MMAs, each CTA
 // holding 128 x rows and 128 W' rows per stage (6 stages); the single-CTA
