@@ -1,8 +1,10 @@
-// stream.cu -- the streaming long-row backward: rows of 32768 columns per
-// CTA (a cluster of C = N / 32768 CTAs per row), each row slice streamed
-// through a shared-memory ring twice -- once for the per-row dot products,
-// once for dx -- instead of being held in shared memory, with the dgamma /
-// dbeta column sums accumulated in tensor memory (TMEM).
+// stream.cu -- the streaming long-row kernels.  Backward: rows of 32768
+// columns per CTA (a cluster of C = N / 32768 CTAs per row), each row slice
+// streamed through a shared-memory ring twice -- once for the per-row dot
+// products, once for dx -- instead of being held in shared memory, with the
+// dgamma / dbeta column sums accumulated in tensor memory (TMEM).  Forward
+// (further down): the same piece sequence for rows wider than a 16-CTA
+// cluster holds, pass 1 the statistics, pass 2 y.
 //
 // "PyTorch atinge desempenho SOTA em normalizacao com torch.compile"
 // (matsubara.tec.br) places the backward's difficulty at very large
@@ -13,7 +15,8 @@
 // SMs).  Here a CTA keeps on chip only what a row does not need twice: the
 // packed gamma of its slice (registers) and the column accumulators (TMEM,
 // 128 KB for RMSNorm, 256 KB with dbeta).  Its 32768-column slice of x and
-// dy passes through a ring of 8192-column pieces:
+// dy passes through a ring of 16384-column pieces (8192 for the fused
+// residual backward, whose dh is a third tensor of the dx pass's pieces):
 //
 //   pass 1 (row j)    sum g and sum g (x - mean) over the slice (g = dy *
 //                     gamma), summed over the CTA, then over the cluster
@@ -683,9 +686,10 @@ const void *stream_ptr(bool cluster) {
 
 }  // namespace
 
-// Instantiated: 2 chunks per thread per piece (8192-column pieces) for both
-// modes, and 4 (16384) for RMSNorm, whose dx pass keeps half the
-// accumulator registers per chunk of LayerNorm's (dgamma only).
+// Instantiated: 4 chunks per thread per piece (16384-column pieces, the
+// default of the plain backward; LayerNorm's dx pass moves its dgamma and
+// dbeta accumulators through registers in batches) and 2 (8192, the fused
+// residual backward's default and the W=8192 override) for both modes.
 const void *stream_kernel_ptr(int mode, int kp, bool cluster, bool resid) {
   if (mode == kLayer) {
     if (kp == 4) return resid ? stream_ptr<kLayer, 4, true>(cluster) : stream_ptr<kLayer, 4, false>(cluster);
