@@ -130,9 +130,10 @@ def test_fp8_zero_rows_and_tiny_blocks():
 def test_fp8_long_rows(mode, M, N, residual):
     """Rows wider than one CTA's registers (long-row kernels, clusters):
     both scalings; with a cluster, per-row scaling sends the CTAs' slice
-    maxima of a row in the next row's exchange round (and one last round
-    after the last row), so every cluster case here has rows that finish in
-    a later round, and the 301-row case gives each cluster several."""
+    maxima of a row in the next row's DSMEM exchange (and one last exchange
+    after the last row), so every cluster case here has rows whose codes
+    are written one exchange later, and the 301-row case gives each cluster
+    several."""
     base = wl.WORKLOADS["layer_32768x4096" if mode else "rms_4096x16384"]
     case = wl.like(base, M, N)
     x, r, g, b, _, _ = [None if t is None else t.cuda()
