@@ -108,6 +108,27 @@ def test_cluster_kernels_full_size(mode, form, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
+@pytest.mark.parametrize("K", [5120, 8192])
+def test_default_kernel_wide(mode, K):
+    """The default kernel at the widest benchmark shapes, 32768 x K x K (CTA
+    pairs, statistics units of 5 and 8 column tiles, 2048-row tile groups):
+    sampled rows against the oracle, every row's rstd against float64
+    statistics."""
+    M = 32768
+    x, gamma, beta, w = _inputs(mode, M, K, K, seed=K + mode)
+    outs = _run(x, gamma, beta, w, mode)
+    rows = pu.sample_rows(M, n=32, seed=K)
+    _compare(x, gamma, beta, w, outs, mode, rows=rows, label=f"default {K}")
+    xd = x.double()
+    if mode == wl.LAYER:
+        var = ((xd - xd.mean(dim=1, keepdim=True)) ** 2).mean(dim=1)
+    else:
+        var = (xd ** 2).mean(dim=1)
+    r64 = 1.0 / torch.sqrt(var + float(np.float32(EPS)))
+    assert (outs[4].double() / r64 - 1).abs().max().item() < 1e-5
+
+
+@pytest.mark.parametrize("mode", [wl.RMS, wl.LAYER])
 @pytest.mark.parametrize("group", ["2", "4"])
 @pytest.mark.parametrize("pair", ["1", "2"])
 def test_statistics_shared_by_column_tiles(mode, group, pair, monkeypatch):
