@@ -45,10 +45,12 @@ struct Pending {
 // RESID: fused residual add -- the stage also holds r; the statistics pass
 // forms h = bf16(x + r) (sum in binary32, round to nearest even), writes it
 // over x in the stage, and the output pass writes h out beside y.
-// OUT: bf16 y (kOutBf16), or E4M3 codes with a per-row scale (kOutFp8Row;
-// in a cluster the CTAs' slice maxima of a row travel in the next row's
-// exchange round, so a row's codes are written one round later) or with
-// per-32-column E8M0 exponents (kOutFp8Mx; slices start on a block).
+// OUT: bf16 y (kOutBf16), or E4M3 codes with a per-row scale (kOutFp8Row:
+// RMSNorm's amax is rstd times the largest |x gamma|, taken in the
+// statistics pass; LayerNorm's needs y, and in a cluster the CTAs' slice
+// maxima of a row travel in the next row's exchange round, so its codes are
+// written one round later) or with per-32-column E8M0 exponents
+// (kOutFp8Mx; slices start on a block).
 template <int MODE, int K, bool CLUSTER, bool EXACT, bool RESID, int OUT = kOutBf16>
 __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const NormArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       pc = n;
     } else {
       float2 q0 = splat2(0.f), q1 = splat2(0.f);
+      float mx = 0.f;  // per-row E4M3: the largest |x gamma| of the slice
       if (active) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -193,6 +196,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
             chunk_to_f2(first_chunk(rowp, k), xf);
             q0 = fma2(xf[0], xf[0], fma2(xf[1], xf[1], q0));
             q1 = fma2(xf[2], xf[2], fma2(xf[3], xf[3], q1));
+            if (OUT == kOutFp8Row) {
+              float2 gf[4];
+              chunk_to_f2(gv[k], gf);
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const float2 pr = mul2(xf[p], gf[p]);
+                mx = fmaxf(mx, fmaxf(fabsf(pr.x), fabsf(pr.y)));
+              }
+            }
           }
         }
       }
@@ -200,16 +212,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       float v[1] = {qt.x + qt.y};
       group_sum<1, EXACT>(v, a.tpr, g, a.G, t, red, rpar);
       pa = v[0];
-      pb = 0.f;
+      pb = OUT == kOutFp8Row ? group_max<true>(mx, a.tpr, g, a.G, t, red, rpar) : 0.f;
       pc = 0.f;
     }
   };
 
   // Output pass of row slot r given the row totals; writes y and the
-  // statistics.  Per-row E4M3 runs in one of three phases: kFp8Whole (no
-  // cluster: the row amax, then the codes), kFp8Amax (cluster: returns this
-  // CTA's slice amax, stores nothing) or kFp8Codes (cluster: the codes with
-  // the row amax `am_row`, then the statistics).
+  // statistics.  Per-row E4M3, LayerNorm, runs in one of three phases:
+  // kFp8Whole (no cluster: the row amax, then the codes), kFp8Amax (cluster:
+  // returns this CTA's slice amax, stores nothing) or kFp8Codes (cluster:
+  // the codes with the row amax `am_row`, then the statistics); RMSNorm
+  // always writes the codes, `am_row` being the row's largest |x gamma|.
   auto output_pass = [&](const unsigned char *st, int64_t row0, int r, float ta, float tb,
                          int phase = kFp8Whole, float am_row = 0.f) -> float {
     float rs, mu = 0.f;
@@ -250,7 +263,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       // amax of the row (of this CTA's slice in a cluster), then the codes
       uint8_t *qrow = a.q + (row0 + r) * a.N + col0 + t * 8;
       float am = am_row;
-      if (phase != kFp8Codes) {
+      if (MODE == kRMS) {
+        // y = x rstd gamma with rstd > 0: the row's amax is rstd times the
+        // largest |x gamma|, which the statistics pass took (am_row), so
+        // there is no y pass for it and, in a cluster, no second exchange.
+        am = rs * am_row;
+      } else if (phase != kFp8Codes) {
         am = 0.f;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -359,15 +377,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
     const int nrows = static_cast<int>(min64(a.RT, a.M - row0));
     const int r = g;
     float ta, tb;
-    fold_totals(cluster_wait_row(r, xch, a.err, abort_flag), ta, tb);
-    if (r < nrows) output_pass(smem + static_cast<size_t>(p.s) * L.stage_bytes, row0, r, ta, tb);
+    const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
+    fold_totals(row, ta, tb);
+    float mx = 0.f;  // per-row E4M3 (RMSNorm): the row's largest |x gamma|
+    if (OUT == kOutFp8Row && MODE == kRMS) {
+      mx = row[1];
+      for (int q = 1; q < xch.C; ++q) mx = fmaxf(mx, row[q * 4 + 1]);
+    }
+    if (r < nrows)
+      output_pass(smem + static_cast<size_t>(p.s) * L.stage_bytes, row0, r, ta, tb, kFp8Codes,
+                  mx);
     release(p.tile, p.s);
   };
-  // Per-row E4M3 in a cluster: one exchange round per tile carries the
-  // tile's statistics partial and, in its fourth float, this CTA's slice
-  // amax of the previous tile, whose codes are written once the round is
-  // in.  (Two rounds per tile -- statistics, then amax -- cannot overlap the
-  // next tile's statistics, since rounds are consumed in push order.)
+  // Per-row E4M3 in a cluster, LayerNorm: one exchange round per tile
+  // carries the tile's statistics partial and, in its fourth float, this
+  // CTA's slice amax of the previous tile, whose codes are written once the
+  // round is in.  (Two rounds per tile -- statistics, then amax -- cannot
+  // overlap the next tile's statistics, since rounds are consumed in push
+  // order.)  RMSNorm's amax travels with its statistics (second float) and
+  // takes the pipelined path of the other outputs.
   float pend_ta = 0.f, pend_tb = 0.f, pend_am = 0.f;
   auto fp8_codes = [&](const Pending &p, const float *row) {
     const int64_t row0 = p.tile * a.RT;
@@ -395,7 +423,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
       cur.tile = tile;
       cur.s = s;
       stats_pass(st, r, r < nrows, cur.a, cur.b, cur.c);
-      if (OUT == kOutFp8Row) {
+      if (OUT == kOutFp8Row && MODE == kLayer) {
         cluster_push(cur.a, cur.b, cur.c, r, t, xch, have_pend ? pend_am : 0.f);
         const float *row = cluster_wait_row(r, xch, a.err, abort_flag);
         float ta, tb;
@@ -418,7 +446,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
         const bool active = r < nrows;
         float pa, pb, pc;
         stats_pass(st, r, active, pa, pb, pc);
-        if (active) output_pass(st, row0, r, pa, pb);
+        if (active) output_pass(st, row0, r, pa, pb, kFp8Whole, pb);
       }
       release(tile, s);
     }
@@ -429,7 +457,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) norm_fwd_long_kernel(const Nor
   }
   if (CLUSTER) {
     if (have_pend) {
-      if (OUT == kOutFp8Row) {
+      if (OUT == kOutFp8Row && MODE == kLayer) {
         // a last round with the last tile's slice maxima only
         cluster_push(0.f, 0.f, 0.f, g, t, xch, pend_am);
         fp8_codes(pend, cluster_wait_row(g, xch, a.err, abort_flag));
